@@ -1,0 +1,275 @@
+"""Plain, slow CPU oracle for the VeriCache draft-then-verify round.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this module: only tests/,
+__graft_entry__.smoke() and bench.py's CPU-baseline / reference leg call it. It shares no code
+with the CUDA library (no helpers, tables, layouts code or constants generators).
+
+Source: "VeriCache: Turning Lossy KV Cache into Lossless LLM Inference" (technical summary
+pages, in Japanese, French and German). The summary states the loop in its "Core algorithm"
+section: (1) draft candidate tokens x with the compressed cache KV_comp, (2) verify all drafts
+in one forward pass over the full cache KV_full, (3) accept up to the first mismatch, plus one
+bonus token when every draft matches, then restart from the last accepted token. Its
+"Architecture support" section names token-drop (SnapKV, KVzip) and quantisation (KIVI)
+compressors behind one interface. Everything numeric (group sizes, bit widths, keep-set rules,
+scale) is not on the pages; the readings used here are listed per function.
+
+Precision: attention runs in float64 (softmax(q K^T / sqrt(d)) V, written out); quantisation
+decisions run in IEEE float32 with round-to-nearest-even, because a float decides an integer
+code there and both sides must take that decision in the same precision (the kernel's).
+
+Every function here is pinned by tests/test_oracle_pins.py to closed forms, brute force on tiny
+inputs and invariants; see that file for which pin guards which step.
+"""
+from __future__ import annotations
+
+import math
+from typing import List, Sequence, Tuple
+
+import numpy as np
+
+GROUP = 32  # quantisation group: 32 tokens per key channel, 32 channels per value token
+
+
+# ----------------------------------------------------------------------------------------------
+# a0. compression: token-drop keep-set
+# ----------------------------------------------------------------------------------------------
+def keep_set(importance: np.ndarray, keep: int, recent: int) -> np.ndarray:
+    """Indices kept by token-drop compression, ascending int32.
+
+    Reading (the pages name SnapKV/KVzip but define no scoring, "Architecture support"): the last
+    `recent` tokens are always kept; the remaining keep-recent slots go to the tokens of
+    [0, ctx-recent) with the largest importance, ties to the lower index; the union is returned
+    sorted ascending. If keep >= ctx every token is kept.
+    """
+    imp = np.asarray(importance, dtype=np.float32)
+    n = imp.shape[0]
+    if keep >= n:
+        return np.arange(n, dtype=np.int32)
+    if not (0 <= recent <= keep):
+        raise ValueError("need 0 <= recent <= keep")
+    n_cand = n - recent
+    cand = np.arange(n_cand)
+    # sort by importance descending, then index ascending (lexsort: last key is primary)
+    order = np.lexsort((cand, -imp[:n_cand].astype(np.float64)))
+    top = order[: keep - recent]
+    sel = np.concatenate([np.sort(top), np.arange(n_cand, n)])
+    return sel.astype(np.int32)
+
+
+# ----------------------------------------------------------------------------------------------
+# a0. compression: groupwise asymmetric b-bit quantisation
+# ----------------------------------------------------------------------------------------------
+def fp16_rne(x: np.ndarray) -> np.ndarray:
+    """float32 -> float16, round to nearest even (IEEE conversion)."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16)
+
+
+def quant_groups(x: np.ndarray, bits: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Quantise each row of x (float32 [..., 32]) as one group.
+
+    Reading (KIVI is named, not defined, on the pages): asymmetric min/max quantisation with
+      s16 = fp16(fp32(max - min) / (2^b - 1)),  z16 = fp16(min),
+      code = clamp(rint_half_even(fp32(x - f32(z16)) / f32(s16)), 0, 2^b - 1),  code = 0 if s16 == 0.
+    Codes come from the stored fp16 scale and zero, so the codes and the dequantised values agree.
+    Returns (codes uint8 [..., 32], s16 float16 [...], z16 float16 [...]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    qmax = np.float32((1 << bits) - 1)
+    mn = x.min(axis=-1)
+    mx = x.max(axis=-1)
+    s16 = fp16_rne((mx - mn) / qmax)
+    z16 = fp16_rne(mn)
+    s32 = s16.astype(np.float32)[..., None]
+    z32 = z16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = (x - z32) / s32
+    codes = np.clip(np.rint(t), 0, qmax)
+    codes = np.where(s32 == 0, 0, codes)
+    return codes.astype(np.uint8), s16, z16
+
+
+def pack(codes: np.ndarray, bits: int) -> np.ndarray:
+    """Pack b-bit codes along the last axis, little-endian within a byte.
+
+    Element e of a run lands in byte e // (8/b) at bit offset b * (e mod 8/b).
+    """
+    per = 8 // bits
+    c = np.asarray(codes, dtype=np.uint8)
+    n = c.shape[-1]
+    assert n % per == 0
+    c = c.reshape(c.shape[:-1] + (n // per, per)).astype(np.uint16)
+    out = np.zeros(c.shape[:-1], dtype=np.uint16)
+    for e in range(per):
+        out |= c[..., e] << (bits * e)
+    return out.astype(np.uint8)
+
+
+def unpack(packed: np.ndarray, bits: int) -> np.ndarray:
+    per = 8 // bits
+    p = np.asarray(packed, dtype=np.uint8)
+    mask = (1 << bits) - 1
+    parts = [(p >> (bits * e)) & mask for e in range(per)]
+    return np.stack(parts, axis=-1).reshape(p.shape[:-1] + (p.shape[-1] * per,)).astype(np.uint8)
+
+
+def quant_layout(ctx: int, residual_min: int = 128) -> Tuple[int, int]:
+    """(ng, n_res): quantised 32-token groups and bf16 residual rows.
+
+    Reading: the configs keep "the last 128 tokens" in bf16; groups stay whole, so the first
+    ng = floor((ctx - 128) / 32) groups are quantised and the residual is the remaining
+    ctx - 32*ng tokens (128 to 159 of them).
+    """
+    ng = max(0, (ctx - residual_min) // GROUP)
+    return ng, ctx - GROUP * ng
+
+
+def quantize_kv(k: np.ndarray, v: np.ndarray, bits: int, residual_min: int = 128) -> dict:
+    """Quantise one request's cache. k, v: float32 images of the bf16 cache, [Hkv][ctx][d].
+
+    Keys: one group per (head, 32-token group, channel), codes packed along the 32 tokens.
+    Values: one group per (head, token, 32-channel group), codes packed along the channels.
+    Layout (all C-contiguous):
+      kc uint8 [Hkv][ng][d][32*b/8]   ks, kz float16 [Hkv][ng][d]
+      vc uint8 [Hkv][Tq][d*b/8]       vs, vz float16 [Hkv][Tq][d/32]
+      k_res, v_res float32 [Hkv][n_res][d]  (tokens Tq..ctx-1, unchanged)
+    """
+    H, ctx, d = k.shape
+    ng, n_res = quant_layout(ctx, residual_min)
+    Tq = GROUP * ng
+    kq = k[:, :Tq, :].reshape(H, ng, GROUP, d).transpose(0, 1, 3, 2)  # [H][ng][d][32 tokens]
+    kcodes, ks, kz = quant_groups(kq, bits)
+    vq = v[:, :Tq, :].reshape(H, Tq, d // GROUP, GROUP)               # [H][Tq][d/32][32 ch]
+    vcodes, vs, vz = quant_groups(vq, bits)
+    return dict(bits=bits, ng=ng, n_res=n_res,
+                kc=pack(kcodes, bits), ks=ks, kz=kz,
+                vc=pack(vcodes.reshape(H, Tq, d), bits), vs=vs, vz=vz,
+                k_res=k[:, Tq:, :].copy(), v_res=v[:, Tq:, :].copy())
+
+
+def dequantize_kv(qkv: dict, d: int) -> Tuple[np.ndarray, np.ndarray]:
+    """x_hat = code * f32(s16) + f32(z16) in float32, back in [Hkv][Tq][d] token-major order."""
+    bits = qkv["bits"]
+    kc = unpack(qkv["kc"], bits).astype(np.float32)            # [H][ng][d][32]
+    kh = kc * qkv["ks"].astype(np.float32)[..., None] + qkv["kz"].astype(np.float32)[..., None]
+    H, ng = kh.shape[0], kh.shape[1]
+    kh = kh.transpose(0, 1, 3, 2).reshape(H, ng * GROUP, d)
+    vc = unpack(qkv["vc"], bits).astype(np.float32)            # [H][Tq][d]
+    Tq = vc.shape[1]
+    vc = vc.reshape(H, Tq, d // GROUP, GROUP)
+    vh = vc * qkv["vs"].astype(np.float32)[..., None] + qkv["vz"].astype(np.float32)[..., None]
+    return kh.astype(np.float32), vh.reshape(H, Tq, d).astype(np.float32)
+
+
+# ----------------------------------------------------------------------------------------------
+# a1/a2. attention
+# ----------------------------------------------------------------------------------------------
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, visible: np.ndarray | None = None) -> np.ndarray:
+    """softmax(q k^T / sqrt(d)) v in float64 for one head.
+
+    q [nq][d], k [n][d], v [n][d]; visible (bool [nq][n]) masks rows' keys, None = all visible.
+    Reading: the pages print no attention formula; the scale 1/sqrt(d) is the standard one (also
+    the one the position-independent-caching page on the same site writes in its score formula).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    s = (q @ k.T) / math.sqrt(q.shape[-1])
+    if visible is not None:
+        s = np.where(visible, s, -np.inf)
+    m = s.max(axis=-1, keepdims=True)
+    p = np.exp(s - m)
+    return (p @ v) / p.sum(axis=-1, keepdims=True)
+
+
+def draft_attn(q: np.ndarray, k_main: np.ndarray, v_main: np.ndarray,
+               k_win: np.ndarray, v_win: np.ndarray) -> np.ndarray:
+    """One draft decode step of one request over the compressed cache ("Core algorithm", step 1).
+
+    q [Hq][d]; KV_comp = the main rows k_main/v_main [Hkv][n][d] (kept rows of a token-drop cache,
+    or the dequantised groups of a quantised cache) followed by the bf16 window k_win/v_win
+    [Hkv][nw][d] (quantised residual, then the drafted tokens' own K/V up to and including the
+    current one). GQA reading: query head h reads KV head h // (Hq / Hkv).
+    Returns float64 [Hq][d].
+    """
+    Hq, d = q.shape
+    Hkv = k_main.shape[0]
+    G = Hq // Hkv
+    out = np.empty((Hq, d), dtype=np.float64)
+    for h in range(Hq):
+        j = h // G
+        K = np.concatenate([k_main[j], k_win[j]], axis=0)
+        V = np.concatenate([v_main[j], v_win[j]], axis=0)
+        out[h] = attention(q[h][None, :], K, V)[0]
+    return out
+
+
+def verify_attn(q: np.ndarray, k_full: np.ndarray, v_full: np.ndarray,
+                k_new: np.ndarray, v_new: np.ndarray) -> np.ndarray:
+    """Verification attention of one request ("Core algorithm", step 2): all n drafted tokens in one pass.
+
+    q [n][Hq][d] are the queries at positions ctx..ctx+n-1; k_full/v_full [Hkv][ctx][d] is KV_full;
+    k_new/v_new [Hkv][n][d] are the drafted tokens' K/V. Row i sees KV_full entirely and the new
+    rows 0..i (causal among the drafts). GQA as in draft_attn. Returns float64 [n][Hq][d].
+    """
+    n, Hq, d = q.shape
+    Hkv, ctx, _ = k_full.shape
+    G = Hq // Hkv
+    vis = np.ones((n, ctx + n), dtype=bool)
+    vis[:, ctx:] = np.tril(np.ones((n, n), dtype=bool))
+    out = np.empty((n, Hq, d), dtype=np.float64)
+    for h in range(Hq):
+        j = h // G
+        K = np.concatenate([k_full[j], k_new[j]], axis=0)
+        V = np.concatenate([v_full[j], v_new[j]], axis=0)
+        out[:, h, :] = attention(q[:, h, :], K, V, vis)
+    return out
+
+
+# ----------------------------------------------------------------------------------------------
+# a3. accept
+# ----------------------------------------------------------------------------------------------
+def accept(logits: np.ndarray, draft: Sequence[int], L: int) -> Tuple[List[int], int]:
+    """Greedy accept of one request ("Core algorithm", step 3).
+
+    logits [>= L+1][V]: row i is the full-cache prediction after the i-th verified input
+    (row 0 follows the last accepted token, row i follows draft x_{i-1}); draft x_0..x_{L-1}.
+    a_i = argmax of row i (first maximal index); n = first i < L with a_i != x_i, else L.
+    Accepted tokens: x_0..x_{n-1} then a_n (the correction, or the bonus when n == L).
+    Returns (tokens, n_acc = n + 1).
+    """
+    a = [int(np.argmax(logits[i])) for i in range(L + 1)]
+    n = L
+    for i in range(L):
+        if a[i] != int(draft[i]):
+            n = i
+            break
+    tokens = [int(draft[i]) for i in range(n)] + [a[n]]
+    return tokens, n + 1
+
+
+# ----------------------------------------------------------------------------------------------
+# helpers for whole requests
+# ----------------------------------------------------------------------------------------------
+def bf16_to_f32(t) -> np.ndarray:
+    """float32 image of a bf16 torch tensor (exact)."""
+    import torch
+    return t.detach().to("cpu").to(torch.float32).numpy()
+
+
+def comp_main_rows(mode: str, k: np.ndarray, v: np.ndarray, *, idx=None, qkv=None):
+    """KV_comp main rows as float32 [Hkv][n][d] for draft_attn."""
+    if mode == "drop":
+        return k[:, idx, :], v[:, idx, :]
+    kh, vh = dequantize_kv(qkv, k.shape[2])
+    return kh, vh
+
+
+def draft_round(q: np.ndarray, k_main, v_main, k_win0, v_win0, k_new, v_new) -> np.ndarray:
+    """All L draft steps of one request: step s attends main + window0 + new[0..s]. Returns [L][Hq][d]."""
+    L = q.shape[0]
+    out = np.empty(q.shape, dtype=np.float64)
+    for s in range(L):
+        kw = np.concatenate([k_win0, k_new[: s + 1].transpose(1, 0, 2)], axis=1)
+        vw = np.concatenate([v_win0, v_new[: s + 1].transpose(1, 0, 2)], axis=1)
+        out[s] = draft_attn(q[s], k_main, v_main, kw, vw)
+    return out
