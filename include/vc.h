@@ -1,0 +1,225 @@
+/*
+ * vc.h — C ABI of the VeriCache draft-then-verify hot path on one GB300 (sm_103a).
+ *
+ * The loop this library runs is the one stated in "VeriCache: Turning Lossy KV Cache into
+ * Lossless LLM Inference", section "Core algorithm":
+ *   1. draft: the target model decodes candidate tokens x with the compressed cache KV_comp;
+ *   2. verify: one forward pass over the full cache KV_full checks all drafts in parallel;
+ *   3. accept: tokens are accepted up to the first mismatch, plus one "bonus" token when every
+ *      draft matches; the next round restarts from the last accepted token.
+ * Section "Architecture support" adds the long-context scenario (KV_comp in GPU HBM, KV_full in
+ * CPU memory, loaded over the host link for each verification) and a single compressor
+ * interface for token-drop and quantising compressors. Section "Cross-resource staggering (P1)"
+ * overlaps the host-link copy of some requests with the drafting of others.
+ *
+ * One attention layer is covered: compress (vc_compress_kv), draft attention (vc_draft_attn),
+ * verify attention (vc_verify_attn), greedy accept (vc_accept) and full-KV staging
+ * (vc_stage_full_kv). Every compute step runs in this library's CUDA kernels.
+ *
+ * Conventions for every call
+ *   - The caller owns every buffer. The library never allocates device or host memory and never
+ *     synchronises a stream. Device pointers must be 16-byte aligned.
+ *   - bf16 tensors are stored as raw 16-bit words (`void*`); fp16 scales/zeros as uint16_t.
+ *   - Host-side validation returns a status and launches nothing when it fails.
+ *   - `dev_status` (may be NULL) is a device int32 the kernels set to a VC_DEV_* code when they
+ *     detect a problem they can survive (an index outside its buffer is skipped, a bounded wait
+ *     gives up); the first code written wins. The caller reads it when convenient.
+ *   - Calls are asynchronous on `stream`; a call returns before its kernels finish.
+ *   - At most VC_MAX_BATCH requests per call (per-request descriptors travel as kernel params).
+ *   - Head dim d is 64 or 128; Hq is a multiple of Hkv; query head h reads KV head h / (Hq/Hkv).
+ */
+#ifndef VC_H_
+#define VC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VC_MAX_BATCH 32
+#define VC_GROUP 32            /* quantisation group size (tokens per key group, channels per value group) */
+
+typedef enum vc_status {
+  VC_OK = 0,
+  VC_ERR_INVALID = 1,      /* null pointer, bad size, misaligned buffer, inconsistent descriptor */
+  VC_ERR_UNSUPPORTED = 2,  /* well-formed but outside what the kernels implement (d, bits, G) */
+  VC_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  VC_ERR_NOT_PINNED = 4,   /* a host source for staging is not page-locked */
+  VC_ERR_WORKSPACE = 5     /* workspace smaller than vc_workspace_size() */
+} vc_status;
+
+/* Codes the kernels write into *dev_status. */
+#define VC_DEV_OK 0
+#define VC_DEV_BOUNDS 1        /* a gather index fell outside its buffer; the row was skipped */
+#define VC_DEV_TIMEOUT 2       /* a bounded wait on a copy gave up; outputs of that block are invalid */
+#define VC_DEV_RANGE 3         /* a quantisation scale or zero is not finite in fp16 */
+
+typedef enum vc_mode { VC_TOKEN_DROP = 0, VC_QUANT = 1 } vc_mode;
+typedef enum vc_call { VC_CALL_DRAFT = 0, VC_CALL_VERIFY = 1 } vc_call;
+
+typedef struct vc_shape {
+  int32_t B;     /* requests in this call, 1..VC_MAX_BATCH */
+  int32_t Hq;    /* query heads */
+  int32_t Hkv;   /* KV heads */
+  int32_t d;     /* head dim: 64 or 128 */
+} vc_shape;
+
+/* One request's full-precision cache KV_full, resident in device memory (HBM, or a staging
+ * buffer filled by vc_stage_full_kv). Rows 0..ctx-1 are valid. */
+typedef struct vc_kv_full {
+  const void* k;     /* bf16 [Hkv][cap][d], head h row t at (h*cap + t)*d */
+  const void* v;     /* bf16 [Hkv][cap][d] */
+  int32_t ctx;       /* tokens held */
+  int32_t cap;       /* rows per head, cap >= ctx */
+} vc_kv_full;
+
+/* One request's compressed cache KV_comp (device memory). Two families share it:
+ *
+ * VC_TOKEN_DROP: a keep-set of `keep` token indices `idx` (ascending). With compact == 0 the
+ *   kept rows are read in place at k_rows[h][idx[j]] (k_rows is normally the full cache); with
+ *   compact == 1 vc_compress_kv gathers them into k_rows[h][j], j < keep, and the draft reads them
+ *   contiguously (needed when KV_full leaves HBM).
+ * VC_QUANT: groupwise asymmetric `bits`-bit codes for the first Tq = 32*ng tokens:
+ *   kc  uint8 [Hkv][ng][d][32*bits/8]  key codes, per (group, channel) the 32 tokens packed
+ *   ks,kz fp16 [Hkv][ng][d]            key scale and zero per (group, channel)
+ *   vc  uint8 [Hkv][Tq][d*bits/8]      value codes, per token the d channels packed
+ *   vs,vz fp16 [Hkv][Tq][d/32]         value scale and zero per (token, 32-channel group)
+ *   packing: code e of a run at byte e/(8/bits), bit offset bits*(e mod 8/bits).
+ *   Dequantised value: code * scale + zero.
+ *
+ * Both families end with a bf16 window k_win/v_win [Hkv][win_cap][d]: for VC_QUANT it starts
+ * with the n_res trailing tokens kept in bf16 (the residual), then — for both — the drafted
+ * tokens' own K/V, one row per draft step. `n_win` counts the rows present before a draft step;
+ * the caller increases it by one after each vc_draft_attn. */
+typedef struct vc_kv_comp {
+  int32_t mode;        /* vc_mode */
+  int32_t bits;        /* VC_QUANT: 2 or 4 */
+  /* VC_TOKEN_DROP */
+  int32_t keep;        /* kept rows */
+  int32_t compact;     /* 0: rows in place at idx; 1: rows gathered contiguously */
+  int32_t* idx;        /* int32 [keep] ascending token indices (written by vc_compress_kv) */
+  void* k_rows;        /* bf16 [Hkv][rows_cap][d] */
+  void* v_rows;
+  int32_t rows_cap;    /* rows per head of k_rows/v_rows (indices must be < rows_cap) */
+  /* VC_QUANT */
+  int32_t ng;          /* quantised 32-token groups (set by vc_compress_kv) */
+  uint8_t* kc;
+  uint16_t* ks;
+  uint16_t* kz;
+  uint8_t* vc;
+  uint16_t* vs;
+  uint16_t* vz;
+  /* bf16 window (both) */
+  void* k_win;         /* bf16 [Hkv][win_cap][d] */
+  void* v_win;
+  int32_t win_cap;
+  int32_t n_win;       /* rows present before this draft step (set to n_res / 0 by vc_compress_kv) */
+} vc_kv_comp;
+
+/* ------------------------------------------------------------------------------------------ */
+/* vc_compress_kv — build KV_comp from KV_full ("Architecture support": one compressor interface
+ * for token drop and quantisation).
+ *
+ * Per request b (all requests of a call use one mode):
+ *   VC_TOKEN_DROP: idx = the `recent` last tokens plus the keep-recent tokens of [0, ctx-recent)
+ *     with the largest importance (fp32 order, -0 == +0, ties to the lower index), ascending.
+ *     keep >= ctx keeps every token. With compact == 1 the kept rows are gathered into k_rows.
+ *     Sets n_win = 0.
+ *   VC_QUANT: ng = max(0, (ctx - residual_min) / 32) groups are quantised (fp32 min/max, scale =
+ *     fp16(fp32(max-min)/(2^bits-1)), zero = fp16(min), code = clamp(rint((x - zero)/scale))
+ *     with IEEE round-to-nearest-even, code 0 when scale == 0); the n_res = ctx - 32*ng
+ *     trailing tokens are copied to window rows 0..n_res-1. Sets ng and n_win = n_res.
+ * importance: host array of B device pointers to fp32 [ctx] (token drop; NULL for quant).
+ * recent: host int32 [B] (token drop; NULL for quant). residual_min: trailing bf16 tokens (128).
+ * comp: host array of B descriptors; mode, bits/keep/compact and the buffers are inputs, ng and
+ *   n_win are written. Requirements: 0 <= recent <= keep; window capacity >= n_res (+ drafts).
+ */
+vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const float* const* importance,
+                         const int32_t* recent, int32_t residual_min, vc_kv_comp* comp,
+                         int32_t* dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* vc_draft_attn — one draft decode step for B requests ("Core algorithm", step 1: drafting with
+ * KV_comp; "Cross-resource staggering (P1)": drafting is bound by HBM bandwidth).
+ *
+ * For each request and query head h: o = softmax(q K^T / sqrt(d)) V over the rows of KV_comp
+ * (kept rows, or dequantised groups) followed by window rows 0..n_win, where window row n_win is
+ * (k_new, v_new). The call also stores k_new/v_new into window row n_win (needs n_win < win_cap).
+ * Accumulation is fp32; the output is rounded to bf16.
+ */
+typedef struct vc_draft_req {
+  const void* q;       /* bf16 [Hq][d]: query of the token drafted at this step */
+  const void* k_new;   /* bf16 [Hkv][d]: its key */
+  const void* v_new;   /* bf16 [Hkv][d]: its value */
+  void* o;             /* bf16 [Hq][d] output */
+  vc_kv_comp comp;     /* the request's compressed cache */
+} vc_draft_req;
+
+vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* vc_verify_attn — verification attention, all drafts of a request in one pass ("Core
+ * algorithm", step 2: one forward pass over KV_full).
+ *
+ * Query row i of a request (0 <= i < n_rows, position ctx+i) and head h attend to KV_full rows
+ * 0..ctx-1 and to the drafted tokens' rows 0..i (causal among the drafts), scale 1/sqrt(d).
+ * Runs the rows of one KV head (n_rows * Hq/Hkv of them) as dense tensor-core tiles.
+ */
+typedef struct vc_verify_req {
+  vc_kv_full full;     /* KV_full in device memory */
+  const void* q;       /* bf16 [n_rows][Hq][d] */
+  const void* k_new;   /* bf16 [Hkv][new_cap][d], rows 0..n_rows-1: the drafted tokens' keys */
+  const void* v_new;
+  int32_t new_cap;     /* rows per head of k_new/v_new */
+  int32_t n_rows;      /* drafted tokens to verify, >= 1 */
+  void* o;             /* bf16 [n_rows][Hq][d] output */
+} vc_verify_req;
+
+vc_status vc_verify_attn(const vc_shape* shape, const vc_verify_req* req, void* ws, size_t ws_bytes,
+                         int32_t* dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* vc_accept — greedy acceptance ("Core algorithm", step 3).
+ *
+ * logits: fp32 [B][L_max+1][V]; row i of request b is the full-cache prediction after its i-th
+ *   verified input (row 0 follows the last accepted token, row i follows draft i-1).
+ * draft: int32 [B][L_max]; L: device int32 [B], 0 <= L[b] <= L_max.
+ * a_i = argmax of row i (first maximal index; logits must be finite); n = first i < L[b] with
+ * a_i != draft[i], else L[b]. Writes out_tokens[b] = draft[0..n-1], a_n, then -1 up to L_max+1
+ * entries, and n_acc[b] = n + 1 (1..L[b]+1).
+ */
+vc_status vc_accept(int32_t B, int32_t L_max, int32_t V, const float* logits, const int32_t* draft,
+                    const int32_t* L, int32_t* out_tokens, int32_t* n_acc, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* vc_stage_full_kv — copy a request's KV_full from page-locked host memory into device memory
+ * ("Architecture support", long-context decoding: KV_full lives in CPU memory and is loaded over
+ * the host link for verification; "Cross-resource staggering (P1)": the copy overlaps other
+ * requests' drafting).
+ *
+ * Issues cudaMemcpyAsync host-to-device copies of `chunk_bytes` (0 = one copy) on copy_stream and
+ * records `done` (may be NULL) on it after the last chunk; the caller makes the verifying stream
+ * wait on `done`. host_src must be page-locked (VC_ERR_NOT_PINNED otherwise).
+ */
+vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, size_t chunk_bytes,
+                           cudaStream_t copy_stream, cudaEvent_t done);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Workspace bytes vc_draft_attn (call = VC_CALL_DRAFT) or vc_verify_attn (VC_CALL_VERIFY) needs
+ * for `shape`; max_rows = the largest n_rows of a verify call (ignored for draft). The workspace
+ * holds per-split partial outputs; it needs no initialisation and is not read after the call. */
+size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows);
+
+const char* vc_status_string(vc_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t vc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VC_H_ */

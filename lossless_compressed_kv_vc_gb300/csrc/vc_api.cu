@@ -1,0 +1,317 @@
+// C-ABI entry points of libvc: argument validation, split planning and kernel launches.
+// Validation failures return a status and launch nothing; nothing here allocates or synchronises.
+#include "vc_internal.cuh"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+namespace vc {
+cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, void* ws, size_t ws_bytes,
+                          int32_t* dev_status, cudaStream_t stream, vc_status* st);
+size_t verify_workspace_size(const vc_shape* shape, int32_t max_rows);
+}  // namespace vc
+
+using namespace vc;
+
+static bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static bool shape_ok(const vc_shape* s) {
+  return s && s->B >= 1 && s->B <= VC_MAX_BATCH && s->Hkv >= 1 && s->Hq >= s->Hkv && s->Hq % s->Hkv == 0 &&
+         (s->d == 64 || s->d == 128);
+}
+
+static int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  return v ? atoi(v) : dflt;
+}
+
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 152;
+  }
+  return n;
+}
+
+extern "C" {
+
+int32_t vc_version(void) { return 100; }
+
+const char* vc_status_string(vc_status s) {
+  switch (s) {
+    case VC_OK: return "ok";
+    case VC_ERR_INVALID: return "invalid argument";
+    case VC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case VC_ERR_CUDA: return "CUDA error";
+    case VC_ERR_NOT_PINNED: return "host buffer is not page-locked";
+    case VC_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows) {
+  if (!shape_ok(shape)) return 0;
+  if (call == VC_CALL_DRAFT) {
+    const size_t slots = (size_t)shape->B * shape->Hq * kDraftMaxSplits;
+    return slots * shape->d * sizeof(float) + slots * sizeof(float) + 256;
+  }
+  if (call == VC_CALL_VERIFY) return verify_workspace_size(shape, max_rows);
+  return 0;
+}
+
+// ---------------------------------------------------------------------------------------------
+vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const float* const* importance,
+                         const int32_t* recent, int32_t residual_min, vc_kv_comp* comp, int32_t* dev_status,
+                         cudaStream_t stream) {
+  if (!shape_ok(shape) || !full || !comp) return VC_ERR_INVALID;
+  const int B = shape->B, d = shape->d;
+  const int mode = comp[0].mode;
+  for (int b = 0; b < B; ++b) {
+    const vc_kv_full& f = full[b];
+    if (comp[b].mode != mode) return VC_ERR_UNSUPPORTED;
+    if (!aligned16(f.k) || !aligned16(f.v) || f.ctx < 1 || f.cap < f.ctx) return VC_ERR_INVALID;
+  }
+  if (mode == VC_TOKEN_DROP) {
+    if (!importance || !recent) return VC_ERR_INVALID;
+    KeepParams kp;
+    memset(&kp, 0, sizeof(kp));
+    kp.B = B;
+    kp.Hkv = shape->Hkv;
+    kp.d = d;
+    kp.dev_status = dev_status;
+    int max_keep = 0;
+    for (int b = 0; b < B; ++b) {
+      vc_kv_comp& c = comp[b];
+      const vc_kv_full& f = full[b];
+      if (!importance[b] || (reinterpret_cast<uintptr_t>(importance[b]) & 3u) || !c.idx) return VC_ERR_INVALID;
+      if (recent[b] < 0 || c.keep < recent[b] || c.keep < 1) return VC_ERR_INVALID;
+      const int keep = c.keep < f.ctx ? c.keep : f.ctx;
+      if (c.compact) {
+        if (!aligned16(c.k_rows) || !aligned16(c.v_rows) || c.rows_cap < keep) return VC_ERR_INVALID;
+      }
+      KeepReq& r = kp.req[b];
+      r.imp = importance[b];
+      r.idx = c.idx;
+      r.ctx = f.ctx;
+      r.keep = c.keep;
+      r.recent = recent[b] < f.ctx ? recent[b] : f.ctx;
+      r.k_src = static_cast<const bf16*>(f.k);
+      r.v_src = static_cast<const bf16*>(f.v);
+      r.src_cap = f.cap;
+      r.k_dst = static_cast<bf16*>(c.k_rows);
+      r.v_dst = static_cast<bf16*>(c.v_rows);
+      r.dst_cap = c.rows_cap;
+      r.compact = c.compact;
+      if (keep > max_keep) max_keep = keep;
+    }
+    if (launch_keepset(kp, max_keep, stream) != cudaSuccess) return VC_ERR_CUDA;
+    for (int b = 0; b < B; ++b) {
+      if (comp[b].keep > full[b].ctx) comp[b].keep = full[b].ctx;
+      comp[b].n_win = 0;
+      if (!comp[b].compact) {
+        comp[b].k_rows = const_cast<void*>(full[b].k);
+        comp[b].v_rows = const_cast<void*>(full[b].v);
+        comp[b].rows_cap = full[b].cap;
+      }
+    }
+    return VC_OK;
+  }
+  if (mode != VC_QUANT) return VC_ERR_INVALID;
+  if (residual_min < 0) return VC_ERR_INVALID;
+  const int bits = comp[0].bits;
+  if (bits != 2 && bits != 4) return VC_ERR_UNSUPPORTED;
+  QuantParams qp;
+  memset(&qp, 0, sizeof(qp));
+  qp.B = B;
+  qp.Hkv = shape->Hkv;
+  qp.d = d;
+  qp.bits = bits;
+  qp.dev_status = dev_status;
+  int max_ng = 0;
+  for (int b = 0; b < B; ++b) {
+    vc_kv_comp& c = comp[b];
+    const vc_kv_full& f = full[b];
+    if (c.bits != bits) return VC_ERR_UNSUPPORTED;
+    const int ng = f.ctx > residual_min ? (f.ctx - residual_min) / VC_GROUP : 0;
+    const int n_res = f.ctx - VC_GROUP * ng;
+    if (ng > 0 && (!aligned16(c.kc) || !aligned16(c.ks) || !aligned16(c.kz) || !aligned16(c.vc) ||
+                   !aligned16(c.vs) || !aligned16(c.vz)))
+      return VC_ERR_INVALID;
+    if (!aligned16(c.k_win) || !aligned16(c.v_win) || c.win_cap < n_res + 1) return VC_ERR_INVALID;
+    QuantReq& r = qp.req[b];
+    r.k = static_cast<const bf16*>(f.k);
+    r.v = static_cast<const bf16*>(f.v);
+    r.cap = f.cap;
+    r.ctx = f.ctx;
+    r.ng = ng;
+    r.n_res = n_res;
+    r.kc = c.kc;
+    r.ks = reinterpret_cast<__half*>(c.ks);
+    r.kz = reinterpret_cast<__half*>(c.kz);
+    r.vc = c.vc;
+    r.vs = reinterpret_cast<__half*>(c.vs);
+    r.vz = reinterpret_cast<__half*>(c.vz);
+    r.k_win = static_cast<bf16*>(c.k_win);
+    r.v_win = static_cast<bf16*>(c.v_win);
+    r.win_cap = c.win_cap;
+    if (ng > max_ng) max_ng = ng;
+  }
+  if (launch_quant(qp, max_ng, VC_GROUP * max_ng, stream) != cudaSuccess) return VC_ERR_CUDA;
+  for (int b = 0; b < B; ++b) {
+    comp[b].ng = qp.req[b].ng;
+    comp[b].n_win = qp.req[b].n_res;
+  }
+  return VC_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, cudaStream_t stream) {
+  if (!shape_ok(shape) || !req) return VC_ERR_INVALID;
+  const int B = shape->B, d = shape->d, Hkv = shape->Hkv, G = shape->Hq / shape->Hkv;
+  if (G > 16) return VC_ERR_UNSUPPORTED;
+  const int mode = req[0].comp.mode;
+  const int bits = req[0].comp.bits;
+  if (mode != VC_TOKEN_DROP && mode != VC_QUANT) return VC_ERR_INVALID;
+  if (mode == VC_QUANT && bits != 2 && bits != 4) return VC_ERR_UNSUPPORTED;
+  const int chunk = mode == VC_QUANT ? 32 : 16;
+
+  DraftParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.Hq = shape->Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
+  p.S_max = kDraftMaxSplits;
+  p.dev_status = dev_status;
+
+  long long total_rows = 0;
+  for (int b = 0; b < B; ++b) {
+    const vc_draft_req& q = req[b];
+    const vc_kv_comp& c = q.comp;
+    if (c.mode != mode || (mode == VC_QUANT && c.bits != bits)) return VC_ERR_UNSUPPORTED;
+    if (!aligned16(q.q) || !aligned16(q.k_new) || !aligned16(q.v_new) || !aligned16(q.o)) return VC_ERR_INVALID;
+    if (!aligned16(c.k_win) || !aligned16(c.v_win) || c.n_win < 0 || c.n_win >= c.win_cap) return VC_ERR_INVALID;
+    int n_main = 0;
+    if (mode == VC_TOKEN_DROP) {
+      if (c.keep < 0 || (c.keep > 0 && (!aligned16(c.k_rows) || !aligned16(c.v_rows) || c.rows_cap < 1)))
+        return VC_ERR_INVALID;
+      if (c.keep > 0 && !c.compact && !c.idx) return VC_ERR_INVALID;
+      if (c.compact && c.keep > c.rows_cap) return VC_ERR_INVALID;
+      n_main = c.keep;
+    } else {
+      if (c.ng < 0) return VC_ERR_INVALID;
+      if (c.ng > 0 && (!aligned16(c.kc) || !aligned16(c.ks) || !aligned16(c.kz) || !aligned16(c.vc) ||
+                       !aligned16(c.vs) || !aligned16(c.vz)))
+        return VC_ERR_INVALID;
+      n_main = VC_GROUP * c.ng;
+    }
+    total_rows += n_main;
+    DraftReqDev& r = p.req[b];
+    r.q = static_cast<const bf16*>(q.q);
+    r.k_new = static_cast<const bf16*>(q.k_new);
+    r.v_new = static_cast<const bf16*>(q.v_new);
+    r.o = static_cast<bf16*>(q.o);
+    r.idx = c.idx;
+    r.k_rows = static_cast<const bf16*>(c.k_rows);
+    r.v_rows = static_cast<const bf16*>(c.v_rows);
+    r.rows_cap = c.rows_cap;
+    r.n_main = n_main;
+    r.compact = c.compact;
+    r.kc = c.kc;
+    r.ks = reinterpret_cast<const __half*>(c.ks);
+    r.kz = reinterpret_cast<const __half*>(c.kz);
+    r.vc = c.vc;
+    r.vs = reinterpret_cast<const __half*>(c.vs);
+    r.vz = reinterpret_cast<const __half*>(c.vz);
+    r.ng = c.ng;
+    r.k_win = static_cast<bf16*>(c.k_win);
+    r.v_win = static_cast<bf16*>(c.v_win);
+    r.win_cap = c.win_cap;
+    r.n_win = c.n_win;
+  }
+  // split plan: about `waves` full waves of 2 CTAs per SM over all (request, KV head) pairs
+  const int target = env_int("VC_DRAFT_CTAS", 4 * 2 * sm_count());
+  const long long per_head_target = target / Hkv > 1 ? target / Hkv : 1;
+  long long rps = (total_rows + per_head_target - 1) / per_head_target;
+  if (rps < 64) rps = 64;
+  rps = (rps + chunk - 1) / chunk * chunk;
+  int total = 0, max_splits = 0;
+  for (int b = 0; b < B; ++b) {
+    DraftReqDev& r = p.req[b];
+    long long my = rps;
+    int ns = r.n_main > 0 ? (int)((r.n_main + my - 1) / my) : 1;
+    if (ns > kDraftMaxSplits) {
+      ns = kDraftMaxSplits;
+      my = ((r.n_main + ns - 1) / ns + chunk - 1) / chunk * chunk;
+      ns = (int)((r.n_main + my - 1) / my);
+    }
+    r.main_per_split = (int32_t)my;
+    r.n_splits = ns;
+    r.split_begin = total;
+    total += ns;
+    if (ns > max_splits) max_splits = ns;
+  }
+  if (max_splits > 1) {
+    const size_t need = vc_workspace_size(VC_CALL_DRAFT, shape, 0);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return VC_ERR_WORKSPACE;
+    const size_t slots = (size_t)B * shape->Hq * kDraftMaxSplits;
+    p.ws_o = static_cast<float*>(ws);
+    p.ws_lse = p.ws_o + slots * d;
+  }
+  const int kind = mode == VC_TOKEN_DROP ? 0 : bits;
+  return launch_draft(p, d, kind, total, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------------------------
+vc_status vc_verify_attn(const vc_shape* shape, const vc_verify_req* req, void* ws, size_t ws_bytes,
+                         int32_t* dev_status, cudaStream_t stream) {
+  vc_status st = VC_OK;
+  cudaError_t e = launch_verify(shape, req, ws, ws_bytes, dev_status, stream, &st);
+  if (st != VC_OK) return st;
+  return e == cudaSuccess ? VC_OK : VC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------------------------
+vc_status vc_accept(int32_t B, int32_t L_max, int32_t V, const float* logits, const int32_t* draft,
+                    const int32_t* L, int32_t* out_tokens, int32_t* n_acc, cudaStream_t stream) {
+  if (B < 1 || L_max < 0 || V < 1 || !logits || !L || !out_tokens || !n_acc) return VC_ERR_INVALID;
+  if (L_max > 0 && !draft) return VC_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) || (reinterpret_cast<uintptr_t>(out_tokens) & 3u)) return VC_ERR_INVALID;
+  AcceptArgs a{logits, draft, L, out_tokens, n_acc, B, L_max, V};
+  return launch_accept(a, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------------------------
+vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, size_t chunk_bytes,
+                           cudaStream_t copy_stream, cudaEvent_t done) {
+  if (!host_src || !dev_dst) return VC_ERR_INVALID;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host_src) != cudaSuccess) {
+    cudaGetLastError();
+    return VC_ERR_NOT_PINNED;
+  }
+  if (at.type != cudaMemoryTypeHost) return VC_ERR_NOT_PINNED;
+  cudaPointerAttributes dt;
+  if (cudaPointerGetAttributes(&dt, dev_dst) != cudaSuccess) {
+    cudaGetLastError();
+    return VC_ERR_INVALID;
+  }
+  if (dt.type != cudaMemoryTypeDevice) return VC_ERR_INVALID;
+  if (chunk_bytes == 0 || chunk_bytes > bytes) chunk_bytes = bytes;
+  const char* s = static_cast<const char*>(host_src);
+  char* dptr = static_cast<char*>(dev_dst);
+  for (size_t off = 0; off < bytes; off += chunk_bytes) {
+    const size_t n = bytes - off < chunk_bytes ? bytes - off : chunk_bytes;
+    if (cudaMemcpyAsync(dptr + off, s + off, n, cudaMemcpyHostToDevice, copy_stream) != cudaSuccess)
+      return VC_ERR_CUDA;
+  }
+  if (done && cudaEventRecord(done, copy_stream) != cudaSuccess) return VC_ERR_CUDA;
+  return VC_OK;
+}
+
+}  // extern "C"

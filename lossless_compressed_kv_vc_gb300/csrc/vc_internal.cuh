@@ -1,0 +1,205 @@
+// Internal declarations shared by the kernels and the C-ABI layer of libvc (sm_103a only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/vc.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "libvc is written for sm_103a (Blackwell); compile with -gencode arch=compute_103a,code=sm_103a"
+#endif
+
+namespace vc {
+
+typedef __nv_bfloat16 bf16;
+
+// Bound on every spin-wait in a kernel: a wait that exceeds it records VC_DEV_TIMEOUT and returns.
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+__device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+// ---- shared-memory addressing, mbarrier and bulk-copy (TMA engine) wrappers -------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: returns false (after recording VC_DEV_TIMEOUT) if the phase never completes.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* st) {
+  for (uint32_t it = 0; it < kSpinLimit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  set_status(st, VC_DEV_TIMEOUT);
+  return false;
+}
+
+// 1-D bulk copy global -> shared through the TMA engine, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---- warp-level tensor-core helpers (mma.sync m16n8k16) -----------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---- per-request kernel descriptors (travel by value in kernel params) -------------------------
+struct DraftReqDev {
+  const bf16* q;
+  const bf16* k_new;
+  const bf16* v_new;
+  bf16* o;
+  // main rows
+  const int32_t* idx;
+  const bf16* k_rows;
+  const bf16* v_rows;
+  int64_t rows_cap;
+  int32_t n_main;      // kept rows (drop) or 32*ng (quant)
+  int32_t compact;
+  const uint8_t* kc;
+  const __half* ks;
+  const __half* kz;
+  const uint8_t* vc;
+  const __half* vs;
+  const __half* vz;
+  int32_t ng;
+  // window
+  bf16* k_win;
+  bf16* v_win;
+  int64_t win_cap;
+  int32_t n_win;
+  // split plan
+  int32_t split_begin;
+  int32_t n_splits;
+  int32_t main_per_split;  // main rows per split (multiple of the chunk)
+};
+
+struct DraftParams {
+  DraftReqDev req[VC_MAX_BATCH];
+  int32_t B, Hq, Hkv, G;
+  float scale_log2;     // log2(e) / sqrt(d)
+  float* ws_o;          // [B][Hq][S_max][d]
+  float* ws_lse;        // [B][Hq][S_max]  (log2 domain)
+  int32_t S_max;
+  int32_t* dev_status;
+};
+
+constexpr int kDraftMaxSplits = 64;
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_draft(const DraftParams& p, int d, int mode_kind, int total_ctas, cudaStream_t s);
+
+struct AcceptArgs {
+  const float* logits;
+  const int32_t* draft;
+  const int32_t* L;
+  int32_t* out_tokens;
+  int32_t* n_acc;
+  int32_t B, L_max, V;
+};
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
+
+struct KeepReq {
+  const float* imp;
+  int32_t* idx;
+  int32_t ctx, keep, recent;
+  // compaction (optional)
+  const bf16* k_src;
+  const bf16* v_src;
+  int64_t src_cap;
+  bf16* k_dst;
+  bf16* v_dst;
+  int64_t dst_cap;
+  int32_t compact;
+};
+struct KeepParams {
+  KeepReq req[VC_MAX_BATCH];
+  int32_t B, Hkv, d;
+  int32_t* dev_status;
+};
+cudaError_t launch_keepset(const KeepParams& p, int max_keep, cudaStream_t s);
+
+struct QuantReq {
+  const bf16* k;
+  const bf16* v;
+  int64_t cap;
+  int32_t ctx, ng, n_res;
+  uint8_t* kc;
+  __half* ks;
+  __half* kz;
+  uint8_t* vc;
+  __half* vs;
+  __half* vz;
+  bf16* k_win;
+  bf16* v_win;
+  int64_t win_cap;
+};
+struct QuantParams {
+  QuantReq req[VC_MAX_BATCH];
+  int32_t B, Hkv, d, bits;
+  int32_t* dev_status;
+};
+cudaError_t launch_quant(const QuantParams& p, int max_ng, int max_tq, cudaStream_t s);
+
+}  // namespace vc

@@ -1,0 +1,194 @@
+"""Per-request buffers and descriptors for one batch of VeriCache requests on one GPU.
+
+A `Batch` owns the device tensors a round needs (full cache, compressed cache, window, outputs)
+and fills the vc.h descriptors that point at them; its methods are one C-ABI call each:
+compress -> L x draft_step -> verify -> accept ("VeriCache: Turning Lossy KV Cache into Lossless
+LLM Inference", "Core algorithm"). torch is used for memory and streams only.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import torch
+
+from . import (vc_shape, vc_kv_full, vc_kv_comp, vc_draft_req, vc_verify_req, vc_compress_kv, vc_draft_attn,
+               vc_verify_attn, vc_accept, vc_workspace_size, VC_TOKEN_DROP, VC_QUANT, VC_CALL_DRAFT,
+               VC_CALL_VERIFY)
+
+GROUP = 32
+
+
+def quant_layout(ctx: int, residual_min: int = 128):
+    """(ng, n_res) the library uses: whole 32-token groups, at least residual_min bf16 rows."""
+    ng = (ctx - residual_min) // GROUP if ctx > residual_min else 0
+    return ng, ctx - GROUP * ng
+
+
+@dataclass
+class Req:
+    mode: int
+    ctx: int
+    L: int
+    k_full: torch.Tensor            # bf16 [Hkv][cap][d] (device, or the staging buffer)
+    v_full: torch.Tensor
+    q: torch.Tensor                 # bf16 [L][Hq][d]
+    k_new: torch.Tensor             # bf16 [L][Hkv][d]
+    v_new: torch.Tensor
+    importance: Optional[torch.Tensor] = None
+    keep: int = 0
+    recent: int = 0
+    compact: bool = False
+    bits: int = 2
+    # owned buffers
+    idx: Optional[torch.Tensor] = None
+    k_rows: Optional[torch.Tensor] = None
+    v_rows: Optional[torch.Tensor] = None
+    kc: Optional[torch.Tensor] = None
+    ks: Optional[torch.Tensor] = None
+    kz: Optional[torch.Tensor] = None
+    vc: Optional[torch.Tensor] = None
+    vs: Optional[torch.Tensor] = None
+    vz: Optional[torch.Tensor] = None
+    k_win: Optional[torch.Tensor] = None
+    v_win: Optional[torch.Tensor] = None
+    o_draft: Optional[torch.Tensor] = None   # bf16 [L][Hq][d]
+    o_verify: Optional[torch.Tensor] = None  # bf16 [L][Hq][d]
+    n_res: int = 0
+
+
+class Batch:
+    """Requests of one compression mode that draft together (<= 32 per C-ABI call)."""
+
+    def __init__(self, Hq: int, Hkv: int, d: int, reqs: List[Req], residual_min: int = 128, device="cuda"):
+        assert len(reqs) >= 1
+        self.Hq, self.Hkv, self.d = Hq, Hkv, d
+        self.reqs = reqs
+        self.residual_min = residual_min
+        self.device = device
+        self.shape = vc_shape(len(reqs), Hq, Hkv, d)
+        self.L_max = max(r.L for r in reqs)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
+        for r in reqs:
+            self._alloc(r)
+        self.full = (vc_kv_full * len(reqs))()
+        self.comp = (vc_kv_comp * len(reqs))()
+        for b, r in enumerate(reqs):
+            self._fill(b, r)
+        self.ws_draft = torch.empty(vc_workspace_size(VC_CALL_DRAFT, self.shape) // 4 + 64, dtype=torch.float32,
+                                    device=device)
+        vb = vc_workspace_size(VC_CALL_VERIFY, self.shape, self.L_max)
+        self.ws_verify = torch.empty(max(vb // 4 + 64, 64), dtype=torch.float32, device=device)
+
+    def _alloc(self, r: Req):
+        Hkv, d, dev = self.Hkv, self.d, self.device
+        if r.mode == VC_TOKEN_DROP:
+            keep = min(r.keep, r.ctx)
+            r.idx = torch.empty(max(keep, 1), dtype=torch.int32, device=dev)
+            if r.compact:
+                r.k_rows = torch.empty((Hkv, keep, d), dtype=torch.bfloat16, device=dev)
+                r.v_rows = torch.empty((Hkv, keep, d), dtype=torch.bfloat16, device=dev)
+            r.n_res = 0
+        else:
+            ng, n_res = quant_layout(r.ctx, self.residual_min)
+            r.n_res = n_res
+            b = r.bits
+            u8, f16 = torch.uint8, torch.float16
+            r.kc = torch.empty((Hkv, max(ng, 1), d, 4 * b), dtype=u8, device=dev)
+            r.ks = torch.empty((Hkv, max(ng, 1), d), dtype=f16, device=dev)
+            r.kz = torch.empty((Hkv, max(ng, 1), d), dtype=f16, device=dev)
+            r.vc = torch.empty((Hkv, max(32 * ng, 1), d * b // 8), dtype=u8, device=dev)
+            r.vs = torch.empty((Hkv, max(32 * ng, 1), d // 32), dtype=f16, device=dev)
+            r.vz = torch.empty((Hkv, max(32 * ng, 1), d // 32), dtype=f16, device=dev)
+        win_cap = r.n_res + r.L + 1
+        r.k_win = torch.zeros((Hkv, win_cap, d), dtype=torch.bfloat16, device=dev)
+        r.v_win = torch.zeros((Hkv, win_cap, d), dtype=torch.bfloat16, device=dev)
+        r.o_draft = torch.empty((r.L, self.Hq, d), dtype=torch.bfloat16, device=dev)
+        r.o_verify = torch.empty((r.L, self.Hq, d), dtype=torch.bfloat16, device=dev)
+
+    def _fill(self, b: int, r: Req):
+        f = self.full[b]
+        f.k, f.v = r.k_full.data_ptr(), r.v_full.data_ptr()
+        f.ctx, f.cap = r.ctx, r.k_full.shape[1]
+        c = self.comp[b]
+        c.mode = r.mode
+        c.bits = r.bits
+        if r.mode == VC_TOKEN_DROP:
+            c.keep = r.keep
+            c.compact = int(r.compact)
+            c.idx = r.idx.data_ptr()
+            if r.compact:
+                c.k_rows, c.v_rows, c.rows_cap = r.k_rows.data_ptr(), r.v_rows.data_ptr(), r.k_rows.shape[1]
+        else:
+            c.kc, c.ks, c.kz = r.kc.data_ptr(), r.ks.data_ptr(), r.kz.data_ptr()
+            c.vc, c.vs, c.vz = r.vc.data_ptr(), r.vs.data_ptr(), r.vz.data_ptr()
+        c.k_win, c.v_win, c.win_cap = r.k_win.data_ptr(), r.v_win.data_ptr(), r.k_win.shape[1]
+
+    def set_full(self, b: int, k: torch.Tensor, v: torch.Tensor):
+        """Point request b's KV_full at other device tensors (e.g. a staging buffer)."""
+        r = self.reqs[b]
+        r.k_full, r.v_full = k, v
+        f = self.full[b]
+        f.k, f.v, f.cap = k.data_ptr(), v.data_ptr(), k.shape[1]
+
+    # ---- the round's calls -------------------------------------------------------------------
+    def compress(self, stream=None):
+        mode = self.reqs[0].mode
+        if mode == VC_TOKEN_DROP:
+            vc_compress_kv(self.shape, self.full, [r.importance for r in self.reqs], [r.recent for r in self.reqs],
+                           self.residual_min, self.comp, self.dev_status, stream)
+        else:
+            vc_compress_kv(self.shape, self.full, None, None, self.residual_min, self.comp, self.dev_status, stream)
+
+    def reset_window(self):
+        for b, r in enumerate(self.reqs):
+            self.comp[b].n_win = r.n_res
+
+    def draft_requests(self, step: int):
+        """vc_draft_req array for step `step` over the requests whose L exceeds it."""
+        act = [b for b, r in enumerate(self.reqs) if step < r.L]
+        arr = (vc_draft_req * len(act))()
+        for i, b in enumerate(act):
+            r = self.reqs[b]
+            e = arr[i]
+            e.q = r.q[step].data_ptr()
+            e.k_new = r.k_new[step].data_ptr()
+            e.v_new = r.v_new[step].data_ptr()
+            e.o = r.o_draft[step].data_ptr()
+            e.comp = self.comp[b]
+        return act, arr
+
+    def draft_step(self, step: int, stream=None):
+        act, arr = self.draft_requests(step)
+        if not act:
+            return
+        shape = vc_shape(len(act), self.Hq, self.Hkv, self.d)
+        vc_draft_attn(shape, arr, self.ws_draft, self.dev_status, stream)
+        for b in act:
+            self.comp[b].n_win += 1
+
+    def verify_requests(self):
+        arr = (vc_verify_req * len(self.reqs))()
+        for b, r in enumerate(self.reqs):
+            e = arr[b]
+            e.full = self.full[b]
+            e.q = r.q.data_ptr()
+            e.k_new = r.k_win.data_ptr() + r.n_res * self.d * 2
+            e.v_new = r.v_win.data_ptr() + r.n_res * self.d * 2
+            e.new_cap = r.k_win.shape[1]
+            e.n_rows = r.L
+            e.o = r.o_verify.data_ptr()
+        return arr
+
+    def verify(self, stream=None):
+        vc_verify_attn(self.shape, self.verify_requests(), self.ws_verify, self.dev_status, stream)
+
+
+def accept(logits: torch.Tensor, draft: torch.Tensor, L: torch.Tensor, out_tokens=None, n_acc=None, stream=None):
+    B, Lp1, V = logits.shape
+    if out_tokens is None:
+        out_tokens = torch.empty((B, Lp1), dtype=torch.int32, device=logits.device)
+    if n_acc is None:
+        n_acc = torch.empty((B,), dtype=torch.int32, device=logits.device)
+    vc_accept(B, Lp1 - 1, V, logits, draft, L, out_tokens, n_acc, stream)
+    return out_tokens, n_acc
