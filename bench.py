@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Benchmark of one VeriCache round on GB300: compress (keep-set) -> L draft steps -> verify -> accept.
+
+Workload: Llama-3-8B attention shape, batch 8, 32/8 heads, d 128, context 32768, 4x token drop
+(keep 8192 = last 512 + top 7680 by importance), L = 32 drafts, vocab 128256, planted match
+probability 0.95; full KV resident in HBM (1.07 GB, larger than L2, so no flush is needed).
+Metric: verified tokens/s = sum of accepted tokens (n_acc) over requests / round time, one
+attention layer (no weights, MLP or LM head: an attention-only proxy).
+
+  python bench.py [--gpus N --steps K --warmup W]      # the product path (CUDA kernels)
+  python bench.py --impl reference ...                  # the CPU oracle on the host cores
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs its own replica of the
+workload (the path has no exchange step): value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified tokens/s/GPU (draft+verify+accept)"
+UNIT = "tokens/s"
+PROFILE = os.path.join(ROOT, "profiles", "draft_attn_llama8b_drop4x.md")
+DRAFT_SOURCES = ["lossless_compressed_kv_vc_gb300/csrc/draft.cu", "lossless_compressed_kv_vc_gb300/csrc/vc_internal.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--sample-heads", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="run only the first B requests (a smaller case for profiler captures)")
+    a = ap.parse_args()
+    global _BATCH
+    _BATCH = a.batch
+    return a
+
+
+_BATCH = None
+
+
+def workload():
+    from workloads import configs
+    w = configs.llama8b_drop()
+    if _BATCH is not None and _BATCH < w.B:
+        w = configs.scaled(w, batch=_BATCH)
+    return w
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle leg (reference arm and cpu_baseline): one request's round on a sample of KV heads
+# ------------------------------------------------------------------------------------------------
+def oracle_round_sample(w, b: int, n_heads: int):
+    """Time the oracle on request b: keep-set, L draft steps and verify for `n_heads` KV heads,
+    accept. Returns (seconds scaled to all KV heads of the request, n_acc)."""
+    import numpy as np
+    import torch
+    import oracle as O
+    from workloads import gen
+    ri = gen.request(w, 0, b, "cpu")
+    draft, logits, L = gen.drafts_and_logits(w, 0, "cpu")
+    f = lambda t: t.to(torch.float32).numpy()
+    kf, vf, q, kn, vn = f(ri.k_full), f(ri.v_full), f(ri.q), f(ri.k_new), f(ri.v_new)
+    imp = ri.importance.numpy()
+    lg, dr = logits[b].numpy(), draft[b].numpy()
+    G = w.Hq // w.Hkv
+    t0 = time.perf_counter()
+    idx = O.keep_set(imp, w.keep[b], w.recent[b])
+    t_keep = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    for hk in range(n_heads):
+        sel = slice(hk * G, (hk + 1) * G)
+        km, vm = kf[hk:hk + 1, idx], vf[hk:hk + 1, idx]
+        empty = np.zeros((1, 0, w.d), np.float32)
+        O.draft_round(q[:, sel], km, vm, empty, empty, kn[:, hk:hk + 1], vn[:, hk:hk + 1])
+        O.verify_attn(q[:, sel], kf[hk:hk + 1], vf[hk:hk + 1], kn[:, hk:hk + 1].transpose(1, 0, 2),
+                      vn[:, hk:hk + 1].transpose(1, 0, 2))
+    t_heads = time.perf_counter() - t1
+    t2 = time.perf_counter()
+    _, n_acc = O.accept(lg, dr, w.L[b])
+    t_acc = time.perf_counter() - t2
+    return t_keep + t_heads * (w.Hkv / n_heads) + t_acc, n_acc
+
+
+def cpu_child(args):
+    """Runs in a fresh single-threaded process (BLAS threads pinned to 1 by the parent)."""
+    w = workload()
+    secs, n_acc = oracle_round_sample(w, 0, args.sample_heads)
+    print(json.dumps({"secs_per_request": secs, "n_acc": n_acc}))
+
+
+def run_cpu_child(sample_heads=1):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    t0 = time.perf_counter()
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", "--sample-heads",
+                          str(sample_heads)], capture_output=True, text=True, env=env, cwd=ROOT)
+    wall = time.perf_counter() - t0
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr[-2000:])
+    r = json.loads(out.stdout.strip().splitlines()[-1])
+    return r, wall
+
+
+def cpu_baseline_obj(w, r):
+    # the oracle processes requests one after another; the batch's expected accepted tokens are
+    # B times the sampled request's (all requests share L and p)
+    value = r["n_acc"] / r["secs_per_request"]
+    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"request 0 of {w.name}: keep-set, {w.L[0]} draft steps and verify on 1 of {w.Hkv} KV heads "
+                      f"(time x{w.Hkv}), accept; numpy float64, one thread"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = workload()
+    times, nacc = [], None
+    for i in range(args.warmup + args.steps):
+        r, _ = run_cpu_child()
+        if i >= args.warmup:
+            times.append(r["secs_per_request"])
+            nacc = r["n_acc"]
+    t = statistics.mean(times)
+    value = nacc / t
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 * w.B,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"per step: request 0 of {w.name}, 1 of {w.Hkv} KV heads timed, x{w.Hkv}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------
+# native leg
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+                out, _ = self.p.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def draft_source_hash():
+    h = hashlib.sha256()
+    for f in DRAFT_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the draft kernel from the committed ncu summary, or None when the
+    kernel source changed since it was taken."""
+    try:
+        txt = open(PROFILE).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch\s*=\s*([0-9.eE+]+)", txt)
+    h = re.search(r"kernel_source_sha256_16\s*=\s*([0-9a-f]+)", txt)
+    if not m or not h or h.group(1) != draft_source_hash():
+        return None
+    return float(m.group(1))
+
+
+def draft_algorithmic_bytes(w):
+    """Bytes one draft step must move, summed over requests, averaged over the L steps: the kept
+    K and V rows (keep x Hkv x 2 x d x 2 B), the window rows read, the index list (once per
+    request), q in and o out, and the new row read and stored."""
+    d, total = w.d, 0.0
+    for b in range(w.B):
+        keep = min(w.keep[b], w.ctx[b])
+        win_avg = (w.L[b] + 1) / 2.0  # window rows 1..L over the round
+        total += w.Hkv * (keep + win_avg) * 2 * d * 2
+        total += keep * 4
+        total += 2 * w.Hq * d * 2
+        total += 2 * 2 * w.Hkv * d * 2
+    return total
+
+
+def setup_native(w, device):
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from lossless_compressed_kv_vc_gb300 import engine, VC_TOKEN_DROP
+    from workloads import gen
+    reqs = []
+    for b in range(w.B):
+        ri = gen.request(w, 0, b, device)
+        reqs.append(engine.Req(mode=VC_TOKEN_DROP, ctx=w.ctx[b], L=w.L[b], k_full=ri.k_full, v_full=ri.v_full,
+                               q=ri.q, k_new=ri.k_new, v_new=ri.v_new, importance=ri.importance, keep=w.keep[b],
+                               recent=w.recent[b]))
+    bt = engine.Batch(w.Hq, w.Hkv, w.d, reqs, device=device)
+    bt.compress()
+    bt.prepare_steps()
+    draft, logits, L = gen.drafts_and_logits(w, 0, device)
+    out_tokens = torch.empty((w.B, w.L_max + 1), dtype=torch.int32, device=device)
+    n_acc = torch.empty((w.B,), dtype=torch.int32, device=device)
+    return bt, draft, logits, L, out_tokens, n_acc
+
+
+def run_native(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    w = workload()
+    bt, draft, logits, L, out_tokens, n_acc = setup_native(w, device)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        bt.run_round(logits, draft, L, out_tokens, n_acc, stream)
+    barrier()
+    assert int(bt.dev_status.item()) == 0, "device status set during warm-up"
+    tokens_per_step = int(n_acc.sum().item())
+
+    # timed region: K rounds, inputs resident in HBM
+    # one event pair around every draft launch of every timed round (same stream as the kernels)
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(w.L_max)]
+          for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        e0.record(stream)
+        for k in range(args.steps):
+            bt.run_round(logits, draft, L, out_tokens, n_acc, stream, draft_events=ev[k])
+        e1.record(stream)
+        barrier()
+    draft_ms = [a.elapsed_time(b) for evk in ev for a, b in evk]
+    t_ms = e0.elapsed_time(e1)
+    t_max = t_ms
+    if dist is not None:
+        tt = torch.tensor([t_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    assert int(bt.dev_status.item()) == 0, "device status set during the timed region"
+    ms_per_step = t_max / args.steps
+    value = tokens_per_step * world * args.steps / (t_max / 1e3)
+
+    # end-to-end through the public API with host buffers: H2D of the round's inputs, round, D2H
+    e2e = run_e2e(w, bt, draft, logits, L, out_tokens, n_acc, stream, args.e2e_steps or max(3, args.steps // 2),
+                  barrier, dist, world, device)
+
+    peaks, peak_kind = measured_peaks()
+    alg = draft_algorithmic_bytes(w)
+    d_ms = statistics.mean(draft_ms)
+    achieved = alg / (d_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "frac": achieved / float(peaks["hbm_gbs"]), "traffic": profiled_traffic(),
+                "kernel": "draft_attn_kernel<128,0> + draft_combine_kernel (one vc_draft_attn call)",
+                "algorithmic_bytes_per_launch": alg, "avg_launch_ms": d_ms, "peak_kind": peak_kind}
+    launches_per_step = 1 + 2 * w.L_max + 2 + 2
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ctx": w.ctx[0],
+                       "keep": w.keep[0], "recent": w.recent[0], "L": w.L[0], "V": w.V, "p": w.p[0],
+                       "tokens_per_step": tokens_per_step,
+                       "l2": "inputs larger than L2 (full KV 1.07 GB, kept rows 268 MB per draft step, logits 135 MB)"},
+            "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "roofline": roofline,
+            "clocks": clk.summary()}
+    if rank == 0 and not args.no_cpu_baseline:
+        r, wall = run_cpu_child()
+        cb = cpu_baseline_obj(w, r)
+        cb["wall_s"] = wall
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(w, bt, draft, logits, L, out_tokens, n_acc, stream, steps, barrier, dist, world, device):
+    """Each step copies that round's inputs from pinned host memory (queries, drafted K/V,
+    importance, drafts, logits, L), runs the round through the C ABI, and reads back n_acc and the
+    accepted tokens."""
+    import torch
+    dev_in = [draft, logits, L]
+    for r in bt.reqs:
+        dev_in += [r.q, r.k_new, r.v_new, r.importance]
+    host_in = [t.detach().to("cpu").pin_memory() for t in dev_in]
+    host_out = [torch.empty(out_tokens.shape, dtype=out_tokens.dtype).pin_memory(),
+                torch.empty(n_acc.shape, dtype=n_acc.dtype).pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        for h, dv in zip(host_in, dev_in):
+            dv.copy_(h, non_blocking=True)
+        bt.run_round(logits, draft, L, out_tokens, n_acc, stream)
+        host_out[0].copy_(out_tokens, non_blocking=True)
+        host_out[1].copy_(n_acc, non_blocking=True)
+
+    step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    barrier()
+    t = e0.elapsed_time(e1)
+    if dist is not None:
+        tt = torch.tensor([t], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    tokens = int(host_out[1].sum().item()) * world * steps
+    return {"value": tokens / (t / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps}
+
+
+def main():
+    args = parse()
+    if args.cpu_child:
+        return cpu_child(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main() or 0)

@@ -56,6 +56,7 @@ typedef enum vc_status {
 #define VC_DEV_BOUNDS 1        /* a gather index fell outside its buffer; the row was skipped */
 #define VC_DEV_TIMEOUT 2       /* a bounded wait on a copy gave up; outputs of that block are invalid */
 #define VC_DEV_RANGE 3         /* a quantisation scale or zero is not finite in fp16 */
+#define VC_DEV_INTERNAL 4      /* a kernel precondition failed (shared-memory alignment); outputs invalid */
 
 typedef enum vc_mode { VC_TOKEN_DROP = 0, VC_QUANT = 1 } vc_mode;
 typedef enum vc_call { VC_CALL_DRAFT = 0, VC_CALL_VERIFY = 1 } vc_call;

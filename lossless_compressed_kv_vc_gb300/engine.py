@@ -167,6 +167,29 @@ class Batch:
         for b in act:
             self.comp[b].n_win += 1
 
+    def prepare_steps(self):
+        """Descriptor arrays of every draft step of a round (window counts as after compress), so
+        a round issues its calls without rebuilding them."""
+        self._steps = []
+        self._verify_arr = self.verify_requests()
+        for s in range(self.L_max):
+            act, arr = self.draft_requests(s)
+            for i, b in enumerate(act):
+                arr[i].comp.n_win = self.reqs[b].n_res + s
+            self._steps.append((vc_shape(len(act), self.Hq, self.Hkv, self.d), arr, act))
+
+    def run_round(self, logits, draft, L, out_tokens, n_acc, stream=None, draft_events=None):
+        """compress -> L_max draft steps -> verify -> accept, all on `stream`."""
+        self.compress(stream)
+        for s, (shape, arr, act) in enumerate(self._steps):
+            if draft_events is not None:
+                draft_events[s][0].record(stream)
+            vc_draft_attn(shape, arr, self.ws_draft, self.dev_status, stream)
+            if draft_events is not None:
+                draft_events[s][1].record(stream)
+        vc_verify_attn(self.shape, self._verify_arr, self.ws_verify, self.dev_status, stream)
+        accept(logits, draft, L, out_tokens, n_acc, stream)
+
     def verify_requests(self):
         arr = (vc_verify_req * len(self.reqs))()
         for b, r in enumerate(self.reqs):

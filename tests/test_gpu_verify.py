@@ -1,0 +1,96 @@
+"""GPU parity of verification attention (tcgen05/TMEM kernel) against the oracle.
+
+Row i of a request attends to KV_full[0:ctx] and to drafted rows 0..i. Cases span several KV tiles
+with a ragged last tile, 1 to 3 query-row tiles (G * n_rows = 32 ... 320), units split across CTAs
+and whole units, d = 64 and 128; full sizes are sampled per (request, KV head)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from workloads import configs
+from tests.util import make_batch, f32, assert_attn_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__ as g
+    g.build()
+
+
+def _fill_window(bt):
+    for r in bt.reqs:
+        r.k_win[:, r.n_res: r.n_res + r.L].copy_(r.k_new.transpose(0, 1))
+        r.v_win[:, r.n_res: r.n_res + r.L].copy_(r.v_new.transpose(0, 1))
+
+
+def _check(w, reqs, heads=None, env_ctas=None, monkeypatch=None):
+    if env_ctas is not None:
+        monkeypatch.setenv("VC_VERIFY_CTAS", str(env_ctas))
+    bt = make_batch(w, reqs)
+    _fill_window(bt)
+    bt.verify()
+    torch.cuda.synchronize()
+    assert int(bt.dev_status.item()) == 0
+    G = w.Hq // w.Hkv
+    for i, b in enumerate(reqs):
+        r = bt.reqs[i]
+        q, kf, vf = f32(r.q), f32(r.k_full), f32(r.v_full)
+        kn, vn = f32(r.k_new).transpose(1, 0, 2), f32(r.v_new).transpose(1, 0, 2)
+        hs = range(w.Hkv) if heads is None else heads
+        for hk in hs:
+            sel = slice(hk * G, (hk + 1) * G)
+            ref = O.verify_attn(q[:, sel], kf[hk:hk + 1], vf[hk:hk + 1], kn[hk:hk + 1], vn[hk:hk + 1])
+            assert_attn_close(r.o_verify[:, sel], ref, f"{w.name} b{b} hk{hk}")
+
+
+def test_verify_tiny():
+    _check(configs.tiny(), [0])
+
+
+def test_verify_llama8b_scaled():
+    _check(configs.scaled(configs.llama8b_drop(), ctx_div=16, batch=3), [0, 1, 2])
+
+
+def test_verify_qwen_ragged_rows():
+    """125 query rows per KV head (L 25 x G 5), context not a multiple of 64."""
+    w = configs.scaled(configs.qwen32b_quant2(), ctx_div=64, batch=2)
+    w.ctx = [1000, 1087]
+    _check(w, [0, 1])
+
+
+def test_verify_llama70b_three_row_tiles():
+    """320 query rows per KV head (L 40 x G 8): three 128-row tiles."""
+    _check(configs.scaled(configs.llama70b_offload4(), ctx_div=128, batch=2), [0, 1])
+
+
+def test_verify_mixed_ragged():
+    w = configs.scaled(configs.mixed_serving(), ctx_div=64, batch=6)
+    _check(w, list(range(6)))
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 7, 1000])
+def test_verify_split_layouts(ctas, monkeypatch):
+    """The same inputs cut into 1 CTA (no splits), a few CTAs, and one CTA per tile."""
+    w = configs.scaled(configs.llama8b_drop(), ctx_div=64, batch=2, L=9)
+    _check(w, [0, 1], env_ctas=ctas, monkeypatch=monkeypatch)
+
+
+@pytest.mark.parametrize("L,ctx", [(1, 1), (1, 64), (70, 65), (64, 200), (3, 5000)])
+def test_verify_edges(L, ctx):
+    """One drafted row, one context token, drafts spanning two tiles, exact tile multiples."""
+    w = configs.scaled(configs.tiny(), batch=1, L=L)
+    w.ctx = [ctx]
+    _check(w, [0])
+
+
+def test_verify_llama8b_full_size_sampled():
+    w = configs.llama8b_drop()
+    _check(w, list(range(8)), heads=[0, 5])
+
+
+def test_verify_qwen32b_full_size_sampled():
+    w = configs.qwen32b_quant2()
+    _check(w, list(range(16)), heads=[2])
