@@ -163,6 +163,25 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
                         int32_t* dev_status, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------ */
+/* vc_draft_attn_noalloc — vc_draft_attn without a caller workspace. The paper has no counterpart:
+ * this is a library convenience for callers that cannot allocate device memory, for example a
+ * plugin whose host application owns every device allocation and gives it no allocator, or a
+ * serving loop that must not call cudaMalloc/cudaFree (those can synchronise the whole device).
+ *
+ * Same arguments and results as vc_draft_attn, minus ws/ws_bytes. The partials live in a fixed
+ * array of VC_DRAFT_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU that loads the
+ * library holds it until the process exits. The first call made with a given device current looks
+ * up the array's device address (cudaGetSymbolAddress) and caches it: make that first call before
+ * any stream capture. The call allocates nothing. Returns VC_ERR_WORKSPACE when the call needs more
+ * scratch than the array holds (vc_workspace_size(VC_CALL_DRAFT, shape, 0) > the limit). All calls
+ * share the array, which keeps the last call's contents (nothing in it needs clearing); calls that
+ * overlap on the GPU race on it, so issue them on one stream or order them with events. */
+#define VC_DRAFT_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+vc_status vc_draft_attn_noalloc(const vc_shape* shape, const vc_draft_req* req, int32_t* dev_status,
+                                cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
 /* vc_verify_attn — verification attention, all drafts of a request in one pass ("Core
  * algorithm", step 2: one forward pass over KV_full).
  *

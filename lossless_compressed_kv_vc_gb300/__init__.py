@@ -57,6 +57,7 @@ class vc_verify_req(C.Structure):
 _lib.vc_compress_kv.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_kv_full), C.POINTER(_p), C.POINTER(_i32),
                                 _i32, C.POINTER(vc_kv_comp), _p, _p]
 _lib.vc_draft_attn.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_draft_req), _p, C.c_size_t, _p, _p]
+_lib.vc_draft_attn_noalloc.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_draft_req), _p, _p]
 _lib.vc_verify_attn.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_verify_req), _p, C.c_size_t, _p, _p]
 _lib.vc_accept.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p, _p, _p]
 _lib.vc_stage_full_kv.argtypes = [_p, _p, C.c_size_t, C.c_size_t, _p, _p]
@@ -65,10 +66,11 @@ _lib.vc_workspace_size.restype = C.c_size_t
 _lib.vc_status_string.argtypes = [_i32]
 _lib.vc_status_string.restype = C.c_char_p
 _lib.vc_version.restype = _i32
-for _f in ("vc_compress_kv", "vc_draft_attn", "vc_verify_attn", "vc_accept", "vc_stage_full_kv"):
+for _f in ("vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_accept",
+           "vc_stage_full_kv"):
     getattr(_lib, _f).restype = _i32
 
-EXPORTS = ["vc_compress_kv", "vc_draft_attn", "vc_verify_attn", "vc_accept", "vc_stage_full_kv",
+EXPORTS = ["vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_accept", "vc_stage_full_kv",
            "vc_workspace_size", "vc_status_string", "vc_version"]
 
 
@@ -132,6 +134,12 @@ def vc_draft_attn(shape: vc_shape, req, ws=None, dev_status=None, stream=None, r
     wsb = ws.numel() * ws.element_size() if ws is not None else 0
     st = _lib.vc_draft_attn(C.byref(shape), req, _ptr(ws), wsb, _ptr(dev_status), _stream(stream))
     return _check(st, "vc_draft_attn", raise_on_error)
+
+
+def vc_draft_attn_noalloc(shape: vc_shape, req, dev_status=None, stream=None, raise_on_error=True) -> int:
+    """vc_draft_attn with the library's built-in scratch instead of a caller workspace (allocates nothing)."""
+    st = _lib.vc_draft_attn_noalloc(C.byref(shape), req, _ptr(dev_status), _stream(stream))
+    return _check(st, "vc_draft_attn_noalloc", raise_on_error)
 
 
 def vc_verify_attn(shape: vc_shape, req, ws=None, dev_status=None, stream=None, raise_on_error=True) -> int:
