@@ -38,13 +38,15 @@ DRAFT_SOURCES = ["lossless_compressed_kv_vc_gb300/csrc/draft.cu", "lossless_comp
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-heads", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--compact", action="store_true",
+                    help="gather the kept rows into a contiguous copy at compress time (inside the timed round)")
     ap.add_argument("--batch", type=int, default=None,
                     help="run only the first B requests (a smaller case for profiler captures)")
     a = ap.parse_args()
@@ -249,7 +251,7 @@ def draft_algorithmic_bytes(w):
     return total
 
 
-def setup_native(w, device):
+def setup_native(w, device, compact=False):
     import torch
     import __graft_entry__ as g
     g.build()
@@ -260,7 +262,7 @@ def setup_native(w, device):
         ri = gen.request(w, 0, b, device)
         reqs.append(engine.Req(mode=VC_TOKEN_DROP, ctx=w.ctx[b], L=w.L[b], k_full=ri.k_full, v_full=ri.v_full,
                                q=ri.q, k_new=ri.k_new, v_new=ri.v_new, importance=ri.importance, keep=w.keep[b],
-                               recent=w.recent[b]))
+                               recent=w.recent[b], compact=compact))
     bt = engine.Batch(w.Hq, w.Hkv, w.d, reqs, device=device)
     bt.compress()
     bt.prepare_steps()
@@ -282,7 +284,7 @@ def run_native(args):
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
     w = workload()
-    bt, draft, logits, L, out_tokens, n_acc = setup_native(w, device)
+    bt, draft, logits, L, out_tokens, n_acc = setup_native(w, device, compact=args.compact)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -320,7 +322,7 @@ def run_native(args):
     value = tokens_per_step * world * args.steps / (t_max / 1e3)
 
     # end-to-end through the public API with host buffers: H2D of the round's inputs, round, D2H
-    e2e = run_e2e(w, bt, draft, logits, L, out_tokens, n_acc, stream, args.e2e_steps or max(3, args.steps // 2),
+    e2e = run_e2e(w, bt, draft, logits, L, out_tokens, n_acc, stream, args.e2e_steps or max(3, min(args.steps, 100)),
                   barrier, dist, world, device)
 
     peaks, peak_kind = measured_peaks()
@@ -331,11 +333,11 @@ def run_native(args):
                 "frac": achieved / float(peaks["hbm_gbs"]), "traffic": profiled_traffic(),
                 "kernel": "draft_attn_kernel<128,0> + draft_combine_kernel (one vc_draft_attn call)",
                 "algorithmic_bytes_per_launch": alg, "avg_launch_ms": d_ms, "peak_kind": peak_kind}
-    launches_per_step = 1 + 2 * w.L_max + 2 + 2
+    launches_per_step = 1 + (1 if args.compact else 0) + 2 * w.L_max + 2 + 2
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ctx": w.ctx[0],
+            "config": {"workload": w.name, "compact_keep_set": bool(args.compact), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ctx": w.ctx[0],
                        "keep": w.keep[0], "recent": w.recent[0], "L": w.L[0], "V": w.V, "p": w.p[0],
                        "tokens_per_step": tokens_per_step,
                        "l2": "inputs larger than L2 (full KV 1.07 GB, kept rows 268 MB per draft step, logits 135 MB)"},

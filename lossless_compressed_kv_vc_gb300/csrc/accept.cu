@@ -23,6 +23,8 @@ __device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
 constexpr int kAcceptThreads = 512;
 
 __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(AcceptArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int row = blockIdx.x;
   const int rows = a.L_max + 1;
   const int b = row / rows, i = row % rows;
@@ -91,6 +93,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(AcceptArg
 }
 
 __global__ void accept_finalize_kernel(AcceptArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= a.B) return;
@@ -115,11 +119,9 @@ __global__ void accept_finalize_kernel(AcceptArgs a) {
 }
 
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
-  accept_argmax_kernel<<<a.B * (a.L_max + 1), kAcceptThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(accept_argmax_kernel, dim3(a.B * (a.L_max + 1)), dim3(kAcceptThreads), 0, s, a);
   if (e != cudaSuccess) return e;
-  accept_finalize_kernel<<<(a.B + 3) / 4, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(accept_finalize_kernel, dim3((a.B + 3) / 4), dim3(128), 0, s, a);
 }
 
 }  // namespace vc

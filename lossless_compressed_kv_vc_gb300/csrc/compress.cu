@@ -49,6 +49,8 @@ __device__ __forceinline__ int block_scan_flag(bool f, int* warp_tot, int& total
 }
 
 __global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_constant__ KeepParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const KeepReq& r = p.req[blockIdx.x];
   const int n = r.ctx, tid = threadIdx.x;
   if (r.keep >= n) {
@@ -127,6 +129,8 @@ __global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_cons
 
 // Gather kept rows into a compact copy: dst[h][j] = src[h][idx[j]] (one warp per row pair).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant__ KeepParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const KeepReq& r = p.req[blockIdx.z];
   if (!r.compact) return;
   const int keep = min(r.keep, r.ctx);
@@ -152,15 +156,11 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant_
 }
 
 cudaError_t launch_keepset(const KeepParams& p, int max_keep, cudaStream_t s) {
-  keepset_kernel<<<p.B, kKeepThreads, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(keepset_kernel, dim3(p.B), dim3(kKeepThreads), 0, s, p);
   if (e != cudaSuccess) return e;
   bool any = false;
   for (int b = 0; b < p.B; ++b) any |= p.req[b].compact != 0;
-  if (any && max_keep > 0) {
-    gather_rows_kernel<<<dim3((max_keep + 7) / 8, p.Hkv, p.B), 256, 0, s>>>(p);
-    e = cudaGetLastError();
-  }
+  if (any && max_keep > 0) e = launch_pdl(gather_rows_kernel, dim3((max_keep + 7) / 8, p.Hkv, p.B), dim3(256), 0, s, p);
   return e;
 }
 

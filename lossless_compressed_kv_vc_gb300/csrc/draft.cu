@@ -4,18 +4,27 @@
 // (drafting with KV_comp) and "Cross-resource staggering (P1)" (drafting is bound by HBM
 // bandwidth: it streams the compressed cache).
 //
-// Design (one launch per draft step, plus a small split-combine launch):
-//   grid  = (sum over requests of its KV splits, Hkv), 128 threads (4 warps).
-//   A CTA owns one (request, KV head, split). The G = Hq/Hkv query heads of the KV head are the
-//   M rows of m16n8k16 tensor-core MMAs (rows >= G are zero), so each KV row read from HBM
-//   serves all G heads. KV rows reach shared memory through 1-D bulk copies on the TMA engine
-//   (one copy per kept row: the gather by index costs no extra instruction per byte), each warp
-//   running its own ring of stages on mbarriers. Quantised groups arrive as raw codes and are
-//   dequantised in registers into a bf16 tile just before the MMAs. Each warp keeps an online
-//   softmax (fp32, exp2 domain); warps merge in shared memory and a split writes either the final
-//   bf16 row or an (o, lse) partial that the combine kernel merges.
-//   The step's own K/V row (k_new, v_new) is read straight from its input and also stored into
-//   window row n_win by the first split (fused append).
+// Work decomposition (one launch per draft step, plus a small combine launch):
+//   For one KV head, each request's rows form a list of chunks: its KV_comp rows (16 kept bf16
+//   rows, or one 32-token quantised group, per chunk) followed by its bf16 window rows (16 per
+//   chunk; the last window row is this step's own K/V). The chunk lists of all requests are
+//   concatenated and cut into equal contiguous ranges, one per warp, over one wave of 4-warp CTAs
+//   and one grid row per KV head, so every warp streams the same number of bytes. A warp owns its
+//   range outright: its own ring of shared-memory stages, its own online softmax, and at each
+//   request boundary either the final bf16 row (the request lay entirely inside the warp's range)
+//   or an (o, lse) partial in slot warp + request, merged by the combine kernel. No CTA barrier.
+//
+// Tensor cores: scores are S^T = K Q^T and the output O^T += V^T P^T on m16n8k16 MMAs with the
+// 16 tokens (or 16 channels) of a tile as M and the query heads of the KV head as N (8 per MMA,
+// zero-padded), so a KV byte serves all G heads and a 16-token tile costs d/8 MMAs. P^T, produced
+// in the accumulator layout, becomes the next B operand through an in-register 8x8 transpose
+// (movmatrix). O^T is rescaled only when some head's running maximum moved.
+//
+// Loads: kept bf16 rows arrive by 16-byte cp.async, two whole rows per warp instruction, gathered by
+// index (indices prefetched one stage ahead); quantised groups arrive as six contiguous 1-D bulk
+// copies on the TMA engine and are dequantised in registers into a bf16 tile before the MMAs.
+// The warp holding a request's first chunk also stores the step's K/V row into window row n_win
+// (fused append); that row is read from its input, so no other warp depends on the store.
 #include "vc_internal.cuh"
 
 #include <math.h>
@@ -28,101 +37,103 @@ struct DraftCfg {
   static constexpr int ROWB = D * 2;                     // bytes of one bf16 row
   static constexpr int RS = ROWB + 16;                   // padded smem row stride (conflict-free ldmatrix)
   static constexpr int TILE = 16 * RS;                   // 16 bf16 rows
-  static constexpr int QRAW = (KIND == 0) ? 0 : 8 * D * (KIND + 1);  // raw bytes of one 32-token group
+  static constexpr int BITS = (KIND == 0) ? 2 : KIND;
+  static constexpr int QRAW = (KIND == 0) ? 0 : 8 * D * (BITS + 1);  // raw bytes of one 32-token group
   static constexpr int STAGE = (2 * TILE > QRAW) ? 2 * TILE : QRAW;
-  static constexpr int NST = (KIND == 0) ? 3 : 2;
+  static constexpr int NST = 2;
+  static constexpr int CTAS_PER_SM = (KIND == 0) ? 3 : 2;
   static constexpr int DQ = (KIND == 0) ? 0 : 2 * TILE;  // dequantised K+V tile (quant only)
   static constexpr int PER_WARP = NST * STAGE + DQ;
   static constexpr int BAR_OFF = NW * PER_WARP;
   static constexpr int SMEM = BAR_OFF + NW * NST * 8;
   static constexpr int CHUNK_MAIN = (KIND == 0) ? 16 : 32;
-  static constexpr int NT = D / 8;                       // output n-tiles
-  static constexpr int KS = D / 16;                      // k-steps over the head dim
+  static constexpr int MT = D / 16;                      // 16-wide tiles over the head dim
   // raw layout of a quantised group inside a stage
+  static constexpr int KCB = D * 4 * BITS;               // key codes of one group
   static constexpr int OFF_KC = 0;
-  static constexpr int OFF_KS = OFF_KC + D * 4 * (KIND == 0 ? 2 : KIND);
+  static constexpr int OFF_KS = OFF_KC + KCB;
   static constexpr int OFF_KZ = OFF_KS + 2 * D;
   static constexpr int OFF_VC = OFF_KZ + 2 * D;
-  static constexpr int OFF_VS = OFF_VC + 4 * D * (KIND == 0 ? 2 : KIND);
+  static constexpr int OFF_VS = OFF_VC + KCB;
   static constexpr int OFF_VZ = OFF_VS + 2 * D;
-  static_assert(NW * PER_WARP <= 112 * 1024, "two CTAs per SM");
+  static_assert(SMEM + 1024 <= 228 * 1024 / CTAS_PER_SM, "CTAs per SM");
 };
 
-// Scores for one 16-token tile, online-softmax update and P*V accumulation.
-template <int D>
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// One 16-token tile: scores, online softmax (per query head, exp2 domain) and P V accumulation.
+// qb: Q^T B fragments [head block][k-step][2]; o: O^T accumulators [head block][channel tile][4];
+// m, l: running max and (lane-partial) sum for this lane's two heads of each head block.
+template <int D, int NHB>
 __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt, int cnt, int RS, float scale_log2,
-                                            const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4], float& m0,
-                                            float& m1, float& l0, float& l1, int lane) {
-  float s[2][4];
+                                            const uint32_t (&qb)[NHB][D / 16][2], float (&o)[NHB][D / 16][4],
+                                            float (&m)[NHB][2], float (&l)[NHB][2], int lane) {
+  float s[NHB][4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+    for (int e = 0; e < 4; ++e) s[hb][e] = 0.f;
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ks += 2) {
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint8_t* a_ptr = kt + ((lane & 7) + 8 * ((lane >> 3) & 1)) * RS + (16 * ks + 8 * (lane >> 4)) * 2;
+    uint32_t a[4];
+    ldsm_x4(a[0], a[1], a[2], a[3], a_ptr);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const uint8_t* a = kt + (nt * 8 + (lane & 7)) * RS + (16 * ks + 8 * (lane >> 3)) * 2;
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(b0, b1, b2, b3, a);
-      mma_bf16_16816(s[nt], qa[ks], b0, b1);
-      mma_bf16_16816(s[nt], qa[ks + 1], b2, b3);
-    }
+    for (int hb = 0; hb < NHB; ++hb) mma_bf16_16816(s[hb], a, qb[hb][ks][0], qb[hb][ks][1]);
   }
-  const int tq = 2 * (lane & 3);
-  float mx0 = -INFINITY, mx1 = -INFINITY;
+  // rows of the accumulator are tokens lane/4 and lane/4 + 8; columns heads 2(lane%4) + {0,1}
+  const bool ok0 = (lane >> 2) < cnt, ok1 = (lane >> 2) + 8 < cnt;
+  float p[NHB][2][2];  // [head block][head e][token row 0/1]
+  bool moved = false;
+  float corr[NHB][2];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const bool ok = (nt * 8 + tq + e) < cnt;
-      s[nt][e] = ok ? s[nt][e] * scale_log2 : -INFINITY;
-      s[nt][e + 2] = ok ? s[nt][e + 2] * scale_log2 : -INFINITY;
-      mx0 = fmaxf(mx0, s[nt][e]);
-      mx1 = fmaxf(mx1, s[nt][e + 2]);
+      const float x0 = ok0 ? s[hb][e] * scale_log2 : -INFINITY;
+      const float x1 = ok1 ? s[hb][e + 2] * scale_log2 : -INFINITY;
+      float mx = fmaxf(x0, x1);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mn = fmaxf(m[hb][e], mx);
+      const float mu = (mn == -INFINITY) ? 0.f : mn;
+      corr[hb][e] = exp2f(m[hb][e] - mu);
+      moved |= mn != m[hb][e];
+      m[hb][e] = mn;
+      p[hb][e][0] = exp2f(x0 - mu);
+      p[hb][e][1] = exp2f(x1 - mu);
+      l[hb][e] = l[hb][e] * corr[hb][e] + p[hb][e][0] + p[hb][e][1];
     }
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-  const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
-  const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
-  const float c0 = exp2f(m0 - mu0), c1 = exp2f(m1 - mu1);
-  m0 = mn0;
-  m1 = mn1;
-  float p[2][4];
-  float ps0 = 0.f, ps1 = 0.f;
+  if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    p[nt][0] = exp2f(s[nt][0] - mu0);
-    p[nt][1] = exp2f(s[nt][1] - mu0);
-    p[nt][2] = exp2f(s[nt][2] - mu1);
-    p[nt][3] = exp2f(s[nt][3] - mu1);
-    ps0 += p[nt][0] + p[nt][1];
-    ps1 += p[nt][2] + p[nt][3];
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        o[hb][mt][0] *= corr[hb][0];
+        o[hb][mt][1] *= corr[hb][1];
+        o[hb][mt][2] *= corr[hb][0];
+        o[hb][mt][3] *= corr[hb][1];
+      }
   }
-  l0 = l0 * c0 + ps0;
-  l1 = l1 * c1 + ps1;
+  // P^T as the B operand (k = token, n = head): transpose the two 8x8 bf16 blocks of the accumulator
+  uint32_t pb[NHB][2];
 #pragma unroll
-  for (int nt = 0; nt < D / 8; ++nt) {
-    o[nt][0] *= c0;
-    o[nt][1] *= c0;
-    o[nt][2] *= c1;
-    o[nt][3] *= c1;
+  for (int hb = 0; hb < NHB; ++hb) {
+    pb[hb][0] = movmatrix_t(pack_bf16x2(p[hb][0][0], p[hb][1][0]));  // tokens 0-7
+    pb[hb][1] = movmatrix_t(pack_bf16x2(p[hb][0][1], p[hb][1][1]));  // tokens 8-15
   }
-  uint32_t pa[4];
-  pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-  pa[1] = pack_bf16x2(p[0][2], p[0][3]);
-  pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-  pa[3] = pack_bf16x2(p[1][2], p[1][3]);
 #pragma unroll
-  for (int nd = 0; nd < D / 16; ++nd) {
-    const uint8_t* a = vt + ((lane & 7) + 8 * ((lane >> 3) & 1)) * RS + (16 * nd + 8 * (lane >> 4)) * 2;
-    uint32_t b0, b1, b2, b3;
-    ldsm_x4_t(b0, b1, b2, b3, a);
-    mma_bf16_16816(o[2 * nd], pa, b0, b1);
-    mma_bf16_16816(o[2 * nd + 1], pa, b2, b3);
+  for (int mt = 0; mt < D / 16; ++mt) {
+    const uint8_t* a_ptr = vt + ((lane & 7) + 8 * (lane >> 4)) * RS + (16 * mt + 8 * ((lane >> 3) & 1)) * 2;
+    uint32_t a[4];
+    ldsm_x4_t(a[0], a[1], a[2], a[3], a_ptr);
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) mma_bf16_16816(o[hb][mt], a, pb[hb][0], pb[hb][1]);
   }
 }
 
@@ -191,259 +202,335 @@ __device__ __forceinline__ void dequant_half(const uint8_t* raw, uint8_t* kt, ui
   }
 }
 
-template <int D, int KIND>
-__global__ void __launch_bounds__(128, 2) draft_attn_kernel(const __grid_constant__ DraftParams p) {
+// Advance a request cursor to the request holding chunk `pos` (positions only grow along a warp's
+// range, so each call site keeps its own cursor).
+__device__ __forceinline__ int draft_find_req(const DraftParams& p, int64_t pos, int& cursor) {
+  while (cursor + 1 < p.B && p.req[cursor + 1].chunk_begin <= pos) ++cursor;
+  return cursor;
+}
+
+// First and last virtual warp whose range holds a chunk of request b (ranges: [w*T/W, (w+1)*T/W)).
+__device__ __forceinline__ void warp_span(const DraftParams& p, int b, int64_t& w0, int64_t& w1) {
+  const int64_t T = p.total_chunks, W = p.n_vwarps;
+  const int64_t c0 = p.req[b].chunk_begin, c1 = c0 + p.req[b].n_chunks;  // [c0, c1)
+  w0 = ((c0 + 1) * W - 1) / T;
+  w1 = (c1 * W - 1) / T;
+}
+
+template <int D, int KIND, int NHB>
+__global__ void __launch_bounds__(128, DraftCfg<D, KIND>::CTAS_PER_SM)
+    draft_attn_kernel(const __grid_constant__ DraftParams p) {
   using C = DraftCfg<D, KIND>;
+  constexpr bool BF16_ROWS = KIND == 0;  // cp.async pipeline; otherwise bulk copies on mbarriers
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hk = blockIdx.y;
-  int b = 0;
-#pragma unroll 1
-  for (int i = 1; i < p.B; ++i)
-    if (p.req[i].split_begin <= (int)blockIdx.x) b = i;
-  const DraftReqDev& r = p.req[b];
-  const int split = (int)blockIdx.x - r.split_begin;
   const int G = p.G;
+  const int64_t T = p.total_chunks, W = p.n_vwarps;
+  const int64_t wg = (int64_t)blockIdx.x * C::NW + warp;
+  const int64_t p0 = wg * T / W, p1 = (wg + 1) * T / W;
+  const int n = (int)(p1 - p0);
+  if (n <= 0) {
+    pdl_launch_dependents();
+    return;
+  }
 
   uint8_t* wb = smem + warp * C::PER_WARP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF) + warp * C::NST;
-
-  // fused append of this step's K/V row into the window (first split only)
-  if (split == 0 && warp == 0) {
-    constexpr int V16 = C::ROWB / 16;
-    const int l = lane & 15;
-    if (l < V16) {
-      const uint4* src = reinterpret_cast<const uint4*>((lane < 16 ? r.k_new : r.v_new) + (size_t)hk * D);
-      bf16* dst_row = (lane < 16 ? r.k_win : r.v_win) + ((size_t)hk * r.win_cap + r.n_win) * D;
-      reinterpret_cast<uint4*>(dst_row)[l] = src[l];
-    }
-  }
-
-  // zero the warp's buffers so rows never written hold finite values (masked with p = 0)
-  for (int i = lane; i < C::PER_WARP / 16; i += 32) reinterpret_cast<uint4*>(wb)[i] = make_uint4(0, 0, 0, 0);
-  if (lane == 0) {
+  if (!BF16_ROWS && lane == 0) {
     for (int s = 0; s < C::NST; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
-  fence_proxy_async_smem();
   __syncwarp();
+  pdl_launch_dependents();
+  pdl_wait();
 
-  // query fragments: rows = heads of this KV head (zero beyond G), columns = head dim
-  uint32_t qa[C::KS][4];
-  {
-    const int g0 = lane >> 2, g1 = g0 + 8;
-    const int cq = 2 * (lane & 3);
-    const bf16* qb = r.q + (size_t)hk * G * D;
-#pragma unroll
-    for (int ks = 0; ks < C::KS; ++ks) {
-      const int c = 16 * ks + cq;
-      qa[ks][0] = g0 < G ? *reinterpret_cast<const uint32_t*>(qb + g0 * D + c) : 0u;
-      qa[ks][1] = g1 < G ? *reinterpret_cast<const uint32_t*>(qb + g1 * D + c) : 0u;
-      qa[ks][2] = g0 < G ? *reinterpret_cast<const uint32_t*>(qb + g0 * D + c + 8) : 0u;
-      qa[ks][3] = g1 < G ? *reinterpret_cast<const uint32_t*>(qb + g1 * D + c + 8) : 0u;
+  // chunk i of this warp -> (request, chunk within request)
+  int cur_row = 0, cur_issue = 0, cur_proc = 0;
+  auto locate = [&](int i, int& b, int& lc, int& cursor) {
+    const int64_t pos = p0 + i;
+    b = draft_find_req(p, pos, cursor);
+    lc = (int)(pos - p.req[b].chunk_begin);
+  };
+  // the row a lane copies for chunk i (its lane & 15 row), or -1: a token index for kept rows,
+  // a window row number for window chunks; loaded one stage ahead of its copy
+  auto row_of = [&](int i) -> int {
+    int b, lc;
+    locate(i, b, lc, cur_row);
+    const DraftReqDev& r = p.req[b];
+    const int row = lane & 15;
+    if (lc < r.n_mc) {
+      if (!BF16_ROWS) return 0;
+      const int j = lc * 16 + row;
+      if (j >= r.n_main) return -1;
+      return r.compact ? j : __ldg(r.idx + j);
     }
-  }
+    const int j = (lc - r.n_mc) * 16 + row;
+    return j <= r.n_win ? j : -1;
+  };
 
-  // chunk list of this split: main chunks, then (last split) window chunks of 16 rows
-  const int m_begin = split * r.main_per_split;
-  const int m_end = min(r.n_main, m_begin + r.main_per_split);
-  const int n_mc = m_end > m_begin ? (m_end - m_begin + C::CHUNK_MAIN - 1) / C::CHUNK_MAIN : 0;
-  const bool last = split == r.n_splits - 1;
-  const int n_w = last ? r.n_win + 1 : 0;
-  const int n_wc = (n_w + 15) / 16;
-  const int n_chunks = n_mc + n_wc;
-  const int my_n = n_chunks > warp ? (n_chunks - warp + C::NW - 1) / C::NW : 0;
-
-  auto issue = [&](int i, int st) {
-    const int c = warp + C::NW * i;
+  auto issue = [&](int i, int st, int t) {
+    int b, lc;
+    locate(i, b, lc, cur_issue);
+    const DraftReqDev& r = p.req[b];
     uint8_t* sb = wb + st * C::STAGE;
-    if (KIND != 0 && c < n_mc) {
+    if (!BF16_ROWS && lc < r.n_mc) {
       // one quantised 32-token group: six contiguous runs
-      const int g = (m_begin / 32) + c;
+      const int g = lc;
       const int Tq = 32 * r.ng;
-      constexpr int KCB = D * 4 * (KIND == 0 ? 2 : KIND);
       if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::QRAW);
       __syncwarp();
-      if (lane == 0) bulk_g2s(sb + C::OFF_KC, r.kc + ((size_t)hk * r.ng + g) * KCB, KCB, &bars[st]);
+      if (lane == 0) bulk_g2s(sb + C::OFF_KC, r.kc + ((size_t)hk * r.ng + g) * C::KCB, C::KCB, &bars[st]);
       if (lane == 1) bulk_g2s(sb + C::OFF_KS, r.ks + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st]);
       if (lane == 2) bulk_g2s(sb + C::OFF_KZ, r.kz + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st]);
-      if (lane == 3) bulk_g2s(sb + C::OFF_VC, r.vc + ((size_t)hk * Tq + 32 * g) * (D * (KIND == 0 ? 2 : KIND) / 8),
-                              KCB, &bars[st]);
+      if (lane == 3) bulk_g2s(sb + C::OFF_VC, r.vc + ((size_t)hk * Tq + 32 * g) * (D * C::BITS / 8), C::KCB, &bars[st]);
       if (lane == 4) bulk_g2s(sb + C::OFF_VS, r.vs + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st]);
       if (lane == 5) bulk_g2s(sb + C::OFF_VZ, r.vz + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st]);
       return;
     }
-    // 16 bf16 rows: lanes 0-15 copy K rows, lanes 16-31 the matching V rows
+    // 16 bf16 rows: lane & 15 names the row; lanes 0-15 own its K row, lanes 16-31 its V row
     const int row = lane & 15;
     const bool isv = lane >= 16;
     const bf16* src = nullptr;
-    if (c < n_mc) {
-      const int j = m_begin + c * 16 + row;
-      if (j < m_end) {
-        int t = r.compact ? j : __ldg(r.idx + j);
-        if (t >= 0 && (int64_t)t < r.rows_cap) {
+    if (lc < r.n_mc) {
+      if (t >= 0) {
+        if ((int64_t)t < r.rows_cap)
           src = (isv ? r.v_rows : r.k_rows) + ((size_t)hk * r.rows_cap + t) * D;
-        } else {
+        else
           set_status(p.dev_status, VC_DEV_BOUNDS);
-        }
       }
-    } else {
-      const int j = (c - n_mc) * 16 + row;
-      if (j < r.n_win) {
-        src = (isv ? r.v_win : r.k_win) + ((size_t)hk * r.win_cap + j) * D;
-      } else if (j == r.n_win) {
-        src = (isv ? r.v_new : r.k_new) + (size_t)hk * D;
+    } else if (t >= 0) {
+      src = t < r.n_win ? (isv ? r.v_win : r.k_win) + ((size_t)hk * r.win_cap + t) * D
+                        : (isv ? r.v_new : r.k_new) + (size_t)hk * D;
+    }
+    if (BF16_ROWS) {
+      // instruction k copies rows RPI*k .. RPI*k+RPI-1 of the 32 (K rows, then V rows): lane l
+      // moves 16-byte piece l % PPR of its row; rows without a source are zero-filled
+      constexpr int PPR = C::ROWB / 16;  // pieces per row: 16 (d=128) or 8 (d=64)
+      constexpr int RPI = 32 / PPR;      // rows per instruction
+      const unsigned long long sp = reinterpret_cast<unsigned long long>(src);
+      const int piece = lane % PPR;
+#pragma unroll
+      for (int k = 0; k < 32 / RPI; ++k) {
+        const int R = RPI * k + lane / PPR;
+        const unsigned long long rs = __shfl_sync(0xffffffffu, sp, R);
+        uint8_t* dst = sb + (R >= 16 ? C::TILE : 0) + (R & 15) * C::RS + piece * 16;
+        const uint8_t* srow = reinterpret_cast<const uint8_t*>(rs);
+        cp_async16(dst, srow ? srow + piece * 16 : reinterpret_cast<const uint8_t*>(r.k_new), srow ? 16u : 0u);
       }
+      cp_async_commit();
+      return;
+    }
+    uint8_t* dst = sb + (isv ? C::TILE : 0) + row * C::RS;
+    if (!src) {
+#pragma unroll
+      for (int e = 0; e < C::ROWB / 16; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
     }
     const unsigned ball = __ballot_sync(0xffffffffu, src != nullptr);
     if (lane == 0) mbar_arrive_expect_tx(&bars[st], __popc(ball) * C::ROWB);
     __syncwarp();
-    if (src) bulk_g2s(sb + (isv ? C::TILE : 0) + row * C::RS, src, C::ROWB, &bars[st]);
+    if (src) bulk_g2s(dst, src, C::ROWB, &bars[st]);
   };
 
-  float o[C::NT][4];
-#pragma unroll
-  for (int nt = 0; nt < C::NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[NHB][C::MT][4];
+  float m[NHB][2], l[NHB][2];
+  uint32_t qb[NHB][C::MT][2];
+  int cur_b = -1;
 
-  const int pre = my_n < C::NST ? my_n : C::NST;
-  for (int i = 0; i < pre; ++i) issue(i, i);
-  bool ok = true;
-#pragma unroll 1
-  for (int i = 0; i < my_n; ++i) {
-    const int st = i % C::NST;
-    if (!mbar_wait_bounded(&bars[st], (i / C::NST) & 1, p.dev_status)) {
-      // drain what is still in flight (bounded) and stop
-      for (int j = i + 1; j < my_n && j < i + C::NST; ++j)
-        mbar_wait_bounded(&bars[j % C::NST], (j / C::NST) & 1, p.dev_status);
-      ok = false;
-      break;
+  auto reset = [&]() {
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[hb][mt][e] = 0.f;
+      m[hb][0] = m[hb][1] = -INFINITY;
+      l[hb][0] = l[hb][1] = 0.f;
     }
-    const int c = warp + C::NW * i;
+  };
+  // Q^T B fragments: k = channel 16ks + 2(lane%4) (+8), n = head 8hb + lane/4 (zero beyond G)
+  auto load_q = [&](int b) {
+    const bf16* qbase = p.req[b].q + (size_t)hk * G * D;
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+      const int h = 8 * hb + (lane >> 2);
+#pragma unroll
+      for (int ks = 0; ks < C::MT; ++ks) {
+        const int c = 16 * ks + 2 * (lane & 3);
+        qb[hb][ks][0] = h < G ? __ldg(reinterpret_cast<const unsigned int*>(qbase + h * D + c)) : 0u;
+        qb[hb][ks][1] = h < G ? __ldg(reinterpret_cast<const unsigned int*>(qbase + h * D + c + 8)) : 0u;
+      }
+    }
+  };
+  // end of request b inside this warp: final bf16 output, or an (o, lse) partial in slot wg + b.
+  // The lane holds O^T[channel 16mt + lane/4 (+8)][head 8hb + 2(lane%4) + e].
+  auto finish = [&](int b) {
+    int64_t w0, w1;
+    warp_span(p, b, w0, w1);
+    const bool whole = w0 == w1;
+    const DraftReqDev& r = p.req[b];
+    const size_t slot = (size_t)hk * (W + p.B) + (size_t)(wg + b);
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float lt = l[hb][e];
+        lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        const int h = 8 * hb + 2 * (lane & 3) + e;
+        if (h >= G) continue;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+          const int c = 16 * mt + (lane >> 2);
+          const float v0 = o[hb][mt][e] * inv, v1 = o[hb][mt][e + 2] * inv;
+          if (whole) {
+            bf16* dst = r.o + (size_t)(hk * G + h) * D;
+            dst[c] = __float2bfloat16_rn(v0);
+            dst[c + 8] = __float2bfloat16_rn(v1);
+          } else {
+            float* dst = p.ws_o + (slot * G + h) * D;
+            dst[c] = v0;
+            dst[c + 8] = v1;
+          }
+        }
+        if (!whole && (lane >> 2) == 0) p.ws_lse[slot * G + h] = lt > 0.f ? m[hb][e] + log2f(lt) : -INFINITY;
+      }
+  };
+
+  const int pre = n < C::NST ? n : C::NST;
+  for (int i = 0; i < pre; ++i) issue(i, i, row_of(i));
+  if (BF16_ROWS)
+    for (int i = pre; i < C::NST; ++i) cp_async_commit();  // one group per stage in flight
+#pragma unroll 1
+  for (int i = 0; i < n; ++i) {
+    const int st = i % C::NST;
+    const int t_next = (i + C::NST < n) ? row_of(i + C::NST) : -1;  // prefetch: consumed after this chunk
+    int b, lc;
+    locate(i, b, lc, cur_proc);
+    if (b != cur_b) {
+      if (cur_b >= 0) finish(cur_b);
+      reset();
+      load_q(b);
+      cur_b = b;
+      if (lc == 0) {
+        // fused append of the step's K/V row (the warp holding the request's first chunk)
+        const DraftReqDev& r = p.req[b];
+        constexpr int V16 = C::ROWB / 16;
+        const int l16 = lane & 15;
+        if (l16 < V16) {
+          const uint4* src = reinterpret_cast<const uint4*>((lane < 16 ? r.k_new : r.v_new) + (size_t)hk * D);
+          bf16* dst_row = (lane < 16 ? r.k_win : r.v_win) + ((size_t)hk * r.win_cap + r.n_win) * D;
+          reinterpret_cast<uint4*>(dst_row)[l16] = __ldg(src + l16);
+        }
+      }
+    }
+    if (BF16_ROWS) {
+      cp_async_wait<C::NST - 1>();  // this lane's copies of chunk i have landed
+      __syncwarp();                  // ... and every other lane's
+    } else if (!mbar_wait_bounded(&bars[st], (i / C::NST) & 1, p.dev_status)) {
+      for (int j = i + 1; j < n && j < i + C::NST; ++j) mbar_wait_bounded(&bars[j % C::NST], (j / C::NST) & 1, p.dev_status);
+      return;
+    }
+    const DraftReqDev& r = p.req[b];
     uint8_t* sb = wb + st * C::STAGE;
-    if (KIND != 0 && c < n_mc) {
+    if (!BF16_ROWS && lc < r.n_mc) {
       uint8_t* kt = wb + C::NST * C::STAGE;
       uint8_t* vt = kt + C::TILE;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
-        dequant_half<D, (KIND == 0 ? 2 : KIND)>(sb, kt, vt, half, lane);
+        dequant_half<D, C::BITS>(sb, kt, vt, half, lane);
         __syncwarp();
-        tile_attend<D>(kt, vt, 16, C::RS, p.scale_log2, qa, o, m0, m1, l0, l1, lane);
+        tile_attend<D, NHB>(kt, vt, 16, C::RS, p.scale_log2, qb, o, m, l, lane);
         __syncwarp();
       }
     } else {
-      const int cnt = (c < n_mc) ? min(16, m_end - (m_begin + c * 16)) : min(16, n_w - (c - n_mc) * 16);
-      tile_attend<D>(sb, sb + C::TILE, cnt, C::RS, p.scale_log2, qa, o, m0, m1, l0, l1, lane);
+      const int cnt = (lc < r.n_mc) ? min(16, r.n_main - lc * 16) : min(16, r.n_win + 1 - (lc - r.n_mc) * 16);
+      tile_attend<D, NHB>(sb, sb + C::TILE, cnt, C::RS, p.scale_log2, qb, o, m, l, lane);
     }
     __syncwarp();
-    if (i + C::NST < my_n) {
-      fence_proxy_async_smem();
-      issue(i + C::NST, st);
+    if (i + C::NST < n) {
+      if (!BF16_ROWS) fence_proxy_async_smem();
+      issue(i + C::NST, st, t_next);
+    } else if (BF16_ROWS) {
+      cp_async_commit();  // empty group: the wait above always leaves NST-1 groups pending
     }
   }
-  (void)ok;
-
-  // per-warp results -> shared memory (reusing the warp's stage area), then merge across warps
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  __syncthreads();  // every warp is done with its stages
-  float* mo = reinterpret_cast<float*>(wb);  // [16][D] o, then m[16], l[16]
-  float* mm = mo + 16 * D;
-  float* ml = mm + 16;
-  {
-    const int g0 = lane >> 2, g1 = g0 + 8;
-    const int cq = 2 * (lane & 3);
-#pragma unroll
-    for (int nt = 0; nt < C::NT; ++nt) {
-      mo[g0 * D + nt * 8 + cq] = o[nt][0];
-      mo[g0 * D + nt * 8 + cq + 1] = o[nt][1];
-      mo[g1 * D + nt * 8 + cq] = o[nt][2];
-      mo[g1 * D + nt * 8 + cq + 1] = o[nt][3];
-    }
-    if ((lane & 3) == 0) {
-      mm[g0] = m0;
-      ml[g0] = l0;
-      mm[g1] = m1;
-      ml[g1] = l1;
-    }
-  }
-  __syncthreads();
-  const bool single = r.n_splits == 1;
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-    const int g = e / D, c = e % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < C::NW; ++w) M = fmaxf(M, reinterpret_cast<float*>(smem + w * C::PER_WARP)[16 * D + g]);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float Ls = 0.f, Os = 0.f;
-#pragma unroll
-    for (int w = 0; w < C::NW; ++w) {
-      const float* base = reinterpret_cast<float*>(smem + w * C::PER_WARP);
-      const float wt = exp2f(base[16 * D + g] - Mu);
-      Ls += wt * base[16 * D + 16 + g];
-      Os += wt * base[g * D + c];
-    }
-    const float val = Ls > 0.f ? Os / Ls : 0.f;
-    const int h = hk * G + g;
-    if (single) {
-      r.o[(size_t)h * D + c] = __float2bfloat16_rn(val);
-    } else {
-      const size_t slot = ((size_t)b * p.Hq + h) * p.S_max + split;
-      p.ws_o[slot * D + c] = val;
-      if (c == 0) p.ws_lse[slot] = Ls > 0.f ? Mu + log2f(Ls) : -INFINITY;
-    }
-  }
+  if (BF16_ROWS) cp_async_wait<0>();
+  finish(cur_b);
 }
 
-// Merge the per-split partials (o_s, lse_s) of one (request, head): o = sum_s 2^(lse_s - LSE) o_s.
+// Merge the per-warp partials of requests split across warps: o = sum_k 2^(lse_k - LSE) o_k.
+// grid (B, Hkv); thread per (query head of the KV head, 4 channels).
 template <int D>
-__global__ void __launch_bounds__(D) draft_combine_kernel(const __grid_constant__ DraftParams p) {
-  const int b = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+__global__ void __launch_bounds__(128) draft_combine_kernel(const __grid_constant__ DraftParams p) {
+  const int b = blockIdx.x, hk = blockIdx.y;
+  pdl_launch_dependents();
+  pdl_wait();
+  int64_t w0, w1;
+  warp_span(p, b, w0, w1);
+  if (w0 == w1) return;
+  const int G = p.G;
   const DraftReqDev& r = p.req[b];
-  if (r.n_splits == 1) return;
-  const size_t base = ((size_t)b * p.Hq + h) * p.S_max;
-  float M = -INFINITY;
-  for (int s = 0; s < r.n_splits; ++s) M = fmaxf(M, p.ws_lse[base + s]);
-  const float Mu = (M == -INFINITY) ? 0.f : M;
-  float acc = 0.f, L = 0.f;
-  for (int s = 0; s < r.n_splits; ++s) {
-    const float w = exp2f(p.ws_lse[base + s] - Mu);
-    L += w;
-    acc += w * p.ws_o[(base + s) * D + c];
+  const size_t base = (size_t)hk * (p.n_vwarps + p.B) + b;
+  for (int item = threadIdx.x; item < G * (D / 4); item += blockDim.x) {
+    const int g = item / (D / 4), c = 4 * (item % (D / 4));
+    float M = -INFINITY;
+    for (int64_t w = w0; w <= w1; ++w) M = fmaxf(M, p.ws_lse[(base + w) * G + g]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int64_t w = w0; w <= w1; ++w) {
+      const float wt = exp2f(p.ws_lse[(base + w) * G + g] - Mu);
+      const float4 v = *reinterpret_cast<const float4*>(p.ws_o + ((base + w) * G + g) * D + c);
+      L += wt;
+      acc.x += wt * v.x;
+      acc.y += wt * v.y;
+      acc.z += wt * v.z;
+      acc.w += wt * v.w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint2 out;
+    out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(r.o + (size_t)(hk * G + g) * D + c) = out;
   }
-  r.o[(size_t)h * D + c] = __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
 }
 
-template <int D, int KIND>
-static cudaError_t launch_draft_t(const DraftParams& p, int total_ctas, cudaStream_t s) {
+template <int D, int KIND, int NHB>
+static cudaError_t launch_draft_t(const DraftParams& p, int ctas_per_head, cudaStream_t s) {
   using C = DraftCfg<D, KIND>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(draft_attn_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(draft_attn_kernel<D, KIND, NHB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  draft_attn_kernel<D, KIND><<<dim3(total_ctas, p.Hkv), 128, C::SMEM, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e =
+      launch_pdl(draft_attn_kernel<D, KIND, NHB>, dim3(ctas_per_head, p.Hkv), dim3(128), C::SMEM, s, p);
   if (e != cudaSuccess) return e;
-  draft_combine_kernel<D><<<dim3(p.B, p.Hq), D, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(draft_combine_kernel<D>, dim3(p.B, p.Hkv), dim3(128), 0, s, p);
 }
 
-cudaError_t launch_draft(const DraftParams& p, int d, int kind, int total_ctas, cudaStream_t s) {
+template <int D, int KIND>
+static cudaError_t launch_draft_g(const DraftParams& p, int ctas_per_head, cudaStream_t s) {
+  return p.G <= 8 ? launch_draft_t<D, KIND, 1>(p, ctas_per_head, s) : launch_draft_t<D, KIND, 2>(p, ctas_per_head, s);
+}
+
+int draft_ctas_per_sm(int kind) { return kind == 0 ? DraftCfg<128, 0>::CTAS_PER_SM : DraftCfg<128, 2>::CTAS_PER_SM; }
+
+cudaError_t launch_draft(const DraftParams& p, int d, int kind, int ctas_per_head, cudaStream_t s) {
   if (d == 128) {
-    if (kind == 0) return launch_draft_t<128, 0>(p, total_ctas, s);
-    if (kind == 2) return launch_draft_t<128, 2>(p, total_ctas, s);
-    if (kind == 4) return launch_draft_t<128, 4>(p, total_ctas, s);
+    if (kind == 0) return launch_draft_g<128, 0>(p, ctas_per_head, s);
+    if (kind == 2) return launch_draft_g<128, 2>(p, ctas_per_head, s);
+    if (kind == 4) return launch_draft_g<128, 4>(p, ctas_per_head, s);
   } else if (d == 64) {
-    if (kind == 0) return launch_draft_t<64, 0>(p, total_ctas, s);
-    if (kind == 2) return launch_draft_t<64, 2>(p, total_ctas, s);
-    if (kind == 4) return launch_draft_t<64, 4>(p, total_ctas, s);
+    if (kind == 0) return launch_draft_g<64, 0>(p, ctas_per_head, s);
+    if (kind == 2) return launch_draft_g<64, 2>(p, ctas_per_head, s);
+    if (kind == 4) return launch_draft_g<64, 4>(p, ctas_per_head, s);
   }
   return cudaErrorInvalidValue;
 }

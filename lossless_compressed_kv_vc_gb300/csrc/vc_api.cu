@@ -36,6 +36,17 @@ static int sm_count() {
   return n;
 }
 
+namespace vc {
+int draft_ctas_per_sm(int kind);
+}
+
+// CTAs per KV head of a draft launch: one wave of the kind's CTAs per SM over all heads
+// (kind 0 = bf16 rows; the workspace bound takes the largest, kind 0).
+static int draft_ctas_per_head_max(int Hkv, int kind = 0) {
+  const int n = vc::draft_ctas_per_sm(kind) * sm_count() / Hkv;
+  return n > 1 ? n : 1;
+}
+
 extern "C" {
 
 int32_t vc_version(void) { return 100; }
@@ -55,8 +66,9 @@ const char* vc_status_string(vc_status s) {
 size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows) {
   if (!shape_ok(shape)) return 0;
   if (call == VC_CALL_DRAFT) {
-    const size_t slots = (size_t)shape->B * shape->Hq * kDraftMaxSplits;
-    return slots * shape->d * sizeof(float) + slots * sizeof(float) + 256;
+    const size_t G = shape->Hq / shape->Hkv;
+    const size_t slots = (size_t)shape->Hkv * (kDraftWarps * draft_ctas_per_head_max(shape->Hkv) + shape->B);
+    return slots * G * (shape->d + 1) * sizeof(float) + 256;
   }
   if (call == VC_CALL_VERIFY) return verify_workspace_size(shape, max_rows);
   return 0;
@@ -186,10 +198,9 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   p.Hkv = Hkv;
   p.G = G;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
-  p.S_max = kDraftMaxSplits;
   p.dev_status = dev_status;
 
-  long long total_rows = 0;
+  int64_t total = 0;
   for (int b = 0; b < B; ++b) {
     const vc_draft_req& q = req[b];
     const vc_kv_comp& c = q.comp;
@@ -210,7 +221,6 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
         return VC_ERR_INVALID;
       n_main = VC_GROUP * c.ng;
     }
-    total_rows += n_main;
     DraftReqDev& r = p.req[b];
     r.q = static_cast<const bf16*>(q.q);
     r.k_new = static_cast<const bf16*>(q.k_new);
@@ -233,38 +243,26 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
     r.v_win = static_cast<bf16*>(c.v_win);
     r.win_cap = c.win_cap;
     r.n_win = c.n_win;
+    r.n_mc = (n_main + chunk - 1) / chunk;
+    r.n_chunks = r.n_mc + (c.n_win + 1 + 15) / 16;
+    r.chunk_begin = (int32_t)total;
+    total += r.n_chunks;
   }
-  // split plan: about `waves` full waves of 2 CTAs per SM over all (request, KV head) pairs
-  const int target = env_int("VC_DRAFT_CTAS", 4 * 2 * sm_count());
-  const long long per_head_target = target / Hkv > 1 ? target / Hkv : 1;
-  long long rps = (total_rows + per_head_target - 1) / per_head_target;
-  if (rps < 64) rps = 64;
-  rps = (rps + chunk - 1) / chunk * chunk;
-  int total = 0, max_splits = 0;
-  for (int b = 0; b < B; ++b) {
-    DraftReqDev& r = p.req[b];
-    long long my = rps;
-    int ns = r.n_main > 0 ? (int)((r.n_main + my - 1) / my) : 1;
-    if (ns > kDraftMaxSplits) {
-      ns = kDraftMaxSplits;
-      my = ((r.n_main + ns - 1) / ns + chunk - 1) / chunk * chunk;
-      ns = (int)((r.n_main + my - 1) / my);
-    }
-    r.main_per_split = (int32_t)my;
-    r.n_splits = ns;
-    r.split_begin = total;
-    total += ns;
-    if (ns > max_splits) max_splits = ns;
-  }
-  if (max_splits > 1) {
-    const size_t need = vc_workspace_size(VC_CALL_DRAFT, shape, 0);
-    if (!ws || ws_bytes < need || !aligned16(ws)) return VC_ERR_WORKSPACE;
-    const size_t slots = (size_t)B * shape->Hq * kDraftMaxSplits;
-    p.ws_o = static_cast<float*>(ws);
-    p.ws_lse = p.ws_o + slots * d;
-  }
+  // one wave of CTAs over the KV heads, but at least ~4 chunks per warp
   const int kind = mode == VC_TOKEN_DROP ? 0 : bits;
-  return launch_draft(p, d, kind, total, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
+  int per_head = draft_ctas_per_head_max(Hkv, kind);
+  const int env = env_int("VC_DRAFT_CTAS", 0);
+  if (env > 0 && env / Hkv < per_head) per_head = env / Hkv > 1 ? env / Hkv : 1;
+  const int64_t by_work = (total + 4 * kDraftWarps - 1) / (4 * kDraftWarps);
+  if (by_work < per_head) per_head = (int)(by_work > 1 ? by_work : 1);
+  p.n_vwarps = (int64_t)per_head * kDraftWarps;
+  p.total_chunks = total;
+  const size_t need = vc_workspace_size(VC_CALL_DRAFT, shape, 0);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return VC_ERR_WORKSPACE;
+  const size_t slots = (size_t)Hkv * (p.n_vwarps + B);
+  p.ws_o = static_cast<float*>(ws);
+  p.ws_lse = p.ws_o + slots * G * d;
+  return launch_draft(p, d, kind, per_head, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/vc.h"
 
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
@@ -78,6 +80,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only); src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src_gmem, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // ---- warp-level tensor-core helpers (mma.sync m16n8k16) -----------------------------------------
 __device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -102,6 +114,29 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---- programmatic dependent launch ----------------------------------------------------------------
+// Every kernel of the round is launched with programmatic stream serialisation: it lets the next
+// kernel in the stream start launching once all of its CTAs are running, and waits for the
+// previous kernel's results (grid completion and memory flush) before touching any global data.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---- per-request kernel descriptors (travel by value in kernel params) -------------------------
@@ -129,26 +164,27 @@ struct DraftReqDev {
   bf16* v_win;
   int64_t win_cap;
   int32_t n_win;
-  // split plan
-  int32_t split_begin;
-  int32_t n_splits;
-  int32_t main_per_split;  // main rows per split (multiple of the chunk)
+  // chunk plan: n_mc chunks of KV_comp rows, then ceil((n_win + 1) / 16) window chunks
+  int32_t chunk_begin;  // first chunk of this request in the per-head concatenation
+  int32_t n_mc;
+  int32_t n_chunks;
 };
 
 struct DraftParams {
   DraftReqDev req[VC_MAX_BATCH];
   int32_t B, Hq, Hkv, G;
-  float scale_log2;     // log2(e) / sqrt(d)
-  float* ws_o;          // [B][Hq][S_max][d]
-  float* ws_lse;        // [B][Hq][S_max]  (log2 domain)
-  int32_t S_max;
+  float scale_log2;      // log2(e) / sqrt(d)
+  float* ws_o;           // [Hkv][n_vwarps + B][G][d] per-warp partials (slot = warp + request)
+  float* ws_lse;         // [Hkv][n_vwarps + B][G]  (log2 domain)
+  int64_t n_vwarps;      // warps per KV head (grid.x * 4)
+  int64_t total_chunks;  // chunks per KV head over all requests
   int32_t* dev_status;
 };
 
-constexpr int kDraftMaxSplits = 64;
+constexpr int kDraftWarps = 4;
 
 // launchers (return cudaError_t of the launch)
-cudaError_t launch_draft(const DraftParams& p, int d, int mode_kind, int total_ctas, cudaStream_t s);
+cudaError_t launch_draft(const DraftParams& p, int d, int mode_kind, int ctas_per_head, cudaStream_t s);
 
 struct AcceptArgs {
   const float* logits;

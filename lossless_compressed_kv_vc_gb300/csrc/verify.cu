@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5;
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte aligned tiles
+    pdl_launch_dependents();
+    pdl_wait();
     if (tid == 0) set_status(p.dev_status, VC_DEV_INTERNAL);
     return;
   }
@@ -107,6 +109,8 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
   tc05::fence_before();
   __syncthreads();
   tc05::fence_after();
+  pdl_launch_dependents();
+  pdl_wait();
   const uint32_t tmem = *tslot;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
   const uint32_t t_s = tmem + lane_off;
@@ -366,6 +370,8 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
 template <int D>
 __global__ void __launch_bounds__(128) verify_combine_kernel(const __grid_constant__ VerifyParams p) {
   const int u = blockIdx.x, r = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   int b = 0;
 #pragma unroll 1
   for (int i = 1; i < p.B; ++i)
@@ -472,11 +478,9 @@ static cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  verify_attn_kernel<D><<<p.n_cta, 128, C::SMEM, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(verify_attn_kernel<D>, dim3(p.n_cta), dim3(128), C::SMEM, s, p);
   if (e != cudaSuccess) return e;
-  verify_combine_kernel<D><<<p.n_units, 128, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(verify_combine_kernel<D>, dim3(p.n_units), dim3(128), 0, s, p);
 }
 
 static bool a16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
