@@ -4,8 +4,8 @@
 //
 // Token drop: one CTA per request selects the keep-set with a 4-pass MSB radix select over the
 // order-preserving uint32 image of the fp32 importance (-0 folded onto +0), then writes the kept
-// indices in ascending order with block-wide ballot scans (ties at the threshold go to the lower
-// indices), then appends the recent window. An optional second launch gathers the kept rows.
+// indices in ascending order from per-thread contiguous segments and two block scans (ties at the
+// threshold go to the lower indices), then appends the recent window. An optional second launch gathers the kept rows.
 // Quantisation: key groups (32 tokens of one channel) one thread per channel; value groups
 // (32 channels of one token) one lane per 4 channels with shuffle min/max; every float decision
 // uses IEEE round-to-nearest (division, rint half-to-even, fp32->fp16), as the format defines.
@@ -22,107 +22,129 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 constexpr int kKeepThreads = 1024;
+constexpr int kKeepCacheKeys = 48 * 1024;  // candidates whose keys fit in shared memory (192 KB)
 
-// Exclusive block scan of one flag per thread; returns the prefix, writes the block total.
-__device__ __forceinline__ int block_scan_flag(bool f, int* warp_tot, int& total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const unsigned ball = __ballot_sync(0xffffffffu, f);
-  const int in_warp = __popc(ball & ((1u << lane) - 1u));
-  if (lane == 0) warp_tot[w] = __popc(ball);
-  __syncthreads();
-  if (w == 0) {
-    int v = warp_tot[lane];
-    int incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    warp_tot[32 + lane] = incl - v;
-    if (lane == 31) warp_tot[64] = incl;
-  }
-  __syncthreads();
-  const int r = warp_tot[32 + w] + in_warp;
-  total = warp_tot[64];
-  __syncthreads();
-  return r;
-}
-
-__global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_constant__ KeepParams p) {
+__global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_constant__ KeepParams p, int cache_keys) {
   pdl_launch_dependents();
   pdl_wait();
   const KeepReq& r = p.req[blockIdx.x];
   const int n = r.ctx, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   if (r.keep >= n) {
     for (int j = tid; j < n; j += kKeepThreads) r.idx[j] = j;
     return;
   }
   const int n_cand = n - r.recent;
   const int need = r.keep - r.recent;
+  extern __shared__ uint32_t kcache[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_prefix, s_mask, s_rem;
-  __shared__ int scan_buf[65];
+  __shared__ int s_cnt[2][32];
+  const bool cached = n_cand <= cache_keys;
+  if (cached) {
+#pragma unroll 4
+    for (int i = tid; i < n_cand; i += kKeepThreads) kcache[i] = order_key(__ldg(r.imp + i));
+  }
   if (tid == 0) {
     s_prefix = 0;
     s_mask = 0;
     s_rem = (uint32_t)need;
   }
   __syncthreads();
+  auto key = [&](int i) -> uint32_t { return cached ? kcache[i] : order_key(__ldg(r.imp + i)); };
+  // 1. radix select, most significant byte first: find the key T of the need-th largest
+  //    candidate and how many candidates equal to T must be kept (s_rem after the passes)
   if (need > 0) {
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int i = tid; i < 256; i += kKeepThreads) hist[i] = 0;
+      if (tid < 256) hist[tid] = 0;
       __syncthreads();
       const uint32_t prefix = s_prefix, mask = s_mask;
-#pragma unroll 1
+#pragma unroll 4
       for (int base = 0; base < n_cand; base += kKeepThreads) {  // whole warps iterate together
         const int i = base + tid;
-        const uint32_t u = i < n_cand ? order_key(__ldg(r.imp + i)) : 0u;
+        const uint32_t u = i < n_cand ? key(i) : 0u;
         const bool in = i < n_cand && (u & mask) == prefix;
         const uint32_t dg = (u >> shift) & 255u;
         // aggregate equal digits of a warp into one shared atomic
         const unsigned act = __ballot_sync(0xffffffffu, in);
         if (in) {
           const unsigned peers = __match_any_sync(act, dg);
-          if ((threadIdx.x & 31) == (__ffs(peers) - 1)) atomicAdd(&hist[dg], (uint32_t)__popc(peers));
+          if (lane == (__ffs(peers) - 1)) atomicAdd(&hist[dg], (uint32_t)__popc(peers));
         }
       }
       __syncthreads();
-      if (tid == 0) {
-        uint32_t rem = s_rem, cum = 0;
-        int sel = 0;
-        for (int dg = 255; dg >= 0; --dg) {
-          if (cum + hist[dg] >= rem) {
-            sel = dg;
-            break;
-          }
-          cum += hist[dg];
+      if (warp == 0) {
+        // lane l owns digits 8l..8l+7; counts of larger digits come from the lanes above
+        uint32_t c[8], own = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          c[k] = hist[8 * lane + k];
+          own += c[k];
         }
-        s_rem = rem - cum;
-        s_prefix = prefix | ((uint32_t)sel << shift);
-        s_mask = mask | (255u << shift);
+        uint32_t above = own;  // inclusive suffix sum over lanes >= l
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t o = __shfl_down_sync(0xffffffffu, above, off);
+          if (lane + off < 32) above += o;
+        }
+        uint32_t cum = above - own;  // candidates with a larger digit than this lane's range
+        const uint32_t rem = s_rem;
+        __syncwarp();  // every lane has read s_rem before the selected lane overwrites it
+#pragma unroll
+        for (int k = 7; k >= 0; --k) {
+          if (cum < rem && cum + c[k] >= rem) {  // exactly one (lane, k) satisfies this
+            s_rem = rem - cum;
+            s_prefix = prefix | ((uint32_t)(8 * lane + k) << shift);
+            s_mask = mask | (255u << shift);
+          }
+          cum += c[k];
+        }
       }
       __syncthreads();
     }
   }
-  const uint32_t T = s_prefix;
-  const int need_eq = need > 0 ? (int)s_rem : 0;
-  int running = 0, eq_seen = 0;
-#pragma unroll 1
-  for (int base = 0; base < n_cand && running < need; base += kKeepThreads) {
-    const int i = base + tid;
-    const uint32_t u = i < n_cand ? order_key(__ldg(r.imp + i)) : 0u;
-    const bool gt = i < n_cand && need > 0 && u > T;
-    const bool eq = i < n_cand && need > 0 && u == T;
-    int tot_eq;
-    const int eq_rank = block_scan_flag(eq, scan_buf, tot_eq);
-    const bool sel = gt || (eq && eq_seen + eq_rank < need_eq);
-    int tot_sel;
-    const int pos = block_scan_flag(sel, scan_buf, tot_sel);
-    if (sel) r.idx[running + pos] = i;
-    running += tot_sel;
-    eq_seen += tot_eq;
+  // 2. ascending compaction over contiguous per-warp segments, 32 elements per ballot: an element's
+  //    slot is the number of larger keys before it plus min(equal keys before it, need_eq)
+  if (need > 0) {
+    const uint32_t T = s_prefix;
+    const int need_eq = (int)s_rem;
+    const int segw = ((n_cand + 31) / 32 + 31) / 32 * 32;
+    const int w0 = min(n_cand, warp * segw), w1 = min(n_cand, w0 + segw);
+    const unsigned lt = (1u << lane) - 1u;
+    int gt = 0, eq = 0;
+#pragma unroll 4
+    for (int base = w0; base < w1; base += 32) {
+      const int i = base + lane;
+      const uint32_t u = i < w1 ? key(i) : 0u;
+      gt += __popc(__ballot_sync(0xffffffffu, i < w1 && u > T));
+      eq += __popc(__ballot_sync(0xffffffffu, i < w1 && u == T));
+    }
+    if (lane == 0) {
+      s_cnt[0][warp] = gt;
+      s_cnt[1][warp] = eq;
+    }
+    __syncthreads();
+    int gt_before = 0, eq_before = 0;
+    for (int w = 0; w < warp; ++w) {
+      gt_before += s_cnt[0][w];
+      eq_before += s_cnt[1][w];
+    }
+    int out = gt_before + min(eq_before, need_eq), eq_run = eq_before;
+#pragma unroll 2
+    for (int base = w0; base < w1; base += 32) {
+      const int i = base + lane;
+      const bool valid = i < w1;
+      const uint32_t u = valid ? key(i) : 0u;
+      const unsigned bgt = __ballot_sync(0xffffffffu, valid && u > T);
+      const unsigned beq = __ballot_sync(0xffffffffu, valid && u == T);
+      const bool take_eq = valid && u == T && eq_run + __popc(beq & lt) < need_eq;
+      const unsigned bsel = bgt | __ballot_sync(0xffffffffu, take_eq);
+      if ((bsel >> lane) & 1u) r.idx[out + __popc(bsel & lt)] = i;
+      out += __popc(bsel);
+      eq_run += __popc(beq);
+    }
   }
   for (int j = tid; j < r.recent; j += kKeepThreads) r.idx[need + j] = n_cand + j;
 }
@@ -156,7 +178,21 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant_
 }
 
 cudaError_t launch_keepset(const KeepParams& p, int max_keep, cudaStream_t s) {
-  cudaError_t e = launch_pdl(keepset_kernel, dim3(p.B), dim3(kKeepThreads), 0, s, p);
+  int max_cand = 0;
+  for (int b = 0; b < p.B; ++b) {
+    const int nc = p.req[b].ctx - p.req[b].recent;
+    if (nc > max_cand) max_cand = nc;
+  }
+  const int cache_keys = max_cand < kKeepCacheKeys ? max_cand : kKeepCacheKeys;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(keepset_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kKeepCacheKeys * (int)sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaError_t e = launch_pdl(keepset_kernel, dim3(p.B), dim3(kKeepThreads), (size_t)cache_keys * sizeof(uint32_t), s,
+                             p, cache_keys);
   if (e != cudaSuccess) return e;
   bool any = false;
   for (int b = 0; b < p.B; ++b) any |= p.req[b].compact != 0;

@@ -31,7 +31,10 @@
 
 namespace vc {
 
-template <int D, int KIND>  // KIND 0: bf16 rows (token drop); 2 or 4: quantised, bits
+// KIND 0: bf16 rows (token drop); 2 or 4: quantised, bits. Bf16-row kernels run three 4-warp CTAs
+// per SM with a 2-stage ring per warp (measured better than 2 CTAs x 3 stages or 1 CTA x 6 stages:
+// more warps in flight beat deeper rings); quantised kernels run two CTAs with a dequant tile.
+template <int D, int KIND>
 struct DraftCfg {
   static constexpr int NW = 4;
   static constexpr int ROWB = D * 2;                     // bytes of one bf16 row
@@ -461,41 +464,65 @@ __global__ void __launch_bounds__(128, DraftCfg<D, KIND>::CTAS_PER_SM)
   finish(cur_b);
 }
 
-// Merge the per-warp partials of requests split across warps: o = sum_k 2^(lse_k - LSE) o_k.
-// grid (B, Hkv); thread per (query head of the KV head, 4 channels).
+// Merge the per-warp partials of requests split across warps: o = sum_k 2^(lse_k - LSE) o_k / L.
+// grid (B, Hkv, G): one CTA per query head; thread = (channel quad, partial group), so the
+// partials are read in parallel, then summed across groups in shared memory.
 template <int D>
 __global__ void __launch_bounds__(128) draft_combine_kernel(const __grid_constant__ DraftParams p) {
-  const int b = blockIdx.x, hk = blockIdx.y;
+  constexpr int QPB = D / 4;          // channel quads per head
+  constexpr int PG = 128 / QPB;       // partial groups
+  const int b = blockIdx.x, hk = blockIdx.y, g = blockIdx.z;
   pdl_launch_dependents();
   pdl_wait();
   int64_t w0, w1;
   warp_span(p, b, w0, w1);
   if (w0 == w1) return;
   const int G = p.G;
-  const DraftReqDev& r = p.req[b];
-  const size_t base = (size_t)hk * (p.n_vwarps + p.B) + b;
-  for (int item = threadIdx.x; item < G * (D / 4); item += blockDim.x) {
-    const int g = item / (D / 4), c = 4 * (item % (D / 4));
-    float M = -INFINITY;
-    for (int64_t w = w0; w <= w1; ++w) M = fmaxf(M, p.ws_lse[(base + w) * G + g]);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int tid = threadIdx.x, cq = tid % QPB, pg = tid / QPB;
+  const int np = (int)(w1 - w0 + 1);
+  const size_t base = (size_t)hk * (p.n_vwarps + p.B) + b + w0;  // slot of partial k: base + k
+  __shared__ float s_max[PG];
+  __shared__ float s_l[PG];
+  __shared__ float4 s_acc[PG][QPB];
+  float mx = -INFINITY;
+  for (int k = pg; k < np; k += PG) mx = fmaxf(mx, p.ws_lse[(base + k) * G + g]);
+  if (cq == 0) s_max[pg] = mx;
+  __syncthreads();
+  float M = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < PG; ++i) M = fmaxf(M, s_max[i]);
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-    for (int64_t w = w0; w <= w1; ++w) {
-      const float wt = exp2f(p.ws_lse[(base + w) * G + g] - Mu);
-      const float4 v = *reinterpret_cast<const float4*>(p.ws_o + ((base + w) * G + g) * D + c);
-      L += wt;
-      acc.x += wt * v.x;
-      acc.y += wt * v.y;
-      acc.z += wt * v.z;
-      acc.w += wt * v.w;
+  for (int k = pg; k < np; k += PG) {
+    const float wt = exp2f(p.ws_lse[(base + k) * G + g] - Mu);
+    const float4 v = *reinterpret_cast<const float4*>(p.ws_o + ((base + k) * G + g) * D + 4 * cq);
+    L += wt;
+    acc.x += wt * v.x;
+    acc.y += wt * v.y;
+    acc.z += wt * v.z;
+    acc.w += wt * v.w;
+  }
+  s_acc[pg][cq] = acc;
+  if (cq == 0) s_l[pg] = L;
+  __syncthreads();
+  if (pg == 0) {
+    float Lt = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < PG; ++i) {
+      Lt += s_l[i];
+      a.x += s_acc[i][cq].x;
+      a.y += s_acc[i][cq].y;
+      a.z += s_acc[i][cq].z;
+      a.w += s_acc[i][cq].w;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
     uint2 out;
-    out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(r.o + (size_t)(hk * G + g) * D + c) = out;
+    out.x = pack_bf16x2(a.x * inv, a.y * inv);
+    out.y = pack_bf16x2(a.z * inv, a.w * inv);
+    *reinterpret_cast<uint2*>(p.req[b].o + (size_t)(hk * G + g) * D + 4 * cq) = out;
   }
 }
 
@@ -512,7 +539,7 @@ static cudaError_t launch_draft_t(const DraftParams& p, int ctas_per_head, cudaS
   cudaError_t e =
       launch_pdl(draft_attn_kernel<D, KIND, NHB>, dim3(ctas_per_head, p.Hkv), dim3(128), C::SMEM, s, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(draft_combine_kernel<D>, dim3(p.B, p.Hkv), dim3(128), 0, s, p);
+  return launch_pdl(draft_combine_kernel<D>, dim3(p.B, p.Hkv, p.G), dim3(128), 0, s, p);
 }
 
 template <int D, int KIND>

@@ -366,10 +366,14 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
   if (warp == 0) tc05::dealloc(tmem, C::TCOLS);
 }
 
-// Merge the partials of units split across CTAs: o = sum_k 2^(lse_k - LSE) o_k (thread per row).
+// Merge the partials of units split across CTAs: o = sum_k 2^(lse_k - LSE) o_k / L.
+// grid (units, 128 / 8): a CTA takes 8 query rows of a unit, a thread one row's 4 channels (d=128) or
+// 2 channels (d=64), so partial reads are spread across threads.
 template <int D>
-__global__ void __launch_bounds__(128) verify_combine_kernel(const __grid_constant__ VerifyParams p) {
-  const int u = blockIdx.x, r = threadIdx.x;
+__global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_constant__ VerifyParams p) {
+  constexpr int TPR = 32;          // threads per row
+  constexpr int CPT = D / TPR;     // channels per thread (4 or 2)
+  const int u = blockIdx.x;
   pdl_launch_dependents();
   pdl_wait();
   int b = 0;
@@ -382,38 +386,42 @@ __global__ void __launch_bounds__(128) verify_combine_kernel(const __grid_consta
   const int64_t T = p.total_tiles, N = p.n_cta;
   const int64_t c0 = ((U0 + 1) * N - 1) / T, c1 = (U1 * N - 1) / T;
   if (c0 == c1) return;
+  const int r = blockIdx.y * 8 + (threadIdx.x / TPR), cc = (threadIdx.x % TPR) * CPT;
   const int hk = ul / R.mtiles, mt = ul % R.mtiles;
   const int Rw = mt * VM + r, qi = Rw / p.G, qg = Rw % p.G;
   if (qi >= R.n_rows) return;
   float M = -INFINITY;
   for (int64_t c = c0; c <= c1; ++c) M = fmaxf(M, p.ws_lse[(c + u) * VM + r]);
   const float Mu = M == -INFINITY ? 0.f : M;
-  float wsum = 0.f;
-  for (int64_t c = c0; c <= c1; ++c) wsum += exp2f(p.ws_lse[(c + u) * VM + r] - Mu);
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  bf16* dst = R.o + ((size_t)qi * p.Hq + hk * p.G + qg) * D;
-#pragma unroll 1
-  for (int cb = 0; cb < D; cb += 8) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int64_t c = c0; c <= c1; ++c) {
-      const float w = exp2f(p.ws_lse[(c + u) * VM + r] - Mu);
-      const float4* src = reinterpret_cast<const float4*>(p.ws_o + ((c + u) * VM + r) * D + cb);
-      const float4 a = src[0], b2 = src[1];
-      acc[0] += w * a.x;
-      acc[1] += w * a.y;
-      acc[2] += w * a.z;
-      acc[3] += w * a.w;
-      acc[4] += w * b2.x;
-      acc[5] += w * b2.y;
-      acc[6] += w * b2.z;
-      acc[7] += w * b2.w;
+  float L = 0.f, acc[CPT];
+#pragma unroll
+  for (int e = 0; e < CPT; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int64_t c = c0; c <= c1; ++c) {
+    const float w = exp2f(p.ws_lse[(c + u) * VM + r] - Mu);
+    const float* src = p.ws_o + ((c + u) * VM + r) * D + cc;
+    L += w;
+    if (CPT == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += w * v.x;
+      acc[1 % CPT] += w * v.y;
+      acc[2 % CPT] += w * v.z;
+      acc[3 % CPT] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += w * v.x;
+      acc[1 % CPT] += w * v.y;
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(dst + cb) = o;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  bf16* dst = R.o + ((size_t)qi * p.Hq + hk * p.G + qg) * D + cc;
+  if (CPT == 4) {
+    uint2 o;
+    o.x = pack_bf16x2(acc[0] * inv, acc[1 % CPT] * inv);
+    o.y = pack_bf16x2(acc[2 % CPT] * inv, acc[3 % CPT] * inv);
+    *reinterpret_cast<uint2*>(dst) = o;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1 % CPT] * inv);
   }
 }
 
@@ -480,7 +488,7 @@ static cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
   }
   cudaError_t e = launch_pdl(verify_attn_kernel<D>, dim3(p.n_cta), dim3(128), C::SMEM, s, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(verify_combine_kernel<D>, dim3(p.n_units), dim3(128), 0, s, p);
+  return launch_pdl(verify_combine_kernel<D>, dim3(p.n_units, VM / 8), dim3(256), 0, s, p);
 }
 
 static bool a16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
