@@ -215,3 +215,86 @@ def accept(logits: torch.Tensor, draft: torch.Tensor, L: torch.Tensor, out_token
         n_acc = torch.empty((B,), dtype=torch.int32, device=logits.device)
     vc_accept(B, Lp1 - 1, V, logits, draft, L, out_tokens, n_acc, stream)
     return out_tokens, n_acc
+
+
+class StaggeredOffload:
+    """Cross-resource staggering for requests whose KV_full lives in pinned host memory
+    ("VeriCache: Turning Lossy KV Cache into Lossless LLM Inference", "Cross-resource staggering
+    (P1)" and "Architecture support", long-context decoding).
+
+    Two groups of requests alternate roles. In each phase one group drafts its L steps on the
+    compute stream (HBM-bound) while the other group's KV_full is copied host-to-device on the copy
+    stream (host-link-bound); the compute stream then waits for that copy and verifies and accepts
+    the staged group. Each group keeps its own device staging slot, so a copy never waits for the
+    other group's verification.
+    """
+
+    def __init__(self, groups: List[Batch], host_kv: List[List[torch.Tensor]], slots: List[List[torch.Tensor]],
+                 copy_stream, compute_stream, chunk_bytes: int = 64 << 20):
+        assert len(groups) == 2
+        self.groups, self.host_kv, self.slots = groups, host_kv, slots
+        self.copy_stream, self.compute_stream = copy_stream, compute_stream
+        self.chunk_bytes = chunk_bytes
+        self.staged = [torch.cuda.Event(), torch.cuda.Event()]
+        self.verified = [torch.cuda.Event(), torch.cuda.Event()]
+        for g in range(2):  # a slot is free before its first copy
+            self.verified[g].record(compute_stream)
+
+    def stage(self, g: int, events=None):
+        """Issue the host-to-device copies of group g's KV_full on the copy stream."""
+        from . import vc_stage_full_kv
+        self.copy_stream.wait_event(self.verified[g])  # its previous verification has read the slot
+        if events is not None:
+            events[0].record(self.copy_stream)
+        for h, d in zip(self.host_kv[g], self.slots[g]):
+            vc_stage_full_kv(h, d, h.numel() * h.element_size(), self.chunk_bytes, self.copy_stream, None)
+        self.staged[g].record(self.copy_stream)
+        if events is not None:
+            events[1].record(self.copy_stream)
+
+    def phase(self, draft_g: int, io, draft_events=None, stage_events=None):
+        """Group draft_g drafts while the other group stages, then the other group verifies and accepts.
+        io[g] = (logits, draft, L, out_tokens, n_acc) of group g."""
+        other = 1 - draft_g
+        self.stage(other, stage_events)
+        bt = self.groups[draft_g]
+        if draft_events is not None:
+            draft_events[0].record(self.compute_stream)
+        for shape, arr, act in bt._steps:
+            vc_draft_attn(shape, arr, bt.ws_draft, bt.dev_status, self.compute_stream)
+        if draft_events is not None:
+            draft_events[1].record(self.compute_stream)
+        self.compute_stream.wait_event(self.staged[other])
+        ob = self.groups[other]
+        vc_verify_attn(ob.shape, ob._verify_arr, ob.ws_verify, ob.dev_status, self.compute_stream)
+        self.verified[other].record(self.compute_stream)
+        lg, dr, L, tok, nacc = io[other]
+        accept(lg, dr, L, tok, nacc, self.compute_stream)
+
+    def period(self, io, events=None):
+        """Both phases: every request drafts once and is verified once."""
+        ev = events or {}
+        self.phase(0, io, ev.get("draft0"), ev.get("stage1"))
+        self.phase(1, io, ev.get("draft1"), ev.get("stage0"))
+
+
+def move_full_kv_to_host(groups: List[Batch]):
+    """After compression, move every request's KV_full to pinned host memory ([K; V] in one buffer
+    per request) and give it a device staging slot of the same layout; the request's KV_full
+    descriptor then points at the slot. Returns (host buffers, slots), per group and request."""
+    host_kv, slots = [], []
+    for bt in groups:
+        hs, ss = [], []
+        for b, r in enumerate(bt.reqs):
+            kv = torch.stack([r.k_full, r.v_full])
+            h = torch.empty(kv.shape, dtype=kv.dtype, pin_memory=True)
+            h.copy_(kv)
+            slot = torch.empty_like(kv)
+            bt.set_full(b, slot[0], slot[1])
+            hs.append(h)
+            ss.append(slot)
+            del kv
+        host_kv.append(hs)
+        slots.append(ss)
+    torch.cuda.synchronize()
+    return host_kv, slots

@@ -1,0 +1,96 @@
+"""Staging KV_full from pinned host memory (vc_stage_full_kv) and the staggered offload round:
+one group drafts while the other group's KV_full crosses the host link, then is verified
+("VeriCache: Turning Lossy KV Cache into Lossless LLM Inference", "Cross-resource staggering (P1)",
+"Architecture support": long-context decoding with KV_full in CPU memory)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from workloads import configs, gen
+from tests.util import make_batch, f32, assert_attn_close, oracle_main
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vc():
+    import __graft_entry__ as g
+    g.build()
+    import lossless_compressed_kv_vc_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("nbytes,chunk", [(37 * (1 << 20) + 48, 1 << 20), (4096, 0), (3 << 20, 5 << 20)])
+def test_stage_copies_every_byte(vc, nbytes, chunk):
+    host = torch.randint(0, 256, (nbytes,), dtype=torch.uint8).pin_memory()
+    dev = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    cs = torch.cuda.Stream()
+    done = torch.cuda.Event()
+    vc.vc_stage_full_kv(host, dev, nbytes, chunk, cs, done)
+    torch.cuda.current_stream().wait_event(done)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), host)
+
+
+def test_stage_refuses_pageable_source(vc):
+    """A host buffer that is not page-locked is refused before any copy is issued."""
+    host = torch.ones(1 << 16, dtype=torch.uint8)  # pageable
+    dev = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    st = vc.vc_stage_full_kv(host, dev, host.numel(), 0, torch.cuda.current_stream(), None, raise_on_error=False)
+    assert st == vc.VC_ERR_NOT_PINNED
+    torch.cuda.synchronize()
+    assert int(dev.sum()) == 0
+
+
+def test_stage_refuses_device_source(vc):
+    a = torch.ones(4096, dtype=torch.uint8, device="cuda")
+    b = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    assert vc.vc_stage_full_kv(a, b, 4096, 0, None, None, raise_on_error=False) == vc.VC_ERR_NOT_PINNED
+
+
+def test_staggered_offload_period_matches_oracle(vc):
+    """Scaled Llama-70B-shape offload workload (4 requests, 64/8 heads, 4-bit): a full period of the
+    two-group stagger gives the oracle's draft outputs, verify outputs and accepted tokens."""
+    from lossless_compressed_kv_vc_gb300 import engine
+    w = configs.scaled(configs.llama70b_offload4(), ctx_div=64, batch=4, L=6)
+    w.V = 5000
+    groups = [make_batch(w, [0, 1]), make_batch(w, [2, 3])]
+    full_ref = {}
+    for gi, bt in enumerate(groups):
+        for i, r in enumerate(bt.reqs):
+            full_ref[2 * gi + i] = (f32(r.k_full), f32(r.v_full))
+        bt.compress()
+    host_kv, slots = engine.move_full_kv_to_host(groups)
+    for bt in groups:
+        bt.prepare_steps()
+    draft, logits, L = gen.drafts_and_logits(w, 0, "cuda")
+    io = []
+    for gi in range(2):
+        sl = slice(2 * gi, 2 * gi + 2)
+        io.append((logits[sl].contiguous(), draft[sl].contiguous(), L[sl].contiguous(),
+                   torch.empty((2, w.L_max + 1), dtype=torch.int32, device="cuda"),
+                   torch.empty((2,), dtype=torch.int32, device="cuda")))
+    cs, ks = torch.cuda.Stream(), torch.cuda.Stream()
+    # the period verifies what each group drafted in the previous phase: draft group 1 first
+    for shape, arr, act in groups[1]._steps:
+        vc.vc_draft_attn(shape, arr, groups[1].ws_draft, groups[1].dev_status, ks)
+    ks.synchronize()
+    sg = engine.StaggeredOffload(groups, host_kv, slots, cs, ks, chunk_bytes=1 << 20)
+    sg.period(io)
+    torch.cuda.synchronize()
+    for gi, bt in enumerate(groups):
+        assert int(bt.dev_status.item()) == 0
+        for i, r in enumerate(bt.reqs):
+            b = 2 * gi + i
+            kf, vf = full_ref[b]
+            assert torch.equal(slots[gi][i].cpu(), host_kv[gi][i])  # staged bytes
+            km, vm, kw0, vw0 = oracle_main(w, b, kf, vf)
+            ref_d = O.draft_round(f32(r.q), km, vm, kw0, vw0, f32(r.k_new), f32(r.v_new))
+            assert_attn_close(r.o_draft, ref_d, f"draft b{b}")
+            ref_v = O.verify_attn(f32(r.q), kf, vf, f32(r.k_new).transpose(1, 0, 2), f32(r.v_new).transpose(1, 0, 2))
+            assert_attn_close(r.o_verify, ref_v, f"verify b{b}")
+        lg, dr, Lg, tok, nacc = io[gi]
+        for i in range(2):
+            rt, rn = O.accept(lg[i].cpu().numpy(), dr[i].cpu().numpy(), int(Lg[i]))
+            assert int(nacc[i]) == rn and tok[i, :rn].cpu().tolist() == rt

@@ -44,3 +44,16 @@ def make_batch(w, reqs, rnd=0, device="cuda", compact=False):
 
 def f32(t):
     return t.detach().to("cpu").to(torch.float32).numpy()
+
+
+def oracle_main(w, b, k_full_f32, v_full_f32, importance=None):
+    """The oracle's KV_comp main rows and initial window for request b of workload w."""
+    import oracle as O
+    if w.mode[b] == DROP:
+        idx = O.keep_set(importance, w.keep[b], w.recent[b])
+        km, vm = O.comp_main_rows("drop", k_full_f32, v_full_f32, idx=idx)
+        z = np.zeros((w.Hkv, 0, w.d), np.float32)
+        return km, vm, z, z
+    qkv = O.quantize_kv(k_full_f32, v_full_f32, w.bits, w.residual_min)
+    km, vm = O.comp_main_rows("quant", k_full_f32, v_full_f32, qkv=qkv)
+    return km, vm, qkv["k_res"], qkv["v_res"]
