@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--workload", default="llama8b_drop", choices=["llama8b_drop", "offload"],
                     help="llama8b_drop: the headline round; offload: Llama-70B-shape 4-bit requests with KV_full "
                          "in pinned host memory, two drafting while two stage and verify")
+    ap.add_argument("--ctx-div", type=int, default=1,
+                    help="offload workload: divide the context (a smaller case for profiler captures)")
     ap.add_argument("--compact", action="store_true",
                     help="gather the kept rows into a contiguous copy at compress time (inside the timed round)")
     ap.add_argument("--batch", type=int, default=None,
@@ -407,6 +409,8 @@ def run_offload(args):
     from lossless_compressed_kv_vc_gb300 import engine, VC_QUANT, vc_stage_full_kv
     from workloads import configs, gen
     w = configs.llama70b_offload4()
+    if args.ctx_div > 1:
+        w = configs.scaled(w, ctx_div=args.ctx_div)
     device = "cuda"
     groups = []
     for grp in ([0, 1], [2, 3]):

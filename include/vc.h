@@ -83,13 +83,22 @@ typedef struct vc_kv_full {
  *   kept rows are read in place at k_rows[h][idx[j]] (k_rows is normally the full cache); with
  *   compact == 1 vc_compress_kv gathers them into k_rows[h][j], j < keep, and the draft reads them
  *   contiguously (needed when KV_full leaves HBM).
- * VC_QUANT: groupwise asymmetric `bits`-bit codes for the first Tq = 32*ng tokens:
- *   kc  uint8 [Hkv][ng][d][32*bits/8]  key codes, per (group, channel) the 32 tokens packed
- *   ks,kz fp16 [Hkv][ng][d]            key scale and zero per (group, channel)
- *   vc  uint8 [Hkv][Tq][d*bits/8]      value codes, per token the d channels packed
+ * VC_QUANT: groupwise asymmetric `bits`-bit codes for the first Tq = 32*ng tokens, in blocks of 32
+ *   tokens (keys: one scale/zero per (block, channel); values: per (token, 32-channel group)):
+ *   kc  uint8 [Hkv][ng][32*d*bits/8]   key codes of each block, in block word order (below)
+ *   ks,kz fp16 [Hkv][ng][d]            key scale and zero per (block, channel)
+ *   vc  uint8 [Hkv][ng][32*d*bits/8]   value codes of each block, in block word order
  *   vs,vz fp16 [Hkv][Tq][d/32]         value scale and zero per (token, 32-channel group)
- *   packing: code e of a run at byte e/(8/bits), bit offset bits*(e mod 8/bits).
  *   Dequantised value: code * scale + zero.
+ *   Block word order: little-endian 32-bit words w[half][j][lane] (4-bit; half = 16-token half,
+ *   j = 16-channel step, lane = 0..31) or w[half][p][lane] (2-bit, p covers j = 2p, 2p+1). With
+ *   a = lane/4, b = lane%4, word (half, j, lane) holds pairs i = 0..3 of (token, channel):
+ *     keys   (t0 = 16 half + a, c0 = 16 j + 2b): (t0, c0|c0+1), (t0+8, c0|c0+1),
+ *                                              (t0, c0+8|c0+9), (t0+8, c0+8|c0+9)
+ *     values (r0 = 16 j + a, k0 = 16 half + 2b): (k0|k0+1, r0), (k0|k0+1, r0+8),
+ *                                              (k0+8|k0+9, r0), (k0+8|k0+9, r0+8)
+ *   pair i' (i' = i, or i + 4(j - 2p) at 2-bit) has its first code at bit bits*i' and its second
+ *   at bit 16 + bits*i': each lane's word is its tensor-core operand fragment for that tile.
  *
  * Both families end with a bf16 window k_win/v_win [Hkv][win_cap][d]: for VC_QUANT it starts
  * with the n_res trailing tokens kept in bf16 (the residual), then — for both — the drafted

@@ -221,12 +221,53 @@ __device__ __forceinline__ uint32_t quant_code(float x, float sf, float zf) {
   return (uint32_t)t;
 }
 
-// keys: grid (ng_max, Hkv, B), block D: thread c quantises channel c over the group's 32 tokens.
+// Storage of one 32-token block's codes: 32-bit words w[half][j][lane] (4-bit) or w[half][p][lane]
+// (2-bit, p covers steps j = 2p and 2p + 1). Word (half, j, lane), a = lane / 4, b = lane % 4, holds
+// four (low, high) code pairs i = 0..3; pair i puts its low code at bit BITS*i' and its high code at
+// bit 16 + BITS*i', with i' = i (4-bit) or i + 4 * (j - 2p) (2-bit). The pairs, as (token, channel):
+//   keys:   t0 = 16 half + a, c0 = 16 j + 2 b:
+//           (t0, c0|c0+1), (t0+8, c0|c0+1), (t0, c0+8|c0+9), (t0+8, c0+8|c0+9)
+//   values: r0 = 16 j + a, k0 = 16 half + 2 b:
+//           (k0|k0+1, r0), (k0|k0+1, r0+8), (k0+8|k0+9, r0), (k0+8|k0+9, r0+8)
+// so a lane's word is exactly the four 16-bit A-fragment registers of an m16n8k16 MMA over that
+// 16 x 16 tile (keys: M = tokens, K = channels; values: M = channels, K = tokens).
+template <int D, int BITS, bool KEYS>
+__device__ __forceinline__ uint32_t block_word(const uint8_t (*codes)[D], int widx) {
+  constexpr int STEPS = BITS == 4 ? D / 16 : D / 32;  // words per (half, lane) row
+  const int lane = widx & 31;
+  const int step = (widx >> 5) % STEPS;
+  const int half = (widx >> 5) / STEPS;
+  const int a = lane >> 2, b = lane & 3;
+  uint32_t w = 0;
+#pragma unroll
+  for (int f = 0; f < (BITS == 4 ? 4 : 8); ++f) {
+    const int j = BITS == 4 ? step : 2 * step + (f >> 2);
+    const int i = f & 3;
+    const int sh = BITS * f;
+    uint32_t lo, hi;
+    if (KEYS) {
+      const int t = 16 * half + a + ((i & 1) ? 8 : 0);
+      const int c = 16 * j + 2 * b + ((i & 2) ? 8 : 0);
+      lo = codes[t][c];
+      hi = codes[t][c + 1];
+    } else {
+      const int r = 16 * j + a + ((i & 1) ? 8 : 0);
+      const int k = 16 * half + 2 * b + ((i & 2) ? 8 : 0);
+      lo = codes[k][r];
+      hi = codes[k + 1][r];
+    }
+    w |= (lo << sh) | (hi << (16 + sh));
+  }
+  return w;
+}
+
+// keys: grid (ng_max, Hkv, B), block D: thread c quantises channel c over the block's 32 tokens.
 template <int D, int BITS>
 __global__ void __launch_bounds__(D) quant_keys_kernel(const __grid_constant__ QuantParams p) {
   const QuantReq& r = p.req[blockIdx.z];
   const int g = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
   if (g >= r.ng) return;
+  __shared__ uint8_t codes[32][D];
   const bf16* src = r.k + ((size_t)h * r.cap + 32 * g) * D + c;
   float x[32];
   float mn = INFINITY, mx = -INFINITY;
@@ -242,70 +283,55 @@ __global__ void __launch_bounds__(D) quant_keys_kernel(const __grid_constant__ Q
   const size_t gi = ((size_t)h * r.ng + g) * D + c;
   r.ks[gi] = s16;
   r.kz[gi] = z16;
-  // 32 codes packed little-endian along tokens: 8 bytes (2-bit) or 16 bytes (4-bit)
-  uint32_t w[BITS];
 #pragma unroll
-  for (int k = 0; k < BITS; ++k) w[k] = 0u;
-#pragma unroll
-  for (int t = 0; t < 32; ++t) {
-    const uint32_t q = quant_code<BITS>(x[t], sf, zf);
-    const int bit = BITS * t;
-    w[bit / 32] |= q << (bit % 32);
-  }
-  uint8_t* dst = r.kc + gi * (4 * BITS);
-  if (BITS == 2) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1 % BITS]);
-  } else {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1 % BITS], w[2 % BITS], w[3 % BITS]);
-  }
+  for (int t = 0; t < 32; ++t) codes[t][c] = (uint8_t)quant_code<BITS>(x[t], sf, zf);
+  __syncthreads();
+  uint32_t* dst = reinterpret_cast<uint32_t*>(r.kc + ((size_t)h * r.ng + g) * (4 * D * BITS));
+  for (int wi = c; wi < D * BITS; wi += D) dst[wi] = block_word<D, BITS, true>(codes, wi);
 }
 
-// values: grid (ceil(Tq/8), Hkv, B), block 256: warp per token, lane per D/32 channels.
+// values: grid (ng_max, Hkv, B), block 256: warp w quantises tokens w, w+8, w+16, w+24 of the
+// block, lane l channels (D/32) l .. (D/32) l + D/32 - 1 (one 32-channel group per D/32 * ... lanes).
 template <int D, int BITS>
 __global__ void __launch_bounds__(256) quant_values_kernel(const __grid_constant__ QuantParams p) {
   const QuantReq& r = p.req[blockIdx.z];
-  const int h = blockIdx.y, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int Tq = 32 * r.ng;
-  if (t >= Tq) return;
+  const int g = blockIdx.x, h = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (g >= r.ng) return;
+  __shared__ uint8_t codes[32][D];
   constexpr int CPL = D / 32;
   constexpr int LPG = 32 / CPL;  // lanes per 32-channel group
   const int c0 = CPL * lane;
-  const bf16* src = r.v + ((size_t)h * r.cap + t) * D + c0;
-  float x[CPL];
-  float mn = INFINITY, mx = -INFINITY;
+#pragma unroll 1
+  for (int tt = warp; tt < 32; tt += 8) {
+    const int t = 32 * g + tt;
+    const bf16* src = r.v + ((size_t)h * r.cap + t) * D + c0;
+    float x[CPL];
+    float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < CPL; ++e) {
-    x[e] = __bfloat162float(src[e]);
-    mn = fminf(mn, x[e]);
-    mx = fmaxf(mx, x[e]);
-  }
+    for (int e = 0; e < CPL; ++e) {
+      x[e] = __bfloat162float(src[e]);
+      mn = fminf(mn, x[e]);
+      mx = fmaxf(mx, x[e]);
+    }
 #pragma unroll
-  for (int off = 1; off < LPG; off <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  }
-  __half s16, z16;
-  float sf, zf;
-  quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
-  uint32_t bitsw = 0;
+    for (int off = 1; off < LPG; off <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    __half s16, z16;
+    float sf, zf;
+    quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
+    const size_t row = (size_t)h * (32 * r.ng) + t;
+    if ((lane % LPG) == 0) {
+      r.vs[row * (D / 32) + c0 / 32] = s16;
+      r.vz[row * (D / 32) + c0 / 32] = z16;
+    }
 #pragma unroll
-  for (int e = 0; e < CPL; ++e) bitsw |= quant_code<BITS>(x[e], sf, zf) << (BITS * e);
-  const size_t row = (size_t)h * Tq + t;
-  if ((lane % LPG) == 0) {
-    r.vs[row * (D / 32) + c0 / 32] = s16;
-    r.vz[row * (D / 32) + c0 / 32] = z16;
+    for (int e = 0; e < CPL; ++e) codes[tt][c0 + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf);
   }
-  uint8_t* dst = r.vc + row * (D * BITS / 8);
-  constexpr int LBITS = CPL * BITS;  // 4, 8 or 16 bits per lane
-  if (LBITS == 4) {
-    const uint32_t nb = __shfl_down_sync(0xffffffffu, bitsw, 1);
-    if ((lane & 1) == 0) dst[lane >> 1] = (uint8_t)(bitsw | (nb << 4));
-  } else if (LBITS == 8) {
-    dst[lane] = (uint8_t)bitsw;
-  } else {
-    reinterpret_cast<uint16_t*>(dst)[lane] = (uint16_t)bitsw;
-  }
+  __syncthreads();
+  uint32_t* dst = reinterpret_cast<uint32_t*>(r.vc + ((size_t)h * r.ng + g) * (4 * D * BITS));
+  for (int wi = threadIdx.x; wi < D * BITS; wi += 256) dst[wi] = block_word<D, BITS, false>(codes, wi);
 }
 
 // residual: rows [Tq, ctx) of K and V -> window rows [0, n_res); grid (ceil(max_res/8), Hkv, B).
@@ -334,7 +360,7 @@ static cudaError_t launch_quant_t(const QuantParams& p, int max_ng, int max_tq, 
     quant_keys_kernel<D, BITS><<<dim3(max_ng, p.Hkv, p.B), D, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    quant_values_kernel<D, BITS><<<dim3((max_tq + 7) / 8, p.Hkv, p.B), 256, 0, s>>>(p);
+    quant_values_kernel<D, BITS><<<dim3(max_ng, p.Hkv, p.B), 256, 0, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -31,9 +31,9 @@
 
 namespace vc {
 
-// KIND 0: bf16 rows (token drop); 2 or 4: quantised, bits. Bf16-row kernels run three 4-warp CTAs
-// per SM with a 2-stage ring per warp (measured better than 2 CTAs x 3 stages or 1 CTA x 6 stages:
-// more warps in flight beat deeper rings); quantised kernels run two CTAs with a dequant tile.
+// KIND 0: bf16 rows (token drop); 2 or 4: quantised, bits. Three 4-warp CTAs per SM with a 2-stage
+// ring per warp (measured better than 2 CTAs x 3 stages or 1 CTA x 6 stages: more warps in flight
+// beat deeper rings).
 template <int D, int KIND>
 struct DraftCfg {
   static constexpr int NW = 4;
@@ -44,9 +44,8 @@ struct DraftCfg {
   static constexpr int QRAW = (KIND == 0) ? 0 : 8 * D * (BITS + 1);  // raw bytes of one 32-token group
   static constexpr int STAGE = (2 * TILE > QRAW) ? 2 * TILE : QRAW;
   static constexpr int NST = 2;
-  static constexpr int CTAS_PER_SM = (KIND == 0) ? 3 : 2;
-  static constexpr int DQ = (KIND == 0) ? 0 : 2 * TILE;  // dequantised K+V tile (quant only)
-  static constexpr int PER_WARP = NST * STAGE + DQ;
+  static constexpr int CTAS_PER_SM = 3;
+  static constexpr int PER_WARP = NST * STAGE;
   static constexpr int BAR_OFF = NW * PER_WARP;
   static constexpr int SMEM = BAR_OFF + NW * NST * 8;
   static constexpr int CHUNK_MAIN = (KIND == 0) ? 16 : 32;
@@ -140,69 +139,168 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
   }
 }
 
-// Dequantise tokens [16*half, 16*half+16) of a raw 32-token group into bf16 K and V tiles.
-template <int D, int BITS>
-__device__ __forceinline__ void dequant_half(const uint8_t* raw, uint8_t* kt, uint8_t* vt, int half, int lane) {
+// Two stored codes of a block word as exact bf16 operands 128 + code (low code -> low half).
+template <int BITS>
+__device__ __forceinline__ uint32_t codes_bf16x2(uint32_t w, int shift) {
+  constexpr uint32_t MASK = BITS == 4 ? 0x000F000Fu : 0x00030003u;
+  return ((w >> shift) & MASK) | 0x43004300u;  // bf16 0x43xx = 128 + xx (xx < 128)
+}
+
+// One quantised 32-token block, read in its stored form (see the block layout in compress.cu): each
+// lane's 32-bit word is exactly its A fragment for an m16n8k16 MMA, so codes enter the tensor cores
+// as exact bf16 integers 128 + code with no dequantised tile in between.
+//   keys (scale s_c, zero z_c per channel):  S^T[t][h] = sum_c (128 + code)(s_c q_hc)
+//                                                     + sum_c (z_c q_hc - 128 s_c q_hc)
+//     -> B operand = (s o q)^T rounded to bf16 once per block, plus a per-head bias;
+//   values (scale s_t, zero z_t per token and 32-channel group g):
+//     O^T[c][h] += sum_t (128 + code)(s_t p_th) + sum_t (z_t p_th - 128 s_t p_th)
+//     -> B operand = (s o p)^T per channel group, plus a per-(group, head) term zs accumulated in the
+//        softmax frame of O and added to O before it is read (fold_zs).
+template <int D, int BITS, int NHB>
+__device__ __forceinline__ void qblock_attend(const uint8_t* raw, int RS_unused, float scale_log2,
+                                              const uint32_t (&qb)[NHB][D / 16][2], float (&o)[NHB][D / 16][4],
+                                              float (&m)[NHB][2], float (&l)[NHB][2], float (&zs)[NHB][D / 32][2],
+                                              int lane) {
   using C = DraftCfg<D, BITS>;
-  constexpr int CPL = D / 32;  // channels per lane
-  constexpr uint32_t MASK = (1u << BITS) - 1u;
-  const int c0 = CPL * lane;
-  // keys: per channel, the 32 tokens' codes are one run of 4*BITS bytes
-  const __half* ks = reinterpret_cast<const __half*>(raw + C::OFF_KS);
-  const __half* kz = reinterpret_cast<const __half*>(raw + C::OFF_KZ);
-  float sk[CPL], zk[CPL];
-  uint64_t wk[CPL];
+  constexpr int MT = D / 16;
+  constexpr int STEPS = BITS == 4 ? D / 16 : D / 32;  // words per (half, lane)
+  const uint32_t* kw = reinterpret_cast<const uint32_t*>(raw + C::OFF_KC);
+  const uint32_t* vw = reinterpret_cast<const uint32_t*>(raw + C::OFF_VC);
+  const __half* ksc = reinterpret_cast<const __half*>(raw + C::OFF_KS);
+  const __half* kze = reinterpret_cast<const __half*>(raw + C::OFF_KZ);
+  const __half* vsc = reinterpret_cast<const __half*>(raw + C::OFF_VS);
+  const __half* vze = reinterpret_cast<const __half*>(raw + C::OFF_VZ);
+  const int b4 = lane & 3, a8 = lane >> 2;
+  // block setup: scaled query fragments and the per-head key bias
+  uint32_t qs[NHB][MT][2];
+  float bias[NHB][2];
 #pragma unroll
-  for (int e = 0; e < CPL; ++e) {
-    const int c = c0 + e;
-    sk[e] = __half2float(ks[c]);
-    zk[e] = __half2float(kz[c]);
-    if (BITS == 2) {
-      wk[e] = *reinterpret_cast<const uint32_t*>(raw + C::OFF_KC + c * 8 + 4 * half);
-    } else {
-      wk[e] = *reinterpret_cast<const uint64_t*>(raw + C::OFF_KC + c * 16 + 8 * half);
+  for (int hb = 0; hb < NHB; ++hb) {
+    float part = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < MT; ++ks)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int c = 16 * ks + 2 * b4 + 8 * r;
+        const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(ksc + c));
+        const float2 ze = __half22float2(*reinterpret_cast<const __half2*>(kze + c));
+        const uint32_t qv = qb[hb][ks][r];
+        const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv));
+        const __nv_bfloat162 qsb = __floats2bfloat162_rn(qf.x * sc.x, qf.y * sc.y);
+        qs[hb][ks][r] = *reinterpret_cast<const uint32_t*>(&qsb);
+        const float2 qsr = __bfloat1622float2(qsb);
+        part += ze.x * qf.x + ze.y * qf.y - 128.f * (qsr.x + qsr.y);
+      }
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);  // bias of head 8hb + lane/4
+    bias[hb][0] = __shfl_sync(0xffffffffu, part, 4 * (2 * b4));
+    bias[hb][1] = __shfl_sync(0xffffffffu, part, 4 * (2 * b4 + 1));
+  }
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    float s[NHB][4];
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[hb][e] = bias[hb][e & 1];
+#pragma unroll
+    for (int ks = 0; ks < MT; ++ks) {
+      const uint32_t w = kw[(half * STEPS + (BITS == 4 ? ks : ks >> 1)) * 32 + lane];
+      const int base = BITS == 4 ? 0 : 4 * BITS * (ks & 1);
+      uint32_t a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = codes_bf16x2<BITS>(w, base + BITS * i);
+#pragma unroll
+      for (int hb = 0; hb < NHB; ++hb) mma_bf16_16816(s[hb], a, qs[hb][ks][0], qs[hb][ks][1]);
+    }
+    // online softmax over the 16 tokens (rows lane/4 and lane/4 + 8; all valid)
+    float p[NHB][2][2];
+    bool moved = false;
+    float corr[NHB][2];
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float x0 = s[hb][e] * scale_log2, x1 = s[hb][e + 2] * scale_log2;
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(m[hb][e], mx);
+        corr[hb][e] = exp2f(m[hb][e] - mn);
+        moved |= mn != m[hb][e];
+        m[hb][e] = mn;
+        p[hb][e][0] = exp2f(x0 - mn);
+        p[hb][e][1] = exp2f(x1 - mn);
+        l[hb][e] = l[hb][e] * corr[hb][e] + p[hb][e][0] + p[hb][e][1];
+      }
+    if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+      for (int hb = 0; hb < NHB; ++hb) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          o[hb][mt][0] *= corr[hb][0];
+          o[hb][mt][1] *= corr[hb][1];
+          o[hb][mt][2] *= corr[hb][0];
+          o[hb][mt][3] *= corr[hb][1];
+        }
+#pragma unroll
+        for (int g = 0; g < D / 32; ++g) {
+          zs[hb][g][0] *= corr[hb][0];
+          zs[hb][g][1] *= corr[hb][1];
+        }
+      }
+    }
+    const int t0 = 16 * half + a8, t1 = t0 + 8;
+#pragma unroll
+    for (int g = 0; g < D / 32; ++g) {
+      const float s0 = __half2float(vsc[t0 * (D / 32) + g]), s1 = __half2float(vsc[t1 * (D / 32) + g]);
+      const float z0 = __half2float(vze[t0 * (D / 32) + g]), z1 = __half2float(vze[t1 * (D / 32) + g]);
+      uint32_t pb[NHB][2];
+#pragma unroll
+      for (int hb = 0; hb < NHB; ++hb) {
+        const __nv_bfloat162 k0 = __floats2bfloat162_rn(p[hb][0][0] * s0, p[hb][1][0] * s0);  // token t0
+        const __nv_bfloat162 k1 = __floats2bfloat162_rn(p[hb][0][1] * s1, p[hb][1][1] * s1);  // token t1
+        const float2 r0 = __bfloat1622float2(k0), r1 = __bfloat1622float2(k1);
+        zs[hb][g][0] += z0 * p[hb][0][0] + z1 * p[hb][0][1] - 128.f * (r0.x + r1.x);
+        zs[hb][g][1] += z0 * p[hb][1][0] + z1 * p[hb][1][1] - 128.f * (r0.y + r1.y);
+        pb[hb][0] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&k0));
+        pb[hb][1] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&k1));
+      }
+#pragma unroll
+      for (int mm = 0; mm < 2; ++mm) {
+        const int mt = 2 * g + mm;
+        const uint32_t w = vw[(half * STEPS + (BITS == 4 ? mt : mt >> 1)) * 32 + lane];
+        const int base = BITS == 4 ? 0 : 4 * BITS * (mt & 1);
+        uint32_t a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = codes_bf16x2<BITS>(w, base + BITS * i);
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) mma_bf16_16816(o[hb][mt], a, pb[hb][0], pb[hb][1]);
+      }
     }
   }
+}
+
+// Add the value zero/offset terms into O (sum over the lanes' tokens first) and clear them.
+template <int D, int NHB>
+__device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zs)[NHB][D / 32][2]) {
 #pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    float x[CPL];
+  for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) x[e] = fmaf((float)((uint32_t)(wk[e] >> (BITS * t)) & MASK), sk[e], zk[e]);
-    uint8_t* dst = kt + t * C::RS + c0 * 2;
-    if (CPL == 4) {
-      uint2 v;
-      v.x = pack_bf16x2(x[0], x[1]);
-      v.y = pack_bf16x2(x[CPL > 2 ? 2 : 0], x[CPL > 3 ? 3 : 0]);
-      *reinterpret_cast<uint2*>(dst) = v;
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(x[0], x[CPL > 1 ? 1 : 0]);
-    }
-  }
-  // values: per token, the D channels' codes are one run of D*BITS/8 bytes
-  const __half* vs = reinterpret_cast<const __half*>(raw + C::OFF_VS);
-  const __half* vz = reinterpret_cast<const __half*>(raw + C::OFF_VZ);
-  const int grp = c0 / 32;
-  const int bit0 = c0 * BITS;
-#pragma unroll 4
-  for (int tt = 0; tt < 16; ++tt) {
-    const int t = 16 * half + tt;
-    const uint32_t w =
-        *reinterpret_cast<const uint32_t*>(raw + C::OFF_VC + t * (D * BITS / 8) + (bit0 / 32) * 4) >> (bit0 % 32);
-    const float s = __half2float(vs[t * (D / 32) + grp]);
-    const float z = __half2float(vz[t * (D / 32) + grp]);
-    float x[CPL];
+    for (int g = 0; g < D / 32; ++g)
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) x[e] = fmaf((float)((w >> (BITS * e)) & MASK), s, z);
-    uint8_t* dst = vt + tt * C::RS + c0 * 2;
-    if (CPL == 4) {
-      uint2 v;
-      v.x = pack_bf16x2(x[0], x[1]);
-      v.y = pack_bf16x2(x[CPL > 2 ? 2 : 0], x[CPL > 3 ? 3 : 0]);
-      *reinterpret_cast<uint2*>(dst) = v;
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(x[0], x[CPL > 1 ? 1 : 0]);
-    }
-  }
+      for (int e = 0; e < 2; ++e) {
+        float z = zs[hb][g][e];
+        z += __shfl_xor_sync(0xffffffffu, z, 4);
+        z += __shfl_xor_sync(0xffffffffu, z, 8);
+        z += __shfl_xor_sync(0xffffffffu, z, 16);
+        o[hb][2 * g][e] += z;
+        o[hb][2 * g][e + 2] += z;
+        o[hb][2 * g + 1][e] += z;
+        o[hb][2 * g + 1][e + 2] += z;
+        zs[hb][g][e] = 0.f;
+      }
 }
 
 // Advance a request cursor to the request holding chunk `pos` (positions only grow along a warp's
@@ -220,8 +318,9 @@ __device__ __forceinline__ void warp_span(const DraftParams& p, int b, int64_t& 
   w1 = (c1 * W - 1) / T;
 }
 
+// More than 8 query heads per KV head (NHB = 2) doubles the accumulators: two CTAs per SM.
 template <int D, int KIND, int NHB>
-__global__ void __launch_bounds__(128, DraftCfg<D, KIND>::CTAS_PER_SM)
+__global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM : 2)
     draft_attn_kernel(const __grid_constant__ DraftParams p) {
   using C = DraftCfg<D, KIND>;
   constexpr bool BF16_ROWS = KIND == 0;  // cp.async pipeline; otherwise bulk copies on mbarriers
@@ -337,8 +436,10 @@ __global__ void __launch_bounds__(128, DraftCfg<D, KIND>::CTAS_PER_SM)
 
   float o[NHB][C::MT][4];
   float m[NHB][2], l[NHB][2];
+  float zs[NHB][D / 32][2];  // value zero/offset terms of quantised blocks not yet folded into o
   uint32_t qb[NHB][C::MT][2];
   int cur_b = -1;
+  bool zs_live = false;
 
   auto reset = [&]() {
 #pragma unroll
@@ -349,6 +450,8 @@ __global__ void __launch_bounds__(128, DraftCfg<D, KIND>::CTAS_PER_SM)
         for (int e = 0; e < 4; ++e) o[hb][mt][e] = 0.f;
       m[hb][0] = m[hb][1] = -INFINITY;
       l[hb][0] = l[hb][1] = 0.f;
+#pragma unroll
+      for (int g = 0; g < D / 32; ++g) zs[hb][g][0] = zs[hb][g][1] = 0.f;
     }
   };
   // Q^T B fragments: k = channel 16ks + 2(lane%4) (+8), n = head 8hb + lane/4 (zero beyond G)
@@ -413,6 +516,10 @@ __global__ void __launch_bounds__(128, DraftCfg<D, KIND>::CTAS_PER_SM)
     int b, lc;
     locate(i, b, lc, cur_proc);
     if (b != cur_b) {
+      if (!BF16_ROWS && zs_live) {
+        fold_zs<D, NHB>(o, zs);
+        zs_live = false;
+      }
       if (cur_b >= 0) finish(cur_b);
       reset();
       load_q(b);
@@ -439,16 +546,13 @@ __global__ void __launch_bounds__(128, DraftCfg<D, KIND>::CTAS_PER_SM)
     const DraftReqDev& r = p.req[b];
     uint8_t* sb = wb + st * C::STAGE;
     if (!BF16_ROWS && lc < r.n_mc) {
-      uint8_t* kt = wb + C::NST * C::STAGE;
-      uint8_t* vt = kt + C::TILE;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        dequant_half<D, C::BITS>(sb, kt, vt, half, lane);
-        __syncwarp();
-        tile_attend<D, NHB>(kt, vt, 16, C::RS, p.scale_log2, qb, o, m, l, lane);
-        __syncwarp();
-      }
+      qblock_attend<D, C::BITS, NHB>(sb, C::RS, p.scale_log2, qb, o, m, l, zs, lane);
+      zs_live = true;
     } else {
+      if (!BF16_ROWS && zs_live) {
+        fold_zs<D, NHB>(o, zs);
+        zs_live = false;
+      }
       const int cnt = (lc < r.n_mc) ? min(16, r.n_main - lc * 16) : min(16, r.n_win + 1 - (lc - r.n_mc) * 16);
       tile_attend<D, NHB>(sb, sb + C::TILE, cnt, C::RS, p.scale_log2, qb, o, m, l, lane);
     }
@@ -461,6 +565,7 @@ __global__ void __launch_bounds__(128, DraftCfg<D, KIND>::CTAS_PER_SM)
     }
   }
   if (BF16_ROWS) cp_async_wait<0>();
+  if (!BF16_ROWS && zs_live) fold_zs<D, NHB>(o, zs);
   finish(cur_b);
 }
 
@@ -547,7 +652,7 @@ static cudaError_t launch_draft_g(const DraftParams& p, int ctas_per_head, cudaS
   return p.G <= 8 ? launch_draft_t<D, KIND, 1>(p, ctas_per_head, s) : launch_draft_t<D, KIND, 2>(p, ctas_per_head, s);
 }
 
-int draft_ctas_per_sm(int kind) { return kind == 0 ? DraftCfg<128, 0>::CTAS_PER_SM : DraftCfg<128, 2>::CTAS_PER_SM; }
+int draft_ctas_per_sm(int G) { return G <= 8 ? DraftCfg<128, 0>::CTAS_PER_SM : 2; }
 
 cudaError_t launch_draft(const DraftParams& p, int d, int kind, int ctas_per_head, cudaStream_t s) {
   if (d == 128) {

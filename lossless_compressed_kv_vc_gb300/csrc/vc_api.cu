@@ -37,13 +37,13 @@ static int sm_count() {
 }
 
 namespace vc {
-int draft_ctas_per_sm(int kind);
+int draft_ctas_per_sm(int G);
 }
 
-// CTAs per KV head of a draft launch: one wave of the kind's CTAs per SM over all heads
-// (kind 0 = bf16 rows; the workspace bound takes the largest, kind 0).
-static int draft_ctas_per_head_max(int Hkv, int kind = 0) {
-  const int n = vc::draft_ctas_per_sm(kind) * sm_count() / Hkv;
+// CTAs per KV head of a draft launch: one wave of CTAs over all heads (the workspace bound takes
+// the largest wave, G <= 8).
+static int draft_ctas_per_head_max(int Hkv, int G = 1) {
+  const int n = vc::draft_ctas_per_sm(G) * sm_count() / Hkv;
   return n > 1 ? n : 1;
 }
 
@@ -250,7 +250,7 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   }
   // one wave of CTAs over the KV heads, but at least ~4 chunks per warp
   const int kind = mode == VC_TOKEN_DROP ? 0 : bits;
-  int per_head = draft_ctas_per_head_max(Hkv, kind);
+  int per_head = draft_ctas_per_head_max(Hkv, G);
   const int env = env_int("VC_DRAFT_CTAS", 0);
   if (env > 0 && env / Hkv < per_head) per_head = env / Hkv > 1 ? env / Hkv : 1;
   const int64_t by_work = (total + 4 * kDraftWarps - 1) / (4 * kDraftWarps);

@@ -94,10 +94,10 @@ class Batch:
             r.n_res = n_res
             b = r.bits
             u8, f16 = torch.uint8, torch.float16
-            r.kc = torch.empty((Hkv, max(ng, 1), d, 4 * b), dtype=u8, device=dev)
+            r.kc = torch.empty((Hkv, max(ng, 1), 4 * d * b), dtype=u8, device=dev)
             r.ks = torch.empty((Hkv, max(ng, 1), d), dtype=f16, device=dev)
             r.kz = torch.empty((Hkv, max(ng, 1), d), dtype=f16, device=dev)
-            r.vc = torch.empty((Hkv, max(32 * ng, 1), d * b // 8), dtype=u8, device=dev)
+            r.vc = torch.empty((Hkv, max(ng, 1), 4 * d * b), dtype=u8, device=dev)
             r.vs = torch.empty((Hkv, max(32 * ng, 1), d // 32), dtype=f16, device=dev)
             r.vz = torch.empty((Hkv, max(32 * ng, 1), d // 32), dtype=f16, device=dev)
         win_cap = r.n_res + r.L + 1

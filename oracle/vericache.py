@@ -123,14 +123,96 @@ def quant_layout(ctx: int, residual_min: int = 128) -> Tuple[int, int]:
     return ng, ctx - GROUP * ng
 
 
+def frag_positions(d: int, kind: str) -> np.ndarray:
+    """Storage order of the codes of one 32-token block (reading: the pages fix no format).
+
+    The codes of a block are stored as 32-bit words w[half][j][lane] (half = 16-token half, j = one
+    16-wide step over the channels, lane = 0..31). Word (half, j, lane) holds four pairs (i = 0..3)
+    of (token, channel) positions, written out below; for keys the pairs run along channels, for
+    values along tokens. Returns int [2][d/16][32][4][2][2]: (token, channel) of the low and the
+    high code of pair i.
+    """
+    pos = np.zeros((2, d // 16, 32, 4, 2, 2), dtype=np.int64)
+    for half in range(2):
+        for j in range(d // 16):
+            for lane in range(32):
+                a, b = lane // 4, lane % 4
+                if kind == "k":
+                    t0, c0 = 16 * half + a, 16 * j + 2 * b
+                    pairs = [((t0, c0), (t0, c0 + 1)), ((t0 + 8, c0), (t0 + 8, c0 + 1)),
+                             ((t0, c0 + 8), (t0, c0 + 9)), ((t0 + 8, c0 + 8), (t0 + 8, c0 + 9))]
+                else:
+                    r0, k0 = 16 * j + a, 16 * half + 2 * b
+                    pairs = [((k0, r0), (k0 + 1, r0)), ((k0, r0 + 8), (k0 + 1, r0 + 8)),
+                             ((k0 + 8, r0), (k0 + 9, r0)), ((k0 + 8, r0 + 8), (k0 + 9, r0 + 8))]
+                pos[half, j, lane] = np.array(pairs)
+    return pos
+
+
+def pack_block(codes: np.ndarray, bits: int, kind: str) -> np.ndarray:
+    """Pack codes [..., 32 tokens, d] of whole blocks into their words, as little-endian bytes.
+
+    4-bit: one word per (half, j, lane): pair i puts its low code at bits 4i and its high code at
+    bits 16 + 4i. 2-bit: one word per (half, p, lane) covering steps j = 2p (pairs f = 0..3) and
+    j = 2p + 1 (pairs f = 4..7): low code at bits 2f, high code at bits 16 + 2f.
+    Output uint8 [..., 32 * d * bits / 8]: words in order [half][j or p][lane].
+    """
+    c = np.asarray(codes, dtype=np.uint32)
+    d = c.shape[-1]
+    lead = c.shape[:-2]
+    pos = frag_positions(d, kind)
+    if bits == 4:
+        w = np.zeros(lead + (2, d // 16, 32), dtype=np.uint32)
+        for i in range(4):
+            sel = pos[:, :, :, i]                       # [2, d/16, 32, 2, 2]
+            lo = c[..., sel[..., 0, 0], sel[..., 0, 1]]
+            hi = c[..., sel[..., 1, 0], sel[..., 1, 1]]
+            w |= (lo << np.uint32(4 * i)) | (hi << np.uint32(16 + 4 * i))
+    else:
+        w = np.zeros(lead + (2, d // 32, 32), dtype=np.uint32)
+        for f in range(8):
+            sel = pos[:, f // 4::2, :, f % 4]           # steps j = 2p + f // 4: [2, d/32, 32, 2, 2]
+            lo = c[..., sel[..., 0, 0], sel[..., 0, 1]]
+            hi = c[..., sel[..., 1, 0], sel[..., 1, 1]]
+            w |= (lo << np.uint32(2 * f)) | (hi << np.uint32(16 + 2 * f))
+    n_words = w.shape[-3] * w.shape[-2] * w.shape[-1]
+    return np.ascontiguousarray(w.astype("<u4")).reshape(lead + (n_words,)).view(np.uint8)
+
+
+def unpack_block(packed: np.ndarray, bits: int, kind: str, d: int) -> np.ndarray:
+    """Inverse of pack_block: uint8 [..., 32 * d * bits / 8] -> codes uint8 [..., 32, d]."""
+    p = np.ascontiguousarray(packed).view("<u4").astype(np.uint32)
+    pos = frag_positions(d, kind)
+    lead = p.shape[:-1]
+    out = np.zeros(lead + (32, d), dtype=np.uint8)
+    mask = np.uint32((1 << bits) - 1)
+    if bits == 4:
+        w = p.reshape(lead + (2, d // 16, 32))
+        for i in range(4):
+            lo = (w >> np.uint32(4 * i)) & mask
+            hi = (w >> np.uint32(16 + 4 * i)) & mask
+            out[..., pos[..., i, 0, 0], pos[..., i, 0, 1]] = lo
+            out[..., pos[..., i, 1, 0], pos[..., i, 1, 1]] = hi
+    else:
+        w = p.reshape(lead + (2, d // 32, 32))
+        for f in range(8):
+            jj, i = f // 4, f % 4
+            lo = (w >> np.uint32(2 * f)) & mask
+            hi = (w >> np.uint32(16 + 2 * f)) & mask
+            sel = pos[:, jj::2, :, i]  # steps j = 2p + jj
+            out[..., sel[..., 0, 0], sel[..., 0, 1]] = lo
+            out[..., sel[..., 1, 0], sel[..., 1, 1]] = hi
+    return out
+
+
 def quantize_kv(k: np.ndarray, v: np.ndarray, bits: int, residual_min: int = 128) -> dict:
     """Quantise one request's cache. k, v: float32 images of the bf16 cache, [Hkv][ctx][d].
 
-    Keys: one group per (head, 32-token group, channel), codes packed along the 32 tokens.
-    Values: one group per (head, token, 32-channel group), codes packed along the channels.
-    Layout (all C-contiguous):
-      kc uint8 [Hkv][ng][d][32*b/8]   ks, kz float16 [Hkv][ng][d]
-      vc uint8 [Hkv][Tq][d*b/8]       vs, vz float16 [Hkv][Tq][d/32]
+    Keys: one group per (head, 32-token block, channel); values: one group per (head, token,
+    32-channel group). Codes of each 32-token block are stored by pack_block (keys pair along
+    channels, values along tokens). Layout (all C-contiguous):
+      kc uint8 [Hkv][ng][32*d*b/8]   ks, kz float16 [Hkv][ng][d]
+      vc uint8 [Hkv][ng][32*d*b/8]   vs, vz float16 [Hkv][Tq][d/32]
       k_res, v_res float32 [Hkv][n_res][d]  (tokens Tq..ctx-1, unchanged)
     """
     H, ctx, d = k.shape
@@ -140,24 +222,24 @@ def quantize_kv(k: np.ndarray, v: np.ndarray, bits: int, residual_min: int = 128
     kcodes, ks, kz = quant_groups(kq, bits)
     vq = v[:, :Tq, :].reshape(H, Tq, d // GROUP, GROUP)               # [H][Tq][d/32][32 ch]
     vcodes, vs, vz = quant_groups(vq, bits)
+    kblk = kcodes.transpose(0, 1, 3, 2)                                # [H][ng][32 tokens][d]
+    vblk = vcodes.reshape(H, ng, GROUP, d)                             # [H][ng][32 tokens][d]
     return dict(bits=bits, ng=ng, n_res=n_res,
-                kc=pack(kcodes, bits), ks=ks, kz=kz,
-                vc=pack(vcodes.reshape(H, Tq, d), bits), vs=vs, vz=vz,
+                kc=pack_block(kblk, bits, "k"), ks=ks, kz=kz,
+                vc=pack_block(vblk, bits, "v"), vs=vs, vz=vz,
                 k_res=k[:, Tq:, :].copy(), v_res=v[:, Tq:, :].copy())
 
 
 def dequantize_kv(qkv: dict, d: int) -> Tuple[np.ndarray, np.ndarray]:
     """x_hat = code * f32(s16) + f32(z16) in float32, back in [Hkv][Tq][d] token-major order."""
     bits = qkv["bits"]
-    kc = unpack(qkv["kc"], bits).astype(np.float32)            # [H][ng][d][32]
-    kh = kc * qkv["ks"].astype(np.float32)[..., None] + qkv["kz"].astype(np.float32)[..., None]
+    kc = unpack_block(qkv["kc"], bits, "k", d).astype(np.float32)     # [H][ng][32][d]
+    kh = kc * qkv["ks"].astype(np.float32)[:, :, None, :] + qkv["kz"].astype(np.float32)[:, :, None, :]
     H, ng = kh.shape[0], kh.shape[1]
-    kh = kh.transpose(0, 1, 3, 2).reshape(H, ng * GROUP, d)
-    vc = unpack(qkv["vc"], bits).astype(np.float32)            # [H][Tq][d]
-    Tq = vc.shape[1]
-    vc = vc.reshape(H, Tq, d // GROUP, GROUP)
+    kh = kh.reshape(H, ng * GROUP, d)
+    vc = unpack_block(qkv["vc"], bits, "v", d).astype(np.float32).reshape(H, ng * GROUP, d // GROUP, GROUP)
     vh = vc * qkv["vs"].astype(np.float32)[..., None] + qkv["vz"].astype(np.float32)[..., None]
-    return kh.astype(np.float32), vh.reshape(H, Tq, d).astype(np.float32)
+    return kh.astype(np.float32), vh.reshape(H, ng * GROUP, d).astype(np.float32)
 
 
 # ----------------------------------------------------------------------------------------------

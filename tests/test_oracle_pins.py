@@ -261,7 +261,7 @@ def test_quantize_dequantize_roundtrip(bits):
     k = rng.standard_normal((H, ctx, d)).astype(np.float32); v = rng.standard_normal((H, ctx, d)).astype(np.float32)
     qkv = O.quantize_kv(k, v, bits)
     ng, nr = O.quant_layout(ctx)
-    assert qkv["kc"].shape == (H, ng, d, 32 * bits // 8) and qkv["vc"].shape == (H, 32 * ng, d * bits // 8)
+    assert qkv["kc"].shape == (H, ng, 32 * d * bits // 8) and qkv["vc"].shape == (H, ng, 32 * d * bits // 8)
     assert qkv["ks"].shape == (H, ng, d) and qkv["vs"].shape == (H, 32 * ng, d // 32)
     kh, vh = O.dequantize_kv(qkv, d)
     tol = {2: 1.6, 4: 0.35}[bits]
@@ -306,3 +306,47 @@ def test_planted_logits_mean_accept_length():
     mean = (1 - p ** (Lb + 1)) / (1 - p)
     var = sum((2 * i + 1) * p ** i for i in range(1, Lb + 1)) + 1 - mean ** 2
     assert abs(np.mean(ns) - mean) < 4 * math.sqrt(var / w.B)
+
+
+def test_block_layout_hand_derived_words():
+    """One nonzero code per block, its word and bit worked out by hand from the layout rule:
+    keys  (4-bit, d=32): code 5 at (token 9, channel 3): token 9 = 8 + lane//4 -> lane//4 = 1,
+          channel 3 = 2*(lane%4) + 1 -> lane%4 = 1, so lane 5, pair 1 (rows +8) high code, bits 20..23
+          of word [half 0][j 0][lane 5] = word 5.
+    keys  (2-bit, d=32): code 3 at (token 2, channel 17): lane//4 = 2, 17 = 16 + 2*0 + 1 -> lane 8,
+          step j = 1 = 2*0 + 1 -> pair f = 4 + 0, high code at bits 16 + 8 = 24 of word [0][0][8] = word 8.
+    values(4-bit, d=32): code 7 at (token 17, channel 10): token 17 = 16*1 + 2*0 + 1 -> half 1,
+          lane%4 = 0, high code; channel 10 = 8 + 2 -> lane//4 = 2, pair 1 -> bits 20..23 of word
+          [half 1][j 0][lane 8] = word (1*2 + 0)*32 + 8 = 72.
+    Catches a transposed pair order, a swapped half or lane mapping, and wrong bit offsets."""
+    cases = [(4, "k", 9, 3, 5, 5, 20), (2, "k", 2, 17, 3, 8, 24), (4, "v", 17, 10, 7, 72, 20)]
+    for bits, kind, t, c, code, word, bit in cases:
+        codes = np.zeros((32, 32), dtype=np.uint8)
+        codes[t, c] = code
+        w = O.pack_block(codes, bits, kind).view("<u4")
+        expect = np.zeros_like(w)
+        expect[word] = code << bit
+        assert np.array_equal(w, expect), (bits, kind, np.nonzero(w), w[np.nonzero(w)])
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("kind", ["k", "v"])
+def test_block_layout_is_a_permutation(bits, kind):
+    """Every (token, channel) of a block appears exactly once, and unpack inverts pack."""
+    d = 128
+    pos = O.frag_positions(d, kind).reshape(-1, 2)
+    assert len({tuple(x) for x in pos}) == 32 * d
+    codes = np.random.default_rng(bits).integers(0, 1 << bits, size=(2, 32, d)).astype(np.uint8)
+    assert np.array_equal(O.unpack_block(O.pack_block(codes, bits, kind), bits, kind, d), codes)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quantize_with_no_whole_block(bits):
+    """ctx < 128 + 32 leaves no whole quantised block: everything stays in the bf16 residual."""
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((2, 140, 64)).astype(np.float32)
+    qkv = O.quantize_kv(k, k, bits)
+    assert qkv["ng"] == 0 and qkv["kc"].shape == (2, 0, 32 * 64 * bits // 8)
+    assert np.array_equal(qkv["k_res"], k)
+    kh, vh = O.dequantize_kv(qkv, 64)
+    assert kh.shape == (2, 0, 64) and vh.shape == (2, 0, 64)
