@@ -345,7 +345,19 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   }
   __syncwarp();
   pdl_launch_dependents();
-  pdl_wait();
+  // Ordering against the previous kernel in the stream (programmatic dependent launch): queries,
+  // kept rows and indices are never written by a draft step, verify or accept, so with p.early the
+  // warp streams them at once and waits only before it reads window rows (the previous step
+  // appended one), stores this step's row, or writes outputs and partials (the previous step's
+  // combine may still be reading the workspace).
+  bool waited = !p.early;
+  if (waited) pdl_wait();
+  auto ensure_wait = [&]() {
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+  };
 
   // chunk i of this warp -> (request, chunk within request)
   int cur_row = 0, cur_issue = 0, cur_proc = 0;
@@ -390,6 +402,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       if (lane == 5) bulk_g2s(sb + C::OFF_VZ, r.vz + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st]);
       return;
     }
+    if (lc >= r.n_mc) ensure_wait();  // window rows: the previous step appended one
     // 16 bf16 rows: lane & 15 names the row; lanes 0-15 own its K row, lanes 16-31 its V row
     const int row = lane & 15;
     const bool isv = lane >= 16;
@@ -471,6 +484,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   // end of request b inside this warp: final bf16 output, or an (o, lse) partial in slot wg + b.
   // The lane holds O^T[channel 16mt + lane/4 (+8)][head 8hb + 2(lane%4) + e].
   auto finish = [&](int b) {
+    ensure_wait();
     int64_t w0, w1;
     warp_span(p, b, w0, w1);
     const bool whole = w0 == w1;
@@ -526,6 +540,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       cur_b = b;
       if (lc == 0) {
         // fused append of the step's K/V row (the warp holding the request's first chunk)
+        ensure_wait();
         const DraftReqDev& r = p.req[b];
         constexpr int V16 = C::ROWB / 16;
         const int l16 = lane & 15;

@@ -6,6 +6,9 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
+#include <unordered_map>
+
 namespace vc {
 cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, void* ws, size_t ws_bytes,
                           int32_t* dev_status, cudaStream_t stream, vc_status* st);
@@ -45,6 +48,24 @@ int draft_ctas_per_sm(int G);
 static int draft_ctas_per_head_max(int Hkv, int G = 1) {
   const int n = vc::draft_ctas_per_sm(G) * sm_count() / Hkv;
   return n > 1 ? n : 1;
+}
+
+// Last library operation launched on each stream. A draft step may start streaming before the
+// kernel ahead of it in the stream finishes unless that kernel is a compress (the only writer of
+// kept rows and indices that triggers its dependents early).
+enum { kOpNone = 0, kOpCompress = 1, kOpDraft = 2, kOpVerify = 3, kOpAccept = 4 };
+static std::mutex g_op_mu;
+static std::unordered_map<cudaStream_t, int> g_last_op;
+
+static int last_op(cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_op_mu);
+  auto it = g_last_op.find(s);
+  return it == g_last_op.end() ? kOpNone : it->second;
+}
+
+static void set_last_op(cudaStream_t s, int op) {
+  std::lock_guard<std::mutex> lock(g_op_mu);
+  g_last_op[s] = op;
 }
 
 extern "C" {
@@ -120,6 +141,7 @@ vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const fl
       if (keep > max_keep) max_keep = keep;
     }
     if (launch_keepset(kp, max_keep, stream) != cudaSuccess) return VC_ERR_CUDA;
+    set_last_op(stream, kOpCompress);
     for (int b = 0; b < B; ++b) {
       if (comp[b].keep > full[b].ctx) comp[b].keep = full[b].ctx;
       comp[b].n_win = 0;
@@ -172,6 +194,7 @@ vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const fl
     if (ng > max_ng) max_ng = ng;
   }
   if (launch_quant(qp, max_ng, VC_GROUP * max_ng, stream) != cudaSuccess) return VC_ERR_CUDA;
+  set_last_op(stream, kOpCompress);
   for (int b = 0; b < B; ++b) {
     comp[b].ng = qp.req[b].ng;
     comp[b].n_win = qp.req[b].n_res;
@@ -262,7 +285,10 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   const size_t slots = (size_t)Hkv * (p.n_vwarps + B);
   p.ws_o = static_cast<float*>(ws);
   p.ws_lse = p.ws_o + slots * G * d;
-  return launch_draft(p, d, kind, per_head, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
+  p.early = last_op(stream) != kOpCompress;
+  if (launch_draft(p, d, kind, per_head, stream) != cudaSuccess) return VC_ERR_CUDA;
+  set_last_op(stream, kOpDraft);
+  return VC_OK;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -271,7 +297,9 @@ vc_status vc_verify_attn(const vc_shape* shape, const vc_verify_req* req, void* 
   vc_status st = VC_OK;
   cudaError_t e = launch_verify(shape, req, ws, ws_bytes, dev_status, stream, &st);
   if (st != VC_OK) return st;
-  return e == cudaSuccess ? VC_OK : VC_ERR_CUDA;
+  if (e != cudaSuccess) return VC_ERR_CUDA;
+  set_last_op(stream, kOpVerify);
+  return VC_OK;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -281,7 +309,9 @@ vc_status vc_accept(int32_t B, int32_t L_max, int32_t V, const float* logits, co
   if (L_max > 0 && !draft) return VC_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(logits) & 3u) || (reinterpret_cast<uintptr_t>(out_tokens) & 3u)) return VC_ERR_INVALID;
   AcceptArgs a{logits, draft, L, out_tokens, n_acc, B, L_max, V};
-  return launch_accept(a, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
+  if (launch_accept(a, stream) != cudaSuccess) return VC_ERR_CUDA;
+  set_last_op(stream, kOpAccept);
+  return VC_OK;
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -179,6 +179,10 @@ struct DraftParams {
   int64_t n_vwarps;      // warps per KV head (grid.x * 4)
   int64_t total_chunks;  // chunks per KV head over all requests
   int32_t* dev_status;
+  // 1: the kernel may stream queries, kept rows and indices before the previous kernel in the
+  // stream has finished (set when that kernel is not a compress); it waits for it before reading
+  // window rows, storing the step's row and writing any output.
+  int32_t early;
 };
 
 constexpr int kDraftWarps = 4;

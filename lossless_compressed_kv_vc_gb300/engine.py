@@ -179,14 +179,16 @@ class Batch:
             self._steps.append((vc_shape(len(act), self.Hq, self.Hkv, self.d), arr, act))
 
     def run_round(self, logits, draft, L, out_tokens, n_acc, stream=None, draft_events=None):
-        """compress -> L_max draft steps -> verify -> accept, all on `stream`."""
+        """compress -> L_max draft steps -> verify -> accept, all on `stream`. draft_events, if
+        given, is a (start, end) pair of CUDA events recorded around the whole draft phase (an
+        event between two draft steps would hold back the next step's early start)."""
         self.compress(stream)
+        if draft_events is not None:
+            draft_events[0].record(stream)
         for s, (shape, arr, act) in enumerate(self._steps):
-            if draft_events is not None:
-                draft_events[s][0].record(stream)
             vc_draft_attn(shape, arr, self.ws_draft, self.dev_status, stream)
-            if draft_events is not None:
-                draft_events[s][1].record(stream)
+        if draft_events is not None:
+            draft_events[1].record(stream)
         vc_verify_attn(self.shape, self._verify_arr, self.ws_verify, self.dev_status, stream)
         accept(logits, draft, L, out_tokens, n_acc, stream)
 
