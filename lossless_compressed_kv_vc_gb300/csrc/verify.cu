@@ -89,17 +89,17 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
   uint8_t* sQ = smem;
   uint8_t* sP = smem + C::OFF_P;
   uint8_t* sST = smem + C::OFF_ST;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // [2]
-  uint64_t* sbar = full + 2;
-  uint64_t* obar = full + 3;
-  uint64_t* xbar = full + 4;  // drain barrier for the error path
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(full + 5);
-  volatile int& s_abort = *reinterpret_cast<volatile int*>(reinterpret_cast<uint8_t*>(full + 5) + 4);
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // [2] K tile landed
+  uint64_t* vfull = kfull + 2;                                          // [2] V tile landed
+  uint64_t* sbar = kfull + 4;                                           // S = Q K^T done
+  uint64_t* obar = kfull + 5;                                           // O += P V done
+  uint64_t* xbar = kfull + 6;                                           // drain on the error path
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(kfull + 7);
+  volatile int& s_abort = *reinterpret_cast<volatile int*>(reinterpret_cast<uint8_t*>(kfull + 7) + 4);
 
   if (warp == 0) tc05::alloc(tslot, C::TCOLS);
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&kfull[i], 1);  // kfull[0..1], vfull[0..1]
     mbar_init(sbar, 1);
     mbar_init(obar, 1);
     mbar_init(xbar, 1);
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
   const int64_t T = p.total_tiles, N = p.n_cta, c = blockIdx.x;
   int64_t pos = c * T / N;
   const int64_t end = (c + 1) * T / N;
-  uint32_t g_tile = 0;    // global tile load counter (stage = g & 1, phase = (g >> 1) & 1)
-  uint32_t g_issued = 0;  // tiles whose TMA load thread 0 has issued (error-path drain)
+  uint32_t g_tile = 0;  // global tile counter (stage = g & 1, phase = (g >> 1) & 1)
+  uint32_t gk_issued = 0, gv_issued = 0;  // K / V tiles whose loads thread 0 has issued (error drain)
   uint32_t s_cnt = 0, o_cnt = 0;
   bool failed = false;
 
@@ -160,25 +160,24 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
     tc05::fence_before();
     __syncthreads();
 
-    auto issue_tile = [&](int j, uint32_t g) {
+    // K and V of a tile have their own barriers: a K stage is reloaded as soon as the S MMA that
+    // read it is done (start of the next-but-one iteration's wait), a V stage once its P V is done,
+    // so each load has about two tile periods to land.
+    auto issue_kv = [&](int j, uint32_t g, bool isv) {
       const int st = g & 1;
-      uint8_t* dk = sST + st * C::STAGE;
-      uint8_t* dv = dk + C::KV_BYTES;
-      mbar_arrive_expect_tx(&full[st], C::STAGE);
-      g_issued = g + 1;
+      uint8_t* dst = sST + st * C::STAGE + (isv ? C::KV_BYTES : 0);
+      uint64_t* bar = isv ? &vfull[st] : &kfull[st];
+      mbar_arrive_expect_tx(bar, C::KV_BYTES);
+      (isv ? gv_issued : gk_issued) = g + 1;
       const bool isnew = j >= R.n_full;
       const int tok = isnew ? (j - R.n_full) * VBN : j * VBN;
-      const void* mk = &tm[isnew ? 2 : 0];
-      const void* mv = &tm[isnew ? 3 : 1];
+      const void* map = &tm[(isnew ? 2 : 0) + (isv ? 1 : 0)];
 #pragma unroll
-      for (int kb = 0; kb < C::KB; ++kb) {
-        tc05::tma_load_3d(dk + kb * (VBN * 128), mk, kb * 64, tok, hk, &full[st]);
-        tc05::tma_load_3d(dv + kb * (VBN * 128), mv, kb * 64, tok, hk, &full[st]);
-      }
+      for (int kb = 0; kb < C::KB; ++kb) tc05::tma_load_3d(dst + kb * (VBN * 128), map, kb * 64, tok, hk, bar);
     };
     auto issue_s = [&](uint32_t g) -> bool {
       const int st = g & 1;
-      if (!mbar_wait_bounded(&full[st], (g >> 1) & 1, p.dev_status)) return false;
+      if (!mbar_wait_bounded(&kfull[st], (g >> 1) & 1, p.dev_status)) return false;
       tc05::fence_after();
       const uint32_t kaddr = aST + st * C::STAGE;
 #pragma unroll
@@ -193,8 +192,12 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
 
     if (tid == 0) {
       tc05::fence_after();
-      issue_tile(j0, g_tile);
-      if (nt > 1) issue_tile(j0 + 1, g_tile + 1);
+      issue_kv(j0, g_tile, false);
+      issue_kv(j0, g_tile, true);
+      if (nt > 1) {
+        issue_kv(j0 + 1, g_tile + 1, false);
+        issue_kv(j0 + 1, g_tile + 1, true);
+      }
       if (!issue_s(g_tile)) s_abort = 1;
     }
 
@@ -206,6 +209,7 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
       bool ok = mbar_wait_bounded(sbar, s_cnt & 1, p.dev_status);
       s_cnt++;
       tc05::fence_after();
+      if (tid == 0 && ok && jj + 2 < nt) issue_kv(j + 2, g + 2, false);  // S_g has read K stage g & 1
       float x[VBN];
       {
         uint32_t r0[32], r1[32];
@@ -218,27 +222,32 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
           x[32 + e] = __uint_as_float(r1[e]);
         }
       }
-      // scale and mask
-      float mx = -INFINITY;
-      if (j < R.n_full) {
-        const int lim = R.ctx - j * VBN;
+      // mask invisible keys (only a ragged last KV_full tile or a drafted-rows tile has any), then
+      // the row max by a tree; the scale is folded into the exponent below
+      {
+        const int last = j < R.n_full ? R.ctx - j * VBN - 1 : qi - (j - R.n_full) * VBN;  // last visible key
+        if (last < VBN - 1) {
 #pragma unroll
-        for (int e = 0; e < VBN; ++e) {
-          x[e] = e < lim ? x[e] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[e]);
+          for (int e = 0; e < VBN; ++e)
+            if (e > last) x[e] = -INFINITY;
         }
-      } else {
-        const int lim = qi - (j - R.n_full) * VBN;  // draft rows 0..qi visible
+      }
+      float mx;
+      {
+        float t[VBN / 2];
 #pragma unroll
-        for (int e = 0; e < VBN; ++e) {
-          x[e] = e <= lim ? x[e] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[e]);
-        }
+        for (int e = 0; e < VBN / 2; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
+#pragma unroll
+        for (int w = VBN / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+        mx = t[0] * p.scale_log2;  // the scale is positive: it keeps the order
       }
       if (jj > 0) {
         ok = mbar_wait_bounded(obar, o_cnt & 1, p.dev_status) && ok;  // P V of the previous tile done
         o_cnt++;
         tc05::fence_after();
+        if (tid == 0 && ok && jj + 1 < nt) issue_kv(j + 1, g + 1, true);  // it has read V stage (g - 1) & 1
       }
       const float m_new = fmaxf(m_run, mx);
       if (jj == 0) {
@@ -249,7 +258,7 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
         const bool need = m_new > m_run + 8.f;
         float f = 1.f;
         if (need) {
-          f = exp2f(m_run - m_new);
+          f = ex2_approx(m_run - m_new);
           l_run *= f;
           m_run = m_new;
         }
@@ -267,20 +276,20 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
         }
       }
       const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-      float ls = 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(x[ch * 8 + 2 * e] - mu);
-          const float p1 = exp2f(x[ch * 8 + 2 * e + 1] - mu);
-          ls += p0 + p1;
+          const float p0 = ex2_approx(fmaf(x[ch * 8 + 2 * e], p.scale_log2, -mu));
+          const float p1 = ex2_approx(fmaf(x[ch * 8 + 2 * e + 1], p.scale_log2, -mu));
+          ls[e] += p0 + p1;
           w[e] = pack_bf16x2(p0, p1);
         }
         *reinterpret_cast<uint4*>(sP + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      l_run += ls;
+      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (!ok) s_abort = 1;
       fence_proxy_async_smem();
       tc05::fence_before();
@@ -291,22 +300,19 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
       }
       if (tid == 0) {
         tc05::fence_after();
-        const uint32_t vaddr = aST + (g & 1) * C::STAGE + C::KV_BYTES;
+        if (!mbar_wait_bounded(&vfull[g & 1], (g >> 1) & 1, p.dev_status)) {
+          s_abort = 1;
+        } else {
+          const uint32_t vaddr = aST + (g & 1) * C::STAGE + C::KV_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < VBN / 16; ++kk) {
-          const uint64_t da = tc05::sdesc_sw128(aP + kk * 32, 16, 1024);
-          const uint64_t db = tc05::sdesc_sw128(vaddr + kk * 2048, VBN * 128, 1024);
-          tc05::mma_bf16(tmem + C::OCOL, da, db, IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < VBN / 16; ++kk) {
+            const uint64_t da = tc05::sdesc_sw128(aP + kk * 32, 16, 1024);
+            const uint64_t db = tc05::sdesc_sw128(vaddr + kk * 2048, VBN * 128, 1024);
+            tc05::mma_bf16(tmem + C::OCOL, da, db, IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         tc05::commit(obar);
         if (jj + 1 < nt && !issue_s(g + 1)) s_abort = 1;
-        if (jj + 2 < nt) {
-          // stage (g & 1) is free once this P V has read its V tile
-          if (mbar_wait_bounded(obar, o_cnt & 1, p.dev_status))
-            issue_tile(j + 2, g + 2);
-          else
-            s_abort = 1;
-        }
       }
     }
     if (failed) break;
@@ -357,8 +363,10 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
     // drain: every MMA issued so far, then (bounded) any TMA still landing
     tc05::commit(xbar);
     mbar_wait_bounded(xbar, 0, p.dev_status);
-    for (uint32_t g = (g_issued > 2 ? g_issued - 2 : 0); g < g_issued; ++g)
-      mbar_wait_bounded(&full[g & 1], (g >> 1) & 1, p.dev_status);
+    for (uint32_t g = (gk_issued > 2 ? gk_issued - 2 : 0); g < gk_issued; ++g)
+      mbar_wait_bounded(&kfull[g & 1], (g >> 1) & 1, p.dev_status);
+    for (uint32_t g = (gv_issued > 2 ? gv_issued - 2 : 0); g < gv_issued; ++g)
+      mbar_wait_bounded(&vfull[g & 1], (g >> 1) & 1, p.dev_status);
   }
   tc05::fence_before();
   __syncthreads();
