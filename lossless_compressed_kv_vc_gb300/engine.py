@@ -169,7 +169,8 @@ class Batch:
 
     def prepare_steps(self):
         """Descriptor arrays of every draft step of a round (window counts as after compress), so
-        a round issues its calls without rebuilding them."""
+        a round issues its calls without rebuilding them. Call it after the first compress: the
+        arrays copy the compressed-cache descriptors, whose sizes compress fills in."""
         self._steps = []
         self._verify_arr = self.verify_requests()
         for s in range(self.L_max):
@@ -192,6 +193,40 @@ class Batch:
         vc_verify_attn(self.shape, self._verify_arr, self.ws_verify, self.dev_status, stream)
         accept(logits, draft, L, out_tokens, n_acc, stream)
 
+    def run_round_from_host(self, hr: "HostRound", stream, copy_stream, draft_events=None):
+        """One round whose inputs sit in pinned host memory and whose results go back to it.
+
+        The inputs the draft phase needs (queries, drafted K/V, importance) are copied on `stream`
+        ahead of compress. The accept inputs (drafts, logits, L) cross the host link on
+        `copy_stream` while the GPU drafts and verifies, so the largest transfer of a round (the
+        logits) hides under the HBM-bound draft phase ("Cross-resource staggering (P1)": keep the
+        host link busy while the GPU drafts); accept waits for them. The logits copy of a round
+        waits until the previous round's accept has read the buffer."""
+        with torch.cuda.stream(stream):
+            for h, d in hr.draft_inputs:
+                d.copy_(h, non_blocking=True)
+        # the large copy starts once the small ones are in (so they never queue behind it on the
+        # copy engine) and after the previous round's accept (stream order)
+        hr.inputs_in.record(stream)
+        copy_stream.wait_event(hr.inputs_in)
+        with torch.cuda.stream(copy_stream):
+            for h, d in hr.accept_inputs:
+                d.copy_(h, non_blocking=True)
+        hr.landed.record(copy_stream)
+        self.compress(stream)
+        if draft_events is not None:
+            draft_events[0].record(stream)
+        for shape, arr, act in self._steps:
+            vc_draft_attn(shape, arr, self.ws_draft, self.dev_status, stream)
+        if draft_events is not None:
+            draft_events[1].record(stream)
+        vc_verify_attn(self.shape, self._verify_arr, self.ws_verify, self.dev_status, stream)
+        stream.wait_event(hr.landed)
+        accept(hr.logits, hr.draft, hr.L, hr.out_tokens, hr.n_acc, stream)
+        with torch.cuda.stream(stream):
+            hr.host_tokens.copy_(hr.out_tokens, non_blocking=True)
+            hr.host_n_acc.copy_(hr.n_acc, non_blocking=True)
+
     def verify_requests(self):
         arr = (vc_verify_req * len(self.reqs))()
         for b, r in enumerate(self.reqs):
@@ -207,6 +242,39 @@ class Batch:
 
     def verify(self, stream=None):
         vc_verify_attn(self.shape, self.verify_requests(), self.ws_verify, self.dev_status, stream)
+
+
+class HostRound:
+    """Pinned host buffers of one round's inputs and results, and the device buffers they land in.
+
+    Inputs: each request's queries, drafted K/V rows and (token drop) importance, which the draft
+    phase reads, and the batch's drafts [B][L_max], logits [B][L_max+1][V] and L [B], which only
+    accept reads. Results: accepted tokens [B][L_max+1] and counts [B], valid on the host once the
+    round's stream has been synchronised."""
+
+    def __init__(self, bt: Batch, logits: torch.Tensor, draft: torch.Tensor, L: torch.Tensor,
+                 out_tokens: torch.Tensor, n_acc: torch.Tensor):
+        pin = lambda t: t.detach().to("cpu").pin_memory()
+        self.draft_inputs = []
+        for r in bt.reqs:
+            for t in (r.q, r.k_new, r.v_new, r.importance):
+                if t is not None:
+                    self.draft_inputs.append((pin(t), t))
+        self.logits, self.draft, self.L = logits, draft, L
+        self.accept_inputs = [(pin(t), t) for t in (draft, logits, L)]
+        self.out_tokens, self.n_acc = out_tokens, n_acc
+        self.host_tokens = torch.empty(out_tokens.shape, dtype=out_tokens.dtype).pin_memory()
+        self.host_n_acc = torch.empty(n_acc.shape, dtype=n_acc.dtype).pin_memory()
+        self.landed = torch.cuda.Event()
+        self.inputs_in = torch.cuda.Event()
+
+    @property
+    def h2d_bytes(self) -> int:
+        return sum(h.numel() * h.element_size() for h, _ in self.draft_inputs + self.accept_inputs)
+
+    @property
+    def d2h_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.host_tokens, self.host_n_acc))
 
 
 def accept(logits: torch.Tensor, draft: torch.Tensor, L: torch.Tensor, out_tokens=None, n_acc=None, stream=None):

@@ -94,3 +94,47 @@ def test_staggered_offload_period_matches_oracle(vc):
         for i in range(2):
             rt, rn = O.accept(lg[i].cpu().numpy(), dr[i].cpu().numpy(), int(Lg[i]))
             assert int(nacc[i]) == rn and tok[i, :rn].cpu().tolist() == rt
+
+
+def test_round_from_host_matches_device_round_and_oracle(vc):
+    """The engine's host-input round (inputs copied from pinned host memory, the accept inputs on a
+    second stream under the draft phase) gives bit-identical draft and verify outputs to the
+    device-resident round, and the oracle's accepted tokens in two successive rounds whose host
+    logits differ (the second round's logits copy must wait for the first round's accept)."""
+    from lossless_compressed_kv_vc_gb300 import engine
+    w = configs.scaled(configs.llama8b_drop(), ctx_div=16, batch=3, L=8)
+    w.V = 5000
+    bt = make_batch(w, [0, 1, 2])
+    bt.compress()
+    bt.prepare_steps()
+    draft, logits, L = gen.drafts_and_logits(w, 0, device="cuda")
+    tok = torch.empty((w.B, w.L_max + 1), dtype=torch.int32, device="cuda")
+    nacc = torch.empty((w.B,), dtype=torch.int32, device="cuda")
+    bt.run_round(logits, draft, L, tok, nacc, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ref_d = [r.o_draft.clone() for r in bt.reqs]
+    ref_v = [r.o_verify.clone() for r in bt.reqs]
+    hr = engine.HostRound(bt, logits, draft, L, tok, nacc)
+    for r in bt.reqs:  # the round must use what it copies
+        for t in (r.q, r.k_new, r.v_new, r.importance, r.o_draft, r.o_verify):
+            t.zero_()
+    for t in (draft, logits, L, tok, nacc):
+        t.zero_()
+    cs = torch.cuda.Stream()
+    s = torch.cuda.current_stream()
+    for rnd in (0, 1):
+        d_h, l_h, L_h = gen.drafts_and_logits(w, rnd)
+        for (h, _), src in zip(hr.accept_inputs, (d_h, l_h, L_h)):
+            h.copy_(src)
+        bt.run_round_from_host(hr, s, cs)
+        torch.cuda.synchronize()
+        assert int(bt.dev_status.item()) == 0
+        if rnd == 0:
+            for b in range(w.B):
+                assert torch.equal(bt.reqs[b].o_draft, ref_d[b])
+                assert torch.equal(bt.reqs[b].o_verify, ref_v[b])
+        lg, dr = l_h.numpy(), d_h.numpy()
+        for b in range(w.B):
+            rt, rn = O.accept(lg[b], dr[b], w.L[b])
+            assert int(hr.host_n_acc[b]) == rn, (rnd, b)
+            assert hr.host_tokens[b, :rn].tolist() == rt
