@@ -336,10 +336,11 @@ def run_native(args):
     achieved = alg / (d_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": achieved / float(peaks["hbm_gbs"]), "traffic": profiled_traffic(),
-                "kernel": "draft_attn_kernel<128,0,1> + draft_combine_kernel (one vc_draft_attn call; mean over "
+                "kernel": "draft_attn_kernel<128,0,1> (one vc_draft_attn call, partial merge included; mean over "
                           "the draft phase of each timed round)",
                 "algorithmic_bytes_per_launch": alg, "avg_launch_ms": d_ms, "peak_kind": peak_kind}
-    launches_per_step = 1 + (1 if args.compact else 0) + 2 * w.L_max + 2 + 2
+    # keep-set (+ gather when compacting), one draft launch per step, verify + its merge, accept (2)
+    launches_per_step = 1 + (1 if args.compact else 0) + w.L_max + 2 + 2
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -362,25 +363,18 @@ def run_native(args):
 
 
 def run_e2e(w, bt, draft, logits, L, out_tokens, n_acc, stream, steps, barrier, dist, world, device):
-    """Each step copies that round's inputs from pinned host memory (queries, drafted K/V,
-    importance, drafts, logits, L), runs the round through the C ABI, and reads back n_acc and the
-    accepted tokens."""
+    """Each step is one call of the engine's host-input round: that round's inputs (queries,
+    drafted K/V, importance, drafts, logits, L) are copied from pinned host memory, the round runs
+    through the C ABI, and n_acc and the accepted tokens are read back into pinned host memory.
+    The accept inputs cross the host link on a second stream while the GPU drafts."""
     import torch
-    dev_in = [draft, logits, L]
-    for r in bt.reqs:
-        dev_in += [r.q, r.k_new, r.v_new, r.importance]
-    host_in = [t.detach().to("cpu").pin_memory() for t in dev_in]
-    host_out = [torch.empty(out_tokens.shape, dtype=out_tokens.dtype).pin_memory(),
-                torch.empty(n_acc.shape, dtype=n_acc.dtype).pin_memory()]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    from lossless_compressed_kv_vc_gb300 import engine
+    hr = engine.HostRound(bt, logits, draft, L, out_tokens, n_acc)
+    copy_stream = torch.cuda.Stream()
+    h2d, d2h = hr.h2d_bytes, hr.d2h_bytes
 
     def step():
-        for h, dv in zip(host_in, dev_in):
-            dv.copy_(h, non_blocking=True)
-        bt.run_round(logits, draft, L, out_tokens, n_acc, stream)
-        host_out[0].copy_(out_tokens, non_blocking=True)
-        host_out[1].copy_(n_acc, non_blocking=True)
+        bt.run_round_from_host(hr, stream, copy_stream)
 
     step()
     barrier()
@@ -396,7 +390,7 @@ def run_e2e(w, bt, draft, logits, L, out_tokens, n_acc, stream, steps, barrier, 
         tt = torch.tensor([t], device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t = float(tt.item())
-    tokens = int(host_out[1].sum().item()) * world * steps
+    tokens = int(hr.host_n_acc.sum().item()) * world * steps
     return {"value": tokens / (t / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps}
 

@@ -240,7 +240,9 @@ vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, si
 /* ------------------------------------------------------------------------------------------ */
 /* Workspace bytes vc_draft_attn (call = VC_CALL_DRAFT) or vc_verify_attn (VC_CALL_VERIFY) needs
  * for `shape`; max_rows = the largest n_rows of a verify call (ignored for draft). The workspace
- * holds per-split partial outputs; it needs no initialisation and is not read after the call. */
+ * holds per-split partial outputs (and, for draft, per-request arrival counters tagged with the
+ * call, so a stale count left by an earlier call is ignored); it needs no initialisation and is
+ * not read after the call. Calls that overlap on the GPU must not share a workspace. */
 size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows);
 
 const char* vc_status_string(vc_status s);

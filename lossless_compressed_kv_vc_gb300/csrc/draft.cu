@@ -4,7 +4,7 @@
 // (drafting with KV_comp) and "Cross-resource staggering (P1)" (drafting is bound by HBM
 // bandwidth: it streams the compressed cache).
 //
-// Work decomposition (one launch per draft step, plus a small combine launch):
+// Work decomposition (one launch per draft step):
 //   For one KV head, each request's rows form a list of chunks: its KV_comp rows (16 kept bf16
 //   rows, or one 32-token quantised group, per chunk) followed by its bf16 window rows (16 per
 //   chunk; the last window row is this step's own K/V). The chunk lists of all requests are
@@ -12,17 +12,21 @@
 //   and one grid row per KV head, so every warp streams the same number of bytes. A warp owns its
 //   range outright: its own ring of shared-memory stages, its own online softmax, and at each
 //   request boundary either the final bf16 row (the request lay entirely inside the warp's range)
-//   or an (o, lse) partial in slot warp + request, merged by the combine kernel. No CTA barrier.
+//   or an (o, lse) partial in slot warp + request. The warp whose partial of a request arrives
+//   last (a per-request arrival counter) merges that request's partials, in warp order, into the
+//   output, so a step needs no second launch. No CTA barrier.
 //
 // Tensor cores: scores are S^T = K Q^T and the output O^T += V^T P^T on m16n8k16 MMAs with the
 // 16 tokens (or 16 channels) of a tile as M and the query heads of the KV head as N (8 per MMA,
 // zero-padded), so a KV byte serves all G heads and a 16-token tile costs d/8 MMAs. P^T, produced
 // in the accumulator layout, becomes the next B operand through an in-register 8x8 transpose
-// (movmatrix). O^T is rescaled only when some head's running maximum moved.
+// (movmatrix). A head's running maximum moves only when a tile exceeds it by more than 2^8, so
+// O^T is rescaled rarely; exponentials use the SFU's ex2.approx.
 //
-// Loads: kept bf16 rows arrive by 16-byte cp.async, two whole rows per warp instruction, gathered by
-// index (indices prefetched one stage ahead); quantised groups arrive as six contiguous 1-D bulk
-// copies on the TMA engine and are dequantised in registers into a bf16 tile before the MMAs.
+// Loads: kept bf16 rows arrive by TMA tile::gather4 (four rows by index per load, whole 128-byte
+// lines, 128-byte swizzle; indices prefetched one stage ahead); quantised groups arrive as six
+// contiguous 1-D bulk copies and enter the MMAs in their stored form; bf16 window rows arrive by
+// 16-byte cp.async into the same swizzled tile layout.
 // The warp holding a request's first chunk also stores the step's K/V row into window row n_win
 // (fused append); that row is read from its input, so no other warp depends on the store.
 #include "vc_internal.cuh"
@@ -38,16 +42,18 @@ template <int D, int KIND>
 struct DraftCfg {
   static constexpr int NW = 4;
   static constexpr int ROWB = D * 2;                     // bytes of one bf16 row
-  static constexpr int RS = ROWB + 16;                   // padded smem row stride (conflict-free ldmatrix)
-  static constexpr int TILE = 16 * RS;                   // 16 bf16 rows
+  static constexpr int HALVES = D / 64;                  // 128-byte column blocks of a row
+  static constexpr int BLK = 16 * 128;                   // one column block of a 16-row tile
+  static constexpr int TILE = HALVES * BLK;              // 16 bf16 rows (swizzled column blocks)
   static constexpr int BITS = (KIND == 0) ? 2 : KIND;
   static constexpr int QRAW = (KIND == 0) ? 0 : 8 * D * (BITS + 1);  // raw bytes of one 32-token group
-  static constexpr int STAGE = (2 * TILE > QRAW) ? 2 * TILE : QRAW;
+  static constexpr int STAGE = ((2 * TILE > QRAW ? 2 * TILE : QRAW) + 1023) / 1024 * 1024;
   static constexpr int NST = 2;
   static constexpr int CTAS_PER_SM = 3;
   static constexpr int PER_WARP = NST * STAGE;
   static constexpr int BAR_OFF = NW * PER_WARP;
-  static constexpr int SMEM = BAR_OFF + NW * NST * 8;
+  static constexpr int SMEM = BAR_OFF + NW * NST * 8 + 1024;  // + slack to put the stages on 1024 B
+  static constexpr int G4_OPS = 2 * HALVES * 4;          // gather4 loads that fill a 16-row K+V stage
   static constexpr int CHUNK_MAIN = (KIND == 0) ? 16 : 32;
   static constexpr int MT = D / 16;                      // 16-wide tiles over the head dim
   // raw layout of a quantised group inside a stage
@@ -61,6 +67,24 @@ struct DraftCfg {
   static_assert(SMEM + 1024 <= 228 * 1024 / CTAS_PER_SM, "CTAs per SM");
 };
 
+// Tensor maps are an argument of the token-drop kernels only.
+struct DraftNoMaps {
+  int32_t unused;
+};
+template <int KIND>
+struct DraftMapsOf {
+  using T = DraftNoMaps;
+};
+template <>
+struct DraftMapsOf<0> {
+  using T = DraftMaps;
+};
+
+// Byte offset of 16-byte chunk cc (8 channels) of row r in a 16-row bf16 tile: column blocks of
+// 16 x 128 bytes, the chunk index XOR (r mod 8) inside a block. This is the TMA 128-byte swizzle on
+// a 1024-byte aligned block, and it keeps the eight rows an ldmatrix reads on distinct banks.
+__device__ __forceinline__ int sw_off(int r, int cc) { return (cc >> 3) * 2048 + r * 128 + (((cc & 7) ^ (r & 7)) << 4); }
+
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -71,7 +95,7 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 // qb: Q^T B fragments [head block][k-step][2]; o: O^T accumulators [head block][channel tile][4];
 // m, l: running max and (lane-partial) sum for this lane's two heads of each head block.
 template <int D, int NHB>
-__device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt, int cnt, int RS, float scale_log2,
+__device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt, int cnt, float scale_log2,
                                             const uint32_t (&qb)[NHB][D / 16][2], float (&o)[NHB][D / 16][4],
                                             float (&m)[NHB][2], float (&l)[NHB][2], int lane) {
   float s[NHB][4];
@@ -81,47 +105,60 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
     for (int e = 0; e < 4; ++e) s[hb][e] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    const uint8_t* a_ptr = kt + ((lane & 7) + 8 * ((lane >> 3) & 1)) * RS + (16 * ks + 8 * (lane >> 4)) * 2;
+    const uint8_t* a_ptr = kt + sw_off((lane & 7) + 8 * ((lane >> 3) & 1), 2 * ks + (lane >> 4));
     uint32_t a[4];
     ldsm_x4(a[0], a[1], a[2], a[3], a_ptr);
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) mma_bf16_16816(s[hb], a, qb[hb][ks][0], qb[hb][ks][1]);
   }
-  // rows of the accumulator are tokens lane/4 and lane/4 + 8; columns heads 2(lane%4) + {0,1}
+  // rows of the accumulator are tokens lane/4 and lane/4 + 8; columns heads 2(lane%4) + {0,1}.
+  // The running maximum m (exp2 domain, per head) moves only when a tile's maximum exceeds it by
+  // more than 8, so weights stay below 2^8 and O is rescaled rarely (never lowering the result's
+  // precision: the final division by l uses the same m).
   const bool ok0 = (lane >> 2) < cnt, ok1 = (lane >> 2) + 8 < cnt;
   float p[NHB][2][2];  // [head block][head e][token row 0/1]
-  bool moved = false;
-  float corr[NHB][2];
+  float tmax[NHB][2];
+  bool need = false;
 #pragma unroll
   for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const float x0 = ok0 ? s[hb][e] * scale_log2 : -INFINITY;
-      const float x1 = ok1 ? s[hb][e + 2] * scale_log2 : -INFINITY;
-      float mx = fmaxf(x0, x1);
+      float mx = fmaxf(ok0 ? s[hb][e] : -INFINITY, ok1 ? s[hb][e + 2] : -INFINITY);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float mn = fmaxf(m[hb][e], mx);
-      const float mu = (mn == -INFINITY) ? 0.f : mn;
-      corr[hb][e] = exp2f(m[hb][e] - mu);
-      moved |= mn != m[hb][e];
-      m[hb][e] = mn;
-      p[hb][e][0] = exp2f(x0 - mu);
-      p[hb][e][1] = exp2f(x1 - mu);
-      l[hb][e] = l[hb][e] * corr[hb][e] + p[hb][e][0] + p[hb][e][1];
+      tmax[hb][e] = mx * scale_log2;  // the scale is positive: it keeps the order
+      need |= tmax[hb][e] > m[hb][e] + 8.f;
     }
-  if (__any_sync(0xffffffffu, moved)) {
+  if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-    for (int hb = 0; hb < NHB; ++hb)
+    for (int hb = 0; hb < NHB; ++hb) {
+      float corr[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float mn = fmaxf(m[hb][e], tmax[hb][e]);
+        corr[e] = ex2_approx(m[hb][e] - mn);  // 0 when m was -inf (nothing accumulated yet)
+        l[hb][e] *= corr[e];
+        m[hb][e] = mn;
+      }
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
-        o[hb][mt][0] *= corr[hb][0];
-        o[hb][mt][1] *= corr[hb][1];
-        o[hb][mt][2] *= corr[hb][0];
-        o[hb][mt][3] *= corr[hb][1];
+        o[hb][mt][0] *= corr[0];
+        o[hb][mt][1] *= corr[1];
+        o[hb][mt][2] *= corr[0];
+        o[hb][mt][3] *= corr[1];
       }
+    }
   }
+#pragma unroll
+  for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float mu = m[hb][e] == -INFINITY ? 0.f : m[hb][e];
+      p[hb][e][0] = ok0 ? ex2_approx(fmaf(s[hb][e], scale_log2, -mu)) : 0.f;
+      p[hb][e][1] = ok1 ? ex2_approx(fmaf(s[hb][e + 2], scale_log2, -mu)) : 0.f;
+      l[hb][e] += p[hb][e][0] + p[hb][e][1];
+    }
   // P^T as the B operand (k = token, n = head): transpose the two 8x8 bf16 blocks of the accumulator
   uint32_t pb[NHB][2];
 #pragma unroll
@@ -131,7 +168,7 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
   }
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
-    const uint8_t* a_ptr = vt + ((lane & 7) + 8 * (lane >> 4)) * RS + (16 * mt + 8 * ((lane >> 3) & 1)) * 2;
+    const uint8_t* a_ptr = vt + sw_off((lane & 7) + 8 * (lane >> 4), 2 * mt + ((lane >> 3) & 1));
     uint32_t a[4];
     ldsm_x4_t(a[0], a[1], a[2], a[3], a_ptr);
 #pragma unroll
@@ -157,7 +194,7 @@ __device__ __forceinline__ uint32_t codes_bf16x2(uint32_t w, int shift) {
 //     -> B operand = (s o p)^T per channel group, plus a per-(group, head) term zs accumulated in the
 //        softmax frame of O and added to O before it is read (fold_zs).
 template <int D, int BITS, int NHB>
-__device__ __forceinline__ void qblock_attend(const uint8_t* raw, int RS_unused, float scale_log2,
+__device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_log2,
                                               const uint32_t (&qb)[NHB][D / 16][2], float (&o)[NHB][D / 16][4],
                                               float (&m)[NHB][2], float (&l)[NHB][2], float (&zs)[NHB][D / 32][2],
                                               int lane) {
@@ -213,44 +250,55 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, int RS_unused,
 #pragma unroll
       for (int hb = 0; hb < NHB; ++hb) mma_bf16_16816(s[hb], a, qs[hb][ks][0], qs[hb][ks][1]);
     }
-    // online softmax over the 16 tokens (rows lane/4 and lane/4 + 8; all valid)
+    // online softmax over the 16 tokens (rows lane/4 and lane/4 + 8; all valid); the running
+    // maximum moves only when a tile exceeds it by more than 8 (exp2 domain), as in tile_attend
     float p[NHB][2][2];
-    bool moved = false;
-    float corr[NHB][2];
+    float tmax[NHB][2];
+    bool need = false;
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float x0 = s[hb][e] * scale_log2, x1 = s[hb][e + 2] * scale_log2;
-        float mx = fmaxf(x0, x1);
+        float mx = fmaxf(s[hb][e], s[hb][e + 2]);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mn = fmaxf(m[hb][e], mx);
-        corr[hb][e] = exp2f(m[hb][e] - mn);
-        moved |= mn != m[hb][e];
-        m[hb][e] = mn;
-        p[hb][e][0] = exp2f(x0 - mn);
-        p[hb][e][1] = exp2f(x1 - mn);
-        l[hb][e] = l[hb][e] * corr[hb][e] + p[hb][e][0] + p[hb][e][1];
+        tmax[hb][e] = mx * scale_log2;
+        need |= tmax[hb][e] > m[hb][e] + 8.f;
       }
-    if (__any_sync(0xffffffffu, moved)) {
+    if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
       for (int hb = 0; hb < NHB; ++hb) {
+        float corr[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float mn = fmaxf(m[hb][e], tmax[hb][e]);
+          corr[e] = ex2_approx(m[hb][e] - mn);
+          l[hb][e] *= corr[e];
+          m[hb][e] = mn;
+        }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          o[hb][mt][0] *= corr[hb][0];
-          o[hb][mt][1] *= corr[hb][1];
-          o[hb][mt][2] *= corr[hb][0];
-          o[hb][mt][3] *= corr[hb][1];
+          o[hb][mt][0] *= corr[0];
+          o[hb][mt][1] *= corr[1];
+          o[hb][mt][2] *= corr[0];
+          o[hb][mt][3] *= corr[1];
         }
 #pragma unroll
         for (int g = 0; g < D / 32; ++g) {
-          zs[hb][g][0] *= corr[hb][0];
-          zs[hb][g][1] *= corr[hb][1];
+          zs[hb][g][0] *= corr[0];
+          zs[hb][g][1] *= corr[1];
         }
       }
     }
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        p[hb][e][0] = ex2_approx(fmaf(s[hb][e], scale_log2, -m[hb][e]));
+        p[hb][e][1] = ex2_approx(fmaf(s[hb][e + 2], scale_log2, -m[hb][e]));
+        l[hb][e] += p[hb][e][0] + p[hb][e][1];
+      }
     const int t0 = 16 * half + a8, t1 = t0 + 8;
 #pragma unroll
     for (int g = 0; g < D / 32; ++g) {
@@ -318,28 +366,126 @@ __device__ __forceinline__ void warp_span(const DraftParams& p, int b, int64_t& 
   w1 = (c1 * W - 1) / T;
 }
 
+// Merge n partials of one query head h (consecutive slots s0 .. s0 + n - 1 of po / pl, in slot
+// order): o = sum_k 2^(lse_k - M) o_k / sum_k 2^(lse_k - M), lse = M + log2(sum_k 2^(lse_k - M)),
+// M the largest lse (log2 domain). One warp; a lane owns D/32 channels. Partials are taken eight
+// at a time with a running maximum (the earlier sum is rescaled when it grows), and each batch's
+// lse values and rows are all loaded before any is used, so a batch costs one trip to L2. Writes
+// the bf16 output row `out` if given, else the merged partial (out_o, out_lse). The partials come
+// from other warps of this launch, so they are read through L2.
+template <int D>
+__device__ __forceinline__ void merge_head(const float* po, const float* pl, int64_t s0, int n, int G, int h, int lane,
+                                           bf16* out, float* out_o, float* out_lse) {
+  constexpr int CPL = D / 32;
+  constexpr int NB = 8;
+  float M = -INFINITY, L = 0.f, acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+#pragma unroll 1
+  for (int j0 = 0; j0 < n; j0 += NB) {
+    float lse[NB], v[NB][CPL];
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj) {
+      lse[jj] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) v[jj][c] = 0.f;
+      if (j0 + jj < n) {
+        const int64_t slot = s0 + j0 + jj;
+        lse[jj] = __ldcg(pl + slot * G + h);
+        const float* row = po + (slot * G + h) * D + CPL * lane;
+        if constexpr (CPL == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4*>(row));
+          v[jj][0] = t.x;
+          v[jj][1 % CPL] = t.y;
+          v[jj][2 % CPL] = t.z;
+          v[jj][3 % CPL] = t.w;
+        } else {
+          const float2 t = __ldcg(reinterpret_cast<const float2*>(row));
+          v[jj][0] = t.x;
+          v[jj][1 % CPL] = t.y;
+        }
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj) mb = fmaxf(mb, lse[jj]);
+    if (mb == -INFINITY) continue;  // nothing to add yet (empty partials)
+    const float f = exp2f(M - mb);  // 0 on the first batch (M = -inf)
+    L *= f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] *= f;
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj) {
+      const float w = exp2f(lse[jj] - mb);  // 0 for padding and empty partials
+      L += w;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[c] += w * v[jj][c];
+    }
+    M = mb;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  if (out) {
+    bf16* dst = out + CPL * lane;
+    if constexpr (CPL == 4) {
+      uint2 o2;
+      o2.x = pack_bf16x2(acc[0] * inv, acc[1 % CPL] * inv);
+      o2.y = pack_bf16x2(acc[2 % CPL] * inv, acc[3 % CPL] * inv);
+      *reinterpret_cast<uint2*>(dst) = o2;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1 % CPL] * inv);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) out_o[CPL * lane + c] = acc[c] * inv;
+    if (lane == 0) *out_lse = L > 0.f ? M + log2f(L) : -INFINITY;
+  }
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Count this CTA's partial of request b (KV head hk) as arrived; true for the CTA that arrives last
+// of the n CTAs holding the request, which then merges. The counter word holds
+// (call tag << 12) | arrivals; a word left with another call's tag (an earlier call, even one that
+// stopped early) counts as zero arrivals, so the workspace needs no initialisation. One thread.
+__device__ __forceinline__ bool cta_arrive(const DraftParams& p, int hk, int b, int n) {
+  uint32_t* ctr = p.ws_ctr + (size_t)hk * VC_MAX_BATCH + b;
+  uint32_t old = *reinterpret_cast<volatile uint32_t*>(ctr), assumed = 0, nv = 0;
+  uint32_t it = 0;
+  do {
+    assumed = old;
+    nv = (assumed >> 12) == p.tag ? assumed + 1 : ((p.tag << 12) | 1u);
+    old = atomicCAS(ctr, assumed, nv);
+  } while (old != assumed && ++it < kSpinLimit);
+  if (old != assumed) {
+    set_status(p.dev_status, VC_DEV_TIMEOUT);
+    return false;
+  }
+  return (nv & 0xFFFu) == (uint32_t)n;
+}
+
 // More than 8 query heads per KV head (NHB = 2) doubles the accumulators: two CTAs per SM.
 template <int D, int KIND, int NHB>
 __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM : 2)
-    draft_attn_kernel(const __grid_constant__ DraftParams p) {
+    draft_attn_kernel(const __grid_constant__ DraftParams p, const __grid_constant__ typename DraftMapsOf<KIND>::T maps) {
   using C = DraftCfg<D, KIND>;
-  constexpr bool BF16_ROWS = KIND == 0;  // cp.async pipeline; otherwise bulk copies on mbarriers
-  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr bool BF16_ROWS = KIND == 0;  // kept rows by TMA gather4; otherwise quantised groups by bulk copies
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // swizzled stages need 1024 B
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hk = blockIdx.y;
   const int G = p.G;
   const int64_t T = p.total_chunks, W = p.n_vwarps;
   const int64_t wg = (int64_t)blockIdx.x * C::NW + warp;
   const int64_t p0 = wg * T / W, p1 = (wg + 1) * T / W;
-  const int n = (int)(p1 - p0);
-  if (n <= 0) {
-    pdl_launch_dependents();
-    return;
-  }
+  const int n = (int)(p1 - p0);  // may be 0: the warp still takes part in the CTA's merge phase
 
+  // Each stage completes on its mbarrier: TMA loads (kept rows, quantised groups) by their bytes,
+  // window rows (cp.async) by a plain arrive once issued, after which the lanes' cp.async groups
+  // are waited for as well. Every stage also commits one cp.async group (possibly empty), so
+  // "all but NST-1 groups done" always means "this stage's copies done".
   uint8_t* wb = smem + warp * C::PER_WARP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF) + warp * C::NST;
-  if (!BF16_ROWS && lane == 0) {
+  if (lane == 0) {
     for (int s = 0; s < C::NST; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
@@ -349,7 +495,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   // kept rows and indices are never written by a draft step, verify or accept, so with p.early the
   // warp streams them at once and waits only before it reads window rows (the previous step
   // appended one), stores this step's row, or writes outputs and partials (the previous step's
-  // combine may still be reading the workspace).
+  // merges may still be reading the workspace).
   bool waited = !p.early;
   if (waited) pdl_wait();
   auto ensure_wait = [&]() {
@@ -388,63 +534,71 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     locate(i, b, lc, cur_issue);
     const DraftReqDev& r = p.req[b];
     uint8_t* sb = wb + st * C::STAGE;
-    if (!BF16_ROWS && lc < r.n_mc) {
-      // one quantised 32-token group: six contiguous runs
-      const int g = lc;
-      const int Tq = 32 * r.ng;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::QRAW);
-      __syncwarp();
-      if (lane == 0) bulk_g2s(sb + C::OFF_KC, r.kc + ((size_t)hk * r.ng + g) * C::KCB, C::KCB, &bars[st]);
-      if (lane == 1) bulk_g2s(sb + C::OFF_KS, r.ks + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st]);
-      if (lane == 2) bulk_g2s(sb + C::OFF_KZ, r.kz + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st]);
-      if (lane == 3) bulk_g2s(sb + C::OFF_VC, r.vc + ((size_t)hk * Tq + 32 * g) * (D * C::BITS / 8), C::KCB, &bars[st]);
-      if (lane == 4) bulk_g2s(sb + C::OFF_VS, r.vs + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st]);
-      if (lane == 5) bulk_g2s(sb + C::OFF_VZ, r.vz + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st]);
-      return;
-    }
-    if (lc >= r.n_mc) ensure_wait();  // window rows: the previous step appended one
-    // 16 bf16 rows: lane & 15 names the row; lanes 0-15 own its K row, lanes 16-31 its V row
-    const int row = lane & 15;
-    const bool isv = lane >= 16;
-    const bf16* src = nullptr;
     if (lc < r.n_mc) {
-      if (t >= 0) {
-        if ((int64_t)t < r.rows_cap)
-          src = (isv ? r.v_rows : r.k_rows) + ((size_t)hk * r.rows_cap + t) * D;
-        else
-          set_status(p.dev_status, VC_DEV_BOUNDS);
-      }
-    } else if (t >= 0) {
-      src = t < r.n_win ? (isv ? r.v_win : r.k_win) + ((size_t)hk * r.win_cap + t) * D
-                        : (isv ? r.v_new : r.k_new) + (size_t)hk * D;
-    }
-    if (BF16_ROWS) {
-      // instruction k copies rows RPI*k .. RPI*k+RPI-1 of the 32 (K rows, then V rows): lane l
-      // moves 16-byte piece l % PPR of its row; rows without a source are zero-filled
-      constexpr int PPR = C::ROWB / 16;  // pieces per row: 16 (d=128) or 8 (d=64)
-      constexpr int RPI = 32 / PPR;      // rows per instruction
-      const unsigned long long sp = reinterpret_cast<unsigned long long>(src);
-      const int piece = lane % PPR;
-#pragma unroll
-      for (int k = 0; k < 32 / RPI; ++k) {
-        const int R = RPI * k + lane / PPR;
-        const unsigned long long rs = __shfl_sync(0xffffffffu, sp, R);
-        uint8_t* dst = sb + (R >= 16 ? C::TILE : 0) + (R & 15) * C::RS + piece * 16;
-        const uint8_t* srow = reinterpret_cast<const uint8_t*>(rs);
-        cp_async16(dst, srow ? srow + piece * 16 : reinterpret_cast<const uint8_t*>(r.k_new), srow ? 16u : 0u);
+      if constexpr (!BF16_ROWS) {
+        // one quantised 32-token group: six contiguous runs
+        const int g = lc;
+        const int Tq = 32 * r.ng;
+        if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::QRAW);
+        __syncwarp();
+        if (lane == 0) bulk_g2s(sb + C::OFF_KC, r.kc + ((size_t)hk * r.ng + g) * C::KCB, C::KCB, &bars[st]);
+        if (lane == 1) bulk_g2s(sb + C::OFF_KS, r.ks + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st]);
+        if (lane == 2) bulk_g2s(sb + C::OFF_KZ, r.kz + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st]);
+        if (lane == 3) bulk_g2s(sb + C::OFF_VC, r.vc + ((size_t)hk * Tq + 32 * g) * (D * C::BITS / 8), C::KCB, &bars[st]);
+        if (lane == 4) bulk_g2s(sb + C::OFF_VS, r.vs + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st]);
+        if (lane == 5) bulk_g2s(sb + C::OFF_VZ, r.vz + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st]);
+      } else {
+        // 16 kept rows by TMA gather4: lane l < G4_OPS loads rows 4(l%4)..4(l%4)+3 of one 64-channel
+        // block of K or V. A row past the kept count repeats the chunk's first row, a kept row
+        // whose probability the softmax sets to zero.
+        int coord = -1;
+        if (t >= 0) {
+          if ((int64_t)t < r.rows_cap)
+            coord = (int)((int64_t)hk * r.rows_cap + t);
+          else
+            set_status(p.dev_status, VC_DEV_BOUNDS);
+        }
+        const int first = __shfl_sync(0xffffffffu, coord, 0);
+        if (coord < 0) coord = first < 0 ? 0 : first;
+        const int g4 = lane & 3;
+        const int c0 = __shfl_sync(0xffffffffu, coord, 4 * g4);
+        const int c1 = __shfl_sync(0xffffffffu, coord, 4 * g4 + 1);
+        const int c2 = __shfl_sync(0xffffffffu, coord, 4 * g4 + 2);
+        const int c3 = __shfl_sync(0xffffffffu, coord, 4 * g4 + 3);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[st], 2 * C::TILE);
+        __syncwarp();
+        if (lane < C::G4_OPS) {
+          const int h = (lane >> 2) % C::HALVES, isv = (lane >> 2) / C::HALVES;
+          tma_gather4(sb + isv * C::TILE + h * C::BLK + g4 * 512, &maps.kv[b][isv], 64 * h, c0, c1, c2, c3,
+                      &bars[st]);
+        }
       }
       cp_async_commit();
       return;
     }
-    uint8_t* dst = sb + (isv ? C::TILE : 0) + row * C::RS;
-    if (!src) {
+    ensure_wait();  // window rows: the previous step appended one
+    // 16 bf16 rows: lane & 15 names the row; lanes 0-15 own its K row, lanes 16-31 its V row
+    const bool isv = lane >= 16;
+    const bf16* src = nullptr;
+    if (t >= 0)
+      src = t < r.n_win ? (isv ? r.v_win : r.k_win) + ((size_t)hk * r.win_cap + t) * D
+                        : (isv ? r.v_new : r.k_new) + (size_t)hk * D;
+    // instruction k copies rows RPI*k .. RPI*k+RPI-1 of the 32 (K rows, then V rows): lane l moves
+    // 16-byte piece l % PPR of its row into the swizzled tile; rows without a source are zero-filled
+    constexpr int PPR = C::ROWB / 16;  // pieces per row: 16 (d=128) or 8 (d=64)
+    constexpr int RPI = 32 / PPR;      // rows per instruction
+    const unsigned long long sp = reinterpret_cast<unsigned long long>(src);
+    const int piece = lane % PPR;
 #pragma unroll
-      for (int e = 0; e < C::ROWB / 16; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < 32 / RPI; ++k) {
+      const int R = RPI * k + lane / PPR;
+      const unsigned long long rs = __shfl_sync(0xffffffffu, sp, R);
+      uint8_t* dst = sb + (R >= 16 ? C::TILE : 0) + sw_off(R & 15, piece);
+      const uint8_t* srow = reinterpret_cast<const uint8_t*>(rs);
+      cp_async16(dst, srow ? srow + piece * 16 : reinterpret_cast<const uint8_t*>(r.k_new), srow ? 16u : 0u);
     }
-    const unsigned ball = __ballot_sync(0xffffffffu, src != nullptr);
-    if (lane == 0) mbar_arrive_expect_tx(&bars[st], __popc(ball) * C::ROWB);
-    __syncwarp();
-    if (src) bulk_g2s(dst, src, C::ROWB, &bars[st]);
+    cp_async_commit();
+    if (lane == 0) mbar_arrive(&bars[st]);
   };
 
   float o[NHB][C::MT][4];
@@ -519,10 +673,10 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       }
   };
 
+  bool aborted = false;
   const int pre = n < C::NST ? n : C::NST;
   for (int i = 0; i < pre; ++i) issue(i, i, row_of(i));
-  if (BF16_ROWS)
-    for (int i = pre; i < C::NST; ++i) cp_async_commit();  // one group per stage in flight
+  for (int i = pre; i < C::NST; ++i) cp_async_commit();  // one group per stage in flight
 #pragma unroll 1
   for (int i = 0; i < n; ++i) {
     const int st = i % C::NST;
@@ -551,17 +705,17 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         }
       }
     }
-    if (BF16_ROWS) {
-      cp_async_wait<C::NST - 1>();  // this lane's copies of chunk i have landed
-      __syncwarp();                  // ... and every other lane's
-    } else if (!mbar_wait_bounded(&bars[st], (i / C::NST) & 1, p.dev_status)) {
+    cp_async_wait<C::NST - 1>();  // this lane's copies of chunk i have landed
+    __syncwarp();                  // ... and every other lane's
+    if (!mbar_wait_bounded(&bars[st], (i / C::NST) & 1, p.dev_status)) {
       for (int j = i + 1; j < n && j < i + C::NST; ++j) mbar_wait_bounded(&bars[j % C::NST], (j / C::NST) & 1, p.dev_status);
-      return;
+      aborted = true;
+      break;
     }
     const DraftReqDev& r = p.req[b];
     uint8_t* sb = wb + st * C::STAGE;
     if (!BF16_ROWS && lc < r.n_mc) {
-      qblock_attend<D, C::BITS, NHB>(sb, C::RS, p.scale_log2, qb, o, m, l, zs, lane);
+      qblock_attend<D, C::BITS, NHB>(sb, p.scale_log2, qb, o, m, l, zs, lane);
       zs_live = true;
     } else {
       if (!BF16_ROWS && zs_live) {
@@ -569,85 +723,73 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         zs_live = false;
       }
       const int cnt = (lc < r.n_mc) ? min(16, r.n_main - lc * 16) : min(16, r.n_win + 1 - (lc - r.n_mc) * 16);
-      tile_attend<D, NHB>(sb, sb + C::TILE, cnt, C::RS, p.scale_log2, qb, o, m, l, lane);
+      tile_attend<D, NHB>(sb, sb + C::TILE, cnt, p.scale_log2, qb, o, m, l, lane);
     }
     __syncwarp();
     if (i + C::NST < n) {
-      if (!BF16_ROWS) fence_proxy_async_smem();
+      fence_proxy_async_smem();  // this warp's reads of the stage come before the TMA overwrites it
       issue(i + C::NST, st, t_next);
-    } else if (BF16_ROWS) {
+    } else {
       cp_async_commit();  // empty group: the wait above always leaves NST-1 groups pending
     }
   }
-  if (BF16_ROWS) cp_async_wait<0>();
-  if (!BF16_ROWS && zs_live) fold_zs<D, NHB>(o, zs);
-  finish(cur_b);
-}
-
-// Merge the per-warp partials of requests split across warps: o = sum_k 2^(lse_k - LSE) o_k / L.
-// grid (B, Hkv, G): one CTA per query head; thread = (channel quad, partial group), so the
-// partials are read in parallel, then summed across groups in shared memory.
-template <int D>
-__global__ void __launch_bounds__(128) draft_combine_kernel(const __grid_constant__ DraftParams p) {
-  constexpr int QPB = D / 4;          // channel quads per head
-  constexpr int PG = 128 / QPB;       // partial groups
-  const int b = blockIdx.x, hk = blockIdx.y, g = blockIdx.z;
-  pdl_launch_dependents();
-  pdl_wait();
-  int64_t w0, w1;
-  warp_span(p, b, w0, w1);
-  if (w0 == w1) return;
-  const int G = p.G;
-  const int tid = threadIdx.x, cq = tid % QPB, pg = tid / QPB;
-  const int np = (int)(w1 - w0 + 1);
-  const size_t base = (size_t)hk * (p.n_vwarps + p.B) + b + w0;  // slot of partial k: base + k
-  __shared__ float s_max[PG];
-  __shared__ float s_l[PG];
-  __shared__ float4 s_acc[PG][QPB];
-  float mx = -INFINITY;
-  for (int k = pg; k < np; k += PG) mx = fmaxf(mx, p.ws_lse[(base + k) * G + g]);
-  if (cq == 0) s_max[pg] = mx;
-  __syncthreads();
-  float M = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < PG; ++i) M = fmaxf(M, s_max[i]);
-  const float Mu = (M == -INFINITY) ? 0.f : M;
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int k = pg; k < np; k += PG) {
-    const float wt = exp2f(p.ws_lse[(base + k) * G + g] - Mu);
-    const float4 v = *reinterpret_cast<const float4*>(p.ws_o + ((base + k) * G + g) * D + 4 * cq);
-    L += wt;
-    acc.x += wt * v.x;
-    acc.y += wt * v.y;
-    acc.z += wt * v.z;
-    acc.w += wt * v.w;
+  cp_async_wait<0>();
+  if (!aborted && cur_b >= 0) {
+    if (!BF16_ROWS && zs_live) fold_zs<D, NHB>(o, zs);
+    finish(cur_b);
   }
-  s_acc[pg][cq] = acc;
-  if (cq == 0) s_l[pg] = L;
-  __syncthreads();
-  if (pg == 0) {
-    float Lt = 0.f;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < PG; ++i) {
-      Lt += s_l[i];
-      a.x += s_acc[i][cq].x;
-      a.y += s_acc[i][cq].y;
-      a.z += s_acc[i][cq].z;
-      a.w += s_acc[i][cq].w;
+
+  // Merge phase, for requests split across warps. First each CTA merges its own warps' partials of
+  // a request (one query head per warp): into the output when the request lies inside this CTA,
+  // else into a CTA partial. Then the CTA that arrives last among those holding the request merges
+  // their CTA partials into the output. Both levels merge in slot order, so results do not depend
+  // on which CTA arrives last. Every condition below is uniform over the CTA.
+  ensure_wait();  // workspace and outputs are written below
+  __syncthreads();  // this CTA's warp partials are written (read back through L2 below)
+  __shared__ int s_last;
+  const int cx = blockIdx.x, NC = gridDim.x;
+  const int64_t q0 = (int64_t)cx * C::NW * T / W, q1 = ((int64_t)cx * C::NW + C::NW) * T / W;  // CTA chunks
+  if (q1 > q0) {
+    int cur = 0;
+    const int bA = draft_find_req(p, q0, cur);
+    const int bB = draft_find_req(p, q1 - 1, cur);
+#pragma unroll 1
+    for (int b = bA; b <= bB; ++b) {
+      int64_t w0, w1;
+      warp_span(p, b, w0, w1);
+      if (w0 == w1) continue;  // inside one warp: its output is written
+      const int64_t cw0 = w0 > (int64_t)cx * C::NW ? w0 : (int64_t)cx * C::NW;
+      const int64_t cw1 = w1 < (int64_t)cx * C::NW + C::NW - 1 ? w1 : (int64_t)cx * C::NW + C::NW - 1;
+      const int64_t c0 = w0 / C::NW, c1 = w1 / C::NW;
+      const bool one_cta = c0 == c1;
+      const int64_t cslot = (int64_t)hk * (NC + p.B) + cx + b;
+      bf16* orow = p.req[b].o + (size_t)hk * G * D;
+      for (int h = warp; h < G; h += C::NW)
+        merge_head<D>(p.ws_o, p.ws_lse, (int64_t)hk * (W + p.B) + b + cw0, (int)(cw1 - cw0 + 1), G, h, lane,
+                      one_cta ? orow + (size_t)h * D : nullptr, p.ws_co + (cslot * G + h) * D, p.ws_clse + cslot * G + h);
+      if (one_cta) continue;
+      // The barrier orders every thread's CTA-partial stores before thread 0's release fence and
+      // arrival; the last arriver's acquire fence and the second barrier order the other CTAs'
+      // partials before this CTA reads them.
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        fence_acq_rel_gpu();
+        const bool last = cta_arrive(p, hk, b, (int)(c1 - c0 + 1));
+        if (last) fence_acq_rel_gpu();
+        s_last = last ? 1 : 0;
+      }
+      __syncthreads();
+      if (s_last) {
+        for (int h = warp; h < G; h += C::NW)
+          merge_head<D>(p.ws_co, p.ws_clse, (int64_t)hk * (NC + p.B) + b + c0, (int)(c1 - c0 + 1), G, h, lane,
+                        orow + (size_t)h * D, nullptr, nullptr);
+      }
     }
-    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
-    uint2 out;
-    out.x = pack_bf16x2(a.x * inv, a.y * inv);
-    out.y = pack_bf16x2(a.z * inv, a.w * inv);
-    *reinterpret_cast<uint2*>(p.req[b].o + (size_t)(hk * G + g) * D + 4 * cq) = out;
   }
 }
 
 template <int D, int KIND, int NHB>
-static cudaError_t launch_draft_t(const DraftParams& p, int ctas_per_head, cudaStream_t s) {
+static cudaError_t launch_draft_t(const DraftParams& p, const DraftMaps* maps, int ctas_per_head, cudaStream_t s) {
   using C = DraftCfg<D, KIND>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -656,28 +798,35 @@ static cudaError_t launch_draft_t(const DraftParams& p, int ctas_per_head, cudaS
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cudaError_t e =
-      launch_pdl(draft_attn_kernel<D, KIND, NHB>, dim3(ctas_per_head, p.Hkv), dim3(128), C::SMEM, s, p);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(draft_combine_kernel<D>, dim3(p.B, p.Hkv, p.G), dim3(128), 0, s, p);
+  cudaError_t e;
+  if constexpr (KIND == 0) {
+    e = launch_pdl(draft_attn_kernel<D, KIND, NHB>, dim3(ctas_per_head, p.Hkv), dim3(128), C::SMEM, s, p, *maps);
+  } else {
+    e = launch_pdl(draft_attn_kernel<D, KIND, NHB>, dim3(ctas_per_head, p.Hkv), dim3(128), C::SMEM, s, p,
+                   DraftNoMaps{0});
+  }
+  return e;
 }
 
 template <int D, int KIND>
-static cudaError_t launch_draft_g(const DraftParams& p, int ctas_per_head, cudaStream_t s) {
-  return p.G <= 8 ? launch_draft_t<D, KIND, 1>(p, ctas_per_head, s) : launch_draft_t<D, KIND, 2>(p, ctas_per_head, s);
+static cudaError_t launch_draft_g(const DraftParams& p, const DraftMaps* maps, int ctas_per_head, cudaStream_t s) {
+  return p.G <= 8 ? launch_draft_t<D, KIND, 1>(p, maps, ctas_per_head, s)
+                  : launch_draft_t<D, KIND, 2>(p, maps, ctas_per_head, s);
 }
 
 int draft_ctas_per_sm(int G) { return G <= 8 ? DraftCfg<128, 0>::CTAS_PER_SM : 2; }
 
-cudaError_t launch_draft(const DraftParams& p, int d, int kind, int ctas_per_head, cudaStream_t s) {
+cudaError_t launch_draft(const DraftParams& p, const DraftMaps* maps, int d, int kind, int ctas_per_head,
+                         cudaStream_t s) {
+  if (kind == 0 && !maps) return cudaErrorInvalidValue;
   if (d == 128) {
-    if (kind == 0) return launch_draft_g<128, 0>(p, ctas_per_head, s);
-    if (kind == 2) return launch_draft_g<128, 2>(p, ctas_per_head, s);
-    if (kind == 4) return launch_draft_g<128, 4>(p, ctas_per_head, s);
+    if (kind == 0) return launch_draft_g<128, 0>(p, maps, ctas_per_head, s);
+    if (kind == 2) return launch_draft_g<128, 2>(p, maps, ctas_per_head, s);
+    if (kind == 4) return launch_draft_g<128, 4>(p, maps, ctas_per_head, s);
   } else if (d == 64) {
-    if (kind == 0) return launch_draft_g<64, 0>(p, ctas_per_head, s);
-    if (kind == 2) return launch_draft_g<64, 2>(p, ctas_per_head, s);
-    if (kind == 4) return launch_draft_g<64, 4>(p, ctas_per_head, s);
+    if (kind == 0) return launch_draft_g<64, 0>(p, maps, ctas_per_head, s);
+    if (kind == 2) return launch_draft_g<64, 2>(p, maps, ctas_per_head, s);
+    if (kind == 4) return launch_draft_g<64, 4>(p, maps, ctas_per_head, s);
   }
   return cudaErrorInvalidValue;
 }

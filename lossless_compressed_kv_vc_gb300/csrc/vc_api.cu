@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -50,6 +51,13 @@ static int draft_ctas_per_head_max(int Hkv, int G = 1) {
   return n > 1 ? n : 1;
 }
 
+// Arrival counters at the start of the draft workspace: one 32-bit word per (KV head, request slot).
+static size_t draft_counter_bytes(int Hkv) { return ((size_t)Hkv * VC_MAX_BATCH * 4 + 255) / 256 * 256; }
+
+// Per-call tag of the draft arrival counters (20 bits; a counter word still holding another
+// call's tag is taken as zero, so the workspace needs no initialisation).
+static std::atomic<uint32_t> g_draft_tag{0};
+
 // Last library operation launched on each stream. A draft step may start streaming before the
 // kernel ahead of it in the stream finishes unless that kernel is a compress (the only writer of
 // kept rows and indices that triggers its dependents early).
@@ -88,8 +96,10 @@ size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows) 
   if (!shape_ok(shape)) return 0;
   if (call == VC_CALL_DRAFT) {
     const size_t G = shape->Hq / shape->Hkv;
-    const size_t slots = (size_t)shape->Hkv * (kDraftWarps * draft_ctas_per_head_max(shape->Hkv) + shape->B);
-    return slots * G * (shape->d + 1) * sizeof(float) + 256;
+    const size_t per_head = draft_ctas_per_head_max(shape->Hkv);
+    const size_t slots = (size_t)shape->Hkv * (kDraftWarps * per_head + shape->B);  // warp partials
+    const size_t cslots = (size_t)shape->Hkv * (per_head + shape->B);               // CTA partials
+    return draft_counter_bytes(shape->Hkv) + (slots + cslots) * G * (shape->d + 1) * sizeof(float) + 512;
   }
   if (call == VC_CALL_VERIFY) return verify_workspace_size(shape, max_rows);
   return 0;
@@ -271,6 +281,18 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
     r.chunk_begin = (int32_t)total;
     total += r.n_chunks;
   }
+  // token drop: tensor maps of the kept K and V rows (2-D over the Hkv * rows_cap rows of each)
+  static thread_local DraftMaps maps;
+  if (mode == VC_TOKEN_DROP) {
+    for (int b = 0; b < B; ++b) {
+      const vc_kv_comp& c = req[b].comp;
+      if (c.keep <= 0) continue;
+      const int64_t rows = (int64_t)Hkv * c.rows_cap;
+      if (rows >= (int64_t(1) << 31)) return VC_ERR_UNSUPPORTED;
+      if (!rows_tmap(&maps.kv[b][0], c.k_rows, d, rows) || !rows_tmap(&maps.kv[b][1], c.v_rows, d, rows))
+        return VC_ERR_CUDA;
+    }
+  }
   // one wave of CTAs over the KV heads, but at least ~4 chunks per warp
   const int kind = mode == VC_TOKEN_DROP ? 0 : bits;
   int per_head = draft_ctas_per_head_max(Hkv, G);
@@ -283,10 +305,15 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   const size_t need = vc_workspace_size(VC_CALL_DRAFT, shape, 0);
   if (!ws || ws_bytes < need || !aligned16(ws)) return VC_ERR_WORKSPACE;
   const size_t slots = (size_t)Hkv * (p.n_vwarps + B);
-  p.ws_o = static_cast<float*>(ws);
+  p.ws_ctr = static_cast<uint32_t*>(ws);
+  p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + draft_counter_bytes(Hkv));
   p.ws_lse = p.ws_o + slots * G * d;
+  const size_t cslots = (size_t)Hkv * (per_head + B);
+  p.ws_co = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(p.ws_lse + slots * G) + 255) & ~uintptr_t(255));
+  p.ws_clse = p.ws_co + cslots * G * d;
+  p.tag = (g_draft_tag.fetch_add(1, std::memory_order_relaxed) + 1) & 0xFFFFFu;
   p.early = last_op(stream) != kOpCompress;
-  if (launch_draft(p, d, kind, per_head, stream) != cudaSuccess) return VC_ERR_CUDA;
+  if (launch_draft(p, &maps, d, kind, per_head, stream) != cudaSuccess) return VC_ERR_CUDA;
   set_last_op(stream, kOpDraft);
   return VC_OK;
 }

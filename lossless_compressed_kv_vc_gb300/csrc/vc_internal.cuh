@@ -1,6 +1,7 @@
 // Internal declarations shared by the kernels and the C-ABI layer of libvc (sm_103a only).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the encoder itself is fetched from the driver at run time)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -77,6 +78,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst_smem)),
       "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Four whole rows of a 2-D tensor map (box 64 elements x 1 row) gathered by row coordinate into
+// four consecutive 128-byte rows of shared memory starting at dst, in the map's swizzle; c0 is the
+// first element of the 64-element column block (a multiple of 64 here, so the 16-byte rule holds).
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int c0, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -184,6 +197,10 @@ struct DraftParams {
   float scale_log2;      // log2(e) / sqrt(d)
   float* ws_o;           // [Hkv][n_vwarps + B][G][d] per-warp partials (slot = warp + request)
   float* ws_lse;         // [Hkv][n_vwarps + B][G]  (log2 domain)
+  float* ws_co;          // [Hkv][CTAs per head + B][G][d] per-CTA partials (slot = CTA + request)
+  float* ws_clse;        // [Hkv][CTAs per head + B][G]
+  uint32_t* ws_ctr;      // [Hkv][VC_MAX_BATCH] CTA-partial arrivals: call tag << 12 | count
+  uint32_t tag;          // this call's tag (20 bits)
   int64_t n_vwarps;      // warps per KV head (grid.x * 4)
   int64_t total_chunks;  // chunks per KV head over all requests
   int32_t* dev_status;
@@ -193,10 +210,26 @@ struct DraftParams {
   int32_t early;
 };
 
+// Tensor maps of the kept K and V rows of each request (token drop): 2-D (d, Hkv * rows_cap) over
+// the bf16 rows, box 64 x 1, 128-byte swizzle. A separate kernel argument, so the combine launch
+// does not carry them.
+struct DraftMaps {
+  CUtensorMap kv[VC_MAX_BATCH][2];
+};
+
 constexpr int kDraftWarps = 4;
 
-// launchers (return cudaError_t of the launch)
-cudaError_t launch_draft(const DraftParams& p, int d, int mode_kind, int ctas_per_head, cudaStream_t s);
+// launchers (return cudaError_t of the launch); maps is read for token drop only
+cudaError_t launch_draft(const DraftParams& p, const DraftMaps* maps, int d, int mode_kind, int ctas_per_head,
+                         cudaStream_t s);
+
+// ---- host: TMA tensor maps --------------------------------------------------------------------------
+// cuTensorMapEncodeTiled from the driver (fetched once through the runtime), or nullptr.
+void* tmap_encoder();
+// 2-D map over `rows` bf16 rows of d elements (row pitch d * 2 bytes): box 64 x 1, 128-byte swizzle,
+// for tile::gather4. Maps are cached per (base, rows, d). False if the encoder is unavailable or
+// rejects the layout.
+bool rows_tmap(CUtensorMap* out, const void* base, int d, int64_t rows);
 
 struct AcceptArgs {
   const float* logits;

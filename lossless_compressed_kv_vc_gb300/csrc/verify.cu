@@ -435,15 +435,7 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_consta
 
 // ------------------------------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tmap_encoder());
 }
 
 // bf16 [Hkv][cap][d] rows 0..rows-1 as a 3-D tensor (d, rows, Hkv); box 64 x 64 x 1, 128-byte swizzle.
