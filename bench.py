@@ -277,6 +277,19 @@ def setup_native(w, device, compact=False):
     return bt, draft, logits, L, out_tokens, n_acc
 
 
+def aggregate(t_ms: float, tokens: int, dist=None, device="cpu"):
+    """Whole-job figures over ranks: (the slowest rank's time in ms, the tokens of all ranks). Each
+    rank passes its own time and token count; without a process group the local figures return."""
+    if dist is None:
+        return t_ms, tokens
+    import torch
+    t = torch.tensor([t_ms], dtype=torch.float64, device=device)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(round(n.item()))
+
+
 def run_native(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -317,14 +330,10 @@ def run_native(args):
         barrier()
     draft_ms = [a.elapsed_time(b) / w.L_max for a, b in ev]  # per draft step (one vc_draft_attn call)
     t_ms = e0.elapsed_time(e1)
-    t_max = t_ms
-    if dist is not None:
-        tt = torch.tensor([t_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max, tokens_all = aggregate(t_ms, tokens_per_step * args.steps, dist, device)
     assert int(bt.dev_status.item()) == 0, "device status set during the timed region"
     ms_per_step = t_max / args.steps
-    value = tokens_per_step * world * args.steps / (t_max / 1e3)
+    value = tokens_all / (t_max / 1e3)
 
     # end-to-end through the public API with host buffers: H2D of the round's inputs, round, D2H
     e2e = run_e2e(w, bt, draft, logits, L, out_tokens, n_acc, stream, args.e2e_steps or max(3, min(args.steps, 100)),
@@ -385,12 +394,7 @@ def run_e2e(w, bt, draft, logits, L, out_tokens, n_acc, stream, steps, barrier, 
         step()
     e1.record(stream)
     barrier()
-    t = e0.elapsed_time(e1)
-    if dist is not None:
-        tt = torch.tensor([t], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
-    tokens = int(hr.host_n_acc.sum().item()) * world * steps
+    t, tokens = aggregate(e0.elapsed_time(e1), int(hr.host_n_acc.sum().item()) * steps, dist, device)
     return {"value": tokens / (t / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps}
 
