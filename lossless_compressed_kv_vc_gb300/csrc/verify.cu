@@ -14,12 +14,16 @@
 // unit writes the bf16 output, otherwise it writes an (o, lse) partial into slot cta + unit, and a
 // small combine kernel merges the partials of split units.
 //
-// Per CTA (128 threads; thread r owns TMEM lane r = query row r):
-//   thread 0 issues TMA loads of K/V tiles (64 tokens, 128-byte swizzle, 2 stages) and the MMAs;
-//   S lands in TMEM columns [0,64), O accumulates in TMEM columns [OCOL, OCOL+d).
-//   Every thread loads its S row (tcgen05.ld), applies scale, mask and online softmax in fp32
-//   (exp2 domain; O is rescaled in TMEM only when the running max grows by more than 8), writes
-//   its P row (bf16) into shared memory in the swizzled K-major layout, and the next MMA reads it.
+// Per CTA (192 threads, three roles that meet on mbarriers):
+//   warps 0-3 (softmax): thread r owns TMEM lane r = query row r; it loads its Q row into the unit's
+//     Q tile, then per KV tile loads its S row (tcgen05.ld), masks, takes the online softmax in fp32
+//     (exp2 domain, ex2.approx; O is rescaled in TMEM only when the row maximum grows by more than
+//     2^8) and writes its P row (bf16) into shared memory in the swizzled K-major layout;
+//   warp 4 (MMA issue): S of tile g = Q K_g^T into TMEM buffer g & 1 (columns [0,64) or [64,128)),
+//     then O += P_{g-1} V_{g-1} (columns [128, 128 + d)), so the next tile's QK^T runs while the
+//     softmax warps work on the current one;
+//   warp 5 (TMA): K and V tiles (64 tokens, 128-byte swizzle) into 2-stage rings, K a tile ahead of
+//     V; a stage is reloaded once the MMA that read it has completed (tcgen05.commit).
 #include "tc05.cuh"
 
 #include <cuda.h>
@@ -54,17 +58,19 @@ struct VerifyParams {
 
 template <int D>
 struct VCfg {
-  static constexpr int KB = D / 64;              // 64-channel (128-byte) blocks
-  static constexpr int Q_BYTES = KB * VM * 128;  // Q tile, K-major SW128
-  static constexpr int P_BYTES = VM * 128;       // P tile (64 tokens), K-major SW128
+  static constexpr int KB = D / 64;                // 64-channel (128-byte) blocks
+  static constexpr int Q_BYTES = KB * VM * 128;    // Q tile, K-major SW128
+  static constexpr int P_BYTES = VM * 128;         // P tile (64 tokens), K-major SW128
   static constexpr int KV_BYTES = KB * VBN * 128;  // one K (or V) tile
-  static constexpr int STAGE = 2 * KV_BYTES;
   static constexpr int OFF_P = Q_BYTES;
-  static constexpr int OFF_ST = OFF_P + P_BYTES;
-  static constexpr int OFF_BAR = OFF_ST + 2 * STAGE;
-  static constexpr int SMEM = OFF_BAR + 64;
-  static constexpr int OCOL = D == 128 ? 128 : 64;
-  static constexpr uint32_t TCOLS = D == 128 ? 256 : 128;
+  static constexpr int OFF_K = OFF_P + P_BYTES;    // K stages [2]
+  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;  // V stages [2]
+  static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256;
+  static constexpr int SCOL = 64;                  // S double buffer: TMEM columns [0,64) and [64,128)
+  static constexpr int OCOL = 128;                 // O: TMEM columns [128, 128 + D)
+  static constexpr uint32_t TCOLS = 256;
+  static constexpr int THREADS = 192;              // warps 0-3 softmax, 4 MMA issue, 5 TMA loads
 };
 
 __device__ __forceinline__ int find_req(const VerifyParams& p, int64_t tile) {
@@ -75,11 +81,39 @@ __device__ __forceinline__ int find_req(const VerifyParams& p, int64_t tile) {
   return b;
 }
 
+// Bounded mbarrier wait that also gives up when another role of the CTA has aborted.
+__device__ __forceinline__ bool vwait(uint64_t* bar, uint32_t parity, int32_t* st, volatile int* abort) {
+  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 31u && *abort) return false;
+  }
+  set_status(st, VC_DEV_TIMEOUT);
+  *abort = 1;
+  return false;
+}
+
+// One piece of the CTA's tile range: tiles [j0, j1) of unit ul of request b.
+struct VPiece {
+  int b, ul, j0, j1;
+};
+
+__device__ __forceinline__ VPiece verify_piece(const VerifyParams& p, int64_t pos, int64_t end) {
+  VPiece q;
+  q.b = find_req(p, pos);
+  const VerifyReqDev& R = p.req[q.b];
+  const int64_t rel = pos - R.tile_begin;
+  q.ul = (int)(rel / R.tiles);
+  q.j0 = (int)(rel % R.tiles);
+  const int64_t left = end - pos;
+  q.j1 = left < (int64_t)(R.tiles - q.j0) ? q.j0 + (int)left : R.tiles;
+  return q;
+}
+
 template <int D>
-__global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_constant__ VerifyParams p) {
+__global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_constant__ VerifyParams p) {
   using C = VCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte aligned tiles
     pdl_launch_dependents();
     pdl_wait();
@@ -88,23 +122,28 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
   }
   uint8_t* sQ = smem;
   uint8_t* sP = smem + C::OFF_P;
-  uint8_t* sST = smem + C::OFF_ST;
-  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // [2] K tile landed
-  uint64_t* vfull = kfull + 2;                                          // [2] V tile landed
-  uint64_t* sbar = kfull + 4;                                           // S = Q K^T done
-  uint64_t* obar = kfull + 5;                                           // O += P V done
-  uint64_t* xbar = kfull + 6;                                           // drain on the error path
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(kfull + 7);
-  volatile int& s_abort = *reinterpret_cast<volatile int*>(reinterpret_cast<uint8_t*>(kfull + 7) + 4);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kfull = bars + 0;   // [2] K tile landed (TMA bytes)
+  uint64_t* vfull = bars + 2;   // [2] V tile landed
+  uint64_t* kempty = bars + 4;  // [2] the S MMA that read a K stage is done
+  uint64_t* vempty = bars + 6;  // [2] the P V MMA that read a V stage is done
+  uint64_t* sfull = bars + 8;   // [2] S tile g in TMEM buffer g & 1
+  uint64_t* pfull = bars + 10;  // P tile in shared memory (4 softmax warps)
+  uint64_t* ofull = bars + 11;  // O += P V done
+  uint64_t* qfull = bars + 12;  // the unit's Q tile in shared memory (4 softmax warps)
+  uint64_t* xbar = bars + 13;   // drain on the error path
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 15);
 
   if (warp == 0) tc05::alloc(tslot, C::TCOLS);
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&kfull[i], 1);  // kfull[0..1], vfull[0..1]
-    mbar_init(sbar, 1);
-    mbar_init(obar, 1);
+    for (int i = 0; i < 10; ++i) mbar_init(&bars[i], 1);
+    mbar_init(pfull, 4);
+    mbar_init(ofull, 1);
+    mbar_init(qfull, 4);
     mbar_init(xbar, 1);
     fence_mbar_init();
-    s_abort = 0;
+    *s_abort = 0;
   }
   tc05::fence_before();
   __syncthreads();
@@ -112,226 +151,252 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
   pdl_launch_dependents();
   pdl_wait();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  const uint32_t t_s = tmem + lane_off;
-  const uint32_t t_o = tmem + lane_off + C::OCOL;
-
-  constexpr uint32_t IDESC_S = tc05::idesc_bf16(VM, VBN, false);
-  constexpr uint32_t IDESC_O = tc05::idesc_bf16(VM, D, true);
-  const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aST = smem_u32(sST);
 
   const int64_t T = p.total_tiles, N = p.n_cta, c = blockIdx.x;
-  int64_t pos = c * T / N;
-  const int64_t end = (c + 1) * T / N;
-  uint32_t g_tile = 0;  // global tile counter (stage = g & 1, phase = (g >> 1) & 1)
-  uint32_t gk_issued = 0, gv_issued = 0;  // K / V tiles whose loads thread 0 has issued (error drain)
-  uint32_t s_cnt = 0, o_cnt = 0;
-  bool failed = false;
+  const int64_t beg = c * T / N, end = (c + 1) * T / N;
 
-#pragma unroll 1
-  while (pos < end && !failed) {
-    const int b = find_req(p, pos);
-    const VerifyReqDev& R = p.req[b];
-    const int64_t rel = pos - R.tile_begin;
-    const int ul = (int)(rel / R.tiles);
-    const int j0 = (int)(rel % R.tiles);
-    const int64_t left = end - pos;
-    const int j1 = left < (int64_t)(R.tiles - j0) ? j0 + (int)left : R.tiles;
-    const int nt = j1 - j0;
-    const int hk = ul / R.mtiles, mt = ul % R.mtiles;
-    const int u_global = R.unit_begin + ul;
-    const CUtensorMap* tm = p.tm[b];
-
-    // this thread's query row
-    const int Rw = mt * VM + tid;
-    const int qi = Rw / p.G, qg = Rw % p.G;
-    const bool row_ok = qi < R.n_rows;
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(R.q + ((size_t)qi * p.Hq + hk * p.G + qg) * D);
+  if (warp == 5) {
+    // ---- TMA producer: K of tile g, then V of tile g - 1 (K runs a tile ahead of V) ----------
+    if (lane == 0) {
+      uint32_t g = 0, gk = 0, gv = 0;  // tiles issued (K, V)
+      int pv_b = 0, pv_hk = 0, pv_j = 0;
+      bool pv_pending = false;
+      auto load = [&](bool isv, uint32_t gi, int b, int hk, int j) -> bool {
+        const int st = gi & 1;
+        if (gi >= 2 && !vwait(isv ? &vempty[st] : &kempty[st], ((gi - 2) >> 1) & 1, p.dev_status, s_abort)) return false;
+        const VerifyReqDev& R = p.req[b];
+        uint64_t* bar = isv ? &vfull[st] : &kfull[st];
+        uint8_t* dst = smem + (isv ? C::OFF_V : C::OFF_K) + st * C::KV_BYTES;
+        const bool isnew = j >= R.n_full;
+        const int tok = isnew ? (j - R.n_full) * VBN : j * VBN;
+        const void* map = &p.tm[b][(isnew ? 2 : 0) + (isv ? 1 : 0)];
+        mbar_arrive_expect_tx(bar, C::KV_BYTES);
 #pragma unroll
-      for (int kb = 0; kb < C::KB; ++kb)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 v = row_ok ? __ldg(src + kb * 8 + ch) : make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(sQ + kb * (VM * 128) + tid * 128 + ((ch ^ (tid & 7)) << 4)) = v;
+        for (int kb = 0; kb < C::KB; ++kb) tc05::tma_load_3d(dst + kb * (VBN * 128), map, kb * 64, tok, hk, bar);
+        return true;
+      };
+      bool ok = true;
+      for (int64_t pos = beg; pos < end && ok;) {
+        const VPiece q = verify_piece(p, pos, end);
+        const int hk = q.ul / p.req[q.b].mtiles;
+        for (int j = q.j0; j < q.j1 && ok; ++j, ++g) {
+          ok = load(false, gk, q.b, hk, j);
+          if (ok) ++gk;
+          if (ok && pv_pending) {
+            ok = load(true, gv, pv_b, pv_hk, pv_j);
+            if (ok) ++gv;
+          }
+          pv_b = q.b, pv_hk = hk, pv_j = j, pv_pending = true;
         }
+        pos += q.j1 - q.j0;
+      }
+      if (ok && pv_pending && load(true, gv, pv_b, pv_hk, pv_j)) ++gv;
+      if (*s_abort) {
+        // drain (bounded): the loads of the last two tiles of each kind may still be landing
+        for (uint32_t gi = (gk > 2 ? gk - 2 : 0); gi < gk; ++gi) mbar_wait_bounded(&kfull[gi & 1], (gi >> 1) & 1, p.dev_status);
+        for (uint32_t gi = (gv > 2 ? gv - 2 : 0); gi < gv; ++gi) mbar_wait_bounded(&vfull[gi & 1], (gi >> 1) & 1, p.dev_status);
+      }
     }
-    fence_proxy_async_smem();
-    tc05::fence_before();
-    __syncthreads();
-
-    // K and V of a tile have their own barriers: a K stage is reloaded as soon as the S MMA that
-    // read it is done (start of the next-but-one iteration's wait), a V stage once its P V is done,
-    // so each load has about two tile periods to land.
-    auto issue_kv = [&](int j, uint32_t g, bool isv) {
-      const int st = g & 1;
-      uint8_t* dst = sST + st * C::STAGE + (isv ? C::KV_BYTES : 0);
-      uint64_t* bar = isv ? &vfull[st] : &kfull[st];
-      mbar_arrive_expect_tx(bar, C::KV_BYTES);
-      (isv ? gv_issued : gk_issued) = g + 1;
-      const bool isnew = j >= R.n_full;
-      const int tok = isnew ? (j - R.n_full) * VBN : j * VBN;
-      const void* map = &tm[(isnew ? 2 : 0) + (isv ? 1 : 0)];
-#pragma unroll
-      for (int kb = 0; kb < C::KB; ++kb) tc05::tma_load_3d(dst + kb * (VBN * 128), map, kb * 64, tok, hk, bar);
-    };
-    auto issue_s = [&](uint32_t g) -> bool {
-      const int st = g & 1;
-      if (!mbar_wait_bounded(&kfull[st], (g >> 1) & 1, p.dev_status)) return false;
-      tc05::fence_after();
-      const uint32_t kaddr = aST + st * C::STAGE;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t da = tc05::sdesc_sw128(aQ + (kk >> 2) * (VM * 128) + (kk & 3) * 32, 16, 1024);
-        const uint64_t db = tc05::sdesc_sw128(kaddr + (kk >> 2) * (VBN * 128) + (kk & 3) * 32, 16, 1024);
-        tc05::mma_bf16(tmem, da, db, IDESC_S, kk > 0);
-      }
-      tc05::commit(sbar);
-      return true;
-    };
-
-    if (tid == 0) {
-      tc05::fence_after();
-      issue_kv(j0, g_tile, false);
-      issue_kv(j0, g_tile, true);
-      if (nt > 1) {
-        issue_kv(j0 + 1, g_tile + 1, false);
-        issue_kv(j0 + 1, g_tile + 1, true);
-      }
-      if (!issue_s(g_tile)) s_abort = 1;
-    }
-
-    float m_run = -INFINITY, l_run = 0.f;
-#pragma unroll 1
-    for (int jj = 0; jj < nt; ++jj) {
-      const int j = j0 + jj;
-      const uint32_t g = g_tile + jj;
-      bool ok = mbar_wait_bounded(sbar, s_cnt & 1, p.dev_status);
-      s_cnt++;
-      tc05::fence_after();
-      if (tid == 0 && ok && jj + 2 < nt) issue_kv(j + 2, g + 2, false);  // S_g has read K stage g & 1
-      float x[VBN];
-      {
-        uint32_t r0[32], r1[32];
-        tc05::ld32(t_s, r0);
-        tc05::ld32(t_s + 32, r1);
-        tc05::wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          x[e] = __uint_as_float(r0[e]);
-          x[32 + e] = __uint_as_float(r1[e]);
-        }
-      }
-      // mask invisible keys (only a ragged last KV_full tile or a drafted-rows tile has any), then
-      // the row max by a tree; the scale is folded into the exponent below
-      {
-        const int last = j < R.n_full ? R.ctx - j * VBN - 1 : qi - (j - R.n_full) * VBN;  // last visible key
-        if (last < VBN - 1) {
-#pragma unroll
-          for (int e = 0; e < VBN; ++e)
-            if (e > last) x[e] = -INFINITY;
-        }
-      }
-      float mx;
-      {
-        float t[VBN / 2];
-#pragma unroll
-        for (int e = 0; e < VBN / 2; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
-#pragma unroll
-        for (int w = VBN / 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
-        mx = t[0] * p.scale_log2;  // the scale is positive: it keeps the order
-      }
-      if (jj > 0) {
-        ok = mbar_wait_bounded(obar, o_cnt & 1, p.dev_status) && ok;  // P V of the previous tile done
-        o_cnt++;
+  } else if (warp == 4) {
+    // ---- MMA issue: S of tile g (into TMEM buffer g & 1) before P V of tile g - 1 -------------
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = tc05::idesc_bf16(VM, VBN, false);
+      constexpr uint32_t IDESC_O = tc05::idesc_bf16(VM, D, true);
+      const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aK = smem_u32(smem + C::OFF_K),
+                     aV = smem_u32(smem + C::OFF_V);
+      uint32_t g = 0, u = 0;
+      bool ok = true;
+      auto issue_pv = [&](uint32_t gp, bool acc) -> bool {
+        if (!vwait(pfull, gp & 1, p.dev_status, s_abort)) return false;
+        if (!vwait(&vfull[gp & 1], (gp >> 1) & 1, p.dev_status, s_abort)) return false;
         tc05::fence_after();
-        if (tid == 0 && ok && jj + 1 < nt) issue_kv(j + 1, g + 1, true);  // it has read V stage (g - 1) & 1
+        const uint32_t vaddr = aV + (gp & 1) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < VBN / 16; ++kk) {
+          const uint64_t da = tc05::sdesc_sw128(aP + kk * 32, 16, 1024);
+          const uint64_t db = tc05::sdesc_sw128(vaddr + kk * 2048, VBN * 128, 1024);
+          tc05::mma_bf16(tmem + C::OCOL, da, db, IDESC_O, (acc || kk > 0) ? 1u : 0u);
+        }
+        tc05::commit(ofull);
+        tc05::commit(&vempty[gp & 1]);
+        return true;
+      };
+      for (int64_t pos = beg; pos < end && ok;) {
+        const VPiece q = verify_piece(p, pos, end);
+        const int nt = q.j1 - q.j0;
+        ok = vwait(qfull, u & 1, p.dev_status, s_abort);
+        ++u;
+        for (int jj = 0; jj < nt && ok; ++jj) {
+          const uint32_t gc = g + jj;
+          if (!vwait(&kfull[gc & 1], (gc >> 1) & 1, p.dev_status, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          const uint32_t kaddr = aK + (gc & 1) * C::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t da = tc05::sdesc_sw128(aQ + (kk >> 2) * (VM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = tc05::sdesc_sw128(kaddr + (kk >> 2) * (VBN * 128) + (kk & 3) * 32, 16, 1024);
+            tc05::mma_bf16(tmem + (gc & 1) * C::SCOL, da, db, IDESC_S, kk > 0);
+          }
+          tc05::commit(&sfull[gc & 1]);
+          tc05::commit(&kempty[gc & 1]);
+          if (jj > 0) ok = issue_pv(gc - 1, jj > 1);
+        }
+        if (ok) ok = issue_pv(g + nt - 1, nt > 1);
+        g += nt;
+        pos += nt;
       }
-      const float m_new = fmaxf(m_run, mx);
-      if (jj == 0) {
-        m_run = m_new;
-      } else {
+      // every MMA issued so far has completed before TMEM is released (bounded, even after an abort)
+      tc05::commit(xbar);
+      mbar_wait_bounded(xbar, 0, p.dev_status);
+    }
+  } else {
+    // ---- softmax warps: thread tid owns TMEM lane tid = query row tid of the tile ---------------
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int64_t pos = beg; pos < end && ok;) {
+      const VPiece q = verify_piece(p, pos, end);
+      const VerifyReqDev& R = p.req[q.b];
+      const int nt = q.j1 - q.j0;
+      const int hk = q.ul / R.mtiles, mt = q.ul % R.mtiles;
+      const int u_global = R.unit_begin + q.ul;
+      const int Rw = mt * VM + tid;
+      const int qi = Rw / p.G, qg = Rw % p.G;
+      const bool row_ok = qi < R.n_rows;
+      // this thread's query row into the swizzled Q tile; the previous unit's MMAs are complete
+      // (its epilogue waited for the last P V, which follows every S of the unit)
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(R.q + ((size_t)qi * p.Hq + hk * p.G + qg) * D);
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 v = row_ok ? __ldg(src + kb * 8 + ch) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sQ + kb * (VM * 128) + tid * 128 + ((ch ^ (tid & 7)) << 4)) = v;
+          }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qfull);
+
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int jj = 0; jj < nt; ++jj) {
+        const int j = q.j0 + jj;
+        const uint32_t gc = g + jj;
+        if (!vwait(&sfull[gc & 1], (gc >> 1) & 1, p.dev_status, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc05::fence_after();
+        float x[VBN];
+        {
+          uint32_t r0[32], r1[32];
+          const uint32_t t_s = tmem + lane_off + (gc & 1) * C::SCOL;
+          tc05::ld32(t_s, r0);
+          tc05::ld32(t_s + 32, r1);
+          tc05::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            x[e] = __uint_as_float(r0[e]);
+            x[32 + e] = __uint_as_float(r1[e]);
+          }
+        }
+        // mask invisible keys (only a ragged last KV_full tile or a drafted-rows tile has any),
+        // then the row max by a tree; the scale is folded into the exponent below
+        {
+          const int last = j < R.n_full ? R.ctx - j * VBN - 1 : qi - (j - R.n_full) * VBN;  // last visible key
+          if (last < VBN - 1) {
+#pragma unroll
+            for (int e = 0; e < VBN; ++e)
+              if (e > last) x[e] = -INFINITY;
+          }
+        }
+        float mx;
+        {
+          float t[VBN / 2];
+#pragma unroll
+          for (int e = 0; e < VBN / 2; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
+#pragma unroll
+          for (int w = VBN / 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+          mx = t[0] * p.scale_log2;  // the scale is positive: it keeps the order
+        }
+        const float m_new = fmaxf(m_run, mx);
         // rescale O only when the running max grew by more than 2^8; TMEM loads/stores are
         // warp-collective, so the warp rescales together (factor 1 for rows that need none)
-        const bool need = m_new > m_run + 8.f;
-        float f = 1.f;
-        if (need) {
-          f = ex2_approx(m_run - m_new);
-          l_run *= f;
-          m_run = m_new;
-        }
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-          for (int cb = 0; cb < D / 32; ++cb) {
-            uint32_t r[32];
-            tc05::ld32(t_o + cb * 32, r);
-            tc05::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-            tc05::st32(t_o + cb * 32, r);
+        const bool need = jj > 0 && m_new > m_run + 8.f;
+        if (jj > 0) {
+          // P V of the previous tile: O is stable and the P buffer is free after it
+          if (!vwait(ofull, (gc - 1) & 1, p.dev_status, s_abort)) {
+            ok = false;
+            break;
           }
-          tc05::wait_st();
+          tc05::fence_after();
         }
-      }
-      const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        if (jj == 0) {
+          m_run = m_new;
+        } else {
+          float f = 1.f;
+          if (need) {
+            f = ex2_approx(m_run - m_new);
+            l_run *= f;
+            m_run = m_new;
+          }
+          if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+            for (int cb = 0; cb < D / 32; ++cb) {
+              uint32_t r[32];
+              const uint32_t t_o = tmem + lane_off + C::OCOL + cb * 32;
+              tc05::ld32(t_o, r);
+              tc05::wait_ld();
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2_approx(fmaf(x[ch * 8 + 2 * e], p.scale_log2, -mu));
-          const float p1 = ex2_approx(fmaf(x[ch * 8 + 2 * e + 1], p.scale_log2, -mu));
-          ls[e] += p0 + p1;
-          w[e] = pack_bf16x2(p0, p1);
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+              tc05::st32(t_o, r);
+            }
+            tc05::wait_st();
+          }
         }
-        *reinterpret_cast<uint4*>(sP + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = ex2_approx(fmaf(x[ch * 8 + 2 * e], p.scale_log2, -mu));
+            const float p1 = ex2_approx(fmaf(x[ch * 8 + 2 * e + 1], p.scale_log2, -mu));
+            ls[e] += p0 + p1;
+            w[e] = pack_bf16x2(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(sP + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        fence_proxy_async_smem();
+        tc05::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull);
       }
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      if (!ok) s_abort = 1;
-      fence_proxy_async_smem();
-      tc05::fence_before();
-      __syncthreads();
-      if (s_abort) {
-        failed = true;
+      if (!ok) break;
+      // output: wait for the unit's last P V
+      if (!vwait(ofull, (g + nt - 1) & 1, p.dev_status, s_abort)) {
+        ok = false;
         break;
       }
-      if (tid == 0) {
-        tc05::fence_after();
-        if (!mbar_wait_bounded(&vfull[g & 1], (g >> 1) & 1, p.dev_status)) {
-          s_abort = 1;
-        } else {
-          const uint32_t vaddr = aST + (g & 1) * C::STAGE + C::KV_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < VBN / 16; ++kk) {
-            const uint64_t da = tc05::sdesc_sw128(aP + kk * 32, 16, 1024);
-            const uint64_t db = tc05::sdesc_sw128(vaddr + kk * 2048, VBN * 128, 1024);
-            tc05::mma_bf16(tmem + C::OCOL, da, db, IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        tc05::commit(obar);
-        if (jj + 1 < nt && !issue_s(g + 1)) s_abort = 1;
-      }
-    }
-    if (failed) break;
-    g_tile += nt;
-    // output: wait for the last P V
-    bool ok = mbar_wait_bounded(obar, o_cnt & 1, p.dev_status);
-    o_cnt++;
-    tc05::fence_after();
-    const bool whole = (j0 == 0 && j1 == R.tiles);
-    const bool store = ok && row_ok;
-    {
+      tc05::fence_after();
+      g += nt;
+      const bool whole = (q.j0 == 0 && q.j1 == R.tiles);
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const size_t slot = (size_t)(c + u_global);
 #pragma unroll 1
       for (int cb = 0; cb < D / 32; ++cb) {
         uint32_t r[32];
-        tc05::ld32(t_o + cb * 32, r);  // warp-collective: every lane loads, valid rows store
+        tc05::ld32(tmem + lane_off + C::OCOL + cb * 32, r);  // warp-collective: every lane loads
         tc05::wait_ld();
-        if (!store) continue;
+        if (!row_ok) continue;
         if (whole) {
           uint4* dst = reinterpret_cast<uint4*>(R.o + ((size_t)qi * p.Hq + hk * p.G + qg) * D + cb * 32);
 #pragma unroll
@@ -350,24 +415,12 @@ __global__ void __launch_bounds__(128, 2) verify_attn_kernel(const __grid_consta
                                  __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
         }
       }
-      if (store && !whole) p.ws_lse[slot * VM + tid] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+      if (row_ok && !whole) p.ws_lse[slot * VM + tid] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+      tc05::fence_before();
+      pos += nt;
     }
-    if (!ok) s_abort = 1;
-    tc05::fence_before();
-    __syncthreads();
-    if (s_abort) failed = true;
-    pos += nt;
   }
 
-  if (failed && tid == 0) {
-    // drain: every MMA issued so far, then (bounded) any TMA still landing
-    tc05::commit(xbar);
-    mbar_wait_bounded(xbar, 0, p.dev_status);
-    for (uint32_t g = (gk_issued > 2 ? gk_issued - 2 : 0); g < gk_issued; ++g)
-      mbar_wait_bounded(&kfull[g & 1], (g >> 1) & 1, p.dev_status);
-    for (uint32_t g = (gv_issued > 2 ? gv_issued - 2 : 0); g < gv_issued; ++g)
-      mbar_wait_bounded(&vfull[g & 1], (g >> 1) & 1, p.dev_status);
-  }
   tc05::fence_before();
   __syncthreads();
   tc05::fence_after();
@@ -486,7 +539,7 @@ static cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  cudaError_t e = launch_pdl(verify_attn_kernel<D>, dim3(p.n_cta), dim3(128), C::SMEM, s, p);
+  cudaError_t e = launch_pdl(verify_attn_kernel<D>, dim3(p.n_cta), dim3(C::THREADS), C::SMEM, s, p);
   if (e != cudaSuccess) return e;
   return launch_pdl(verify_combine_kernel<D>, dim3(p.n_units, VM / 8), dim3(256), 0, s, p);
 }
