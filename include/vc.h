@@ -180,8 +180,8 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
  * Same arguments and results as vc_draft_attn, minus ws/ws_bytes. The partials live in a fixed
  * array of VC_DRAFT_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU that loads the
  * library holds it until the process exits. The first call made with a given device current looks
- * up the array's device address (cudaGetSymbolAddress) and caches it: make that first call before
- * any stream capture. The call allocates nothing. Returns VC_ERR_WORKSPACE when the call needs more
+ * up the array's device address (cudaGetSymbolAddress), zero-fills the array on `stream` and
+ * caches the address: make that first call before any stream capture. The call allocates nothing. Returns VC_ERR_WORKSPACE when the call needs more
  * scratch than the array holds (vc_workspace_size(VC_CALL_DRAFT, shape, 0) > the limit). All calls
  * share the array, which keeps the last call's contents (nothing in it needs clearing); calls that
  * overlap on the GPU race on it, so issue them on one stream or order them with events. */
@@ -240,9 +240,10 @@ vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, si
 /* ------------------------------------------------------------------------------------------ */
 /* Workspace bytes vc_draft_attn (call = VC_CALL_DRAFT) or vc_verify_attn (VC_CALL_VERIFY) needs
  * for `shape`; max_rows = the largest n_rows of a verify call (ignored for draft). The workspace
- * holds per-split partial outputs (and, for draft, per-request arrival counters tagged with the
- * call, so a stale count left by an earlier call is ignored); it needs no initialisation and is
- * not read after the call. Calls that overlap on the GPU must not share a workspace. */
+ * holds per-split partial outputs. The draft workspace also starts with per-(KV head, request)
+ * arrival counters: zero-fill a draft workspace once before its first call; every call returns the
+ * counters to zero. The verify workspace needs no initialisation. Calls that overlap on the GPU
+ * must not share a workspace. */
 size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows);
 
 const char* vc_status_string(vc_status s);

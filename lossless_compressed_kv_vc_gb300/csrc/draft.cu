@@ -444,23 +444,64 @@ __device__ __forceinline__ void merge_head(const float* po, const float* pl, int
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // Count this CTA's partial of request b (KV head hk) as arrived; true for the CTA that arrives last
-// of the n CTAs holding the request, which then merges. The counter word holds
-// (call tag << 12) | arrivals; a word left with another call's tag (an earlier call, even one that
-// stopped early) counts as zero arrivals, so the workspace needs no initialisation. One thread.
+// of the n CTAs holding the request, which then merges. atomicInc wraps the word back to zero on
+// the last arrival, so a counter is zero between calls: the workspace starts zeroed and every CTA
+// arrives exactly once per split request, also when a wait of its own gave up. One thread.
 __device__ __forceinline__ bool cta_arrive(const DraftParams& p, int hk, int b, int n) {
-  uint32_t* ctr = p.ws_ctr + (size_t)hk * VC_MAX_BATCH + b;
-  uint32_t old = *reinterpret_cast<volatile uint32_t*>(ctr), assumed = 0, nv = 0;
-  uint32_t it = 0;
-  do {
-    assumed = old;
-    nv = (assumed >> 12) == p.tag ? assumed + 1 : ((p.tag << 12) | 1u);
-    old = atomicCAS(ctr, assumed, nv);
-  } while (old != assumed && ++it < kSpinLimit);
-  if (old != assumed) {
-    set_status(p.dev_status, VC_DEV_TIMEOUT);
-    return false;
+  const uint32_t old = atomicInc(p.ws_ctr + (size_t)hk * VC_MAX_BATCH + b, (uint32_t)(n - 1));
+  return old == (uint32_t)(n - 1);
+}
+
+// Merge the partials of one CTA for query head h, each given by its o row base (head 0) and lse
+// base, in warp order (a null slot holds none); they live in this CTA's shared memory or were
+// written by this CTA's warps to the workspace, so plain loads see them after the CTA barrier.
+// Output as in merge_head.
+template <int D, int NW>
+__device__ __forceinline__ void merge_local(const float* const (&po)[NW], const float* const (&pl)[NW], int G,
+                                            int h, int lane, bf16* out, float* out_o, float* out_lse) {
+  constexpr int CPL = D / 32;
+  float lse[NW], v[NW][CPL];
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NW; ++k) {
+    lse[k] = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) v[k][c] = 0.f;
+    if (po[k]) {
+      lse[k] = pl[k][h];
+      const float* row = po[k] + (size_t)h * D + CPL * lane;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) v[k][c] = row[c];
+      M = fmaxf(M, lse[k]);
+    }
   }
-  return (nv & 0xFFFu) == (uint32_t)n;
+  if (M == -INFINITY) M = 0.f;
+  float L = 0.f, acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+#pragma unroll
+  for (int k = 0; k < NW; ++k) {
+    const float w = exp2f(lse[k] - M);
+    L += w;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] += w * v[k][c];
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  if (out) {
+    bf16* dst = out + CPL * lane;
+    if constexpr (CPL == 4) {
+      uint2 o2;
+      o2.x = pack_bf16x2(acc[0] * inv, acc[1 % CPL] * inv);
+      o2.y = pack_bf16x2(acc[2 % CPL] * inv, acc[3 % CPL] * inv);
+      *reinterpret_cast<uint2*>(dst) = o2;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1 % CPL] * inv);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) out_o[CPL * lane + c] = acc[c] * inv;
+    if (lane == 0) *out_lse = L > 0.f ? M + log2f(L) : -INFINITY;
+  }
 }
 
 // More than 8 query heads per KV head (NHB = 2) doubles the accumulators: two CTAs per SM.
@@ -484,6 +525,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   // are waited for as well. Every stage also commits one cp.async group (possibly empty), so
   // "all but NST-1 groups done" always means "this stage's copies done".
   uint8_t* wb = smem + warp * C::PER_WARP;
+  const uint64_t stream_pol = l2_evict_first_policy();  // KV_comp is read once per step
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF) + warp * C::NST;
   if (lane == 0) {
     for (int s = 0; s < C::NST; ++s) mbar_init(&bars[s], 1);
@@ -541,12 +583,13 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         const int Tq = 32 * r.ng;
         if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::QRAW);
         __syncwarp();
-        if (lane == 0) bulk_g2s(sb + C::OFF_KC, r.kc + ((size_t)hk * r.ng + g) * C::KCB, C::KCB, &bars[st]);
-        if (lane == 1) bulk_g2s(sb + C::OFF_KS, r.ks + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st]);
-        if (lane == 2) bulk_g2s(sb + C::OFF_KZ, r.kz + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st]);
-        if (lane == 3) bulk_g2s(sb + C::OFF_VC, r.vc + ((size_t)hk * Tq + 32 * g) * (D * C::BITS / 8), C::KCB, &bars[st]);
-        if (lane == 4) bulk_g2s(sb + C::OFF_VS, r.vs + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st]);
-        if (lane == 5) bulk_g2s(sb + C::OFF_VZ, r.vz + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st]);
+        if (lane == 0) bulk_g2s_hint(sb + C::OFF_KC, r.kc + ((size_t)hk * r.ng + g) * C::KCB, C::KCB, &bars[st], stream_pol);
+        if (lane == 1) bulk_g2s_hint(sb + C::OFF_KS, r.ks + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st], stream_pol);
+        if (lane == 2) bulk_g2s_hint(sb + C::OFF_KZ, r.kz + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st], stream_pol);
+        if (lane == 3)
+          bulk_g2s_hint(sb + C::OFF_VC, r.vc + ((size_t)hk * Tq + 32 * g) * (D * C::BITS / 8), C::KCB, &bars[st], stream_pol);
+        if (lane == 4) bulk_g2s_hint(sb + C::OFF_VS, r.vs + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st], stream_pol);
+        if (lane == 5) bulk_g2s_hint(sb + C::OFF_VZ, r.vz + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st], stream_pol);
       } else {
         // 16 kept rows by TMA gather4: lane l < G4_OPS loads rows 4(l%4)..4(l%4)+3 of one 64-channel
         // block of K or V. A row past the kept count repeats the chunk's first row, a kept row
@@ -570,7 +613,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         if (lane < C::G4_OPS) {
           const int h = (lane >> 2) % C::HALVES, isv = (lane >> 2) / C::HALVES;
           tma_gather4(sb + isv * C::TILE + h * C::BLK + g4 * 512, &maps.kv[b][isv], 64 * h, c0, c1, c2, c3,
-                      &bars[st]);
+                      &bars[st], stream_pol);
         }
       }
       cp_async_commit();
@@ -635,9 +678,10 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       }
     }
   };
-  // end of request b inside this warp: final bf16 output, or an (o, lse) partial in slot wg + b.
-  // The lane holds O^T[channel 16mt + lane/4 (+8)][head 8hb + 2(lane%4) + e].
-  auto finish = [&](int b) {
+  // end of request b inside this warp: final bf16 output, or an (o, lse) partial — in slot wg + b
+  // of the workspace, or (the warp's last request, to_smem) in the warp's drained stage ring as
+  // [G][D] o then [G] lse. The lane holds O^T[channel 16mt + lane/4 (+8)][head 8hb + 2(lane%4) + e].
+  auto finish = [&](int b, bool to_smem) {
     ensure_wait();
     int64_t w0, w1;
     warp_span(p, b, w0, w1);
@@ -664,12 +708,15 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
             dst[c] = __float2bfloat16_rn(v0);
             dst[c + 8] = __float2bfloat16_rn(v1);
           } else {
-            float* dst = p.ws_o + (slot * G + h) * D;
+            float* dst = to_smem ? reinterpret_cast<float*>(wb) + h * D : p.ws_o + (slot * G + h) * D;
             dst[c] = v0;
             dst[c + 8] = v1;
           }
         }
-        if (!whole && (lane >> 2) == 0) p.ws_lse[slot * G + h] = lt > 0.f ? m[hb][e] + log2f(lt) : -INFINITY;
+        if (!whole && (lane >> 2) == 0) {
+          float* dst = to_smem ? reinterpret_cast<float*>(wb) + G * D + h : p.ws_lse + slot * G + h;
+          *dst = lt > 0.f ? m[hb][e] + log2f(lt) : -INFINITY;
+        }
       }
   };
 
@@ -688,7 +735,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         fold_zs<D, NHB>(o, zs);
         zs_live = false;
       }
-      if (cur_b >= 0) finish(cur_b);
+      if (cur_b >= 0) finish(cur_b, false);
       reset();
       load_q(b);
       cur_b = b;
@@ -736,7 +783,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   cp_async_wait<0>();
   if (!aborted && cur_b >= 0) {
     if (!BF16_ROWS && zs_live) fold_zs<D, NHB>(o, zs);
-    finish(cur_b);
+    finish(cur_b, true);  // the stage ring is drained: the warp's last partial stays in shared memory
   }
 
   // Merge phase, for requests split across warps. First each CTA merges its own warps' partials of
@@ -764,9 +811,33 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       const bool one_cta = c0 == c1;
       const int64_t cslot = (int64_t)hk * (NC + p.B) + cx + b;
       bf16* orow = p.req[b].o + (size_t)hk * G * D;
+      // where each of this CTA's partials of b is: in the warp's stage ring when b is the warp's
+      // last request, else in the workspace (written when the warp moved on to its next request)
+      // (a warp whose range is empty — fewer chunks than warps in a one-CTA launch — holds none)
+      // Slot k is warp cw0 + k, empty (null) past cw1 or for a warp whose range is empty; the
+      // indices are compile-time so the pointers stay in registers.
+      const float* po[C::NW];
+      const float* pl[C::NW];
+#pragma unroll
+      for (int k = 0; k < C::NW; ++k) {
+        po[k] = pl[k] = nullptr;
+        const int64_t w = cw0 + k;
+        const int64_t e0 = w * T / W, e1 = (w + 1) * T / W;
+        if (w <= cw1 && e1 > e0) {
+          const int lw = (int)(w - (int64_t)cx * C::NW);
+          int cur2 = 0;
+          if (draft_find_req(p, e1 - 1, cur2) == b) {
+            po[k] = reinterpret_cast<const float*>(smem + lw * C::PER_WARP);
+            pl[k] = po[k] + G * D;
+          } else {
+            po[k] = p.ws_o + ((int64_t)hk * (W + p.B) + w + b) * G * D;
+            pl[k] = p.ws_lse + ((int64_t)hk * (W + p.B) + w + b) * G;
+          }
+        }
+      }
       for (int h = warp; h < G; h += C::NW)
-        merge_head<D>(p.ws_o, p.ws_lse, (int64_t)hk * (W + p.B) + b + cw0, (int)(cw1 - cw0 + 1), G, h, lane,
-                      one_cta ? orow + (size_t)h * D : nullptr, p.ws_co + (cslot * G + h) * D, p.ws_clse + cslot * G + h);
+        merge_local<D, C::NW>(po, pl, G, h, lane, one_cta ? orow + (size_t)h * D : nullptr,
+                              p.ws_co + (cslot * G + h) * D, p.ws_clse + cslot * G + h);
       if (one_cta) continue;
       // The barrier orders every thread's CTA-partial stores before thread 0's release fence and
       // arrival; the last arriver's acquire fence and the second barrier order the other CTAs'

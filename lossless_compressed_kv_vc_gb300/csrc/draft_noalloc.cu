@@ -9,9 +9,11 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the library holds it until
 // the process exits. In host code its name is only a host-side stand-in, so its device address is
 // looked up once per device with cudaGetSymbolAddress (on the first call made with that device
-// current) and cached. All calls share the array and it keeps the last call's contents; the draft
-// kernels write every partial before reading it, so nothing needs clearing between calls. Calls
-// that overlap on the GPU (different streams, or graph replays running concurrently) race on it.
+// current) and cached; that first call also zero-fills the array on the caller's stream (the
+// draft kernel's arrival counters start at zero and every call returns them to zero). All calls
+// share the array and it keeps the last call's contents; the draft kernels write every partial
+// before reading it. Calls that overlap on the GPU (different streams, or graph replays running
+// concurrently) race on it.
 #include "vc_internal.cuh"
 
 #include <mutex>
@@ -40,7 +42,8 @@ extern "C" vc_status vc_draft_attn_noalloc(const vc_shape* shape, const vc_draft
     std::lock_guard<std::mutex> lock(g_mu);
     ptr = g_scratch_ptr[dev];
     if (!ptr) {
-      if (cudaGetSymbolAddress(&ptr, g_draft_scratch) != cudaSuccess || !ptr) {
+      if (cudaGetSymbolAddress(&ptr, g_draft_scratch) != cudaSuccess || !ptr ||
+          cudaMemsetAsync(ptr, 0, kScratchBytes, stream) != cudaSuccess) {
         cudaGetLastError();
         return VC_ERR_CUDA;
       }

@@ -6,7 +6,6 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -53,10 +52,6 @@ static int draft_ctas_per_head_max(int Hkv, int G = 1) {
 
 // Arrival counters at the start of the draft workspace: one 32-bit word per (KV head, request slot).
 static size_t draft_counter_bytes(int Hkv) { return ((size_t)Hkv * VC_MAX_BATCH * 4 + 255) / 256 * 256; }
-
-// Per-call tag of the draft arrival counters (20 bits; a counter word still holding another
-// call's tag is taken as zero, so the workspace needs no initialisation).
-static std::atomic<uint32_t> g_draft_tag{0};
 
 // Last library operation launched on each stream. A draft step may start streaming before the
 // kernel ahead of it in the stream finishes unless that kernel is a compress (the only writer of
@@ -311,7 +306,6 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   const size_t cslots = (size_t)Hkv * (per_head + B);
   p.ws_co = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(p.ws_lse + slots * G) + 255) & ~uintptr_t(255));
   p.ws_clse = p.ws_co + cslots * G * d;
-  p.tag = (g_draft_tag.fetch_add(1, std::memory_order_relaxed) + 1) & 0xFFFFFu;
   p.early = last_op(stream) != kOpCompress;
   if (launch_draft(p, &maps, d, kind, per_head, stream) != cudaSuccess) return VC_ERR_CUDA;
   set_last_op(stream, kOpDraft);

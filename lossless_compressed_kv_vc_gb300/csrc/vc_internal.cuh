@@ -81,15 +81,34 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       : "memory");
 }
 
+// L2 policy for data a kernel reads once while streaming far more than the L2 holds: evict it
+// first, so that small data written and read back within the launch (split partials) stays.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // Four whole rows of a 2-D tensor map (box 64 elements x 1 row) gathered by row coordinate into
 // four consecutive 128-byte rows of shared memory starting at dst, in the map's swizzle; c0 is the
 // first element of the 64-element column block (a multiple of 64 here, so the 16-byte rule holds).
+// `pol` is an L2 cache policy (l2_evict_first_policy).
 __device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int c0, int r0, int r1, int r2, int r3,
-                                            uint64_t* bar) {
+                                            uint64_t* bar, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared with an L2 cache policy, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 
@@ -199,8 +218,7 @@ struct DraftParams {
   float* ws_lse;         // [Hkv][n_vwarps + B][G]  (log2 domain)
   float* ws_co;          // [Hkv][CTAs per head + B][G][d] per-CTA partials (slot = CTA + request)
   float* ws_clse;        // [Hkv][CTAs per head + B][G]
-  uint32_t* ws_ctr;      // [Hkv][VC_MAX_BATCH] CTA-partial arrivals: call tag << 12 | count
-  uint32_t tag;          // this call's tag (20 bits)
+  uint32_t* ws_ctr;      // [Hkv][VC_MAX_BATCH] CTA-partial arrival counts (zero between calls)
   int64_t n_vwarps;      // warps per KV head (grid.x * 4)
   int64_t total_chunks;  // chunks per KV head over all requests
   int32_t* dev_status;

@@ -75,7 +75,8 @@ class Batch:
         self.comp = (vc_kv_comp * len(reqs))()
         for b, r in enumerate(reqs):
             self._fill(b, r)
-        self.ws_draft = torch.empty(vc_workspace_size(VC_CALL_DRAFT, self.shape) // 4 + 64, dtype=torch.float32,
+        # zero-filled once: the draft call's arrival counters start at zero and return to zero
+        self.ws_draft = torch.zeros(vc_workspace_size(VC_CALL_DRAFT, self.shape) // 4 + 64, dtype=torch.float32,
                                     device=device)
         vb = vc_workspace_size(VC_CALL_VERIFY, self.shape, self.L_max)
         self.ws_verify = torch.empty(max(vb // 4 + 64, 64), dtype=torch.float32, device=device)

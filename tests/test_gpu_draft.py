@@ -88,6 +88,16 @@ def test_draft_quant_d64_ragged(bits):
     _check_all_steps(w, [0, 1, 2])
 
 
+@pytest.mark.parametrize("keep,ctx,L", [(10, 64, 3), (17, 40, 17), (1, 8, 2)])
+def test_draft_fewer_chunks_than_warps(keep, ctx, L):
+    """One request whose step has only 2-3 chunks per head (16-row kept chunks, then window
+    chunks): a one-CTA launch where some warps hold no chunk; the split partials of the request
+    must be merged from the warps that hold it only."""
+    w = configs.scaled(configs.tiny(), batch=1, L=L)
+    w.ctx, w.keep, w.recent = [ctx], [keep], [0]
+    _check_all_steps(w, [0])
+
+
 def test_draft_keep_all_equals_full_attention_on_gpu():
     """keep = ctx: the draft output equals attention over the whole cache (NS invariant)."""
     w = configs.scaled(configs.tiny(), batch=2, L=3)
