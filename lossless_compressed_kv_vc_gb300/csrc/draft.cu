@@ -351,20 +351,23 @@ __device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zs)[
       }
 }
 
+// The request lookups below read cb = each request's first chunk, cb[B] = total chunks, copied
+// into shared memory at kernel start: the kernel parameters are too large for the constant cache,
+// and a lookup chain that misses it costs a memory round trip per step.
+
 // Advance a request cursor to the request holding chunk `pos` (positions only grow along a warp's
 // range, so each call site keeps its own cursor).
-__device__ __forceinline__ int draft_find_req(const DraftParams& p, int64_t pos, int& cursor) {
-  while (cursor + 1 < p.B && p.req[cursor + 1].chunk_begin <= pos) ++cursor;
+__device__ __forceinline__ int draft_find_req(const int32_t* cb, int B, int64_t pos, int& cursor) {
+  while (cursor + 1 < B && cb[cursor + 1] <= pos) ++cursor;
   return cursor;
 }
 
-// First and last virtual warp whose range holds a chunk of request b (ranges: [w*T/W, (w+1)*T/W)).
-__device__ __forceinline__ void warp_span(const DraftParams& p, int b, int64_t& w0, int64_t& w1) {
-  const int64_t T = p.total_chunks, W = p.n_vwarps;
-  const int64_t c0 = p.req[b].chunk_begin, c1 = c0 + p.req[b].n_chunks;  // [c0, c1)
-  w0 = ((c0 + 1) * W - 1) / T;
-  w1 = (c1 * W - 1) / T;
-}
+// Warp ranges cut T chunks into W parts: warp w holds [w*T/W, (w+1)*T/W). The host guarantees
+// T * (W + 1) < 2^32, so these products and quotients are 32-bit (a 64-bit division is a long
+// software routine).
+__device__ __forceinline__ uint32_t range_edge(uint32_t w, uint32_t T, uint32_t W) { return w * T / W; }
+
+
 
 // Merge n partials of one query head h (consecutive slots s0 .. s0 + n - 1 of po / pl, in slot
 // order): o = sum_k 2^(lse_k - M) o_k / sum_k 2^(lse_k - M), lse = M + log2(sum_k 2^(lse_k - M)),
@@ -515,9 +518,9 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hk = blockIdx.y;
   const int G = p.G;
-  const int64_t T = p.total_chunks, W = p.n_vwarps;
+  const uint32_t T = (uint32_t)p.total_chunks, W = (uint32_t)p.n_vwarps;
   const int64_t wg = (int64_t)blockIdx.x * C::NW + warp;
-  const int64_t p0 = wg * T / W, p1 = (wg + 1) * T / W;
+  const int64_t p0 = range_edge((uint32_t)wg, T, W), p1 = range_edge((uint32_t)wg + 1, T, W);
   const int n = (int)(p1 - p0);  // may be 0: the warp still takes part in the CTA's merge phase
 
   // Each stage completes on its mbarrier: TMA loads (kept rows, quantised groups) by their bytes,
@@ -531,7 +534,18 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     for (int s = 0; s < C::NST; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  __shared__ int32_t s_cb[VC_MAX_BATCH + 1];  // first chunk of each request; s_cb[B] = total chunks
+  __shared__ int32_t s_w0[VC_MAX_BATCH], s_w1[VC_MAX_BATCH];  // first / last warp holding each request
+  __shared__ bf16* s_o[VC_MAX_BATCH];         // output rows of each request
+  __shared__ int32_t s_first[C::NW], s_final[C::NW];  // each warp's first and last request (-1: none)
+  if (threadIdx.x < p.B) {
+    s_cb[threadIdx.x] = p.req[threadIdx.x].chunk_begin;
+    s_w0[threadIdx.x] = p.req[threadIdx.x].w0;
+    s_w1[threadIdx.x] = p.req[threadIdx.x].w1;
+    s_o[threadIdx.x] = p.req[threadIdx.x].o;
+  }
+  if (threadIdx.x == 0) s_cb[p.B] = (int32_t)p.total_chunks;
+  __syncthreads();
   pdl_launch_dependents();
   // Ordering against the previous kernel in the stream (programmatic dependent launch): queries,
   // kept rows and indices are never written by a draft step, verify or accept, so with p.early the
@@ -549,10 +563,15 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
 
   // chunk i of this warp -> (request, chunk within request)
   int cur_row = 0, cur_issue = 0, cur_proc = 0;
+  if (lane == 0) {
+    int c = 0;
+    s_first[warp] = n > 0 ? draft_find_req(s_cb, p.B, p0, c) : -1;
+    s_final[warp] = n > 0 ? draft_find_req(s_cb, p.B, p1 - 1, c) : -1;
+  }
   auto locate = [&](int i, int& b, int& lc, int& cursor) {
     const int64_t pos = p0 + i;
-    b = draft_find_req(p, pos, cursor);
-    lc = (int)(pos - p.req[b].chunk_begin);
+    b = draft_find_req(s_cb, p.B, pos, cursor);
+    lc = (int)(pos - s_cb[b]);
   };
   // the row a lane copies for chunk i (its lane & 15 row), or -1: a token index for kept rows,
   // a window row number for window chunks; loaded one stage ahead of its copy
@@ -683,9 +702,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   // [G][D] o then [G] lse. The lane holds O^T[channel 16mt + lane/4 (+8)][head 8hb + 2(lane%4) + e].
   auto finish = [&](int b, bool to_smem) {
     ensure_wait();
-    int64_t w0, w1;
-    warp_span(p, b, w0, w1);
-    const bool whole = w0 == w1;
+    const bool whole = s_w0[b] == s_w1[b];
     const DraftReqDev& r = p.req[b];
     const size_t slot = (size_t)hk * (W + p.B) + (size_t)(wg + b);
 #pragma unroll
@@ -795,38 +812,39 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   __syncthreads();  // this CTA's warp partials are written (read back through L2 below)
   __shared__ int s_last;
   const int cx = blockIdx.x, NC = gridDim.x;
-  const int64_t q0 = (int64_t)cx * C::NW * T / W, q1 = ((int64_t)cx * C::NW + C::NW) * T / W;  // CTA chunks
-  if (q1 > q0) {
-    int cur = 0;
-    const int bA = draft_find_req(p, q0, cur);
-    const int bB = draft_find_req(p, q1 - 1, cur);
+  // the CTA's requests: from its first warp's first to its last warp's last (warps hold
+  // consecutive ranges; an empty warp holds none)
+  int bA = VC_MAX_BATCH, bB = -1;
+#pragma unroll
+  for (int k = 0; k < C::NW; ++k) {
+    if (s_first[k] >= 0 && s_first[k] < bA) bA = s_first[k];
+    if (s_final[k] > bB) bB = s_final[k];
+  }
+  {
 #pragma unroll 1
     for (int b = bA; b <= bB; ++b) {
-      int64_t w0, w1;
-      warp_span(p, b, w0, w1);
+      const int64_t w0 = s_w0[b], w1 = s_w1[b];
       if (w0 == w1) continue;  // inside one warp: its output is written
       const int64_t cw0 = w0 > (int64_t)cx * C::NW ? w0 : (int64_t)cx * C::NW;
       const int64_t cw1 = w1 < (int64_t)cx * C::NW + C::NW - 1 ? w1 : (int64_t)cx * C::NW + C::NW - 1;
+      if (cw0 > cw1) continue;  // (cannot happen: b lies in this CTA's range)
       const int64_t c0 = w0 / C::NW, c1 = w1 / C::NW;
       const bool one_cta = c0 == c1;
       const int64_t cslot = (int64_t)hk * (NC + p.B) + cx + b;
-      bf16* orow = p.req[b].o + (size_t)hk * G * D;
+      bf16* orow = s_o[b] + (size_t)hk * G * D;
       // where each of this CTA's partials of b is: in the warp's stage ring when b is the warp's
-      // last request, else in the workspace (written when the warp moved on to its next request)
-      // (a warp whose range is empty — fewer chunks than warps in a one-CTA launch — holds none)
-      // Slot k is warp cw0 + k, empty (null) past cw1 or for a warp whose range is empty; the
-      // indices are compile-time so the pointers stay in registers.
+      // last request, else in the workspace (written when the warp moved on to its next request).
+      // Slot k is warp cw0 + k, empty (null) past cw1 or for a warp with no chunks; the indices
+      // are compile-time so the pointers stay in registers.
       const float* po[C::NW];
       const float* pl[C::NW];
 #pragma unroll
       for (int k = 0; k < C::NW; ++k) {
         po[k] = pl[k] = nullptr;
         const int64_t w = cw0 + k;
-        const int64_t e0 = w * T / W, e1 = (w + 1) * T / W;
-        if (w <= cw1 && e1 > e0) {
-          const int lw = (int)(w - (int64_t)cx * C::NW);
-          int cur2 = 0;
-          if (draft_find_req(p, e1 - 1, cur2) == b) {
+        const int lw = (int)(w - (int64_t)cx * C::NW);
+        if (w <= cw1 && s_final[lw & (C::NW - 1)] >= 0) {
+          if (s_final[lw] == b) {
             po[k] = reinterpret_cast<const float*>(smem + lw * C::PER_WARP);
             pl[k] = po[k] + G * D;
           } else {

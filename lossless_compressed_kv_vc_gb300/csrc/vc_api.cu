@@ -297,6 +297,13 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   if (by_work < per_head) per_head = (int)(by_work > 1 ? by_work : 1);
   p.n_vwarps = (int64_t)per_head * kDraftWarps;
   p.total_chunks = total;
+  if ((uint64_t)total * (uint64_t)(p.n_vwarps + 1) >= (uint64_t(1) << 32)) return VC_ERR_UNSUPPORTED;  // 32-bit range math
+  for (int b = 0; b < B; ++b) {  // warps w hold chunks [w*T/W, (w+1)*T/W): the span of each request
+    DraftReqDev& r = p.req[b];
+    const int64_t c0 = r.chunk_begin, c1 = c0 + r.n_chunks, W = p.n_vwarps;
+    r.w0 = (int32_t)(((c0 + 1) * W - 1) / total);
+    r.w1 = (int32_t)((c1 * W - 1) / total);
+  }
   const size_t need = vc_workspace_size(VC_CALL_DRAFT, shape, 0);
   if (!ws || ws_bytes < need || !aligned16(ws)) return VC_ERR_WORKSPACE;
   const size_t slots = (size_t)Hkv * (p.n_vwarps + B);

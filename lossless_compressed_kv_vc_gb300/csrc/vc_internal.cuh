@@ -208,6 +208,7 @@ struct DraftReqDev {
   int32_t chunk_begin;  // first chunk of this request in the per-head concatenation
   int32_t n_mc;
   int32_t n_chunks;
+  int32_t w0, w1;       // first and last warp (of a head) whose range holds a chunk of it
 };
 
 struct DraftParams {
