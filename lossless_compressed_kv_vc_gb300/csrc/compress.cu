@@ -2,10 +2,12 @@
 // Inference", "Architecture support" — the framework plugs token-drop (SnapKV, KVzip) and
 // quantising (KIVI) compressors in without touching scheduling or verification.
 //
-// Token drop: one CTA per request selects the keep-set with a 4-pass MSB radix select over the
-// order-preserving uint32 image of the fp32 importance (-0 folded onto +0), then writes the kept
-// indices in ascending order from per-thread contiguous segments and two block scans (ties at the
-// threshold go to the lower indices), then appends the recent window. An optional second launch gathers the kept rows.
+// Token drop: one 8-CTA thread-block cluster per request selects the keep-set with a 4-pass MSB
+// radix select over the order-preserving uint32 image of the fp32 importance (-0 folded onto +0),
+// summing the CTAs' histograms through distributed shared memory, then writes the kept indices in
+// ascending order (each CTA its slice, offset by the lower-ranked CTAs' counts; ties at the
+// threshold go to the lower indices), then appends the recent window. An optional second launch
+// gathers the kept rows.
 // Quantisation: key groups (32 tokens of one channel) one thread per channel; value groups
 // (32 channels of one token) one lane per 4 channels with shuffle min/max; every float decision
 // uses IEEE round-to-nearest (division, rint half-to-even, fp32->fp16), as the format defines.
@@ -21,29 +23,61 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-constexpr int kKeepThreads = 1024;
-constexpr int kKeepCacheKeys = 48 * 1024;  // candidates whose keys fit in shared memory (192 KB)
+constexpr int kKeepCL = 8;                 // CTAs per request: one thread-block cluster
+constexpr int kKeepThreads = 512;
+constexpr int kKeepWarps = kKeepThreads / 32;
+constexpr int kKeepCacheKeys = 48 * 1024;  // keys of a CTA's slice that fit in shared memory (192 KB)
 
-__global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_constant__ KeepParams p, int cache_keys) {
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives; shared-memory writes before it are visible to
+// the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A word of CTA `rank`'s shared memory at the address of `p` in this CTA's.
+__device__ __forceinline__ uint32_t ld_cluster_u32(const void* p, uint32_t rank) {
+  uint32_t a, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// One cluster of kKeepCL CTAs per request; CTA `rank` owns candidates [rank*n/CL, (rank+1)*n/CL).
+// The radix passes sum the CTAs' 256-bin histograms through distributed shared memory after a
+// cluster barrier (every CTA then takes the same digit), and the compaction offsets a CTA's slice
+// by the kept counts of the lower-ranked CTAs.
+__global__ void __cluster_dims__(kKeepCL, 1, 1) __launch_bounds__(kKeepThreads)
+    keepset_kernel(const __grid_constant__ KeepParams p, int cache_keys) {
   pdl_launch_dependents();
   pdl_wait();
-  const KeepReq& r = p.req[blockIdx.x];
+  const int b = blockIdx.x / kKeepCL;
+  const uint32_t rank = cluster_rank();
+  const KeepReq& r = p.req[b];
   const int n = r.ctx, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  if (r.keep >= n) {
-    for (int j = tid; j < n; j += kKeepThreads) r.idx[j] = j;
+  if (r.keep >= n) {  // keep everything (uniform over the cluster: no shared state is touched)
+    const int j0 = (int)((int64_t)rank * n / kKeepCL), j1 = (int)((int64_t)(rank + 1) * n / kKeepCL);
+    for (int j = j0 + tid; j < j1; j += kKeepThreads) r.idx[j] = j;
     return;
   }
   const int n_cand = n - r.recent;
   const int need = r.keep - r.recent;
+  const int s0 = (int)((int64_t)rank * n_cand / kKeepCL), s1 = (int)((int64_t)(rank + 1) * n_cand / kKeepCL);
+  const int ns = s1 - s0;  // this CTA's candidates
   extern __shared__ uint32_t kcache[];
-  __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist[2][256];  // this CTA's histogram, double-buffered by pass
+  __shared__ uint32_t tot[256];      // the cluster's histogram
   __shared__ uint32_t s_prefix, s_mask, s_rem;
-  __shared__ int s_cnt[2][32];
-  const bool cached = n_cand <= cache_keys;
+  __shared__ int s_cnt[2][kKeepWarps];
+  __shared__ int s_cta[2];           // this CTA's candidates above T and equal to T
+  const bool cached = ns <= cache_keys;
   if (cached) {
 #pragma unroll 4
-    for (int i = tid; i < n_cand; i += kKeepThreads) kcache[i] = order_key(__ldg(r.imp + i));
+    for (int i = tid; i < ns; i += kKeepThreads) kcache[i] = order_key(__ldg(r.imp + s0 + i));
   }
   if (tid == 0) {
     s_prefix = 0;
@@ -51,28 +85,37 @@ __global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_cons
     s_rem = (uint32_t)need;
   }
   __syncthreads();
-  auto key = [&](int i) -> uint32_t { return cached ? kcache[i] : order_key(__ldg(r.imp + i)); };
-  // 1. radix select, most significant byte first: find the key T of the need-th largest
-  //    candidate and how many candidates equal to T must be kept (s_rem after the passes)
+  auto key = [&](int i) -> uint32_t { return cached ? kcache[i] : order_key(__ldg(r.imp + s0 + i)); };
+  // 1. radix select, most significant byte first, over the whole request: the key T of the
+  //    need-th largest candidate and how many candidates equal to T are kept (s_rem at the end)
   if (need > 0) {
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      if (tid < 256) hist[tid] = 0;
+      uint32_t* h = hist[pass & 1];  // last read by the cluster before the previous cluster barrier
+      if (tid < 256) h[tid] = 0;
       __syncthreads();
       const uint32_t prefix = s_prefix, mask = s_mask;
 #pragma unroll 4
-      for (int base = 0; base < n_cand; base += kKeepThreads) {  // whole warps iterate together
+      for (int base = 0; base < ns; base += kKeepThreads) {  // whole warps iterate together
         const int i = base + tid;
-        const uint32_t u = i < n_cand ? key(i) : 0u;
-        const bool in = i < n_cand && (u & mask) == prefix;
+        const uint32_t u = i < ns ? key(i) : 0u;
+        const bool in = i < ns && (u & mask) == prefix;
         const uint32_t dg = (u >> shift) & 255u;
         // aggregate equal digits of a warp into one shared atomic
         const unsigned act = __ballot_sync(0xffffffffu, in);
         if (in) {
           const unsigned peers = __match_any_sync(act, dg);
-          if (lane == (__ffs(peers) - 1)) atomicAdd(&hist[dg], (uint32_t)__popc(peers));
+          if (lane == (__ffs(peers) - 1)) atomicAdd(&h[dg], (uint32_t)__popc(peers));
         }
+      }
+      __syncthreads();
+      cluster_sync();  // every CTA's histogram of this pass is complete
+      if (tid < 256) {
+        uint32_t t = 0;
+#pragma unroll
+        for (int q = 0; q < kKeepCL; ++q) t += ld_cluster_u32(&h[tid], (uint32_t)q);
+        tot[tid] = t;
       }
       __syncthreads();
       if (warp == 0) {
@@ -80,7 +123,7 @@ __global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_cons
         uint32_t c[8], own = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          c[k] = hist[8 * lane + k];
+          c[k] = tot[8 * lane + k];
           own += c[k];
         }
         uint32_t above = own;  // inclusive suffix sum over lanes >= l
@@ -106,12 +149,13 @@ __global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_cons
     }
   }
   // 2. ascending compaction over contiguous per-warp segments, 32 elements per ballot: an element's
-  //    slot is the number of larger keys before it plus min(equal keys before it, need_eq)
+  //    slot is the number of larger keys before it plus min(equal keys before it, need_eq), where
+  //    "before" spans the lower-ranked CTAs' slices too
   if (need > 0) {
     const uint32_t T = s_prefix;
     const int need_eq = (int)s_rem;
-    const int segw = ((n_cand + 31) / 32 + 31) / 32 * 32;
-    const int w0 = min(n_cand, warp * segw), w1 = min(n_cand, w0 + segw);
+    const int segw = ((ns + 31) / 32 + kKeepWarps - 1) / kKeepWarps * 32;
+    const int w0 = min(ns, warp * segw), w1 = min(ns, w0 + segw);
     const unsigned lt = (1u << lane) - 1u;
     int gt = 0, eq = 0;
 #pragma unroll 4
@@ -126,7 +170,22 @@ __global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_cons
       s_cnt[1][warp] = eq;
     }
     __syncthreads();
+    if (tid == 0) {
+      int g = 0, e = 0;
+      for (int w = 0; w < kKeepWarps; ++w) {
+        g += s_cnt[0][w];
+        e += s_cnt[1][w];
+      }
+      s_cta[0] = g;
+      s_cta[1] = e;
+    }
+    __syncthreads();
+    cluster_sync();  // every CTA's counts are complete
     int gt_before = 0, eq_before = 0;
+    for (uint32_t q = 0; q < rank; ++q) {
+      gt_before += (int)ld_cluster_u32(&s_cta[0], q);
+      eq_before += (int)ld_cluster_u32(&s_cta[1], q);
+    }
     for (int w = 0; w < warp; ++w) {
       gt_before += s_cnt[0][w];
       eq_before += s_cnt[1][w];
@@ -141,12 +200,16 @@ __global__ void __launch_bounds__(kKeepThreads) keepset_kernel(const __grid_cons
       const unsigned beq = __ballot_sync(0xffffffffu, valid && u == T);
       const bool take_eq = valid && u == T && eq_run + __popc(beq & lt) < need_eq;
       const unsigned bsel = bgt | __ballot_sync(0xffffffffu, take_eq);
-      if ((bsel >> lane) & 1u) r.idx[out + __popc(bsel & lt)] = i;
+      if ((bsel >> lane) & 1u) r.idx[out + __popc(bsel & lt)] = s0 + i;
       out += __popc(bsel);
       eq_run += __popc(beq);
     }
   }
-  for (int j = tid; j < r.recent; j += kKeepThreads) r.idx[need + j] = n_cand + j;
+  {
+    const int j0 = (int)((int64_t)rank * r.recent / kKeepCL), j1 = (int)((int64_t)(rank + 1) * r.recent / kKeepCL);
+    for (int j = j0 + tid; j < j1; j += kKeepThreads) r.idx[need + j] = n_cand + j;
+  }
+  cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // Gather kept rows into a compact copy: dst[h][j] = src[h][idx[j]] (one warp per row pair).
@@ -178,12 +241,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __grid_constant_
 }
 
 cudaError_t launch_keepset(const KeepParams& p, int max_keep, cudaStream_t s) {
-  int max_cand = 0;
+  int max_slice = 0;
   for (int b = 0; b < p.B; ++b) {
     const int nc = p.req[b].ctx - p.req[b].recent;
-    if (nc > max_cand) max_cand = nc;
+    const int sl = (nc + kKeepCL - 1) / kKeepCL;
+    if (sl > max_slice) max_slice = sl;
   }
-  const int cache_keys = max_cand < kKeepCacheKeys ? max_cand : kKeepCacheKeys;
+  const int cache_keys = max_slice < kKeepCacheKeys ? max_slice : kKeepCacheKeys;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(keepset_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -191,8 +255,8 @@ cudaError_t launch_keepset(const KeepParams& p, int max_keep, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  cudaError_t e = launch_pdl(keepset_kernel, dim3(p.B), dim3(kKeepThreads), (size_t)cache_keys * sizeof(uint32_t), s,
-                             p, cache_keys);
+  cudaError_t e = launch_pdl(keepset_kernel, dim3(p.B * kKeepCL), dim3(kKeepThreads),
+                             (size_t)(cache_keys > 0 ? cache_keys : 1) * sizeof(uint32_t), s, p, cache_keys);
   if (e != cudaSuccess) return e;
   bool any = false;
   for (int b = 0; b < p.B; ++b) any |= p.req[b].compact != 0;
