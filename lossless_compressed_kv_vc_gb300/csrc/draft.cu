@@ -7,15 +7,15 @@
 // Work decomposition (one launch per draft step):
 //   For one KV head, each request's rows form a list of chunks: its KV_comp rows (16 kept bf16
 //   rows, or one 32-token quantised group, per chunk) followed by its bf16 window rows (16 per
-//   chunk; the last window row is this step's own K/V). The chunk lists of all requests are
-//   concatenated and cut into equal contiguous ranges, one per warp, over one wave of 4-warp CTAs
-//   and one grid row per KV head, so every warp streams the same number of bytes. A warp owns its
-//   range outright: its own ring of shared-memory stages, its own online softmax, and at each
-//   request boundary either the final bf16 row (the request lay entirely inside the warp's range)
-//   or an (o, lse) partial in slot warp + request. The warp whose partial of a request arrives
-//   last (a per-request arrival counter) merges that request's partials, in warp order, into the
-//   output, so a step needs no second launch. No CTA barrier.
-//
+//   chunk; the last window row is this step's own K/V). The host gives each request a whole number
+//   of warps in proportion to its chunks (one wave of 4-warp CTAs, one grid row per KV head), and
+//   a request's chunks are cut into equal contiguous ranges over its warps, so no warp holds two
+//   requests. A warp owns its range outright: its own ring of shared-memory stages and its own
+//   online softmax; its (o, lse) partial stays in its drained ring. At the end each CTA merges,
+//   per request it holds, its warps' partials into the output (the request lies in this CTA) or
+//   into a CTA partial; the CTA that arrives last among the request's CTAs (a per-request arrival
+//   counter) merges those, in CTA order, so a step needs no second launch.
+
 // Tensor cores: scores are S^T = K Q^T and the output O^T += V^T P^T on m16n8k16 MMAs with the
 // 16 tokens (or 16 channels) of a tile as M and the query heads of the KV head as N (8 per MMA,
 // zero-padded), so a KV byte serves all G heads and a 16-token tile costs d/8 MMAs. P^T, produced
@@ -351,20 +351,8 @@ __device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zs)[
       }
 }
 
-// The request lookups below read cb = each request's first chunk, cb[B] = total chunks, copied
-// into shared memory at kernel start: the kernel parameters are too large for the constant cache,
-// and a lookup chain that misses it costs a memory round trip per step.
-
-// Advance a request cursor to the request holding chunk `pos` (positions only grow along a warp's
-// range, so each call site keeps its own cursor).
-__device__ __forceinline__ int draft_find_req(const int32_t* cb, int B, int64_t pos, int& cursor) {
-  while (cursor + 1 < B && cb[cursor + 1] <= pos) ++cursor;
-  return cursor;
-}
-
-// Warp ranges cut T chunks into W parts: warp w holds [w*T/W, (w+1)*T/W). The host guarantees
-// T * (W + 1) < 2^32, so these products and quotients are 32-bit (a 64-bit division is a long
-// software routine).
+// Edge w of T chunks cut into W equal ranges: w * T / W. The host bounds T * (W + 1) below 2^32,
+// so this stays 32-bit (a 64-bit division is a long software routine).
 __device__ __forceinline__ uint32_t range_edge(uint32_t w, uint32_t T, uint32_t W) { return w * T / W; }
 
 
@@ -518,10 +506,6 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hk = blockIdx.y;
   const int G = p.G;
-  const uint32_t T = (uint32_t)p.total_chunks, W = (uint32_t)p.n_vwarps;
-  const int64_t wg = (int64_t)blockIdx.x * C::NW + warp;
-  const int64_t p0 = range_edge((uint32_t)wg, T, W), p1 = range_edge((uint32_t)wg + 1, T, W);
-  const int n = (int)(p1 - p0);  // may be 0: the warp still takes part in the CTA's merge phase
 
   // Each stage completes on its mbarrier: TMA loads (kept rows, quantised groups) by their bytes,
   // window rows (cp.async) by a plain arrive once issued, after which the lanes' cp.async groups
@@ -535,17 +519,33 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     fence_mbar_init();
   }
   __shared__ int32_t s_cb[VC_MAX_BATCH + 1];  // first chunk of each request; s_cb[B] = total chunks
-  __shared__ int32_t s_w0[VC_MAX_BATCH], s_w1[VC_MAX_BATCH];  // first / last warp holding each request
+  __shared__ int32_t s_wb[VC_MAX_BATCH + 1];  // first warp (of a head) of each request; s_wb[B] = warps
   __shared__ bf16* s_o[VC_MAX_BATCH];         // output rows of each request
-  __shared__ int32_t s_first[C::NW], s_final[C::NW];  // each warp's first and last request (-1: none)
+  __shared__ int32_t s_wreq[C::NW];           // each warp's request (-1: none)
+  __shared__ int32_t s_has[C::NW];            // the warp left a partial in its stage ring
   if (threadIdx.x < p.B) {
     s_cb[threadIdx.x] = p.req[threadIdx.x].chunk_begin;
-    s_w0[threadIdx.x] = p.req[threadIdx.x].w0;
-    s_w1[threadIdx.x] = p.req[threadIdx.x].w1;
+    s_wb[threadIdx.x] = p.req[threadIdx.x].warp_begin;
     s_o[threadIdx.x] = p.req[threadIdx.x].o;
   }
-  if (threadIdx.x == 0) s_cb[p.B] = (int32_t)p.total_chunks;
+  if (threadIdx.x == 0) {
+    s_cb[p.B] = (int32_t)p.total_chunks;
+    s_wb[p.B] = p.n_warp_head;
+  }
   __syncthreads();
+  // This warp's request rb (warps [s_wb[rb], s_wb[rb+1]) of the head hold it) and its range: the
+  // request's chunks cut evenly over its warps (32-bit: the host bounds the products). Warps past
+  // the last request's (the tail of the last CTA) hold nothing.
+  const int wgl = (int)blockIdx.x * C::NW + warp;
+  int rb = 0;
+  while (rb + 1 < p.B && s_wb[rb + 1] <= wgl) ++rb;
+  const bool in_part = wgl < s_wb[p.B];
+  const uint32_t nb = (uint32_t)(s_cb[rb + 1] - s_cb[rb]), kw = (uint32_t)(s_wb[rb + 1] - s_wb[rb]);
+  const uint32_t wr = (uint32_t)(wgl - s_wb[rb]);
+  const int64_t p0 = s_cb[rb] + (in_part ? (int64_t)range_edge(wr, nb, kw) : 0);
+  const int64_t p1 = s_cb[rb] + (in_part ? (int64_t)range_edge(wr + 1, nb, kw) : 0);
+  const int n = (int)(p1 - p0);  // may be 0: the warp still takes part in the CTA's merge
+  if (lane == 0) s_wreq[warp] = in_part ? rb : -1;
   pdl_launch_dependents();
   // Ordering against the previous kernel in the stream (programmatic dependent launch): queries,
   // kept rows and indices are never written by a draft step, verify or accept, so with p.early the
@@ -561,17 +561,11 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     }
   };
 
-  // chunk i of this warp -> (request, chunk within request)
+  // chunk i of this warp -> (request, chunk within request); a warp holds one request only
   int cur_row = 0, cur_issue = 0, cur_proc = 0;
-  if (lane == 0) {
-    int c = 0;
-    s_first[warp] = n > 0 ? draft_find_req(s_cb, p.B, p0, c) : -1;
-    s_final[warp] = n > 0 ? draft_find_req(s_cb, p.B, p1 - 1, c) : -1;
-  }
-  auto locate = [&](int i, int& b, int& lc, int& cursor) {
-    const int64_t pos = p0 + i;
-    b = draft_find_req(s_cb, p.B, pos, cursor);
-    lc = (int)(pos - s_cb[b]);
+  auto locate = [&](int i, int& b, int& lc, int& /*cursor*/) {
+    b = rb;
+    lc = (int)(p0 + i - s_cb[rb]);
   };
   // the row a lane copies for chunk i (its lane & 15 row), or -1: a token index for kept rows,
   // a window row number for window chunks; loaded one stage ahead of its copy
@@ -697,14 +691,9 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       }
     }
   };
-  // end of request b inside this warp: final bf16 output, or an (o, lse) partial — in slot wg + b
-  // of the workspace, or (the warp's last request, to_smem) in the warp's drained stage ring as
+  // end of the warp's range: its (o, lse) partial, normalised, into its drained stage ring as
   // [G][D] o then [G] lse. The lane holds O^T[channel 16mt + lane/4 (+8)][head 8hb + 2(lane%4) + e].
-  auto finish = [&](int b, bool to_smem) {
-    ensure_wait();
-    const bool whole = s_w0[b] == s_w1[b];
-    const DraftReqDev& r = p.req[b];
-    const size_t slot = (size_t)hk * (W + p.B) + (size_t)(wg + b);
+  auto finish = [&]() {
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
@@ -716,24 +705,14 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         const int h = 8 * hb + 2 * (lane & 3) + e;
         if (h >= G) continue;
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        float* dst = reinterpret_cast<float*>(wb) + h * D;
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
           const int c = 16 * mt + (lane >> 2);
-          const float v0 = o[hb][mt][e] * inv, v1 = o[hb][mt][e + 2] * inv;
-          if (whole) {
-            bf16* dst = r.o + (size_t)(hk * G + h) * D;
-            dst[c] = __float2bfloat16_rn(v0);
-            dst[c + 8] = __float2bfloat16_rn(v1);
-          } else {
-            float* dst = to_smem ? reinterpret_cast<float*>(wb) + h * D : p.ws_o + (slot * G + h) * D;
-            dst[c] = v0;
-            dst[c + 8] = v1;
-          }
+          dst[c] = o[hb][mt][e] * inv;
+          dst[c + 8] = o[hb][mt][e + 2] * inv;
         }
-        if (!whole && (lane >> 2) == 0) {
-          float* dst = to_smem ? reinterpret_cast<float*>(wb) + G * D + h : p.ws_lse + slot * G + h;
-          *dst = lt > 0.f ? m[hb][e] + log2f(lt) : -INFINITY;
-        }
+        if ((lane >> 2) == 0) reinterpret_cast<float*>(wb)[G * D + h] = lt > 0.f ? m[hb][e] + log2f(lt) : -INFINITY;
       }
   };
 
@@ -752,7 +731,6 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         fold_zs<D, NHB>(o, zs);
         zs_live = false;
       }
-      if (cur_b >= 0) finish(cur_b, false);
       reset();
       load_q(b);
       cur_b = b;
@@ -798,81 +776,60 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     }
   }
   cp_async_wait<0>();
-  if (!aborted && cur_b >= 0) {
+  const bool has = !aborted && cur_b >= 0;
+  if (has) {
     if (!BF16_ROWS && zs_live) fold_zs<D, NHB>(o, zs);
-    finish(cur_b, true);  // the stage ring is drained: the warp's last partial stays in shared memory
+    finish();  // the stage ring is drained: the partial stays in shared memory
   }
+  if (lane == 0) s_has[warp] = has ? 1 : 0;
 
-  // Merge phase, for requests split across warps. First each CTA merges its own warps' partials of
-  // a request (one query head per warp): into the output when the request lies inside this CTA,
-  // else into a CTA partial. Then the CTA that arrives last among those holding the request merges
-  // their CTA partials into the output. Both levels merge in slot order, so results do not depend
-  // on which CTA arrives last. Every condition below is uniform over the CTA.
-  ensure_wait();  // workspace and outputs are written below
-  __syncthreads();  // this CTA's warp partials are written (read back through L2 below)
+  // Merge, per request held by this CTA (by the partition, so every CTA arrives once for each of
+  // its requests even when a wait of its own gave up): the CTA's warps' partials of the request
+  // (one query head per warp) go into the output when the request lies in this CTA alone, else
+  // into the CTA's partial slot (CTA + request); the CTA that arrives last among the request's
+  // CTAs then merges their partials, in CTA order, into the output.
+  ensure_wait();  // the workspace and outputs are written below
+  __syncthreads();
   __shared__ int s_last;
-  const int cx = blockIdx.x, NC = gridDim.x;
-  // the CTA's requests: from its first warp's first to its last warp's last (warps hold
-  // consecutive ranges; an empty warp holds none)
+  const int cx = blockIdx.x, NC = p.n_cta_head;
   int bA = VC_MAX_BATCH, bB = -1;
 #pragma unroll
   for (int k = 0; k < C::NW; ++k) {
-    if (s_first[k] >= 0 && s_first[k] < bA) bA = s_first[k];
-    if (s_final[k] > bB) bB = s_final[k];
+    if (s_wreq[k] >= 0 && s_wreq[k] < bA) bA = s_wreq[k];
+    if (s_wreq[k] > bB) bB = s_wreq[k];
   }
-  {
 #pragma unroll 1
-    for (int b = bA; b <= bB; ++b) {
-      const int64_t w0 = s_w0[b], w1 = s_w1[b];
-      if (w0 == w1) continue;  // inside one warp: its output is written
-      const int64_t cw0 = w0 > (int64_t)cx * C::NW ? w0 : (int64_t)cx * C::NW;
-      const int64_t cw1 = w1 < (int64_t)cx * C::NW + C::NW - 1 ? w1 : (int64_t)cx * C::NW + C::NW - 1;
-      if (cw0 > cw1) continue;  // (cannot happen: b lies in this CTA's range)
-      const int64_t c0 = w0 / C::NW, c1 = w1 / C::NW;
-      const bool one_cta = c0 == c1;
-      const int64_t cslot = (int64_t)hk * (NC + p.B) + cx + b;
-      bf16* orow = s_o[b] + (size_t)hk * G * D;
-      // where each of this CTA's partials of b is: in the warp's stage ring when b is the warp's
-      // last request, else in the workspace (written when the warp moved on to its next request).
-      // Slot k is warp cw0 + k, empty (null) past cw1 or for a warp with no chunks; the indices
-      // are compile-time so the pointers stay in registers.
-      const float* po[C::NW];
-      const float* pl[C::NW];
+  for (int b = bA; b <= bB; ++b) {
+    const int c0 = s_wb[b] / C::NW, c1 = (s_wb[b + 1] - 1) / C::NW;  // CTAs holding b
+    const bool one_cta = c0 == c1;
+    const float* po[C::NW];
+    const float* pl[C::NW];
 #pragma unroll
-      for (int k = 0; k < C::NW; ++k) {
-        po[k] = pl[k] = nullptr;
-        const int64_t w = cw0 + k;
-        const int lw = (int)(w - (int64_t)cx * C::NW);
-        if (w <= cw1 && s_final[lw & (C::NW - 1)] >= 0) {
-          if (s_final[lw] == b) {
-            po[k] = reinterpret_cast<const float*>(smem + lw * C::PER_WARP);
-            pl[k] = po[k] + G * D;
-          } else {
-            po[k] = p.ws_o + ((int64_t)hk * (W + p.B) + w + b) * G * D;
-            pl[k] = p.ws_lse + ((int64_t)hk * (W + p.B) + w + b) * G;
-          }
-        }
-      }
+    for (int k = 0; k < C::NW; ++k) {
+      po[k] = (s_wreq[k] == b && s_has[k]) ? reinterpret_cast<const float*>(smem + k * C::PER_WARP) : nullptr;
+      pl[k] = po[k] ? po[k] + G * D : nullptr;
+    }
+    bf16* orow = s_o[b] + (size_t)hk * G * D;
+    const int64_t cslot = (int64_t)hk * (NC + p.B) + cx + b;
+    for (int h = warp; h < G; h += C::NW)
+      merge_local<D, C::NW>(po, pl, G, h, lane, one_cta ? orow + (size_t)h * D : nullptr,
+                            p.ws_o + (cslot * G + h) * D, p.ws_lse + cslot * G + h);
+    if (one_cta) continue;
+    // The barrier orders every thread's CTA-partial stores before thread 0's release fence and
+    // arrival; the last arriver's acquire fence and the second barrier order the other CTAs'
+    // partials before this CTA reads them.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      fence_acq_rel_gpu();
+      const bool last = cta_arrive(p, hk, b, c1 - c0 + 1);
+      if (last) fence_acq_rel_gpu();
+      s_last = last ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_last) {
       for (int h = warp; h < G; h += C::NW)
-        merge_local<D, C::NW>(po, pl, G, h, lane, one_cta ? orow + (size_t)h * D : nullptr,
-                              p.ws_co + (cslot * G + h) * D, p.ws_clse + cslot * G + h);
-      if (one_cta) continue;
-      // The barrier orders every thread's CTA-partial stores before thread 0's release fence and
-      // arrival; the last arriver's acquire fence and the second barrier order the other CTAs'
-      // partials before this CTA reads them.
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        fence_acq_rel_gpu();
-        const bool last = cta_arrive(p, hk, b, (int)(c1 - c0 + 1));
-        if (last) fence_acq_rel_gpu();
-        s_last = last ? 1 : 0;
-      }
-      __syncthreads();
-      if (s_last) {
-        for (int h = warp; h < G; h += C::NW)
-          merge_head<D>(p.ws_co, p.ws_clse, (int64_t)hk * (NC + p.B) + b + c0, (int)(c1 - c0 + 1), G, h, lane,
-                        orow + (size_t)h * D, nullptr, nullptr);
-      }
+        merge_head<D>(p.ws_o, p.ws_lse, (int64_t)hk * (NC + p.B) + b + c0, c1 - c0 + 1, G, h, lane,
+                      orow + (size_t)h * D, nullptr, nullptr);
     }
   }
 }

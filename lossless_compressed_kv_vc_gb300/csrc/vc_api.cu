@@ -90,11 +90,10 @@ const char* vc_status_string(vc_status s) {
 size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows) {
   if (!shape_ok(shape)) return 0;
   if (call == VC_CALL_DRAFT) {
+    // CTA partials: slots (CTA + request) per head, CTAs per head at most one wave plus B
     const size_t G = shape->Hq / shape->Hkv;
-    const size_t per_head = draft_ctas_per_head_max(shape->Hkv);
-    const size_t slots = (size_t)shape->Hkv * (kDraftWarps * per_head + shape->B);  // warp partials
-    const size_t cslots = (size_t)shape->Hkv * (per_head + shape->B);               // CTA partials
-    return draft_counter_bytes(shape->Hkv) + (slots + cslots) * G * (shape->d + 1) * sizeof(float) + 512;
+    const size_t slots = (size_t)shape->Hkv * (draft_ctas_per_head_max(shape->Hkv) + 2 * shape->B);
+    return draft_counter_bytes(shape->Hkv) + slots * G * (shape->d + 1) * sizeof(float) + 256;
   }
   if (call == VC_CALL_VERIFY) return verify_workspace_size(shape, max_rows);
   return 0;
@@ -288,33 +287,54 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
         return VC_ERR_CUDA;
     }
   }
-  // one wave of CTAs over the KV heads, but at least ~4 chunks per warp
+  // Warps per KV head: one wave of CTAs over the heads (and on average at least ~4 chunks per
+  // warp). Each request gets a whole number of warps in proportion to its chunks, so no warp holds
+  // two requests; warps left over go, a whole tier at a time, to the requests with the largest
+  // chunks-per-warp load, and only while that lowers it.
   const int kind = mode == VC_TOKEN_DROP ? 0 : bits;
-  int per_head = draft_ctas_per_head_max(Hkv, G);
+  int P = draft_ctas_per_head_max(Hkv, G);
   const int env = env_int("VC_DRAFT_CTAS", 0);
-  if (env > 0 && env / Hkv < per_head) per_head = env / Hkv > 1 ? env / Hkv : 1;
+  if (env > 0 && env / Hkv < P) P = env / Hkv > 1 ? env / Hkv : 1;
   const int64_t by_work = (total + 4 * kDraftWarps - 1) / (4 * kDraftWarps);
-  if (by_work < per_head) per_head = (int)(by_work > 1 ? by_work : 1);
-  p.n_vwarps = (int64_t)per_head * kDraftWarps;
-  p.total_chunks = total;
-  if ((uint64_t)total * (uint64_t)(p.n_vwarps + 1) >= (uint64_t(1) << 32)) return VC_ERR_UNSUPPORTED;  // 32-bit range math
-  for (int b = 0; b < B; ++b) {  // warps w hold chunks [w*T/W, (w+1)*T/W): the span of each request
-    DraftReqDev& r = p.req[b];
-    const int64_t c0 = r.chunk_begin, c1 = c0 + r.n_chunks, W = p.n_vwarps;
-    r.w0 = (int32_t)(((c0 + 1) * W - 1) / total);
-    r.w1 = (int32_t)((c1 * W - 1) / total);
+  if (by_work < P) P = (int)(by_work > 1 ? by_work : 1);
+  const int Wmax = P * kDraftWarps;
+  int kw[VC_MAX_BATCH];
+  int used = 0;
+  for (int b = 0; b < B; ++b) {
+    const int64_t share = Wmax > B ? (int64_t)p.req[b].n_chunks * Wmax / total : 1;
+    kw[b] = share > 1 ? (int)share : 1;
+    used += kw[b];
   }
+  for (int left = Wmax - used; left > 0;) {
+    int bm = 0;  // the largest load n_b / k_b, compared exactly by cross products
+    for (int b = 1; b < B; ++b)
+      if ((int64_t)p.req[b].n_chunks * kw[bm] > (int64_t)p.req[bm].n_chunks * kw[b]) bm = b;
+    int tier = 0;
+    for (int b = 0; b < B; ++b)
+      tier += (int64_t)p.req[b].n_chunks * kw[bm] == (int64_t)p.req[bm].n_chunks * kw[b];
+    if (tier > left) break;
+    for (int b = 0; b < B; ++b)
+      if ((int64_t)p.req[b].n_chunks * kw[bm] == (int64_t)p.req[bm].n_chunks * kw[b]) ++kw[b];
+    left -= tier;
+  }
+  int n_warp = 0;
+  for (int b = 0; b < B; ++b) {
+    // a warp's range edge is w * n_b / k_b with w <= k_b, computed in 32 bits
+    if ((uint64_t)p.req[b].n_chunks * (uint64_t)(kw[b] + 1) >= (uint64_t(1) << 32)) return VC_ERR_UNSUPPORTED;
+    p.req[b].warp_begin = n_warp;
+    n_warp += kw[b];
+  }
+  const int n_cta = (n_warp + kDraftWarps - 1) / kDraftWarps;
+  p.n_warp_head = n_warp;
+  p.n_cta_head = n_cta;
+  p.total_chunks = total;
   const size_t need = vc_workspace_size(VC_CALL_DRAFT, shape, 0);
   if (!ws || ws_bytes < need || !aligned16(ws)) return VC_ERR_WORKSPACE;
-  const size_t slots = (size_t)Hkv * (p.n_vwarps + B);
   p.ws_ctr = static_cast<uint32_t*>(ws);
   p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + draft_counter_bytes(Hkv));
-  p.ws_lse = p.ws_o + slots * G * d;
-  const size_t cslots = (size_t)Hkv * (per_head + B);
-  p.ws_co = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(p.ws_lse + slots * G) + 255) & ~uintptr_t(255));
-  p.ws_clse = p.ws_co + cslots * G * d;
+  p.ws_lse = p.ws_o + (size_t)Hkv * (n_cta + B) * G * d;
   p.early = last_op(stream) != kOpCompress;
-  if (launch_draft(p, &maps, d, kind, per_head, stream) != cudaSuccess) return VC_ERR_CUDA;
+  if (launch_draft(p, &maps, d, kind, n_cta, stream) != cudaSuccess) return VC_ERR_CUDA;
   set_last_op(stream, kOpDraft);
   return VC_OK;
 }

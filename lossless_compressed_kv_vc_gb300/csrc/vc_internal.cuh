@@ -208,19 +208,18 @@ struct DraftReqDev {
   int32_t chunk_begin;  // first chunk of this request in the per-head concatenation
   int32_t n_mc;
   int32_t n_chunks;
-  int32_t w0, w1;       // first and last warp (of a head) whose range holds a chunk of it
+  int32_t warp_begin;   // first warp (of a head's grid row) holding it; it holds them up to the next request's
 };
 
 struct DraftParams {
   DraftReqDev req[VC_MAX_BATCH];
   int32_t B, Hq, Hkv, G;
   float scale_log2;      // log2(e) / sqrt(d)
-  float* ws_o;           // [Hkv][n_vwarps + B][G][d] per-warp partials (slot = warp + request)
-  float* ws_lse;         // [Hkv][n_vwarps + B][G]  (log2 domain)
-  float* ws_co;          // [Hkv][CTAs per head + B][G][d] per-CTA partials (slot = CTA + request)
-  float* ws_clse;        // [Hkv][CTAs per head + B][G]
+  float* ws_o;           // [Hkv][n_cta_head + B][G][d] per-CTA partials (slot = CTA + request)
+  float* ws_lse;         // [Hkv][n_cta_head + B][G]  (log2 domain)
   uint32_t* ws_ctr;      // [Hkv][VC_MAX_BATCH] CTA-partial arrival counts (zero between calls)
-  int64_t n_vwarps;      // warps per KV head (grid.x * 4)
+  int32_t n_cta_head;    // CTAs per KV head (grid.x)
+  int32_t n_warp_head;   // warps per KV head that hold work (the last CTA may hold fewer)
   int64_t total_chunks;  // chunks per KV head over all requests
   int32_t* dev_status;
   // 1: the kernel may stream queries, kept rows and indices before the previous kernel in the
@@ -230,8 +229,8 @@ struct DraftParams {
 };
 
 // Tensor maps of the kept K and V rows of each request (token drop): 2-D (d, Hkv * rows_cap) over
-// the bf16 rows, box 64 x 1, 128-byte swizzle. A separate kernel argument, so the combine launch
-// does not carry them.
+// the bf16 rows, box 64 x 1, 128-byte swizzle. A separate kernel argument: the kernels for
+// quantised caches take none.
 struct DraftMaps {
   CUtensorMap kv[VC_MAX_BATCH][2];
 };

@@ -56,7 +56,7 @@ def test_noalloc_matches_workspace_entry_point_twice(vc, which):
 
 def test_noalloc_rejects_calls_beyond_its_scratch(vc):
     """A shape whose partials exceed the static array is refused with VC_ERR_WORKSPACE, launching nothing."""
-    big = vc.vc_shape(32, 512, 8, 128)
+    big = vc.vc_shape(32, 1024, 8, 128)
     assert vc.vc_workspace_size(vc.VC_CALL_DRAFT, big) > (32 << 20)
     st = vc.vc_draft_attn_noalloc(big, None, raise_on_error=False, stream=0)
     assert st == vc.VC_ERR_WORKSPACE
