@@ -84,11 +84,12 @@ typedef struct vc_kv_full {
  *   compact == 1 vc_compress_kv gathers them into k_rows[h][j], j < keep, and the draft reads them
  *   contiguously (needed when KV_full leaves HBM).
  * VC_QUANT: groupwise asymmetric `bits`-bit codes for the first Tq = 32*ng tokens, in blocks of 32
- *   tokens (keys: one scale/zero per (block, channel); values: per (token, 32-channel group)):
- *   kc  uint8 [Hkv][ng][32*d*bits/8]   key codes of each block, in block word order (below)
- *   ks,kz fp16 [Hkv][ng][d]            key scale and zero per (block, channel)
- *   vc  uint8 [Hkv][ng][32*d*bits/8]   value codes of each block, in block word order
- *   vs,vz fp16 [Hkv][Tq][d/32]         value scale and zero per (token, 32-channel group)
+ *   tokens (keys: one scale/zero per (block, channel); values: per (token, 32-channel group)),
+ *   in buffers sized for ng_cap >= ng blocks (the head stride, so blocks can be appended):
+ *   kc  uint8 [Hkv][ng_cap][32*d*bits/8]   key codes of each block, in block word order (below)
+ *   ks,kz fp16 [Hkv][ng_cap][d]            key scale and zero per (block, channel)
+ *   vc  uint8 [Hkv][ng_cap][32*d*bits/8]   value codes of each block, in block word order
+ *   vs,vz fp16 [Hkv][32*ng_cap][d/32]      value scale and zero per (token, 32-channel group)
  *   Dequantised value: code * scale + zero.
  *   Block word order: little-endian 32-bit words w[half][j][lane] (4-bit; half = 16-token half,
  *   j = 16-channel step, lane = 0..31) or w[half][p][lane] (2-bit, p covers j = 2p, 2p+1). With
@@ -127,6 +128,7 @@ typedef struct vc_kv_comp {
   void* v_win;
   int32_t win_cap;
   int32_t n_win;       /* rows present before this draft step (set to n_res / 0 by vc_compress_kv) */
+  int32_t ng_cap;      /* VC_QUANT: blocks the quantised buffers hold per head (>= ng) */
 } vc_kv_comp;
 
 /* ------------------------------------------------------------------------------------------ */
@@ -150,6 +152,34 @@ typedef struct vc_kv_comp {
 vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const float* const* importance,
                          const int32_t* recent, int32_t residual_min, vc_kv_comp* comp,
                          int32_t* dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* vc_append_kv — after accept, grow the caches by the accepted drafted tokens ("Core algorithm":
+ * the loop restarts from the last accepted token, so the tokens before it are now context).
+ *
+ * For each request b the first n_rows rows of k_rows/v_rows (the drafted tokens' K/V, in draft
+ * order; n_rows = n_acc - 1, the accepted drafts without the bonus/correction token, whose K/V the
+ * next forward pass produces) become KV_full rows ctx .. ctx+n_rows-1 and full[b].ctx grows by
+ * n_rows. VC_QUANT requests also grow KV_comp: with ctx' = ctx + n_rows, ng' = max(0, (ctx' -
+ * residual_min) / 32) blocks are kept quantised; the ng' - ng blocks that became whole are
+ * quantised from the residual and the new rows exactly as vc_compress_kv would (same rule, same
+ * words), and the window restarts with the n_res' = ctx' - 32*ng' trailing tokens; comp[b].ng and
+ * comp[b].n_win are updated. The state equals vc_compress_kv of the grown KV_full. VC_TOKEN_DROP
+ * requests keep their keep-set until the next vc_compress_kv.
+ * Requirements: ctx + n_rows <= full[b].cap; VC_QUANT: ng' <= ng_cap, the residual plus n_rows
+ * at most VC_APPEND_MAX_ROWS rows. Returns VC_ERR_INVALID / VC_ERR_UNSUPPORTED before launching
+ * anything when a requirement fails. */
+#define VC_APPEND_MAX_ROWS 256
+
+typedef struct vc_append_req {
+  const void* k_rows;  /* bf16 [>= n_rows][Hkv][d]: the accepted drafts' keys (as the verification
+                          pass computed them), in draft order; not inside this request's window */
+  const void* v_rows;  /* bf16 [>= n_rows][Hkv][d] */
+  int32_t n_rows;      /* rows to append (>= 0) */
+} vc_append_req;
+
+vc_status vc_append_kv(const vc_shape* shape, vc_kv_full* full, vc_kv_comp* comp, const vc_append_req* req,
+                       int32_t residual_min, int32_t* dev_status, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------ */
 /* vc_draft_attn — one draft decode step for B requests ("Core algorithm", step 1: drafting with

@@ -1,7 +1,7 @@
 """Python binding of libvc, the GB300 (sm_103a) VeriCache draft/verify/accept hot path.
 
 Argument marshalling only: every step runs in the library's CUDA kernels. The names follow the
-C ABI in include/vc.h (vc_compress_kv, vc_draft_attn, vc_verify_attn, vc_accept,
+C ABI in include/vc.h (vc_compress_kv, vc_draft_attn, vc_verify_attn, vc_accept, vc_append_kv,
 vc_stage_full_kv, vc_workspace_size, vc_status_string). Tensors are torch tensors on the GPU;
 their data pointers and the current (or given) CUDA stream are passed through.
 
@@ -25,6 +25,7 @@ VC_DEV_OK, VC_DEV_BOUNDS, VC_DEV_TIMEOUT, VC_DEV_RANGE = range(4)
 VC_TOKEN_DROP, VC_QUANT = 0, 1
 VC_CALL_DRAFT, VC_CALL_VERIFY = 0, 1
 VC_MAX_BATCH = 32
+VC_APPEND_MAX_ROWS = 256
 
 _p = C.c_void_p
 _i32 = C.c_int32
@@ -42,11 +43,15 @@ class vc_kv_comp(C.Structure):
     _fields_ = [("mode", _i32), ("bits", _i32), ("keep", _i32), ("compact", _i32), ("idx", _p),
                 ("k_rows", _p), ("v_rows", _p), ("rows_cap", _i32), ("ng", _i32),
                 ("kc", _p), ("ks", _p), ("kz", _p), ("vc", _p), ("vs", _p), ("vz", _p),
-                ("k_win", _p), ("v_win", _p), ("win_cap", _i32), ("n_win", _i32)]
+                ("k_win", _p), ("v_win", _p), ("win_cap", _i32), ("n_win", _i32), ("ng_cap", _i32)]
 
 
 class vc_draft_req(C.Structure):
     _fields_ = [("q", _p), ("k_new", _p), ("v_new", _p), ("o", _p), ("comp", vc_kv_comp)]
+
+
+class vc_append_req(C.Structure):
+    _fields_ = [("k_rows", _p), ("v_rows", _p), ("n_rows", _i32)]
 
 
 class vc_verify_req(C.Structure):
@@ -60,6 +65,8 @@ _lib.vc_draft_attn.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_draft_req), _p,
 _lib.vc_draft_attn_noalloc.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_draft_req), _p, _p]
 _lib.vc_verify_attn.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_verify_req), _p, C.c_size_t, _p, _p]
 _lib.vc_accept.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p, _p, _p]
+_lib.vc_append_kv.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_kv_full), C.POINTER(vc_kv_comp),
+                              C.POINTER(vc_append_req), _i32, _p, _p]
 _lib.vc_stage_full_kv.argtypes = [_p, _p, C.c_size_t, C.c_size_t, _p, _p]
 _lib.vc_workspace_size.argtypes = [_i32, C.POINTER(vc_shape), _i32]
 _lib.vc_workspace_size.restype = C.c_size_t
@@ -67,11 +74,11 @@ _lib.vc_status_string.argtypes = [_i32]
 _lib.vc_status_string.restype = C.c_char_p
 _lib.vc_version.restype = _i32
 for _f in ("vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_accept",
-           "vc_stage_full_kv"):
+           "vc_stage_full_kv", "vc_append_kv"):
     getattr(_lib, _f).restype = _i32
 
 EXPORTS = ["vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_accept", "vc_stage_full_kv",
-           "vc_workspace_size", "vc_status_string", "vc_version"]
+           "vc_append_kv", "vc_workspace_size", "vc_status_string", "vc_version"]
 
 
 class VCError(RuntimeError):
@@ -153,6 +160,14 @@ def vc_accept(B: int, L_max: int, V: int, logits, draft, L, out_tokens, n_acc, s
     st = _lib.vc_accept(B, L_max, V, _ptr(logits), _ptr(draft), _ptr(L), _ptr(out_tokens), _ptr(n_acc),
                         _stream(stream))
     return _check(st, "vc_accept", raise_on_error)
+
+
+def vc_append_kv(shape: vc_shape, full, comp, req, residual_min: int, dev_status=None, stream=None,
+                 raise_on_error=True) -> int:
+    """full: vc_kv_full array [B] (ctx updated in place); comp: vc_kv_comp array [B] (ng, n_win
+    updated in place for VC_QUANT); req: vc_append_req array [B]."""
+    st = _lib.vc_append_kv(C.byref(shape), full, comp, req, residual_min, _ptr(dev_status), _stream(stream))
+    return _check(st, "vc_append_kv", raise_on_error)
 
 
 def vc_stage_full_kv(host_src, dev_dst, nbytes: int, chunk_bytes: int = 0, copy_stream=None, done=None,

@@ -344,13 +344,13 @@ __global__ void __launch_bounds__(D) quant_keys_kernel(const __grid_constant__ Q
   __half s16, z16;
   float sf, zf;
   quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
-  const size_t gi = ((size_t)h * r.ng + g) * D + c;
+  const size_t gi = ((size_t)h * r.ng_cap + g) * D + c;
   r.ks[gi] = s16;
   r.kz[gi] = z16;
 #pragma unroll
   for (int t = 0; t < 32; ++t) codes[t][c] = (uint8_t)quant_code<BITS>(x[t], sf, zf);
   __syncthreads();
-  uint32_t* dst = reinterpret_cast<uint32_t*>(r.kc + ((size_t)h * r.ng + g) * (4 * D * BITS));
+  uint32_t* dst = reinterpret_cast<uint32_t*>(r.kc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
   for (int wi = c; wi < D * BITS; wi += D) dst[wi] = block_word<D, BITS, true>(codes, wi);
 }
 
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(256) quant_values_kernel(const __grid_constant
     __half s16, z16;
     float sf, zf;
     quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
-    const size_t row = (size_t)h * (32 * r.ng) + t;
+    const size_t row = (size_t)h * (32 * r.ng_cap) + t;
     if ((lane % LPG) == 0) {
       r.vs[row * (D / 32) + c0 / 32] = s16;
       r.vz[row * (D / 32) + c0 / 32] = z16;
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(256) quant_values_kernel(const __grid_constant
     for (int e = 0; e < CPL; ++e) codes[tt][c0 + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf);
   }
   __syncthreads();
-  uint32_t* dst = reinterpret_cast<uint32_t*>(r.vc + ((size_t)h * r.ng + g) * (4 * D * BITS));
+  uint32_t* dst = reinterpret_cast<uint32_t*>(r.vc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
   for (int wi = threadIdx.x; wi < D * BITS; wi += 256) dst[wi] = block_word<D, BITS, false>(codes, wi);
 }
 
@@ -430,6 +430,137 @@ static cudaError_t launch_quant_t(const QuantParams& p, int max_ng, int max_tq, 
   }
   if (max_res > 0) copy_residual_kernel<<<dim3((max_res + 7) / 8, p.Hkv, p.B), 256, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Append after accept: grid (Hkv, B), block 256, dynamic shared memory for the extended residual.
+// Every request: KV_full rows ctx .. ctx+n-1 <- the new rows. VC_QUANT requests: the residual
+// (window rows [0, n_res)) followed by the new rows is staged in shared memory; its first
+// 32 * (ng_new - ng) rows become blocks ng .. ng_new-1 by the same arithmetic and word order as
+// quant_keys_kernel / quant_values_kernel, and the rest is written back as the new window. One CTA
+// owns a (request, head), so the window is rewritten from its staged copy without hazards.
+constexpr int kAppendThreads = 256;
+
+template <int D, int BITS>
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_constant__ AppendParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const AppendReq& r = p.req[blockIdx.y];
+  const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = r.n_rows;
+  if (n <= 0) return;
+  constexpr int V16 = D * 2 / 16;  // 16-byte pieces of a bf16 row
+  for (int e = tid; e < n * 2 * V16; e += kAppendThreads) {
+    const int i = e / (2 * V16), q = e % (2 * V16);
+    const bool isv = q >= V16;
+    const uint4* src = reinterpret_cast<const uint4*>((isv ? r.v_rows : r.k_rows) + ((size_t)i * p.Hkv + h) * D);
+    uint4* dst = reinterpret_cast<uint4*>((isv ? r.v_full : r.k_full) + ((size_t)h * r.cap + r.ctx + i) * D);
+    dst[q % V16] = __ldg(src + q % V16);
+  }
+  if (!r.quant) return;
+  extern __shared__ uint4 ext_raw[];
+  const int n_res = r.ctx - VC_GROUP * r.ng, n_ext = n_res + n;
+  bf16* ek = reinterpret_cast<bf16*>(ext_raw);  // [n_ext][D] keys, then [n_ext][D] values
+  bf16* ev = ek + (size_t)n_ext * D;
+  for (int e = tid; e < n_ext * 2 * V16; e += kAppendThreads) {
+    const int j = e / (2 * V16), q = e % (2 * V16);
+    const bool isv = q >= V16;
+    const bf16* row = j < n_res ? (isv ? r.v_win : r.k_win) + ((size_t)h * r.win_cap + j) * D
+                                : (isv ? r.v_rows : r.k_rows) + ((size_t)(j - n_res) * p.Hkv + h) * D;
+    reinterpret_cast<uint4*>((isv ? ev : ek) + (size_t)j * D)[q % V16] = reinterpret_cast<const uint4*>(row)[q % V16];
+  }
+  __syncthreads();
+  __shared__ uint8_t codes[32][D];
+  constexpr int CPL = D / 32;    // channels per lane (values)
+  constexpr int LPG = 32 / CPL;  // lanes per 32-channel group
+  for (int gi = 0; gi < r.ng_new - r.ng; ++gi) {
+    const int g = r.ng + gi;
+    const bf16* kb = ek + (size_t)(VC_GROUP * gi) * D;
+    const bf16* vb = ev + (size_t)(VC_GROUP * gi) * D;
+    // keys: thread c quantises channel c over the block's 32 tokens
+    if (tid < D) {
+      const int c = tid;
+      float x[32];
+      float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        x[t] = __bfloat162float(kb[(size_t)t * D + c]);
+        mn = fminf(mn, x[t]);
+        mx = fmaxf(mx, x[t]);
+      }
+      __half s16, z16;
+      float sf, zf;
+      quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
+      const size_t gidx = ((size_t)h * r.ng_cap + g) * D + c;
+      r.ks[gidx] = s16;
+      r.kz[gidx] = z16;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) codes[t][c] = (uint8_t)quant_code<BITS>(x[t], sf, zf);
+    }
+    __syncthreads();
+    uint32_t* kdst = reinterpret_cast<uint32_t*>(r.kc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
+    for (int wi = tid; wi < D * BITS; wi += kAppendThreads) kdst[wi] = block_word<D, BITS, true>(codes, wi);
+    __syncthreads();
+    // values: warp w quantises tokens w, w+8, w+16, w+24; lane l channels CPL*l .. CPL*l+CPL-1
+    const int c0 = CPL * lane;
+    for (int tt = warp; tt < 32; tt += kAppendThreads / 32) {
+      float x[CPL];
+      float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) {
+        x[e] = __bfloat162float(vb[(size_t)tt * D + c0 + e]);
+        mn = fminf(mn, x[e]);
+        mx = fmaxf(mx, x[e]);
+      }
+#pragma unroll
+      for (int off = 1; off < LPG; off <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      }
+      __half s16, z16;
+      float sf, zf;
+      quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
+      const size_t row = (size_t)h * (VC_GROUP * (size_t)r.ng_cap) + VC_GROUP * g + tt;
+      if ((lane % LPG) == 0) {
+        r.vs[row * (D / 32) + c0 / 32] = s16;
+        r.vz[row * (D / 32) + c0 / 32] = z16;
+      }
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) codes[tt][c0 + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf);
+    }
+    __syncthreads();
+    uint32_t* vdst = reinterpret_cast<uint32_t*>(r.vc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
+    for (int wi = tid; wi < D * BITS; wi += kAppendThreads) vdst[wi] = block_word<D, BITS, false>(codes, wi);
+    __syncthreads();
+  }
+  // the new residual: staged rows [32 * (ng_new - ng), n_ext) -> window rows [0, ...)
+  const int sh = VC_GROUP * (r.ng_new - r.ng);
+  for (int e = tid; e < (n_ext - sh) * 2 * V16; e += kAppendThreads) {
+    const int j = e / (2 * V16), q = e % (2 * V16);
+    const bool isv = q >= V16;
+    uint4* dst = reinterpret_cast<uint4*>((isv ? r.v_win : r.k_win) + ((size_t)h * r.win_cap + j) * D);
+    dst[q % V16] = reinterpret_cast<const uint4*>((isv ? ev : ek) + (size_t)(sh + j) * D)[q % V16];
+  }
+}
+
+template <int D, int BITS>
+static cudaError_t launch_append_t(const AppendParams& p, int max_ext_rows, cudaStream_t s) {
+  const size_t smem = (size_t)(max_ext_rows > 0 ? max_ext_rows : 1) * 2 * D * sizeof(bf16);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(append_kernel<D, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         VC_APPEND_MAX_ROWS * 2 * D * (int)sizeof(bf16));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(append_kernel<D, BITS>, dim3(p.Hkv, p.B), dim3(kAppendThreads), smem, s, p);
+}
+
+cudaError_t launch_append(const AppendParams& p, int max_ext_rows, cudaStream_t s) {
+  const int bits = p.bits == 4 ? 4 : 2;  // token-drop-only calls take the 2-bit instance (no blocks)
+  if (p.d == 128) return bits == 2 ? launch_append_t<128, 2>(p, max_ext_rows, s) : launch_append_t<128, 4>(p, max_ext_rows, s);
+  if (p.d == 64) return bits == 2 ? launch_append_t<64, 2>(p, max_ext_rows, s) : launch_append_t<64, 4>(p, max_ext_rows, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_quant(const QuantParams& p, int max_ng, int max_tq, cudaStream_t s) {

@@ -593,12 +593,12 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       if constexpr (!BF16_ROWS) {
         // one quantised 32-token group: six contiguous runs
         const int g = lc;
-        const int Tq = 32 * r.ng;
+        const int Tq = 32 * r.ng_cap;  // the head stride of the value scales (blocks can be appended)
         if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::QRAW);
         __syncwarp();
-        if (lane == 0) bulk_g2s_hint(sb + C::OFF_KC, r.kc + ((size_t)hk * r.ng + g) * C::KCB, C::KCB, &bars[st], stream_pol);
-        if (lane == 1) bulk_g2s_hint(sb + C::OFF_KS, r.ks + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st], stream_pol);
-        if (lane == 2) bulk_g2s_hint(sb + C::OFF_KZ, r.kz + ((size_t)hk * r.ng + g) * D, 2 * D, &bars[st], stream_pol);
+        if (lane == 0) bulk_g2s_hint(sb + C::OFF_KC, r.kc + ((size_t)hk * r.ng_cap + g) * C::KCB, C::KCB, &bars[st], stream_pol);
+        if (lane == 1) bulk_g2s_hint(sb + C::OFF_KS, r.ks + ((size_t)hk * r.ng_cap + g) * D, 2 * D, &bars[st], stream_pol);
+        if (lane == 2) bulk_g2s_hint(sb + C::OFF_KZ, r.kz + ((size_t)hk * r.ng_cap + g) * D, 2 * D, &bars[st], stream_pol);
         if (lane == 3)
           bulk_g2s_hint(sb + C::OFF_VC, r.vc + ((size_t)hk * Tq + 32 * g) * (D * C::BITS / 8), C::KCB, &bars[st], stream_pol);
         if (lane == 4) bulk_g2s_hint(sb + C::OFF_VS, r.vs + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st], stream_pol);

@@ -54,8 +54,9 @@ static int draft_ctas_per_head_max(int Hkv, int G = 1) {
 static size_t draft_counter_bytes(int Hkv) { return ((size_t)Hkv * VC_MAX_BATCH * 4 + 255) / 256 * 256; }
 
 // Last library operation launched on each stream. A draft step may start streaming before the
-// kernel ahead of it in the stream finishes unless that kernel is a compress (the only writer of
-// kept rows and indices that triggers its dependents early).
+// kernel ahead of it in the stream finishes unless that kernel writes KV_comp (a compress or an
+// append after accept: the only writers of kept rows, indices and quantised blocks among the
+// library's kernels, all of which trigger their dependents early).
 enum { kOpNone = 0, kOpCompress = 1, kOpDraft = 2, kOpVerify = 3, kOpAccept = 4 };
 static std::mutex g_op_mu;
 static std::unordered_map<cudaStream_t, int> g_last_op;
@@ -175,6 +176,7 @@ vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const fl
     if (c.bits != bits) return VC_ERR_UNSUPPORTED;
     const int ng = f.ctx > residual_min ? (f.ctx - residual_min) / VC_GROUP : 0;
     const int n_res = f.ctx - VC_GROUP * ng;
+    if (ng > c.ng_cap) return VC_ERR_INVALID;  // the buffers hold ng_cap blocks per head
     if (ng > 0 && (!aligned16(c.kc) || !aligned16(c.ks) || !aligned16(c.kz) || !aligned16(c.vc) ||
                    !aligned16(c.vs) || !aligned16(c.vz)))
       return VC_ERR_INVALID;
@@ -185,6 +187,7 @@ vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const fl
     r.cap = f.cap;
     r.ctx = f.ctx;
     r.ng = ng;
+    r.ng_cap = c.ng_cap;
     r.n_res = n_res;
     r.kc = c.kc;
     r.ks = reinterpret_cast<__half*>(c.ks);
@@ -202,6 +205,82 @@ vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const fl
   for (int b = 0; b < B; ++b) {
     comp[b].ng = qp.req[b].ng;
     comp[b].n_win = qp.req[b].n_res;
+  }
+  return VC_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+vc_status vc_append_kv(const vc_shape* shape, vc_kv_full* full, vc_kv_comp* comp, const vc_append_req* req,
+                       int32_t residual_min, int32_t* dev_status, cudaStream_t stream) {
+  if (!shape_ok(shape) || !full || !comp || !req || residual_min < 0) return VC_ERR_INVALID;
+  const int B = shape->B, d = shape->d;
+  AppendParams ap;
+  memset(&ap, 0, sizeof(ap));
+  ap.B = B;
+  ap.Hkv = shape->Hkv;
+  ap.d = d;
+  ap.bits = 0;
+  ap.dev_status = dev_status;
+  int max_ext = 0, ng_new[VC_MAX_BATCH], n_win_new[VC_MAX_BATCH];
+  bool any = false;
+  for (int b = 0; b < B; ++b) {
+    const vc_append_req& q = req[b];
+    const vc_kv_full& f = full[b];
+    const vc_kv_comp& c = comp[b];
+    if (q.n_rows < 0) return VC_ERR_INVALID;
+    if (q.n_rows > 0 && (!aligned16(q.k_rows) || !aligned16(q.v_rows))) return VC_ERR_INVALID;
+    if (!aligned16(f.k) || !aligned16(f.v) || f.ctx < 1 || (int64_t)f.ctx + q.n_rows > f.cap) return VC_ERR_INVALID;
+    AppendReq& r = ap.req[b];
+    r.k_rows = static_cast<const bf16*>(q.k_rows);
+    r.v_rows = static_cast<const bf16*>(q.v_rows);
+    r.n_rows = q.n_rows;
+    r.k_full = static_cast<bf16*>(const_cast<void*>(f.k));
+    r.v_full = static_cast<bf16*>(const_cast<void*>(f.v));
+    r.cap = f.cap;
+    r.ctx = f.ctx;
+    r.quant = c.mode == VC_QUANT;
+    ng_new[b] = c.ng;
+    n_win_new[b] = c.n_win;
+    if (r.quant) {
+      if (c.bits != 2 && c.bits != 4) return VC_ERR_UNSUPPORTED;
+      if (ap.bits == 0) ap.bits = c.bits;
+      if (c.bits != ap.bits) return VC_ERR_UNSUPPORTED;
+      const int ctx2 = f.ctx + q.n_rows;
+      const int ng2 = ctx2 > residual_min ? (ctx2 - residual_min) / VC_GROUP : 0;
+      const int n_res = f.ctx - VC_GROUP * c.ng, n_ext = n_res + q.n_rows;
+      if (c.ng < 0 || ng2 < c.ng || ng2 > c.ng_cap || n_res < 0 || n_res > c.win_cap) return VC_ERR_INVALID;
+      if (n_ext > VC_APPEND_MAX_ROWS) return VC_ERR_UNSUPPORTED;
+      if (n_ext - VC_GROUP * (ng2 - c.ng) > c.win_cap) return VC_ERR_INVALID;
+      if (ng2 > 0 && (!aligned16(c.kc) || !aligned16(c.ks) || !aligned16(c.kz) || !aligned16(c.vc) ||
+                      !aligned16(c.vs) || !aligned16(c.vz)))
+        return VC_ERR_INVALID;
+      if (!aligned16(c.k_win) || !aligned16(c.v_win)) return VC_ERR_INVALID;
+      r.ng = c.ng;
+      r.ng_new = ng2;
+      r.ng_cap = c.ng_cap;
+      r.kc = c.kc;
+      r.ks = reinterpret_cast<__half*>(c.ks);
+      r.kz = reinterpret_cast<__half*>(c.kz);
+      r.vc = c.vc;
+      r.vs = reinterpret_cast<__half*>(c.vs);
+      r.vz = reinterpret_cast<__half*>(c.vz);
+      r.k_win = static_cast<bf16*>(c.k_win);
+      r.v_win = static_cast<bf16*>(c.v_win);
+      r.win_cap = c.win_cap;
+      if (q.n_rows > 0 && n_ext > max_ext) max_ext = n_ext;
+      ng_new[b] = ng2;
+      n_win_new[b] = n_ext - VC_GROUP * (ng2 - c.ng);
+    }
+    any |= q.n_rows > 0;
+  }
+  if (!any) return VC_OK;
+  if (launch_append(ap, max_ext, stream) != cudaSuccess) return VC_ERR_CUDA;
+  // it rewrites KV_comp and KV_full: a draft step after it must not start before it finishes
+  set_last_op(stream, kOpCompress);
+  for (int b = 0; b < B; ++b) {
+    full[b].ctx += req[b].n_rows;
+    comp[b].ng = ng_new[b];
+    comp[b].n_win = n_win_new[b];
   }
   return VC_OK;
 }
@@ -242,7 +321,7 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
       if (c.compact && c.keep > c.rows_cap) return VC_ERR_INVALID;
       n_main = c.keep;
     } else {
-      if (c.ng < 0) return VC_ERR_INVALID;
+      if (c.ng < 0 || c.ng > c.ng_cap) return VC_ERR_INVALID;
       if (c.ng > 0 && (!aligned16(c.kc) || !aligned16(c.ks) || !aligned16(c.kz) || !aligned16(c.vc) ||
                        !aligned16(c.vs) || !aligned16(c.vz)))
         return VC_ERR_INVALID;
@@ -266,6 +345,7 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
     r.vs = reinterpret_cast<const __half*>(c.vs);
     r.vz = reinterpret_cast<const __half*>(c.vz);
     r.ng = c.ng;
+    r.ng_cap = c.ng_cap;
     r.k_win = static_cast<bf16*>(c.k_win);
     r.v_win = static_cast<bf16*>(c.v_win);
     r.win_cap = c.win_cap;

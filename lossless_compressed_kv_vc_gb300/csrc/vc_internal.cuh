@@ -199,6 +199,7 @@ struct DraftReqDev {
   const __half* vs;
   const __half* vz;
   int32_t ng;
+  int32_t ng_cap;       // head stride of the quantised buffers, in blocks
   // window
   bf16* k_win;
   bf16* v_win;
@@ -284,6 +285,7 @@ struct QuantReq {
   const bf16* v;
   int64_t cap;
   int32_t ctx, ng, n_res;
+  int32_t ng_cap;  // head stride of the quantised buffers, in blocks
   uint8_t* kc;
   __half* ks;
   __half* kz;
@@ -300,5 +302,35 @@ struct QuantParams {
   int32_t* dev_status;
 };
 cudaError_t launch_quant(const QuantParams& p, int max_ng, int max_tq, cudaStream_t s);
+
+// Append accepted drafted rows to KV_full and, for quantised caches, quantise the blocks that
+// became whole and rewrite the residual window (one CTA per request and KV head).
+struct AppendReq {
+  const bf16* k_rows;  // [n_rows][Hkv][d]
+  const bf16* v_rows;
+  int32_t n_rows;
+  bf16* k_full;        // [Hkv][cap][d]
+  bf16* v_full;
+  int64_t cap;
+  int32_t ctx;         // before the append
+  int32_t quant;       // 1: VC_QUANT request
+  int32_t ng, ng_new;  // quantised blocks before / after
+  int32_t ng_cap;
+  uint8_t* kc;
+  __half* ks;
+  __half* kz;
+  uint8_t* vc;
+  __half* vs;
+  __half* vz;
+  bf16* k_win;
+  bf16* v_win;
+  int64_t win_cap;
+};
+struct AppendParams {
+  AppendReq req[VC_MAX_BATCH];
+  int32_t B, Hkv, d, bits;
+  int32_t* dev_status;
+};
+cudaError_t launch_append(const AppendParams& p, int max_ext_rows, cudaStream_t s);
 
 }  // namespace vc

@@ -2,8 +2,9 @@
 
 A `Batch` owns the device tensors a round needs (full cache, compressed cache, window, outputs)
 and fills the vc.h descriptors that point at them; its methods are one C-ABI call each:
-compress -> L x draft_step -> verify -> accept ("VeriCache: Turning Lossy KV Cache into Lossless
-LLM Inference", "Core algorithm"). torch is used for memory and streams only.
+compress -> L x draft_step -> verify -> accept, then append_accepted to carry the accepted tokens
+into the next round ("VeriCache: Turning Lossy KV Cache into Lossless LLM Inference", "Core
+algorithm"). torch is used for memory and streams only.
 """
 from __future__ import annotations
 
@@ -12,9 +13,9 @@ from typing import List, Optional
 
 import torch
 
-from . import (vc_shape, vc_kv_full, vc_kv_comp, vc_draft_req, vc_verify_req, vc_compress_kv, vc_draft_attn,
-               vc_verify_attn, vc_accept, vc_workspace_size, VC_TOKEN_DROP, VC_QUANT, VC_CALL_DRAFT,
-               VC_CALL_VERIFY)
+from . import (vc_shape, vc_kv_full, vc_kv_comp, vc_draft_req, vc_verify_req, vc_append_req, vc_compress_kv,
+               vc_draft_attn, vc_verify_attn, vc_accept, vc_append_kv, vc_workspace_size, VC_TOKEN_DROP, VC_QUANT,
+               VC_CALL_DRAFT, VC_CALL_VERIFY)
 
 GROUP = 32
 
@@ -40,6 +41,7 @@ class Req:
     recent: int = 0
     compact: bool = False
     bits: int = 2
+    grow: int = 0                   # tokens the context may gain through append_accepted
     # owned buffers
     idx: Optional[torch.Tensor] = None
     k_rows: Optional[torch.Tensor] = None
@@ -93,15 +95,21 @@ class Batch:
         else:
             ng, n_res = quant_layout(r.ctx, self.residual_min)
             r.n_res = n_res
+            # room for the blocks the context fills as it grows by up to r.grow tokens
+            ng_cap = max(quant_layout(r.ctx + r.grow, self.residual_min)[0], 1)
             b = r.bits
             u8, f16 = torch.uint8, torch.float16
-            r.kc = torch.empty((Hkv, max(ng, 1), 4 * d * b), dtype=u8, device=dev)
-            r.ks = torch.empty((Hkv, max(ng, 1), d), dtype=f16, device=dev)
-            r.kz = torch.empty((Hkv, max(ng, 1), d), dtype=f16, device=dev)
-            r.vc = torch.empty((Hkv, max(ng, 1), 4 * d * b), dtype=u8, device=dev)
-            r.vs = torch.empty((Hkv, max(32 * ng, 1), d // 32), dtype=f16, device=dev)
-            r.vz = torch.empty((Hkv, max(32 * ng, 1), d // 32), dtype=f16, device=dev)
-        win_cap = r.n_res + r.L + 1
+            r.kc = torch.empty((Hkv, ng_cap, 4 * d * b), dtype=u8, device=dev)
+            r.ks = torch.empty((Hkv, ng_cap, d), dtype=f16, device=dev)
+            r.kz = torch.empty((Hkv, ng_cap, d), dtype=f16, device=dev)
+            r.vc = torch.empty((Hkv, ng_cap, 4 * d * b), dtype=u8, device=dev)
+            r.vs = torch.empty((Hkv, GROUP * ng_cap, d // 32), dtype=f16, device=dev)
+            r.vz = torch.empty((Hkv, GROUP * ng_cap, d // 32), dtype=f16, device=dev)
+        # the residual never exceeds residual_min + 31 rows once the context passes residual_min
+        res_max = r.n_res
+        if r.mode == VC_QUANT and r.grow > 0:
+            res_max = max(r.n_res, min(r.ctx + r.grow, self.residual_min + GROUP - 1))
+        win_cap = res_max + r.L + 1
         r.k_win = torch.zeros((Hkv, win_cap, d), dtype=torch.bfloat16, device=dev)
         r.v_win = torch.zeros((Hkv, win_cap, d), dtype=torch.bfloat16, device=dev)
         r.o_draft = torch.empty((r.L, self.Hq, d), dtype=torch.bfloat16, device=dev)
@@ -123,6 +131,7 @@ class Batch:
         else:
             c.kc, c.ks, c.kz = r.kc.data_ptr(), r.ks.data_ptr(), r.kz.data_ptr()
             c.vc, c.vs, c.vz = r.vc.data_ptr(), r.vs.data_ptr(), r.vz.data_ptr()
+            c.ng_cap = r.kc.shape[1]
         c.k_win, c.v_win, c.win_cap = r.k_win.data_ptr(), r.v_win.data_ptr(), r.k_win.shape[1]
 
     def set_full(self, b: int, k: torch.Tensor, v: torch.Tensor):
@@ -180,11 +189,13 @@ class Batch:
                 arr[i].comp.n_win = self.reqs[b].n_res + s
             self._steps.append((vc_shape(len(act), self.Hq, self.Hkv, self.d), arr, act))
 
-    def run_round(self, logits, draft, L, out_tokens, n_acc, stream=None, draft_events=None):
+    def run_round(self, logits, draft, L, out_tokens, n_acc, stream=None, draft_events=None, compress=True):
         """compress -> L_max draft steps -> verify -> accept, all on `stream`. draft_events, if
         given, is a (start, end) pair of CUDA events recorded around the whole draft phase (an
-        event between two draft steps would hold back the next step's early start)."""
-        self.compress(stream)
+        event between two draft steps would hold back the next step's early start). compress=False
+        drafts from the caches as they stand (quantised caches kept current by append_accepted)."""
+        if compress:
+            self.compress(stream)
         if draft_events is not None:
             draft_events[0].record(stream)
         for s, (shape, arr, act) in enumerate(self._steps):
@@ -227,6 +238,25 @@ class Batch:
         with torch.cuda.stream(stream):
             hr.host_tokens.copy_(hr.out_tokens, non_blocking=True)
             hr.host_n_acc.copy_(hr.n_acc, non_blocking=True)
+
+    def append_accepted(self, n_acc, stream=None):
+        """Carry a round's accepted drafts into the caches ("Core algorithm": the next round
+        starts after the last accepted token). n_acc: host sequence of accepted counts per request
+        (accepted drafts + the bonus/correction token). The n_acc - 1 accepted drafts' K/V (this
+        round's k_new/v_new rows) are appended to KV_full and, for quantised requests, the blocks
+        that became whole are quantised and the window restarts with the new residual. The bonus
+        token's K/V belongs to the next round. The round's descriptor arrays are rebuilt."""
+        arr = (vc_append_req * len(self.reqs))()
+        for b, r in enumerate(self.reqs):
+            n = max(0, min(int(n_acc[b]) - 1, r.L))
+            arr[b].k_rows, arr[b].v_rows, arr[b].n_rows = r.k_new.data_ptr(), r.v_new.data_ptr(), n
+        vc_append_kv(self.shape, self.full, self.comp, arr, self.residual_min, self.dev_status, stream)
+        for b, r in enumerate(self.reqs):
+            r.ctx = self.full[b].ctx
+            if r.mode == VC_QUANT:
+                r.n_res = r.ctx - GROUP * self.comp[b].ng
+        if getattr(self, "_steps", None) is not None:
+            self.prepare_steps()
 
     def verify_requests(self):
         arr = (vc_verify_req * len(self.reqs))()

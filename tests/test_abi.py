@@ -29,7 +29,7 @@ def declared_symbols():
 
 def test_header_declares_the_round_calls():
     names = declared_symbols()
-    for n in ["vc_compress_kv", "vc_draft_attn", "vc_verify_attn", "vc_accept", "vc_stage_full_kv",
+    for n in ["vc_compress_kv", "vc_draft_attn", "vc_verify_attn", "vc_accept", "vc_stage_full_kv", "vc_append_kv",
               "vc_workspace_size", "vc_status_string"]:
         assert n in names
 
@@ -63,3 +63,32 @@ def test_validation_rejects_without_launching(lib):
     assert vc.vc_workspace_size(vc.VC_CALL_DRAFT, bad) == 0
     ok = vc.vc_shape(8, 32, 8, 128)
     assert vc.vc_workspace_size(vc.VC_CALL_DRAFT, ok) > 0
+
+
+def test_append_validation_rejects_without_launching(lib):
+    """vc_append_kv checks capacities before launching; a call with nothing to append launches
+    nothing and succeeds. The pointers are fake (aligned, never dereferenced on these paths)."""
+    import lossless_compressed_kv_vc_gb300 as vc
+    shp = vc.vc_shape(1, 8, 2, 64)
+
+    def call(ctx, cap, n, quant=False, ng=0, ng_cap=0, bits=2, win_cap=512):
+        full = (vc.vc_kv_full * 1)()
+        full[0].k, full[0].v, full[0].ctx, full[0].cap = 1 << 12, 1 << 13, ctx, cap
+        comp = (vc.vc_kv_comp * 1)()
+        c = comp[0]
+        c.mode, c.bits, c.ng, c.ng_cap, c.win_cap, c.n_win = (vc.VC_QUANT if quant else vc.VC_TOKEN_DROP), bits, ng, \
+            ng_cap, win_cap, 0
+        for f in ("kc", "ks", "kz", "vc", "vs", "vz", "k_win", "v_win", "idx"):
+            setattr(c, f, 1 << 14)
+        req = (vc.vc_append_req * 1)()
+        req[0].k_rows, req[0].v_rows, req[0].n_rows = 1 << 15, 1 << 16, n
+        st = vc.vc_append_kv(shp, full, comp, req, 128, None, stream=0, raise_on_error=False)
+        return st, full[0].ctx
+    assert call(100, 110, 11) == (vc.VC_ERR_INVALID, 100)                 # past KV_full's capacity
+    assert call(100, 110, -1)[0] == vc.VC_ERR_INVALID
+    assert call(100, 110, 0) == (vc.VC_OK, 100)                           # nothing to do
+    assert call(300, 1000, 0, quant=True, ng=5, ng_cap=5) == (vc.VC_OK, 300)
+    assert call(300, 1000, 32, quant=True, ng=5, ng_cap=5)[0] == vc.VC_ERR_INVALID   # needs block 6
+    assert call(300, 1000, 117, quant=True, ng=5, ng_cap=50)[0] == vc.VC_ERR_UNSUPPORTED  # 140+117 rows
+    assert call(300, 1000, 8, quant=True, ng=5, ng_cap=50, bits=3)[0] == vc.VC_ERR_UNSUPPORTED
+    assert call(300, 1000, 8, quant=True, ng=5, ng_cap=50, win_cap=100)[0] == vc.VC_ERR_INVALID  # residual > window

@@ -6,7 +6,7 @@ import torch
 
 import oracle as O
 from workloads import configs, gen
-from tests.util import make_batch, f32
+from tests.util import make_batch, f32, assert_quant_state
 
 pytestmark = pytest.mark.gpu
 
@@ -72,18 +72,7 @@ def _quant_case(w, reqs):
     assert int(bt.dev_status.item()) == 0
     for i, b in enumerate(reqs):
         r = bt.reqs[i]
-        ref = O.quantize_kv(f32(r.k_full), f32(r.v_full), w.bits, w.residual_min)
-        ng = ref["ng"]
-        assert bt.comp[i].ng == ng and bt.comp[i].n_win == ref["n_res"]
-        if ng > 0:
-            assert np.array_equal(r.kc[:, :ng].cpu().numpy(), ref["kc"])
-            assert np.array_equal(r.ks[:, :ng].cpu().numpy().view(np.uint16), ref["ks"].view(np.uint16))
-            assert np.array_equal(r.kz[:, :ng].cpu().numpy().view(np.uint16), ref["kz"].view(np.uint16))
-            assert np.array_equal(r.vc[:, :ng].cpu().numpy(), ref["vc"])
-            assert np.array_equal(r.vs[:, : 32 * ng].cpu().numpy().view(np.uint16), ref["vs"].view(np.uint16))
-            assert np.array_equal(r.vz[:, : 32 * ng].cpu().numpy().view(np.uint16), ref["vz"].view(np.uint16))
-        assert np.array_equal(f32(r.k_win[:, : ref["n_res"]]), ref["k_res"])
-        assert np.array_equal(f32(r.v_win[:, : ref["n_res"]]), ref["v_res"])
+        assert_quant_state(bt, i, f32(r.k_full), f32(r.v_full), w.bits, w.residual_min)
 
 
 def test_quant2_qwen_shape_scaled():

@@ -29,21 +29,51 @@ def assert_attn_close(gpu, ref, what=""):
     return float(err.max())
 
 
-def make_batch(w, reqs, rnd=0, device="cuda", compact=False):
-    """Engine Batch for requests `reqs` of workload w, inputs from the seeded generator."""
+def make_batch(w, reqs, rnd=0, device="cuda", compact=False, grow=0):
+    """Engine Batch for requests `reqs` of workload w, inputs from the seeded generator. With
+    grow > 0 each KV_full (and importance array) has room for `grow` more tokens."""
     from lossless_compressed_kv_vc_gb300 import engine, VC_TOKEN_DROP, VC_QUANT
     rs = []
     for b in reqs:
         ri = gen.request(w, rnd, b, device)
+        kf, vf, imp = ri.k_full, ri.v_full, ri.importance
+        if grow > 0:
+            kf = torch.zeros((w.Hkv, w.ctx[b] + grow, w.d), dtype=torch.bfloat16, device=device)
+            vf = torch.zeros_like(kf)
+            kf[:, : w.ctx[b]] = ri.k_full
+            vf[:, : w.ctx[b]] = ri.v_full
+            if imp is not None:
+                imp = gen.importance(w, b, device, n=w.ctx[b] + grow)
         mode = VC_TOKEN_DROP if w.mode[b] == DROP else VC_QUANT
-        rs.append(engine.Req(mode=mode, ctx=w.ctx[b], L=w.L[b], k_full=ri.k_full, v_full=ri.v_full, q=ri.q,
-                             k_new=ri.k_new, v_new=ri.v_new, importance=ri.importance, keep=w.keep[b],
-                             recent=w.recent[b], compact=compact, bits=w.bits))
+        rs.append(engine.Req(mode=mode, ctx=w.ctx[b], L=w.L[b], k_full=kf, v_full=vf, q=ri.q,
+                             k_new=ri.k_new, v_new=ri.v_new, importance=imp, keep=w.keep[b],
+                             recent=w.recent[b], compact=compact, bits=w.bits, grow=grow))
     return engine.Batch(w.Hq, w.Hkv, w.d, rs, residual_min=w.residual_min, device=device)
 
 
 def f32(t):
     return t.detach().to("cpu").to(torch.float32).numpy()
+
+
+def assert_quant_state(bt, i, kf, vf, bits, residual_min):
+    """Request i of Batch bt holds, bit for bit, the oracle's quantisation of the float32 cache
+    kf, vf [Hkv][ctx][d]: block count, codes, fp16 scales and zeros, and the residual window."""
+    import oracle as O
+    r, c = bt.reqs[i], bt.comp[i]
+    ref = O.quantize_kv(kf, vf, bits, residual_min)
+    ng = ref["ng"]
+    assert (c.ng, c.n_win) == (ng, ref["n_res"]), (c.ng, c.n_win, ng, ref["n_res"])
+    if ng > 0:
+        u16 = lambda t: t.cpu().numpy().view(np.uint16)
+        assert np.array_equal(r.kc[:, :ng].cpu().numpy(), ref["kc"])
+        assert np.array_equal(u16(r.ks[:, :ng]), ref["ks"].view(np.uint16))
+        assert np.array_equal(u16(r.kz[:, :ng]), ref["kz"].view(np.uint16))
+        assert np.array_equal(r.vc[:, :ng].cpu().numpy(), ref["vc"])
+        assert np.array_equal(u16(r.vs[:, : 32 * ng]), ref["vs"].view(np.uint16))
+        assert np.array_equal(u16(r.vz[:, : 32 * ng]), ref["vz"].view(np.uint16))
+    assert np.array_equal(f32(r.k_win[:, : ref["n_res"]]), ref["k_res"])
+    assert np.array_equal(f32(r.v_win[:, : ref["n_res"]]), ref["v_res"])
+    return ref
 
 
 def oracle_main(w, b, k_full_f32, v_full_f32, importance=None):

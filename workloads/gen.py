@@ -26,7 +26,7 @@ import torch
 
 from .configs import Workload, DROP
 
-KIND_K, KIND_V, KIND_IMP, KIND_Q, KIND_KNEW, KIND_VNEW, KIND_DRAFT, KIND_LOGITS, KIND_PLANT = range(9)
+KIND_K, KIND_V, KIND_IMP, KIND_Q, KIND_KNEW, KIND_VNEW, KIND_DRAFT, KIND_LOGITS, KIND_PLANT, KIND_APPK, KIND_APPV = range(11)
 
 
 def _gen(w: Workload, rnd: int, b: int, kind: int, device) -> torch.Generator:
@@ -56,9 +56,17 @@ def full_kv(w: Workload, b: int, device="cpu"):
             randn_bf16(shape, _gen(w, 0, b, KIND_V, device), device))
 
 
-def importance(w: Workload, b: int, device="cpu") -> torch.Tensor:
+def importance(w: Workload, b: int, device="cpu", n: int | None = None) -> torch.Tensor:
+    """fp32 [n] ~ U[0,1) (n defaults to the context; a longer array serves a context that grows)."""
     g = _gen(w, 0, b, KIND_IMP, device)
-    return torch.rand((w.ctx[b],), generator=g, device=device, dtype=torch.float32)
+    return torch.rand((w.ctx[b] if n is None else n,), generator=g, device=device, dtype=torch.float32)
+
+
+def appended_rows(w: Workload, rnd: int, b: int, n: int, device="cpu"):
+    """(k, v) bf16 [n][Hkv][d] ~ N(0,1): rows a request's cache gains after round rnd."""
+    shape = (n, w.Hkv, w.d)
+    return (randn_bf16(shape, _gen(w, rnd, b, KIND_APPK, device), device),
+            randn_bf16(shape, _gen(w, rnd, b, KIND_APPV, device), device))
 
 
 def round_queries(w: Workload, rnd: int, b: int, device="cpu"):
