@@ -55,6 +55,11 @@ def parse():
                     help="gather the kept rows into a contiguous copy at compress time (inside the timed round)")
     ap.add_argument("--batch", type=int, default=None,
                     help="run only the first B requests (a smaller case for profiler captures)")
+    ap.add_argument("--head-chunks", type=int, default=1,
+                    help="offload workload: stage KV_full in this many KV-head ranges and verify each range as "
+                         "soon as it lands (1 = stage the whole group, then verify)")
+    ap.add_argument("--draft-steps", type=int, default=None,
+                    help="offload workload: drafts per round (default: the workload's L)")
     a = ap.parse_args()
     global _BATCH
     _BATCH = a.batch
@@ -420,8 +425,8 @@ def run_offload(args):
     from lossless_compressed_kv_vc_gb300 import engine, VC_QUANT, vc_stage_full_kv
     from workloads import configs, gen
     w = configs.llama70b_offload4()
-    if args.ctx_div > 1:
-        w = configs.scaled(w, ctx_div=args.ctx_div)
+    if args.ctx_div > 1 or args.draft_steps is not None:
+        w = configs.scaled(w, ctx_div=args.ctx_div, L=args.draft_steps)
     device = "cuda"
     groups = []
     for grp in ([0, 1], [2, 3]):
@@ -444,7 +449,7 @@ def run_offload(args):
                    torch.empty((2, w.L_max + 1), dtype=torch.int32, device=device),
                    torch.empty((2,), dtype=torch.int32, device=device)))
     cs, ks = torch.cuda.Stream(), torch.cuda.Stream()
-    sg = engine.StaggeredOffload(groups, host_kv, slots, cs, ks)
+    sg = engine.StaggeredOffload(groups, host_kv, slots, cs, ks, head_chunks=args.head_chunks)
     mk = lambda: [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
     stage_bytes = sum(h.numel() * h.element_size() for h in host_kv[0])
     # host link alone: one group's KV_full, nothing else running
@@ -463,6 +468,8 @@ def run_offload(args):
         sg.period(io)
     torch.cuda.synchronize()
     evs = [{k: mk() for k in ("draft0", "draft1", "stage0", "stage1")} for _ in range(args.steps)]
+    for ev in evs:
+        ev["verified0"], ev["verified1"] = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0, e1 = mk()
     with ClockSampler(0) as clk:
         torch.cuda.synchronize()
@@ -483,6 +490,13 @@ def run_offload(args):
             draft_iv.append((e0.elapsed_time(ev[dk][0]), e0.elapsed_time(ev[dk][1])))
         for sk in ("stage0", "stage1"):
             copy_iv.append((e0.elapsed_time(ev[sk][0]), e0.elapsed_time(ev[sk][1])))
+    # verification left once a group's copy has landed and the other group's drafting is done (the
+    # verify of a group follows the drafting phase on the compute stream)
+    exposed = []
+    for ev in evs:
+        for g_ver, dk in ((1, "draft0"), (0, "draft1")):
+            ready = max(e0.elapsed_time(ev["stage%d" % g_ver][1]), e0.elapsed_time(ev[dk][1]))
+            exposed.append(e0.elapsed_time(ev["verified%d" % g_ver]) - ready)
     copy_ms = [b - a for a, b in copy_iv]
     draft_ms = [b - a for a, b in draft_iv]
     overlap = [sum(max(0.0, min(b, d1) - max(a, d0)) for d0, d1 in draft_iv) / max(1e-9, b - a) for a, b in copy_iv]
@@ -502,7 +516,8 @@ def run_offload(args):
                        "step": "one period: each of the 4 requests drafts L steps and is staged, verified and accepted once"},
             "stage": {"bytes_per_copy": stage_bytes, "link_alone_gbs": link_alone, "link_during_draft_gbs": link_loaded,
                       "frac_of_link": link_loaded / link_alone, "copy_ms": statistics.mean(copy_ms),
-                      "draft_phase_ms": statistics.mean(draft_ms), "copy_overlapped_by_draft": statistics.mean(overlap)},
+                      "draft_phase_ms": statistics.mean(draft_ms), "copy_overlapped_by_draft": statistics.mean(overlap),
+                      "head_chunks": args.head_chunks, "verify_after_copy_and_draft_ms": statistics.mean(exposed)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                          "frac": achieved / float(peaks["hbm_gbs"]), "traffic": None,
                          "kernel": "draft_attn_kernel<128,4> (2 requests per call), mean over a draft phase",

@@ -13,8 +13,9 @@
  * overlaps the host-link copy of some requests with the drafting of others.
  *
  * One attention layer is covered: compress (vc_compress_kv), draft attention (vc_draft_attn),
- * verify attention (vc_verify_attn), greedy accept (vc_accept) and full-KV staging
- * (vc_stage_full_kv). Every compute step runs in this library's CUDA kernels.
+ * verify attention (vc_verify_attn, vc_verify_attn_heads), greedy accept (vc_accept), full-KV
+ * staging (vc_stage_full_kv) and the post-accept cache update (vc_append_kv). Every compute step
+ * runs in this library's CUDA kernels.
  *
  * Conventions for every call
  *   - The caller owns every buffer. The library never allocates device or host memory and never
@@ -240,6 +241,22 @@ typedef struct vc_verify_req {
 
 vc_status vc_verify_attn(const vc_shape* shape, const vc_verify_req* req, void* ws, size_t ws_bytes,
                          int32_t* dev_status, cudaStream_t stream);
+
+/* vc_verify_attn_heads — vc_verify_attn restricted to the query heads of KV heads
+ * kv_head_begin .. kv_head_end-1 (0 <= begin < end <= Hkv); outputs of the other heads are not
+ * written, and only those KV heads' rows of KV_full, k_new and v_new are read.
+ *
+ * For chunk-pipelined staging ("Cross-resource staggering (P1)": the host-link copy of KV_full
+ * overlaps work on the GPU; here the copy also overlaps the verification itself): KV_full is
+ * [Hkv][cap][d], so one KV head's K (and V) rows are one contiguous range. A caller copies KV_full
+ * a head range at a time, records an event per range, and verifies each range as soon as its
+ * event completes; only the last range's verification remains after the copy ends.
+ * Same arguments, workspace (vc_workspace_size(VC_CALL_VERIFY, ...) covers every range) and
+ * errors as vc_verify_attn; a bad head range returns VC_ERR_INVALID before launching anything.
+ * Calls issued in order on one stream may share one workspace. */
+vc_status vc_verify_attn_heads(const vc_shape* shape, const vc_verify_req* req, int32_t kv_head_begin,
+                               int32_t kv_head_end, void* ws, size_t ws_bytes, int32_t* dev_status,
+                               cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------ */
 /* vc_accept — greedy acceptance ("Core algorithm", step 3).

@@ -1,7 +1,7 @@
 """Python binding of libvc, the GB300 (sm_103a) VeriCache draft/verify/accept hot path.
 
 Argument marshalling only: every step runs in the library's CUDA kernels. The names follow the
-C ABI in include/vc.h (vc_compress_kv, vc_draft_attn, vc_verify_attn, vc_accept, vc_append_kv,
+C ABI in include/vc.h (vc_compress_kv, vc_draft_attn, vc_verify_attn(_heads), vc_accept, vc_append_kv,
 vc_stage_full_kv, vc_workspace_size, vc_status_string). Tensors are torch tensors on the GPU;
 their data pointers and the current (or given) CUDA stream are passed through.
 
@@ -64,6 +64,8 @@ _lib.vc_compress_kv.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_kv_full), C.PO
 _lib.vc_draft_attn.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_draft_req), _p, C.c_size_t, _p, _p]
 _lib.vc_draft_attn_noalloc.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_draft_req), _p, _p]
 _lib.vc_verify_attn.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_verify_req), _p, C.c_size_t, _p, _p]
+_lib.vc_verify_attn_heads.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_verify_req), _i32, _i32, _p, C.c_size_t,
+                                      _p, _p]
 _lib.vc_accept.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p, _p, _p]
 _lib.vc_append_kv.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_kv_full), C.POINTER(vc_kv_comp),
                               C.POINTER(vc_append_req), _i32, _p, _p]
@@ -73,12 +75,12 @@ _lib.vc_workspace_size.restype = C.c_size_t
 _lib.vc_status_string.argtypes = [_i32]
 _lib.vc_status_string.restype = C.c_char_p
 _lib.vc_version.restype = _i32
-for _f in ("vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_accept",
-           "vc_stage_full_kv", "vc_append_kv"):
+for _f in ("vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
+           "vc_accept", "vc_stage_full_kv", "vc_append_kv"):
     getattr(_lib, _f).restype = _i32
 
-EXPORTS = ["vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_accept", "vc_stage_full_kv",
-           "vc_append_kv", "vc_workspace_size", "vc_status_string", "vc_version"]
+EXPORTS = ["vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
+           "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_workspace_size", "vc_status_string", "vc_version"]
 
 
 class VCError(RuntimeError):
@@ -153,6 +155,14 @@ def vc_verify_attn(shape: vc_shape, req, ws=None, dev_status=None, stream=None, 
     wsb = ws.numel() * ws.element_size() if ws is not None else 0
     st = _lib.vc_verify_attn(C.byref(shape), req, _ptr(ws), wsb, _ptr(dev_status), _stream(stream))
     return _check(st, "vc_verify_attn", raise_on_error)
+
+
+def vc_verify_attn_heads(shape: vc_shape, req, kv_head_begin: int, kv_head_end: int, ws=None, dev_status=None,
+                         stream=None, raise_on_error=True) -> int:
+    wsb = ws.numel() * ws.element_size() if ws is not None else 0
+    st = _lib.vc_verify_attn_heads(C.byref(shape), req, kv_head_begin, kv_head_end, _ptr(ws), wsb, _ptr(dev_status),
+                                   _stream(stream))
+    return _check(st, "vc_verify_attn_heads", raise_on_error)
 
 
 def vc_accept(B: int, L_max: int, V: int, logits, draft, L, out_tokens, n_acc, stream=None,

@@ -10,8 +10,8 @@
 #include <unordered_map>
 
 namespace vc {
-cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, void* ws, size_t ws_bytes,
-                          int32_t* dev_status, cudaStream_t stream, vc_status* st);
+cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h0, int h1, void* ws,
+                          size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, vc_status* st);
 size_t verify_workspace_size(const vc_shape* shape, int32_t max_rows);
 }  // namespace vc
 
@@ -420,14 +420,21 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
 }
 
 // ---------------------------------------------------------------------------------------------
-vc_status vc_verify_attn(const vc_shape* shape, const vc_verify_req* req, void* ws, size_t ws_bytes,
-                         int32_t* dev_status, cudaStream_t stream) {
+vc_status vc_verify_attn_heads(const vc_shape* shape, const vc_verify_req* req, int32_t kv_head_begin,
+                               int32_t kv_head_end, void* ws, size_t ws_bytes, int32_t* dev_status,
+                               cudaStream_t stream) {
   vc_status st = VC_OK;
-  cudaError_t e = launch_verify(shape, req, ws, ws_bytes, dev_status, stream, &st);
+  cudaError_t e = launch_verify(shape, req, kv_head_begin, kv_head_end, ws, ws_bytes, dev_status, stream, &st);
   if (st != VC_OK) return st;
   if (e != cudaSuccess) return VC_ERR_CUDA;
   set_last_op(stream, kOpVerify);
   return VC_OK;
+}
+
+vc_status vc_verify_attn(const vc_shape* shape, const vc_verify_req* req, void* ws, size_t ws_bytes,
+                         int32_t* dev_status, cudaStream_t stream) {
+  if (!shape) return VC_ERR_INVALID;
+  return vc_verify_attn_heads(shape, req, 0, shape->Hkv, ws, ws_bytes, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------------------------

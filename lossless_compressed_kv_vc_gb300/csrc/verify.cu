@@ -49,6 +49,7 @@ struct VerifyParams {
   CUtensorMap tm[VC_MAX_BATCH][4];  // K full, V full, K new, V new
   VerifyReqDev req[VC_MAX_BATCH];
   int32_t B, Hq, Hkv, G, n_cta, n_units;
+  int32_t h0;  // first KV head of the call's head range (units cover heads h0 .. h0 + nh - 1)
   int64_t total_tiles;
   float scale_log2;
   float* ws_o;    // [slots][128][d]
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
       bool ok = true;
       for (int64_t pos = beg; pos < end && ok;) {
         const VPiece q = verify_piece(p, pos, end);
-        const int hk = q.ul / p.req[q.b].mtiles;
+        const int hk = p.h0 + q.ul / p.req[q.b].mtiles;
         for (int j = q.j0; j < q.j1 && ok; ++j, ++g) {
           ok = load(false, gk, q.b, hk, j);
           if (ok) ++gk;
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
       const VPiece q = verify_piece(p, pos, end);
       const VerifyReqDev& R = p.req[q.b];
       const int nt = q.j1 - q.j0;
-      const int hk = q.ul / R.mtiles, mt = q.ul % R.mtiles;
+      const int hk = p.h0 + q.ul / R.mtiles, mt = q.ul % R.mtiles;
       const int u_global = R.unit_begin + q.ul;
       const int Rw = mt * VM + tid;
       const int qi = Rw / p.G, qg = Rw % p.G;
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_consta
   const int64_t c0 = ((U0 + 1) * N - 1) / T, c1 = (U1 * N - 1) / T;
   if (c0 == c1) return;
   const int r = blockIdx.y * 8 + (threadIdx.x / TPR), cc = (threadIdx.x % TPR) * CPT;
-  const int hk = ul / R.mtiles, mt = ul % R.mtiles;
+  const int hk = p.h0 + ul / R.mtiles, mt = ul % R.mtiles;
   const int Rw = mt * VM + r, qi = Rw / p.G, qg = Rw % p.G;
   if (qi >= R.n_rows) return;
   float M = -INFINITY;
@@ -546,11 +547,11 @@ static cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
 
 static bool a16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, void* ws, size_t ws_bytes,
-                          int32_t* dev_status, cudaStream_t stream, vc_status* st) {
+cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h0, int h1, void* ws,
+                          size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, vc_status* st) {
   *st = VC_OK;
   if (!shape || shape->B < 1 || shape->B > VC_MAX_BATCH || shape->Hkv < 1 || shape->Hq < shape->Hkv ||
-      shape->Hq % shape->Hkv != 0 || !req) {
+      shape->Hq % shape->Hkv != 0 || !req || h0 < 0 || h1 <= h0 || h1 > shape->Hkv) {
     *st = VC_ERR_INVALID;
     return cudaSuccess;
   }
@@ -565,6 +566,8 @@ cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, void*
   p.Hq = shape->Hq;
   p.Hkv = shape->Hkv;
   p.G = G;
+  p.h0 = h0;
+  const int nh = h1 - h0;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
   p.dev_status = dev_status;
   int64_t tiles = 0;
@@ -594,8 +597,8 @@ cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, void*
     R.tiles = R.n_full + (r.n_rows + VBN - 1) / VBN;
     R.unit_begin = units;
     R.tile_begin = tiles;
-    units += shape->Hkv * R.mtiles;
-    tiles += (int64_t)shape->Hkv * R.mtiles * R.tiles;
+    units += nh * R.mtiles;
+    tiles += (int64_t)nh * R.mtiles * R.tiles;
     if (r.n_rows > max_rows) max_rows = r.n_rows;
   }
   p.total_tiles = tiles;

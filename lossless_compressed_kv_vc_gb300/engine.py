@@ -14,8 +14,8 @@ from typing import List, Optional
 import torch
 
 from . import (vc_shape, vc_kv_full, vc_kv_comp, vc_draft_req, vc_verify_req, vc_append_req, vc_compress_kv,
-               vc_draft_attn, vc_verify_attn, vc_accept, vc_append_kv, vc_workspace_size, VC_TOKEN_DROP, VC_QUANT,
-               VC_CALL_DRAFT, VC_CALL_VERIFY)
+               vc_draft_attn, vc_verify_attn, vc_verify_attn_heads, vc_accept, vc_append_kv, vc_workspace_size,
+               VC_TOKEN_DROP, VC_QUANT, VC_CALL_DRAFT, VC_CALL_VERIFY)
 
 GROUP = 32
 
@@ -328,34 +328,50 @@ class StaggeredOffload:
     stream (host-link-bound); the compute stream then waits for that copy and verifies and accepts
     the staged group. Each group keeps its own device staging slot, so a copy never waits for the
     other group's verification.
+
+    head_chunks > 1 pipelines the copy into the verification ("Cross-resource staggering (P1)"
+    applied to the verification itself): a group's KV_full is copied a range of KV heads at a time
+    (each head's K and V rows are contiguous in the [K; V][Hkv][cap][d] layout), each range records
+    its own event, and the compute stream verifies each head range (vc_verify_attn_heads) as soon as
+    it has landed, so only the last range's verification remains once the copy ends.
     """
 
     def __init__(self, groups: List[Batch], host_kv: List[List[torch.Tensor]], slots: List[List[torch.Tensor]],
-                 copy_stream, compute_stream, chunk_bytes: int = 64 << 20):
+                 copy_stream, compute_stream, chunk_bytes: int = 64 << 20, head_chunks: int = 1):
         assert len(groups) == 2
+        Hkv = groups[0].Hkv
+        assert 1 <= head_chunks <= Hkv and groups[1].Hkv == Hkv
         self.groups, self.host_kv, self.slots = groups, host_kv, slots
         self.copy_stream, self.compute_stream = copy_stream, compute_stream
         self.chunk_bytes = chunk_bytes
-        self.staged = [torch.cuda.Event(), torch.cuda.Event()]
+        self.edges = [c * Hkv // head_chunks for c in range(head_chunks + 1)]
+        self.staged = [[torch.cuda.Event() for _ in range(head_chunks)] for _ in range(2)]
         self.verified = [torch.cuda.Event(), torch.cuda.Event()]
         for g in range(2):  # a slot is free before its first copy
             self.verified[g].record(compute_stream)
 
     def stage(self, g: int, events=None):
-        """Issue the host-to-device copies of group g's KV_full on the copy stream."""
+        """Issue the host-to-device copies of group g's KV_full on the copy stream, one KV-head range
+        at a time (K then V rows of those heads, for every request of the group)."""
         from . import vc_stage_full_kv
         self.copy_stream.wait_event(self.verified[g])  # its previous verification has read the slot
         if events is not None:
             events[0].record(self.copy_stream)
-        for h, d in zip(self.host_kv[g], self.slots[g]):
-            vc_stage_full_kv(h, d, h.numel() * h.element_size(), self.chunk_bytes, self.copy_stream, None)
-        self.staged[g].record(self.copy_stream)
+        for c in range(len(self.edges) - 1):
+            h0, h1 = self.edges[c], self.edges[c + 1]
+            for h, d in zip(self.host_kv[g], self.slots[g]):
+                for kv in range(2):
+                    src, dst = h[kv, h0:h1], d[kv, h0:h1]
+                    vc_stage_full_kv(src, dst, src.numel() * src.element_size(), self.chunk_bytes, self.copy_stream,
+                                     None)
+            self.staged[g][c].record(self.copy_stream)
         if events is not None:
             events[1].record(self.copy_stream)
 
-    def phase(self, draft_g: int, io, draft_events=None, stage_events=None):
+    def phase(self, draft_g: int, io, draft_events=None, stage_events=None, verify_event=None):
         """Group draft_g drafts while the other group stages, then the other group verifies and accepts.
-        io[g] = (logits, draft, L, out_tokens, n_acc) of group g."""
+        io[g] = (logits, draft, L, out_tokens, n_acc) of group g. verify_event, if given, is recorded
+        on the compute stream once the other group's last head range is verified."""
         other = 1 - draft_g
         self.stage(other, stage_events)
         bt = self.groups[draft_g]
@@ -365,18 +381,22 @@ class StaggeredOffload:
             vc_draft_attn(shape, arr, bt.ws_draft, bt.dev_status, self.compute_stream)
         if draft_events is not None:
             draft_events[1].record(self.compute_stream)
-        self.compute_stream.wait_event(self.staged[other])
         ob = self.groups[other]
-        vc_verify_attn(ob.shape, ob._verify_arr, ob.ws_verify, ob.dev_status, self.compute_stream)
+        for c in range(len(self.edges) - 1):
+            self.compute_stream.wait_event(self.staged[other][c])
+            vc_verify_attn_heads(ob.shape, ob._verify_arr, self.edges[c], self.edges[c + 1], ob.ws_verify,
+                                 ob.dev_status, self.compute_stream)
         self.verified[other].record(self.compute_stream)
+        if verify_event is not None:
+            verify_event.record(self.compute_stream)
         lg, dr, L, tok, nacc = io[other]
         accept(lg, dr, L, tok, nacc, self.compute_stream)
 
     def period(self, io, events=None):
         """Both phases: every request drafts once and is verified once."""
         ev = events or {}
-        self.phase(0, io, ev.get("draft0"), ev.get("stage1"))
-        self.phase(1, io, ev.get("draft1"), ev.get("stage0"))
+        self.phase(0, io, ev.get("draft0"), ev.get("stage1"), ev.get("verified1"))
+        self.phase(1, io, ev.get("draft1"), ev.get("stage0"), ev.get("verified0"))
 
 
 def move_full_kv_to_host(groups: List[Batch]):

@@ -29,7 +29,7 @@ def declared_symbols():
 
 def test_header_declares_the_round_calls():
     names = declared_symbols()
-    for n in ["vc_compress_kv", "vc_draft_attn", "vc_verify_attn", "vc_accept", "vc_stage_full_kv", "vc_append_kv",
+    for n in ["vc_compress_kv", "vc_draft_attn", "vc_verify_attn", "vc_verify_attn_heads", "vc_accept", "vc_stage_full_kv", "vc_append_kv",
               "vc_workspace_size", "vc_status_string"]:
         assert n in names
 
@@ -92,3 +92,11 @@ def test_append_validation_rejects_without_launching(lib):
     assert call(300, 1000, 117, quant=True, ng=5, ng_cap=50)[0] == vc.VC_ERR_UNSUPPORTED  # 140+117 rows
     assert call(300, 1000, 8, quant=True, ng=5, ng_cap=50, bits=3)[0] == vc.VC_ERR_UNSUPPORTED
     assert call(300, 1000, 8, quant=True, ng=5, ng_cap=50, win_cap=100)[0] == vc.VC_ERR_INVALID  # residual > window
+
+
+def test_verify_head_range_rejected_before_launch(lib):
+    import lossless_compressed_kv_vc_gb300 as vc
+    shp = vc.vc_shape(1, 8, 2, 64)
+    arr = (vc.vc_verify_req * 1)()
+    for h0, h1 in [(-1, 1), (1, 1), (0, 3), (2, 1)]:
+        assert vc.vc_verify_attn_heads(shp, arr, h0, h1, None, None, stream=0, raise_on_error=False) == vc.VC_ERR_INVALID

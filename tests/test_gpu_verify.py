@@ -94,3 +94,42 @@ def test_verify_llama8b_full_size_sampled():
 def test_verify_qwen32b_full_size_sampled():
     w = configs.qwen32b_quant2()
     _check(w, list(range(16)), heads=[2])
+
+
+@pytest.mark.parametrize("ranges", [[(0, 8)], [(0, 3), (3, 5), (5, 8)], [(h, h + 1) for h in range(8)], [(2, 6)]])
+def test_verify_head_ranges(ranges):
+    """vc_verify_attn_heads over KV-head ranges: the heads in the ranges match the oracle and the
+    other heads' outputs are left as they were (NaN here)."""
+    import lossless_compressed_kv_vc_gb300 as vc
+    w = configs.scaled(configs.llama8b_drop(), ctx_div=32, batch=3, L=7)
+    bt = make_batch(w, [0, 1, 2])
+    _fill_window(bt)
+    for r in bt.reqs:
+        r.o_verify.fill_(float("nan"))
+    arr = bt.verify_requests()
+    for h0, h1 in ranges:
+        vc.vc_verify_attn_heads(bt.shape, arr, h0, h1, bt.ws_verify, bt.dev_status)
+    torch.cuda.synchronize()
+    assert int(bt.dev_status.item()) == 0
+    G = w.Hq // w.Hkv
+    done = set(h for h0, h1 in ranges for h in range(h0, h1))
+    for i, r in enumerate(bt.reqs):
+        q, kf, vf = f32(r.q), f32(r.k_full), f32(r.v_full)
+        kn, vn = f32(r.k_new).transpose(1, 0, 2), f32(r.v_new).transpose(1, 0, 2)
+        for hk in range(w.Hkv):
+            sel = slice(hk * G, (hk + 1) * G)
+            if hk in done:
+                ref = O.verify_attn(q[:, sel], kf[hk:hk + 1], vf[hk:hk + 1], kn[hk:hk + 1], vn[hk:hk + 1])
+                assert_attn_close(r.o_verify[:, sel], ref, f"b{i} hk{hk}")
+            else:
+                assert torch.isnan(r.o_verify[:, sel].float()).all(), f"b{i} hk{hk} written outside the range"
+
+
+def test_verify_head_range_validation():
+    import lossless_compressed_kv_vc_gb300 as vc
+    w = configs.tiny()
+    bt = make_batch(w, [0])
+    arr = bt.verify_requests()
+    for h0, h1 in [(-1, 1), (1, 1), (0, w.Hkv + 1), (2, 1)]:
+        st = vc.vc_verify_attn_heads(bt.shape, arr, h0, h1, bt.ws_verify, bt.dev_status, raise_on_error=False)
+        assert st == vc.VC_ERR_INVALID
