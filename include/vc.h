@@ -285,6 +285,35 @@ vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, si
                            cudaStream_t copy_stream, cudaEvent_t done);
 
 /* ------------------------------------------------------------------------------------------ */
+/* vc_plan_stagger — choose the two alternating groups of cross-resource staggering ("Cross-resource
+ * staggering (P1)": while some requests draft, bound by HBM bandwidth, the KV_full of others moves
+ * over the host link and is verified; the pages fix no rule for choosing who does which).
+ *
+ * A period has two phases. In phase 1 group A drafts (its L draft steps) while group B's KV_full is
+ * copied to the GPU, then B is verified; phase 2 swaps the groups. Verification waits for both the
+ * drafting ahead of it on the compute stream and its own copy, so with per-request costs d (draft
+ * phase), v (verification and accept) and s (copy; 0 for a request whose KV_full stays in HBM):
+ *     T(A) = max(D_A, S_B) + V_B + max(D_B, S_A) + V_A,
+ * D_X, S_X, V_X the sums over group X. T(A) = T(B). The call returns, in group[r] (0 = A, 1 = B),
+ * a split of minimum T with request 0 in A; among equal T it takes the smallest sum of
+ * group[r] * 2^(r-1) over r >= 1. period_ns (may be NULL) receives that T. Exact: all 2^(n-1)
+ * splits are enumerated in Gray-code order, O(1) each (about 8 M at n = VC_STAGGER_MAX).
+ * Errors: VC_ERR_INVALID (null pointers, n < 1, a negative cost or one above 2^40 ns);
+ * VC_ERR_UNSUPPORTED (n > VC_STAGGER_MAX). Host only, no GPU work. */
+#define VC_STAGGER_MAX 24
+
+typedef struct vc_stagger_cost {
+  int64_t draft_ns;   /* GPU time of the request's draft phase */
+  int64_t verify_ns;  /* GPU time of its verification and acceptance */
+  int64_t stage_ns;   /* host-link time of copying its KV_full (0 when KV_full stays in HBM) */
+} vc_stagger_cost;
+
+vc_status vc_plan_stagger(const vc_stagger_cost* cost, int32_t n, int32_t* group, int64_t* period_ns);
+
+/* T of a given split (group[r] in {0, 1}) under the same model; same errors, any n >= 1. */
+vc_status vc_stagger_period(const vc_stagger_cost* cost, int32_t n, const int32_t* group, int64_t* period_ns);
+
+/* ------------------------------------------------------------------------------------------ */
 /* Workspace bytes vc_draft_attn (call = VC_CALL_DRAFT) or vc_verify_attn (VC_CALL_VERIFY) needs
  * for `shape`; max_rows = the largest n_rows of a verify call (ignored for draft). The workspace
  * holds per-split partial outputs. The draft workspace also starts with per-(KV head, request)

@@ -26,6 +26,7 @@ VC_TOKEN_DROP, VC_QUANT = 0, 1
 VC_CALL_DRAFT, VC_CALL_VERIFY = 0, 1
 VC_MAX_BATCH = 32
 VC_APPEND_MAX_ROWS = 256
+VC_STAGGER_MAX = 24
 
 _p = C.c_void_p
 _i32 = C.c_int32
@@ -54,6 +55,10 @@ class vc_append_req(C.Structure):
     _fields_ = [("k_rows", _p), ("v_rows", _p), ("n_rows", _i32)]
 
 
+class vc_stagger_cost(C.Structure):
+    _fields_ = [("draft_ns", C.c_int64), ("verify_ns", C.c_int64), ("stage_ns", C.c_int64)]
+
+
 class vc_verify_req(C.Structure):
     _fields_ = [("full", vc_kv_full), ("q", _p), ("k_new", _p), ("v_new", _p), ("new_cap", _i32),
                 ("n_rows", _i32), ("o", _p)]
@@ -70,17 +75,20 @@ _lib.vc_accept.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p, _p, _p]
 _lib.vc_append_kv.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_kv_full), C.POINTER(vc_kv_comp),
                               C.POINTER(vc_append_req), _i32, _p, _p]
 _lib.vc_stage_full_kv.argtypes = [_p, _p, C.c_size_t, C.c_size_t, _p, _p]
+_lib.vc_plan_stagger.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
+_lib.vc_stagger_period.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
 _lib.vc_workspace_size.argtypes = [_i32, C.POINTER(vc_shape), _i32]
 _lib.vc_workspace_size.restype = C.c_size_t
 _lib.vc_status_string.argtypes = [_i32]
 _lib.vc_status_string.restype = C.c_char_p
 _lib.vc_version.restype = _i32
 for _f in ("vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
-           "vc_accept", "vc_stage_full_kv", "vc_append_kv"):
+           "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_plan_stagger", "vc_stagger_period"):
     getattr(_lib, _f).restype = _i32
 
 EXPORTS = ["vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
-           "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_workspace_size", "vc_status_string", "vc_version"]
+           "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_plan_stagger", "vc_stagger_period",
+           "vc_workspace_size", "vc_status_string", "vc_version"]
 
 
 class VCError(RuntimeError):
@@ -185,6 +193,33 @@ def vc_stage_full_kv(host_src, dev_dst, nbytes: int, chunk_bytes: int = 0, copy_
     ev = done.cuda_event if done is not None and not isinstance(done, int) else done
     st = _lib.vc_stage_full_kv(_ptr(host_src), _ptr(dev_dst), nbytes, chunk_bytes, _stream(copy_stream), ev)
     return _check(st, "vc_stage_full_kv", raise_on_error)
+
+
+def _costs(costs):
+    """costs: sequence of (draft_ns, verify_ns, stage_ns) integers."""
+    arr = (vc_stagger_cost * len(costs))()
+    for r, (d, v, s) in enumerate(costs):
+        arr[r].draft_ns, arr[r].verify_ns, arr[r].stage_ns = int(d), int(v), int(s)
+    return arr
+
+
+def vc_plan_stagger(costs, raise_on_error=True):
+    """Exact two-group split of cross-resource staggering. Returns (status, groups list, period_ns)."""
+    n = len(costs)
+    grp = (_i32 * max(n, 1))()
+    t = C.c_int64(0)
+    st = _lib.vc_plan_stagger(_costs(costs) if n else None, n, grp, C.byref(t))
+    _check(st, "vc_plan_stagger", raise_on_error)
+    return st, list(grp)[:n], t.value
+
+
+def vc_stagger_period(costs, groups, raise_on_error=True):
+    n = len(costs)
+    grp = (_i32 * max(n, 1))(*groups)
+    t = C.c_int64(0)
+    st = _lib.vc_stagger_period(_costs(costs) if n else None, n, grp, C.byref(t))
+    _check(st, "vc_stagger_period", raise_on_error)
+    return st, t.value
 
 
 def lib_handle():

@@ -330,6 +330,44 @@ def accept(logits: np.ndarray, draft: Sequence[int], L: int) -> Tuple[List[int],
 
 
 # ----------------------------------------------------------------------------------------------
+# staggering plan (two alternating groups)
+# ----------------------------------------------------------------------------------------------
+def stagger_period(costs: Sequence[Tuple[int, int, int]], groups: Sequence[int]) -> int:
+    """Period of the two-phase stagger ("Cross-resource staggering (P1)"; the pages fix no formula,
+    this is the reading stated with the library's planner).
+
+    costs[r] = (d, v, s): draft-phase time, verification-and-accept time and host-link copy time of
+    request r (s = 0 when its KV_full stays in HBM); groups[r] in {0, 1}. Phase 1: group 0 drafts
+    while group 1 is copied, then group 1 verifies; phase 2 swaps. A verification waits for the
+    drafting before it and for its own copy:
+        T = max(D_0, S_1) + V_1 + max(D_1, S_0) + V_0.
+    """
+    D = [0, 0]
+    S = [0, 0]
+    V = [0, 0]
+    for (d, v, s), g in zip(costs, groups):
+        D[g] += d
+        S[g] += s
+        V[g] += v
+    return max(D[0], S[1]) + V[1] + max(D[1], S[0]) + V[0]
+
+
+def plan_stagger(costs: Sequence[Tuple[int, int, int]]) -> Tuple[List[int], int]:
+    """Best split by brute force: every assignment with request 0 in group 0, minimum period, ties
+    to the smallest sum of groups[r] * 2^(r-1). Returns (groups, period)."""
+    import itertools
+    n = len(costs)
+    best = None
+    for tail in itertools.product((0, 1), repeat=n - 1):
+        groups = [0] + list(tail)
+        key = sum(g << (r - 1) for r, g in enumerate(groups) if r >= 1)
+        t = stagger_period(costs, groups)
+        if best is None or (t, key) < (best[0], best[1]):
+            best = (t, key, groups)
+    return best[2], best[0]
+
+
+# ----------------------------------------------------------------------------------------------
 # helpers for whole requests
 # ----------------------------------------------------------------------------------------------
 def bf16_to_f32(t) -> np.ndarray:

@@ -100,3 +100,40 @@ def test_verify_head_range_rejected_before_launch(lib):
     arr = (vc.vc_verify_req * 1)()
     for h0, h1 in [(-1, 1), (1, 1), (0, 3), (2, 1)]:
         assert vc.vc_verify_attn_heads(shp, arr, h0, h1, None, None, stream=0, raise_on_error=False) == vc.VC_ERR_INVALID
+
+
+def test_plan_stagger_equals_oracle_brute_force():
+    """The library's Gray-code enumeration against the oracle's itertools brute force: the same
+    split (with the same tie-break) and period on random integer costs, resident requests mixed in."""
+    import numpy as np
+    import oracle as O
+    import lossless_compressed_kv_vc_gb300 as vc
+    rng = np.random.default_rng(11)
+    for n in list(range(1, 13)) + [12, 12]:
+        for _ in range(6):
+            costs = []
+            for r in range(n):
+                d, v, s = (int(x) for x in rng.integers(0, 5_000_000, 3))
+                if rng.random() < 0.4:
+                    s = 0
+                costs.append((d, v, s))
+            st, groups, t = vc.vc_plan_stagger(costs)
+            ref_groups, ref_t = O.plan_stagger(costs)
+            assert st == vc.VC_OK and groups == ref_groups and t == ref_t, (n, costs)
+            assert vc.vc_stagger_period(costs, groups)[1] == O.stagger_period(costs, groups)
+
+
+def test_plan_stagger_ties_and_limits():
+    import time
+    import lossless_compressed_kv_vc_gb300 as vc
+    st, groups, t = vc.vc_plan_stagger([(10, 1, 10)] * 6)
+    assert groups == [0, 1, 1, 1, 0, 0] and t == 66
+    costs = [(1000 + 37 * r, 100, 900 + 53 * r) for r in range(vc.VC_STAGGER_MAX)]
+    t0 = time.time()
+    st, groups, t = vc.vc_plan_stagger(costs)
+    assert st == vc.VC_OK and time.time() - t0 < 5.0
+    assert vc.vc_stagger_period(costs, groups)[1] == t
+    assert vc.vc_plan_stagger(costs + [(1, 1, 1)], raise_on_error=False)[0] == vc.VC_ERR_UNSUPPORTED
+    assert vc.vc_plan_stagger([(1, -1, 0)], raise_on_error=False)[0] == vc.VC_ERR_INVALID
+    assert vc.vc_plan_stagger([(1 << 41, 0, 0)], raise_on_error=False)[0] == vc.VC_ERR_INVALID
+    assert vc.vc_stagger_period([(1, 1, 1)], [2], raise_on_error=False)[0] == vc.VC_ERR_INVALID

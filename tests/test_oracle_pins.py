@@ -350,3 +350,73 @@ def test_quantize_with_no_whole_block(bits):
     assert np.array_equal(qkv["k_res"], k)
     kh, vh = O.dequantize_kv(qkv, 64)
     assert kh.shape == (2, 0, 64) and vh.shape == (2, 0, 64)
+
+
+# ---------------------------------------------------------------------------- staggering plan --
+def _simulate_stagger(costs, groups):
+    """Event-by-event schedule of one period: a compute stream that drafts one group request by
+    request, then verifies the other group request by request once each request's copy has
+    landed; a copy stream that copies the verified group's requests one after another from the
+    phase start. Returns the period (end of the second phase)."""
+    t = 0
+    for drafting in (0, 1):
+        verifying = 1 - drafting
+        compute = t
+        for (d, v, s), g in zip(costs, groups):
+            if g == drafting:
+                compute += d
+        copy = t
+        landed = []
+        for (d, v, s), g in zip(costs, groups):
+            if g == verifying:
+                copy += s
+                landed.append(copy)
+        # verification starts once drafting is over and every copy of the group has landed
+        start = max([compute] + landed)
+        for (d, v, s), g in zip(costs, groups):
+            if g == verifying:
+                start += v
+        t = start
+    return t
+
+
+def test_stagger_period_matches_event_simulation():
+    rng = np.random.default_rng(7)
+    for _ in range(200):
+        n = int(rng.integers(1, 7))
+        costs = [tuple(int(x) for x in rng.integers(0, 50, 3)) for _ in range(n)]
+        groups = [int(x) for x in rng.integers(0, 2, n)]
+        assert O.stagger_period(costs, groups) == _simulate_stagger(costs, groups)
+
+
+def test_stagger_identical_requests_split_evenly():
+    """n = 6 requests with d = s = 10, v = 1: k in group 0 gives 2 * 10 * max(k, 6 - k) + 6, least
+    at k = 3: 66, and the smallest mask with three of requests 1..5 in group 1 is 0b00111."""
+    groups, t = O.plan_stagger([(10, 1, 10)] * 6)
+    assert t == 66 and groups == [0, 1, 1, 1, 0, 0]
+
+
+def test_stagger_resident_only_any_split():
+    """No copies: every split costs D + V, so the tie-break keeps everyone in group 0."""
+    costs = [(5, 2, 0), (7, 1, 0), (3, 3, 0), (11, 0, 0)]
+    groups, t = O.plan_stagger(costs)
+    assert t == 26 + 6 and groups == [0, 0, 0, 0]
+
+
+def test_stagger_copy_hidden_under_other_drafts():
+    """One request with a long copy (100) and two resident requests drafting 50 each: the copy
+    hides under their drafting only when they form the other group: T = 1 + 100 = 101."""
+    groups, t = O.plan_stagger([(1, 0, 100), (50, 0, 0), (50, 0, 0)])
+    assert groups == [0, 1, 1] and t == 101
+    assert O.stagger_period([(1, 0, 100), (50, 0, 0), (50, 0, 0)], [0, 0, 1]) == 151
+
+
+def test_stagger_bounds_and_symmetry():
+    rng = np.random.default_rng(3)
+    for _ in range(100):
+        n = int(rng.integers(1, 8))
+        costs = [tuple(int(x) for x in rng.integers(0, 100, 3)) for _ in range(n)]
+        D, V, S = (sum(c[i] for c in costs) for i in range(3))
+        groups, t = O.plan_stagger(costs)
+        assert max(D, S) + V <= t <= D + S + V
+        assert O.stagger_period(costs, [1 - g for g in groups]) == t
