@@ -46,9 +46,11 @@ def parse():
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-heads", type=int, default=1, help=argparse.SUPPRESS)
     ap.add_argument("--child-steps", type=int, default=1, help=argparse.SUPPRESS)
-    ap.add_argument("--workload", default="llama8b_drop", choices=["llama8b_drop", "offload"],
+    ap.add_argument("--workload", default="llama8b_drop", choices=["llama8b_drop", "offload", "stagger"],
                     help="llama8b_drop: the headline round; offload: Llama-70B-shape 4-bit requests with KV_full "
-                         "in pinned host memory, two drafting while two stage and verify")
+                         "in pinned host memory, two drafting while two stage and verify; stagger: the 16 "
+                         "2-bit requests of the mixed serving workload (half with KV_full on the host) under "
+                         "a naive split and under the planner's split")
     ap.add_argument("--ctx-div", type=int, default=1,
                     help="offload workload: divide the context (a smaller case for profiler captures)")
     ap.add_argument("--compact", action="store_true",
@@ -59,7 +61,8 @@ def parse():
                     help="offload workload: stage KV_full in this many KV-head ranges and verify each range as "
                          "soon as it lands (1 = stage the whole group, then verify)")
     ap.add_argument("--draft-steps", type=int, default=None,
-                    help="offload workload: drafts per round (default: the workload's L)")
+                    help="offload and stagger workloads: drafts per round for every request (default: the "
+                         "workload's L)")
     a = ap.parse_args()
     global _BATCH
     _BATCH = a.batch
@@ -527,6 +530,129 @@ def run_offload(args):
     return 0
 
 
+def run_stagger(args):
+    """The quantised requests of the mixed serving workload (contexts log-uniform 8K-256K, L 25-40,
+    KV_full of half of them in pinned host memory) staggered in two groups. Per-request costs come
+    from rates measured on the workload itself (the whole batch's draft phase and verification,
+    one request's copy alone) times each request's bytes; the period is then measured for a naive
+    split (first half / second half), an alternating split and the planner's split."""
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from lossless_compressed_kv_vc_gb300 import (engine, VC_QUANT, vc_draft_attn, vc_verify_attn, vc_stage_full_kv,
+                                                 vc_stagger_period)
+    from workloads import configs, gen
+    full = configs.mixed_serving()
+    w = configs.subset(full, full.request_indices("quant"), name="mixed_quant2_stagger_16req_ctx8k_256k")
+    if args.ctx_div > 1 or args.draft_steps is not None:
+        w = configs.scaled(w, ctx_div=args.ctx_div, L=args.draft_steps)
+    dev = "cuda"
+    reqs, host, slot = [], [], []
+    for b in range(w.B):
+        ri = gen.request(w, 0, b, dev)
+        kf, vf = ri.k_full, ri.v_full
+        h = s = None
+        if w.on_host[b]:
+            s = torch.stack([kf, vf])  # device staging slot; the request's KV_full descriptor points at it
+            h = torch.empty(s.shape, dtype=s.dtype, pin_memory=True)
+            h.copy_(s)
+            kf, vf = s[0], s[1]
+        host.append(h)
+        slot.append(s)
+        reqs.append(engine.Req(mode=VC_QUANT, ctx=w.ctx[b], L=w.L[b], k_full=kf, v_full=vf, q=ri.q, k_new=ri.k_new,
+                               v_new=ri.v_new, bits=w.bits))
+    del ri
+    cs, ks = torch.cuda.Stream(), torch.cuda.Stream()
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+    def timed(fn, stream, reps=3):
+        best = float("inf")
+        for _ in range(reps + 1):
+            e = mk()
+            torch.cuda.synchronize()
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            best = min(best, e[0].elapsed_time(e[1]))
+        return best * 1e6  # ns
+
+    # rates measured on the whole batch
+    cal = engine.Batch(w.Hq, w.Hkv, w.d, reqs, residual_min=w.residual_min, device=dev)
+    cal.compress()
+    cal.prepare_steps()
+    t_draft = timed(lambda: [vc_draft_attn(sh, arr, cal.ws_draft, cal.dev_status, ks) for sh, arr, act in cal._steps], ks)
+    t_verify = timed(lambda: vc_verify_attn(cal.shape, cal._verify_arr, cal.ws_verify, cal.dev_status, ks), ks)
+    assert int(cal.dev_status.item()) == 0
+    del cal
+    d, b8 = w.d, w.bits
+    ng = [max(0, (c - w.residual_min) // 32) for c in w.ctx]
+    step_bytes = [w.Hkv * (32 * n * (2 * d * b8 // 8 + 2 * 4 * d // 32) + (c - 32 * n + (L + 1) / 2) * 2 * d * 2)
+                  for n, c, L in zip(ng, w.ctx, w.L)]
+    draft_bytes = [L * sb for L, sb in zip(w.L, step_bytes)]
+    verify_bytes = [w.Hkv * (c + L) * 2 * d * 2 + (L + 1) * w.V * 4 for c, L in zip(w.ctx, w.L)]
+    full_bytes = [2 * w.Hkv * c * d * 2 for c in w.ctx]
+    hb = next(b for b in range(w.B) if w.on_host[b])
+    t_link = timed(lambda: vc_stage_full_kv(host[hb], slot[hb], full_bytes[hb], 64 << 20, cs, None), cs)
+    rate_d, rate_v = sum(draft_bytes) / t_draft, sum(verify_bytes) / t_verify
+    rate_s = full_bytes[hb] / t_link
+    costs = engine.stagger_costs([x / rate_d for x in draft_bytes], [x / rate_v for x in verify_bytes],
+                                 [fb / rate_s if w.on_host[b] else 0 for b, fb in enumerate(full_bytes)])
+    g0, g1, t_plan = engine.plan_groups(costs)
+    half = w.B // 2
+    splits = {"halves": [0] * half + [1] * (w.B - half), "alternate": [b % 2 for b in range(w.B)],
+              "planned": [0 if b in g0 else 1 for b in range(w.B)]}
+    draft, logits, Lt = gen.drafts_and_logits(w, 0, dev)
+    out = {}
+    for name, grp in splits.items():
+        idx = [[b for b in range(w.B) if grp[b] == gi] for gi in (0, 1)]
+        if not idx[0] or not idx[1]:
+            out[name] = {"skipped": "empty group"}
+            continue
+        groups, io = [], []
+        for gi in (0, 1):
+            bt = engine.Batch(w.Hq, w.Hkv, w.d, [reqs[b] for b in idx[gi]], residual_min=w.residual_min, device=dev)
+            bt.compress()
+            bt.prepare_steps()
+            groups.append(bt)
+            sel = torch.tensor(idx[gi], device=dev)
+            n = len(idx[gi])
+            io.append((logits[sel].contiguous(), draft[sel].contiguous(), Lt[sel].contiguous(),
+                       torch.empty((n, w.L_max + 1), dtype=torch.int32, device=dev),
+                       torch.empty((n,), dtype=torch.int32, device=dev)))
+        sg = engine.StaggeredOffload(groups, [[host[b] for b in idx[gi]] for gi in (0, 1)],
+                                     [[slot[b] for b in idx[gi]] for gi in (0, 1)], cs, ks)
+        for _ in range(args.warmup):
+            sg.period(io)
+        torch.cuda.synchronize()
+        e = mk()
+        e[0].record(ks)
+        for _ in range(args.steps):
+            sg.period(io)
+        e[1].record(ks)
+        torch.cuda.synchronize()
+        for bt in groups:
+            assert int(bt.dev_status.item()) == 0
+        t_ms = e[0].elapsed_time(e[1])
+        tokens = int(io[0][4].sum().item() + io[1][4].sum().item())
+        out[name] = {"groups": grp, "period_ms": t_ms / args.steps, "modelled_ms": vc_stagger_period(costs, grp)[1] / 1e6,
+                     "tokens_per_s": tokens * args.steps / (t_ms / 1e3)}
+        del groups, io, sg
+    best_naive = max(v.get("tokens_per_s", 0.0) for k, v in out.items() if k != "planned")
+    line = {"metric": METRIC, "value": out["planned"]["tokens_per_s"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": out["planned"]["period_ms"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ctx": w.ctx, "L": w.L,
+                       "bits": w.bits, "on_host": w.on_host,
+                       "step": "one period: every request drafts its L steps, is staged if its KV_full is on the "
+                               "host, verified and accepted once"},
+            "stagger": {"rates_gbs": {"draft": rate_d, "verify": rate_v, "link": rate_s},
+                        "costs_ns": costs, "planned_period_ms": t_plan / 1e6, "splits": out,
+                        "planned_over_best_naive": out["planned"]["tokens_per_s"] / best_naive if best_naive else None}}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse()
     if args.cpu_child:
@@ -535,6 +661,8 @@ def main():
         return run_reference(args)
     if args.workload == "offload":
         return run_offload(args)
+    if args.workload == "stagger":
+        return run_stagger(args)
     return run_native(args)
 
 

@@ -289,15 +289,18 @@ vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, si
  * staggering (P1)": while some requests draft, bound by HBM bandwidth, the KV_full of others moves
  * over the host link and is verified; the pages fix no rule for choosing who does which).
  *
- * A period has two phases. In phase 1 group A drafts (its L draft steps) while group B's KV_full is
- * copied to the GPU, then B is verified; phase 2 swaps the groups. Verification waits for both the
- * drafting ahead of it on the compute stream and its own copy, so with per-request costs d (draft
- * phase), v (verification and accept) and s (copy; 0 for a request whose KV_full stays in HBM):
- *     T(A) = max(D_A, S_B) + V_B + max(D_B, S_A) + V_A,
- * D_X, S_X, V_X the sums over group X. T(A) = T(B). The call returns, in group[r] (0 = A, 1 = B),
- * a split of minimum T with request 0 in A; among equal T it takes the smallest sum of
- * group[r] * 2^(r-1) over r >= 1. period_ns (may be NULL) receives that T. Exact: all 2^(n-1)
- * splits are enumerated in Gray-code order, O(1) each (about 8 M at n = VC_STAGGER_MAX).
+ * The schedule: a compute stream repeats [draft A, verify B, draft B, verify A] and a copy stream
+ * repeats [copy B, copy A]; verify X waits for copy X (of the same period), and copy X waits for
+ * the previous verification of X (its staging slot is free again). With per-request costs d (draft
+ * phase), v (verification and accept) and s (copy; 0 for a request whose KV_full stays in HBM) and
+ * D_X, S_X, V_X their sums over group X (D, S, V over all requests), the steady-state period is
+ * the maximum cycle mean of that dependency graph (max-plus algebra):
+ *     T(A) = max(D + V, S, S_A + V_A, S_B + V_B, (S + V + D_A) / 2, (S + V + D_B) / 2).
+ * T(A) = T(B). The call returns, in group[r] (0 = A, 1 = B), a split of minimum T with request 0
+ * in A and, when n >= 2, both groups non-empty; among equal T (compared exactly, as 2T) it takes
+ * the smallest sum of group[r] * 2^(r-1) over r >= 1. period_ns (may be NULL) receives T rounded
+ * up to a whole ns. Exact: all 2^(n-1) - 1 such splits are enumerated in Gray-code order, O(1)
+ * each (about 8 M at n = VC_STAGGER_MAX).
  * Errors: VC_ERR_INVALID (null pointers, n < 1, a negative cost or one above 2^40 ns);
  * VC_ERR_UNSUPPORTED (n > VC_STAGGER_MAX). Host only, no GPU work. */
 #define VC_STAGGER_MAX 24

@@ -22,9 +22,20 @@ bool costs_ok(const vc_stagger_cost* c, int32_t n) {
   return true;
 }
 
-// max(D_A, S_B) + max(D_B, S_A): the period without the verification sum, which no split changes.
-inline int64_t phase_sum(int64_t dA, int64_t sA, int64_t D, int64_t S) {
-  return max64(dA, S - sA) + max64(D - dA, sA);
+// Twice the steady-state period of split (A, B): the largest cycle mean of the schedule's
+// dependency graph, doubled so that the two-period cycles stay integers.
+//   compute: draft A -> verify B -> draft B -> verify A -> (next period);  copy: copy B -> copy A
+//   verify X after copy X; copy X after the previous verify X.
+// Cycles (weight / periods spanned): the compute loop (D + V) / 1, the copy loop S / 1, copy X then
+// verify X (S_X + V_X) / 1, and the two loops through both streams (S + V + D_X) / 2.
+inline int64_t period2(int64_t dA, int64_t sA, int64_t vA, int64_t D, int64_t S, int64_t V) {
+  int64_t t = 2 * (D + V);
+  t = max64(t, 2 * S);
+  t = max64(t, 2 * (sA + vA));
+  t = max64(t, 2 * ((S - sA) + (V - vA)));
+  t = max64(t, S + V + dA);
+  t = max64(t, S + V + (D - dA));
+  return t;
 }
 
 }  // namespace
@@ -33,7 +44,7 @@ extern "C" vc_status vc_stagger_period(const vc_stagger_cost* cost, int32_t n, c
                                        int64_t* period_ns) {
   if (!cost || !group || !period_ns || n < 1) return VC_ERR_INVALID;
   if (!costs_ok(cost, n)) return VC_ERR_INVALID;
-  int64_t D = 0, S = 0, V = 0, dA = 0, sA = 0;
+  int64_t D = 0, S = 0, V = 0, dA = 0, sA = 0, vA = 0;
   for (int32_t r = 0; r < n; ++r) {
     if (group[r] != 0 && group[r] != 1) return VC_ERR_INVALID;
     D += cost[r].draft_ns;
@@ -42,9 +53,10 @@ extern "C" vc_status vc_stagger_period(const vc_stagger_cost* cost, int32_t n, c
     if (group[r] == 0) {
       dA += cost[r].draft_ns;
       sA += cost[r].stage_ns;
+      vA += cost[r].verify_ns;
     }
   }
-  *period_ns = V + phase_sum(dA, sA, D, S);
+  *period_ns = (period2(dA, sA, vA, D, S, V) + 1) / 2;
   return VC_OK;
 }
 
@@ -59,11 +71,12 @@ extern "C" vc_status vc_plan_stagger(const vc_stagger_cost* cost, int32_t n, int
     V += cost[r].verify_ns;
   }
   // bit r-1 of the mask = group of request r (request 0 stays in A); start with everyone in A and
-  // walk the reflected Gray code, which flips one request per step
+  // walk the reflected Gray code, which flips one request per step. Mask 0 (B empty) is a split
+  // only when there is a single request.
   const uint32_t count = 1u << (n - 1);
   uint32_t mask = 0, best_mask = 0;
-  int64_t dA = D, sA = S;
-  int64_t best = phase_sum(dA, sA, D, S);
+  int64_t dA = D, sA = S, vA = V;
+  int64_t best = n == 1 ? period2(dA, sA, vA, D, S, V) : INT64_MAX;
   for (uint32_t i = 1; i < count; ++i) {
     const int bit = __builtin_ctz(i);
     const vc_stagger_cost& c = cost[bit + 1];
@@ -71,11 +84,13 @@ extern "C" vc_status vc_plan_stagger(const vc_stagger_cost* cost, int32_t n, int
     if (mask & (1u << bit)) {  // request bit+1 moved to B
       dA -= c.draft_ns;
       sA -= c.stage_ns;
+      vA -= c.verify_ns;
     } else {
       dA += c.draft_ns;
       sA += c.stage_ns;
+      vA += c.verify_ns;
     }
-    const int64_t t = phase_sum(dA, sA, D, S);
+    const int64_t t = period2(dA, sA, vA, D, S, V);
     if (t < best || (t == best && mask < best_mask)) {
       best = t;
       best_mask = mask;
@@ -83,6 +98,6 @@ extern "C" vc_status vc_plan_stagger(const vc_stagger_cost* cost, int32_t n, int
   }
   group[0] = 0;
   for (int32_t r = 1; r < n; ++r) group[r] = (int32_t)((best_mask >> (r - 1)) & 1u);
-  if (period_ns) *period_ns = V + best;
+  if (period_ns) *period_ns = (best + 1) / 2;
   return VC_OK;
 }

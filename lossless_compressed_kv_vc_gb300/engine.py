@@ -334,9 +334,14 @@ class StaggeredOffload:
     (each head's K and V rows are contiguous in the [K; V][Hkv][cap][d] layout), each range records
     its own event, and the compute stream verifies each head range (vc_verify_attn_heads) as soon as
     it has landed, so only the last range's verification remains once the copy ends.
+
+    host_kv[g][i] (pinned [K; V] buffer) and slots[g][i] (its device copy, which request i's KV_full
+    descriptor points at) are None for a request whose KV_full stays in HBM; such a request drafts
+    and verifies in its group's phases with nothing to copy. plan_groups chooses the groups.
     """
 
-    def __init__(self, groups: List[Batch], host_kv: List[List[torch.Tensor]], slots: List[List[torch.Tensor]],
+    def __init__(self, groups: List[Batch], host_kv: List[List[Optional[torch.Tensor]]],
+                 slots: List[List[Optional[torch.Tensor]]],
                  copy_stream, compute_stream, chunk_bytes: int = 64 << 20, head_chunks: int = 1):
         assert len(groups) == 2
         Hkv = groups[0].Hkv
@@ -360,6 +365,8 @@ class StaggeredOffload:
         for c in range(len(self.edges) - 1):
             h0, h1 = self.edges[c], self.edges[c + 1]
             for h, d in zip(self.host_kv[g], self.slots[g]):
+                if h is None:  # this request's KV_full stays in HBM
+                    continue
                 for kv in range(2):
                     src, dst = h[kv, h0:h1], d[kv, h0:h1]
                     vc_stage_full_kv(src, dst, src.numel() * src.element_size(), self.chunk_bytes, self.copy_stream,
@@ -397,6 +404,19 @@ class StaggeredOffload:
         ev = events or {}
         self.phase(0, io, ev.get("draft0"), ev.get("stage1"), ev.get("verified1"))
         self.phase(1, io, ev.get("draft1"), ev.get("stage0"), ev.get("verified0"))
+
+
+def stagger_costs(draft_ns, verify_ns, stage_ns):
+    """(draft, verify, stage) integer nanoseconds per request, as vc_plan_stagger takes them."""
+    return [(int(round(d)), int(round(v)), int(round(s))) for d, v, s in zip(draft_ns, verify_ns, stage_ns)]
+
+
+def plan_groups(costs):
+    """Split requests into the two alternating groups of StaggeredOffload by the library's exact
+    planner (vc_plan_stagger). Returns ([indices of group 0], [indices of group 1], period_ns)."""
+    from . import vc_plan_stagger
+    st, groups, t = vc_plan_stagger(costs)
+    return [r for r, g in enumerate(groups) if g == 0], [r for r, g in enumerate(groups) if g == 1], t
 
 
 def move_full_kv_to_host(groups: List[Batch]):

@@ -332,15 +332,16 @@ def accept(logits: np.ndarray, draft: Sequence[int], L: int) -> Tuple[List[int],
 # ----------------------------------------------------------------------------------------------
 # staggering plan (two alternating groups)
 # ----------------------------------------------------------------------------------------------
-def stagger_period(costs: Sequence[Tuple[int, int, int]], groups: Sequence[int]) -> int:
-    """Period of the two-phase stagger ("Cross-resource staggering (P1)"; the pages fix no formula,
-    this is the reading stated with the library's planner).
+def stagger_period2(costs: Sequence[Tuple[int, int, int]], groups: Sequence[int]) -> int:
+    """Twice the steady-state period of the two-group stagger ("Cross-resource staggering (P1)";
+    the pages fix no schedule, this is the reading stated with the library's planner).
 
     costs[r] = (d, v, s): draft-phase time, verification-and-accept time and host-link copy time of
-    request r (s = 0 when its KV_full stays in HBM); groups[r] in {0, 1}. Phase 1: group 0 drafts
-    while group 1 is copied, then group 1 verifies; phase 2 swaps. A verification waits for the
-    drafting before it and for its own copy:
-        T = max(D_0, S_1) + V_1 + max(D_1, S_0) + V_0.
+    request r (s = 0 when its KV_full stays in HBM); groups[r] in {0, 1}. Schedule: the compute
+    stream repeats [draft 0, verify 1, draft 1, verify 0], the copy stream [copy 1, copy 0]; a
+    verification waits for its group's copy of the same period, a copy for its group's previous
+    verification. The period is the largest cycle mean of that max-plus system:
+        T = max(D + V, S, S_0 + V_0, S_1 + V_1, (S + V + D_0) / 2, (S + V + D_1) / 2).
     """
     D = [0, 0]
     S = [0, 0]
@@ -349,22 +350,31 @@ def stagger_period(costs: Sequence[Tuple[int, int, int]], groups: Sequence[int])
         D[g] += d
         S[g] += s
         V[g] += v
-    return max(D[0], S[1]) + V[1] + max(D[1], S[0]) + V[0]
+    Dt, St, Vt = sum(D), sum(S), sum(V)
+    return max(2 * (Dt + Vt), 2 * St, 2 * (S[0] + V[0]), 2 * (S[1] + V[1]), St + Vt + D[0], St + Vt + D[1])
+
+
+def stagger_period(costs: Sequence[Tuple[int, int, int]], groups: Sequence[int]) -> int:
+    """The period, rounded up to a whole unit."""
+    return (stagger_period2(costs, groups) + 1) // 2
 
 
 def plan_stagger(costs: Sequence[Tuple[int, int, int]]) -> Tuple[List[int], int]:
-    """Best split by brute force: every assignment with request 0 in group 0, minimum period, ties
-    to the smallest sum of groups[r] * 2^(r-1). Returns (groups, period)."""
+    """Best split by brute force: every assignment with request 0 in group 0 and, for n >= 2, at
+    least one request in group 1; minimum period (compared as 2T), ties to the smallest sum of
+    groups[r] * 2^(r-1). Returns (groups, period)."""
     import itertools
     n = len(costs)
     best = None
     for tail in itertools.product((0, 1), repeat=n - 1):
+        if n >= 2 and not any(tail):
+            continue
         groups = [0] + list(tail)
         key = sum(g << (r - 1) for r, g in enumerate(groups) if r >= 1)
-        t = stagger_period(costs, groups)
-        if best is None or (t, key) < (best[0], best[1]):
-            best = (t, key, groups)
-    return best[2], best[0]
+        t2 = stagger_period2(costs, groups)
+        if best is None or (t2, key) < (best[0], best[1]):
+            best = (t2, key, groups)
+    return best[2], (best[0] + 1) // 2
 
 
 # ----------------------------------------------------------------------------------------------

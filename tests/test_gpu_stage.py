@@ -141,3 +141,70 @@ def test_round_from_host_matches_device_round_and_oracle(vc):
             rt, rn = O.accept(lg[b], dr[b], w.L[b])
             assert int(hr.host_n_acc[b]) == rn, (rnd, b)
             assert hr.host_tokens[b, :rn].tolist() == rt
+
+
+def test_planned_stagger_with_resident_requests_matches_oracle(vc):
+    """Six 2-bit requests of the mixed serving workload (scaled), three with KV_full on the host and
+    three resident: groups from the planner, one period; drafts, verifications and accepted tokens
+    match the oracle, and the host requests' slots hold the staged bytes."""
+    from lossless_compressed_kv_vc_gb300 import engine
+    full = configs.mixed_serving()
+    w = configs.subset(full, full.request_indices("quant")[:6])
+    w = configs.scaled(w, ctx_div=64, L=5)
+    w.V = 3000
+    reqs, host, slot, ref = [], [], [], []
+    for b in range(w.B):
+        ri = gen.request(w, 0, b, "cuda")
+        ref.append((f32(ri.k_full), f32(ri.v_full)))
+        kf, vf, h, s = ri.k_full, ri.v_full, None, None
+        if w.on_host[b]:
+            s = torch.stack([kf, vf])
+            h = torch.empty(s.shape, dtype=s.dtype, pin_memory=True)
+            h.copy_(s)
+            kf, vf = s[0], s[1]
+        host.append(h)
+        slot.append(s)
+        reqs.append(engine.Req(mode=vc.VC_QUANT, ctx=w.ctx[b], L=w.L[b], k_full=kf, v_full=vf, q=ri.q,
+                               k_new=ri.k_new, v_new=ri.v_new, bits=w.bits))
+    costs = engine.stagger_costs([w.ctx[b] * w.L[b] for b in range(w.B)], [w.ctx[b] for b in range(w.B)],
+                                 [8 * w.ctx[b] if w.on_host[b] else 0 for b in range(w.B)])
+    g0, g1, _ = engine.plan_groups(costs)
+    assert g0 and g1
+    idx = [g0, g1]
+    groups = [engine.Batch(w.Hq, w.Hkv, w.d, [reqs[b] for b in ix], residual_min=w.residual_min) for ix in idx]
+    for bt in groups:
+        bt.compress()
+        bt.prepare_steps()
+    draft, logits, L = gen.drafts_and_logits(w, 0, "cuda")
+    io = []
+    for ix in idx:
+        sel = torch.tensor(ix, device="cuda")
+        io.append((logits[sel].contiguous(), draft[sel].contiguous(), L[sel].contiguous(),
+                   torch.empty((len(ix), w.L_max + 1), dtype=torch.int32, device="cuda"),
+                   torch.empty((len(ix),), dtype=torch.int32, device="cuda")))
+    for s in slot:  # the staged copies must bring the bytes back
+        if s is not None:
+            s.zero_()
+    cs, ks = torch.cuda.Stream(), torch.cuda.Stream()
+    for shape, arr, act in groups[1]._steps:
+        vc.vc_draft_attn(shape, arr, groups[1].ws_draft, groups[1].dev_status, ks)
+    ks.synchronize()
+    sg = engine.StaggeredOffload(groups, [[host[b] for b in ix] for ix in idx], [[slot[b] for b in ix] for ix in idx],
+                                 cs, ks, chunk_bytes=1 << 20)
+    sg.period(io)
+    torch.cuda.synchronize()
+    for gi, (bt, ix) in enumerate(zip(groups, idx)):
+        assert int(bt.dev_status.item()) == 0
+        lg, dr, Lg, tok, nacc = io[gi]
+        for i, b in enumerate(ix):
+            r = bt.reqs[i]
+            kf, vf = ref[b]
+            if host[b] is not None:
+                assert torch.equal(slot[b].cpu(), host[b])
+            km, vm, kw0, vw0 = oracle_main(w, b, kf, vf)
+            assert_attn_close(r.o_draft, O.draft_round(f32(r.q), km, vm, kw0, vw0, f32(r.k_new), f32(r.v_new)),
+                              f"draft b{b}")
+            ref_v = O.verify_attn(f32(r.q), kf, vf, f32(r.k_new).transpose(1, 0, 2), f32(r.v_new).transpose(1, 0, 2))
+            assert_attn_close(r.o_verify, ref_v, f"verify b{b}")
+            rt, rn = O.accept(lg[i].cpu().numpy(), dr[i].cpu().numpy(), int(Lg[i]))
+            assert int(nacc[i]) == rn and tok[i, :rn].cpu().tolist() == rt

@@ -353,62 +353,66 @@ def test_quantize_with_no_whole_block(bits):
 
 
 # ---------------------------------------------------------------------------- staggering plan --
-def _simulate_stagger(costs, groups):
-    """Event-by-event schedule of one period: a compute stream that drafts one group request by
-    request, then verifies the other group request by request once each request's copy has
-    landed; a copy stream that copies the verified group's requests one after another from the
-    phase start. Returns the period (end of the second phase)."""
-    t = 0
-    for drafting in (0, 1):
-        verifying = 1 - drafting
+def _simulate_streams(costs, groups, periods=1680):
+    """Run the two streams of the stagger for many periods, event by event: the copy stream copies
+    group 1 then group 0, each copy waiting for the previous verification of its group (its
+    staging slot); the compute stream drafts group 0, verifies group 1 (after that period's copy of
+    group 1), drafts group 1, verifies group 0 (after its copy). Returns twice the mean period over
+    the second half (840 periods: a multiple of every cyclicity a six-event system can have)."""
+    from fractions import Fraction
+    tot = lambda g, i: sum(c[i] for c, x in zip(costs, groups) if x == g)
+    d0, v0, s0 = tot(0, 0), tot(0, 1), tot(0, 2)
+    d1, v1, s1 = tot(1, 0), tot(1, 1), tot(1, 2)
+    compute = copy = ver0 = ver1 = 0
+    ends = []
+    for _ in range(periods):
+        c1 = max(copy, ver1) + s1
+        c0 = max(c1, ver0) + s0
+        copy = c0
+        t = compute + d0
+        t = max(t, c1) + v1
+        ver1 = t
+        t = t + d1
+        t = max(t, c0) + v0
+        ver0 = t
         compute = t
-        for (d, v, s), g in zip(costs, groups):
-            if g == drafting:
-                compute += d
-        copy = t
-        landed = []
-        for (d, v, s), g in zip(costs, groups):
-            if g == verifying:
-                copy += s
-                landed.append(copy)
-        # verification starts once drafting is over and every copy of the group has landed
-        start = max([compute] + landed)
-        for (d, v, s), g in zip(costs, groups):
-            if g == verifying:
-                start += v
-        t = start
-    return t
+        ends.append(t)
+    h = periods // 2
+    return Fraction(2 * (ends[-1] - ends[h - 1]), periods - h)
 
 
-def test_stagger_period_matches_event_simulation():
+def test_stagger_period_matches_stream_simulation():
     rng = np.random.default_rng(7)
-    for _ in range(200):
+    for _ in range(300):
         n = int(rng.integers(1, 7))
         costs = [tuple(int(x) for x in rng.integers(0, 50, 3)) for _ in range(n)]
         groups = [int(x) for x in rng.integers(0, 2, n)]
-        assert O.stagger_period(costs, groups) == _simulate_stagger(costs, groups)
+        assert O.stagger_period2(costs, groups) == _simulate_streams(costs, groups)
 
 
-def test_stagger_identical_requests_split_evenly():
-    """n = 6 requests with d = s = 10, v = 1: k in group 0 gives 2 * 10 * max(k, 6 - k) + 6, least
-    at k = 3: 66, and the smallest mask with three of requests 1..5 in group 1 is 0b00111."""
-    groups, t = O.plan_stagger([(10, 1, 10)] * 6)
-    assert t == 66 and groups == [0, 1, 1, 1, 0, 0]
+def test_stagger_copy_bound_pairs_split():
+    """Two requests each copying 100 and verifying 50, no drafting: together in one group the copy
+    and its verification chain (S_0 + V_0 = 300); split, the copy stream bounds it (S = 200)."""
+    groups, t = O.plan_stagger([(0, 50, 100), (0, 50, 100)])
+    assert groups == [0, 1] and t == 200
+    assert O.stagger_period([(0, 50, 100), (0, 50, 100)], [0, 0]) == 300
+
+
+def test_stagger_balanced_split_unique_size():
+    """Four requests (d 0, v 10, s 10): k of them in group 0 give max(40, 40, 20k, 20(4 - k), 40,
+    40), least (40) only at k = 2; the smallest mask with two of requests 1..3 in group 1 is 0b011."""
+    groups, t = O.plan_stagger([(0, 10, 10)] * 4)
+    assert groups == [0, 1, 1, 0] and t == 40
 
 
 def test_stagger_resident_only_any_split():
-    """No copies: every split costs D + V, so the tie-break keeps everyone in group 0."""
+    """No copies: every split costs D + V, so the tie-break takes the smallest non-empty group 1
+    (request 1 alone). A single request stays alone in group 0: its copy overlaps its own drafting
+    and its verification follows the copy, max(D, S) + V = max(5, 9) + 2 = 11."""
     costs = [(5, 2, 0), (7, 1, 0), (3, 3, 0), (11, 0, 0)]
     groups, t = O.plan_stagger(costs)
-    assert t == 26 + 6 and groups == [0, 0, 0, 0]
-
-
-def test_stagger_copy_hidden_under_other_drafts():
-    """One request with a long copy (100) and two resident requests drafting 50 each: the copy
-    hides under their drafting only when they form the other group: T = 1 + 100 = 101."""
-    groups, t = O.plan_stagger([(1, 0, 100), (50, 0, 0), (50, 0, 0)])
-    assert groups == [0, 1, 1] and t == 101
-    assert O.stagger_period([(1, 0, 100), (50, 0, 0), (50, 0, 0)], [0, 0, 1]) == 151
+    assert t == 26 + 6 and groups == [0, 1, 0, 0]
+    assert O.plan_stagger([(5, 2, 9)]) == ([0], 11)
 
 
 def test_stagger_bounds_and_symmetry():
@@ -418,5 +422,5 @@ def test_stagger_bounds_and_symmetry():
         costs = [tuple(int(x) for x in rng.integers(0, 100, 3)) for _ in range(n)]
         D, V, S = (sum(c[i] for c in costs) for i in range(3))
         groups, t = O.plan_stagger(costs)
-        assert max(D, S) + V <= t <= D + S + V
-        assert O.stagger_period(costs, [1 - g for g in groups]) == t
+        assert max(D + V, S) <= t <= D + S + V
+        assert O.stagger_period2(costs, [1 - g for g in groups]) == O.stagger_period2(costs, groups)

@@ -111,6 +111,14 @@ def mixed_serving(seed: int = 0) -> Workload:
                     L, 128256, p, on_host, rounds=20, seed=seed)
 
 
+def subset(w: Workload, pick: List[int], name: str | None = None) -> Workload:
+    """The requests `pick` of w, in that order, as a workload of their own (same shapes)."""
+    sel = lambda xs: [xs[b] for b in pick]
+    return Workload(name or (w.name + f"_sub{len(pick)}"), len(pick), w.Hq, w.Hkv, w.d, sel(w.ctx), sel(w.mode),
+                    sel(w.keep), sel(w.recent), w.bits, w.residual_min, sel(w.L), w.V, sel(w.p), sel(w.on_host),
+                    w.rounds, w.seed)
+
+
 ALL = [tiny, llama8b_drop, qwen32b_quant2, llama70b_offload4, mixed_serving]
 
 
