@@ -46,11 +46,13 @@ def parse():
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-heads", type=int, default=1, help=argparse.SUPPRESS)
     ap.add_argument("--child-steps", type=int, default=1, help=argparse.SUPPRESS)
-    ap.add_argument("--workload", default="llama8b_drop", choices=["llama8b_drop", "offload", "stagger"],
+    ap.add_argument("--workload", default="llama8b_drop", choices=["llama8b_drop", "offload", "stagger", "importance"],
                     help="llama8b_drop: the headline round; offload: Llama-70B-shape 4-bit requests with KV_full "
                          "in pinned host memory, two drafting while two stage and verify; stagger: the 16 "
                          "2-bit requests of the mixed serving workload (half with KV_full on the host) under "
-                         "a naive split and under the planner's split")
+                         "a naive split and under the planner's split; importance: SnapKV-style importance of the "
+                         "headline workload's contexts from a 32-token observation window")
+    ap.add_argument("--window", type=int, default=32, help="importance workload: observation window")
     ap.add_argument("--ctx-div", type=int, default=1,
                     help="offload workload: divide the context (a smaller case for profiler captures)")
     ap.add_argument("--compact", action="store_true",
@@ -653,6 +655,53 @@ def run_stagger(args):
     return 0
 
 
+def run_importance(args):
+    """SnapKV-style importance (vc_snapkv_importance, 4 launches) for every request of the headline
+    workload (8 x 32768 context tokens, 32/8 heads, d 128), window 32, max pooling of width 7.
+    value = context tokens scored per second. Roofline: the two passes read every key twice
+    (2 x Hkv x ctx x d x 2 B per request) and do 2 x 2 x (W G) x ctx x d x Hkv flops."""
+    import torch
+    from workloads import gen
+    w = workload()
+    device = "cuda"
+    bt, *_ = setup_native(w, device)
+    q_obs = [gen.observation_queries(w, b, args.window, device) for b in range(w.B)]
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        bt.snapkv_importance(q_obs, args.window, 7, stream=stream)
+    torch.cuda.synchronize()
+    assert int(bt.dev_status.item()) == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            bt.snapkv_importance(q_obs, args.window, 7, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    t_ms = e0.elapsed_time(e1) / args.steps
+    G, R = w.Hq // w.Hkv, args.window * w.Hq // w.Hkv
+    tokens = sum(w.ctx)
+    key_bytes = sum(2 * w.Hkv * c * w.d * 2 for c in w.ctx)
+    flops = sum(2 * 2 * R * c * w.d * w.Hkv for c in w.ctx)
+    peaks, kind = measured_peaks()
+    gbs, tfs = key_bytes / (t_ms / 1e3) / 1e9, flops / (t_ms / 1e3) / 1e12
+    line = {"metric": "SnapKV-style importance: context tokens scored/s", "value": tokens / (t_ms / 1e3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name + "_importance", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                       "ctx": w.ctx[0], "window": args.window, "rows_per_kv_head": R, "pool": "max 7",
+                       "l2": "keys 1.07 GB per pass, larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                         "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                         "tensor_tflops": tfs, "tensor_frac_of_bf16_peak": tfs / float(peaks["bf16_tflops"]),
+                         "kernel": "imp_stats + imp_lse + imp_votes + imp_pool (one vc_snapkv_importance call)",
+                         "algorithmic_bytes_per_launch": key_bytes, "flops_per_launch": flops, "peak_kind": kind},
+            "clocks": clk.summary()}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse()
     if args.cpu_child:
@@ -663,6 +712,8 @@ def main():
         return run_offload(args)
     if args.workload == "stagger":
         return run_stagger(args)
+    if args.workload == "importance":
+        return run_importance(args)
     return run_native(args)
 
 

@@ -285,6 +285,40 @@ vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, si
                            cudaStream_t copy_stream, cudaEvent_t done);
 
 /* ------------------------------------------------------------------------------------------ */
+/* vc_snapkv_importance — token importance for the keep-set of a token-drop request, SnapKV style
+ * ("Architecture support": SnapKV is one of the token-drop compressors behind the compressor
+ * interface; the pages name it without defining its scoring, so this is a plain reading of it).
+ *
+ * The last `window` = W context tokens form the observation window; their queries q_obs attend,
+ * causally, to the keys of KV_full (window query i sits at position ctx - W + i and sees keys
+ * 0 .. ctx - W + i), scale 1/sqrt(d), GQA as in the other calls. The vote of key t is the sum of
+ * its softmax weights over the W queries and all Hq query heads; importance[t] pools the votes over
+ * |u - t| <= pool_kernel / 2: VC_POOL_MAX takes the largest in-range vote, VC_POOL_AVG the sum of
+ * the in-range votes divided by pool_kernel (zero padding). pool_kernel = 1 leaves the votes as
+ * they are. The result feeds vc_compress_kv's importance (any scale: only the order matters).
+ * Arithmetic: bf16 products accumulated in fp32 on the tensor cores, softmax in fp32 (exp2 domain).
+ *
+ * Requirements: d = 64 or 128; W * (Hq/Hkv) a multiple of 32 and at most 256; pool_kernel odd,
+ * 1..65; W <= ctx <= cap for every request; k, q_obs 16-byte aligned, importance 4-byte aligned.
+ * The workspace (256-byte aligned) holds per-chunk row statistics and per-KV-head votes:
+ * vc_importance_workspace_size(shape, W, max_ctx) bytes cover requests of up to max_ctx tokens.
+ * Returns VC_ERR_INVALID / VC_ERR_UNSUPPORTED / VC_ERR_WORKSPACE before launching anything. */
+#define VC_POOL_MAX 0
+#define VC_POOL_AVG 1
+
+typedef struct vc_importance_req {
+  vc_kv_full full;        /* keys read: K rows 0..ctx-1 of every KV head (V is not read) */
+  const void* q_obs;      /* bf16 [W][Hq][d]: queries of context tokens ctx-W .. ctx-1 */
+  float* importance;      /* fp32 [ctx] output */
+} vc_importance_req;
+
+vc_status vc_snapkv_importance(const vc_shape* shape, const vc_importance_req* req, int32_t window,
+                               int32_t pool_kernel, int32_t pool_kind, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, cudaStream_t stream);
+
+size_t vc_importance_workspace_size(const vc_shape* shape, int32_t window, int32_t max_ctx);
+
+/* ------------------------------------------------------------------------------------------ */
 /* vc_plan_stagger — choose the two alternating groups of cross-resource staggering ("Cross-resource
  * staggering (P1)": while some requests draft, bound by HBM bandwidth, the KV_full of others moves
  * over the host link and is verified; the pages fix no rule for choosing who does which).

@@ -27,6 +27,7 @@ VC_CALL_DRAFT, VC_CALL_VERIFY = 0, 1
 VC_MAX_BATCH = 32
 VC_APPEND_MAX_ROWS = 256
 VC_STAGGER_MAX = 24
+VC_POOL_MAX, VC_POOL_AVG = 0, 1
 
 _p = C.c_void_p
 _i32 = C.c_int32
@@ -55,6 +56,10 @@ class vc_append_req(C.Structure):
     _fields_ = [("k_rows", _p), ("v_rows", _p), ("n_rows", _i32)]
 
 
+class vc_importance_req(C.Structure):
+    _fields_ = [("full", vc_kv_full), ("q_obs", _p), ("importance", _p)]
+
+
 class vc_stagger_cost(C.Structure):
     _fields_ = [("draft_ns", C.c_int64), ("verify_ns", C.c_int64), ("stage_ns", C.c_int64)]
 
@@ -75,6 +80,10 @@ _lib.vc_accept.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p, _p, _p]
 _lib.vc_append_kv.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_kv_full), C.POINTER(vc_kv_comp),
                               C.POINTER(vc_append_req), _i32, _p, _p]
 _lib.vc_stage_full_kv.argtypes = [_p, _p, C.c_size_t, C.c_size_t, _p, _p]
+_lib.vc_snapkv_importance.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_importance_req), _i32, _i32, _i32, _p,
+                                      C.c_size_t, _p, _p]
+_lib.vc_importance_workspace_size.argtypes = [C.POINTER(vc_shape), _i32, _i32]
+_lib.vc_importance_workspace_size.restype = C.c_size_t
 _lib.vc_plan_stagger.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
 _lib.vc_stagger_period.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
 _lib.vc_workspace_size.argtypes = [_i32, C.POINTER(vc_shape), _i32]
@@ -83,12 +92,14 @@ _lib.vc_status_string.argtypes = [_i32]
 _lib.vc_status_string.restype = C.c_char_p
 _lib.vc_version.restype = _i32
 for _f in ("vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
-           "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_plan_stagger", "vc_stagger_period"):
+           "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_plan_stagger", "vc_stagger_period",
+           "vc_snapkv_importance"):
     getattr(_lib, _f).restype = _i32
 
 EXPORTS = ["vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
            "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_plan_stagger", "vc_stagger_period",
-           "vc_workspace_size", "vc_status_string", "vc_version"]
+           "vc_snapkv_importance", "vc_importance_workspace_size", "vc_workspace_size", "vc_status_string",
+           "vc_version"]
 
 
 class VCError(RuntimeError):
@@ -193,6 +204,19 @@ def vc_stage_full_kv(host_src, dev_dst, nbytes: int, chunk_bytes: int = 0, copy_
     ev = done.cuda_event if done is not None and not isinstance(done, int) else done
     st = _lib.vc_stage_full_kv(_ptr(host_src), _ptr(dev_dst), nbytes, chunk_bytes, _stream(copy_stream), ev)
     return _check(st, "vc_stage_full_kv", raise_on_error)
+
+
+def vc_importance_workspace_size(shape: vc_shape, window: int, max_ctx: int) -> int:
+    return _lib.vc_importance_workspace_size(C.byref(shape), window, max_ctx)
+
+
+def vc_snapkv_importance(shape: vc_shape, req, window: int, pool_kernel: int = 7, pool_kind: int = VC_POOL_MAX,
+                         ws=None, dev_status=None, stream=None, raise_on_error=True) -> int:
+    """req: vc_importance_req array [B]; writes each request's importance [ctx]."""
+    wsb = ws.numel() * ws.element_size() if ws is not None else 0
+    st = _lib.vc_snapkv_importance(C.byref(shape), req, window, pool_kernel, pool_kind, _ptr(ws), wsb,
+                                   _ptr(dev_status), _stream(stream))
+    return _check(st, "vc_snapkv_importance", raise_on_error)
 
 
 def _costs(costs):

@@ -13,7 +13,8 @@ from typing import List, Optional
 
 import torch
 
-from . import (vc_shape, vc_kv_full, vc_kv_comp, vc_draft_req, vc_verify_req, vc_append_req, vc_compress_kv,
+from . import (vc_shape, vc_kv_full, vc_kv_comp, vc_draft_req, vc_verify_req, vc_append_req, vc_importance_req,
+               vc_snapkv_importance, vc_importance_workspace_size, VC_POOL_MAX, vc_compress_kv,
                vc_draft_attn, vc_verify_attn, vc_verify_attn_heads, vc_accept, vc_append_kv, vc_workspace_size,
                VC_TOKEN_DROP, VC_QUANT, VC_CALL_DRAFT, VC_CALL_VERIFY)
 
@@ -142,6 +143,25 @@ class Batch:
         f.k, f.v, f.cap = k.data_ptr(), v.data_ptr(), k.shape[1]
 
     # ---- the round's calls -------------------------------------------------------------------
+    def snapkv_importance(self, q_obs, window: int, pool_kernel: int = 7, pool_kind: int = VC_POOL_MAX, stream=None):
+        """Fill every token-drop request's importance from its observation window (SnapKV style,
+        vc_snapkv_importance): q_obs[b] is request b's bf16 [window][Hq][d] queries of its last
+        `window` context tokens. The next compress selects the keep-set from it."""
+        drop = [b for b, r in enumerate(self.reqs) if r.mode == VC_TOKEN_DROP]
+        if not drop:
+            return
+        arr = (vc_importance_req * len(drop))()
+        for i, b in enumerate(drop):
+            arr[i].full = self.full[b]
+            arr[i].q_obs = q_obs[b].data_ptr()
+            arr[i].importance = self.reqs[b].importance.data_ptr()
+        shape = vc_shape(len(drop), self.Hq, self.Hkv, self.d)
+        need = vc_importance_workspace_size(shape, window, max(self.reqs[b].ctx for b in drop))
+        ws = getattr(self, "ws_importance", None)
+        if ws is None or ws.numel() * 4 < need:
+            ws = self.ws_importance = torch.empty(need // 4 + 64, dtype=torch.float32, device=self.device)
+        vc_snapkv_importance(shape, arr, window, pool_kernel, pool_kind, ws, self.dev_status, stream)
+
     def compress(self, stream=None):
         mode = self.reqs[0].mode
         if mode == VC_TOKEN_DROP:

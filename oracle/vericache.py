@@ -330,6 +330,47 @@ def accept(logits: np.ndarray, draft: Sequence[int], L: int) -> Tuple[List[int],
 
 
 # ----------------------------------------------------------------------------------------------
+# a0 input. SnapKV-style importance (observation-window votes, pooled)
+# ----------------------------------------------------------------------------------------------
+def snapkv_votes(q_obs: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """Votes of the observation window ("Architecture support" names SnapKV among the token-drop
+    compressors; the pages do not define its scoring, this is the plain reading).
+
+    q_obs [W][Hq][d]: queries of the last W context tokens (window query i at position
+    ctx - W + i); k [Hkv][ctx][d]: KV_full keys. Query head h reads KV head h // (Hq/Hkv). Row
+    (i, h) takes the softmax of q k^T / sqrt(d) over keys 0 .. ctx - W + i; vote[t] is the sum of
+    key t's weights over every row. float64, returns [ctx]."""
+    W, Hq, d = q_obs.shape
+    Hkv, ctx, _ = k.shape
+    G = Hq // Hkv
+    votes = np.zeros(ctx, dtype=np.float64)
+    for h in range(Hq):
+        scores = q_obs[:, h, :].astype(np.float64) @ k[h // G].astype(np.float64).T / math.sqrt(d)
+        for i in range(W):
+            pos = ctx - W + i
+            s = scores[i, : pos + 1]
+            a = np.exp(s - s.max())
+            votes[: pos + 1] += a / a.sum()
+    return votes
+
+
+def pool_votes(votes: np.ndarray, kernel: int, kind: str) -> np.ndarray:
+    """1-D pooling of width `kernel` (odd) centred on each token: "max" takes the largest vote in
+    range, "avg" the in-range sum divided by the width (zero padding outside the context)."""
+    half = kernel // 2
+    n = len(votes)
+    out = np.empty(n, dtype=np.float64)
+    for t in range(n):
+        win = votes[max(0, t - half): min(n, t + half + 1)]
+        out[t] = win.max() if kind == "max" else win.sum() / kernel
+    return out
+
+
+def snapkv_importance(q_obs: np.ndarray, k: np.ndarray, pool_kernel: int = 7, pool: str = "max") -> np.ndarray:
+    return pool_votes(snapkv_votes(q_obs, k), pool_kernel, pool)
+
+
+# ----------------------------------------------------------------------------------------------
 # staggering plan (two alternating groups)
 # ----------------------------------------------------------------------------------------------
 def stagger_period2(costs: Sequence[Tuple[int, int, int]], groups: Sequence[int]) -> int:

@@ -29,7 +29,7 @@ def declared_symbols():
 
 def test_header_declares_the_round_calls():
     names = declared_symbols()
-    for n in ["vc_compress_kv", "vc_draft_attn", "vc_verify_attn", "vc_verify_attn_heads", "vc_accept", "vc_stage_full_kv", "vc_append_kv",
+    for n in ["vc_compress_kv", "vc_draft_attn", "vc_verify_attn", "vc_verify_attn_heads", "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_snapkv_importance", "vc_plan_stagger",
               "vc_workspace_size", "vc_status_string"]:
         assert n in names
 
@@ -137,3 +137,23 @@ def test_plan_stagger_ties_and_limits():
     assert vc.vc_plan_stagger([(1, -1, 0)], raise_on_error=False)[0] == vc.VC_ERR_INVALID
     assert vc.vc_plan_stagger([(1 << 41, 0, 0)], raise_on_error=False)[0] == vc.VC_ERR_INVALID
     assert vc.vc_stagger_period([(1, 1, 1)], [2], raise_on_error=False)[0] == vc.VC_ERR_INVALID
+
+
+def test_importance_validation_rejects_without_launching(lib):
+    import lossless_compressed_kv_vc_gb300 as vc
+    arr = (vc.vc_importance_req * 1)()
+    arr[0].full.k, arr[0].full.v, arr[0].full.ctx, arr[0].full.cap = 1 << 12, 1 << 13, 100, 100
+    arr[0].q_obs, arr[0].importance = 1 << 14, 1 << 15
+    shp = vc.vc_shape(1, 8, 2, 128)  # G = 4
+    call = lambda W, k=7, kind=vc.VC_POOL_MAX, s=shp: vc.vc_snapkv_importance(s, arr, W, k, kind, None, None,
+                                                                                stream=0, raise_on_error=False)
+    assert call(6) == vc.VC_ERR_UNSUPPORTED       # 24 window rows: not a multiple of 32
+    assert call(128) == vc.VC_ERR_UNSUPPORTED     # 512 rows
+    assert call(8, k=4) == vc.VC_ERR_INVALID      # even pooling width
+    assert call(8, k=67) == vc.VC_ERR_UNSUPPORTED  # wider than 65
+    assert call(8, kind=2) == vc.VC_ERR_INVALID
+    assert call(8) == vc.VC_ERR_WORKSPACE         # valid request, no workspace
+    assert call(8, s=vc.vc_shape(1, 8, 2, 96)) == vc.VC_ERR_UNSUPPORTED
+    arr[0].full.ctx = 7
+    assert call(8) == vc.VC_ERR_INVALID           # context shorter than the window
+    assert vc.vc_importance_workspace_size(shp, 8, 100) > 0

@@ -424,3 +424,43 @@ def test_stagger_bounds_and_symmetry():
         groups, t = O.plan_stagger(costs)
         assert max(D + V, S) <= t <= D + S + V
         assert O.stagger_period2(costs, [1 - g for g in groups]) == O.stagger_period2(costs, groups)
+
+
+# ---------------------------------------------------------------------------- SnapKV importance --
+def test_snapkv_votes_sum_to_rows():
+    """Every (window query, head) row is a softmax over its visible keys: the votes sum to W * Hq."""
+    rng = np.random.default_rng(5)
+    q, k = rng.standard_normal((6, 8, 16)), rng.standard_normal((2, 50, 16))
+    assert math.isclose(O.snapkv_votes(q, k).sum(), 6 * 8, rel_tol=1e-12)
+
+
+def test_snapkv_single_query_is_attention_weights():
+    """W = 1, one head: the votes are the last query's attention weights, i.e. the (pinned)
+    attention of that query over the keys with one-hot values."""
+    rng = np.random.default_rng(6)
+    q, k = rng.standard_normal((1, 1, 16)), rng.standard_normal((1, 40, 16))
+    ref = O.attention(q[0], k[0], np.eye(40))[0]
+    assert np.allclose(O.snapkv_votes(q, k), ref, rtol=1e-12, atol=1e-15)
+
+
+def test_snapkv_constant_keys_closed_form():
+    """Identical keys make every row uniform over its visible keys: with ctx = 10 and W = 3, query i
+    sees keys 0 .. 7 + i, so vote[t] = Hq * sum over i with t <= 7 + i of 1 / (8 + i)."""
+    rng = np.random.default_rng(8)
+    q = rng.standard_normal((3, 4, 8))
+    k = np.tile(rng.standard_normal((1, 1, 8)), (2, 10, 1))
+    ref = np.array([4 * sum(1.0 / (8 + i) for i in range(3) if t <= 7 + i) for t in range(10)])
+    assert np.allclose(O.snapkv_votes(q, k), ref, rtol=1e-12)
+
+
+@pytest.mark.parametrize("kernel", [1, 3, 7])
+def test_pool_votes_matches_torch_pooling(kernel):
+    """Max pooling = torch max_pool1d with -inf padding; average pooling = avg_pool1d with zero
+    padding counted in the width (its default)."""
+    rng = np.random.default_rng(kernel)
+    v = rng.random(37)
+    t = torch.from_numpy(v)[None, None]
+    mx = torch.nn.functional.max_pool1d(t, kernel, stride=1, padding=kernel // 2)[0, 0].numpy()
+    av = torch.nn.functional.avg_pool1d(t, kernel, stride=1, padding=kernel // 2)[0, 0].numpy()
+    assert np.allclose(O.pool_votes(v, kernel, "max"), mx, rtol=0, atol=0)
+    assert np.allclose(O.pool_votes(v, kernel, "avg"), av, rtol=1e-12, atol=1e-15)

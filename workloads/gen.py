@@ -26,7 +26,8 @@ import torch
 
 from .configs import Workload, DROP
 
-KIND_K, KIND_V, KIND_IMP, KIND_Q, KIND_KNEW, KIND_VNEW, KIND_DRAFT, KIND_LOGITS, KIND_PLANT, KIND_APPK, KIND_APPV = range(11)
+(KIND_K, KIND_V, KIND_IMP, KIND_Q, KIND_KNEW, KIND_VNEW, KIND_DRAFT, KIND_LOGITS, KIND_PLANT, KIND_APPK, KIND_APPV,
+ KIND_QOBS) = range(12)
 
 
 def _gen(w: Workload, rnd: int, b: int, kind: int, device) -> torch.Generator:
@@ -60,6 +61,11 @@ def importance(w: Workload, b: int, device="cpu", n: int | None = None) -> torch
     """fp32 [n] ~ U[0,1) (n defaults to the context; a longer array serves a context that grows)."""
     g = _gen(w, 0, b, KIND_IMP, device)
     return torch.rand((w.ctx[b] if n is None else n,), generator=g, device=device, dtype=torch.float32)
+
+
+def observation_queries(w: Workload, b: int, window: int, device="cpu") -> torch.Tensor:
+    """bf16 [window][Hq][d] ~ N(0,1): queries of the request's last `window` context tokens."""
+    return randn_bf16((window, w.Hq, w.d), _gen(w, 0, b, KIND_QOBS, device), device)
 
 
 def appended_rows(w: Workload, rnd: int, b: int, n: int, device="cpu"):
