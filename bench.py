@@ -46,8 +46,10 @@ def parse():
     ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-heads", type=int, default=1, help=argparse.SUPPRESS)
     ap.add_argument("--child-steps", type=int, default=1, help=argparse.SUPPRESS)
-    ap.add_argument("--workload", default="llama8b_drop", choices=["llama8b_drop", "offload", "stagger", "importance"],
-                    help="llama8b_drop: the headline round; offload: Llama-70B-shape 4-bit requests with KV_full "
+    ap.add_argument("--workload", default="llama8b_drop",
+                    choices=["llama8b_drop", "qwen_quant2", "offload", "stagger", "importance"],
+                    help="llama8b_drop: the headline round; qwen_quant2: the same round on the Qwen-32B-like "
+                         "2-bit workload (16 x 65536 tokens, L 25); offload: Llama-70B-shape 4-bit requests with KV_full "
                          "in pinned host memory, two drafting while two stage and verify; stagger: the 16 "
                          "2-bit requests of the mixed serving workload (half with KV_full on the host) under "
                          "a naive split and under the planner's split; importance: SnapKV-style importance of the "
@@ -66,17 +68,19 @@ def parse():
                     help="offload and stagger workloads: drafts per round for every request (default: the "
                          "workload's L)")
     a = ap.parse_args()
-    global _BATCH
+    global _BATCH, _WORKLOAD
     _BATCH = a.batch
+    _WORKLOAD = a.workload
     return a
 
 
 _BATCH = None
+_WORKLOAD = "llama8b_drop"
 
 
 def workload():
     from workloads import configs
-    w = configs.llama8b_drop()
+    w = configs.qwen32b_quant2() if _WORKLOAD == "qwen_quant2" else configs.llama8b_drop()
     if _BATCH is not None and _BATCH < w.B:
         w = configs.scaled(w, batch=_BATCH)
     return w
@@ -267,12 +271,18 @@ def draft_algorithmic_bytes(w):
     """Bytes one draft step must move, summed over requests, averaged over the L steps: the kept
     K and V rows (keep x Hkv x 2 x d x 2 B), the window rows read, the index list (once per
     request), q in and o out, and the new row read and stored."""
+    from workloads import DROP
     d, total = w.d, 0.0
     for b in range(w.B):
-        keep = min(w.keep[b], w.ctx[b])
         win_avg = (w.L[b] + 1) / 2.0  # window rows 1..L over the round
-        total += w.Hkv * (keep + win_avg) * 2 * d * 2
-        total += keep * 4
+        if w.mode[b] == DROP:
+            keep = min(w.keep[b], w.ctx[b])
+            total += w.Hkv * (keep + win_avg) * 2 * d * 2
+            total += keep * 4
+        else:  # quantised groups: codes, fp16 scales and zeros; then the bf16 residual and window
+            ng = max(0, (w.ctx[b] - w.residual_min) // 32)
+            total += w.Hkv * 32 * ng * (2 * d * w.bits // 8 + 2 * 4 * d // 32)
+            total += w.Hkv * (w.ctx[b] - 32 * ng + win_avg) * 2 * d * 2
         total += 2 * w.Hq * d * 2
         total += 2 * 2 * w.Hkv * d * 2
     return total
@@ -282,15 +292,16 @@ def setup_native(w, device, compact=False):
     import torch
     import __graft_entry__ as g
     g.build()
-    from lossless_compressed_kv_vc_gb300 import engine, VC_TOKEN_DROP
-    from workloads import gen
+    from lossless_compressed_kv_vc_gb300 import engine, VC_TOKEN_DROP, VC_QUANT
+    from workloads import gen, DROP
     reqs = []
     for b in range(w.B):
         ri = gen.request(w, 0, b, device)
-        reqs.append(engine.Req(mode=VC_TOKEN_DROP, ctx=w.ctx[b], L=w.L[b], k_full=ri.k_full, v_full=ri.v_full,
-                               q=ri.q, k_new=ri.k_new, v_new=ri.v_new, importance=ri.importance, keep=w.keep[b],
-                               recent=w.recent[b], compact=compact))
-    bt = engine.Batch(w.Hq, w.Hkv, w.d, reqs, device=device)
+        reqs.append(engine.Req(mode=VC_TOKEN_DROP if w.mode[b] == DROP else VC_QUANT, ctx=w.ctx[b], L=w.L[b],
+                               k_full=ri.k_full, v_full=ri.v_full, q=ri.q, k_new=ri.k_new, v_new=ri.v_new,
+                               importance=ri.importance, keep=w.keep[b], recent=w.recent[b], compact=compact,
+                               bits=w.bits))
+    bt = engine.Batch(w.Hq, w.Hkv, w.d, reqs, residual_min=w.residual_min, device=device)
     bt.compress()
     bt.prepare_steps()
     draft, logits, L = gen.drafts_and_logits(w, 0, device)
@@ -362,26 +373,33 @@ def run_native(args):
                   barrier, dist, world, device)
 
     peaks, peak_kind = measured_peaks()
+    from workloads import DROP
+    quant = 0 if w.mode[0] == DROP else 1
     alg = draft_algorithmic_bytes(w)
     d_ms = statistics.mean(draft_ms)
     achieved = alg / (d_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                 "frac": achieved / float(peaks["hbm_gbs"]), "traffic": profiled_traffic(),
-                "kernel": "draft_attn_kernel<128,0,1> (one vc_draft_attn call, partial merge included; mean over "
-                          "the draft phase of each timed round)",
+                "kernel": "draft_attn_kernel<128,%d,1> (one vc_draft_attn call, partial merge included; mean over "
+                          "the draft phase of each timed round)" % (0 if quant == 0 else w.bits),
                 "algorithmic_bytes_per_launch": alg, "avg_launch_ms": d_ms, "peak_kind": peak_kind}
     # keep-set (+ gather when compacting), one draft launch per step, verify + its merge, accept (2)
-    launches_per_step = 1 + (1 if args.compact else 0) + w.L_max + 2 + 2
+    launches_per_step = (3 if quant else 1) + (1 if args.compact else 0) + w.L_max + 2 + 2
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "compact_keep_set": bool(args.compact), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "ctx": w.ctx[0],
                        "keep": w.keep[0], "recent": w.recent[0], "L": w.L[0], "V": w.V, "p": w.p[0],
                        "tokens_per_step": tokens_per_step,
-                       "l2": "inputs larger than L2 (full KV 1.07 GB, kept rows 268 MB per draft step, logits 135 MB)"},
+                       "l2": "inputs larger than L2 (full KV 1.07 GB, kept rows 268 MB per draft step, logits 135 MB)"
+                       if not quant else "inputs larger than L2 (full KV 4.3 GB, quantised cache 812 MB per draft "
+                                         "step, logits 243 MB)"},
             "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "roofline": roofline,
             "clocks": clk.summary()}
-    if rank == 0 and not args.no_cpu_baseline:
+    if quant:
+        line["config"].update({"bits": w.bits, "keep": None, "recent": None})
+        line["roofline"]["traffic"] = None
+    if rank == 0 and not args.no_cpu_baseline and not quant:
         rs, wall = run_cpu_child(w.Hkv, w.B)
         cb = cpu_baseline_obj(w, rs)
         cb["wall_s"] = wall

@@ -265,25 +265,41 @@ cudaError_t launch_keepset(const KeepParams& p, int max_keep, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// rs = the correctly rounded reciprocal of sf (0 when sf is 0), for quant_code.
 template <int BITS>
 __device__ __forceinline__ void quant_params(float mn, float mx, __half& s16, __half& z16, float& sf, float& zf,
-                                             int32_t* st) {
+                                             float& rs, int32_t* st) {
   constexpr float QMAX = (float)((1 << BITS) - 1);
   s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), QMAX));
   z16 = __float2half_rn(mn);
   sf = __half2float(s16);
   zf = __half2float(z16);
+  rs = sf != 0.f ? __frcp_rn(sf) : 0.f;
   if (!isfinite(sf) || !isfinite(zf)) set_status(st, VC_DEV_RANGE);
 }
 
+// code = clamp(rint(fl((x - z) / s)), 0, 2^BITS - 1) with fl the IEEE float32 quotient, computed as
+// y = fl(a * rs): rs is within 2^-24 of 1/s (relative) and the product adds one rounding, so
+// |y - a/s| <= 2^-23 |y| (+ tiny), below 3e-6 wherever the clamp does not decide (|y| <= 17). When
+// y is at least 1e-4 away from every half-integer, y, a/s and fl(a/s) lie strictly between the
+// same two half-integers and round to the same integer; otherwise (rarely) the quotient itself is
+// taken.
 template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float x, float sf, float zf) {
+__device__ __forceinline__ uint32_t quant_code(float x, float sf, float zf, float rs) {
   constexpr float QMAX = (float)((1 << BITS) - 1);
   if (sf == 0.f) return 0u;
-  float t = rintf(__fdiv_rn(__fsub_rn(x, zf), sf));
+  const float a = __fsub_rn(x, zf);
+  const float y = __fmul_rn(a, rs);
+  float t = rintf(y);
+  if (fabsf(y) <= QMAX + 2.f && fabsf(y - t) > 0.5f - 1e-4f) t = rintf(__fdiv_rn(a, sf));
   t = fminf(fmaxf(t, 0.f), QMAX);
   return (uint32_t)t;
 }
+
+// A 32-token block's codes in shared memory, one byte per (token or channel row, column); rows are
+// padded by 4 bytes so that eight consecutive rows fall on eight different banks.
+template <int D>
+using CodeTile = uint8_t[32][D + 4];
 
 // Storage of one 32-token block's codes: 32-bit words w[half][j][lane] (4-bit) or w[half][p][lane]
 // (2-bit, p covers steps j = 2p and 2p + 1). Word (half, j, lane), a = lane / 4, b = lane % 4, holds
@@ -296,7 +312,7 @@ __device__ __forceinline__ uint32_t quant_code(float x, float sf, float zf) {
 // so a lane's word is exactly the four 16-bit A-fragment registers of an m16n8k16 MMA over that
 // 16 x 16 tile (keys: M = tokens, K = channels; values: M = channels, K = tokens).
 template <int D, int BITS, bool KEYS>
-__device__ __forceinline__ uint32_t block_word(const uint8_t (*codes)[D], int widx) {
+__device__ __forceinline__ uint32_t block_word(const uint8_t (*codes)[D + 4], int widx) {
   constexpr int STEPS = BITS == 4 ? D / 16 : D / 32;  // words per (half, lane) row
   const int lane = widx & 31;
   const int step = (widx >> 5) % STEPS;
@@ -325,30 +341,35 @@ __device__ __forceinline__ uint32_t block_word(const uint8_t (*codes)[D], int wi
   return w;
 }
 
-// keys: grid (ng_max, Hkv, B), block D: thread c quantises channel c over the block's 32 tokens.
+// keys: grid (ng_max, Hkv, B), block D. The block's 32 x D keys (contiguous rows) are staged with
+// 16-byte loads; thread c then quantises channel c over the 32 tokens.
 template <int D, int BITS>
 __global__ void __launch_bounds__(D) quant_keys_kernel(const __grid_constant__ QuantParams p) {
   const QuantReq& r = p.req[blockIdx.z];
   const int g = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
   if (g >= r.ng) return;
-  __shared__ uint8_t codes[32][D];
-  const bf16* src = r.k + ((size_t)h * r.cap + 32 * g) * D + c;
+  __shared__ __align__(16) bf16 tile[32 * D];
+  __shared__ CodeTile<D> codes;
+  const uint4* src = reinterpret_cast<const uint4*>(r.k + ((size_t)h * r.cap + 32 * g) * D);
+#pragma unroll
+  for (int e = c; e < 32 * D / 8; e += D) reinterpret_cast<uint4*>(tile)[e] = __ldg(src + e);
+  __syncthreads();
   float x[32];
   float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
-    x[t] = __bfloat162float(src[(size_t)t * D]);
+    x[t] = __bfloat162float(tile[t * D + c]);
     mn = fminf(mn, x[t]);
     mx = fmaxf(mx, x[t]);
   }
   __half s16, z16;
-  float sf, zf;
-  quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
+  float sf, zf, rs;
+  quant_params<BITS>(mn, mx, s16, z16, sf, zf, rs, p.dev_status);
   const size_t gi = ((size_t)h * r.ng_cap + g) * D + c;
   r.ks[gi] = s16;
   r.kz[gi] = z16;
 #pragma unroll
-  for (int t = 0; t < 32; ++t) codes[t][c] = (uint8_t)quant_code<BITS>(x[t], sf, zf);
+  for (int t = 0; t < 32; ++t) codes[t][c] = (uint8_t)quant_code<BITS>(x[t], sf, zf, rs);
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(r.kc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
   for (int wi = c; wi < D * BITS; wi += D) dst[wi] = block_word<D, BITS, true>(codes, wi);
@@ -361,14 +382,19 @@ __global__ void __launch_bounds__(256) quant_values_kernel(const __grid_constant
   const QuantReq& r = p.req[blockIdx.z];
   const int g = blockIdx.x, h = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (g >= r.ng) return;
-  __shared__ uint8_t codes[32][D];
+  __shared__ __align__(16) bf16 tile[32 * D];
+  __shared__ CodeTile<D> codes;
   constexpr int CPL = D / 32;
   constexpr int LPG = 32 / CPL;  // lanes per 32-channel group
   const int c0 = CPL * lane;
+  const uint4* vsrc = reinterpret_cast<const uint4*>(r.v + ((size_t)h * r.cap + 32 * g) * D);
+#pragma unroll
+  for (int e = threadIdx.x; e < 32 * D / 8; e += 256) reinterpret_cast<uint4*>(tile)[e] = __ldg(vsrc + e);
+  __syncthreads();
 #pragma unroll 1
   for (int tt = warp; tt < 32; tt += 8) {
     const int t = 32 * g + tt;
-    const bf16* src = r.v + ((size_t)h * r.cap + t) * D + c0;
+    const bf16* src = tile + tt * D + c0;
     float x[CPL];
     float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
@@ -383,15 +409,15 @@ __global__ void __launch_bounds__(256) quant_values_kernel(const __grid_constant
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     }
     __half s16, z16;
-    float sf, zf;
-    quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
+    float sf, zf, rs;
+    quant_params<BITS>(mn, mx, s16, z16, sf, zf, rs, p.dev_status);
     const size_t row = (size_t)h * (32 * r.ng_cap) + t;
     if ((lane % LPG) == 0) {
       r.vs[row * (D / 32) + c0 / 32] = s16;
       r.vz[row * (D / 32) + c0 / 32] = z16;
     }
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) codes[tt][c0 + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf);
+    for (int e = 0; e < CPL; ++e) codes[tt][c0 + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf, rs);
   }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(r.vc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
@@ -470,7 +496,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
     reinterpret_cast<uint4*>((isv ? ev : ek) + (size_t)j * D)[q % V16] = reinterpret_cast<const uint4*>(row)[q % V16];
   }
   __syncthreads();
-  __shared__ uint8_t codes[32][D];
+  __shared__ CodeTile<D> codes;
   constexpr int CPL = D / 32;    // channels per lane (values)
   constexpr int LPG = 32 / CPL;  // lanes per 32-channel group
   for (int gi = 0; gi < r.ng_new - r.ng; ++gi) {
@@ -489,13 +515,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
         mx = fmaxf(mx, x[t]);
       }
       __half s16, z16;
-      float sf, zf;
-      quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
+      float sf, zf, rs;
+      quant_params<BITS>(mn, mx, s16, z16, sf, zf, rs, p.dev_status);
       const size_t gidx = ((size_t)h * r.ng_cap + g) * D + c;
       r.ks[gidx] = s16;
       r.kz[gidx] = z16;
 #pragma unroll
-      for (int t = 0; t < 32; ++t) codes[t][c] = (uint8_t)quant_code<BITS>(x[t], sf, zf);
+      for (int t = 0; t < 32; ++t) codes[t][c] = (uint8_t)quant_code<BITS>(x[t], sf, zf, rs);
     }
     __syncthreads();
     uint32_t* kdst = reinterpret_cast<uint32_t*>(r.kc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
@@ -518,15 +544,15 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       }
       __half s16, z16;
-      float sf, zf;
-      quant_params<BITS>(mn, mx, s16, z16, sf, zf, p.dev_status);
+      float sf, zf, rs;
+      quant_params<BITS>(mn, mx, s16, z16, sf, zf, rs, p.dev_status);
       const size_t row = (size_t)h * (VC_GROUP * (size_t)r.ng_cap) + VC_GROUP * g + tt;
       if ((lane % LPG) == 0) {
         r.vs[row * (D / 32) + c0 / 32] = s16;
         r.vz[row * (D / 32) + c0 / 32] = z16;
       }
 #pragma unroll
-      for (int e = 0; e < CPL; ++e) codes[tt][c0 + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf);
+      for (int e = 0; e < CPL; ++e) codes[tt][c0 + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf, rs);
     }
     __syncthreads();
     uint32_t* vdst = reinterpret_cast<uint32_t*>(r.vc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));

@@ -143,3 +143,29 @@ def test_accept_edges():
             rt, rn = O.accept(lg[b], dr[b], int(L[b]))
             assert int(nacc[b]) == rn and tok[b, :rn].cpu().tolist() == rt
         assert nacc.cpu().tolist() == [Lm + 1, 1, Lm + 1, 1]
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quant_half_integer_ties(bits):
+    """Every key channel and value group spans 0 .. 2^bits - 1 in steps of 1/2 (times a power of two
+    per channel), so the scale is exactly a power of two and half the quotients (x - z) / s are
+    exact half-integers: the codes must take round-half-even exactly as the oracle does."""
+    w = configs.scaled(configs.qwen32b_quant2(), ctx_div=256, batch=1)
+    w.bits = bits
+    w.ctx = [128 + 96]
+    bt = make_batch(w, [0])
+    r = bt.reqs[0]
+    M = 2 * ((1 << bits) - 1) + 1
+    t = torch.arange(w.ctx[0], dtype=torch.float32)[:, None]
+    c = torch.arange(w.d, dtype=torch.float32)[None, :]
+    ramp = torch.remainder(t, M) / 2                            # 0, 0.5, ..., 2^bits - 1
+    kv = ramp * torch.pow(2.0, torch.remainder(c, 3) - 1)       # exact in bf16
+    vv = (torch.remainder(c + t, M) / 2) * torch.pow(2.0, torch.remainder(t, 3) - 1)
+    for h in range(w.Hkv):
+        r.k_full[h, : w.ctx[0]].copy_(kv.to(torch.bfloat16))
+        r.v_full[h, : w.ctx[0]].copy_(vv.to(torch.bfloat16))
+    bt.compress()
+    torch.cuda.synchronize()
+    assert int(bt.dev_status.item()) == 0
+    ref = assert_quant_state(bt, 0, f32(r.k_full), f32(r.v_full), bits, w.residual_min)
+    assert ref["ng"] == 3
