@@ -105,8 +105,10 @@ __device__ __forceinline__ void it_scores(float (&s)[4][4], const uint8_t* kt, c
   }
 }
 
+// Three 4-warp CTAs per SM (the register cap that allows is met without spills): the MMAs are
+// issue-bound, so the extra warps matter more than registers.
 template <int D, int NW>
-__global__ void __launch_bounds__(NW * 32) imp_stats_kernel(const __grid_constant__ ImpParams p) {
+__global__ void __launch_bounds__(NW * 32, NW <= 4 ? 12 / NW : 1) imp_stats_kernel(const __grid_constant__ ImpParams p) {
   pdl_launch_dependents();
   pdl_wait();
   const int chunk = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
