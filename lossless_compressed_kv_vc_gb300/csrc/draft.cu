@@ -176,26 +176,80 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
   }
 }
 
-// Two stored codes of a block word as exact bf16 operands 128 + code (low code -> low half).
+// Two stored codes of a block word as one fp16x2 operand, by a single LOP3: the code at bit position
+// P of each 16-bit half (P + BITS <= 8) lands in the mantissa of 2^(10-P), giving the exact value
+// 2^(10-P) + code. The offset depends only on P, so it is taken out afterwards by a constant MMA.
+template <int BITS, int P>
+__device__ __forceinline__ uint32_t code_f16x2(uint32_t w) {
+  constexpr uint32_t m = ((1u << BITS) - 1u) << P;
+  constexpr uint32_t e = (25u - P) << 10;  // fp16 exponent field of 2^(10-P)
+  return (w & (m | (m << 16))) | (e | (e << 16));
+}
+
+// The four A-fragment registers of k-step ks held by block word w (see the block layout in
+// compress.cu): 2-bit words carry two k-steps (the odd one in bits 8-15 of each half), 4-bit words
+// one (registers 2 and 3 in bits 8-15). One shift per word, one LOP3 per register.
 template <int BITS>
-__device__ __forceinline__ uint32_t codes_bf16x2(uint32_t w, int shift) {
-  constexpr uint32_t MASK = BITS == 4 ? 0x000F000Fu : 0x00030003u;
-  return ((w >> shift) & MASK) | 0x43004300u;  // bf16 0x43xx = 128 + xx (xx < 128)
+__device__ __forceinline__ void code_frag(uint32_t w, int ks, uint32_t (&a)[4]) {
+  if constexpr (BITS == 2) {
+    const uint32_t x = (ks & 1) ? (w >> 8) : w;
+    a[0] = code_f16x2<2, 0>(x);
+    a[1] = code_f16x2<2, 2>(x);
+    a[2] = code_f16x2<2, 4>(x);
+    a[3] = code_f16x2<2, 6>(x);
+  } else {
+    const uint32_t x = w >> 8;
+    a[0] = code_f16x2<4, 0>(w);
+    a[1] = code_f16x2<4, 4>(w);
+    a[2] = code_f16x2<4, 0>(x);
+    a[3] = code_f16x2<4, 4>(x);
+  }
+}
+
+// minus the offsets of code_frag's registers, as a constant A fragment (fp16 pairs): an MMA of it
+// with the same B operand subtracts exactly what the offsets added.
+template <int BITS>
+__device__ __forceinline__ void code_offsets(uint32_t (&a)[4]) {
+  if constexpr (BITS == 2) {
+    a[0] = 0xE400E400u;  // -1024
+    a[1] = 0xDC00DC00u;  // -256
+    a[2] = 0xD400D400u;  // -64
+    a[3] = 0xCC00CC00u;  // -16
+  } else {
+    a[0] = 0xE400E400u;  // -1024
+    a[1] = 0xD400D400u;  // -64
+    a[2] = 0xE400E400u;
+    a[3] = 0xD400D400u;
+  }
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, __half2 y) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&x), y);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // One quantised 32-token block, read in its stored form (see the block layout in compress.cu): each
-// lane's 32-bit word is exactly its A fragment for an m16n8k16 MMA, so codes enter the tensor cores
-// as exact bf16 integers 128 + code with no dequantised tile in between.
-//   keys (scale s_c, zero z_c per channel):  S^T[t][h] = sum_c (128 + code)(s_c q_hc)
-//                                                     + sum_c (z_c q_hc - 128 s_c q_hc)
-//     -> B operand = (s o q)^T rounded to bf16 once per block, plus a per-head bias;
-//   values (scale s_t, zero z_t per token and 32-channel group g):
-//     O^T[c][h] += sum_t (128 + code)(s_t p_th) + sum_t (z_t p_th - 128 s_t p_th)
-//     -> B operand = (s o p)^T per channel group, plus a per-(group, head) term zs accumulated in the
-//        softmax frame of O and added to O before it is read (fold_zs).
+// lane's 32-bit word is its A fragment for an m16n8k16 MMA, turned into exact fp16 operands by one
+// LOP3 per register (code_frag); the tensor cores take the codes with no dequantised tile between.
+// qn holds the query as fp16 scaled by 2^-E (|qn| < 1, E per warp), scale_q = log2(e)/sqrt(d) * 2^E.
+//   keys (scale s_c, zero z_c per channel):
+//     S^T[t][h] = sum_c code (s_c qn_hc) + sum_c z_c qn_hc
+//     -> B operand fp16(s o qn) per block (B <= s: no overflow); the per-head term z . qn and the
+//        removal of the code offsets are MMAs (z broadcast over tokens, resp. the constant offsets,
+//        against qn, resp. the scaled query), once per block for both 16-token halves;
+//   values (scale s_t, zero z_t per token and 32-channel group g), P <= 1 (the running maximum moves
+//   at every new maximum inside quantised blocks):
+//     O^T[c][h] += sum_t code (s_t p_th) + sum_t z_t p_th
+//     -> B operand fp16(s o p) per channel group with an offset-removal MMA, plus a per-(group,
+//        head) zero term zs accumulated in the softmax frame of O and added before O is read.
 template <int D, int BITS, int NHB>
-__device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_log2,
-                                              const uint32_t (&qb)[NHB][D / 16][2], float (&o)[NHB][D / 16][4],
+__device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
+                                              const uint32_t (&qn)[NHB][D / 16][2], float (&o)[NHB][D / 16][4],
                                               float (&m)[NHB][2], float (&l)[NHB][2], float (&zs)[NHB][D / 32][2],
                                               int lane) {
   using C = DraftCfg<D, BITS>;
@@ -208,30 +262,30 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_lo
   const __half* vsc = reinterpret_cast<const __half*>(raw + C::OFF_VS);
   const __half* vze = reinterpret_cast<const __half*>(raw + C::OFF_VZ);
   const int b4 = lane & 3, a8 = lane >> 2;
-  // block setup: scaled query fragments and the per-head key bias
+  uint32_t acorr[4];
+  code_offsets<BITS>(acorr);
+  // block setup: scaled query fragments and the per-(row half, head) term of both halves
   uint32_t qs[NHB][MT][2];
-  float bias[NHB][2];
+  float cb[NHB][4];
 #pragma unroll
-  for (int hb = 0; hb < NHB; ++hb) {
-    float part = 0.f;
+  for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
-    for (int ks = 0; ks < MT; ++ks)
+    for (int e = 0; e < 4; ++e) cb[hb][e] = 0.f;
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int c = 16 * ks + 2 * b4 + 8 * r;
-        const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(ksc + c));
-        const float2 ze = __half22float2(*reinterpret_cast<const __half2*>(kze + c));
-        const uint32_t qv = qb[hb][ks][r];
-        const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv));
-        const __nv_bfloat162 qsb = __floats2bfloat162_rn(qf.x * sc.x, qf.y * sc.y);
-        qs[hb][ks][r] = *reinterpret_cast<const uint32_t*>(&qsb);
-        const float2 qsr = __bfloat1622float2(qsb);
-        part += ze.x * qf.x + ze.y * qf.y - 128.f * (qsr.x + qsr.y);
-      }
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);  // bias of head 8hb + lane/4
-    bias[hb][0] = __shfl_sync(0xffffffffu, part, 4 * (2 * b4));
-    bias[hb][1] = __shfl_sync(0xffffffffu, part, 4 * (2 * b4 + 1));
+  for (int ks = 0; ks < MT; ++ks) {
+    const int c = 16 * ks + 2 * b4;
+    const __half2 s0 = *reinterpret_cast<const __half2*>(ksc + c);
+    const __half2 s1 = *reinterpret_cast<const __half2*>(ksc + c + 8);
+    uint32_t az[4];
+    az[0] = az[1] = *reinterpret_cast<const uint32_t*>(kze + c);
+    az[2] = az[3] = *reinterpret_cast<const uint32_t*>(kze + c + 8);
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+      qs[hb][ks][0] = hmul2_u32(qn[hb][ks][0], s0);
+      qs[hb][ks][1] = hmul2_u32(qn[hb][ks][1], s1);
+      mma_f16_16816(cb[hb], az, qn[hb][ks][0], qn[hb][ks][1]);
+      mma_f16_16816(cb[hb], acorr, qs[hb][ks][0], qs[hb][ks][1]);
+    }
   }
 #pragma unroll 1
   for (int half = 0; half < 2; ++half) {
@@ -239,19 +293,16 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_lo
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[hb][e] = bias[hb][e & 1];
+      for (int e = 0; e < 4; ++e) s[hb][e] = cb[hb][e];
 #pragma unroll
     for (int ks = 0; ks < MT; ++ks) {
-      const uint32_t w = kw[(half * STEPS + (BITS == 4 ? ks : ks >> 1)) * 32 + lane];
-      const int base = BITS == 4 ? 0 : 4 * BITS * (ks & 1);
       uint32_t a[4];
+      code_frag<BITS>(kw[(half * STEPS + (BITS == 4 ? ks : ks >> 1)) * 32 + lane], ks, a);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = codes_bf16x2<BITS>(w, base + BITS * i);
-#pragma unroll
-      for (int hb = 0; hb < NHB; ++hb) mma_bf16_16816(s[hb], a, qs[hb][ks][0], qs[hb][ks][1]);
+      for (int hb = 0; hb < NHB; ++hb) mma_f16_16816(s[hb], a, qs[hb][ks][0], qs[hb][ks][1]);
     }
-    // online softmax over the 16 tokens (rows lane/4 and lane/4 + 8; all valid); the running
-    // maximum moves only when a tile exceeds it by more than 8 (exp2 domain), as in tile_attend
+    // online softmax over the 16 tokens (rows lane/4 and lane/4 + 8; all valid); inside quantised
+    // blocks the running maximum follows every new maximum, so the weights stay <= 1 (fp16 B)
     float p[NHB][2][2];
     float tmax[NHB][2];
     bool need = false;
@@ -263,8 +314,8 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_lo
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        tmax[hb][e] = mx * scale_log2;
-        need |= tmax[hb][e] > m[hb][e] + 8.f;
+        tmax[hb][e] = mx * scale_q;
+        need |= tmax[hb][e] > m[hb][e];
       }
     if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -291,40 +342,43 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_lo
         }
       }
     }
+    uint32_t pt0[NHB], pt1[NHB];  // fp16 weights of tokens t0, t1 for this lane's two heads
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        p[hb][e][0] = ex2_approx(fmaf(s[hb][e], scale_log2, -m[hb][e]));
-        p[hb][e][1] = ex2_approx(fmaf(s[hb][e + 2], scale_log2, -m[hb][e]));
+        p[hb][e][0] = ex2_approx(fmaf(s[hb][e], scale_q, -m[hb][e]));
+        p[hb][e][1] = ex2_approx(fmaf(s[hb][e + 2], scale_q, -m[hb][e]));
         l[hb][e] += p[hb][e][0] + p[hb][e][1];
       }
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+      pt0[hb] = pack_half2(p[hb][0][0], p[hb][1][0]);
+      pt1[hb] = pack_half2(p[hb][0][1], p[hb][1][1]);
+    }
     const int t0 = 16 * half + a8, t1 = t0 + 8;
 #pragma unroll
     for (int g = 0; g < D / 32; ++g) {
-      const float s0 = __half2float(vsc[t0 * (D / 32) + g]), s1 = __half2float(vsc[t1 * (D / 32) + g]);
+      const __half2 s0 = __half2half2(vsc[t0 * (D / 32) + g]), s1 = __half2half2(vsc[t1 * (D / 32) + g]);
       const float z0 = __half2float(vze[t0 * (D / 32) + g]), z1 = __half2float(vze[t1 * (D / 32) + g]);
       uint32_t pb[NHB][2];
 #pragma unroll
       for (int hb = 0; hb < NHB; ++hb) {
-        const __nv_bfloat162 k0 = __floats2bfloat162_rn(p[hb][0][0] * s0, p[hb][1][0] * s0);  // token t0
-        const __nv_bfloat162 k1 = __floats2bfloat162_rn(p[hb][0][1] * s1, p[hb][1][1] * s1);  // token t1
-        const float2 r0 = __bfloat1622float2(k0), r1 = __bfloat1622float2(k1);
-        zs[hb][g][0] += z0 * p[hb][0][0] + z1 * p[hb][0][1] - 128.f * (r0.x + r1.x);
-        zs[hb][g][1] += z0 * p[hb][1][0] + z1 * p[hb][1][1] - 128.f * (r0.y + r1.y);
-        pb[hb][0] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&k0));
-        pb[hb][1] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&k1));
+        zs[hb][g][0] += z0 * p[hb][0][0] + z1 * p[hb][0][1];
+        zs[hb][g][1] += z0 * p[hb][1][0] + z1 * p[hb][1][1];
+        pb[hb][0] = movmatrix_t(hmul2_u32(pt0[hb], s0));
+        pb[hb][1] = movmatrix_t(hmul2_u32(pt1[hb], s1));
       }
 #pragma unroll
       for (int mm = 0; mm < 2; ++mm) {
         const int mt = 2 * g + mm;
-        const uint32_t w = vw[(half * STEPS + (BITS == 4 ? mt : mt >> 1)) * 32 + lane];
-        const int base = BITS == 4 ? 0 : 4 * BITS * (mt & 1);
         uint32_t a[4];
+        code_frag<BITS>(vw[(half * STEPS + (BITS == 4 ? mt : mt >> 1)) * 32 + lane], mt, a);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = codes_bf16x2<BITS>(w, base + BITS * i);
-#pragma unroll
-        for (int hb = 0; hb < NHB; ++hb) mma_bf16_16816(o[hb][mt], a, pb[hb][0], pb[hb][1]);
+        for (int hb = 0; hb < NHB; ++hb) {
+          mma_f16_16816(o[hb][mt], a, pb[hb][0], pb[hb][1]);
+          mma_f16_16816(o[hb][mt], acorr, pb[hb][0], pb[hb][1]);
+        }
       }
     }
   }
@@ -691,6 +745,40 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       }
     }
   };
+  // For quantised blocks the same registers hold the query as fp16 scaled by 2^-E, E the exponent
+  // of the warp's largest |q| (so |qn| < 1 and the scaled query s o qn stays below the key scale);
+  // the softmax then uses scale_q = scale_log2 * 2^E. Window tiles reload the bf16 query.
+  float scale_q = p.scale_log2;
+  bool q_f16 = false;
+  auto load_qn = [&](int b) {
+    load_q(b);
+    float mx = 0.f;
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+      for (int ks = 0; ks < C::MT; ++ks)
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qb[hb][ks][r2]));
+          mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    int E = 0;
+    if (mx > 0.f) frexpf(mx, &E);  // mx = f 2^E with f in [0.5, 1)
+    const float inv = ldexpf(1.f, -E);
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+      for (int ks = 0; ks < C::MT; ++ks)
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qb[hb][ks][r2]));
+          qb[hb][ks][r2] = pack_half2(f.x * inv, f.y * inv);
+        }
+    scale_q = ldexpf(p.scale_log2, E);
+    q_f16 = true;
+  };
   // end of the warp's range: its (o, lse) partial, normalised, into its drained stage ring as
   // [G][D] o then [G] lse. The lane holds O^T[channel 16mt + lane/4 (+8)][head 8hb + 2(lane%4) + e].
   auto finish = [&]() {
@@ -732,7 +820,10 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         zs_live = false;
       }
       reset();
-      load_q(b);
+      if (!BF16_ROWS && lc < p.req[b].n_mc)
+        load_qn(b);
+      else
+        load_q(b);
       cur_b = b;
       if (lc == 0) {
         // fused append of the step's K/V row (the warp holding the request's first chunk)
@@ -757,12 +848,16 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     const DraftReqDev& r = p.req[b];
     uint8_t* sb = wb + st * C::STAGE;
     if (!BF16_ROWS && lc < r.n_mc) {
-      qblock_attend<D, C::BITS, NHB>(sb, p.scale_log2, qb, o, m, l, zs, lane);
+      qblock_attend<D, C::BITS, NHB>(sb, scale_q, qb, o, m, l, zs, lane);
       zs_live = true;
     } else {
       if (!BF16_ROWS && zs_live) {
         fold_zs<D, NHB>(o, zs);
         zs_live = false;
+      }
+      if (!BF16_ROWS && q_f16) {
+        load_q(b);
+        q_f16 = false;
       }
       const int cnt = (lc < r.n_mc) ? min(16, r.n_main - lc * 16) : min(16, r.n_win + 1 - (lc - r.n_mc) * 16);
       tile_attend<D, NHB>(sb, sb + C::TILE, cnt, p.scale_log2, qb, o, m, l, lane);
