@@ -162,10 +162,11 @@ class Batch:
             ws = self.ws_importance = torch.empty(need // 4 + 64, dtype=torch.float32, device=self.device)
         vc_snapkv_importance(shape, arr, window, pool_kernel, pool_kind, ws, self.dev_status, stream)
 
-    def compress(self, stream=None):
+    def compress(self, stream=None, importance=None):
         mode = self.reqs[0].mode
         if mode == VC_TOKEN_DROP:
-            vc_compress_kv(self.shape, self.full, [r.importance for r in self.reqs], [r.recent for r in self.reqs],
+            imp = importance if importance is not None else [r.importance for r in self.reqs]
+            vc_compress_kv(self.shape, self.full, imp, [r.recent for r in self.reqs],
                            self.residual_min, self.comp, self.dev_status, stream)
         else:
             vc_compress_kv(self.shape, self.full, None, None, self.residual_min, self.comp, self.dev_status, stream)
@@ -228,33 +229,36 @@ class Batch:
     def run_round_from_host(self, hr: "HostRound", stream, copy_stream, draft_events=None):
         """One round whose inputs sit in pinned host memory and whose results go back to it.
 
-        The inputs the draft phase needs (queries, drafted K/V, importance) are copied on `stream`
-        ahead of compress. The accept inputs (drafts, logits, L) cross the host link on
-        `copy_stream` while the GPU drafts and verifies, so the largest transfer of a round (the
-        logits) hides under the HBM-bound draft phase ("Cross-resource staggering (P1)": keep the
-        host link busy while the GPU drafts); accept waits for them. The logits copy of a round
-        waits until the previous round's accept has read the buffer."""
-        with torch.cuda.stream(stream):
-            for h, d in hr.draft_inputs:
-                d.copy_(h, non_blocking=True)
-        # the large copy starts once the small ones are in (so they never queue behind it on the
-        # copy engine) and after the previous round's accept (stream order)
-        hr.inputs_in.record(stream)
-        copy_stream.wait_event(hr.inputs_in)
+        All of the round's inputs cross the host link on `copy_stream` into the next of the
+        HostRound's device slots, once that slot's previous round has accepted: the draft inputs
+        (queries, drafted K/V, importance) first, then the accept inputs (drafts, logits, L). The
+        compute stream waits for the draft inputs before compress and for the accept inputs before
+        accept, so the largest transfer of a round (the logits) hides under the HBM-bound draft
+        phase ("Cross-resource staggering (P1)": keep the host link busy while the GPU drafts),
+        and with two slots a round's copies overlap the previous round on the GPU."""
+        sl = hr.next_slot()
+        copy_stream.wait_event(sl.free)
         with torch.cuda.stream(copy_stream):
-            for h, d in hr.accept_inputs:
+            for h, d in zip(hr.draft_host, sl.draft_dev):
                 d.copy_(h, non_blocking=True)
-        hr.landed.record(copy_stream)
-        self.compress(stream)
+        sl.ready.record(copy_stream)
+        with torch.cuda.stream(copy_stream):
+            for h, d in zip(hr.accept_host, sl.accept_dev):
+                d.copy_(h, non_blocking=True)
+        sl.landed.record(copy_stream)
+        stream.wait_event(sl.ready)
+        self.compress(stream, importance=sl.importance)
         if draft_events is not None:
             draft_events[0].record(stream)
-        for shape, arr, act in self._steps:
+        for shape, arr, act in sl.steps:
             vc_draft_attn(shape, arr, self.ws_draft, self.dev_status, stream)
         if draft_events is not None:
             draft_events[1].record(stream)
-        vc_verify_attn(self.shape, self._verify_arr, self.ws_verify, self.dev_status, stream)
-        stream.wait_event(hr.landed)
-        accept(hr.logits, hr.draft, hr.L, hr.out_tokens, hr.n_acc, stream)
+        vc_verify_attn(self.shape, sl.verify_arr, self.ws_verify, self.dev_status, stream)
+        stream.wait_event(sl.landed)
+        draft, logits, L = sl.accept_dev
+        accept(logits, draft, L, hr.out_tokens, hr.n_acc, stream)
+        sl.free.record(stream)
         with torch.cuda.stream(stream):
             hr.host_tokens.copy_(hr.out_tokens, non_blocking=True)
             hr.host_n_acc.copy_(hr.n_acc, non_blocking=True)
@@ -295,33 +299,63 @@ class Batch:
         vc_verify_attn(self.shape, self.verify_requests(), self.ws_verify, self.dev_status, stream)
 
 
+class _Slot:
+    """One set of device input buffers of a HostRound with the descriptor arrays that point at
+    them, and its events: ready (draft inputs landed), landed (accept inputs landed), free (the
+    slot's last round has accepted)."""
+
+    def __init__(self, draft_dev, accept_dev, importance, steps, verify_arr, stream):
+        self.draft_dev, self.accept_dev, self.importance = draft_dev, accept_dev, importance
+        self.steps, self.verify_arr = steps, verify_arr
+        self.ready, self.landed, self.free = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+        self.free.record(stream)
+
+
 class HostRound:
-    """Pinned host buffers of one round's inputs and results, and the device buffers they land in.
+    """Pinned host buffers of one round's inputs and results, and `slots` sets of device buffers
+    they land in, used round-robin (the first is the batch's own tensors).
 
     Inputs: each request's queries, drafted K/V rows and (token drop) importance, which the draft
     phase reads, and the batch's drafts [B][L_max], logits [B][L_max+1][V] and L [B], which only
     accept reads. Results: accepted tokens [B][L_max+1] and counts [B], valid on the host once the
-    round's stream has been synchronised."""
+    round's stream has been synchronised. Build it after the batch's first compress (it rebuilds
+    the batch's descriptor arrays for every slot)."""
 
     def __init__(self, bt: Batch, logits: torch.Tensor, draft: torch.Tensor, L: torch.Tensor,
-                 out_tokens: torch.Tensor, n_acc: torch.Tensor):
+                 out_tokens: torch.Tensor, n_acc: torch.Tensor, slots: int = 2):
         pin = lambda t: t.detach().to("cpu").pin_memory()
-        self.draft_inputs = []
-        for r in bt.reqs:
-            for t in (r.q, r.k_new, r.v_new, r.importance):
-                if t is not None:
-                    self.draft_inputs.append((pin(t), t))
-        self.logits, self.draft, self.L = logits, draft, L
-        self.accept_inputs = [(pin(t), t) for t in (draft, logits, L)]
+        names = ("q", "k_new", "v_new", "importance")
+        fields = [(r, n) for r in bt.reqs for n in names if getattr(r, n) is not None]
+        self.draft_host = [pin(getattr(r, n)) for r, n in fields]
+        self.accept_host = [pin(t) for t in (draft, logits, L)]
+        self.accept_inputs = list(zip(self.accept_host, (draft, logits, L)))
         self.out_tokens, self.n_acc = out_tokens, n_acc
         self.host_tokens = torch.empty(out_tokens.shape, dtype=out_tokens.dtype).pin_memory()
         self.host_n_acc = torch.empty(n_acc.shape, dtype=n_acc.dtype).pin_memory()
-        self.landed = torch.cuda.Event()
-        self.inputs_in = torch.cuda.Event()
+        stream = torch.cuda.current_stream()
+        self.slots = []
+        own = [getattr(r, n) for r, n in fields]
+        for s in range(slots):
+            dev = own if s == 0 else [torch.empty_like(t) for t in own]
+            acc = [draft, logits, L] if s == 0 else [torch.empty_like(t) for t in (draft, logits, L)]
+            for (r, n), t in zip(fields, dev):  # build this slot's descriptor arrays
+                setattr(r, n, t)
+            bt.prepare_steps()
+            imp = [r.importance for r in bt.reqs]
+            self.slots.append(_Slot(dev, acc, imp, bt._steps, bt._verify_arr, stream))
+        for (r, n), t in zip(fields, own):
+            setattr(r, n, t)
+        bt.prepare_steps()
+        self._next = 0
+
+    def next_slot(self) -> _Slot:
+        sl = self.slots[self._next]
+        self._next = (self._next + 1) % len(self.slots)
+        return sl
 
     @property
     def h2d_bytes(self) -> int:
-        return sum(h.numel() * h.element_size() for h, _ in self.draft_inputs + self.accept_inputs)
+        return sum(h.numel() * h.element_size() for h in self.draft_host + self.accept_host)
 
     @property
     def d2h_bytes(self) -> int:

@@ -103,7 +103,8 @@ def test_round_from_host_matches_device_round_and_oracle(vc):
     """The engine's host-input round (inputs copied from pinned host memory, the accept inputs on a
     second stream under the draft phase) gives bit-identical draft and verify outputs to the
     device-resident round, and the oracle's accepted tokens in two successive rounds whose host
-    logits differ (the second round's logits copy must wait for the first round's accept)."""
+    logits differ; a third round reuses the first round's device slot, whose copies must wait
+    for that round's accept."""
     from lossless_compressed_kv_vc_gb300 import engine
     w = configs.scaled(configs.llama8b_drop(), ctx_div=16, batch=3, L=8)
     w.V = 5000
@@ -125,7 +126,7 @@ def test_round_from_host_matches_device_round_and_oracle(vc):
         t.zero_()
     cs = torch.cuda.Stream()
     s = torch.cuda.current_stream()
-    for rnd in (0, 1):
+    for rnd in (0, 1, 2):
         d_h, l_h, L_h = gen.drafts_and_logits(w, rnd)
         for (h, _), src in zip(hr.accept_inputs, (d_h, l_h, L_h)):
             h.copy_(src)
