@@ -220,6 +220,26 @@ struct DraftReqDev {
   int32_t warp_begin;   // first warp (of a head's grid row) holding it; it holds them up to the next request's
 };
 
+// The observation-window passes of the SnapKV-style importance, run by the verification kernel's
+// row-statistics and column-sum modes (verify.cu).
+struct ObsReq {
+  const bf16* k;   // KV_full keys [Hkv][cap][d]
+  const bf16* q;   // window queries [W][Hq][d]
+  int32_t ctx, cap;
+  float* lse;      // [Hkv][mtiles * 128] window rows' log-sum-exp (exp2 domain)
+  float* votes;    // [Hkv * mtiles][ctx] per-tile column sums
+};
+struct ObsArgs {
+  ObsReq req[VC_MAX_BATCH];
+  int32_t B, Hq, Hkv, d, W;
+  float* ws_lse;   // split-unit partials
+  size_t ws_lse_floats;
+  int32_t* dev_status;
+};
+int obs_mtiles(int W, int G);
+size_t obs_slot_floats(int B, int Hkv, int mtiles);
+cudaError_t launch_obs_passes(const ObsArgs& a, cudaStream_t s);
+
 struct DraftParams {
   DraftReqDev req[VC_MAX_BATCH];
   int32_t B, Hq, Hkv, G;

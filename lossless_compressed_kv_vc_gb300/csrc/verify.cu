@@ -43,7 +43,15 @@ struct VerifyReqDev {
   int32_t ctx, n_rows, mtiles, n_full, tiles;
   int32_t unit_begin;
   int64_t tile_begin;
+  // row-statistics / column-sum modes (the importance votes): lse [Hkv][mtiles * 128] (written by
+  // the statistics pass, read by the votes pass) and votes [Hkv * mtiles][ctx + n_rows]
+  float* lse;
+  float* votes;
 };
+
+// Kernel modes: attention (verification), the rows' log-sum-exp only, and the column sums of the
+// normalised weights (sum over the tile's rows of 2^(s - lse) for every key).
+constexpr int VMODE_ATTN = 0, VMODE_STATS = 1, VMODE_VOTES = 2;
 
 struct VerifyParams {
   CUtensorMap tm[VC_MAX_BATCH][4];  // K full, V full, K new, V new
@@ -72,6 +80,10 @@ struct VCfg {
   static constexpr int OCOL = 128;                 // O: TMEM columns [128, 128 + D)
   static constexpr uint32_t TCOLS = 256;
   static constexpr int THREADS = 192;              // warps 0-3 softmax, 4 MMA issue, 5 TMA loads
+  // votes mode: an fp16 all-ones [128][128] A operand over the (unused) V stages
+  static constexpr int ONES_BYTES = VM * 128 * 2;
+  static constexpr int OFF_BAR_VOTES = OFF_V + ONES_BYTES > OFF_BAR ? OFF_V + ONES_BYTES : OFF_BAR;
+  static constexpr int SMEM_VOTES = OFF_BAR_VOTES + 256;
 };
 
 __device__ __forceinline__ int find_req(const VerifyParams& p, int64_t tile) {
@@ -110,7 +122,7 @@ __device__ __forceinline__ VPiece verify_piece(const VerifyParams& p, int64_t po
   return q;
 }
 
-template <int D>
+template <int D, int MODE>
 __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_constant__ VerifyParams p) {
   using C = VCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -123,7 +135,7 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
   }
   uint8_t* sQ = smem;
   uint8_t* sP = smem + C::OFF_P;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (MODE == VMODE_VOTES ? C::OFF_BAR_VOTES : C::OFF_BAR));
   uint64_t* kfull = bars + 0;   // [2] K tile landed (TMA bytes)
   uint64_t* vfull = bars + 2;   // [2] V tile landed
   uint64_t* kempty = bars + 4;  // [2] the S MMA that read a K stage is done
@@ -139,12 +151,25 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
   if (warp == 0) tc05::alloc(tslot, C::TCOLS);
   if (tid == 0) {
     for (int i = 0; i < 10; ++i) mbar_init(&bars[i], 1);
+    // statistics mode: the (unused) V barriers become per-S-buffer releases by the 4 softmax warps.
+    // A single release barrier could complete two phases (two tiles read) before the MMA warp
+    // waits for the first, and the parity wait would then miss it; per buffer, a phase can only
+    // complete after the MMA warp has waited for the previous one (it issues that buffer's next S).
+    if (MODE == VMODE_STATS) {
+      mbar_init(&vfull[0], 4);
+      mbar_init(&vfull[1], 4);
+    }
     mbar_init(pfull, 4);
     mbar_init(ofull, 1);
     mbar_init(qfull, 4);
     mbar_init(xbar, 1);
     fence_mbar_init();
     *s_abort = 0;
+  }
+  if constexpr (MODE == VMODE_VOTES) {
+    for (int e = tid; e < C::ONES_BYTES / 16; e += C::THREADS)
+      reinterpret_cast<uint4*>(smem + C::OFF_V)[e] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+    fence_proxy_async_smem();  // the tensor cores read it
   }
   tc05::fence_before();
   __syncthreads();
@@ -183,7 +208,7 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
         for (int j = q.j0; j < q.j1 && ok; ++j, ++g) {
           ok = load(false, gk, q.b, hk, j);
           if (ok) ++gk;
-          if (ok && pv_pending) {
+          if (MODE == VMODE_ATTN && ok && pv_pending) {
             ok = load(true, gv, pv_b, pv_hk, pv_j);
             if (ok) ++gv;
           }
@@ -191,7 +216,7 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
         }
         pos += q.j1 - q.j0;
       }
-      if (ok && pv_pending && load(true, gv, pv_b, pv_hk, pv_j)) ++gv;
+      if (MODE == VMODE_ATTN && ok && pv_pending && load(true, gv, pv_b, pv_hk, pv_j)) ++gv;
       if (*s_abort) {
         // drain (bounded): the loads of the last two tiles of each kind may still be landing
         for (uint32_t gi = (gk > 2 ? gk - 2 : 0); gi < gk; ++gi) mbar_wait_bounded(&kfull[gi & 1], (gi >> 1) & 1, p.dev_status);
@@ -208,7 +233,25 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
       uint32_t g = 0, u = 0;
       bool ok = true;
       auto issue_pv = [&](uint32_t gp, bool acc) -> bool {
+        if constexpr (MODE == VMODE_STATS) {
+          // tile gp's S has been read: its TMEM buffer may take tile gp + 2
+          return vwait(&vfull[gp & 1], (gp >> 1) & 1, p.dev_status, s_abort);
+        }
         if (!vwait(pfull, gp & 1, p.dev_status, s_abort)) return false;
+        if constexpr (MODE == VMODE_VOTES) {
+          // column sums of P (fp16, [128 rows = K][64 keys = N], MN-major) by an all-ones A
+          constexpr uint32_t IDESC_C = tc05::idesc_f16(VM, VBN, true);
+          const uint32_t aOnes = smem_u32(smem + C::OFF_V);
+          tc05::fence_after();
+#pragma unroll
+          for (int kk = 0; kk < VM / 16; ++kk) {
+            const uint64_t da = tc05::sdesc_sw128(aOnes + (kk >> 2) * (VM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = tc05::sdesc_sw128(aP + kk * 2048, VM * 128, 1024);
+            tc05::mma_bf16(tmem + C::OCOL + (gp & 1) * VBN, da, db, IDESC_C, kk > 0 ? 1u : 0u);
+          }
+          tc05::commit(ofull);
+          return true;
+        }
         if (!vwait(&vfull[gp & 1], (gp >> 1) & 1, p.dev_status, s_abort)) return false;
         tc05::fence_after();
         const uint32_t vaddr = aV + (gp & 1) * C::KV_BYTES;
@@ -283,6 +326,7 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(qfull);
 
+      if constexpr (MODE == VMODE_ATTN) {
       float m_run = -INFINITY, l_run = 0.f;
       for (int jj = 0; jj < nt; ++jj) {
         const int j = q.j0 + jj;
@@ -417,6 +461,144 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
         }
       }
       if (row_ok && !whole) p.ws_lse[slot * VM + tid] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+      } else if constexpr (MODE == VMODE_STATS) {
+        // the row's maximum and sum of 2^(s scale - max) over the piece's tiles, exactly tracked
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int jj = 0; jj < nt; ++jj) {
+          const int j = q.j0 + jj;
+          const uint32_t gc = g + jj;
+          if (!vwait(&sfull[gc & 1], (gc >> 1) & 1, p.dev_status, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          float x[VBN];
+          {
+            uint32_t r0[32], r1[32];
+            const uint32_t t_s = tmem + lane_off + (gc & 1) * C::SCOL;
+            tc05::ld32(t_s, r0);
+            tc05::ld32(t_s + 32, r1);
+            tc05::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              x[e] = __uint_as_float(r0[e]) * p.scale_log2;
+              x[32 + e] = __uint_as_float(r1[e]) * p.scale_log2;
+            }
+          }
+          tc05::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&vfull[gc & 1]);  // this warp is done with the S buffer
+          const int last = j < R.n_full ? R.ctx - j * VBN - 1 : qi - (j - R.n_full) * VBN;
+          if (last < VBN - 1) {
+#pragma unroll
+            for (int e = 0; e < VBN; ++e)
+              if (e > last) x[e] = -INFINITY;
+          }
+          float mx = x[0];
+#pragma unroll
+          for (int e = 1; e < VBN; ++e) mx = fmaxf(mx, x[e]);
+          const float m_new = fmaxf(m_run, mx);
+          if (m_new != -INFINITY) {
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < VBN; ++e) sum += ex2_approx(x[e] - m_new);
+            l_run = l_run * ex2_approx(m_run - m_new) + sum;
+            m_run = m_new;
+          }
+        }
+        if (!ok) break;
+        g += nt;
+        const bool whole = (q.j0 == 0 && q.j1 == R.tiles);
+        const float lse = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+        if (row_ok) {
+          if (whole)
+            R.lse[((size_t)hk * R.mtiles + mt) * VM + tid] = lse;
+          else
+            p.ws_lse[(size_t)(c + u_global) * VM + tid] = lse;
+        }
+      } else {
+        // votes: P = 2^(s scale - lse) (0 for padding rows and invisible keys) in fp16 for the
+        // column-sum MMA; warp 0 reads each tile's sums (every row of them is the same) and stores
+        // the keys' votes of this 128-row tile
+        const float lse = row_ok ? R.lse[((size_t)hk * R.mtiles + mt) * VM + tid] : 0.f;
+        float* vdst = R.votes + ((size_t)hk * R.mtiles + mt) * (size_t)(R.ctx + R.n_rows);
+        auto store_votes = [&](uint32_t gp, int jp) {
+          uint32_t r0[32], r1[32];
+          const uint32_t t_c = tmem + C::OCOL + (gp & 1) * VBN;  // warp 0: lanes 0-31
+          tc05::ld32(t_c, r0);
+          tc05::ld32(t_c + 32, r1);
+          tc05::wait_ld();
+          float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e == lane) {
+              v0 = __uint_as_float(r0[e]);
+              v1 = __uint_as_float(r1[e]);
+            }
+          const int j = q.j0 + jp;
+          const int key0 = j < R.n_full ? j * VBN : R.ctx + (j - R.n_full) * VBN;
+          const int nv = j < R.n_full ? min(VBN, R.ctx - j * VBN) : min(VBN, R.n_rows - (j - R.n_full) * VBN);
+          if (lane < nv) vdst[key0 + lane] = v0;
+          if (32 + lane < nv) vdst[key0 + 32 + lane] = v1;
+        };
+        for (int jj = 0; jj < nt; ++jj) {
+          const int j = q.j0 + jj;
+          const uint32_t gc = g + jj;
+          if (!vwait(&sfull[gc & 1], (gc >> 1) & 1, p.dev_status, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          float x[VBN];
+          {
+            uint32_t r0[32], r1[32];
+            const uint32_t t_s = tmem + lane_off + (gc & 1) * C::SCOL;
+            tc05::ld32(t_s, r0);
+            tc05::ld32(t_s + 32, r1);
+            tc05::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              x[e] = __uint_as_float(r0[e]);
+              x[32 + e] = __uint_as_float(r1[e]);
+            }
+          }
+          const int last = !row_ok ? -1 : j < R.n_full ? R.ctx - j * VBN - 1 : qi - (j - R.n_full) * VBN;
+          if (jj > 0) {
+            // the previous tile's column sums are done, so the P buffer is free
+            if (!vwait(ofull, (gc - 1) & 1, p.dev_status, s_abort)) {
+              ok = false;
+              break;
+            }
+            tc05::fence_after();
+            if (warp == 0) store_votes(gc - 1, jj - 1);
+          }
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k0 = ch * 8 + 2 * e;
+              const float p0 = k0 <= last ? ex2_approx(fmaf(x[k0], p.scale_log2, -lse)) : 0.f;
+              const float p1 = k0 + 1 <= last ? ex2_approx(fmaf(x[k0 + 1], p.scale_log2, -lse)) : 0.f;
+              const __half2 h = __floats2half2_rn(p0, p1);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(sP + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          tc05::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pfull);
+        }
+        if (!ok) break;
+        if (!vwait(ofull, (g + nt - 1) & 1, p.dev_status, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc05::fence_after();
+        if (warp == 0) store_votes(g + nt - 1, nt - 1);
+        g += nt;
+      }
       tc05::fence_before();
       pos += nt;
     }
@@ -531,21 +713,114 @@ size_t verify_workspace_size(const vc_shape* s, int32_t max_rows) {
   return (size_t)slots * VM * (s->d + 1) * sizeof(float) + 256;
 }
 
-template <int D>
-static cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
+template <int D, int MODE>
+static cudaError_t launch_modes_t(const VerifyParams& p, cudaStream_t s) {
   using C = VCfg<D>;
+  constexpr int SMEM = MODE == VMODE_VOTES ? C::SMEM_VOTES : C::SMEM;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(verify_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(verify_attn_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  cudaError_t e = launch_pdl(verify_attn_kernel<D>, dim3(p.n_cta), dim3(C::THREADS), C::SMEM, s, p);
+  return launch_pdl(verify_attn_kernel<D, MODE>, dim3(p.n_cta), dim3(C::THREADS), SMEM, s, p);
+}
+
+template <int D>
+static cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
+  cudaError_t e = launch_modes_t<D, VMODE_ATTN>(p, s);
   if (e != cudaSuccess) return e;
   return launch_pdl(verify_combine_kernel<D>, dim3(p.n_units, VM / 8), dim3(256), 0, s, p);
 }
 
+// Row log-sum-exp of units split across CTAs (statistics mode): LSE = log2 sum_k 2^lse_k over the
+// unit's CTA slots; grid (units), a thread per row. Whole units were written by the kernel.
+__global__ void __launch_bounds__(VM) stats_combine_kernel(const __grid_constant__ VerifyParams p) {
+  const int u = blockIdx.x, r = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  int b = 0;
+#pragma unroll 1
+  for (int i = 1; i < p.B; ++i)
+    if (p.req[i].unit_begin <= u) b = i;
+  const VerifyReqDev& R = p.req[b];
+  const int ul = u - R.unit_begin;
+  const int64_t U0 = R.tile_begin + (int64_t)ul * R.tiles, U1 = U0 + R.tiles;
+  const int64_t T = p.total_tiles, N = p.n_cta;
+  const int64_t c0 = ((U0 + 1) * N - 1) / T, c1 = (U1 * N - 1) / T;
+  if (c0 == c1) return;
+  const int hk = p.h0 + ul / R.mtiles, mt = ul % R.mtiles;
+  if (mt * VM + r >= R.n_rows * p.G) return;
+  float M = -INFINITY;
+  for (int64_t c = c0; c <= c1; ++c) M = fmaxf(M, p.ws_lse[(c + u) * VM + r]);
+  float L = 0.f;
+  if (M != -INFINITY)
+    for (int64_t c = c0; c <= c1; ++c) L += exp2f(p.ws_lse[(c + u) * VM + r] - M);
+  R.lse[((size_t)hk * R.mtiles + mt) * VM + r] = L > 0.f ? M + log2f(L) : -INFINITY;
+}
+
 static bool a16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int obs_mtiles(int W, int G) { return (W * G + VM - 1) / VM; }
+
+size_t obs_slot_floats(int B, int Hkv, int mtiles) {
+  return ((size_t)B * Hkv * mtiles + 2 * (size_t)sm_count_v() + 8) * VM;
+}
+
+// The observation window's two passes on the tensor cores: for request b, the W window queries
+// q_obs attend to keys 0 .. ctx-W-1 of KV_full (the "full" part) and, causally, to the window's own
+// W keys (the "new" part: KV_full rows ctx-W .. ctx-1, row stride cap); the statistics pass writes
+// each window row's log-sum-exp, the votes pass each 128-row tile's column sums per key.
+cudaError_t launch_obs_passes(const ObsArgs& a, cudaStream_t s) {
+  const int d = a.d, G = a.Hq / a.Hkv;
+  VerifyParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = G;
+  p.h0 = 0;
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
+  p.dev_status = a.dev_status;
+  int64_t tiles = 0;
+  int32_t units = 0;
+  const int mtiles = obs_mtiles(a.W, G);
+  for (int b = 0; b < a.B; ++b) {
+    const ObsReq& q = a.req[b];
+    const int full = q.ctx - a.W;
+    const bf16* knew = q.k + (size_t)full * d;
+    if (!make_map(&p.tm[b][0], q.k, d, full > 0 ? full : 1, q.cap, a.Hkv) ||
+        !make_map(&p.tm[b][2], knew, d, a.W, q.cap, a.Hkv))
+      return cudaErrorInvalidValue;
+    p.tm[b][1] = p.tm[b][0];
+    p.tm[b][3] = p.tm[b][2];
+    VerifyReqDev& R = p.req[b];
+    R.q = q.q;
+    R.o = nullptr;
+    R.ctx = full;
+    R.n_rows = a.W;
+    R.mtiles = mtiles;
+    R.n_full = (full + VBN - 1) / VBN;
+    R.tiles = R.n_full + (a.W + VBN - 1) / VBN;
+    R.unit_begin = units;
+    R.tile_begin = tiles;
+    R.lse = q.lse;
+    R.votes = q.votes;
+    units += a.Hkv * mtiles;
+    tiles += (int64_t)a.Hkv * mtiles * R.tiles;
+  }
+  p.total_tiles = tiles;
+  p.n_cta = (int32_t)verify_ctas(tiles);
+  p.n_units = units;
+  if (((size_t)p.n_cta + units) * VM > a.ws_lse_floats) return cudaErrorInvalidValue;
+  p.ws_o = nullptr;
+  p.ws_lse = a.ws_lse;
+  cudaError_t e = d == 128 ? launch_modes_t<128, VMODE_STATS>(p, s) : launch_modes_t<64, VMODE_STATS>(p, s);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(stats_combine_kernel, dim3(p.n_units), dim3(VM), 0, s, p);
+  if (e != cudaSuccess) return e;
+  return d == 128 ? launch_modes_t<128, VMODE_VOTES>(p, s) : launch_modes_t<64, VMODE_VOTES>(p, s);
+}
 
 cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h0, int h1, void* ws,
                           size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, vc_status* st) {

@@ -1,11 +1,12 @@
 """GPU parity of the SnapKV-style importance (vc_snapkv_importance) against the oracle.
 
-Votes are sums of softmax weights (bf16 products accumulated in fp32 on the tensor cores, softmax
-in fp32) against the oracle's float64: each element must satisfy |gpu - oracle| <= 1e-3 |oracle|
-+ 1e-6 max|oracle| (a vote's relative error is about 1e-5: fp32 scores of magnitude <= 40 carry
-~4e-6 absolute error into the exponent). Cases cover 32 to 256 window rows per KV head (1 to 8
-warps), d = 64 and 128, max and average pooling of widths 1, 5 and 7, contexts that are not tile
-or chunk multiples, a context equal to the window, and full Llama-3-8B-shape contexts."""
+Scores are bf16 products accumulated in fp32 on the tensor cores, the softmax runs in fp32, and a
+key's sum over 128 window rows is an MMA of the fp16-rounded weights (relative error <= 2^-11 per
+weight, weights <= 1), against the oracle's float64: each element must satisfy
+|gpu - oracle| <= 1e-3 |oracle| + 1e-6 max|oracle|. Cases cover 20 to 400 window rows per KV head
+(one to four 128-row tiles, ragged), d = 64 and 128, max and average pooling of widths 1, 5 and 7,
+contexts that are not tile multiples, a context equal to the window, and full Llama-3-8B-shape
+contexts."""
 import numpy as np
 import pytest
 import torch
@@ -53,9 +54,10 @@ def _case(w, reqs, window, pool_kernel=7, pool="max", check_keep=False):
             assert np.array_equal(r.idx[: len(ref)].cpu().numpy(), ref)
 
 
-@pytest.mark.parametrize("window,pool_kernel,pool", [(8, 7, "max"), (16, 5, "avg"), (32, 1, "max"), (64, 7, "avg")])
+@pytest.mark.parametrize("window,pool_kernel,pool", [(8, 7, "max"), (16, 5, "avg"), (32, 1, "max"), (64, 7, "avg"),
+                                                     (5, 3, "max"), (100, 5, "avg")])
 def test_importance_tiny_d64(window, pool_kernel, pool):
-    """Tiny workload (d 64, G 4): 32, 64, 128 and 256 window rows per KV head."""
+    """Tiny workload (d 64, G 4): 32, 64, 128, 256, 20 and 400 window rows per KV head."""
     _case(configs.tiny(), [0], window, pool_kernel, pool)
 
 
