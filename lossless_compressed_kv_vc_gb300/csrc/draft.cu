@@ -357,10 +357,21 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
       pt1[hb] = pack_half2(p[hb][0][1], p[hb][1][1]);
     }
     const int t0 = 16 * half + a8, t1 = t0 + 8;
+    // the scales and zeros of all D/32 channel groups of tokens t0 and t1 (adjacent in the block)
+    __half2 vs0[D / 64], vs1[D / 64], vz0[D / 64], vz1[D / 64];
+#pragma unroll
+    for (int k = 0; k < D / 64; ++k) {
+      vs0[k] = reinterpret_cast<const __half2*>(vsc + t0 * (D / 32))[k];
+      vs1[k] = reinterpret_cast<const __half2*>(vsc + t1 * (D / 32))[k];
+      vz0[k] = reinterpret_cast<const __half2*>(vze + t0 * (D / 32))[k];
+      vz1[k] = reinterpret_cast<const __half2*>(vze + t1 * (D / 32))[k];
+    }
 #pragma unroll
     for (int g = 0; g < D / 32; ++g) {
-      const __half2 s0 = __half2half2(vsc[t0 * (D / 32) + g]), s1 = __half2half2(vsc[t1 * (D / 32) + g]);
-      const float z0 = __half2float(vze[t0 * (D / 32) + g]), z1 = __half2float(vze[t1 * (D / 32) + g]);
+      const __half2 s0 = (g & 1) ? __high2half2(vs0[g >> 1]) : __low2half2(vs0[g >> 1]);
+      const __half2 s1 = (g & 1) ? __high2half2(vs1[g >> 1]) : __low2half2(vs1[g >> 1]);
+      const float z0 = (g & 1) ? __high2float(vz0[g >> 1]) : __low2float(vz0[g >> 1]);
+      const float z1 = (g & 1) ? __high2float(vz1[g >> 1]) : __low2float(vz1[g >> 1]);
       uint32_t pb[NHB][2];
 #pragma unroll
       for (int hb = 0; hb < NHB; ++hb) {
