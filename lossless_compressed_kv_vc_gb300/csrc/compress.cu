@@ -375,53 +375,45 @@ __global__ void __launch_bounds__(D) quant_keys_kernel(const __grid_constant__ Q
   for (int wi = c; wi < D * BITS; wi += D) dst[wi] = block_word<D, BITS, true>(codes, wi);
 }
 
-// values: grid (ng_max, Hkv, B), block 256: warp w quantises tokens w, w+8, w+16, w+24 of the
-// block, lane l channels (D/32) l .. (D/32) l + D/32 - 1 (one 32-channel group per D/32 * ... lanes).
+// values: grid (ng_max, Hkv, B), block D: thread i quantises token i / (D/32) of the block over
+// its 32-channel group i % (D/32), reading the group's 64 contiguous bytes with four 16-byte loads
+// (a warp covers 2 KB of consecutive rows); the codes meet in shared memory for the word packing.
 template <int D, int BITS>
-__global__ void __launch_bounds__(256) quant_values_kernel(const __grid_constant__ QuantParams p) {
+__global__ void __launch_bounds__(D) quant_values_kernel(const __grid_constant__ QuantParams p) {
   const QuantReq& r = p.req[blockIdx.z];
-  const int g = blockIdx.x, h = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = blockIdx.x, h = blockIdx.y;
   if (g >= r.ng) return;
-  __shared__ __align__(16) bf16 tile[32 * D];
   __shared__ CodeTile<D> codes;
-  constexpr int CPL = D / 32;
-  constexpr int LPG = 32 / CPL;  // lanes per 32-channel group
-  const int c0 = CPL * lane;
-  const uint4* vsrc = reinterpret_cast<const uint4*>(r.v + ((size_t)h * r.cap + 32 * g) * D);
+  constexpr int NG = D / 32;  // channel groups per token
+  const int tt = threadIdx.x / NG, cg = threadIdx.x % NG;
+  const int t = 32 * g + tt;
+  const uint4* src = reinterpret_cast<const uint4*>(r.v + ((size_t)h * r.cap + t) * D + 32 * cg);
+  float x[32];
+  float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-  for (int e = threadIdx.x; e < 32 * D / 8; e += 256) reinterpret_cast<uint4*>(tile)[e] = __ldg(vsrc + e);
-  __syncthreads();
-#pragma unroll 1
-  for (int tt = warp; tt < 32; tt += 8) {
-    const int t = 32 * g + tt;
-    const bf16* src = tile + tt * D + c0;
-    float x[CPL];
-    float mn = INFINITY, mx = -INFINITY;
+  for (int k = 0; k < 4; ++k) {
+    const uint4 u = __ldg(src + k);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) {
-      x[e] = __bfloat162float(src[e]);
-      mn = fminf(mn, x[e]);
-      mx = fmaxf(mx, x[e]);
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      x[8 * k + 2 * e] = f.x;
+      x[8 * k + 2 * e + 1] = f.y;
+      mn = fminf(mn, fminf(f.x, f.y));
+      mx = fmaxf(mx, fmaxf(f.x, f.y));
     }
-#pragma unroll
-    for (int off = 1; off < LPG; off <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    }
-    __half s16, z16;
-    float sf, zf, rs;
-    quant_params<BITS>(mn, mx, s16, z16, sf, zf, rs, p.dev_status);
-    const size_t row = (size_t)h * (32 * r.ng_cap) + t;
-    if ((lane % LPG) == 0) {
-      r.vs[row * (D / 32) + c0 / 32] = s16;
-      r.vz[row * (D / 32) + c0 / 32] = z16;
-    }
-#pragma unroll
-    for (int e = 0; e < CPL; ++e) codes[tt][c0 + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf, rs);
   }
+  __half s16, z16;
+  float sf, zf, rs;
+  quant_params<BITS>(mn, mx, s16, z16, sf, zf, rs, p.dev_status);
+  const size_t row = (size_t)h * (32 * r.ng_cap) + t;
+  r.vs[row * NG + cg] = s16;
+  r.vz[row * NG + cg] = z16;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) codes[tt][32 * cg + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf, rs);
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(r.vc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
-  for (int wi = threadIdx.x; wi < D * BITS; wi += 256) dst[wi] = block_word<D, BITS, false>(codes, wi);
+  for (int wi = threadIdx.x; wi < D * BITS; wi += D) dst[wi] = block_word<D, BITS, false>(codes, wi);
 }
 
 // residual: rows [Tq, ctx) of K and V -> window rows [0, n_res); grid (ceil(max_res/8), Hkv, B).
@@ -450,7 +442,7 @@ static cudaError_t launch_quant_t(const QuantParams& p, int max_ng, int max_tq, 
     quant_keys_kernel<D, BITS><<<dim3(max_ng, p.Hkv, p.B), D, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    quant_values_kernel<D, BITS><<<dim3(max_ng, p.Hkv, p.B), 256, 0, s>>>(p);
+    quant_values_kernel<D, BITS><<<dim3(max_ng, p.Hkv, p.B), D, 0, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
