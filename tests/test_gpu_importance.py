@@ -85,3 +85,14 @@ def test_importance_context_equals_window():
 def test_importance_llama8b_full_size():
     """Two requests of the full Llama-3-8B-shape workload (context 32768), window 32."""
     _case(configs.llama8b_drop(), [0, 1], 32, 7, "max")
+
+
+@pytest.mark.parametrize("window", [32, 48])
+def test_importance_llama70b_shape_g8(window):
+    """64/8 heads (G = 8): 256 or 384 window rows per KV head, i.e. two or three 128-row tiles whose
+    column sums are separate partials, d = 128."""
+    w = configs.scaled(configs.llama70b_offload4(), ctx_div=64, batch=2)
+    w.mode = ["drop", "drop"]
+    w.keep = [512, 512]
+    w.recent = [32, 32]
+    _case(w, [0, 1], window, 7, "max")
