@@ -248,12 +248,10 @@ cudaError_t launch_keepset(const KeepParams& p, int max_keep, cudaStream_t s) {
     if (sl > max_slice) max_slice = sl;
   }
   const int cache_keys = max_slice < kKeepCacheKeys ? max_slice : kKeepCacheKeys;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(keepset_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kKeepCacheKeys * (int)sizeof(uint32_t));
+  static std::atomic<uint64_t> attr{0};
+  {
+    cudaError_t e = raise_smem_limit(keepset_kernel, kKeepCacheKeys * (int)sizeof(uint32_t), attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   cudaError_t e = launch_pdl(keepset_kernel, dim3(p.B * kKeepCL), dim3(kKeepThreads),
                              (size_t)(cache_keys > 0 ? cache_keys : 1) * sizeof(uint32_t), s, p, cache_keys);
@@ -564,12 +562,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
 template <int D, int BITS>
 static cudaError_t launch_append_t(const AppendParams& p, int max_ext_rows, cudaStream_t s) {
   const size_t smem = (size_t)(max_ext_rows > 0 ? max_ext_rows : 1) * 2 * D * sizeof(bf16);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(append_kernel<D, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         VC_APPEND_MAX_ROWS * 2 * D * (int)sizeof(bf16));
+  static std::atomic<uint64_t> attr{0};
+  {
+    cudaError_t e = raise_smem_limit(append_kernel<D, BITS>, VC_APPEND_MAX_ROWS * 2 * D * (int)sizeof(bf16), attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   return launch_pdl(append_kernel<D, BITS>, dim3(p.Hkv, p.B), dim3(kAppendThreads), smem, s, p);
 }

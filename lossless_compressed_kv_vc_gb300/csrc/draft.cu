@@ -943,12 +943,10 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
 template <int D, int KIND, int NHB>
 static cudaError_t launch_draft_t(const DraftParams& p, const DraftMaps* maps, int ctas_per_head, cudaStream_t s) {
   using C = DraftCfg<D, KIND>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(draft_attn_kernel<D, KIND, NHB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
+  static std::atomic<uint64_t> attr{0};
+  {
+    cudaError_t e = raise_smem_limit(draft_attn_kernel<D, KIND, NHB>, C::SMEM, attr);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   cudaError_t e;
   if constexpr (KIND == 0) {

@@ -1,6 +1,7 @@
 // Internal declarations shared by the kernels and the C-ABI layer of libvc (sm_103a only).
 #pragma once
 
+#include <atomic>
 #include <cuda.h>  // CUtensorMap (the encoder itself is fetched from the driver at run time)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -162,6 +163,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---- launch helpers ---------------------------------------------------------------------------------
+// Raise a kernel's dynamic shared-memory limit on the current device, once per device (the
+// attribute belongs to the device's context, so a process driving several GPUs sets it on each).
+template <typename Kernel>
+inline cudaError_t raise_smem_limit(Kernel kernel, int bytes, std::atomic<uint64_t>& devices_done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit && (devices_done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) devices_done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 // ---- programmatic dependent launch ----------------------------------------------------------------

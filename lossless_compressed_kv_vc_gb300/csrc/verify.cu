@@ -717,11 +717,10 @@ template <int D, int MODE>
 static cudaError_t launch_modes_t(const VerifyParams& p, cudaStream_t s) {
   using C = VCfg<D>;
   constexpr int SMEM = MODE == VMODE_VOTES ? C::SMEM_VOTES : C::SMEM;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(verify_attn_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  static std::atomic<uint64_t> attr{0};
+  {
+    cudaError_t e = raise_smem_limit(verify_attn_kernel<D, MODE>, SMEM, attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   return launch_pdl(verify_attn_kernel<D, MODE>, dim3(p.n_cta), dim3(C::THREADS), SMEM, s, p);
 }
