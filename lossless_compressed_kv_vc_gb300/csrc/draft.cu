@@ -611,6 +611,24 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   const int64_t p1 = s_cb[rb] + (in_part ? (int64_t)range_edge(wr + 1, nb, kw) : 0);
   const int n = (int)(p1 - p0);  // may be 0: the warp still takes part in the CTA's merge
   if (lane == 0) s_wreq[warp] = in_part ? rb : -1;
+  // Quantised groups: lane k < 6 streams one of a group's six contiguous runs (key codes, key
+  // scales, key zeros, value codes, value scales, value zeros); group g's run starts at this
+  // head's base plus g times a fixed stride, so the addresses are set up once per warp.
+  const uint8_t* q_src = nullptr;
+  uint32_t q_stride = 0, q_dst = 0;
+  if (!BF16_ROWS && in_part && lane < 6) {
+    const DraftReqDev& r = p.req[rb];
+    const size_t gcap = (size_t)hk * r.ng_cap;  // this head's first group (groups can be appended)
+    constexpr uint32_t SC = 2 * D;               // bytes of a group's scales (or zeros), keys or values
+    switch (lane) {
+      case 0: q_src = r.kc + gcap * C::KCB, q_stride = C::KCB, q_dst = C::OFF_KC; break;
+      case 1: q_src = reinterpret_cast<const uint8_t*>(r.ks) + gcap * SC, q_stride = SC, q_dst = C::OFF_KS; break;
+      case 2: q_src = reinterpret_cast<const uint8_t*>(r.kz) + gcap * SC, q_stride = SC, q_dst = C::OFF_KZ; break;
+      case 3: q_src = r.vc + gcap * C::KCB, q_stride = C::KCB, q_dst = C::OFF_VC; break;
+      case 4: q_src = reinterpret_cast<const uint8_t*>(r.vs) + gcap * SC, q_stride = SC, q_dst = C::OFF_VS; break;
+      default: q_src = reinterpret_cast<const uint8_t*>(r.vz) + gcap * SC, q_stride = SC, q_dst = C::OFF_VZ; break;
+    }
+  }
   pdl_launch_dependents();
   // Ordering against the previous kernel in the stream (programmatic dependent launch): queries,
   // kept rows and indices are never written by a draft step, verify or accept, so with p.early the
@@ -656,18 +674,11 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     uint8_t* sb = wb + st * C::STAGE;
     if (lc < r.n_mc) {
       if constexpr (!BF16_ROWS) {
-        // one quantised 32-token group: six contiguous runs
-        const int g = lc;
-        const int Tq = 32 * r.ng_cap;  // the head stride of the value scales (blocks can be appended)
+        // one quantised 32-token group: six contiguous runs, one per lane 0-5 (set up above)
         if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::QRAW);
         __syncwarp();
-        if (lane == 0) bulk_g2s_hint(sb + C::OFF_KC, r.kc + ((size_t)hk * r.ng_cap + g) * C::KCB, C::KCB, &bars[st], stream_pol);
-        if (lane == 1) bulk_g2s_hint(sb + C::OFF_KS, r.ks + ((size_t)hk * r.ng_cap + g) * D, 2 * D, &bars[st], stream_pol);
-        if (lane == 2) bulk_g2s_hint(sb + C::OFF_KZ, r.kz + ((size_t)hk * r.ng_cap + g) * D, 2 * D, &bars[st], stream_pol);
-        if (lane == 3)
-          bulk_g2s_hint(sb + C::OFF_VC, r.vc + ((size_t)hk * Tq + 32 * g) * (D * C::BITS / 8), C::KCB, &bars[st], stream_pol);
-        if (lane == 4) bulk_g2s_hint(sb + C::OFF_VS, r.vs + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st], stream_pol);
-        if (lane == 5) bulk_g2s_hint(sb + C::OFF_VZ, r.vz + ((size_t)hk * Tq + 32 * g) * (D / 32), 2 * D, &bars[st], stream_pol);
+        if (lane < 6)
+          bulk_g2s_hint(sb + q_dst, q_src + (size_t)lc * q_stride, q_stride, &bars[st], stream_pol);
       } else {
         // 16 kept rows by TMA gather4: lane l < G4_OPS loads rows 4(l%4)..4(l%4)+3 of one 64-channel
         // block of K or V. A row past the kept count repeats the chunk's first row, a kept row
