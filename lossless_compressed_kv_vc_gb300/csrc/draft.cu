@@ -54,7 +54,8 @@ struct DraftCfg {
   static constexpr int BAR_OFF = NW * PER_WARP;
   static constexpr int SMEM = BAR_OFF + NW * NST * 8 + 1024;  // + slack to put the stages on 1024 B
   static constexpr int G4_OPS = 2 * HALVES * 4;          // gather4 loads that fill a 16-row K+V stage
-  static constexpr int CHUNK_MAIN = (KIND == 0) ? 16 : 32;
+  static constexpr int GPC = (KIND == 2) ? 2 : 1;       // quantised groups per chunk (two 2-bit groups fit a stage)
+  static constexpr int CHUNK_MAIN = (KIND == 0) ? 16 : 32 * GPC;
   static constexpr int MT = D / 16;                      // 16-wide tiles over the head dim
   // raw layout of a quantised group inside a stage
   static constexpr int KCB = D * 4 * BITS;               // key codes of one group
@@ -65,6 +66,7 @@ struct DraftCfg {
   static constexpr int OFF_VS = OFF_VC + KCB;
   static constexpr int OFF_VZ = OFF_VS + 2 * D;
   static_assert(SMEM + 1024 <= 228 * 1024 / CTAS_PER_SM, "CTAs per SM");
+  static_assert(GPC * QRAW <= STAGE && QRAW % 16 == 0, "quantised groups of a chunk in one stage");
 };
 
 // Tensor maps are an argument of the token-drop kernels only.
@@ -614,13 +616,18 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   // Quantised groups: lane k < 6 streams one of a group's six contiguous runs (key codes, key
   // scales, key zeros, value codes, value scales, value zeros); group g's run starts at this
   // head's base plus g times a fixed stride, so the addresses are set up once per warp.
+  // With C::GPC = 2 (2-bit), lanes 6-11 stream the chunk's second group into the stage's second half.
   const uint8_t* q_src = nullptr;
   uint32_t q_stride = 0, q_dst = 0;
-  if (!BF16_ROWS && in_part && lane < 6) {
+  int q_grp = 0;
+  int q_ng = 0;  // the request's quantised groups
+  if (!BF16_ROWS && in_part) q_ng = p.req[rb].n_main / VC_GROUP;
+  if (!BF16_ROWS && in_part && lane < 6 * C::GPC) {
     const DraftReqDev& r = p.req[rb];
     const size_t gcap = (size_t)hk * r.ng_cap;  // this head's first group (groups can be appended)
     constexpr uint32_t SC = 2 * D;               // bytes of a group's scales (or zeros), keys or values
-    switch (lane) {
+    q_grp = lane / 6;
+    switch (lane % 6) {
       case 0: q_src = r.kc + gcap * C::KCB, q_stride = C::KCB, q_dst = C::OFF_KC; break;
       case 1: q_src = reinterpret_cast<const uint8_t*>(r.ks) + gcap * SC, q_stride = SC, q_dst = C::OFF_KS; break;
       case 2: q_src = reinterpret_cast<const uint8_t*>(r.kz) + gcap * SC, q_stride = SC, q_dst = C::OFF_KZ; break;
@@ -628,6 +635,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       case 4: q_src = reinterpret_cast<const uint8_t*>(r.vs) + gcap * SC, q_stride = SC, q_dst = C::OFF_VS; break;
       default: q_src = reinterpret_cast<const uint8_t*>(r.vz) + gcap * SC, q_stride = SC, q_dst = C::OFF_VZ; break;
     }
+    q_dst += q_grp * C::QRAW;
   }
   pdl_launch_dependents();
   // Ordering against the previous kernel in the stream (programmatic dependent launch): queries,
@@ -674,11 +682,14 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     uint8_t* sb = wb + st * C::STAGE;
     if (lc < r.n_mc) {
       if constexpr (!BF16_ROWS) {
-        // one quantised 32-token group: six contiguous runs, one per lane 0-5 (set up above)
-        if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::QRAW);
+        // the chunk's quantised groups (C::GPC, fewer at an odd end): six contiguous runs each, one
+        // per lane (set up above)
+        const int g0 = C::GPC * lc;
+        const int ngc = q_ng - g0 < C::GPC ? q_ng - g0 : C::GPC;
+        if (lane == 0) mbar_arrive_expect_tx(&bars[st], C::QRAW * ngc);
         __syncwarp();
-        if (lane < 6)
-          bulk_g2s_hint(sb + q_dst, q_src + (size_t)lc * q_stride, q_stride, &bars[st], stream_pol);
+        if (lane < 6 * ngc)
+          bulk_g2s_hint(sb + q_dst, q_src + (size_t)(g0 + q_grp) * q_stride, q_stride, &bars[st], stream_pol);
       } else {
         // 16 kept rows by TMA gather4: lane l < G4_OPS loads rows 4(l%4)..4(l%4)+3 of one 64-channel
         // block of K or V. A row past the kept count repeats the chunk's first row, a kept row
@@ -871,6 +882,8 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     uint8_t* sb = wb + st * C::STAGE;
     if (!BF16_ROWS && lc < r.n_mc) {
       qblock_attend<D, C::BITS, NHB>(sb, scale_q, qb, o, m, l, zs, lane);
+      if (C::GPC == 2 && C::GPC * lc + 1 < q_ng)
+        qblock_attend<D, C::BITS, NHB>(sb + C::QRAW, scale_q, qb, o, m, l, zs, lane);
       zs_live = true;
     } else {
       if (!BF16_ROWS && zs_live) {

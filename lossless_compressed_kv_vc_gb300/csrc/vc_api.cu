@@ -295,7 +295,8 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   const int bits = req[0].comp.bits;
   if (mode != VC_TOKEN_DROP && mode != VC_QUANT) return VC_ERR_INVALID;
   if (mode == VC_QUANT && bits != 2 && bits != 4) return VC_ERR_UNSUPPORTED;
-  const int chunk = mode == VC_QUANT ? 32 : 16;
+  // main chunk: 16 kept rows, one 4-bit group, or two 2-bit groups (the draft kernel's layout)
+  const int chunk = mode == VC_QUANT ? (bits == 2 ? 64 : 32) : 16;
 
   DraftParams p;
   memset(&p, 0, sizeof(p));
