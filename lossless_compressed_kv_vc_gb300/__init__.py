@@ -21,7 +21,7 @@ if not os.path.exists(LIB_PATH):
 _lib = C.CDLL(LIB_PATH)
 
 VC_OK, VC_ERR_INVALID, VC_ERR_UNSUPPORTED, VC_ERR_CUDA, VC_ERR_NOT_PINNED, VC_ERR_WORKSPACE = range(6)
-VC_DEV_OK, VC_DEV_BOUNDS, VC_DEV_TIMEOUT, VC_DEV_RANGE = range(4)
+VC_DEV_OK, VC_DEV_BOUNDS, VC_DEV_TIMEOUT, VC_DEV_RANGE, VC_DEV_INTERNAL = range(5)
 VC_TOKEN_DROP, VC_QUANT = 0, 1
 VC_CALL_DRAFT, VC_CALL_VERIFY = 0, 1
 VC_MAX_BATCH = 32

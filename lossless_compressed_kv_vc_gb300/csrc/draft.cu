@@ -658,7 +658,8 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     b = rb;
     lc = (int)(p0 + i - s_cb[rb]);
   };
-  // the row a lane copies for chunk i (its lane & 15 row), or -1: a token index for kept rows,
+  // the row a lane copies for chunk i (its lane & 15 row), or -1 for a padding row: a token index
+  // for kept rows (a negative one from the caller becomes INT_MAX, so the bounds check flags it),
   // a window row number for window chunks; loaded one stage ahead of its copy
   auto row_of = [&](int i) -> int {
     int b, lc;
@@ -669,7 +670,9 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       if (!BF16_ROWS) return 0;
       const int j = lc * 16 + row;
       if (j >= r.n_main) return -1;
-      return r.compact ? j : __ldg(r.idx + j);
+      if (r.compact) return j;
+      const int t = __ldg(r.idx + j);
+      return t < 0 ? INT_MAX : t;
     }
     const int j = (lc - r.n_mc) * 16 + row;
     return j <= r.n_win ? j : -1;

@@ -169,3 +169,21 @@ def test_quant_half_integer_ties(bits):
     assert int(bt.dev_status.item()) == 0
     ref = assert_quant_state(bt, 0, f32(r.k_full), f32(r.v_full), bits, w.residual_min)
     assert ref["ng"] == 3
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quant_flags_scale_out_of_fp16_range(bits):
+    """A key channel spanning more than 65504 x (2^bits - 1) in one group has no finite fp16 scale
+    (nor, at -6e5, a finite fp16 zero): compress sets VC_DEV_RANGE in the caller's status word."""
+    import lossless_compressed_kv_vc_gb300 as vc
+    w = configs.scaled(configs.qwen32b_quant2(), ctx_div=256, batch=1)
+    w.bits = bits
+    w.ctx = [224]
+    bt = make_batch(w, [0])
+    r = bt.reqs[0]
+    r.k_full[0, 0, 3] = 6.0e5
+    r.k_full[0, 1, 3] = -6.0e5
+    bt.dev_status.zero_()
+    bt.compress()
+    torch.cuda.synchronize()
+    assert int(bt.dev_status.item()) == vc.VC_DEV_RANGE

@@ -136,3 +136,23 @@ def test_draft_llama8b_full_size_sampled():
 def test_draft_qwen32b_quant2_full_size_sampled():
     w = configs.qwen32b_quant2()
     _sampled_full_size(w, [0, 15] + list(range(1, 15)), steps=[0, 24], heads=[3])
+
+
+@pytest.mark.parametrize("bad", ["past_end", "negative"])
+def test_draft_flags_out_of_range_keep_index(bad):
+    """A keep-set index at or past KV_full's rows, or a negative one, is not read: the draft step
+    sets VC_DEV_BOUNDS in the caller's status word, a kept row of the same chunk stands in, and
+    the outputs stay finite."""
+    import lossless_compressed_kv_vc_gb300 as vc
+    w = configs.scaled(configs.llama8b_drop(), ctx_div=32, batch=1, L=2)
+    bt = make_batch(w, [0])
+    bt.compress()
+    torch.cuda.synchronize()
+    r = bt.reqs[0]
+    r.idx[7] = w.ctx[0] + 10 if bad == "past_end" else -3
+    bt.dev_status.zero_()
+    bt.reset_window()
+    bt.draft_step(0)
+    torch.cuda.synchronize()
+    assert int(bt.dev_status.item()) == vc.VC_DEV_BOUNDS
+    assert torch.isfinite(r.o_draft[0].float()).all()
