@@ -494,14 +494,27 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
             for (int e = 0; e < VBN; ++e)
               if (e > last) x[e] = -INFINITY;
           }
-          float mx = x[0];
+          // tree reductions: a linear chain of 64 dependent max (or add) steps per tile would leave
+          // the two softmax warps per scheduler waiting on their own latency
+          float mx;
+          {
+            float t[VBN / 2];
 #pragma unroll
-          for (int e = 1; e < VBN; ++e) mx = fmaxf(mx, x[e]);
+            for (int e = 0; e < VBN / 2; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
+#pragma unroll
+            for (int w = VBN / 4; w >= 1; w >>= 1)
+#pragma unroll
+              for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+            mx = t[0];
+          }
           const float m_new = fmaxf(m_run, mx);
           if (m_new != -INFINITY) {
-            float sum = 0.f;
+            float acc[8];
 #pragma unroll
-            for (int e = 0; e < VBN; ++e) sum += ex2_approx(x[e] - m_new);
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int e = 0; e < VBN; ++e) acc[e & 7] += ex2_approx(x[e] - m_new);
+            const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             l_run = l_run * ex2_approx(m_run - m_new) + sum;
             m_run = m_new;
           }
