@@ -296,11 +296,13 @@ vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, si
  * |u - t| <= pool_kernel / 2: VC_POOL_MAX takes the largest in-range vote, VC_POOL_AVG the sum of
  * the in-range votes divided by pool_kernel (zero padding). pool_kernel = 1 leaves the votes as
  * they are. The result feeds vc_compress_kv's importance (any scale: only the order matters).
- * Arithmetic: bf16 products accumulated in fp32 on the tensor cores, softmax in fp32 (exp2 domain).
+ * Arithmetic: bf16 products accumulated in fp32 on the tensor cores, softmax in fp32 (exp2 domain),
+ * each key's sum over 128 window rows of the fp16-rounded weights (<= 1) on the tensor cores.
  *
- * Requirements: d = 64 or 128; W * (Hq/Hkv) a multiple of 32 and at most 256; pool_kernel odd,
- * 1..65; W <= ctx <= cap for every request; k, q_obs 16-byte aligned, importance 4-byte aligned.
- * The workspace (256-byte aligned) holds per-chunk row statistics and per-KV-head votes:
+ * Requirements: d = 64 or 128; any W >= 1 (the W * Hq/Hkv window rows of a KV head are processed
+ * in 128-row tiles); pool_kernel odd, 1..65; W <= ctx <= cap for every request; k, q_obs 16-byte
+ * aligned, importance 4-byte aligned. The workspace (256-byte aligned) holds the window rows'
+ * log-sum-exp (and per-CTA partials of it) and one vote partial per (KV head, row tile):
  * vc_importance_workspace_size(shape, W, max_ctx) bytes cover requests of up to max_ctx tokens.
  * Returns VC_ERR_INVALID / VC_ERR_UNSUPPORTED / VC_ERR_WORKSPACE before launching anything. */
 #define VC_POOL_MAX 0
