@@ -294,6 +294,35 @@ __device__ __forceinline__ uint32_t quant_code(float x, float sf, float zf, floa
   return (uint32_t)t;
 }
 
+// quant_code for two values at once: x - z and (x - z) * rs as packed f32x2 instructions, each lane
+// rounded exactly like the scalar ones, so the codes are the same.
+__device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi) {
+  return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
+}
+template <int BITS>
+__device__ __forceinline__ void quant_code2(float x0, float x1, float sf, float zf, float rs, uint32_t& c0,
+                                            uint32_t& c1) {
+  constexpr float QMAX = (float)((1 << BITS) - 1);
+  if (sf == 0.f) {
+    c0 = c1 = 0u;
+    return;
+  }
+  unsigned long long a2, y2;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(a2) : "l"(f32x2_pack(x0, x1)), "l"(f32x2_pack(-zf, -zf)));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y2) : "l"(a2), "l"(f32x2_pack(rs, rs)));
+  const float a[2] = {__uint_as_float((uint32_t)a2), __uint_as_float((uint32_t)(a2 >> 32))};
+  const float y[2] = {__uint_as_float((uint32_t)y2), __uint_as_float((uint32_t)(y2 >> 32))};
+  uint32_t c[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    float t = rintf(y[k]);
+    if (fabsf(y[k]) <= QMAX + 2.f && fabsf(y[k] - t) > 0.5f - 1e-4f) t = rintf(__fdiv_rn(a[k], sf));
+    c[k] = (uint32_t)fminf(fmaxf(t, 0.f), QMAX);
+  }
+  c0 = c[0];
+  c1 = c[1];
+}
+
 // A 32-token block's codes in shared memory, one byte per (token or channel row, column); rows are
 // padded by 4 bytes so that eight consecutive rows fall on eight different banks.
 template <int D>
@@ -367,7 +396,12 @@ __global__ void __launch_bounds__(D) quant_keys_kernel(const __grid_constant__ Q
   r.ks[gi] = s16;
   r.kz[gi] = z16;
 #pragma unroll
-  for (int t = 0; t < 32; ++t) codes[t][c] = (uint8_t)quant_code<BITS>(x[t], sf, zf, rs);
+  for (int t = 0; t < 32; t += 2) {
+    uint32_t c0, c1;
+    quant_code2<BITS>(x[t], x[t + 1], sf, zf, rs, c0, c1);
+    codes[t][c] = (uint8_t)c0;
+    codes[t + 1][c] = (uint8_t)c1;
+  }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(r.kc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
   for (int wi = c; wi < D * BITS; wi += D) dst[wi] = block_word<D, BITS, true>(codes, wi);
@@ -408,7 +442,12 @@ __global__ void __launch_bounds__(D) quant_values_kernel(const __grid_constant__
   r.vs[row * NG + cg] = s16;
   r.vz[row * NG + cg] = z16;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) codes[tt][32 * cg + e] = (uint8_t)quant_code<BITS>(x[e], sf, zf, rs);
+  for (int e = 0; e < 32; e += 2) {
+    uint32_t c0, c1;
+    quant_code2<BITS>(x[e], x[e + 1], sf, zf, rs, c0, c1);
+    codes[tt][32 * cg + e] = (uint8_t)c0;
+    codes[tt][32 * cg + e + 1] = (uint8_t)c1;
+  }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(r.vc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
   for (int wi = threadIdx.x; wi < D * BITS; wi += D) dst[wi] = block_word<D, BITS, false>(codes, wi);
