@@ -267,12 +267,14 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
   uint32_t acorr[4];
   code_offsets<BITS>(acorr);
   // block setup: scaled query fragments and the per-(row half, head) term of both halves
+  // (the zero term and the offset removal accumulate in separate registers: two independent MMA
+  // chains of MT instead of one of 2 MT)
   uint32_t qs[NHB][MT][2];
-  float cb[NHB][4];
+  float cb[NHB][4], co[NHB][4];
 #pragma unroll
   for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) cb[hb][e] = 0.f;
+    for (int e = 0; e < 4; ++e) cb[hb][e] = co[hb][e] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < MT; ++ks) {
     const int c = 16 * ks + 2 * b4;
@@ -286,23 +288,35 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
       qs[hb][ks][0] = hmul2_u32(qn[hb][ks][0], s0);
       qs[hb][ks][1] = hmul2_u32(qn[hb][ks][1], s1);
       mma_f16_16816(cb[hb], az, qn[hb][ks][0], qn[hb][ks][1]);
-      mma_f16_16816(cb[hb], acorr, qs[hb][ks][0], qs[hb][ks][1]);
+      mma_f16_16816(co[hb], acorr, qs[hb][ks][0], qs[hb][ks][1]);
     }
   }
+#pragma unroll
+  for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cb[hb][e] += co[hb][e];
 #pragma unroll 1
   for (int half = 0; half < 2; ++half) {
-    float s[NHB][4];
+    // even and odd k-steps in separate accumulators (two chains of MT / 2), added afterwards
+    float s[NHB][4], s2[NHB][4];
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[hb][e] = cb[hb][e];
+      for (int e = 0; e < 4; ++e) {
+        s[hb][e] = cb[hb][e];
+        s2[hb][e] = 0.f;
+      }
 #pragma unroll
     for (int ks = 0; ks < MT; ++ks) {
       uint32_t a[4];
       code_frag<BITS>(kw[(half * STEPS + (BITS == 4 ? ks : ks >> 1)) * 32 + lane], ks, a);
 #pragma unroll
-      for (int hb = 0; hb < NHB; ++hb) mma_f16_16816(s[hb], a, qs[hb][ks][0], qs[hb][ks][1]);
+      for (int hb = 0; hb < NHB; ++hb) mma_f16_16816((ks & 1) ? s2[hb] : s[hb], a, qs[hb][ks][0], qs[hb][ks][1]);
     }
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[hb][e] += s2[hb][e];
     // online softmax over the 16 tokens (rows lane/4 and lane/4 + 8; all valid); inside quantised
     // blocks the running maximum follows every new maximum, so the weights stay <= 1 (fp16 B)
     float p[NHB][2][2];
