@@ -294,33 +294,36 @@ __device__ __forceinline__ uint32_t quant_code(float x, float sf, float zf, floa
   return (uint32_t)t;
 }
 
-// quant_code for two values at once: x - z and (x - z) * rs as packed f32x2 instructions, each lane
-// rounded exactly like the scalar ones, so the codes are the same.
+// quant_code for two values that share a scale and zero, by packed f32x2 arithmetic: with
+// a = x - z, u = fl(a rs + 1.5 * 2^23) holds rint of the exact product a rs (half to even) in its bit
+// pattern (kMagicBits + rint for |a rs| < 2^22, and ordered like a rs outside), so an integer clamp
+// of the pattern gives the clamped code; d = fl(a rs - rint) is the product's distance from it.
+// Where the clamp does not decide (|a rs| <= 2^b + 1), a rs is within 2^-23 (2^b + 1) < 2.1e-6 of
+// fl(a / s), so a product at least 1e-5 from every half-integer rounds like the quotient; a pair
+// with either value nearer (or not a number) is recomputed by quant_code.
+constexpr float kMagic = 12582912.f;
+constexpr int32_t kMagicBits = 0x4B400000;
+constexpr float kTieGuard = 0.5f - 1e-5f;
 __device__ __forceinline__ unsigned long long f32x2_pack(float lo, float hi) {
   return (unsigned long long)__float_as_uint(lo) | ((unsigned long long)__float_as_uint(hi) << 32);
 }
 template <int BITS>
 __device__ __forceinline__ void quant_code2(float x0, float x1, float sf, float zf, float rs, uint32_t& c0,
                                             uint32_t& c1) {
-  constexpr float QMAX = (float)((1 << BITS) - 1);
-  if (sf == 0.f) {
-    c0 = c1 = 0u;
+  constexpr int32_t QMAX = (1 << BITS) - 1;
+  const unsigned long long m2 = f32x2_pack(kMagic, kMagic), rs2 = f32x2_pack(rs, rs);
+  unsigned long long a2, u2, tn2, d2;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(a2) : "l"(f32x2_pack(x0, x1)), "l"(f32x2_pack(-zf, -zf)));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(u2) : "l"(a2), "l"(rs2), "l"(m2));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(tn2) : "l"(m2), "l"(u2));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d2) : "l"(a2), "l"(rs2), "l"(tn2));
+  if (!(fabsf(__uint_as_float((uint32_t)d2)) <= kTieGuard) || !(fabsf(__uint_as_float((uint32_t)(d2 >> 32))) <= kTieGuard)) {
+    c0 = quant_code<BITS>(x0, sf, zf, rs);
+    c1 = quant_code<BITS>(x1, sf, zf, rs);
     return;
   }
-  unsigned long long a2, y2;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(a2) : "l"(f32x2_pack(x0, x1)), "l"(f32x2_pack(-zf, -zf)));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y2) : "l"(a2), "l"(f32x2_pack(rs, rs)));
-  const float a[2] = {__uint_as_float((uint32_t)a2), __uint_as_float((uint32_t)(a2 >> 32))};
-  const float y[2] = {__uint_as_float((uint32_t)y2), __uint_as_float((uint32_t)(y2 >> 32))};
-  uint32_t c[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    float t = rintf(y[k]);
-    if (fabsf(y[k]) <= QMAX + 2.f && fabsf(y[k] - t) > 0.5f - 1e-4f) t = rintf(__fdiv_rn(a[k], sf));
-    c[k] = (uint32_t)fminf(fmaxf(t, 0.f), QMAX);
-  }
-  c0 = c[0];
-  c1 = c[1];
+  c0 = (uint32_t)(min(max((int32_t)(uint32_t)u2, kMagicBits), kMagicBits + QMAX) - kMagicBits);
+  c1 = (uint32_t)(min(max((int32_t)(uint32_t)(u2 >> 32), kMagicBits), kMagicBits + QMAX) - kMagicBits);
 }
 
 // A 32-token block's codes in shared memory, one byte per (token or channel row, column); rows are
