@@ -9,8 +9,10 @@
 // threshold go to the lower indices), then appends the recent window. An optional second launch
 // gathers the kept rows.
 // Quantisation: key groups (32 tokens of one channel) one thread per channel; value groups
-// (32 channels of one token) one lane per 4 channels with shuffle min/max; every float decision
-// uses IEEE round-to-nearest (division, rint half-to-even, fp32->fp16), as the format defines.
+// (32 channels of one token) one thread per group (the post-accept append: one lane per D/32
+// channels with shuffle min/max); every code equals the format's definition with IEEE
+// round-to-nearest (division, rint half-to-even, fp32->fp16), by a fast rounding whose result is
+// proven equal away from half-integers and the exact division near them.
 #include "vc_internal.cuh"
 
 #include <math.h>
