@@ -328,6 +328,29 @@ __device__ __forceinline__ void quant_code2(float x0, float x1, float sf, float 
   c1 = (uint32_t)(min(max((int32_t)(uint32_t)(u2 >> 32), kMagicBits), kMagicBits + QMAX) - kMagicBits);
 }
 
+// A group's minimum and maximum from 16 bf16x2 words by pairwise trees (min and max select exactly,
+// so the order does not change the result): the two lanes of the results hold the minimum (maximum)
+// over the words' low and high halves.
+__device__ __forceinline__ void minmax_tree16(const uint32_t (&w)[16], __nv_bfloat162& mn, __nv_bfloat162& mx) {
+  __nv_bfloat162 lo[8], hi[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[2 * k]);
+    const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(&w[2 * k + 1]);
+    lo[k] = __hmin2(x, y);
+    hi[k] = __hmax2(x, y);
+  }
+#pragma unroll
+  for (int st = 4; st >= 1; st >>= 1)
+#pragma unroll
+    for (int k = 0; k < st; ++k) {
+      lo[k] = __hmin2(lo[k], lo[k + st]);
+      hi[k] = __hmax2(hi[k], hi[k + st]);
+    }
+  mn = lo[0];
+  mx = hi[0];
+}
+
 // A 32-token block's codes in shared memory, one byte per (token or channel row, column); rows are
 // padded by 4 bytes so that eight consecutive rows fall on eight different banks.
 template <int D>
@@ -416,7 +439,7 @@ __global__ void __launch_bounds__(D) quant_keys_kernel(const __grid_constant__ Q
 // its 32-channel group i % (D/32), reading the group's 64 contiguous bytes with four 16-byte loads
 // (a warp covers 2 KB of consecutive rows); the codes meet in shared memory for the word packing.
 template <int D, int BITS>
-__global__ void __launch_bounds__(D) quant_values_kernel(const __grid_constant__ QuantParams p) {
+__global__ void __launch_bounds__(D, 12) quant_values_kernel(const __grid_constant__ QuantParams p) {
   const QuantReq& r = p.req[blockIdx.z];
   const int g = blockIdx.x, h = blockIdx.y;
   if (g >= r.ng) return;
@@ -425,21 +448,20 @@ __global__ void __launch_bounds__(D) quant_values_kernel(const __grid_constant__
   const int tt = threadIdx.x / NG, cg = threadIdx.x % NG;
   const int t = 32 * g + tt;
   const uint4* src = reinterpret_cast<const uint4*>(r.v + ((size_t)h * r.cap + t) * D + 32 * cg);
-  float x[32];
-  float mn = INFINITY, mx = -INFINITY;
+  // the group's 32 values stay bf16, paired (channels 2e, 2e + 1) in 16 registers
+  uint32_t xw[16];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint4 u = __ldg(src + k);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-      x[8 * k + 2 * e] = f.x;
-      x[8 * k + 2 * e + 1] = f.y;
-      mn = fminf(mn, fminf(f.x, f.y));
-      mx = fmaxf(mx, fmaxf(f.x, f.y));
-    }
+    xw[4 * k] = u.x;
+    xw[4 * k + 1] = u.y;
+    xw[4 * k + 2] = u.z;
+    xw[4 * k + 3] = u.w;
   }
+  __nv_bfloat162 mn2, mx2;
+  minmax_tree16(xw, mn2, mx2);
+  const float mn = fminf(__low2float(mn2), __high2float(mn2));
+  const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
   __half s16, z16;
   float sf, zf, rs;
   quant_params<BITS>(mn, mx, s16, z16, sf, zf, rs, p.dev_status);
@@ -447,11 +469,11 @@ __global__ void __launch_bounds__(D) quant_values_kernel(const __grid_constant__
   r.vs[row * NG + cg] = s16;
   r.vz[row * NG + cg] = z16;
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
+  for (int e = 0; e < 16; ++e) {
     uint32_t c0, c1;
-    quant_code2<BITS>(x[e], x[e + 1], sf, zf, rs, c0, c1);
-    codes[tt][32 * cg + e] = (uint8_t)c0;
-    codes[tt][32 * cg + e + 1] = (uint8_t)c1;
+    quant_code2<BITS>(__uint_as_float(xw[e] << 16), __uint_as_float(xw[e] & 0xFFFF0000u), sf, zf, rs, c0, c1);
+    codes[tt][32 * cg + 2 * e] = (uint8_t)c0;
+    codes[tt][32 * cg + 2 * e + 1] = (uint8_t)c1;
   }
   __syncthreads();
   uint32_t* dst = reinterpret_cast<uint32_t*>(r.vc + ((size_t)h * r.ng_cap + g) * (4 * D * BITS));
