@@ -1,9 +1,10 @@
 """Python binding of libvc, the GB300 (sm_103a) VeriCache draft/verify/accept hot path.
 
 Argument marshalling only: every step runs in the library's CUDA kernels. The names follow the
-C ABI in include/vc.h (vc_compress_kv, vc_draft_attn, vc_verify_attn(_heads), vc_accept, vc_append_kv,
-vc_stage_full_kv, vc_workspace_size, vc_status_string). Tensors are torch tensors on the GPU;
-their data pointers and the current (or given) CUDA stream are passed through.
+C ABI in include/vc.h (vc_compress_kv, vc_draft_attn(_noalloc), vc_verify_attn(_heads), vc_accept,
+vc_append_kv, vc_stage_full_kv, vc_snapkv_importance, vc_plan_stagger, vc_stagger_period and the
+workspace-size / status-string calls). Tensors are torch tensors on the GPU; their data pointers
+and the current (or given) CUDA stream are passed through.
 
 Importing this package loads libvc.so and raises ImportError when it has not been built
 (`python -c "import __graft_entry__ as g; g.build()"`); there is no fallback path.

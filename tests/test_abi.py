@@ -156,3 +156,18 @@ def test_importance_validation_rejects_without_launching(lib):
     arr[0].full.ctx = 7
     assert call(8) == vc.VC_ERR_INVALID           # context shorter than the window
     assert vc.vc_importance_workspace_size(shp, 8, 100) > 0
+
+
+def test_binding_refuses_to_import_without_the_library(tmp_path):
+    """No fallback path: the package raises ImportError when libvc.so is absent."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "lossless_compressed_kv_vc_gb300"
+    pkg.mkdir()
+    shutil.copy(os.path.join(ROOT, "lossless_compressed_kv_vc_gb300", "__init__.py"), pkg / "__init__.py")
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "try:\n    import lossless_compressed_kv_vc_gb300\nexcept ImportError as e:\n"
+            "    print('refused:', e); sys.exit(0)\nsys.exit(3)\n") % str(tmp_path)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=str(tmp_path))
+    assert r.returncode == 0 and "libvc.so is not built" in r.stdout, (r.returncode, r.stdout, r.stderr)
