@@ -352,6 +352,20 @@ vc_status vc_plan_stagger(const vc_stagger_cost* cost, int32_t n, int32_t* group
 /* T of a given split (group[r] in {0, 1}) under the same model; same errors, any n >= 1. */
 vc_status vc_stagger_period(const vc_stagger_cost* cost, int32_t n, const int32_t* group, int64_t* period_ns);
 
+/* vc_plan_stagger_local — a split for batches beyond the exact planner's reach (any n up to
+ * VC_STAGGER_LOCAL_MAX), under the same model, arguments and output convention (request 0 in A,
+ * both groups non-empty when n >= 2, period_ns may be NULL). Local search, no optimality
+ * guarantee: three seeds (first half / second half, alternating, and a greedy pass by decreasing
+ * d + s + v that adds each request where the split-dependent part of 2T over the partial sums is
+ * lower) are each improved by first-improvement descent over single moves and swaps of one request
+ * of each group, compared exactly as 2T; the best result (ties: the earlier seed) is returned. The
+ * returned split is one that no single move and no swap improves, unless a descent reached its
+ * limit of 64 n + 1024 improving steps. O(n^2) per improving step; deterministic.
+ * Errors: VC_ERR_INVALID (as vc_plan_stagger); VC_ERR_UNSUPPORTED (n > VC_STAGGER_LOCAL_MAX).
+ * Host only, no GPU work. */
+#define VC_STAGGER_LOCAL_MAX 4096
+vc_status vc_plan_stagger_local(const vc_stagger_cost* cost, int32_t n, int32_t* group, int64_t* period_ns);
+
 /* ------------------------------------------------------------------------------------------ */
 /* Workspace bytes vc_draft_attn (call = VC_CALL_DRAFT) or vc_verify_attn (VC_CALL_VERIFY) needs
  * for `shape`; max_rows = the largest n_rows of a verify call (ignored for draft). The workspace

@@ -2,7 +2,7 @@
 
 Argument marshalling only: every step runs in the library's CUDA kernels. The names follow the
 C ABI in include/vc.h (vc_compress_kv, vc_draft_attn(_noalloc), vc_verify_attn(_heads), vc_accept,
-vc_append_kv, vc_stage_full_kv, vc_snapkv_importance, vc_plan_stagger, vc_stagger_period and the
+vc_append_kv, vc_stage_full_kv, vc_snapkv_importance, vc_plan_stagger(_local), vc_stagger_period and the
 workspace-size / status-string calls). Tensors are torch tensors on the GPU; their data pointers
 and the current (or given) CUDA stream are passed through.
 
@@ -28,6 +28,7 @@ VC_CALL_DRAFT, VC_CALL_VERIFY = 0, 1
 VC_MAX_BATCH = 32
 VC_APPEND_MAX_ROWS = 256
 VC_STAGGER_MAX = 24
+VC_STAGGER_LOCAL_MAX = 4096
 VC_POOL_MAX, VC_POOL_AVG = 0, 1
 
 _p = C.c_void_p
@@ -87,6 +88,7 @@ _lib.vc_importance_workspace_size.argtypes = [C.POINTER(vc_shape), _i32, _i32]
 _lib.vc_importance_workspace_size.restype = C.c_size_t
 _lib.vc_plan_stagger.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
 _lib.vc_stagger_period.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
+_lib.vc_plan_stagger_local.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
 _lib.vc_workspace_size.argtypes = [_i32, C.POINTER(vc_shape), _i32]
 _lib.vc_workspace_size.restype = C.c_size_t
 _lib.vc_status_string.argtypes = [_i32]
@@ -94,12 +96,12 @@ _lib.vc_status_string.restype = C.c_char_p
 _lib.vc_version.restype = _i32
 for _f in ("vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
            "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_plan_stagger", "vc_stagger_period",
-           "vc_snapkv_importance"):
+           "vc_plan_stagger_local", "vc_snapkv_importance"):
     getattr(_lib, _f).restype = _i32
 
 EXPORTS = ["vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
            "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_plan_stagger", "vc_stagger_period",
-           "vc_snapkv_importance", "vc_importance_workspace_size", "vc_workspace_size", "vc_status_string",
+           "vc_plan_stagger_local", "vc_snapkv_importance", "vc_importance_workspace_size", "vc_workspace_size", "vc_status_string",
            "vc_version"]
 
 
@@ -235,6 +237,17 @@ def vc_plan_stagger(costs, raise_on_error=True):
     t = C.c_int64(0)
     st = _lib.vc_plan_stagger(_costs(costs) if n else None, n, grp, C.byref(t))
     _check(st, "vc_plan_stagger", raise_on_error)
+    return st, list(grp)[:n], t.value
+
+
+def vc_plan_stagger_local(costs, raise_on_error=True):
+    """Local-search two-group split for any batch up to VC_STAGGER_LOCAL_MAX requests (no
+    optimality guarantee). Returns (status, groups list, period_ns)."""
+    n = len(costs)
+    grp = (_i32 * max(n, 1))()
+    t = C.c_int64(0)
+    st = _lib.vc_plan_stagger_local(_costs(costs) if n else None, n, grp, C.byref(t))
+    _check(st, "vc_plan_stagger_local", raise_on_error)
     return st, list(grp)[:n], t.value
 
 

@@ -6,7 +6,9 @@
 // model and the exact split are stated in include/vc.h (vc_plan_stagger).
 #include "vc.h"
 
+#include <algorithm>
 #include <cstdint>
+#include <vector>
 
 namespace {
 
@@ -98,6 +100,144 @@ extern "C" vc_status vc_plan_stagger(const vc_stagger_cost* cost, int32_t n, int
   }
   group[0] = 0;
   for (int32_t r = 1; r < n; ++r) group[r] = (int32_t)((best_mask >> (r - 1)) & 1u);
+  if (period_ns) *period_ns = (best + 1) / 2;
+  return VC_OK;
+}
+
+namespace {
+
+// A split with group A's sums, kept in step with its moves.
+struct Split {
+  std::vector<int32_t> g;  // 0 = A, 1 = B
+  int64_t dA = 0, sA = 0, vA = 0;
+  int32_t nA = 0;
+};
+
+void sums_of(Split& sp, const vc_stagger_cost* c, int32_t n) {
+  sp.dA = sp.sA = sp.vA = 0;
+  sp.nA = 0;
+  for (int32_t r = 0; r < n; ++r)
+    if (sp.g[r] == 0) {
+      sp.dA += c[r].draft_ns;
+      sp.sA += c[r].stage_ns;
+      sp.vA += c[r].verify_ns;
+      ++sp.nA;
+    }
+}
+
+// First-improvement descent: scan the single moves (request r to the other group, both groups
+// staying non-empty) in index order, then the swaps (r in A with q in B) in (r, q) order; apply the
+// first that lowers 2T and start over. Stops when none does or after max_steps improvements.
+void descend(Split& sp, const vc_stagger_cost* c, int32_t n, int64_t D, int64_t S, int64_t V, int64_t max_steps) {
+  int64_t cur = period2(sp.dA, sp.sA, sp.vA, D, S, V);
+  for (int64_t step = 0; step < max_steps; ++step) {
+    bool moved = false;
+    for (int32_t r = 0; r < n && !moved; ++r) {
+      const bool inA = sp.g[r] == 0;
+      if (inA ? sp.nA == 1 : sp.nA == n - 1) continue;
+      const int64_t sg = inA ? -1 : 1;
+      const int64_t t = period2(sp.dA + sg * c[r].draft_ns, sp.sA + sg * c[r].stage_ns,
+                                sp.vA + sg * c[r].verify_ns, D, S, V);
+      if (t < cur) {
+        sp.g[r] ^= 1;
+        sp.dA += sg * c[r].draft_ns;
+        sp.sA += sg * c[r].stage_ns;
+        sp.vA += sg * c[r].verify_ns;
+        sp.nA += inA ? -1 : 1;
+        cur = t;
+        moved = true;
+      }
+    }
+    for (int32_t r = 0; r < n && !moved; ++r) {
+      if (sp.g[r] != 0) continue;
+      for (int32_t q = 0; q < n && !moved; ++q) {
+        if (sp.g[q] != 1) continue;
+        const int64_t dA = sp.dA - c[r].draft_ns + c[q].draft_ns;
+        const int64_t sA = sp.sA - c[r].stage_ns + c[q].stage_ns;
+        const int64_t vA = sp.vA - c[r].verify_ns + c[q].verify_ns;
+        const int64_t t = period2(dA, sA, vA, D, S, V);
+        if (t < cur) {
+          sp.g[r] = 1;
+          sp.g[q] = 0;
+          sp.dA = dA;
+          sp.sA = sA;
+          sp.vA = vA;
+          cur = t;
+          moved = true;
+        }
+      }
+    }
+    if (!moved) return;
+  }
+}
+
+}  // namespace
+
+extern "C" vc_status vc_plan_stagger_local(const vc_stagger_cost* cost, int32_t n, int32_t* group,
+                                           int64_t* period_ns) {
+  if (!cost || !group || n < 1) return VC_ERR_INVALID;
+  if (n > VC_STAGGER_LOCAL_MAX) return VC_ERR_UNSUPPORTED;
+  if (!costs_ok(cost, n)) return VC_ERR_INVALID;
+  int64_t D = 0, S = 0, V = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    D += cost[r].draft_ns;
+    S += cost[r].stage_ns;
+    V += cost[r].verify_ns;
+  }
+  if (n == 1) {
+    group[0] = 0;
+    if (period_ns) *period_ns = (period2(D, S, V, D, S, V) + 1) / 2;
+    return VC_OK;
+  }
+  // seeds: first half / second half, alternating, and a greedy pass that takes the requests by
+  // decreasing d + s + v and puts each where the split-dependent part of 2T over the partial sums,
+  // max(2 (S_A + V_A), 2 (S_B + V_B), S + V + D_A, S + V + D_B), comes out lower (ties: the group
+  // with fewer requests, then A)
+  std::vector<Split> seeds(3);
+  for (auto& sp : seeds) sp.g.assign(n, 0);
+  for (int32_t r = 0; r < n; ++r) {
+    seeds[0].g[r] = r < (n + 1) / 2 ? 0 : 1;
+    seeds[1].g[r] = r & 1;
+  }
+  {
+    std::vector<int32_t> order(n);
+    for (int32_t r = 0; r < n; ++r) order[r] = r;
+    auto load = [&](int32_t r) { return cost[r].draft_ns + cost[r].stage_ns + cost[r].verify_ns; };
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return load(a) > load(b); });
+    const int64_t W = S + V;
+    int64_t x[2] = {0, 0}, y[2] = {0, 0};
+    int32_t cnt[2] = {0, 0};
+    for (int32_t r : order) {
+      const int64_t xr = cost[r].stage_ns + cost[r].verify_ns, yr = cost[r].draft_ns;
+      int64_t part[2];
+      for (int k = 0; k < 2; ++k) {
+        const int64_t x0 = x[0] + (k == 0 ? xr : 0), x1 = x[1] + (k == 1 ? xr : 0);
+        const int64_t y0 = y[0] + (k == 0 ? yr : 0), y1 = y[1] + (k == 1 ? yr : 0);
+        part[k] = max64(max64(2 * x0, 2 * x1), max64(W + y0, W + y1));
+      }
+      const int k = part[1] < part[0] || (part[1] == part[0] && cnt[1] < cnt[0]) ? 1 : 0;
+      seeds[2].g[r] = k;
+      x[k] += xr;
+      y[k] += yr;
+      ++cnt[k];
+    }
+    if (cnt[0] == 0 || cnt[1] == 0) seeds[2].g[order[n - 1]] ^= 1;  // keep both groups non-empty
+  }
+  const int64_t max_steps = 64 * (int64_t)n + 1024;
+  int best_i = -1;
+  int64_t best = INT64_MAX;
+  for (int i = 0; i < 3; ++i) {
+    sums_of(seeds[i], cost, n);
+    descend(seeds[i], cost, n, D, S, V, max_steps);
+    const int64_t t = period2(seeds[i].dA, seeds[i].sA, seeds[i].vA, D, S, V);
+    if (t < best) {
+      best = t;
+      best_i = i;
+    }
+  }
+  const std::vector<int32_t>& g = seeds[best_i].g;
+  const int32_t flip = g[0];  // T(A) = T(B): name the group of request 0 A
+  for (int32_t r = 0; r < n; ++r) group[r] = g[r] ^ flip;
   if (period_ns) *period_ns = (best + 1) / 2;
   return VC_OK;
 }

@@ -466,10 +466,12 @@ def stagger_costs(draft_ns, verify_ns, stage_ns):
 
 
 def plan_groups(costs):
-    """Split requests into the two alternating groups of StaggeredOffload by the library's exact
-    planner (vc_plan_stagger). Returns ([indices of group 0], [indices of group 1], period_ns)."""
-    from . import vc_plan_stagger
-    st, groups, t = vc_plan_stagger(costs)
+    """Split requests into the two alternating groups of StaggeredOffload by the library's planner:
+    exact (vc_plan_stagger) up to VC_STAGGER_MAX requests, local search (vc_plan_stagger_local)
+    beyond. Returns ([indices of group 0], [indices of group 1], period_ns)."""
+    from . import vc_plan_stagger, vc_plan_stagger_local, VC_STAGGER_MAX
+    plan = vc_plan_stagger if len(costs) <= VC_STAGGER_MAX else vc_plan_stagger_local
+    st, groups, t = plan(costs)
     return [r for r, g in enumerate(groups) if g == 0], [r for r, g in enumerate(groups) if g == 1], t
 
 

@@ -139,6 +139,87 @@ def test_plan_stagger_ties_and_limits():
     assert vc.vc_stagger_period([(1, 1, 1)], [2], raise_on_error=False)[0] == vc.VC_ERR_INVALID
 
 
+def _random_costs(rng, n):
+    costs = []
+    for _ in range(n):
+        d, v, s = (int(x) for x in rng.integers(0, 5_000_000, 3))
+        if rng.random() < 0.4:
+            s = 0  # KV_full resident in HBM
+        costs.append((d, v, s))
+    return costs
+
+
+def test_plan_stagger_local_is_a_local_optimum_of_the_oracle_period():
+    """Beyond the exact planner: the split is valid, its period is the oracle's period of that
+    split, and no single move or swap of two requests lowers the oracle's 2T."""
+    import numpy as np
+    import oracle as O
+    import lossless_compressed_kv_vc_gb300 as vc
+    rng = np.random.default_rng(23)
+    for n in (2, 3, 5, 9, 17, 25, 33, 64):
+        for _ in range(3):
+            costs = _random_costs(rng, n)
+            st, groups, t = vc.vc_plan_stagger_local(costs)
+            assert st == vc.VC_OK and groups[0] == 0 and 0 < sum(groups) < n
+            assert t == O.stagger_period(costs, groups)
+            t2 = O.stagger_period2(costs, groups)
+            for r in range(n):
+                g = list(groups)
+                g[r] ^= 1
+                if 0 < sum(g) < n:
+                    assert O.stagger_period2(costs, g) >= t2, (n, r)
+            for r in [i for i in range(n) if groups[i] == 0]:
+                for q in [i for i in range(n) if groups[i] == 1]:
+                    g = list(groups)
+                    g[r], g[q] = 1, 0
+                    assert O.stagger_period2(costs, g) >= t2, (n, r, q)
+
+
+def test_plan_stagger_local_against_the_exact_split():
+    """Never below the oracle's exact optimum (it cannot be), and on these random batches it finds it."""
+    import numpy as np
+    import oracle as O
+    import lossless_compressed_kv_vc_gb300 as vc
+    rng = np.random.default_rng(29)
+    found = total = 0
+    for n in range(2, 12):
+        for _ in range(8):
+            costs = _random_costs(rng, n)
+            t = vc.vc_plan_stagger_local(costs)[2]
+            t_exact = O.plan_stagger(costs)[1]
+            assert t >= t_exact
+            found += t == t_exact
+            total += 1
+    assert found >= 0.9 * total, (found, total)
+
+
+def test_plan_stagger_local_limits_and_engine_choice():
+    import time
+    import numpy as np
+    import oracle as O
+    import lossless_compressed_kv_vc_gb300 as vc
+    from lossless_compressed_kv_vc_gb300 import engine
+    st, groups, t = vc.vc_plan_stagger_local([(5, 3, 7)])
+    assert (st, groups, t) == (vc.VC_OK, [0], O.stagger_period([(5, 3, 7)], [0]))
+    rng = np.random.default_rng(31)
+    big = _random_costs(rng, vc.VC_STAGGER_LOCAL_MAX)
+    t0 = time.time()
+    st, groups, t = vc.vc_plan_stagger_local(big)
+    assert st == vc.VC_OK and time.time() - t0 < 10.0 and 0 < sum(groups) < len(big)
+    assert vc.vc_stagger_period(big, groups)[1] == t
+    assert vc.vc_plan_stagger_local(big + [(1, 1, 1)], raise_on_error=False)[0] == vc.VC_ERR_UNSUPPORTED
+    assert vc.vc_plan_stagger_local([], raise_on_error=False)[0] == vc.VC_ERR_INVALID
+    assert vc.vc_plan_stagger_local([(1, -1, 0)], raise_on_error=False)[0] == vc.VC_ERR_INVALID
+    # the engine plans exactly up to VC_STAGGER_MAX requests and by local search beyond
+    small = _random_costs(rng, 10)
+    a, b, t = engine.plan_groups(small)
+    assert t == O.plan_stagger(small)[1] and sorted(a + b) == list(range(10))
+    many = _random_costs(rng, vc.VC_STAGGER_MAX + 6)
+    a, b, t = engine.plan_groups(many)
+    assert a and b and sorted(a + b) == list(range(len(many)))
+    assert t == vc.vc_plan_stagger_local(many)[2]
+
+
 def test_importance_validation_rejects_without_launching(lib):
     import lossless_compressed_kv_vc_gb300 as vc
     arr = (vc.vc_importance_req * 1)()
