@@ -190,7 +190,13 @@ vc_status vc_append_kv(const vc_shape* shape, vc_kv_full* full, vc_kv_comp* comp
  * (kept rows, or dequantised groups) followed by window rows 0..n_win, where window row n_win is
  * (k_new, v_new). The call also stores k_new/v_new into window row n_win (needs n_win < win_cap).
  * Accumulation is fp32; the output is rounded to bf16.
+ * ws: a workspace of at least vc_workspace_size(VC_CALL_DRAFT, shape, 0) bytes whose first
+ * VC_DRAFT_COUNTER_BYTES were zero-filled once (see vc_workspace_size). Hkv <= VC_DRAFT_MAX_KV_HEADS
+ * and Hq/Hkv <= 16 (VC_ERR_UNSUPPORTED otherwise).
  */
+#define VC_DRAFT_MAX_KV_HEADS 256                                   /* Hkv limit of a draft call */
+#define VC_DRAFT_COUNTER_BYTES ((size_t)VC_DRAFT_MAX_KV_HEADS * VC_MAX_BATCH * 4)  /* 32 KiB */
+
 typedef struct vc_draft_req {
   const void* q;       /* bf16 [Hq][d]: query of the token drafted at this step */
   const void* k_new;   /* bf16 [Hkv][d]: its key */
@@ -212,10 +218,14 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
  * array of VC_DRAFT_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU that loads the
  * library holds it until the process exits. The first call made with a given device current looks
  * up the array's device address (cudaGetSymbolAddress), zero-fills the array on `stream` and
- * caches the address: make that first call before any stream capture. The call allocates nothing. Returns VC_ERR_WORKSPACE when the call needs more
- * scratch than the array holds (vc_workspace_size(VC_CALL_DRAFT, shape, 0) > the limit). All calls
- * share the array, which keeps the last call's contents (nothing in it needs clearing); calls that
- * overlap on the GPU race on it, so issue them on one stream or order them with events. */
+ * caches the address: make that first call before any stream capture. The call allocates nothing.
+ * Returns VC_ERR_WORKSPACE when the call needs more scratch than the array holds
+ * (vc_workspace_size(VC_CALL_DRAFT, shape, 0) > the limit). All calls share the array, which keeps
+ * the last call's contents: its arrival counters (the first VC_DRAFT_COUNTER_BYTES, at the same
+ * place for every shape) start at zero and every call leaves them at zero, and the partials after
+ * them are written before they are read, so calls of different shapes may follow one another.
+ * Calls that overlap on the GPU race on the array, so issue them on one stream or order them with
+ * events. */
 #define VC_DRAFT_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
 vc_status vc_draft_attn_noalloc(const vc_shape* shape, const vc_draft_req* req, int32_t* dev_status,
@@ -263,7 +273,8 @@ vc_status vc_verify_attn_heads(const vc_shape* shape, const vc_verify_req* req, 
  *
  * logits: fp32 [B][L_max+1][V]; row i of request b is the full-cache prediction after its i-th
  *   verified input (row 0 follows the last accepted token, row i follows draft i-1).
- * draft: int32 [B][L_max]; L: device int32 [B], 0 <= L[b] <= L_max.
+ * draft: int32 [B][L_max]; L: device int32 [B], 0 <= L[b] <= L_max (a value outside that range is
+ * clamped to it on the device, so no row outside request b's is read).
  * a_i = argmax of row i (first maximal index; logits must be finite); n = first i < L[b] with
  * a_i != draft[i], else L[b]. Writes out_tokens[b] = draft[0..n-1], a_n, then -1 up to L_max+1
  * entries, and n_acc[b] = n + 1 (1..L[b]+1).
@@ -369,10 +380,12 @@ vc_status vc_plan_stagger_local(const vc_stagger_cost* cost, int32_t n, int32_t*
 /* ------------------------------------------------------------------------------------------ */
 /* Workspace bytes vc_draft_attn (call = VC_CALL_DRAFT) or vc_verify_attn (VC_CALL_VERIFY) needs
  * for `shape`; max_rows = the largest n_rows of a verify call (ignored for draft). The workspace
- * holds per-split partial outputs. The draft workspace also starts with per-(KV head, request)
- * arrival counters: zero-fill a draft workspace once before its first call; every call returns the
- * counters to zero. The verify workspace needs no initialisation. Calls that overlap on the GPU
- * must not share a workspace. */
+ * holds per-split partial outputs. The draft workspace also starts with a block of
+ * VC_DRAFT_COUNTER_BYTES of per-(KV head, request) arrival counters, the same bytes for every
+ * shape (room for VC_DRAFT_MAX_KV_HEADS heads): zero-fill at least that block once before the
+ * first call; every call returns the counters to zero, so one workspace can serve calls of any
+ * shape it is large enough for. The verify workspace needs no initialisation. Calls that overlap
+ * on the GPU must not share a workspace. */
 size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows);
 
 const char* vc_status_string(vc_status s);

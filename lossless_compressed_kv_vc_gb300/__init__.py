@@ -30,6 +30,9 @@ VC_APPEND_MAX_ROWS = 256
 VC_STAGGER_MAX = 24
 VC_STAGGER_LOCAL_MAX = 4096
 VC_POOL_MAX, VC_POOL_AVG = 0, 1
+VC_DRAFT_MAX_KV_HEADS = 256
+VC_DRAFT_COUNTER_BYTES = VC_DRAFT_MAX_KV_HEADS * VC_MAX_BATCH * 4
+VC_DRAFT_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _p = C.c_void_p
 _i32 = C.c_int32

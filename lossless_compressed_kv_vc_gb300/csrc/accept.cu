@@ -20,6 +20,9 @@ __device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
   }
 }
 
+// L[b] from the device, held to [0, L_max] so that no row or draft outside request b's is read.
+__device__ __forceinline__ int clamp_L(int Lb, int L_max) { return Lb < 0 ? 0 : (Lb > L_max ? L_max : Lb); }
+
 constexpr int kAcceptThreads = 512;
 
 __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(AcceptArgs a) {
@@ -28,7 +31,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(AcceptArg
   const int row = blockIdx.x;
   const int rows = a.L_max + 1;
   const int b = row / rows, i = row % rows;
-  if (i > __ldg(a.L + b)) return;
+  if (i > clamp_L(__ldg(a.L + b), a.L_max)) return;
   const float* x = a.logits + (size_t)row * a.V;
   const int V = a.V;
   float bv = -INFINITY;
@@ -99,7 +102,7 @@ __global__ void accept_finalize_kernel(AcceptArgs a) {
   const int lane = threadIdx.x & 31;
   if (b >= a.B) return;
   const int rows = a.L_max + 1;
-  const int Lb = __ldg(a.L + b);
+  const int Lb = clamp_L(__ldg(a.L + b), a.L_max);
   int32_t* out = a.out_tokens + (size_t)b * rows;
   const int32_t* x = a.draft + (size_t)b * a.L_max;
   int n = Lb;

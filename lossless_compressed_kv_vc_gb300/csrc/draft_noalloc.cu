@@ -11,9 +11,11 @@
 // looked up once per device with cudaGetSymbolAddress (on the first call made with that device
 // current) and cached; that first call also zero-fills the array on the caller's stream (the
 // draft kernel's arrival counters start at zero and every call returns them to zero). All calls
-// share the array and it keeps the last call's contents; the draft kernels write every partial
-// before reading it. Calls that overlap on the GPU (different streams, or graph replays running
-// concurrently) race on it.
+// share the array and it keeps the last call's contents. The counters occupy a block at the start
+// whose size and place do not depend on the call's shape, so a call with more KV heads than the
+// one before finds zero counters, not the earlier call's partials; the draft kernels write every
+// partial before reading it. Calls that overlap on the GPU (different streams, or graph replays
+// running concurrently) race on it.
 #include "vc_internal.cuh"
 
 #include <mutex>

@@ -50,8 +50,13 @@ static int draft_ctas_per_head_max(int Hkv, int G = 1) {
   return n > 1 ? n : 1;
 }
 
-// Arrival counters at the start of the draft workspace: one 32-bit word per (KV head, request slot).
-static size_t draft_counter_bytes(int Hkv) { return ((size_t)Hkv * VC_MAX_BATCH * 4 + 255) / 256 * 256; }
+// Arrival counters at the start of the draft workspace: one 32-bit word per (KV head, request slot),
+// in a block of fixed size for up to VC_DRAFT_MAX_KV_HEADS heads. The block does not depend on the
+// call's shape, so the counters of every head sit at the same bytes for every call: a workspace
+// zero-filled once keeps zero counters whatever shapes later calls have (a shape-dependent block
+// would let a call with more KV heads read an earlier call's partials as counters).
+static_assert(VC_DRAFT_COUNTER_BYTES % 256 == 0, "partials start 256-byte aligned");
+static size_t draft_counter_bytes() { return VC_DRAFT_COUNTER_BYTES; }
 
 // Last library operation launched on each stream. A draft step may start streaming before the
 // kernel ahead of it in the stream finishes unless that kernel writes KV_comp (a compress or an
@@ -94,7 +99,7 @@ size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows) 
     // CTA partials: slots (CTA + request) per head, CTAs per head at most one wave plus B
     const size_t G = shape->Hq / shape->Hkv;
     const size_t slots = (size_t)shape->Hkv * (draft_ctas_per_head_max(shape->Hkv) + 2 * shape->B);
-    return draft_counter_bytes(shape->Hkv) + slots * G * (shape->d + 1) * sizeof(float) + 256;
+    return draft_counter_bytes() + slots * G * (shape->d + 1) * sizeof(float) + 256;
   }
   if (call == VC_CALL_VERIFY) return verify_workspace_size(shape, max_rows);
   return 0;
@@ -290,7 +295,7 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
                         int32_t* dev_status, cudaStream_t stream) {
   if (!shape_ok(shape) || !req) return VC_ERR_INVALID;
   const int B = shape->B, d = shape->d, Hkv = shape->Hkv, G = shape->Hq / shape->Hkv;
-  if (G > 16) return VC_ERR_UNSUPPORTED;
+  if (G > 16 || Hkv > VC_DRAFT_MAX_KV_HEADS) return VC_ERR_UNSUPPORTED;
   const int mode = req[0].comp.mode;
   const int bits = req[0].comp.bits;
   if (mode != VC_TOKEN_DROP && mode != VC_QUANT) return VC_ERR_INVALID;
@@ -412,7 +417,7 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   const size_t need = vc_workspace_size(VC_CALL_DRAFT, shape, 0);
   if (!ws || ws_bytes < need || !aligned16(ws)) return VC_ERR_WORKSPACE;
   p.ws_ctr = static_cast<uint32_t*>(ws);
-  p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + draft_counter_bytes(Hkv));
+  p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + draft_counter_bytes());
   p.ws_lse = p.ws_o + (size_t)Hkv * (n_cta + B) * G * d;
   p.early = last_op(stream) != kOpCompress;
   if (launch_draft(p, &maps, d, kind, n_cta, stream) != cudaSuccess) return VC_ERR_CUDA;

@@ -65,6 +65,25 @@ def test_validation_rejects_without_launching(lib):
     assert vc.vc_workspace_size(vc.VC_CALL_DRAFT, ok) > 0
 
 
+def test_draft_counter_block_does_not_depend_on_the_shape(lib):
+    """The draft workspace starts with a fixed block of arrival counters (VC_DRAFT_COUNTER_BYTES,
+    room for VC_DRAFT_MAX_KV_HEADS heads), so a workspace zero-filled once keeps zero counters for
+    calls of any shape: the partials start at the same offset whatever Hkv is, and a workspace's
+    size grows with the partials only."""
+    import lossless_compressed_kv_vc_gb300 as vc
+    hdr = open(os.path.join(ROOT, "include", "vc.h")).read()
+    assert re.search(r"#define VC_DRAFT_MAX_KV_HEADS\s+%d\b" % vc.VC_DRAFT_MAX_KV_HEADS, hdr)
+    assert re.search(r"#define VC_DRAFT_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)32 << 20\)", hdr)
+    assert vc.VC_DRAFT_COUNTER_BYTES == vc.VC_DRAFT_MAX_KV_HEADS * vc.VC_MAX_BATCH * 4
+    for B, Hq, Hkv, d in ((1, 8, 2, 64), (8, 32, 8, 128), (16, 40, 8, 128), (4, 256, 256, 128)):
+        ws = vc.vc_workspace_size(vc.VC_CALL_DRAFT, vc.vc_shape(B, Hq, Hkv, d))
+        assert ws > vc.VC_DRAFT_COUNTER_BYTES
+    # beyond the counter block's heads: refused before anything is launched
+    big = vc.vc_shape(1, 257, 257, 128)
+    req = (vc.vc_draft_req * 1)()
+    assert vc.vc_draft_attn(big, req, stream=0, raise_on_error=False) == vc.VC_ERR_UNSUPPORTED
+
+
 def test_append_validation_rejects_without_launching(lib):
     """vc_append_kv checks capacities before launching; a call with nothing to append launches
     nothing and succeeds. The pointers are fake (aligned, never dereferenced on these paths)."""
