@@ -269,6 +269,79 @@ def test_quantize_dequantize_roundtrip(bits):
     assert np.array_equal(qkv["k_res"], k[:, 32 * ng:])
 
 
+def _grid_cache(bits, H=2, ng=3, d=64, seed=5):
+    """K and V [H][32 ng + 128][d] whose every quantisation group lies on its own grid z + c s, with
+    s and z exact in fp16, distinct per group, and codes 0 and 2^b - 1 both present, so that
+    quantize_kv finds exactly (s, z, c) and the dequantised values equal the inputs bit for bit.
+    Keys group 32 tokens per (block, channel), values 32 channels per token. Returns (k, v, key
+    codes [H][Tq][d], value codes [H][Tq][d])."""
+    rng = np.random.default_rng(seed)
+    qmax = (1 << bits) - 1
+    Tq, ctx = 32 * ng, 32 * ng + 128
+
+    def grid(n_groups):
+        c = rng.integers(0, qmax + 1, size=(n_groups, 32))
+        for g in range(n_groups):
+            a, b = rng.choice(32, size=2, replace=False)
+            c[g, a], c[g, b] = 0, qmax
+        s = rng.integers(1, 64, size=(n_groups, 1)) * 2.0 ** -6    # 1/64 .. 63/64, exact in fp16
+        z = rng.integers(-256, 256, size=(n_groups, 1)) * 2.0 ** -7  # exact in fp16
+        return c, (z + c * s).astype(np.float32)
+
+    kc, kx = grid(H * ng * d)                      # groups (h, block, channel) x 32 tokens
+    k = np.zeros((H, ctx, d), np.float32)
+    k[:, :Tq] = kx.reshape(H, ng, d, 32).transpose(0, 1, 3, 2).reshape(H, Tq, d)
+    vc, vx = grid(H * Tq * (d // 32))              # groups (h, token, channel group) x 32 channels
+    v = np.zeros((H, ctx, d), np.float32)
+    v[:, :Tq] = vx.reshape(H, Tq, d)
+    k[:, Tq:] = rng.standard_normal((H, 128, d)).astype(np.float32)
+    v[:, Tq:] = rng.standard_normal((H, 128, d)).astype(np.float32)
+    kcodes = kc.reshape(H, ng, d, 32).transpose(0, 1, 3, 2).reshape(H, Tq, d)
+    return k, v, kcodes, vc.reshape(H, Tq, d)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_dequantize_exact_on_grid(bits):
+    """Groups on an exact grid come back bit for bit through quantize_kv -> dequantize_kv (every
+    code, scale and zero is exact, so x_hat = c s + z reproduces x). Catches a dequantiser that adds
+    half a step, swaps the scale and zero of neighbouring groups, or reads the words in another
+    order: every group has its own s and z, and codes 0 and 2^b - 1 both occur."""
+    k, v, kcodes, vcodes = _grid_cache(bits)
+    qkv = O.quantize_kv(k, v, bits)
+    ng, Tq = qkv["ng"], 32 * qkv["ng"]
+    assert ng == 3
+    assert np.array_equal(O.unpack_block(qkv["kc"], bits, "k", 64).reshape(2, Tq, 64), kcodes)
+    assert np.array_equal(O.unpack_block(qkv["vc"], bits, "v", 64).reshape(2, Tq, 64), vcodes)
+    kh, vh = O.dequantize_kv(qkv, 64)
+    assert kh.dtype == np.float32 and vh.dtype == np.float32
+    assert np.array_equal(kh, k[:, :Tq]) and np.array_equal(vh, v[:, :Tq])
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_dequantize_error_bound(bits):
+    """|x - dequantize_kv(quantize_kv(x))| <= s/2 plus the fp16 rounding of s and z, computed
+    through dequantize_kv itself, with each element's own group scale: key (h, block, channel),
+    value (h, token, channel group). A half-step offset breaks the bound on about half the
+    elements."""
+    rng = np.random.default_rng(31 + bits)
+    H, d, ng = 2, 64, 5
+    ctx = 32 * ng + 128
+    k = (rng.standard_normal((H, ctx, d)) * rng.uniform(0.05, 8, size=(H, 1, d))).astype(np.float32)
+    v = (rng.standard_normal((H, ctx, d)) * rng.uniform(0.05, 8, size=(H, ctx, 1))).astype(np.float32)
+    qkv = O.quantize_kv(k, v, bits)
+    kh, vh = O.dequantize_kv(qkv, d)
+    Tq, qmax = 32 * ng, (1 << bits) - 1
+    ks = np.repeat(qkv["ks"].astype(np.float32), 32, axis=1)          # [H][Tq][d]: block of the token
+    kz = np.repeat(qkv["kz"].astype(np.float32), 32, axis=1)
+    vs = np.repeat(qkv["vs"].astype(np.float32), 32, axis=2)          # [H][Tq][d]: group of the channel
+    vz = np.repeat(qkv["vz"].astype(np.float32), 32, axis=2)
+    for x, xh, s, z in ((k[:, :Tq], kh, ks, kz), (v[:, :Tq], vh, vs, vz)):
+        bound = s / 2 + np.abs(z) * 2.0 ** -11 + qmax * s * 2.0 ** -11 + np.abs(x) * 2.0 ** -20
+        assert np.all(np.abs(x - xh) <= bound * (1 + 1e-6))
+        # and the bound is not loose: some element sits near half a step from its value
+        assert np.max(np.abs(x - xh) / s) > 0.4
+
+
 # ---------------------------------------------------------------- accept -----------------------
 def test_accept_golden(golden_dir):
     cs = json.load(open(os.path.join(golden_dir, "accept_cases.json")))["cases"]
