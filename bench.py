@@ -20,7 +20,6 @@ import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -31,7 +30,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verified tokens/s/GPU (draft+verify+accept)"
 UNIT = "tokens/s"
-PROFILE = os.path.join(ROOT, "profiles", "draft_attn_llama8b_drop4x.md")
+TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 DRAFT_SOURCES = ["lossless_compressed_kv_vc_gb300/csrc/draft.cu", "lossless_compressed_kv_vc_gb300/csrc/vc_internal.cuh"]
 
 
@@ -43,18 +42,21 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--sample-heads", type=int, default=1, help=argparse.SUPPRESS)
-    ap.add_argument("--child-steps", type=int, default=1, help=argparse.SUPPRESS)
-    ap.add_argument("--workload", default="llama8b_drop",
-                    choices=["llama8b_drop", "qwen_quant2", "offload", "stagger", "importance"],
-                    help="llama8b_drop: the headline round; qwen_quant2: the same round on the Qwen-32B-like "
+    ap.add_argument("--workload", default="mixed",
+                    choices=["mixed", "llama8b_drop", "qwen_quant2", "offload", "stagger", "importance"],
+                    help="mixed (default): the mixed staggered serving batch, 32 requests of 8K-256K tokens, half "
+                         "token drop and half 2-bit, half with KV_full in pinned host memory, two groups planned by "
+                         "the staggering planner; llama8b_drop: the Llama-3-8B-shape drop-4x round; "
+                         "qwen_quant2: the same round on the Qwen-32B-like "
                          "2-bit workload (16 x 65536 tokens, L 25); offload: Llama-70B-shape 4-bit requests with KV_full "
                          "in pinned host memory, two drafting while two stage and verify; stagger: the 16 "
                          "2-bit requests of the mixed serving workload (half with KV_full on the host) under "
                          "a naive split and under the planner's split; importance: SnapKV-style importance of the "
                          "headline workload's contexts from a 32-token observation window")
     ap.add_argument("--window", type=int, default=32, help="importance workload: observation window")
+    ap.add_argument("--timeline", default=None,
+                    help="mixed workload: write the first periods' CUDA-event intervals (draft calls, verification, "
+                         "staging copies; ms from the start of the timed region) to this JSON file")
     ap.add_argument("--ctx-div", type=int, default=1,
                     help="offload workload: divide the context (a smaller case for profiler captures)")
     ap.add_argument("--compact", action="store_true",
@@ -75,111 +77,199 @@ def parse():
 
 
 _BATCH = None
-_WORKLOAD = "llama8b_drop"
+_WORKLOAD = "mixed"
 
 
 def workload():
     from workloads import configs
-    w = configs.qwen32b_quant2() if _WORKLOAD == "qwen_quant2" else configs.llama8b_drop()
+    if _WORKLOAD == "mixed":
+        w = configs.mixed_serving()
+    else:
+        w = configs.qwen32b_quant2() if _WORKLOAD == "qwen_quant2" else configs.llama8b_drop()
     if _BATCH is not None and _BATCH < w.B:
         w = configs.scaled(w, batch=_BATCH)
     return w
 
 
 # ------------------------------------------------------------------------------------------------
-# CPU oracle leg (reference arm and cpu_baseline): one request's round on a sample of KV heads
+# CPU oracle legs (reference arm and cpu_baseline)
 # ------------------------------------------------------------------------------------------------
-def oracle_inputs(w, b: int):
-    """Request b's round inputs as float32 numpy arrays (generated once per child process)."""
-    import torch
-    from workloads import gen
-    ri = gen.request(w, 0, b, "cpu")
-    draft, logits, L = gen.drafts_and_logits(w, 0, "cpu")
-    f = lambda t: t.to(torch.float32).numpy()
-    return (f(ri.k_full), f(ri.v_full), f(ri.q), f(ri.k_new), f(ri.v_new), ri.importance.numpy(),
-            logits[b].numpy(), draft[b].numpy())
+# The oracle runs on the host cores as a fixed pool of worker processes (spawn context: the parent
+# may hold a CUDA context). One "wave" is one request of the workload: its query heads are split
+# evenly over the workers (consecutive heads, so a worker's heads share KV heads), every worker
+# prepares its inputs, all meet at a barrier, the parent starts its clock, the workers run the
+# oracle's round for their heads (all draft steps, verification, and -- worker 0 -- accept), all meet
+# at a second barrier and the clock stops. So a wave's time is the measured wall time of the
+# round's arithmetic on all workers at once. Preparation (input generation, the keep-set and the
+# quantisation of KV_comp, which the GPU round also does once per request, outside the round) is
+# outside the clock. The credited tokens of a wave are the request's accepted tokens.
 
-
-def oracle_round_sample(w, b: int, n_heads: int, inputs=None):
-    """Time the oracle on request b: keep-set, L draft steps and verify for `n_heads` KV heads,
-    accept. Returns (seconds scaled to all KV heads of the request, n_acc)."""
+def _oracle_worker(wid, nworkers, task_q, result_q, barrier):
+    import os as _os
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        _os.environ[k] = "1"
     import numpy as np
+    import torch
+    torch.set_num_threads(1)
     import oracle as O
-    kf, vf, q, kn, vn, imp, lg, dr = inputs if inputs is not None else oracle_inputs(w, b)
-    G = w.Hq // w.Hkv
-    t0 = time.perf_counter()
-    idx = O.keep_set(imp, w.keep[b], w.recent[b])
-    t_keep = time.perf_counter() - t0
-    t1 = time.perf_counter()
-    for hk in range(n_heads):
-        sel = slice(hk * G, (hk + 1) * G)
-        km, vm = kf[hk:hk + 1, idx], vf[hk:hk + 1, idx]
-        empty = np.zeros((1, 0, w.d), np.float32)
-        O.draft_round(q[:, sel], km, vm, empty, empty, kn[:, hk:hk + 1], vn[:, hk:hk + 1])
-        O.verify_attn(q[:, sel], kf[hk:hk + 1], vf[hk:hk + 1], kn[:, hk:hk + 1].transpose(1, 0, 2),
-                      vn[:, hk:hk + 1].transpose(1, 0, 2))
-    t_heads = time.perf_counter() - t1
-    t2 = time.perf_counter()
-    _, n_acc = O.accept(lg, dr, w.L[b])
-    t_acc = time.perf_counter() - t2
-    return t_keep + t_heads * (w.Hkv / n_heads) + t_acc, n_acc
+    from workloads import gen, DROP
+    while True:
+        task = task_q.get()
+        if task is None:
+            return
+        w, b = task
+        err, secs, n_acc = None, 0.0, 0
+        try:
+            G = w.Hq // w.Hkv
+            h0, h1 = wid * w.Hq // nworkers, (wid + 1) * w.Hq // nworkers
+            f = lambda t: t.to(torch.float32).numpy()
+            k, v = gen.full_kv(w, b)
+            q, kn, vn = gen.round_queries(w, 0, b)
+            q, kn, vn = f(q), f(kn), f(vn)
+            prep = []
+            for j in sorted({h // G for h in range(h0, h1)}):
+                kf, vf = f(k[j:j + 1]), f(v[j:j + 1])
+                if w.mode[b] == DROP:
+                    idx = O.keep_set(gen.importance(w, b).numpy(), w.keep[b], w.recent[b])
+                    km, vm = O.comp_main_rows("drop", kf, vf, idx=idx)
+                    kw0 = vw0 = np.zeros((1, 0, w.d), np.float32)
+                else:
+                    qkv = O.quantize_kv(kf, vf, w.bits, w.residual_min)
+                    km, vm = O.comp_main_rows("quant", kf, vf, qkv=qkv)
+                    kw0, vw0 = qkv["k_res"], qkv["v_res"]
+                sel = [h for h in range(h0, h1) if h // G == j]
+                prep.append((sel, kf, vf, km, vm, kw0, vw0, kn[:, j:j + 1], vn[:, j:j + 1]))
+            del k, v
+            dr, lg = gen.request_logits(w, 0, b) if wid == 0 else (None, None)
+        except Exception as e:  # still meet the barriers, report the error
+            err, prep = repr(e), []
+        barrier.wait()
+        t0 = time.perf_counter()
+        try:
+            for sel, kf, vf, km, vm, kw0, vw0, knj, vnj in prep:
+                qs = q[:, sel]
+                O.draft_round(qs, km, vm, kw0, vw0, knj, vnj)
+                O.verify_attn(qs, kf, vf, knj.transpose(1, 0, 2), vnj.transpose(1, 0, 2))
+            if wid == 0 and err is None:
+                n_acc = O.accept(lg.numpy(), dr.numpy(), w.L[b])[1]
+        except Exception as e:
+            err = repr(e)
+        secs = time.perf_counter() - t0
+        barrier.wait()
+        result_q.put((wid, err, secs, n_acc))
 
 
-def cpu_child(args):
-    """Runs in a fresh single-threaded process (BLAS threads pinned to 1 by the parent): oracle
-    samples of request (i mod B) for i < child_steps, each on `sample_heads` KV heads; prints one
-    JSON list of {secs_per_request, n_acc}."""
-    w = workload()
-    out, cache = [], {}
-    for i in range(args.child_steps):
-        b = i % w.B
-        if b not in cache:
-            cache[b] = oracle_inputs(w, b)
-        secs, n_acc = oracle_round_sample(w, b, args.sample_heads, cache[b])
-        out.append({"secs_per_request": secs, "n_acc": n_acc})
-    print(json.dumps(out))
+class OraclePool:
+    """Worker processes that run the oracle's round of one request per wave (see above)."""
+
+    def __init__(self, workers=None):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.n = workers or (os.cpu_count() or 1)
+        self.barrier = ctx.Barrier(self.n + 1)
+        self.result_q = ctx.Queue()
+        self.task_q = [ctx.Queue() for _ in range(self.n)]
+        env_keep = {k: os.environ.get(k) for k in ("CUDA_VISIBLE_DEVICES",)}
+        os.environ["CUDA_VISIBLE_DEVICES"] = ""  # the workers never touch a GPU
+        try:
+            self.procs = [ctx.Process(target=_oracle_worker, args=(i, self.n, self.task_q[i], self.result_q,
+                                                                   self.barrier), daemon=True)
+                          for i in range(self.n)]
+            for p in self.procs:
+                p.start()
+        finally:
+            for k, v in env_keep.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def wave(self, w, b, timeout=1800):
+        """Run request b's round on all workers; returns (wall seconds of the compute, summed
+        worker seconds, accepted tokens)."""
+        for q in self.task_q:
+            q.put((w, b))
+        self.barrier.wait(timeout)
+        t0 = time.perf_counter()
+        self.barrier.wait(timeout)
+        wall = time.perf_counter() - t0
+        res = [self.result_q.get(timeout=timeout) for _ in range(self.n)]
+        errs = [e for _, e, _, _ in res if e]
+        if errs:
+            raise RuntimeError("oracle worker failed: " + errs[0])
+        return wall, sum(r[2] for r in res), sum(r[3] for r in res)
+
+    def close(self):
+        for q in self.task_q:
+            q.put(None)
+        for p in self.procs:
+            p.join(timeout=30)
 
 
-def run_cpu_child(sample_heads=1, steps=1):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    t0 = time.perf_counter()
-    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", "--sample-heads",
-                          str(sample_heads), "--child-steps", str(steps)], capture_output=True, text=True, env=env,
-                         cwd=ROOT)
-    wall = time.perf_counter() - t0
-    if out.returncode != 0:
-        raise RuntimeError(out.stderr[-2000:])
-    return json.loads(out.stdout.strip().splitlines()[-1]), wall
+def sample_requests(w, per_mode=1):
+    """Requests of each compression mode whose contexts are nearest the mode's median (the
+    cpu_baseline's bounded sample)."""
+    import numpy as np
+    out = []
+    for m in sorted(set(w.mode)):
+        idx = [b for b in range(w.B) if w.mode[b] == m]
+        med = float(np.median([w.ctx[b] for b in idx]))
+        out += sorted(idx, key=lambda b: (abs(w.ctx[b] - med), b))[:per_mode]
+    return sorted(out)
 
 
-def cpu_baseline_obj(w, rs):
-    """The oracle over one whole round: every request, every KV head (no scaling)."""
-    secs = sum(r["secs_per_request"] for r in rs)
-    n_acc = sum(r["n_acc"] for r in rs)
-    return {"value": n_acc / secs, "unit": UNIT, "cores": 1, "kind": "oracle", "cpu_s": secs,
-            "sample": f"one whole round of {w.name}: {w.B} requests x {w.Hkv} KV heads, keep-set, {w.L[0]} draft "
-                      f"steps, verify and accept; numpy float64, one thread"}
+def cpu_baseline_oracle(w):
+    """The oracle on all host cores over a bounded sample: one round of each sampled request."""
+    pool = OraclePool()
+    try:
+        reqs = sample_requests(w)
+        walls, cpu, tok = 0.0, 0.0, 0
+        for b in reqs:
+            wall, c, n = pool.wave(w, b)
+            walls, cpu, tok = walls + wall, cpu + c, tok + n
+    finally:
+        pool.close()
+    return {"value": tok / walls, "unit": UNIT, "cores": pool.n, "host_cores": os.cpu_count(), "kind": "oracle",
+            "single_thread_value": tok / cpu, "wall_s": walls, "cpu_s": cpu,
+            "sample": "one round (all draft steps, verification and accept, every query head) of requests %s of %s "
+                      "(the requests of each compression mode whose contexts are nearest the mode's median: %s "
+                      "tokens), split over %d worker processes of one thread each; value = their accepted tokens / "
+                      "the measured wall time of the arithmetic (KV_comp built beforehand, as on the GPU); "
+                      "single_thread_value = the same tokens / the workers' summed seconds"
+                      % (reqs, w.name, [w.ctx[b] for b in reqs], pool.n)}
 
 
 def run_reference(args):
+    """The oracle as the reference arm: one wave (one request's whole round on all host cores) per
+    step, cycling through the workload's requests; value = accepted tokens of the timed waves / their
+    measured wall time, ms_per_step = the mean wave wall time."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     w = workload()
-    # one single-threaded child runs every step: step i samples request (i mod B) on one KV head
-    # (time x Hkv), so a step is ~0.1 s of oracle work and the whole run a few minutes at most
-    rs, _ = run_cpu_child(1, args.warmup + args.steps)
-    timed = rs[args.warmup:]
-    t = statistics.mean(r["secs_per_request"] for r in timed)
-    value = sum(r["n_acc"] for r in timed) / sum(r["secs_per_request"] for r in timed)
+    order = list(range(w.B))
+    pool = OraclePool()
+    walls, toks, cpu = [], [], 0.0
+    try:
+        for i in range(args.warmup + args.steps):
+            wall, c, n = pool.wave(w, order[i % w.B])
+            if i >= args.warmup:
+                walls.append(wall)
+                toks.append(n)
+                cpu += c
+    finally:
+        pool.close()
+    value = sum(toks) / sum(walls)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 * w.B,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(walls) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"per step: request (step mod {w.B}) of {w.name}, 1 of {w.Hkv} KV heads "
-                                       f"timed, x{w.Hkv}; ms_per_step is per round of {w.B} requests"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.n, "host_cores": os.cpu_count(),
+                             "kind": "oracle", "single_thread_value": sum(toks) / cpu,
+                             "sample": "per step: the whole round of one request of %s (requests in order, "
+                                       "cycling), its query heads split over %d single-thread worker processes; "
+                                       "the step time is the measured wall time of that arithmetic"
+                                       % (w.name, pool.n)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -253,18 +343,18 @@ def draft_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """Per-launch DRAM bytes of the draft kernel from the committed ncu summary, or None when the
-    kernel source changed since it was taken."""
+def profiled_traffic(kernel, workload_name):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of `kernel` on
+    `workload_name` from profiles/traffic.json (written from an ncu capture), or None when there is
+    no entry or the draft kernel's source changed since the capture."""
     try:
-        txt = open(PROFILE).read()
-    except OSError:
+        entries = json.load(open(TRAFFIC))["entries"]
+    except (OSError, ValueError, KeyError):
         return None
-    m = re.search(r"traffic_bytes_per_launch\s*=\s*([0-9.eE+]+)", txt)
-    h = re.search(r"kernel_source_sha256_16\s*=\s*([0-9a-f]+)", txt)
-    if not m or not h or h.group(1) != draft_source_hash():
-        return None
-    return float(m.group(1))
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload_name:
+            return float(e["bytes_per_launch"]) if e.get("source_sha16") == draft_source_hash() else None
+    return None
 
 
 def draft_algorithmic_bytes(w):
@@ -379,7 +469,8 @@ def run_native(args):
     d_ms = statistics.mean(draft_ms)
     achieved = alg / (d_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                "frac": achieved / float(peaks["hbm_gbs"]), "traffic": profiled_traffic(),
+                "frac": achieved / float(peaks["hbm_gbs"]),
+                "traffic": profiled_traffic("draft_attn_kernel<128,%d,1>" % (0 if quant == 0 else w.bits), w.name),
                 "kernel": "draft_attn_kernel<128,%d,1> (one vc_draft_attn call, partial merge included; mean over "
                           "the draft phase of each timed round)" % (0 if quant == 0 else w.bits),
                 "algorithmic_bytes_per_launch": alg, "avg_launch_ms": d_ms, "peak_kind": peak_kind}
@@ -399,15 +490,284 @@ def run_native(args):
     if quant:
         line["config"].update({"bits": w.bits, "keep": None, "recent": None})
         line["roofline"]["traffic"] = None
-    if rank == 0 and not args.no_cpu_baseline and not quant:
-        rs, wall = run_cpu_child(w.Hkv, w.B)
-        cb = cpu_baseline_obj(w, rs)
-        cb["wall_s"] = wall
-        line["cpu_baseline"] = cb
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_oracle(w)
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------
+# mixed staggered serving batch (the default workload)
+# ------------------------------------------------------------------------------------------------
+def request_step_bytes(w, b, s, sz):
+    """Algorithmic bytes of request b's draft step s: its KV_comp (kept K and V rows and the index
+    list, or the quantised codes, fp16 scales and zeros), the window rows it reads (residual, the
+    drafted rows so far and this step's own), q in, o out, and the new K/V row read and stored.
+    sz: the request's vc_comp_bytes."""
+    from workloads import DROP
+    d, H = w.d, w.Hkv
+    if w.mode[b] == DROP:
+        main = H * sz.keep * 2 * d * 2 + sz.keep * 4
+        win = s + 1
+    else:
+        ng = sz.ng
+        main = H * 32 * ng * (2 * d * w.bits // 8) + H * ng * 2 * 2 * d + H * 32 * ng * 2 * 2 * (d // 32)
+        win = sz.n_res + s + 1
+    return main + H * win * 2 * d * 2 + 2 * w.Hq * d * 2 + 2 * 2 * H * d * 2
+
+
+def request_verify_work(w, b):
+    """(bytes, flops) of request b's verification: KV_full and the drafted rows read once per KV
+    head, q in and o out; QK^T and PV over ctx + (i + 1) keys for draft row i."""
+    d, H, G, L, ctx = w.d, w.Hkv, w.Hq // w.Hkv, w.L[b], w.ctx[b]
+    byts = H * (ctx + L) * 2 * d * 2 + 2 * L * w.Hq * d * 2
+    flops = 4 * d * G * H * (L * ctx + L * (L + 1) // 2)
+    return byts, flops
+
+
+def _covered(iv, cover):
+    """Fraction of interval iv = (a, b) inside the union of the intervals `cover`."""
+    a, b = iv
+    pts = sorted((max(a, c0), min(b, c1)) for c0, c1 in cover if min(b, c1) > max(a, c0))
+    tot, end = 0.0, a
+    for c0, c1 in pts:
+        if c1 > end:
+            tot += c1 - max(c0, end)
+            end = c1
+    return tot / max(1e-12, b - a)
+
+
+def run_mixed(args):
+    """The mixed staggered serving batch: 32 requests, contexts log-uniform in 8K-256K, half token
+    drop 4x (even requests) and half 2-bit (odd), KV_full of half of them in pinned host memory, L
+    uniform in 25-40. KV_comp is built once per request (outside the timed region). A step is one
+    period of cross-resource staggering over two groups chosen by the staggering planner from costs
+    measured on the workload: group A drafts (one C-ABI call per compression mode per draft step)
+    while group B's host-resident KV_full is staged over the host link, then B is verified and
+    accepted; then the roles swap. Every request drafts its L steps, is staged if its KV_full is on
+    the host, verified and accepted once per step."""
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from lossless_compressed_kv_vc_gb300 import (engine, VC_TOKEN_DROP, VC_QUANT, vc_draft_attn, vc_verify_attn,
+                                                 vc_stage_full_kv, vc_comp_bytes, vc_shape, vc_stagger_period)
+    from workloads import configs, gen, DROP
+    w = configs.mixed_serving()
+    if args.ctx_div > 1:
+        w = configs.scaled(w, ctx_div=args.ctx_div)
+    if args.batch is not None and args.batch < w.B:
+        w = configs.subset(w, list(range(args.batch)))
+    dev = "cuda"
+    torch.cuda.set_device(0)
+    B, d = w.B, w.d
+    sizes = [vc_comp_bytes(vc_shape(1, w.Hq, w.Hkv, d), VC_TOKEN_DROP if w.mode[b] == DROP else VC_QUANT, w.bits,
+                           w.ctx[b], w.ctx[b], w.keep[b], w.residual_min, w.L[b]) for b in range(B)]
+    reqs = []
+    for b in range(B):
+        ri = gen.request(w, 0, b, dev)
+        drop = w.mode[b] == DROP
+        reqs.append(engine.Req(mode=VC_TOKEN_DROP if drop else VC_QUANT, ctx=w.ctx[b], L=w.L[b], k_full=ri.k_full,
+                               v_full=ri.v_full, q=ri.q, k_new=ri.k_new, v_new=ri.v_new,
+                               importance=ri.importance if drop else None, keep=w.keep[b], recent=w.recent[b],
+                               compact=bool(drop and w.on_host[b]), bits=w.bits))
+    del ri
+    draft_b = [sum(request_step_bytes(w, b, s, sizes[b]) for s in range(w.L[b])) for b in range(B)]
+    verify_b = [request_verify_work(w, b) for b in range(B)]
+    full_b = [2 * w.Hkv * w.ctx[b] * d * 2 for b in range(B)]
+    cs, ks = torch.cuda.Stream(), torch.cuda.Stream()
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+    def timed(fn, stream, reps=2):
+        best = float("inf")
+        for _ in range(reps + 1):
+            e = mk()
+            torch.cuda.synchronize()
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            best = min(best, e[0].elapsed_time(e[1]))
+        return best * 1e6  # ns
+
+    # --- costs for the planner: rates measured on the workload itself (each mode's whole draft
+    # phase, the whole verification, one host-resident request's copy alone) times each request's bytes
+    modes = [m for m in (DROP, "quant") if m in w.mode]
+    rate = {}
+    ver_ns, ver_bytes = 0.0, 0
+    for m in modes:
+        idx = [b for b in range(B) if w.mode[b] == m]
+        cal = engine.Batch(w.Hq, w.Hkv, d, [reqs[b] for b in idx], residual_min=w.residual_min, device=dev)
+        cal.compress(ks)
+        cal.prepare_steps()
+        t = timed(lambda: [vc_draft_attn(sh, arr, cal.ws_draft, cal.dev_status, ks) for sh, arr, act in cal._steps], ks)
+        rate[m] = sum(draft_b[b] for b in idx) / t
+        ver_ns += timed(lambda: vc_verify_attn(cal.shape, cal._verify_arr, cal.ws_verify, cal.dev_status, ks), ks)
+        ver_bytes += sum(verify_b[b][0] for b in idx)
+        assert int(cal.dev_status.item()) == 0
+        del cal
+    rate_v = ver_bytes / ver_ns
+    host_reqs = [b for b in range(B) if w.on_host[b]]
+    rate_s, link_alone = None, None
+    if host_reqs:
+        hb = min(host_reqs, key=lambda b: abs(w.ctx[b] - sorted(w.ctx)[B // 2]))
+        src = torch.empty((full_b[hb] // 2,), dtype=torch.bfloat16, pin_memory=True)
+        dst = torch.empty((full_b[hb] // 2,), dtype=torch.bfloat16, device=dev)
+        t = timed(lambda: vc_stage_full_kv(src, dst, full_b[hb], 64 << 20, cs, None), cs)
+        rate_s = full_b[hb] / t
+        link_alone = rate_s
+        del src, dst
+    costs = engine.stagger_costs([draft_b[b] / rate[w.mode[b]] for b in range(B)],
+                                 [verify_b[b][0] / rate_v for b in range(B)],
+                                 [full_b[b] / rate_s if w.on_host[b] else 0 for b in range(B)])
+    g0, g1, t_plan = engine.plan_groups(costs)
+    split = [0 if b in g0 else 1 for b in range(B)]
+
+    # --- the two groups, one batch per compression mode in each; KV_comp built once
+    draft, logits, Lt = gen.drafts_and_logits(w, 0, dev)
+    groups, members, host_kv, slots = engine.staggered_groups(w.Hq, w.Hkv, d, reqs, split, w.on_host,
+                                                              w.residual_min, dev, ks)
+    io = engine.group_io(members, logits, draft, Lt)
+    torch.cuda.synchronize()
+    sg = engine.StaggeredOffload(groups, host_kv, slots, cs, ks, head_chunks=args.head_chunks)
+    for _ in range(args.warmup):
+        sg.period(io)
+    torch.cuda.synchronize()
+    for bts in groups:
+        for bt in bts:
+            assert int(bt.dev_status.item()) == 0, "device status set during warm-up"
+    tokens = sum(int(t[4].sum().item()) for gi in (0, 1) for t in io[gi])
+
+    evs = []
+    for _ in range(args.steps):
+        ev = {"draft%d" % gi: [mk() for _ in groups[gi]] for gi in (0, 1)}
+        ev.update({k: mk() for k in ("stage0", "stage1", "verify0", "verify1")})
+        evs.append(ev)
+    e0, e1 = mk()
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        e0.record(ks)
+        cs.wait_event(e0)
+        for k in range(args.steps):
+            sg.period(io, evs[k])
+        e1.record(ks)
+        torch.cuda.synchronize()
+    t_ms = e0.elapsed_time(e1)
+    for bts in groups:
+        for bt in bts:
+            assert int(bt.dev_status.item()) == 0, "device status set during the timed region"
+    value = tokens * args.steps / (t_ms / 1e3)
+
+    # --- per-kernel time from the events (each interval on the stream that ran it)
+    rel = lambda e: e0.elapsed_time(e)
+    kind_ms = {m: 0.0 for m in modes}
+    kind_launch = {m: 0 for m in modes}
+    kind_bytes = {m: 0.0 for m in modes}
+    comp_iv, copy_iv = [], []
+    for ev in evs:
+        for gi in (0, 1):
+            for (a, b_), bt, idx in zip(ev["draft%d" % gi], groups[gi], members[gi]):
+                m = w.mode[idx[0]]
+                kind_ms[m] += a.elapsed_time(b_)
+                kind_launch[m] += len(bt._steps)
+                kind_bytes[m] += sum(draft_b[b] for b in idx)
+                comp_iv.append((rel(a), rel(b_)))
+            a, b_ = ev["verify%d" % gi]
+            comp_iv.append((rel(a), rel(b_)))
+            a, b_ = ev["stage%d" % gi]
+            if sg.stage_bytes(gi):
+                copy_iv.append((rel(a), rel(b_)))
+    ver_ms = sum(ev["verify%d" % gi][0].elapsed_time(ev["verify%d" % gi][1]) for ev in evs for gi in (0, 1))
+    stage_ms = sum(b_ - a for a, b_ in copy_iv)
+    peaks, peak_kind = measured_peaks()
+    hbm, bf16 = float(peaks["hbm_gbs"]), float(peaks["bf16_tflops_sustained"])
+    ver_bytes_p = sum(v[0] for v in verify_b)
+    ver_flops_p = sum(v[1] for v in verify_b)
+    ver_tflops = ver_flops_p * args.steps / (ver_ms / 1e3) / 1e12
+    stage_bytes_p = sum(sg.stage_bytes(gi) for gi in (0, 1))
+    dom = max(kind_ms, key=kind_ms.get)
+    dom_ms = kind_ms[dom] / kind_launch[dom]
+    dom_alg = kind_bytes[dom] / kind_launch[dom]
+    achieved = dom_alg / (dom_ms / 1e3) / 1e9
+    kname = "draft_attn_kernel<128,%s,1>" % ("0" if dom == DROP else str(w.bits))
+    total_kernel_ms = sum(kind_ms.values()) + ver_ms
+    launches = sum(len(bt._steps) + 2 * args.head_chunks + 2 for bts in groups for bt in bts)
+    overlap = statistics.mean(_covered(iv, comp_iv) for iv in copy_iv) if copy_iv else None
+    if args.timeline:
+        tl = [{"period": k, "draft": [[rel(a), rel(b_)] for gi in (0, 1) for a, b_ in evs[k]["draft%d" % gi]],
+               "verify": [[rel(evs[k]["verify%d" % gi][0]), rel(evs[k]["verify%d" % gi][1])] for gi in (0, 1)],
+               "stage": [[rel(evs[k]["stage%d" % gi][0]), rel(evs[k]["stage%d" % gi][1])] for gi in (0, 1)]}
+              for k in range(min(3, args.steps))]
+        json.dump({"t_ms": t_ms, "steps": args.steps, "periods": tl}, open(args.timeline, "w"))
+
+    # --- end to end through the engine's host-input period: every period copies each batch's
+    # queries and drafted K/V rows, drafts, logits and L from pinned host memory and returns the
+    # accepted tokens and counts to pinned host memory, besides staging the host-resident KV_full
+    hrs = [[engine.HostRound(bt, *io[gi][j], names=("q", "k_new", "v_new")) for j, bt in enumerate(groups[gi])]
+           for gi in (0, 1)]
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))
+    for _ in range(2):
+        sg.period(None, host_rounds=hrs)
+    torch.cuda.synchronize()
+    f0, f1 = mk()
+    torch.cuda.synchronize()
+    f0.record(ks)
+    cs.wait_event(f0)
+    for _ in range(e2e_steps):
+        sg.period(None, host_rounds=hrs)
+    f1.record(ks)
+    torch.cuda.synchronize()
+    e2e_tokens = sum(int(hr.host_n_acc.sum().item()) for gi in (0, 1) for hr in hrs[gi])
+    assert e2e_tokens == tokens, (e2e_tokens, tokens)
+    h2d = stage_bytes_p + sum(hr.h2d_bytes for gi in (0, 1) for hr in hrs[gi])
+    d2h = sum(hr.d2h_bytes for gi in (0, 1) for hr in hrs[gi])
+    e2e = {"value": tokens * e2e_steps / (f0.elapsed_time(f1) / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "path": "engine.StaggeredOffload.period(host_rounds=...): round inputs from pinned host memory, "
+                   "host-resident KV_full staged, accepted tokens and counts back to pinned host memory"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "Hq": w.Hq, "Hkv": w.Hkv, "d": d,
+                       "ctx_min": min(w.ctx), "ctx_max": max(w.ctx), "ctx_mean": sum(w.ctx) / B,
+                       "L_min": min(w.L), "L_max": w.L_max, "V": w.V, "bits": w.bits,
+                       "requests_token_drop": sum(m == DROP for m in w.mode), "requests_on_host": sum(w.on_host),
+                       "tokens_per_step": tokens, "groups": split, "head_chunks": args.head_chunks,
+                       "step": "one staggering period: every request drafts its L steps (one draft call per mode "
+                               "and step), host-resident KV_full is staged, every request is verified and accepted",
+                       "l2": "inputs larger than L2 (full KV %.1f GB, per draft step up to %.2f GB of KV_comp, logits "
+                             "%.2f GB)" % (sum(full_b) / 1e9, max(kind_bytes[m] / kind_launch[m] for m in modes) / 1e9 * 1,
+                                            logits.numel() * 4 / 1e9)},
+            "e2e": e2e, "gpu_launches": launches * args.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": profiled_traffic(kname, w.name),
+                         "kernel": kname + " (the largest GPU-time share of the period: one vc_draft_attn call; "
+                                           "mean over every draft call of its mode in the timed periods)",
+                         "algorithmic_bytes_per_launch": dom_alg, "avg_launch_ms": dom_ms, "peak_kind": peak_kind,
+                         "share_of_kernel_time": kind_ms[dom] / total_kernel_ms},
+            "kernels": {**{"draft_" + m: {"ms_per_step": kind_ms[m] / args.steps, "launches_per_step":
+                                          kind_launch[m] // args.steps,
+                                          "gbs": kind_bytes[m] / (kind_ms[m] / 1e3) / 1e9,
+                                          "frac_of_hbm": kind_bytes[m] / (kind_ms[m] / 1e3) / 1e9 / hbm}
+                           for m in modes},
+                        "verify": {"ms_per_step": ver_ms / args.steps, "gbs": ver_bytes_p * args.steps / (ver_ms / 1e3) / 1e9,
+                                   "frac_of_hbm": ver_bytes_p * args.steps / (ver_ms / 1e3) / 1e9 / hbm,
+                                   "tflops": ver_tflops, "tensor_frac_of_bf16_sustained": ver_tflops / bf16,
+                                   "flops_per_step": ver_flops_p}},
+            "stage": {"bytes_per_step": stage_bytes_p, "gbs": stage_bytes_p * args.steps / (stage_ms / 1e3) / 1e9
+                      if stage_ms else None, "link_alone_gbs": link_alone,
+                      "frac_of_link": (stage_bytes_p * args.steps / (stage_ms / 1e3) / 1e9) / link_alone
+                      if stage_ms and link_alone else None,
+                      "copy_time_under_compute": overlap, "copy_ms_per_step": stage_ms / args.steps},
+            "plan": {"modelled_period_ms": t_plan / 1e6, "rates_gbs": {**{"draft_" + m: rate[m] for m in modes},
+                                                                     "verify": rate_v, "link": rate_s}},
+            "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_oracle(w)
+    print(json.dumps(line))
     return 0
 
 
@@ -722,8 +1082,6 @@ def run_importance(args):
 
 def main():
     args = parse()
-    if args.cpu_child:
-        return cpu_child(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "offload":
@@ -732,6 +1090,8 @@ def main():
         return run_stagger(args)
     if args.workload == "importance":
         return run_importance(args)
+    if args.workload == "mixed":
+        return run_mixed(args)
     return run_native(args)
 
 

@@ -133,6 +133,36 @@ typedef struct vc_kv_comp {
 } vc_kv_comp;
 
 /* ------------------------------------------------------------------------------------------ */
+/* vc_comp_bytes — the buffers one request's KV_comp needs, by the rules vc_compress_kv,
+ * vc_draft_attn and vc_append_kv follow ("Architecture support": one compressor interface), so a
+ * caller sizes them without restating those rules.
+ *
+ * VC_QUANT: ng = max(0, (ctx - residual_min) / 32) blocks are quantised and n_res = ctx - 32 ng
+ * rows stay bf16; ng_cap = the blocks of a context grown to max_ctx (at least 1), the head stride of
+ * kc/ks/kz/vc/vs/vz. VC_TOKEN_DROP: keep = min(keep, ctx) kept rows (idx; k_rows/v_rows when
+ * compact). Both: win_cap = the largest residual over contexts ctx .. max_ctx (0 for token drop)
+ * plus max_drafts + 1 window rows. Byte counts are for one buffer each (k and v alike).
+ * Errors: VC_ERR_INVALID (null pointers, a bad shape, ctx < 1, max_ctx < ctx, negative keep,
+ * residual_min or max_drafts); VC_ERR_UNSUPPORTED (bits not 2 or 4 for VC_QUANT). Host only. */
+typedef struct vc_comp_sizes {
+  int32_t ng;            /* VC_QUANT: quantised 32-token blocks at ctx tokens */
+  int32_t n_res;         /* VC_QUANT: bf16 residual rows at ctx tokens (window rows 0..n_res-1) */
+  int32_t ng_cap;        /* VC_QUANT: blocks to allocate per head (>= ng, >= 1) */
+  int32_t win_cap;       /* window rows to allocate per head */
+  int32_t keep;          /* VC_TOKEN_DROP: kept rows */
+  int32_t pad_;
+  size_t idx_bytes;      /* VC_TOKEN_DROP: int32 [keep] (at least 4) */
+  size_t rows_bytes;     /* VC_TOKEN_DROP, compact: each of k_rows, v_rows, bf16 [Hkv][keep][d] */
+  size_t codes_bytes;    /* VC_QUANT: each of kc, vc, uint8 [Hkv][ng_cap][32*d*bits/8] */
+  size_t kscale_bytes;   /* VC_QUANT: each of ks, kz, fp16 [Hkv][ng_cap][d] */
+  size_t vscale_bytes;   /* VC_QUANT: each of vs, vz, fp16 [Hkv][32*ng_cap][d/32] */
+  size_t win_bytes;      /* each of k_win, v_win, bf16 [Hkv][win_cap][d] */
+} vc_comp_sizes;
+
+vc_status vc_comp_bytes(const vc_shape* shape, int32_t mode, int32_t bits, int32_t ctx, int32_t max_ctx,
+                        int32_t keep, int32_t residual_min, int32_t max_drafts, vc_comp_sizes* out);
+
+/* ------------------------------------------------------------------------------------------ */
 /* vc_compress_kv — build KV_comp from KV_full ("Architecture support": one compressor interface
  * for token drop and quantisation).
  *

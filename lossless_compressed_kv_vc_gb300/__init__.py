@@ -1,7 +1,7 @@
 """Python binding of libvc, the GB300 (sm_103a) VeriCache draft/verify/accept hot path.
 
 Argument marshalling only: every step runs in the library's CUDA kernels. The names follow the
-C ABI in include/vc.h (vc_compress_kv, vc_draft_attn(_noalloc), vc_verify_attn(_heads), vc_accept,
+C ABI in include/vc.h (vc_comp_bytes, vc_compress_kv, vc_draft_attn(_noalloc), vc_verify_attn(_heads), vc_accept,
 vc_append_kv, vc_stage_full_kv, vc_snapkv_importance, vc_plan_stagger(_local), vc_stagger_period and the
 workspace-size / status-string calls). Tensors are torch tensors on the GPU; their data pointers
 and the current (or given) CUDA stream are passed through.
@@ -69,6 +69,12 @@ class vc_stagger_cost(C.Structure):
     _fields_ = [("draft_ns", C.c_int64), ("verify_ns", C.c_int64), ("stage_ns", C.c_int64)]
 
 
+class vc_comp_sizes(C.Structure):
+    _fields_ = [("ng", _i32), ("n_res", _i32), ("ng_cap", _i32), ("win_cap", _i32), ("keep", _i32), ("pad_", _i32),
+                ("idx_bytes", C.c_size_t), ("rows_bytes", C.c_size_t), ("codes_bytes", C.c_size_t),
+                ("kscale_bytes", C.c_size_t), ("vscale_bytes", C.c_size_t), ("win_bytes", C.c_size_t)]
+
+
 class vc_verify_req(C.Structure):
     _fields_ = [("full", vc_kv_full), ("q", _p), ("k_new", _p), ("v_new", _p), ("new_cap", _i32),
                 ("n_rows", _i32), ("o", _p)]
@@ -92,6 +98,7 @@ _lib.vc_importance_workspace_size.restype = C.c_size_t
 _lib.vc_plan_stagger.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
 _lib.vc_stagger_period.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
 _lib.vc_plan_stagger_local.argtypes = [C.POINTER(vc_stagger_cost), _i32, C.POINTER(_i32), C.POINTER(C.c_int64)]
+_lib.vc_comp_bytes.argtypes = [C.POINTER(vc_shape), _i32, _i32, _i32, _i32, _i32, _i32, _i32, C.POINTER(vc_comp_sizes)]
 _lib.vc_workspace_size.argtypes = [_i32, C.POINTER(vc_shape), _i32]
 _lib.vc_workspace_size.restype = C.c_size_t
 _lib.vc_status_string.argtypes = [_i32]
@@ -99,13 +106,13 @@ _lib.vc_status_string.restype = C.c_char_p
 _lib.vc_version.restype = _i32
 for _f in ("vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
            "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_plan_stagger", "vc_stagger_period",
-           "vc_plan_stagger_local", "vc_snapkv_importance"):
+           "vc_plan_stagger_local", "vc_snapkv_importance", "vc_comp_bytes"):
     getattr(_lib, _f).restype = _i32
 
 EXPORTS = ["vc_compress_kv", "vc_draft_attn", "vc_draft_attn_noalloc", "vc_verify_attn", "vc_verify_attn_heads",
            "vc_accept", "vc_stage_full_kv", "vc_append_kv", "vc_plan_stagger", "vc_stagger_period",
            "vc_plan_stagger_local", "vc_snapkv_importance", "vc_importance_workspace_size", "vc_workspace_size", "vc_status_string",
-           "vc_version"]
+           "vc_version", "vc_comp_bytes"]
 
 
 class VCError(RuntimeError):
@@ -147,6 +154,16 @@ def vc_version() -> int:
 
 def vc_workspace_size(call: int, shape: vc_shape, max_rows: int = 0) -> int:
     return _lib.vc_workspace_size(call, C.byref(shape), max_rows)
+
+
+def vc_comp_bytes(shape: vc_shape, mode: int, bits: int, ctx: int, max_ctx: int = 0, keep: int = 0,
+                  residual_min: int = 128, max_drafts: int = 0) -> vc_comp_sizes:
+    """Sizes of one request's compressed-cache buffers (max_ctx 0 = ctx). Raises VCError on bad arguments."""
+    out = vc_comp_sizes()
+    st = _lib.vc_comp_bytes(C.byref(shape), mode, bits, ctx, max_ctx or ctx, keep, residual_min, max_drafts,
+                            C.byref(out))
+    _check(st, "vc_comp_bytes", True)
+    return out
 
 
 def vc_compress_kv(shape: vc_shape, full, importance, recent, residual_min: int, comp, dev_status=None,

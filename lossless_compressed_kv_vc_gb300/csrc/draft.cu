@@ -225,6 +225,39 @@ __device__ __forceinline__ void code_offsets(uint32_t (&a)[4]) {
   }
 }
 
+// The value side's A fragment as exact, centred fp16 codes: code - C0 with C0 = (2^BITS - 1) / 2, so
+// the products with the B operand (scale o weight) have zero mean and the fp32 accumulator only ever
+// holds sums of the output's own size. (Leaving the codes offset by 2^(10-P) and removing the offset
+// with a second MMA adds and then subtracts 2^(10-P) * sum(scale o weight) in the accumulator; at
+// 65K tokens the truncation of those transients reached 0.5% of the output.) The word is shifted so
+// that each code sits at an odd bit position P' (P' + BITS <= 9): 2^(10-P') + C0 is then exact in
+// fp16 (a half-integer needs an ulp <= 0.5, i.e. 2^(10-P') <= 512), and one HSUB2 per register
+// leaves code - C0 exactly.
+template <int BITS, int P>
+__device__ __forceinline__ uint32_t code_centred_f16x2(uint32_t w) {
+  constexpr float c = (float)(1 << (10 - P)) + 0.5f * (float)((1 << BITS) - 1);
+  const uint32_t x = code_f16x2<BITS, P>(w);
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&x), __float2half2_rn(c));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+template <int BITS>
+__device__ __forceinline__ void code_frag_centred(uint32_t w, int ks, uint32_t (&a)[4]) {
+  if constexpr (BITS == 2) {
+    const uint32_t x = (ks & 1) ? (w >> 7) : (w << 1);  // codes of pair i at bits 2i + 1 of each half
+    a[0] = code_centred_f16x2<2, 1>(x);
+    a[1] = code_centred_f16x2<2, 3>(x);
+    a[2] = code_centred_f16x2<2, 5>(x);
+    a[3] = code_centred_f16x2<2, 7>(x);
+  } else {
+    const uint32_t x0 = w << 1, x1 = w >> 7;  // codes at bits 1 and 5 of each half
+    a[0] = code_centred_f16x2<4, 1>(x0);
+    a[1] = code_centred_f16x2<4, 5>(x0);
+    a[2] = code_centred_f16x2<4, 1>(x1);
+    a[3] = code_centred_f16x2<4, 5>(x1);
+  }
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, __half2 y) {
   const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&x), y);
   return *reinterpret_cast<const uint32_t*>(&r);
@@ -245,9 +278,9 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 //        removal of the code offsets are MMAs (z broadcast over tokens, resp. the constant offsets,
 //        against qn, resp. the scaled query), once per block for both 16-token halves;
 //   values (scale s_t, zero z_t per token and 32-channel group g), P <= 1 (the running maximum moves
-//   at every new maximum inside quantised blocks):
-//     O^T[c][h] += sum_t code (s_t p_th) + sum_t z_t p_th
-//     -> B operand fp16(s o p) per channel group with an offset-removal MMA, plus a per-(group,
+//   at every new maximum inside quantised blocks), codes centred (code_frag_centred, C0 = mid code):
+//     O^T[c][h] += sum_t (code - C0) (s_t p_th) + sum_t (z_t + C0 s_t) p_th
+//     -> A = exact fp16 code - C0, B operand fp16(s o p) per channel group, plus a per-(group,
 //        head) zero term zs accumulated in the softmax frame of O and added before O is read.
 template <int D, int BITS, int NHB>
 __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
@@ -373,14 +406,16 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
       pt1[hb] = pack_half2(p[hb][0][1], p[hb][1][1]);
     }
     const int t0 = 16 * half + a8, t1 = t0 + 8;
-    // the scales and zeros of all D/32 channel groups of tokens t0 and t1 (adjacent in the block)
+    // the scales and zeros of all D/32 channel groups of tokens t0 and t1 (adjacent in the block);
+    // the zeros take the centring: z + C0 s (fp16, one rounding of a value of the data's size)
+    const __half2 c0h = __float2half2_rn(0.5f * (float)((1 << BITS) - 1));
     __half2 vs0[D / 64], vs1[D / 64], vz0[D / 64], vz1[D / 64];
 #pragma unroll
     for (int k = 0; k < D / 64; ++k) {
       vs0[k] = reinterpret_cast<const __half2*>(vsc + t0 * (D / 32))[k];
       vs1[k] = reinterpret_cast<const __half2*>(vsc + t1 * (D / 32))[k];
-      vz0[k] = reinterpret_cast<const __half2*>(vze + t0 * (D / 32))[k];
-      vz1[k] = reinterpret_cast<const __half2*>(vze + t1 * (D / 32))[k];
+      vz0[k] = __hfma2(c0h, vs0[k], reinterpret_cast<const __half2*>(vze + t0 * (D / 32))[k]);
+      vz1[k] = __hfma2(c0h, vs1[k], reinterpret_cast<const __half2*>(vze + t1 * (D / 32))[k]);
     }
 #pragma unroll
     for (int g = 0; g < D / 32; ++g) {
@@ -400,12 +435,9 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
       for (int mm = 0; mm < 2; ++mm) {
         const int mt = 2 * g + mm;
         uint32_t a[4];
-        code_frag<BITS>(vw[(half * STEPS + (BITS == 4 ? mt : mt >> 1)) * 32 + lane], mt, a);
+        code_frag_centred<BITS>(vw[(half * STEPS + (BITS == 4 ? mt : mt >> 1)) * 32 + lane], mt, a);
 #pragma unroll
-        for (int hb = 0; hb < NHB; ++hb) {
-          mma_f16_16816(o[hb][mt], a, pb[hb][0], pb[hb][1]);
-          mma_f16_16816(o[hb][mt], acorr, pb[hb][0], pb[hb][1]);
-        }
+        for (int hb = 0; hb < NHB; ++hb) mma_f16_16816(o[hb][mt], a, pb[hb][0], pb[hb][1]);
       }
     }
   }

@@ -106,6 +106,41 @@ size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows) 
 }
 
 // ---------------------------------------------------------------------------------------------
+// The quantised layout rule every call shares: whole 32-token blocks while at least residual_min
+// trailing tokens stay bf16.
+static int quant_blocks(int ctx, int residual_min) { return ctx > residual_min ? (ctx - residual_min) / VC_GROUP : 0; }
+
+vc_status vc_comp_bytes(const vc_shape* shape, int32_t mode, int32_t bits, int32_t ctx, int32_t max_ctx,
+                        int32_t keep, int32_t residual_min, int32_t max_drafts, vc_comp_sizes* out) {
+  if (!out || !shape || shape->Hkv < 1 || (shape->d != 64 && shape->d != 128)) return VC_ERR_INVALID;
+  if (ctx < 1 || max_ctx < ctx || keep < 0 || residual_min < 0 || max_drafts < 0) return VC_ERR_INVALID;
+  if (mode != VC_TOKEN_DROP && mode != VC_QUANT) return VC_ERR_INVALID;
+  memset(out, 0, sizeof(*out));
+  const size_t Hkv = shape->Hkv, d = shape->d;
+  int res_max = 0;
+  if (mode == VC_QUANT) {
+    if (bits != 2 && bits != 4) return VC_ERR_UNSUPPORTED;
+    out->ng = quant_blocks(ctx, residual_min);
+    out->n_res = ctx - VC_GROUP * out->ng;
+    const int cap = quant_blocks(max_ctx, residual_min);
+    out->ng_cap = cap > 1 ? cap : 1;
+    // the residual of a context c > residual_min is residual_min .. residual_min + 31 rows
+    const int grown = max_ctx < residual_min + VC_GROUP - 1 ? max_ctx : residual_min + VC_GROUP - 1;
+    res_max = max_ctx > ctx && grown > out->n_res ? grown : out->n_res;
+    out->codes_bytes = Hkv * out->ng_cap * (VC_GROUP * d * bits / 8);
+    out->kscale_bytes = Hkv * out->ng_cap * d * 2;
+    out->vscale_bytes = Hkv * (size_t)VC_GROUP * out->ng_cap * (d / VC_GROUP) * 2;
+  } else {
+    out->keep = keep < ctx ? keep : ctx;
+    out->idx_bytes = (size_t)(out->keep > 1 ? out->keep : 1) * 4;
+    out->rows_bytes = Hkv * out->keep * d * 2;
+  }
+  out->win_cap = res_max + max_drafts + 1;
+  out->win_bytes = Hkv * out->win_cap * d * 2;
+  return VC_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
 vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const float* const* importance,
                          const int32_t* recent, int32_t residual_min, vc_kv_comp* comp, int32_t* dev_status,
                          cudaStream_t stream) {
@@ -179,7 +214,7 @@ vc_status vc_compress_kv(const vc_shape* shape, const vc_kv_full* full, const fl
     vc_kv_comp& c = comp[b];
     const vc_kv_full& f = full[b];
     if (c.bits != bits) return VC_ERR_UNSUPPORTED;
-    const int ng = f.ctx > residual_min ? (f.ctx - residual_min) / VC_GROUP : 0;
+    const int ng = quant_blocks(f.ctx, residual_min);
     const int n_res = f.ctx - VC_GROUP * ng;
     if (ng > c.ng_cap) return VC_ERR_INVALID;  // the buffers hold ng_cap blocks per head
     if (ng > 0 && (!aligned16(c.kc) || !aligned16(c.ks) || !aligned16(c.kz) || !aligned16(c.vc) ||
@@ -251,7 +286,7 @@ vc_status vc_append_kv(const vc_shape* shape, vc_kv_full* full, vc_kv_comp* comp
       if (ap.bits == 0) ap.bits = c.bits;
       if (c.bits != ap.bits) return VC_ERR_UNSUPPORTED;
       const int ctx2 = f.ctx + q.n_rows;
-      const int ng2 = ctx2 > residual_min ? (ctx2 - residual_min) / VC_GROUP : 0;
+      const int ng2 = quant_blocks(ctx2, residual_min);
       const int n_res = f.ctx - VC_GROUP * c.ng, n_ext = n_res + q.n_rows;
       if (c.ng < 0 || ng2 < c.ng || ng2 > c.ng_cap || n_res < 0 || n_res > c.win_cap) return VC_ERR_INVALID;
       if (n_ext > VC_APPEND_MAX_ROWS) return VC_ERR_UNSUPPORTED;

@@ -14,17 +14,9 @@ from typing import List, Optional
 import torch
 
 from . import (vc_shape, vc_kv_full, vc_kv_comp, vc_draft_req, vc_verify_req, vc_append_req, vc_importance_req,
-               vc_snapkv_importance, vc_importance_workspace_size, VC_POOL_MAX, vc_compress_kv,
+               vc_snapkv_importance, vc_importance_workspace_size, VC_POOL_MAX, vc_compress_kv, vc_comp_bytes,
                vc_draft_attn, vc_verify_attn, vc_verify_attn_heads, vc_accept, vc_append_kv, vc_workspace_size,
                VC_TOKEN_DROP, VC_QUANT, VC_CALL_DRAFT, VC_CALL_VERIFY)
-
-GROUP = 32
-
-
-def quant_layout(ctx: int, residual_min: int = 128):
-    """(ng, n_res) the library uses: whole 32-token groups, at least residual_min bf16 rows."""
-    ng = (ctx - residual_min) // GROUP if ctx > residual_min else 0
-    return ng, ctx - GROUP * ng
 
 
 @dataclass
@@ -85,32 +77,30 @@ class Batch:
         self.ws_verify = torch.empty(max(vb // 4 + 64, 64), dtype=torch.float32, device=device)
 
     def _alloc(self, r: Req):
+        """Buffers of one request, sized by the library's own layout query (vc_comp_bytes): the
+        residual and block counts, the block capacity for a context grown by r.grow tokens and the
+        window rows are the library's rules, not restated here."""
         Hkv, d, dev = self.Hkv, self.d, self.device
+        sz = vc_comp_bytes(vc_shape(1, self.Hq, Hkv, d), r.mode, r.bits, r.ctx, r.ctx + r.grow, r.keep,
+                           self.residual_min, r.L)
         if r.mode == VC_TOKEN_DROP:
-            keep = min(r.keep, r.ctx)
-            r.idx = torch.empty(max(keep, 1), dtype=torch.int32, device=dev)
+            keep = sz.keep
+            r.idx = torch.empty(sz.idx_bytes // 4, dtype=torch.int32, device=dev)
             if r.compact:
                 r.k_rows = torch.empty((Hkv, keep, d), dtype=torch.bfloat16, device=dev)
                 r.v_rows = torch.empty((Hkv, keep, d), dtype=torch.bfloat16, device=dev)
             r.n_res = 0
         else:
-            ng, n_res = quant_layout(r.ctx, self.residual_min)
-            r.n_res = n_res
-            # room for the blocks the context fills as it grows by up to r.grow tokens
-            ng_cap = max(quant_layout(r.ctx + r.grow, self.residual_min)[0], 1)
-            b = r.bits
+            r.n_res = sz.n_res
+            ng_cap = sz.ng_cap
             u8, f16 = torch.uint8, torch.float16
-            r.kc = torch.empty((Hkv, ng_cap, 4 * d * b), dtype=u8, device=dev)
+            r.kc = torch.empty((Hkv, ng_cap, sz.codes_bytes // (Hkv * ng_cap)), dtype=u8, device=dev)
             r.ks = torch.empty((Hkv, ng_cap, d), dtype=f16, device=dev)
             r.kz = torch.empty((Hkv, ng_cap, d), dtype=f16, device=dev)
-            r.vc = torch.empty((Hkv, ng_cap, 4 * d * b), dtype=u8, device=dev)
-            r.vs = torch.empty((Hkv, GROUP * ng_cap, d // 32), dtype=f16, device=dev)
-            r.vz = torch.empty((Hkv, GROUP * ng_cap, d // 32), dtype=f16, device=dev)
-        # the residual never exceeds residual_min + 31 rows once the context passes residual_min
-        res_max = r.n_res
-        if r.mode == VC_QUANT and r.grow > 0:
-            res_max = max(r.n_res, min(r.ctx + r.grow, self.residual_min + GROUP - 1))
-        win_cap = res_max + r.L + 1
+            r.vc = torch.empty((Hkv, ng_cap, sz.codes_bytes // (Hkv * ng_cap)), dtype=u8, device=dev)
+            r.vs = torch.empty((Hkv, sz.vscale_bytes // (2 * Hkv * (d // 32)), d // 32), dtype=f16, device=dev)
+            r.vz = torch.empty((Hkv, sz.vscale_bytes // (2 * Hkv * (d // 32)), d // 32), dtype=f16, device=dev)
+        win_cap = sz.win_cap
         r.k_win = torch.zeros((Hkv, win_cap, d), dtype=torch.bfloat16, device=dev)
         r.v_win = torch.zeros((Hkv, win_cap, d), dtype=torch.bfloat16, device=dev)
         r.o_draft = torch.empty((r.L, self.Hq, d), dtype=torch.bfloat16, device=dev)
@@ -278,7 +268,7 @@ class Batch:
         for b, r in enumerate(self.reqs):
             r.ctx = self.full[b].ctx
             if r.mode == VC_QUANT:
-                r.n_res = r.ctx - GROUP * self.comp[b].ng
+                r.n_res = self.comp[b].n_win  # the window restarts with the new residual
         if getattr(self, "_steps", None) is not None:
             self.prepare_steps()
 
@@ -322,9 +312,11 @@ class HostRound:
     the batch's descriptor arrays for every slot)."""
 
     def __init__(self, bt: Batch, logits: torch.Tensor, draft: torch.Tensor, L: torch.Tensor,
-                 out_tokens: torch.Tensor, n_acc: torch.Tensor, slots: int = 2):
+                 out_tokens: torch.Tensor, n_acc: torch.Tensor, slots: int = 2,
+                 names=("q", "k_new", "v_new", "importance")):
+        """names: the per-request inputs the round reads and so copies (importance only when the
+        round compresses)."""
         pin = lambda t: t.detach().to("cpu").pin_memory()
-        names = ("q", "k_new", "v_new", "importance")
         fields = [(r, n) for r in bt.reqs for n in names if getattr(r, n) is not None]
         self.draft_host = [pin(getattr(r, n)) for r, n in fields]
         self.accept_host = [pin(t) for t in (draft, logits, L)]
@@ -380,27 +372,34 @@ class StaggeredOffload:
     Two groups of requests alternate roles. In each phase one group drafts its L steps on the
     compute stream (HBM-bound) while the other group's KV_full is copied host-to-device on the copy
     stream (host-link-bound); the compute stream then waits for that copy and verifies and accepts
-    the staged group. Each group keeps its own device staging slot, so a copy never waits for the
+    the staged group. Each request keeps its own device staging slot, so a copy never waits for the
     other group's verification.
+
+    A group is one Batch or a list of Batches (one per compression mode: a batch that mixes token
+    drop and quantisation drafts with one C-ABI call per mode); host_kv[g] and slots[g] list the
+    group's requests in that order (batch by batch). host_kv[g][i] (pinned [K; V] buffer) and
+    slots[g][i] (its device copy, which the request's KV_full descriptor points at) are None for a
+    request whose KV_full stays in HBM; such a request drafts and verifies in its group's phases
+    with nothing to copy. plan_groups chooses the groups.
 
     head_chunks > 1 pipelines the copy into the verification ("Cross-resource staggering (P1)"
     applied to the verification itself): a group's KV_full is copied a range of KV heads at a time
     (each head's K and V rows are contiguous in the [K; V][Hkv][cap][d] layout), each range records
     its own event, and the compute stream verifies each head range (vc_verify_attn_heads) as soon as
     it has landed, so only the last range's verification remains once the copy ends.
-
-    host_kv[g][i] (pinned [K; V] buffer) and slots[g][i] (its device copy, which request i's KV_full
-    descriptor points at) are None for a request whose KV_full stays in HBM; such a request drafts
-    and verifies in its group's phases with nothing to copy. plan_groups chooses the groups.
     """
 
-    def __init__(self, groups: List[Batch], host_kv: List[List[Optional[torch.Tensor]]],
+    def __init__(self, groups, host_kv: List[List[Optional[torch.Tensor]]],
                  slots: List[List[Optional[torch.Tensor]]],
                  copy_stream, compute_stream, chunk_bytes: int = 64 << 20, head_chunks: int = 1):
         assert len(groups) == 2
-        Hkv = groups[0].Hkv
-        assert 1 <= head_chunks <= Hkv and groups[1].Hkv == Hkv
-        self.groups, self.host_kv, self.slots = groups, host_kv, slots
+        self.groups = [list(g) if isinstance(g, (list, tuple)) else [g] for g in groups]
+        self.single = [not isinstance(g, (list, tuple)) for g in groups]
+        Hkv = self.groups[0][0].Hkv
+        assert 1 <= head_chunks <= Hkv and all(bt.Hkv == Hkv for grp in self.groups for bt in grp)
+        for g in range(2):
+            assert len(host_kv[g]) == len(slots[g]) == sum(len(bt.reqs) for bt in self.groups[g])
+        self.host_kv, self.slots = host_kv, slots
         self.copy_stream, self.compute_stream = copy_stream, compute_stream
         self.chunk_bytes = chunk_bytes
         self.edges = [c * Hkv // head_chunks for c in range(head_chunks + 1)]
@@ -408,10 +407,14 @@ class StaggeredOffload:
         self.verified = [torch.cuda.Event(), torch.cuda.Event()]
         for g in range(2):  # a slot is free before its first copy
             self.verified[g].record(compute_stream)
+        self._cur = [None, None]  # host-input periods: the HostRound slot each batch last drafted from
+
+    def stage_bytes(self, g: int) -> int:
+        return sum(h.numel() * h.element_size() for h in self.host_kv[g] if h is not None)
 
     def stage(self, g: int, events=None):
         """Issue the host-to-device copies of group g's KV_full on the copy stream, one KV-head range
-        at a time (K then V rows of those heads, for every request of the group)."""
+        at a time (K then V rows of those heads, for every host-resident request of the group)."""
         from . import vc_stage_full_kv
         self.copy_stream.wait_event(self.verified[g])  # its previous verification has read the slot
         if events is not None:
@@ -429,35 +432,97 @@ class StaggeredOffload:
         if events is not None:
             events[1].record(self.copy_stream)
 
-    def phase(self, draft_g: int, io, draft_events=None, stage_events=None, verify_event=None):
-        """Group draft_g drafts while the other group stages, then the other group verifies and accepts.
-        io[g] = (logits, draft, L, out_tokens, n_acc) of group g. verify_event, if given, is recorded
-        on the compute stream once the other group's last head range is verified."""
-        other = 1 - draft_g
-        self.stage(other, stage_events)
-        bt = self.groups[draft_g]
-        if draft_events is not None:
-            draft_events[0].record(self.compute_stream)
-        for shape, arr, act in bt._steps:
-            vc_draft_attn(shape, arr, bt.ws_draft, bt.dev_status, self.compute_stream)
-        if draft_events is not None:
-            draft_events[1].record(self.compute_stream)
-        ob = self.groups[other]
-        for c in range(len(self.edges) - 1):
-            self.compute_stream.wait_event(self.staged[other][c])
-            vc_verify_attn_heads(ob.shape, ob._verify_arr, self.edges[c], self.edges[c + 1], ob.ws_verify,
-                                 ob.dev_status, self.compute_stream)
-        self.verified[other].record(self.compute_stream)
-        if verify_event is not None:
-            verify_event.record(self.compute_stream)
-        lg, dr, L, tok, nacc = io[other]
-        accept(lg, dr, L, tok, nacc, self.compute_stream)
+    def _io(self, io, g):
+        return [io[g]] if self.single[g] else list(io[g])
 
-    def period(self, io, events=None):
-        """Both phases: every request drafts once and is verified once."""
+    def phase(self, draft_g: int, io, draft_events=None, stage_events=None, verify_event=None, host_rounds=None,
+              verify_events=None):
+        """Group draft_g drafts while the other group stages, then the other group verifies and
+        accepts. io[g] = (logits, draft, L, out_tokens, n_acc) of group g's single batch, or a list
+        of such tuples, one per batch of the group. draft_events: a (start, end) pair around the
+        draft phase, or a list of pairs, one per batch; verify_events: a (start, end) pair around the
+        other group's verification; verify_event (legacy) is recorded once it is verified.
+
+        host_rounds[g][j] (a HostRound of batch j of group g; io is then ignored): the drafting
+        group's round inputs are first copied from pinned host memory on the copy stream (its query
+        and drafted K/V rows before the other group's KV_full, its drafts, logits and L after it: they
+        are read only when it is verified, in the next phase), and the verified group's accepted
+        tokens and counts go back to pinned host memory."""
+        other = 1 - draft_g
+        cs, ks = self.copy_stream, self.compute_stream
+        dgrp, ogrp = self.groups[draft_g], self.groups[other]
+        if host_rounds is not None:
+            sls = []
+            for hr in host_rounds[draft_g]:
+                sl = hr.next_slot()
+                cs.wait_event(sl.free)
+                with torch.cuda.stream(cs):
+                    for h, d in zip(hr.draft_host, sl.draft_dev):
+                        d.copy_(h, non_blocking=True)
+                sl.ready.record(cs)
+                sls.append(sl)
+            self._cur[draft_g] = sls
+        self.stage(other, stage_events)
+        if host_rounds is not None:
+            for hr, sl in zip(host_rounds[draft_g], self._cur[draft_g]):
+                with torch.cuda.stream(cs):
+                    for h, d in zip(hr.accept_host, sl.accept_dev):
+                        d.copy_(h, non_blocking=True)
+                sl.landed.record(cs)
+        per_batch = isinstance(draft_events, (list, tuple)) and len(draft_events) == len(dgrp) and \
+            isinstance(draft_events[0], (list, tuple))
+        if draft_events is not None and not per_batch:
+            draft_events[0].record(ks)
+        for j, bt in enumerate(dgrp):
+            steps = bt._steps
+            if host_rounds is not None:
+                sl = self._cur[draft_g][j]
+                ks.wait_event(sl.ready)
+                steps = sl.steps
+            if per_batch:
+                draft_events[j][0].record(ks)
+            for shape, arr, act in steps:
+                vc_draft_attn(shape, arr, bt.ws_draft, bt.dev_status, ks)
+            if per_batch:
+                draft_events[j][1].record(ks)
+        if draft_events is not None and not per_batch:
+            draft_events[1].record(ks)
+        if verify_events is not None:
+            verify_events[0].record(ks)
+        for c in range(len(self.edges) - 1):
+            ks.wait_event(self.staged[other][c])
+            for j, ob in enumerate(ogrp):
+                varr = ob._verify_arr
+                if host_rounds is not None and self._cur[other] is not None:
+                    varr = self._cur[other][j].verify_arr
+                vc_verify_attn_heads(ob.shape, varr, self.edges[c], self.edges[c + 1], ob.ws_verify,
+                                     ob.dev_status, ks)
+        self.verified[other].record(ks)
+        if verify_events is not None:
+            verify_events[1].record(ks)
+        if verify_event is not None:
+            verify_event.record(ks)
+        if host_rounds is not None:
+            for j, hr in enumerate(host_rounds[other]):
+                sl = self._cur[other][j] if self._cur[other] is not None else hr.slots[0]
+                ks.wait_event(sl.landed)
+                dr, lg, Lt = sl.accept_dev
+                accept(lg, dr, Lt, hr.out_tokens, hr.n_acc, ks)
+                sl.free.record(ks)
+                with torch.cuda.stream(ks):
+                    hr.host_tokens.copy_(hr.out_tokens, non_blocking=True)
+                    hr.host_n_acc.copy_(hr.n_acc, non_blocking=True)
+            return
+        for lg, dr, L, tok, nacc in self._io(io, other):
+            accept(lg, dr, L, tok, nacc, ks)
+
+    def period(self, io, events=None, host_rounds=None):
+        """Both phases: every request drafts once and is verified once. events: optional dict with
+        draft0/draft1 (a pair, or a list of pairs, one per batch of the group), stage0/stage1,
+        verify0/verify1 (pairs) and verified0/verified1 (single events)."""
         ev = events or {}
-        self.phase(0, io, ev.get("draft0"), ev.get("stage1"), ev.get("verified1"))
-        self.phase(1, io, ev.get("draft1"), ev.get("stage0"), ev.get("verified0"))
+        self.phase(0, io, ev.get("draft0"), ev.get("stage1"), ev.get("verified1"), host_rounds, ev.get("verify1"))
+        self.phase(1, io, ev.get("draft1"), ev.get("stage0"), ev.get("verified0"), host_rounds, ev.get("verify0"))
 
 
 def stagger_costs(draft_ns, verify_ns, stage_ns):
@@ -473,6 +538,82 @@ def plan_groups(costs):
     plan = vc_plan_stagger if len(costs) <= VC_STAGGER_MAX else vc_plan_stagger_local
     st, groups, t = plan(costs)
     return [r for r, g in enumerate(groups) if g == 0], [r for r, g in enumerate(groups) if g == 1], t
+
+
+def staggered_groups(Hq: int, Hkv: int, d: int, reqs: List[Req], split, on_host, residual_min: int = 128,
+                     device="cuda", stream=None):
+    """The two groups of StaggeredOffload for a batch that mixes compression modes and residencies:
+    request r goes to group split[r]; each group holds one Batch per compression mode (a draft call
+    serves one mode); every Batch compresses (KV_comp is built once per request, while KV_full is
+    still in HBM); then the KV_full of the requests with on_host[r] moves to pinned host memory,
+    each with a device staging slot. A token-drop request whose KV_full leaves HBM must keep its
+    kept rows in a compact copy (Req.compact). Returns (groups, members, host_kv, slots): groups[g]
+    the Batches of group g, members[g][j] the request indices of its Batch j, host_kv[g] / slots[g]
+    flat over the group's requests in batch order (None for HBM-resident requests)."""
+    groups, members, host_kv, slots = [], [], [], []
+    modes = sorted({r.mode for r in reqs})
+    for gi in (0, 1):
+        bts, mem = [], []
+        for m in modes:
+            idx = [i for i, r in enumerate(reqs) if split[i] == gi and r.mode == m]
+            if not idx:
+                continue
+            for i in idx:
+                assert m != VC_TOKEN_DROP or reqs[i].compact or not on_host[i], \
+                    "a token-drop request with KV_full on the host needs compact kept rows"
+            bt = Batch(Hq, Hkv, d, [reqs[i] for i in idx], residual_min=residual_min, device=device)
+            bt.compress(stream)
+            bts.append(bt)
+            mem.append(idx)
+        groups.append(bts)
+        members.append(mem)
+    torch.cuda.synchronize()
+    for gi in (0, 1):
+        h, sl = move_some_full_kv_to_host(groups[gi], [[on_host[i] for i in idx] for idx in members[gi]])
+        host_kv.append(h)
+        slots.append(sl)
+        for bt in groups[gi]:
+            bt.prepare_steps()
+    return groups, members, host_kv, slots
+
+
+def group_io(members, logits: torch.Tensor, draft: torch.Tensor, L: torch.Tensor):
+    """Per group, per Batch: (logits, draft, L, out_tokens, n_acc) of the Batch's requests, the
+    first three gathered from the whole batch's tensors."""
+    io = []
+    for mem in members:
+        row = []
+        for idx in mem:
+            sel = torch.tensor(idx, device=logits.device)
+            row.append((logits[sel].contiguous(), draft[sel].contiguous(), L[sel].contiguous(),
+                        torch.empty((len(idx), logits.shape[1]), dtype=torch.int32, device=logits.device),
+                        torch.empty((len(idx),), dtype=torch.int32, device=logits.device)))
+        io.append(row)
+    return io
+
+
+def move_some_full_kv_to_host(batches: List[Batch], on_host):
+    """Like move_full_kv_to_host for the requests with on_host[j][i] true (batch j, request i);
+    the others keep KV_full in HBM (None entries). Returns flat (host buffers, slots) lists over
+    the batches' requests in order."""
+    hs, ss = [], []
+    for bt, flags in zip(batches, on_host):
+        for b, (r, f) in enumerate(zip(bt.reqs, flags)):
+            if not f:
+                hs.append(None)
+                ss.append(None)
+                continue
+            kv = torch.stack([r.k_full, r.v_full])
+            h = torch.empty(kv.shape, dtype=kv.dtype, pin_memory=True)
+            h.copy_(kv)
+            slot = torch.empty_like(kv)
+            slot.copy_(kv)
+            bt.set_full(b, slot[0], slot[1])
+            hs.append(h)
+            ss.append(slot)
+            del kv
+    torch.cuda.synchronize()
+    return hs, ss
 
 
 def move_full_kv_to_host(groups: List[Batch]):

@@ -84,6 +84,32 @@ def test_draft_counter_block_does_not_depend_on_the_shape(lib):
     assert vc.vc_draft_attn(big, req, stream=0, raise_on_error=False) == vc.VC_ERR_UNSUPPORTED
 
 
+def test_comp_bytes_follows_the_layout_rule():
+    """vc_comp_bytes (host only) against the oracle's statement of the quantised layout: blocks and
+    residual at ctx, block capacity for the grown context, window rows = the largest residual on the
+    way there + drafts + 1, and each buffer's bytes from its documented shape."""
+    import oracle as O
+    import lossless_compressed_kv_vc_gb300 as vc
+    sh = vc.vc_shape(1, 32, 8, 128)
+    for ctx, grow, bits, L in ((1000, 0, 2, 8), (65536, 0, 2, 25), (131072, 0, 4, 40), (100, 0, 2, 3),
+                               (300, 2, 4, 5), (300, 200, 2, 5), (128, 40, 2, 1), (160, 0, 4, 0)):
+        sz = vc.vc_comp_bytes(sh, vc.VC_QUANT, bits, ctx, ctx + grow, 0, 128, L)
+        ng, nr = O.quant_layout(ctx, 128)
+        cap = max(O.quant_layout(ctx + grow, 128)[0], 1)
+        res_max = max([O.quant_layout(c, 128)[1] for c in range(ctx, ctx + grow + 1)])
+        assert (sz.ng, sz.n_res, sz.ng_cap) == (ng, nr, cap)
+        assert res_max <= sz.win_cap - L - 1 <= max(nr, 128 + 31)  # covers every residual on the way
+        assert sz.codes_bytes == 8 * cap * 32 * 128 * bits // 8
+        assert sz.kscale_bytes == 8 * cap * 128 * 2 and sz.vscale_bytes == 8 * 32 * cap * 4 * 2
+        assert sz.win_bytes == 8 * sz.win_cap * 128 * 2
+    sz = vc.vc_comp_bytes(sh, vc.VC_TOKEN_DROP, 0, 32768, 32768, 8192, 128, 32)
+    assert (sz.keep, sz.idx_bytes, sz.rows_bytes, sz.win_cap) == (8192, 8192 * 4, 8 * 8192 * 128 * 2, 33)
+    assert vc.vc_comp_bytes(sh, vc.VC_TOKEN_DROP, 0, 100, 100, 500).keep == 100
+    for args in ((vc.VC_QUANT, 3, 1000), (vc.VC_QUANT, 2, 0), (7, 2, 1000)):
+        with pytest.raises(vc.VCError):
+            vc.vc_comp_bytes(sh, *args)
+
+
 def test_append_validation_rejects_without_launching(lib):
     """vc_append_kv checks capacities before launching; a call with nothing to append launches
     nothing and succeeds. The pointers are fake (aligned, never dereferenced on these paths)."""

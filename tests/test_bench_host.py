@@ -81,7 +81,32 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     def boom():
         raise AssertionError("a rank other than 0 ran the oracle")
 
-    monkeypatch.setattr(bench, "run_cpu_child", boom)
+    monkeypatch.setattr(bench, "OraclePool", boom)
     args = bench.argparse.Namespace(warmup=1, steps=1, gpus=2)
     assert bench.run_reference(args) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_oracle_pool_wave_counts_the_requests_accepted_tokens():
+    """One wave of the CPU legs' worker pool (two spawned single-thread workers splitting the query
+    heads) returns the request's accepted tokens as the oracle's accept gives them, and positive wall
+    and worker times."""
+    import oracle as O
+    from workloads import configs, gen
+    w = configs.scaled(configs.mixed_serving(), ctx_div=128, batch=2, vocab=2000)
+    pool = bench.OraclePool(2)
+    try:
+        for b in range(2):
+            wall, cpu, n = pool.wave(w, b)
+            dr, lg = gen.request_logits(w, 0, b)
+            assert n == O.accept(lg.numpy(), dr.numpy(), w.L[b])[1]
+            assert wall > 0 and cpu > 0
+    finally:
+        pool.close()
+
+
+def test_interval_coverage():
+    """The overlap figure: the part of a copy interval under the union of compute intervals."""
+    assert bench._covered((0.0, 10.0), [(2.0, 4.0), (3.0, 6.0), (8.0, 20.0)]) == pytest.approx(0.6)
+    assert bench._covered((0.0, 10.0), []) == 0.0
+    assert bench._covered((5.0, 6.0), [(0.0, 100.0)]) == pytest.approx(1.0)

@@ -44,7 +44,7 @@ def test_dropped_chunks_fail(case):
     for c in (3, 100, 257, 500):  # four 16-row chunks
         keep[16 * c:16 * c + 16] = False
     bad = _bf16(O.draft_attn(q, k[:, keep], v[:, keep], empty, empty))
-    n1, rel, n3 = attn_errors(bad, ref)
+    n1, rel, n3, _ = attn_errors(bad, ref)
     assert rel > REL_L2 and n3 > 0, (n1, rel, n3)
     with pytest.raises(AssertionError):
         assert_attn_close(bad, ref, "64 rows dropped")
@@ -53,7 +53,7 @@ def test_dropped_chunks_fail(case):
 def test_scaled_softmax_fails(case):
     q, k, v, empty, ref = case
     bad = _bf16(O.draft_attn(0.95 * q, k, v, empty, empty))
-    n1, rel, n3 = attn_errors(bad, ref)
+    n1, rel, n3, _ = attn_errors(bad, ref)
     assert rel > REL_L2 and n3 > 0, (n1, rel, n3)
     with pytest.raises(AssertionError):
         assert_attn_close(bad, ref, "scale x 0.95")

@@ -91,6 +91,31 @@ def request(w: Workload, rnd: int, b: int, device="cpu") -> RequestInputs:
     return RequestInputs(k, v, imp, q, kn, vn)
 
 
+def request_logits(w: Workload, rnd: int, b: int, device="cpu", vocab: int | None = None, out=None):
+    """Request b's row of drafts_and_logits: (draft int32 [L_max], logits fp32 [L_max+1][V]), written
+    into `out` = (draft row, logits row) when given."""
+    V = vocab if vocab is not None else w.V
+    Lm, Lb = w.L_max, w.L[b]
+    draft, logits = out if out is not None else (torch.zeros((Lm,), dtype=torch.int32, device=device),
+                                                 torch.empty((Lm + 1, V), dtype=torch.float32, device=device))
+    gd = _gen(w, rnd, b, KIND_DRAFT, device)
+    draft[:Lb] = torch.randint(0, V, (Lb,), generator=gd, device=device, dtype=torch.int64).to(torch.int32)
+    gl = _gen(w, rnd, b, KIND_LOGITS, device)
+    logits[:] = torch.randn((Lm + 1, V), generator=gl, device=device, dtype=torch.float32)
+    gp = _gen(w, rnd, b, KIND_PLANT, device)
+    u = torch.rand((Lm,), generator=gp, device=device, dtype=torch.float64)
+    rows = logits[:Lb]
+    x = draft[:Lb].long()
+    rmax = rows.max(dim=1).values
+    rmin = rows.min(dim=1).values
+    am = rows.argmax(dim=1)
+    plant = u[:Lb] < w.p[b]
+    ar = torch.arange(Lb, device=device)
+    hit = torch.where(plant, rmax + 1.0, torch.where(am == x, rmin - 1.0, rows[ar, x]))
+    rows[ar, x] = hit
+    return draft, logits
+
+
 def drafts_and_logits(w: Workload, rnd: int, device="cpu", vocab: int | None = None):
     """(draft int32 [B][L_max], logits fp32 [B][L_max+1][V], L int32 [B]) with planted matches."""
     V = vocab if vocab is not None else w.V
@@ -98,21 +123,6 @@ def drafts_and_logits(w: Workload, rnd: int, device="cpu", vocab: int | None = N
     draft = torch.zeros((B, Lm), dtype=torch.int32, device=device)
     logits = torch.empty((B, Lm + 1, V), dtype=torch.float32, device=device)
     for b in range(B):
-        Lb = w.L[b]
-        gd = _gen(w, rnd, b, KIND_DRAFT, device)
-        draft[b, :Lb] = torch.randint(0, V, (Lb,), generator=gd, device=device, dtype=torch.int64).to(torch.int32)
-        gl = _gen(w, rnd, b, KIND_LOGITS, device)
-        logits[b] = torch.randn((Lm + 1, V), generator=gl, device=device, dtype=torch.float32)
-        gp = _gen(w, rnd, b, KIND_PLANT, device)
-        u = torch.rand((Lm,), generator=gp, device=device, dtype=torch.float64)
-        rows = logits[b, :Lb]
-        x = draft[b, :Lb].long()
-        rmax = rows.max(dim=1).values
-        rmin = rows.min(dim=1).values
-        am = rows.argmax(dim=1)
-        plant = u[:Lb] < w.p[b]
-        ar = torch.arange(Lb, device=device)
-        hit = torch.where(plant, rmax + 1.0, torch.where(am == x, rmin - 1.0, rows[ar, x]))
-        rows[ar, x] = hit
+        request_logits(w, rnd, b, device, V, out=(draft[b], logits[b]))
     Lt = torch.tensor(w.L, dtype=torch.int32, device=device)
     return draft, logits, Lt
