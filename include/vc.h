@@ -28,6 +28,11 @@
  *   - Calls are asynchronous on `stream`; a call returns before its kernels finish.
  *   - At most VC_MAX_BATCH requests per call (per-request descriptors travel as kernel params).
  *   - Head dim d is 64 or 128; Hq is a multiple of Hkv; query head h reads KV head h / (Hq/Hkv).
+ *   - Every wait inside a kernel is bounded; one that gives up records VC_DEV_TIMEOUT, waits (with
+ *     the full bound) for the copies it has already issued, and returns. The environment variable
+ *     VC_SPIN_LIMIT (read by each vc_draft_attn call) sets how many tries a draft warp's wait for its
+ *     next stage of data makes before it gives up (default 4194304; 0 gives up at once): a short
+ *     limit makes that wait run out without any fault, which is how its error path is tested.
  */
 #ifndef VC_H_
 #define VC_H_
@@ -320,7 +325,10 @@ vc_status vc_accept(int32_t B, int32_t L_max, int32_t V, const float* logits, co
  *
  * Issues cudaMemcpyAsync host-to-device copies of `chunk_bytes` (0 = one copy) on copy_stream and
  * records `done` (may be NULL) on it after the last chunk; the caller makes the verifying stream
- * wait on `done`. host_src must be page-locked (VC_ERR_NOT_PINNED otherwise).
+ * wait on `done`. host_src must be page-locked (VC_ERR_NOT_PINNED otherwise). A copy that cannot be
+ * issued returns VC_ERR_CUDA: the chunks before it are in flight, none after it is issued and `done`
+ * is not recorded. Test hook: with the environment variable VC_FAIL_STAGE_CHUNK=k the call treats
+ * chunk k (0-based) as such a failed copy.
  */
 vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, size_t chunk_bytes,
                            cudaStream_t copy_stream, cudaEvent_t done);

@@ -922,8 +922,11 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     }
     cp_async_wait<C::NST - 1>();  // this lane's copies of chunk i have landed
     __syncwarp();                  // ... and every other lane's
-    if (!mbar_wait_bounded(&bars[st], (i / C::NST) & 1, p.dev_status)) {
-      for (int j = i + 1; j < n && j < i + C::NST; ++j) mbar_wait_bounded(&bars[j % C::NST], (j / C::NST) & 1, p.dev_status);
+    if (!mbar_wait_bounded(&bars[st], (i / C::NST) & 1, p.dev_status, p.spin_limit)) {
+      // give up on this range, but not on the copies already issued into the ring (this stage's
+      // and the ones after it): wait for them with the full bound so that no copy is still
+      // writing shared memory when the CTA exits
+      for (int j = i; j < n && j < i + C::NST; ++j) mbar_wait_bounded(&bars[j % C::NST], (j / C::NST) & 1, p.dev_status);
       aborted = true;
       break;
     }

@@ -346,6 +346,11 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   p.G = G;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
   p.dev_status = dev_status;
+  // VC_SPIN_LIMIT (tries; default kSpinLimit): how long a warp waits for a stage's data before it
+  // records VC_DEV_TIMEOUT and leaves its range (a short limit makes the wait run out on purpose,
+  // with every copy still completing; used to test the timeout path)
+  const int spin = env_int("VC_SPIN_LIMIT", -1);
+  p.spin_limit = spin >= 0 ? (uint32_t)spin : kSpinLimit;
 
   int64_t total = 0;
   for (int b = 0; b < B; ++b) {
@@ -509,9 +514,13 @@ vc_status vc_stage_full_kv(const void* host_src, void* dev_dst, size_t bytes, si
   if (chunk_bytes == 0 || chunk_bytes > bytes) chunk_bytes = bytes;
   const char* s = static_cast<const char*>(host_src);
   char* dptr = static_cast<char*>(dev_dst);
-  for (size_t off = 0; off < bytes; off += chunk_bytes) {
+  // VC_FAIL_STAGE_CHUNK=k (test hook, host side): chunk k's copy is treated as a failed
+  // cudaMemcpyAsync; nothing after it is issued and `done` is not recorded
+  const int fail_at = env_int("VC_FAIL_STAGE_CHUNK", -1);
+  int chunk = 0;
+  for (size_t off = 0; off < bytes; off += chunk_bytes, ++chunk) {
     const size_t n = bytes - off < chunk_bytes ? bytes - off : chunk_bytes;
-    if (cudaMemcpyAsync(dptr + off, s + off, n, cudaMemcpyHostToDevice, copy_stream) != cudaSuccess)
+    if (chunk == fail_at || cudaMemcpyAsync(dptr + off, s + off, n, cudaMemcpyHostToDevice, copy_stream) != cudaSuccess)
       return VC_ERR_CUDA;
   }
   if (done && cudaEventRecord(done, copy_stream) != cudaSuccess) return VC_ERR_CUDA;

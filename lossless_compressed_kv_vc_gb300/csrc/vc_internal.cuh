@@ -65,9 +65,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: returns false (after recording VC_DEV_TIMEOUT) if the phase never completes.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* st) {
-  for (uint32_t it = 0; it < kSpinLimit; ++it)
+// Bounded wait: returns false (after recording VC_DEV_TIMEOUT) if the phase does not complete
+// within `limit` tries.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* st,
+                                                  uint32_t limit = kSpinLimit) {
+  for (uint32_t it = 0; it < limit; ++it)
     if (mbar_try_wait(bar, parity)) return true;
   set_status(st, VC_DEV_TIMEOUT);
   return false;
@@ -267,6 +269,9 @@ struct DraftParams {
   int32_t n_warp_head;   // warps per KV head that hold work (the last CTA may hold fewer)
   int64_t total_chunks;  // chunks per KV head over all requests
   int32_t* dev_status;
+  // tries of a warp's wait for a stage's data before it gives up (VC_DEV_TIMEOUT); its drain of the
+  // copies still in flight then waits with the full kSpinLimit
+  uint32_t spin_limit;
   // 1: the kernel may stream queries, kept rows and indices before the previous kernel in the
   // stream has finished (set when that kernel is not a compress); it waits for it before reading
   // window rows, storing the step's row and writing any output.

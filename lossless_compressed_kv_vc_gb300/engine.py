@@ -216,7 +216,7 @@ class Batch:
         vc_verify_attn(self.shape, self._verify_arr, self.ws_verify, self.dev_status, stream)
         accept(logits, draft, L, out_tokens, n_acc, stream)
 
-    def run_round_from_host(self, hr: "HostRound", stream, copy_stream, draft_events=None):
+    def run_round_from_host(self, hr: "HostRound", stream, copy_stream, draft_events=None, compress=True):
         """One round whose inputs sit in pinned host memory and whose results go back to it.
 
         All of the round's inputs cross the host link on `copy_stream` into the next of the
@@ -237,7 +237,8 @@ class Batch:
                 d.copy_(h, non_blocking=True)
         sl.landed.record(copy_stream)
         stream.wait_event(sl.ready)
-        self.compress(stream, importance=sl.importance)
+        if compress:
+            self.compress(stream, importance=sl.importance)
         if draft_events is not None:
             draft_events[0].record(stream)
         for shape, arr, act in sl.steps:
