@@ -55,8 +55,9 @@ def parse():
                          "headline workload's contexts from a 32-token observation window")
     ap.add_argument("--window", type=int, default=32, help="importance workload: observation window")
     ap.add_argument("--timeline", default=None,
-                    help="mixed workload: write the first periods' CUDA-event intervals (draft calls, verification, "
-                         "staging copies; ms from the start of the timed region) to this JSON file")
+                    help="mixed workload: write every timed period's CUDA-event intervals (draft calls, verification, "
+                         "staging copies; ms from the start of the timed region) and the host's issue times to this "
+                         "JSON file")
     ap.add_argument("--ctx-div", type=int, default=1,
                     help="offload workload: divide the context (a smaller case for profiler captures)")
     ap.add_argument("--compact", action="store_true",
@@ -279,7 +280,10 @@ def run_reference(args):
 # native leg
 # ------------------------------------------------------------------------------------------------
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs. Entering waits
+    (up to 5 s) for the first sample, so that nvidia-smi's start-up (NVML initialisation, which can
+    hold up GPU work for tens of ms) happens before the timed region; the summary uses the samples
+    taken after that."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
@@ -287,26 +291,41 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.p = None
+        self.lines = []
+        self._all = []
+
+    def _read(self):
+        for line in self.p.stdout:
+            if line.strip():
+                self._all.append(line)
 
     def __enter__(self):
+        import threading
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
                                        "--format=csv,noheader,nounits", "-lms", "200"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.p = None
+            return self
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        t0 = time.time()
+        while not self._all and time.time() - t0 < 5.0 and self.p.poll() is None:
+            time.sleep(0.02)
+        self._mark = len(self._all)
         return self
 
     def __exit__(self, *a):
-        self.lines = []
         if self.p is not None:
             self.p.terminate()
             try:
-                out, _ = self.p.communicate(timeout=5)
+                self.p.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.p.kill()
-                out, _ = self.p.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                self.p.wait()
+            self._t.join(timeout=5)
+            self.lines = self._all[self._mark:]
 
     def summary(self):
         sm, mx, reasons = [], [], set()
@@ -652,9 +671,13 @@ def run_mixed(args):
         torch.cuda.synchronize()
         e0.record(ks)
         cs.wait_event(e0)
+        h0 = time.perf_counter()
+        host_t = []
         for k in range(args.steps):
+            host_t.append((time.perf_counter() - h0) * 1e3)
             sg.period(io, evs[k])
         e1.record(ks)
+        host_ms = (time.perf_counter() - h0) * 1e3  # the host's time to issue every call of the timed periods
         torch.cuda.synchronize()
     t_ms = e0.elapsed_time(e1)
     for bts in groups:
@@ -698,10 +721,11 @@ def run_mixed(args):
     launches = sum(len(bt._steps) + 2 * args.head_chunks + 2 for bts in groups for bt in bts)
     overlap = statistics.mean(_covered(iv, comp_iv) for iv in copy_iv) if copy_iv else None
     if args.timeline:
-        tl = [{"period": k, "draft": [[rel(a), rel(b_)] for gi in (0, 1) for a, b_ in evs[k]["draft%d" % gi]],
+        tl = [{"period": k, "host_issue_start_ms": host_t[k],
+               "draft": [[rel(a), rel(b_)] for gi in (0, 1) for a, b_ in evs[k]["draft%d" % gi]],
                "verify": [[rel(evs[k]["verify%d" % gi][0]), rel(evs[k]["verify%d" % gi][1])] for gi in (0, 1)],
                "stage": [[rel(evs[k]["stage%d" % gi][0]), rel(evs[k]["stage%d" % gi][1])] for gi in (0, 1)]}
-              for k in range(min(3, args.steps))]
+              for k in range(args.steps)]
         json.dump({"t_ms": t_ms, "steps": args.steps, "periods": tl}, open(args.timeline, "w"))
 
     # --- end to end through the engine's host-input period: every period copies each batch's
@@ -738,6 +762,7 @@ def run_mixed(args):
                        "L_min": min(w.L), "L_max": w.L_max, "V": w.V, "bits": w.bits,
                        "requests_token_drop": sum(m == DROP for m in w.mode), "requests_on_host": sum(w.on_host),
                        "tokens_per_step": tokens, "groups": split, "head_chunks": args.head_chunks,
+                       "host_issue_ms_per_step": host_ms / args.steps,
                        "step": "one staggering period: every request drafts its L steps (one draft call per mode "
                                "and step), host-resident KV_full is staged, every request is verified and accepted",
                        "l2": "inputs larger than L2 (full KV %.1f GB, per draft step up to %.2f GB of KV_comp, logits "

@@ -35,9 +35,12 @@
 
 namespace vc {
 
-// KIND 0: bf16 rows (token drop); 2 or 4: quantised, bits. Three 4-warp CTAs per SM with a 2-stage
-// ring per warp (measured better than 2 CTAs x 3 stages or 1 CTA x 6 stages: more warps in flight
-// beat deeper rings).
+// KIND 0: bf16 rows (token drop); 2 or 4: quantised, bits. A 2-stage ring per warp (measured better
+// than 3 stages with fewer CTAs: more warps in flight beat deeper rings). Token drop: three 4-warp
+// CTAs per SM, a stage holds a 16-row K and V tile. Quantised: a stage holds one chunk of quantised
+// groups (6 KB at d 128), and a window chunk -- only at the end of a warp's range -- takes the
+// whole ring (WIN_SPANS: it is issued once nothing else is in flight), so four CTAs (16 warps) fit
+// per SM: the quantised steps are bound by instruction latency, and more warps hide more of it.
 template <int D, int KIND>
 struct DraftCfg {
   static constexpr int NW = 4;
@@ -47,14 +50,15 @@ struct DraftCfg {
   static constexpr int TILE = HALVES * BLK;              // 16 bf16 rows (swizzled column blocks)
   static constexpr int BITS = (KIND == 0) ? 2 : KIND;
   static constexpr int QRAW = (KIND == 0) ? 0 : 8 * D * (BITS + 1);  // raw bytes of one 32-token group
-  static constexpr int STAGE = ((2 * TILE > QRAW ? 2 * TILE : QRAW) + 1023) / 1024 * 1024;
+  static constexpr int GPC = (KIND == 2) ? 2 : 1;       // quantised groups per chunk (two 2-bit groups fit a stage)
+  static constexpr int STAGE = (KIND == 0 ? 2 * TILE : GPC * QRAW + 1023) / 1024 * 1024;
   static constexpr int NST = 2;
-  static constexpr int CTAS_PER_SM = 3;
+  static constexpr bool WIN_SPANS = STAGE < 2 * TILE;   // a window tile needs more than one stage
+  static constexpr int CTAS_PER_SM = (KIND == 0) ? 3 : 4;
   static constexpr int PER_WARP = NST * STAGE;
   static constexpr int BAR_OFF = NW * PER_WARP;
   static constexpr int SMEM = BAR_OFF + NW * NST * 8 + 1024;  // + slack to put the stages on 1024 B
   static constexpr int G4_OPS = 2 * HALVES * 4;          // gather4 loads that fill a 16-row K+V stage
-  static constexpr int GPC = (KIND == 2) ? 2 : 1;       // quantised groups per chunk (two 2-bit groups fit a stage)
   static constexpr int CHUNK_MAIN = (KIND == 0) ? 16 : 32 * GPC;
   static constexpr int MT = D / 16;                      // 16-wide tiles over the head dim
   // raw layout of a quantised group inside a stage
@@ -67,6 +71,8 @@ struct DraftCfg {
   static constexpr int OFF_VZ = OFF_VS + 2 * D;
   static_assert(SMEM + 1024 <= 228 * 1024 / CTAS_PER_SM, "CTAs per SM");
   static_assert(GPC * QRAW <= STAGE && QRAW % 16 == 0, "quantised groups of a chunk in one stage");
+  static_assert(NST * STAGE >= 2 * TILE, "a window tile fits the ring");
+  static_assert(PER_WARP >= 16 * (D + 1) * 4, "a warp's partial fits its drained ring");
 };
 
 // Tensor maps are an argument of the token-drop kernels only.
@@ -769,6 +775,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       return;
     }
     ensure_wait();  // window rows: the previous step appended one
+    if constexpr (C::WIN_SPANS) sb = wb;  // a window tile takes the whole ring (issued when it is empty)
     // 16 bf16 rows: lane & 15 names the row; lanes 0-15 own its K row, lanes 16-31 its V row
     const bool isv = lane >= 16;
     const bf16* src = nullptr;
@@ -887,13 +894,25 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   };
 
   bool aborted = false;
-  const int pre = n < C::NST ? n : C::NST;
-  for (int i = 0; i < pre; ++i) issue(i, i, row_of(i));
-  for (int i = pre; i < C::NST; ++i) cp_async_commit();  // one group per stage in flight
+  // Chunks are issued in order, NST ahead; chunk k completes on bars[k % NST]. When a window tile
+  // spans the ring (WIN_SPANS), the warp's window chunks (they follow all its KV_comp chunks) are
+  // issued one at a time, each once the chunk before it has been read.
+  int iw = n;  // the warp's first window chunk
+  if constexpr (C::WIN_SPANS) {
+    const int64_t first_win = (int64_t)s_cb[rb] + p.req[rb].n_mc - p0;
+    iw = first_win < 0 ? 0 : (first_win < n ? (int)first_win : n);
+  }
+  int issued = 0;
+  while (issued < n && issued < C::NST && (issued < iw || issued == 0)) {
+    issue(issued, issued, row_of(issued));
+    ++issued;
+  }
+  for (int k = issued; k < C::NST; ++k) cp_async_commit();  // one group per stage in flight
 #pragma unroll 1
   for (int i = 0; i < n; ++i) {
     const int st = i % C::NST;
-    const int t_next = (i + C::NST < n) ? row_of(i + C::NST) : -1;  // prefetch: consumed after this chunk
+    const bool win_span = C::WIN_SPANS && i >= iw;
+    const int t_next = (!C::WIN_SPANS && i + C::NST < n) ? row_of(i + C::NST) : -1;  // prefetch: used after this chunk
     int b, lc;
     locate(i, b, lc, cur_proc);
     if (b != cur_b) {
@@ -920,18 +939,21 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         }
       }
     }
-    cp_async_wait<C::NST - 1>();  // this lane's copies of chunk i have landed
-    __syncwarp();                  // ... and every other lane's
+    if (win_span)
+      cp_async_wait<0>();            // nothing else is in flight: all this lane's copies
+    else
+      cp_async_wait<C::NST - 1>();   // this lane's copies of chunk i have landed
+    __syncwarp();                    // ... and every other lane's
     if (!mbar_wait_bounded(&bars[st], (i / C::NST) & 1, p.dev_status, p.spin_limit)) {
-      // give up on this range, but not on the copies already issued into the ring (this stage's
+      // give up on this range, but not on the copies already issued into the ring (this chunk's
       // and the ones after it): wait for them with the full bound so that no copy is still
       // writing shared memory when the CTA exits
-      for (int j = i; j < n && j < i + C::NST; ++j) mbar_wait_bounded(&bars[j % C::NST], (j / C::NST) & 1, p.dev_status);
+      for (int j = i; j < issued; ++j) mbar_wait_bounded(&bars[j % C::NST], (j / C::NST) & 1, p.dev_status);
       aborted = true;
       break;
     }
     const DraftReqDev& r = p.req[b];
-    uint8_t* sb = wb + st * C::STAGE;
+    uint8_t* sb = win_span ? wb : wb + st * C::STAGE;
     if (!BF16_ROWS && lc < r.n_mc) {
       qblock_attend<D, C::BITS, NHB>(sb, scale_q, qb, o, m, l, zs, lane);
       if (C::GPC == 2 && C::GPC * lc + 1 < q_ng)
@@ -950,9 +972,14 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       tile_attend<D, NHB>(sb, sb + C::TILE, cnt, p.scale_log2, qb, o, m, l, lane);
     }
     __syncwarp();
-    if (i + C::NST < n) {
+    // next issue: a KV_comp chunk into the stage just read (NST ahead), or -- spanning the ring --
+    // a window chunk once this was the last chunk in flight
+    const bool go = C::WIN_SPANS ? (issued < n && (issued < iw ? issued == i + C::NST : issued == i + 1))
+                                 : (i + C::NST < n);
+    if (go) {
       fence_proxy_async_smem();  // this warp's reads of the stage come before the TMA overwrites it
-      issue(i + C::NST, st, t_next);
+      issue(issued, issued % C::NST, C::WIN_SPANS ? row_of(issued) : t_next);
+      ++issued;
     } else {
       cp_async_commit();  // empty group: the wait above always leaves NST-1 groups pending
     }
@@ -1040,7 +1067,10 @@ static cudaError_t launch_draft_g(const DraftParams& p, const DraftMaps* maps, i
                   : launch_draft_t<D, KIND, 2>(p, maps, ctas_per_head, s);
 }
 
-int draft_ctas_per_sm(int G) { return G <= 8 ? DraftCfg<128, 0>::CTAS_PER_SM : 2; }
+int draft_ctas_per_sm(int G, int kind) {
+  if (G > 8) return 2;
+  return kind == 0 ? DraftCfg<128, 0>::CTAS_PER_SM : DraftCfg<128, 2>::CTAS_PER_SM;
+}
 
 cudaError_t launch_draft(const DraftParams& p, const DraftMaps* maps, int d, int kind, int ctas_per_head,
                          cudaStream_t s) {

@@ -40,13 +40,13 @@ static int sm_count() {
 }
 
 namespace vc {
-int draft_ctas_per_sm(int G);
+int draft_ctas_per_sm(int G, int kind);
 }
 
 // CTAs per KV head of a draft launch: one wave of CTAs over all heads (the workspace bound takes
-// the largest wave, G <= 8).
-static int draft_ctas_per_head_max(int Hkv, int G = 1) {
-  const int n = vc::draft_ctas_per_sm(G) * sm_count() / Hkv;
+// the largest wave of any kind, G <= 8 and quantised).
+static int draft_ctas_per_head_max(int Hkv, int G = 1, int kind = 2) {
+  const int n = vc::draft_ctas_per_sm(G, kind) * sm_count() / Hkv;
   return n > 1 ? n : 1;
 }
 
@@ -418,7 +418,7 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   // two requests; warps left over go, a whole tier at a time, to the requests with the largest
   // chunks-per-warp load, and only while that lowers it.
   const int kind = mode == VC_TOKEN_DROP ? 0 : bits;
-  int P = draft_ctas_per_head_max(Hkv, G);
+  int P = draft_ctas_per_head_max(Hkv, G, kind);
   const int env = env_int("VC_DRAFT_CTAS", 0);
   if (env > 0 && env / Hkv < P) P = env / Hkv > 1 ? env / Hkv : 1;
   const int64_t by_work = (total + 4 * kDraftWarps - 1) / (4 * kDraftWarps);
