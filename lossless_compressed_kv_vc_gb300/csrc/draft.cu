@@ -239,11 +239,23 @@ __device__ __forceinline__ void code_offsets(uint32_t (&a)[4]) {
 // that each code sits at an odd bit position P' (P' + BITS <= 9): 2^(10-P') + C0 is then exact in
 // fp16 (a half-integer needs an ulp <= 0.5, i.e. 2^(10-P') <= 512), and one HSUB2 per register
 // leaves code - C0 exactly.
+// fp16 bits of 2^E + C0 (C0 = (2^BITS - 1) / 2), both halves of the pair, as a compile-time
+// immediate: exponent field E + 15, fraction field C0 * 2^(10-E) (an integer when the value is
+// exact in fp16, which the assertion checks).
+template <int BITS, int E>
+__host__ __device__ constexpr uint32_t centre_f16x2() {
+  constexpr uint32_t c0x2 = (1u << BITS) - 1u;           // 2 C0 (an integer)
+  constexpr uint32_t frac = (c0x2 << 10) >> (E + 1);    // C0 * 2^(10-E)
+  static_assert(((c0x2 << 10) % (1u << (E + 1))) == 0, "2^E + C0 exact in fp16");
+  constexpr uint32_t h = ((uint32_t)(E + 15) << 10) | frac;
+  return h | (h << 16);
+}
+
 template <int BITS, int P>
 __device__ __forceinline__ uint32_t code_centred_f16x2(uint32_t w) {
-  constexpr float c = (float)(1 << (10 - P)) + 0.5f * (float)((1 << BITS) - 1);
+  constexpr uint32_t cb = centre_f16x2<BITS, 10 - P>();
   const uint32_t x = code_f16x2<BITS, P>(w);
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&x), __float2half2_rn(c));
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&x), *reinterpret_cast<const __half2*>(&cb));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
@@ -414,7 +426,8 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
     const int t0 = 16 * half + a8, t1 = t0 + 8;
     // the scales and zeros of all D/32 channel groups of tokens t0 and t1 (adjacent in the block);
     // the zeros take the centring: z + C0 s (fp16, one rounding of a value of the data's size)
-    const __half2 c0h = __float2half2_rn(0.5f * (float)((1 << BITS) - 1));
+    constexpr uint32_t c0b = BITS == 2 ? 0x3E003E00u : 0x47804780u;  // fp16 1.5 / 7.5, both halves
+    const __half2 c0h = *reinterpret_cast<const __half2*>(&c0b);
     __half2 vs0[D / 64], vs1[D / 64], vz0[D / 64], vz1[D / 64];
 #pragma unroll
     for (int k = 0; k < D / 64; ++k) {

@@ -41,7 +41,8 @@ struct VerifyReqDev {
   const bf16* q;
   bf16* o;
   int32_t ctx, n_rows, mtiles, n_full, tiles;
-  int32_t unit_begin;
+  int32_t unit_begin;   // first (KV head, row tile) unit of the request
+  int32_t ug_begin;     // row-tile mode: first (KV head) unit of the request
   int64_t tile_begin;
   // row-statistics / column-sum modes (the importance votes): lse [Hkv][mtiles * 128] (written by
   // the statistics pass, read by the votes pass) and votes [Hkv * mtiles][ctx + n_rows]
@@ -50,14 +51,20 @@ struct VerifyReqDev {
 };
 
 // Kernel modes: attention (verification), the rows' log-sum-exp only, and the column sums of the
-// normalised weights (sum over the tile's rows of 2^(s - lse) for every key).
-constexpr int VMODE_ATTN = 0, VMODE_STATS = 1, VMODE_VOTES = 2;
+// normalised weights (sum over the tile's rows of 2^(s - lse) for every key). VMODE_ROWS (opt-in,
+// VC_VERIFY_ROWS=1) is attention with every 128-row tile of a (request, KV head) in one CTA: a
+// unit is the KV head, each K/V tile is loaded once and serves all its row tiles (up to VROWS), one
+// O accumulator per row tile in TMEM. By default a KV head with more than 128 rows (L x G > 128) is
+// one unit per row tile and streams its K and V once per row tile.
+constexpr int VMODE_ATTN = 0, VMODE_STATS = 1, VMODE_VOTES = 2, VMODE_ROWS = 3;
+constexpr int VROWS = 3;  // row tiles a row-tile-mode CTA holds (3 x 128 O columns + S fill TMEM)
 
 struct VerifyParams {
   CUtensorMap tm[VC_MAX_BATCH][4];  // K full, V full, K new, V new
   VerifyReqDev req[VC_MAX_BATCH];
   int32_t B, Hq, Hkv, G, n_cta, n_units;
   int32_t h0;  // first KV head of the call's head range (units cover heads h0 .. h0 + nh - 1)
+  int32_t rows;  // 1: row-tile mode (the tile sequence runs over (request, KV head), all row tiles per unit)
   int64_t total_tiles;
   float scale_log2;
   float* ws_o;    // [slots][128][d]
@@ -65,20 +72,21 @@ struct VerifyParams {
   int32_t* dev_status;
 };
 
-template <int D>
+template <int D, int NQ = 1>
 struct VCfg {
   static constexpr int KB = D / 64;                // 64-channel (128-byte) blocks
-  static constexpr int Q_BYTES = KB * VM * 128;    // Q tile, K-major SW128
+  static constexpr int Q_BYTES = KB * VM * 128;    // Q tile, K-major SW128 (NQ of them)
   static constexpr int P_BYTES = VM * 128;         // P tile (64 tokens), K-major SW128
   static constexpr int KV_BYTES = KB * VBN * 128;  // one K (or V) tile
-  static constexpr int OFF_P = Q_BYTES;
+  static constexpr int OFF_P = NQ * Q_BYTES;
   static constexpr int OFF_K = OFF_P + P_BYTES;    // K stages [2]
   static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;  // V stages [2]
   static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr int SMEM = OFF_BAR + 256;
   static constexpr int SCOL = 64;                  // S double buffer: TMEM columns [0,64) and [64,128)
-  static constexpr int OCOL = 128;                 // O: TMEM columns [128, 128 + D)
-  static constexpr uint32_t TCOLS = 256;
+  static constexpr int OCOL = 128;                 // O: TMEM columns [128, 128 + D) (row tile m: + m D)
+  static constexpr uint32_t TCOLS = NQ == 1 ? 256 : 512;
+  static_assert(OCOL + NQ * D <= (int)TCOLS, "O accumulators fit the TMEM allocation");
   static constexpr int THREADS = 192;              // warps 0-3 softmax, 4 MMA issue, 5 TMA loads
   // votes mode: an fp16 all-ones [128][128] A operand over the (unused) V stages
   static constexpr int ONES_BYTES = VM * 128 * 2;
@@ -123,8 +131,8 @@ __device__ __forceinline__ VPiece verify_piece(const VerifyParams& p, int64_t po
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_constant__ VerifyParams p) {
-  using C = VCfg<D>;
+__global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_kernel(const __grid_constant__ VerifyParams p) {
+  using C = VCfg<D, MODE == VMODE_ROWS ? VROWS : 1>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte aligned tiles
@@ -204,11 +212,11 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
       bool ok = true;
       for (int64_t pos = beg; pos < end && ok;) {
         const VPiece q = verify_piece(p, pos, end);
-        const int hk = p.h0 + q.ul / p.req[q.b].mtiles;
+        const int hk = p.h0 + (MODE == VMODE_ROWS ? q.ul : q.ul / p.req[q.b].mtiles);
         for (int j = q.j0; j < q.j1 && ok; ++j, ++g) {
           ok = load(false, gk, q.b, hk, j);
           if (ok) ++gk;
-          if (MODE == VMODE_ATTN && ok && pv_pending) {
+          if ((MODE == VMODE_ATTN || MODE == VMODE_ROWS) && ok && pv_pending) {
             ok = load(true, gv, pv_b, pv_hk, pv_j);
             if (ok) ++gv;
           }
@@ -216,7 +224,7 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
         }
         pos += q.j1 - q.j0;
       }
-      if (MODE == VMODE_ATTN && ok && pv_pending && load(true, gv, pv_b, pv_hk, pv_j)) ++gv;
+      if ((MODE == VMODE_ATTN || MODE == VMODE_ROWS) && ok && pv_pending && load(true, gv, pv_b, pv_hk, pv_j)) ++gv;
       if (*s_abort) {
         // drain (bounded): the loads of the last two tiles of each kind may still be landing
         for (uint32_t gi = (gk > 2 ? gk - 2 : 0); gi < gk; ++gi) mbar_wait_bounded(&kfull[gi & 1], (gi >> 1) & 1, p.dev_status);
@@ -265,7 +273,61 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
         tc05::commit(&vempty[gp & 1]);
         return true;
       };
-      for (int64_t pos = beg; pos < end && ok;) {
+      // row-tile mode: steps are (KV tile, row tile) pairs, S of step v before P V of step v - 1;
+      // a K stage is released after its last row tile's S, a V stage after its last row tile's P V
+      uint32_t vg = 0;  // steps issued
+      auto issue_pv_rows = [&](uint32_t vp, uint32_t gp, int m, bool first_v, bool last_v, bool acc) -> bool {
+        if (!vwait(pfull, vp & 1, p.dev_status, s_abort)) return false;
+        if (first_v && !vwait(&vfull[gp & 1], (gp >> 1) & 1, p.dev_status, s_abort)) return false;
+        tc05::fence_after();
+        const uint32_t vaddr = aV + (gp & 1) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < VBN / 16; ++kk) {
+          const uint64_t da = tc05::sdesc_sw128(aP + kk * 32, 16, 1024);
+          const uint64_t db = tc05::sdesc_sw128(vaddr + kk * 2048, VBN * 128, 1024);
+          tc05::mma_bf16(tmem + C::OCOL + m * D, da, db, IDESC_O, (acc || kk > 0) ? 1u : 0u);
+        }
+        tc05::commit(ofull);
+        if (last_v) tc05::commit(&vempty[gp & 1]);
+        return true;
+      };
+      for (int64_t pos = beg; pos < end && ok && MODE == VMODE_ROWS;) {
+        const VPiece q = verify_piece(p, pos, end);
+        const int nt = q.j1 - q.j0, mt = p.req[q.b].mtiles;
+        ok = vwait(qfull, u & 1, p.dev_status, s_abort);
+        ++u;
+        bool pend = false, pv_first = false, pv_last = false, pv_acc = false;
+        uint32_t pv_v = 0, pv_g = 0;
+        int pv_m = 0;
+        for (int jj = 0; jj < nt && ok; ++jj) {
+          const uint32_t gc = g + jj;
+          if (!vwait(&kfull[gc & 1], (gc >> 1) & 1, p.dev_status, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          const uint32_t kaddr = aK + (gc & 1) * C::KV_BYTES;
+          for (int m = 0; m < mt && ok; ++m) {
+            const uint32_t vc = vg++;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t da =
+                  tc05::sdesc_sw128(aQ + m * C::Q_BYTES + (kk >> 2) * (VM * 128) + (kk & 3) * 32, 16, 1024);
+              const uint64_t db = tc05::sdesc_sw128(kaddr + (kk >> 2) * (VBN * 128) + (kk & 3) * 32, 16, 1024);
+              tc05::mma_bf16(tmem + (vc & 1) * C::SCOL, da, db, IDESC_S, kk > 0);
+            }
+            tc05::commit(&sfull[vc & 1]);
+            if (m == mt - 1) tc05::commit(&kempty[gc & 1]);
+            if (pend) ok = issue_pv_rows(pv_v, pv_g, pv_m, pv_first, pv_last, pv_acc);
+            pend = true;
+            pv_v = vc, pv_g = gc, pv_m = m, pv_first = m == 0, pv_last = m == mt - 1, pv_acc = jj > 0;
+          }
+        }
+        if (ok && pend) ok = issue_pv_rows(pv_v, pv_g, pv_m, pv_first, pv_last, pv_acc);
+        g += nt;
+        pos += nt;
+      }
+      for (int64_t pos = beg; pos < end && ok && MODE != VMODE_ROWS;) {
         const VPiece q = verify_piece(p, pos, end);
         const int nt = q.j1 - q.j0;
         ok = vwait(qfull, u & 1, p.dev_status, s_abort);
@@ -301,7 +363,189 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     uint32_t g = 0;
     bool ok = true;
-    for (int64_t pos = beg; pos < end && ok;) {
+    // row-tile mode: thread tid owns row tid of every row tile of the unit; steps (KV tile, row
+    // tile) in the MMA warp's order, one running maximum and sum per row tile
+    uint32_t vg = 0;  // steps consumed
+    for (int64_t pos = beg; pos < end && ok && MODE == VMODE_ROWS;) {
+      const VPiece q = verify_piece(p, pos, end);
+      const VerifyReqDev& R = p.req[q.b];
+      const int nt = q.j1 - q.j0, mt = R.mtiles;
+      const int hk = p.h0 + q.ul;
+      const int ug_global = R.ug_begin + q.ul;
+      // this thread's query row of each row tile into its swizzled Q tile (the previous unit's MMAs
+      // are complete: its epilogue waited for the last P V, which follows every S of the unit)
+      for (int m = 0; m < mt; ++m) {
+        const int Rw = m * VM + tid, qi = Rw / p.G, qg = Rw % p.G;
+        const bool row_ok = qi < R.n_rows;
+        const uint4* src = reinterpret_cast<const uint4*>(R.q + ((size_t)qi * p.Hq + hk * p.G + qg) * D);
+        uint8_t* dQ = sQ + m * C::Q_BYTES;
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 v = row_ok ? __ldg(src + kb * 8 + ch) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dQ + kb * (VM * 128) + tid * 128 + ((ch ^ (tid & 7)) << 4)) = v;
+          }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qfull);
+      float mr[VROWS], lr[VROWS];
+#pragma unroll
+      for (int m = 0; m < VROWS; ++m) mr[m] = -INFINITY, lr[m] = 0.f;
+      const uint32_t v0 = vg;
+      for (int jj = 0; jj < nt && ok; ++jj) {
+        const int j = q.j0 + jj;
+        for (int m = 0; m < mt && ok; ++m) {
+          const uint32_t vc = vg++;
+          const int qi = (m * VM + tid) / p.G;
+          if (!vwait(&sfull[vc & 1], (vc >> 1) & 1, p.dev_status, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          float x[VBN];
+          {
+            uint32_t r0[32], r1[32];
+            const uint32_t t_s = tmem + lane_off + (vc & 1) * C::SCOL;
+            tc05::ld32(t_s, r0);
+            tc05::ld32(t_s + 32, r1);
+            tc05::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              x[e] = __uint_as_float(r0[e]);
+              x[32 + e] = __uint_as_float(r1[e]);
+            }
+          }
+          {
+            const int last = j < R.n_full ? R.ctx - j * VBN - 1 : qi - (j - R.n_full) * VBN;  // last visible key
+            if (last < VBN - 1) {
+#pragma unroll
+              for (int e = 0; e < VBN; ++e)
+                if (e > last) x[e] = -INFINITY;
+            }
+          }
+          float mx;
+          {
+            float t[VBN / 2];
+#pragma unroll
+            for (int e = 0; e < VBN / 2; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
+#pragma unroll
+            for (int w = VBN / 4; w >= 1; w >>= 1)
+#pragma unroll
+              for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+            mx = t[0] * p.scale_log2;
+          }
+          float m_run = m == 0 ? mr[0] : (m == 1 ? mr[1] : mr[2]);
+          float l_run = m == 0 ? lr[0] : (m == 1 ? lr[1] : lr[2]);
+          const float m_new = fmaxf(m_run, mx);
+          const bool need = jj > 0 && m_new > m_run + 8.f;
+          if (vc > v0) {
+            // P V of the previous step: the P buffer is free and this row tile's O is stable
+            if (!vwait(ofull, (vc - 1) & 1, p.dev_status, s_abort)) {
+              ok = false;
+              break;
+            }
+            tc05::fence_after();
+          }
+          if (jj == 0) {
+            m_run = m_new;
+          } else {
+            float f = 1.f;
+            if (need) {
+              f = ex2_approx(m_run - m_new);
+              l_run *= f;
+              m_run = m_new;
+            }
+            if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+              for (int cb = 0; cb < D / 32; ++cb) {
+                uint32_t r[32];
+                const uint32_t t_o = tmem + lane_off + C::OCOL + m * D + cb * 32;
+                tc05::ld32(t_o, r);
+                tc05::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                tc05::st32(t_o, r);
+              }
+              tc05::wait_st();
+            }
+          }
+          const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p0 = ex2_approx(fmaf(x[ch * 8 + 2 * e], p.scale_log2, -mu));
+              const float p1 = ex2_approx(fmaf(x[ch * 8 + 2 * e + 1], p.scale_log2, -mu));
+              ls[e] += p0 + p1;
+              w[e] = pack_bf16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(sP + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          if (m == 0) {
+            mr[0] = m_run, lr[0] = l_run;
+          } else if (m == 1) {
+            mr[1] = m_run, lr[1] = l_run;
+          } else {
+            mr[2] = m_run, lr[2] = l_run;
+          }
+          fence_proxy_async_smem();
+          tc05::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pfull);
+        }
+      }
+      if (!ok) break;
+      // outputs: wait for the unit's last P V, then each row tile's O
+      if (!vwait(ofull, (vg - 1) & 1, p.dev_status, s_abort)) {
+        ok = false;
+        break;
+      }
+      tc05::fence_after();
+      g += nt;
+      const bool whole = (q.j0 == 0 && q.j1 == R.tiles);
+#pragma unroll 1
+      for (int m = 0; m < mt; ++m) {
+        const int Rw = m * VM + tid, qi = Rw / p.G, qg = Rw % p.G;
+        const bool row_ok = qi < R.n_rows;
+        const float l_run = m == 0 ? lr[0] : (m == 1 ? lr[1] : lr[2]);
+        const float m_run = m == 0 ? mr[0] : (m == 1 ? mr[1] : mr[2]);
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const size_t slot = (size_t)(c + ug_global) * VROWS + m;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t r[32];
+          tc05::ld32(tmem + lane_off + C::OCOL + m * D + cb * 32, r);  // warp-collective: every lane loads
+          tc05::wait_ld();
+          if (!row_ok) continue;
+          if (whole) {
+            uint4* dst = reinterpret_cast<uint4*>(R.o + ((size_t)qi * p.Hq + hk * p.G + qg) * D + cb * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * e]) * inv, __uint_as_float(r[8 * v + 2 * e + 1]) * inv);
+              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * VM + tid) * D + cb * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                   __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+          }
+        }
+        if (row_ok && !whole) p.ws_lse[slot * VM + tid] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+      }
+      tc05::fence_before();
+      pos += nt;
+    }
+    for (int64_t pos = beg; pos < end && ok && MODE != VMODE_ROWS;) {
       const VPiece q = verify_piece(p, pos, end);
       const VerifyReqDev& R = p.req[q.b];
       const int nt = q.j1 - q.j0;
@@ -529,7 +773,7 @@ __global__ void __launch_bounds__(192, 2) verify_attn_kernel(const __grid_consta
           else
             p.ws_lse[(size_t)(c + u_global) * VM + tid] = lse;
         }
-      } else {
+      } else if constexpr (MODE == VMODE_VOTES) {
         // votes: P = 2^(s scale - lse) (0 for padding rows and invisible keys) in fp16 for the
         // column-sum MMA; warp 0 reads each tile's sums (every row of them is the same) and stores
         // the keys' votes of this 128-row tile
@@ -639,24 +883,30 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_consta
     if (p.req[i].unit_begin <= u) b = i;
   const VerifyReqDev& R = p.req[b];
   const int ul = u - R.unit_begin;
-  const int64_t U0 = R.tile_begin + (int64_t)ul * R.tiles, U1 = U0 + R.tiles;
+  // the unit's tiles in the call's tile sequence: per (KV head, row tile), or in row-tile mode per
+  // KV head (its row tiles share the tiles); a CTA c that held part of it left its partial in slot
+  // c + unit (row-tile mode: (c + KV-head unit) * VROWS + row tile)
+  const int hl = ul / R.mtiles, mt = ul % R.mtiles;
+  const int64_t U0 = R.tile_begin + (int64_t)(p.rows ? hl : ul) * R.tiles, U1 = U0 + R.tiles;
   const int64_t T = p.total_tiles, N = p.n_cta;
   const int64_t c0 = ((U0 + 1) * N - 1) / T, c1 = (U1 * N - 1) / T;
   if (c0 == c1) return;
   const int r = blockIdx.y * 8 + (threadIdx.x / TPR), cc = (threadIdx.x % TPR) * CPT;
-  const int hk = p.h0 + ul / R.mtiles, mt = ul % R.mtiles;
+  const int hk = p.h0 + hl;
   const int Rw = mt * VM + r, qi = Rw / p.G, qg = Rw % p.G;
   if (qi >= R.n_rows) return;
+  auto slot_of = [&](int64_t c) -> int64_t { return p.rows ? (c + R.ug_begin + hl) * VROWS + mt : c + u; };
   float M = -INFINITY;
-  for (int64_t c = c0; c <= c1; ++c) M = fmaxf(M, p.ws_lse[(c + u) * VM + r]);
+  for (int64_t c = c0; c <= c1; ++c) M = fmaxf(M, p.ws_lse[slot_of(c) * VM + r]);
   const float Mu = M == -INFINITY ? 0.f : M;
   float L = 0.f, acc[CPT];
 #pragma unroll
   for (int e = 0; e < CPT; ++e) acc[e] = 0.f;
 #pragma unroll 4
   for (int64_t c = c0; c <= c1; ++c) {
-    const float w = exp2f(p.ws_lse[(c + u) * VM + r] - Mu);
-    const float* src = p.ws_o + ((c + u) * VM + r) * D + cc;
+    const int64_t sl = slot_of(c);
+    const float w = exp2f(p.ws_lse[sl * VM + r] - Mu);
+    const float* src = p.ws_o + (sl * VM + r) * D + cc;
     L += w;
     if (CPT == 4) {
       const float4 v = *reinterpret_cast<const float4*>(src);
@@ -710,9 +960,9 @@ static int sm_count_v() {
   return n;
 }
 
-static int64_t verify_ctas(int64_t T) {
+static int64_t verify_ctas(int64_t T, int per_sm = 2) {
   const char* e = getenv("VC_VERIFY_CTAS");
-  int64_t n = e ? atoll(e) : 2 * (int64_t)sm_count_v();
+  int64_t n = e ? atoll(e) : per_sm * (int64_t)sm_count_v();
   if (n < 1) n = 1;
   return n < T ? n : T;
 }
@@ -722,13 +972,19 @@ size_t verify_workspace_size(const vc_shape* s, int32_t max_rows) {
   const int G = s->Hq / s->Hkv;
   const int64_t mtiles = ((int64_t)max_rows * G + VM - 1) / VM;
   const int64_t units = (int64_t)s->B * s->Hkv * mtiles;
-  const int64_t slots = units + 2 * (int64_t)sm_count_v() + 8;
+  // CTAs of a launch: two per SM (one in row-tile mode), or VC_VERIFY_CTAS when set
+  const char* ev = getenv("VC_VERIFY_CTAS");
+  const int64_t ctas = ev && atoll(ev) > 2 * (int64_t)sm_count_v() ? atoll(ev) : 2 * (int64_t)sm_count_v();
+  int64_t slots = units + ctas + 8;
+  // row-tile mode: VROWS slots per (CTA + KV-head unit)
+  const int64_t rslots = ((int64_t)s->B * s->Hkv + ctas + 8) * VROWS;
+  if (rslots > slots) slots = rslots;
   return (size_t)slots * VM * (s->d + 1) * sizeof(float) + 256;
 }
 
 template <int D, int MODE>
 static cudaError_t launch_modes_t(const VerifyParams& p, cudaStream_t s) {
-  using C = VCfg<D>;
+  using C = VCfg<D, MODE == VMODE_ROWS ? VROWS : 1>;
   constexpr int SMEM = MODE == VMODE_VOTES ? C::SMEM_VOTES : C::SMEM;
   static std::atomic<uint64_t> attr{0};
   {
@@ -740,7 +996,7 @@ static cudaError_t launch_modes_t(const VerifyParams& p, cudaStream_t s) {
 
 template <int D>
 static cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
-  cudaError_t e = launch_modes_t<D, VMODE_ATTN>(p, s);
+  cudaError_t e = p.rows ? launch_modes_t<D, VMODE_ROWS>(p, s) : launch_modes_t<D, VMODE_ATTN>(p, s);
   if (e != cudaSuccess) return e;
   return launch_pdl(verify_combine_kernel<D>, dim3(p.n_units, VM / 8), dim3(256), 0, s, p);
 }
@@ -857,8 +1113,22 @@ cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h
   const int nh = h1 - h0;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
   p.dev_status = dev_status;
+  // row-tile mode, on request (VC_VERIFY_ROWS=1), when some KV head has more than one 128-row tile
+  // and none more than VROWS. It reads each K/V tile once (1.00x the algorithmic bytes at 320 rows
+  // per KV head against 3.00x), but holding three O accumulators takes all of TMEM, so it runs one
+  // CTA (four softmax warps) per SM and its softmax is latency-bound: measured 1.36x slower at 320
+  // rows and 2x slower on the mixed serving batch than one unit per row tile at two CTAs per SM.
+  int max_mt = 1;
+  for (int b = 0; b < shape->B; ++b) {
+    const int mtb = (req[b].n_rows * G + VM - 1) / VM;
+    if (mtb > max_mt) max_mt = mtb;
+  }
+  {
+    const char* ev = getenv("VC_VERIFY_ROWS");
+    p.rows = max_mt >= 2 && max_mt <= VROWS && ev && atoi(ev) == 1 ? 1 : 0;
+  }
   int64_t tiles = 0;
-  int32_t units = 0, max_rows = 0;
+  int32_t units = 0, ugs = 0, max_rows = 0;
   for (int b = 0; b < shape->B; ++b) {
     const vc_verify_req& r = req[b];
     const vc_kv_full& f = r.full;
@@ -883,15 +1153,17 @@ cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h
     R.n_full = (f.ctx + VBN - 1) / VBN;
     R.tiles = R.n_full + (r.n_rows + VBN - 1) / VBN;
     R.unit_begin = units;
+    R.ug_begin = ugs;
     R.tile_begin = tiles;
     units += nh * R.mtiles;
-    tiles += (int64_t)nh * R.mtiles * R.tiles;
+    ugs += nh;
+    tiles += (int64_t)nh * (p.rows ? 1 : R.mtiles) * R.tiles;
     if (r.n_rows > max_rows) max_rows = r.n_rows;
   }
   p.total_tiles = tiles;
-  p.n_cta = (int32_t)verify_ctas(tiles);
+  p.n_cta = (int32_t)verify_ctas(tiles, p.rows ? 1 : 2);
   p.n_units = units;
-  const size_t slots = (size_t)p.n_cta + units;
+  const size_t slots = p.rows ? ((size_t)p.n_cta + ugs) * VROWS : (size_t)p.n_cta + units;
   const size_t need = slots * VM * (d + 1) * sizeof(float);
   if (!ws || ws_bytes < need || !a16(ws)) {
     *st = VC_ERR_WORKSPACE;

@@ -78,6 +78,29 @@ def test_verify_split_layouts(ctas, monkeypatch):
     _check(w, [0, 1], env_ctas=ctas, monkeypatch=monkeypatch)
 
 
+@pytest.mark.parametrize("ctas", [1, 5, 1000])
+@pytest.mark.parametrize("rows_mode", ["1", "0"])
+def test_verify_row_tiles_split_layouts(ctas, rows_mode, monkeypatch):
+    """More than 128 query rows per KV head (L 40 x G 8 = 320: three row tiles), ragged context:
+    every row tile of a KV head in one CTA, each K/V tile loaded once for all of them (row-tile
+    mode, VC_VERIFY_ROWS=1) and one unit per row tile (the default), cut into
+    one CTA, a few CTAs and one CTA per KV tile, so units split across CTAs merge their partials."""
+    monkeypatch.setenv("VC_VERIFY_ROWS", rows_mode)
+    w = configs.scaled(configs.llama70b_offload4(), ctx_div=256, batch=2)
+    w.ctx = [517, 1000]
+    _check(w, [0, 1], env_ctas=ctas, monkeypatch=monkeypatch)
+
+
+@pytest.mark.parametrize("rows_mode", ["1", "0"])
+def test_verify_row_tiles_mixed_one_and_two(rows_mode, monkeypatch):
+    """One call with KV heads of one row tile (L 25 x G 4 = 100 rows) and of two (L 40: 160 rows):
+    the row-tile mode holds both kinds of units."""
+    monkeypatch.setenv("VC_VERIFY_ROWS", rows_mode)
+    w = configs.scaled(configs.mixed_serving(), ctx_div=32, batch=4)
+    w.L = [25, 40, 33, 32]
+    _check(w, [0, 1, 2, 3])
+
+
 @pytest.mark.parametrize("L,ctx", [(1, 1), (1, 64), (70, 65), (64, 200), (3, 5000)])
 def test_verify_edges(L, ctx):
     """One drafted row, one context token, drafts spanning two tiles, exact tile multiples."""
