@@ -630,6 +630,8 @@ def run_mixed(args):
         assert int(cal.dev_status.item()) == 0
         del cal
     rate_v = ver_bytes / ver_ns
+    ver_alone = {"tflops": sum(verify_b[b][1] for b in range(B)) / ver_ns / 1e3, "gbs": rate_v,
+                 "ms": ver_ns / 1e6}  # every request verified, one call per mode, nothing else running
     host_reqs = [b for b in range(B) if w.on_host[b]]
     rate_s, link_alone = None, None
     if host_reqs:
@@ -783,7 +785,11 @@ def run_mixed(args):
                         "verify": {"ms_per_step": ver_ms / args.steps, "gbs": ver_bytes_p * args.steps / (ver_ms / 1e3) / 1e9,
                                    "frac_of_hbm": ver_bytes_p * args.steps / (ver_ms / 1e3) / 1e9 / hbm,
                                    "tflops": ver_tflops, "tensor_frac_of_bf16_sustained": ver_tflops / bf16,
-                                   "flops_per_step": ver_flops_p}},
+                                   "flops_per_step": ver_flops_p,
+                                   "note": "in-period intervals include waiting for the group's copy; 'alone' is "
+                                           "the same work with nothing else running",
+                                   "alone": {**ver_alone, "frac_of_hbm": ver_alone["gbs"] / hbm,
+                                             "tensor_frac_of_bf16": ver_alone["tflops"] / float(peaks["bf16_tflops"])}}},
             "stage": {"bytes_per_step": stage_bytes_p, "gbs": stage_bytes_p * args.steps / (stage_ms / 1e3) / 1e9
                       if stage_ms else None, "link_alone_gbs": link_alone,
                       "frac_of_link": (stage_bytes_p * args.steps / (stage_ms / 1e3) / 1e9) / link_alone
