@@ -54,6 +54,9 @@ def parse():
                          "a naive split and under the planner's split; importance: SnapKV-style importance of the "
                          "headline workload's contexts from a 32-token observation window")
     ap.add_argument("--window", type=int, default=32, help="importance workload: observation window")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="mixed workload: issue every draft call from the host instead of replaying each batch's "
+                         "draft series as a captured CUDA graph")
     ap.add_argument("--timeline", default=None,
                     help="mixed workload: write every timed period's CUDA-event intervals (draft calls, verification, "
                          "staging copies; ms from the start of the timed region) and the host's issue times to this "
@@ -655,8 +658,10 @@ def run_mixed(args):
     io = engine.group_io(members, logits, draft, Lt)
     torch.cuda.synchronize()
     sg = engine.StaggeredOffload(groups, host_kv, slots, cs, ks, head_chunks=args.head_chunks)
-    for _ in range(args.warmup):
+    for k in range(args.warmup):
         sg.period(io)
+        if k == 0 and not args.no_graphs:
+            sg.capture_drafts()  # each batch's draft series as one CUDA graph (one host launch)
     torch.cuda.synchronize()
     for bts in groups:
         for bt in bts:
@@ -736,8 +741,10 @@ def run_mixed(args):
     hrs = [[engine.HostRound(bt, *io[gi][j], names=("q", "k_new", "v_new")) for j, bt in enumerate(groups[gi])]
            for gi in (0, 1)]
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))
-    for _ in range(2):
+    for k in range(2):
         sg.period(None, host_rounds=hrs)
+        if k == 0 and not args.no_graphs:
+            sg.capture_drafts(host_rounds=hrs)
     torch.cuda.synchronize()
     f0, f1 = mk()
     torch.cuda.synchronize()
@@ -764,7 +771,7 @@ def run_mixed(args):
                        "L_min": min(w.L), "L_max": w.L_max, "V": w.V, "bits": w.bits,
                        "requests_token_drop": sum(m == DROP for m in w.mode), "requests_on_host": sum(w.on_host),
                        "tokens_per_step": tokens, "groups": split, "head_chunks": args.head_chunks,
-                       "host_issue_ms_per_step": host_ms / args.steps,
+                       "host_issue_ms_per_step": host_ms / args.steps, "draft_graphs": not args.no_graphs,
                        "step": "one staggering period: every request drafts its L steps (one draft call per mode "
                                "and step), host-resident KV_full is staged, every request is verified and accepted",
                        "l2": "inputs larger than L2 (full KV %.1f GB, per draft step up to %.2f GB of KV_comp, logits "

@@ -409,6 +409,47 @@ class StaggeredOffload:
         for g in range(2):  # a slot is free before its first copy
             self.verified[g].record(compute_stream)
         self._cur = [None, None]  # host-input periods: the HostRound slot each batch last drafted from
+        self._graphs = {}  # (id of a descriptor-array list) -> CUDA graph of that draft series
+
+    def capture_drafts(self, host_rounds=None):
+        """Capture each batch's draft series (its L_max vc_draft_attn calls, one per step, with the
+        descriptor arrays they use in a period: the batch's own, and those of each HostRound slot
+        when host_rounds is given) as a CUDA graph on the compute stream; phase() then replays the
+        graph instead of issuing the calls one by one. The calls are the same kernels with the same
+        arguments (the arrays are fixed per step); a replay costs the host one launch instead of
+        L_max C-ABI calls, so the host keeps ahead of the GPU. Call it after a first period (the
+        kernels' one-time set-up has run) and before the timed ones."""
+        ks = self.compute_stream
+        series = []
+        for grp in self.groups:
+            for bt in grp:
+                series.append((bt, bt._steps))
+        if host_rounds is not None:
+            for g in range(2):
+                for j, hr in enumerate(host_rounds[g]):
+                    for sl in hr.slots:
+                        series.append((self.groups[g][j], sl.steps))
+        torch.cuda.synchronize()
+        for bt, steps in series:
+            if id(steps) in self._graphs:
+                continue
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=ks):
+                for shape, arr, act in steps:
+                    vc_draft_attn(shape, arr, bt.ws_draft, bt.dev_status, ks)
+            self._graphs[id(steps)] = (graph, steps)
+        torch.cuda.synchronize()
+
+    def _draft(self, bt, steps):
+        """The batch's draft series on the compute stream: a graph replay when captured."""
+        ks = self.compute_stream
+        got = self._graphs.get(id(steps))
+        if got is not None and got[1] is steps:
+            with torch.cuda.stream(ks):
+                got[0].replay()
+            return
+        for shape, arr, act in steps:
+            vc_draft_attn(shape, arr, bt.ws_draft, bt.dev_status, ks)
 
     def stage_bytes(self, g: int) -> int:
         return sum(h.numel() * h.element_size() for h in self.host_kv[g] if h is not None)
@@ -482,8 +523,7 @@ class StaggeredOffload:
                 steps = sl.steps
             if per_batch:
                 draft_events[j][0].record(ks)
-            for shape, arr, act in steps:
-                vc_draft_attn(shape, arr, bt.ws_draft, bt.dev_status, ks)
+            self._draft(bt, steps)
             if per_batch:
                 draft_events[j][1].record(ks)
         if draft_events is not None and not per_batch:

@@ -49,12 +49,13 @@ def test_stage_refuses_device_source(vc):
     assert vc.vc_stage_full_kv(a, b, 4096, 0, None, None, raise_on_error=False) == vc.VC_ERR_NOT_PINNED
 
 
-@pytest.mark.parametrize("head_chunks", [1, 3, 8])
-def test_staggered_offload_period_matches_oracle(vc, head_chunks):
+@pytest.mark.parametrize("head_chunks,graphs", [(1, False), (3, False), (8, False), (1, True)])
+def test_staggered_offload_period_matches_oracle(vc, head_chunks, graphs):
     """Scaled Llama-70B-shape offload workload (4 requests, 64/8 heads, 4-bit): a full period of the
     two-group stagger gives the oracle's draft outputs, verify outputs and accepted tokens, with
     the copy staged whole (1) or a KV-head range at a time and verified range by range (3: uneven
-    ranges of 2, 3 and 3 heads; 8: one head per range)."""
+    ranges of 2, 3 and 3 heads; 8: one head per range), and with each group's draft series
+    replayed from a captured CUDA graph."""
     from lossless_compressed_kv_vc_gb300 import engine
     w = configs.scaled(configs.llama70b_offload4(), ctx_div=64, batch=4, L=6)
     w.V = 5000
@@ -80,6 +81,9 @@ def test_staggered_offload_period_matches_oracle(vc, head_chunks):
         vc.vc_draft_attn(shape, arr, groups[1].ws_draft, groups[1].dev_status, ks)
     ks.synchronize()
     sg = engine.StaggeredOffload(groups, host_kv, slots, cs, ks, chunk_bytes=1 << 20, head_chunks=head_chunks)
+    if graphs:  # each group's draft series replayed as a captured CUDA graph
+        sg.capture_drafts()
+        assert len(sg._graphs) == 2
     sg.period(io)
     torch.cuda.synchronize()
     for gi, bt in enumerate(groups):
