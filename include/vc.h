@@ -382,8 +382,10 @@ size_t vc_importance_workspace_size(const vc_shape* shape, int32_t window, int32
  * the maximum cycle mean of that dependency graph (max-plus algebra):
  *     T(A) = max(D + V, S, S_A + V_A, S_B + V_B, (S + V + D_A) / 2, (S + V + D_B) / 2).
  * T(A) = T(B). The call returns, in group[r] (0 = A, 1 = B), a split of minimum T with request 0
- * in A and, when n >= 2, both groups non-empty; among equal T (compared exactly, as 2T) it takes
- * the smallest sum of group[r] * 2^(r-1) over r >= 1. period_ns (may be NULL) receives T rounded
+ * in A and, when n >= 2, both groups non-empty; among equal T (compared exactly, as 2T) the one
+ * with the smallest longer phase, max(D_A + V_B, D_B + V_A) (balanced phases: a lopsided split
+ * that the model ties with a balanced one measured slower), then the smallest sum of
+ * group[r] * 2^(r-1) over r >= 1. period_ns (may be NULL) receives T rounded
  * up to a whole ns. Exact: all 2^(n-1) - 1 such splits are enumerated in Gray-code order, O(1)
  * each (about 8 M at n = VC_STAGGER_MAX).
  * Errors: VC_ERR_INVALID (null pointers, n < 1, a negative cost or one above 2^40 ns);
@@ -407,7 +409,8 @@ vc_status vc_stagger_period(const vc_stagger_cost* cost, int32_t n, const int32_
  * guarantee: three seeds (first half / second half, alternating, and a greedy pass by decreasing
  * d + s + v that adds each request where the split-dependent part of 2T over the partial sums is
  * lower) are each improved by first-improvement descent over single moves and swaps of one request
- * of each group, compared exactly as 2T; the best result (ties: the earlier seed) is returned. The
+ * of each group, compared exactly as (2T, longer phase) as above; the best result (ties: the
+ * earlier seed) is returned. The
  * returned split is one that no single move and no swap improves, unless a descent reached its
  * limit of 64 n + 1024 improving steps. O(n^2) per improving step; deterministic.
  * Errors: VC_ERR_INVALID (as vc_plan_stagger); VC_ERR_UNSUPPORTED (n > VC_STAGGER_LOCAL_MAX).

@@ -40,6 +40,19 @@ inline int64_t period2(int64_t dA, int64_t sA, int64_t vA, int64_t D, int64_t S,
   return t;
 }
 
+// Tie-break of splits with equal 2T: the longer phase's GPU work, max(D_A + V_B, D_B + V_A) (phase
+// 1 drafts A and verifies B, phase 2 the reverse). The period model cannot tell such splits apart
+// (it is set by a bound they share, often D + V), but a lopsided split leaves one phase with little
+// drafting to cover the other group's copy and with launches of little work; measured on the
+// mixed workload's quantised half at its own draft lengths, request 1 alone in B ran 3.5% slower
+// than halves.
+inline int64_t phase_max(int64_t dA, int64_t vA, int64_t D, int64_t V) {
+  return max64(dA + (V - vA), (D - dA) + vA);
+}
+
+// (2T, phase work) compared lexicographically
+inline bool better(int64_t t, int64_t ph, int64_t bt, int64_t bph) { return t < bt || (t == bt && ph < bph); }
+
 }  // namespace
 
 extern "C" vc_status vc_stagger_period(const vc_stagger_cost* cost, int32_t n, const int32_t* group,
@@ -79,6 +92,7 @@ extern "C" vc_status vc_plan_stagger(const vc_stagger_cost* cost, int32_t n, int
   uint32_t mask = 0, best_mask = 0;
   int64_t dA = D, sA = S, vA = V;
   int64_t best = n == 1 ? period2(dA, sA, vA, D, S, V) : INT64_MAX;
+  int64_t best_ph = n == 1 ? phase_max(dA, vA, D, V) : INT64_MAX;
   for (uint32_t i = 1; i < count; ++i) {
     const int bit = __builtin_ctz(i);
     const vc_stagger_cost& c = cost[bit + 1];
@@ -93,8 +107,10 @@ extern "C" vc_status vc_plan_stagger(const vc_stagger_cost* cost, int32_t n, int
       vA += c.verify_ns;
     }
     const int64_t t = period2(dA, sA, vA, D, S, V);
-    if (t < best || (t == best && mask < best_mask)) {
+    const int64_t ph = phase_max(dA, vA, D, V);
+    if (better(t, ph, best, best_ph) || (t == best && ph == best_ph && mask < best_mask)) {
       best = t;
+      best_ph = ph;
       best_mask = mask;
     }
   }
@@ -127,9 +143,11 @@ void sums_of(Split& sp, const vc_stagger_cost* c, int32_t n) {
 
 // First-improvement descent: scan the single moves (request r to the other group, both groups
 // staying non-empty) in index order, then the swaps (r in A with q in B) in (r, q) order; apply the
-// first that lowers 2T and start over. Stops when none does or after max_steps improvements.
+// first that lowers (2T, phase work) and start over. Stops when none does or after max_steps
+// improvements.
 void descend(Split& sp, const vc_stagger_cost* c, int32_t n, int64_t D, int64_t S, int64_t V, int64_t max_steps) {
   int64_t cur = period2(sp.dA, sp.sA, sp.vA, D, S, V);
+  int64_t cur_ph = phase_max(sp.dA, sp.vA, D, V);
   for (int64_t step = 0; step < max_steps; ++step) {
     bool moved = false;
     for (int32_t r = 0; r < n && !moved; ++r) {
@@ -138,13 +156,15 @@ void descend(Split& sp, const vc_stagger_cost* c, int32_t n, int64_t D, int64_t 
       const int64_t sg = inA ? -1 : 1;
       const int64_t t = period2(sp.dA + sg * c[r].draft_ns, sp.sA + sg * c[r].stage_ns,
                                 sp.vA + sg * c[r].verify_ns, D, S, V);
-      if (t < cur) {
+      const int64_t ph = phase_max(sp.dA + sg * c[r].draft_ns, sp.vA + sg * c[r].verify_ns, D, V);
+      if (better(t, ph, cur, cur_ph)) {
         sp.g[r] ^= 1;
         sp.dA += sg * c[r].draft_ns;
         sp.sA += sg * c[r].stage_ns;
         sp.vA += sg * c[r].verify_ns;
         sp.nA += inA ? -1 : 1;
         cur = t;
+        cur_ph = ph;
         moved = true;
       }
     }
@@ -156,13 +176,15 @@ void descend(Split& sp, const vc_stagger_cost* c, int32_t n, int64_t D, int64_t 
         const int64_t sA = sp.sA - c[r].stage_ns + c[q].stage_ns;
         const int64_t vA = sp.vA - c[r].verify_ns + c[q].verify_ns;
         const int64_t t = period2(dA, sA, vA, D, S, V);
-        if (t < cur) {
+        const int64_t ph = phase_max(dA, vA, D, V);
+        if (better(t, ph, cur, cur_ph)) {
           sp.g[r] = 1;
           sp.g[q] = 0;
           sp.dA = dA;
           sp.sA = sA;
           sp.vA = vA;
           cur = t;
+          cur_ph = ph;
           moved = true;
         }
       }
@@ -225,13 +247,15 @@ extern "C" vc_status vc_plan_stagger_local(const vc_stagger_cost* cost, int32_t 
   }
   const int64_t max_steps = 64 * (int64_t)n + 1024;
   int best_i = -1;
-  int64_t best = INT64_MAX;
+  int64_t best = INT64_MAX, best_ph = INT64_MAX;
   for (int i = 0; i < 3; ++i) {
     sums_of(seeds[i], cost, n);
     descend(seeds[i], cost, n, D, S, V, max_steps);
     const int64_t t = period2(seeds[i].dA, seeds[i].sA, seeds[i].vA, D, S, V);
-    if (t < best) {
+    const int64_t ph = phase_max(seeds[i].dA, seeds[i].vA, D, V);
+    if (better(t, ph, best, best_ph)) {
       best = t;
+      best_ph = ph;
       best_i = i;
     }
   }

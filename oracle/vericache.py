@@ -400,10 +400,22 @@ def stagger_period(costs: Sequence[Tuple[int, int, int]], groups: Sequence[int])
     return (stagger_period2(costs, groups) + 1) // 2
 
 
+def stagger_phase_work(costs: Sequence[Tuple[int, int, int]], groups: Sequence[int]) -> int:
+    """The longer phase's GPU work of a split: phase 1 drafts group 0 and verifies group 1, phase 2
+    the reverse, so max(D_0 + V_1, D_1 + V_0). Splits of equal period are told apart by it (the
+    balanced one leaves each phase enough drafting to cover the other group's copy)."""
+    D = [0, 0]
+    V = [0, 0]
+    for (d, v, s), g in zip(costs, groups):
+        D[g] += d
+        V[g] += v
+    return max(D[0] + V[1], D[1] + V[0])
+
+
 def plan_stagger(costs: Sequence[Tuple[int, int, int]]) -> Tuple[List[int], int]:
     """Best split by brute force: every assignment with request 0 in group 0 and, for n >= 2, at
-    least one request in group 1; minimum period (compared as 2T), ties to the smallest sum of
-    groups[r] * 2^(r-1). Returns (groups, period)."""
+    least one request in group 1; minimum period (compared as 2T), then minimum phase work
+    (stagger_phase_work), then the smallest sum of groups[r] * 2^(r-1). Returns (groups, period)."""
     import itertools
     n = len(costs)
     best = None
@@ -413,9 +425,10 @@ def plan_stagger(costs: Sequence[Tuple[int, int, int]]) -> Tuple[List[int], int]
         groups = [0] + list(tail)
         key = sum(g << (r - 1) for r, g in enumerate(groups) if r >= 1)
         t2 = stagger_period2(costs, groups)
-        if best is None or (t2, key) < (best[0], best[1]):
-            best = (t2, key, groups)
-    return best[2], (best[0] + 1) // 2
+        ph = stagger_phase_work(costs, groups)
+        if best is None or (t2, ph, key) < best[:3]:
+            best = (t2, ph, key, groups)
+    return best[3], (best[0] + 1) // 2
 
 
 # ----------------------------------------------------------------------------------------------

@@ -479,12 +479,16 @@ def test_stagger_balanced_split_unique_size():
 
 
 def test_stagger_resident_only_any_split():
-    """No copies: every split costs D + V, so the tie-break takes the smallest non-empty group 1
-    (request 1 alone). A single request stays alone in group 0: its copy overlaps its own drafting
-    and its verification follows the copy, max(D, S) + V = max(5, 9) + 2 = 11."""
+    """No copies: every split costs D + V = 32, so the phase work max(D_0 + V_1, D_1 + V_0) decides.
+    Worked by hand over the 7 splits: group 1 = {3} gives max(15 + 0, 11 + 6) = 17, {2, 3} gives
+    max(12 + 3, 14 + 3) = 17, every other split more (request 1 alone: max(19 + 1, 7 + 5) = 20); of
+    the two, the smaller mask 0b100 (request 3). A single request stays alone in group 0: its copy
+    overlaps its own drafting and its verification follows the copy, max(D, S) + V = 11."""
     costs = [(5, 2, 0), (7, 1, 0), (3, 3, 0), (11, 0, 0)]
     groups, t = O.plan_stagger(costs)
-    assert t == 26 + 6 and groups == [0, 1, 0, 0]
+    assert t == 26 + 6 and groups == [0, 0, 0, 1]
+    assert O.stagger_phase_work(costs, groups) == 17
+    assert O.stagger_phase_work(costs, [0, 1, 0, 0]) == 20 and O.stagger_phase_work(costs, [0, 0, 1, 1]) == 17
     assert O.plan_stagger([(5, 2, 9)]) == ([0], 11)
 
 
