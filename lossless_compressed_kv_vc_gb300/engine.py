@@ -75,6 +75,22 @@ class Batch:
                                     device=device)
         vb = vc_workspace_size(VC_CALL_VERIFY, self.shape, self.L_max)
         self.ws_verify = torch.empty(max(vb // 4 + 64, 64), dtype=torch.float32, device=device)
+        # The zero fills above run on the current stream; a call this Batch issues on another
+        # stream (a compress writing the windows, a draft reading the counters) must follow them,
+        # so each stream it is given waits for this event once, before its first call.
+        self._built = torch.cuda.Event()
+        self._built.record()
+        self._ordered = set()
+
+    def _order(self, *streams):
+        for s in streams:
+            if s is None:
+                continue
+            if not isinstance(s, torch.cuda.Stream):
+                s = torch.cuda.ExternalStream(int(s))
+            if s.cuda_stream not in self._ordered:
+                s.wait_event(self._built)
+                self._ordered.add(s.cuda_stream)
 
     def _alloc(self, r: Req):
         """Buffers of one request, sized by the library's own layout query (vc_comp_bytes): the
@@ -150,9 +166,11 @@ class Batch:
         ws = getattr(self, "ws_importance", None)
         if ws is None or ws.numel() * 4 < need:
             ws = self.ws_importance = torch.empty(need // 4 + 64, dtype=torch.float32, device=self.device)
+        self._order(stream)
         vc_snapkv_importance(shape, arr, window, pool_kernel, pool_kind, ws, self.dev_status, stream)
 
     def compress(self, stream=None, importance=None):
+        self._order(stream)
         mode = self.reqs[0].mode
         if mode == VC_TOKEN_DROP:
             imp = importance if importance is not None else [r.importance for r in self.reqs]
@@ -184,6 +202,7 @@ class Batch:
         if not act:
             return
         shape = vc_shape(len(act), self.Hq, self.Hkv, self.d)
+        self._order(stream)
         vc_draft_attn(shape, arr, self.ws_draft, self.dev_status, stream)
         for b in act:
             self.comp[b].n_win += 1
@@ -205,6 +224,7 @@ class Batch:
         given, is a (start, end) pair of CUDA events recorded around the whole draft phase (an
         event between two draft steps would hold back the next step's early start). compress=False
         drafts from the caches as they stand (quantised caches kept current by append_accepted)."""
+        self._order(stream)
         if compress:
             self.compress(stream)
         if draft_events is not None:
@@ -226,6 +246,7 @@ class Batch:
         accept, so the largest transfer of a round (the logits) hides under the HBM-bound draft
         phase ("Cross-resource staggering (P1)": keep the host link busy while the GPU drafts),
         and with two slots a round's copies overlap the previous round on the GPU."""
+        self._order(stream, copy_stream)
         sl = hr.next_slot()
         copy_stream.wait_event(sl.free)
         with torch.cuda.stream(copy_stream):
@@ -265,6 +286,7 @@ class Batch:
         for b, r in enumerate(self.reqs):
             n = max(0, min(int(n_acc[b]) - 1, r.L))
             arr[b].k_rows, arr[b].v_rows, arr[b].n_rows = r.k_new.data_ptr(), r.v_new.data_ptr(), n
+        self._order(stream)
         vc_append_kv(self.shape, self.full, self.comp, arr, self.residual_min, self.dev_status, stream)
         for b, r in enumerate(self.reqs):
             r.ctx = self.full[b].ctx
@@ -287,6 +309,7 @@ class Batch:
         return arr
 
     def verify(self, stream=None):
+        self._order(stream)
         vc_verify_attn(self.shape, self.verify_requests(), self.ws_verify, self.dev_status, stream)
 
 
@@ -406,6 +429,11 @@ class StaggeredOffload:
         self.edges = [c * Hkv // head_chunks for c in range(head_chunks + 1)]
         self.staged = [[torch.cuda.Event() for _ in range(head_chunks)] for _ in range(2)]
         self.verified = [torch.cuda.Event(), torch.cuda.Event()]
+        # the batches, slots and round tensors were made on the current stream: both streams
+        # start after that work
+        cur = torch.cuda.current_stream()
+        copy_stream.wait_stream(cur)
+        compute_stream.wait_stream(cur)
         for g in range(2):  # a slot is free before its first copy
             self.verified[g].record(compute_stream)
         self._cur = [None, None]  # host-input periods: the HostRound slot each batch last drafted from

@@ -213,3 +213,32 @@ def test_planned_stagger_with_resident_requests_matches_oracle(vc):
             assert_attn_close(r.o_verify, ref_v, f"verify b{b}")
             rt, rn = O.accept(lg[i].cpu().numpy(), dr[i].cpu().numpy(), int(Lg[i]))
             assert int(nacc[i]) == rn and tok[i, :rn].cpu().tolist() == rt
+
+
+def test_batch_calls_on_another_stream_follow_its_construction(vc):
+    """A Batch is built on the current stream (KV_full written, windows and workspace zero-filled
+    there) and then compressed and drafted on a side stream, as the staggered round does. The side
+    stream must start after that work: here the current stream is held back by a bounded sleep
+    kernel before the inputs are even generated, so without the ordering the compress would read
+    KV_full before it is written or have its residual window wiped by a late zero fill. Codes,
+    scales, zeros and the window are compared bit for bit with the oracle's quantisation, and the
+    first draft step with the oracle's attention."""
+    from tests.util import assert_quant_state
+    w = configs.scaled(configs.qwen32b_quant2(), ctx_div=64, batch=2, L=2)
+    ks = torch.cuda.Stream()
+    torch.cuda._sleep(100_000_000)  # about 50 ms of device time on the current stream
+    bt = make_batch(w, list(range(w.B)))
+    bt.compress(ks)
+    bt.draft_step(0, ks)
+    ks.synchronize()
+    torch.cuda.synchronize()
+    assert int(bt.dev_status.item()) == 0
+    bt.reset_window()  # the window counts as after compress (the draft step appended a row)
+    for i in range(w.B):
+        r = bt.reqs[i]
+        kf, vf = f32(r.k_full[:, : w.ctx[i]]), f32(r.v_full[:, : w.ctx[i]])
+        assert_quant_state(bt, i, kf, vf, w.bits, w.residual_min)
+        km, vm, kw0, vw0 = oracle_main(w, i, kf, vf)
+        kn, vn = f32(r.k_new[:1]).transpose(1, 0, 2), f32(r.v_new[:1]).transpose(1, 0, 2)
+        ref = O.draft_attn(f32(r.q[0]), km, vm, np.concatenate([kw0, kn], 1), np.concatenate([vw0, vn], 1))
+        assert_attn_close(r.o_draft[0], ref, f"request {i} on a side stream")
