@@ -460,7 +460,15 @@ vc_status vc_draft_attn(const vc_shape* shape, const vc_draft_req* req, void* ws
   p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + draft_counter_bytes());
   p.ws_lse = p.ws_o + (size_t)Hkv * (n_cta + B) * G * d;
   p.early = last_op(stream) != kOpCompress;
-  if (launch_draft(p, &maps, d, kind, n_cta, stream) != cudaSuccess) return VC_ERR_CUDA;
+  // VC_DRAFT_TC=1: quantised caches at d = 128 with up to 8 query heads per KV head on the tcgen05
+  // kernel (draft_tc.cu). Same results; measured about 3x slower than the mma.sync kernel, whose
+  // independent warps hide latency that the tcgen05 pipeline serialises, so it is not the default.
+  const bool tc = kind != 0 && d == 128 && G <= 8 && env_int("VC_DRAFT_TC", 0) != 0;
+  if (tc) {
+    if (launch_draft_tc(p, kind, sm_count(), stream) != cudaSuccess) return VC_ERR_CUDA;
+  } else if (launch_draft(p, &maps, d, kind, n_cta, stream) != cudaSuccess) {
+    return VC_ERR_CUDA;
+  }
   set_last_op(stream, kOpDraft);
   return VC_OK;
 }

@@ -236,6 +236,11 @@ struct DraftReqDev {
   int32_t n_mc;
   int32_t n_chunks;
   int32_t warp_begin;   // first warp (of a head's grid row) holding it; it holds them up to the next request's
+  // unit plan of the tcgen05 quantised kernel (draft_tc.cu): tc_nqb blocks of four groups (cost 1
+  // each), then tc_nwb window blocks of 128 rows (cost WW each), from cost tc_ucb of the head's
+  // concatenation; CTAs tc_c0 .. tc_c1 of the grid row hold its units
+  int64_t tc_ucb;
+  int32_t tc_nqb, tc_nwb, tc_c0, tc_c1;
 };
 
 // The observation-window passes of the SnapKV-style importance, run by the verification kernel's
@@ -276,6 +281,7 @@ struct DraftParams {
   // stream has finished (set when that kernel is not a compress); it waits for it before reading
   // window rows, storing the step's row and writing any output.
   int32_t early;
+  int64_t tc_total;      // tcgen05 quantised kernel: unit cost per KV head over all requests
 };
 
 // Tensor maps of the kept K and V rows of each request (token drop): 2-D (d, Hkv * rows_cap) over
@@ -290,6 +296,10 @@ constexpr int kDraftWarps = 4;
 // launchers (return cudaError_t of the launch); maps is read for token drop only
 cudaError_t launch_draft(const DraftParams& p, const DraftMaps* maps, int d, int mode_kind, int ctas_per_head,
                          cudaStream_t s);
+// quantised caches at d = 128 with at most 8 query heads per KV head on the tcgen05 kernel: one CTA
+// per SM, draft_tc_ctas_per_head(Hkv) per KV head; fills in its own unit plan and CTA partial slots
+cudaError_t launch_draft_tc(const DraftParams& p, int kind, int sm_count, cudaStream_t s);
+int draft_tc_ctas_per_head(int Hkv, int sm_count);
 
 // ---- host: TMA tensor maps --------------------------------------------------------------------------
 // cuTensorMapEncodeTiled from the driver (fetched once through the runtime), or nullptr.

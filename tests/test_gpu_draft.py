@@ -69,12 +69,17 @@ def test_draft_drop_compact():
     _check_all_steps(w, [0, 1], compact=True)
 
 
-def test_draft_quant2_qwen_scaled():
+# kernel: the mma.sync kernel (default) or the tcgen05 one (VC_DRAFT_TC=1); same results
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+def test_draft_quant2_qwen_scaled(kernel, monkeypatch):
+    monkeypatch.setenv("VC_DRAFT_TC", "1" if kernel == "tc" else "0")
     w = configs.scaled(configs.qwen32b_quant2(), ctx_div=32, batch=3, L=5)
     _check_all_steps(w, [0, 1, 2])
 
 
-def test_draft_quant4_llama70b_scaled():
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+def test_draft_quant4_llama70b_scaled(kernel, monkeypatch):
+    monkeypatch.setenv("VC_DRAFT_TC", "1" if kernel == "tc" else "0")
     w = configs.scaled(configs.llama70b_offload4(), ctx_div=128, batch=2, L=5)
     _check_all_steps(w, [0, 1])
 
@@ -133,7 +138,9 @@ def test_draft_llama8b_full_size_sampled():
     _sampled_full_size(w, list(range(8)), steps=[0, 31], heads=[0, 7])
 
 
-def test_draft_qwen32b_quant2_full_size_sampled():
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+def test_draft_qwen32b_quant2_full_size_sampled(kernel, monkeypatch):
+    monkeypatch.setenv("VC_DRAFT_TC", "1" if kernel == "tc" else "0")
     w = configs.qwen32b_quant2()
     _sampled_full_size(w, [0, 15] + list(range(1, 15)), steps=[0, 24], heads=[3])
 

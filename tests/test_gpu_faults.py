@@ -50,8 +50,11 @@ def test_stage_reports_a_failed_chunk_and_issues_nothing_after_it(vc, monkeypatc
     assert torch.equal(dev.cpu(), host)
 
 
-@pytest.mark.parametrize("which", ["drop", "quant"])
+@pytest.mark.parametrize("which", ["drop", "quant", "quant_tc"])
 def test_draft_wait_runs_out_then_the_context_stays_usable(vc, monkeypatch, which):
+    """quant_tc: the tcgen05 draft kernel (VC_DRAFT_TC=1), whose roles give up together through a
+    shared flag, wait for their copies and MMAs, free TMEM and leave zero (finite) outputs."""
+    monkeypatch.setenv("VC_DRAFT_TC", "1" if which == "quant_tc" else "0")
     if which == "drop":
         w = configs.scaled(configs.llama8b_drop(), ctx_div=32, batch=2, L=2)
     else:
