@@ -31,13 +31,16 @@ sys.path.insert(0, ROOT)
 METRIC = "verified tokens/s/GPU (draft+verify+accept)"
 UNIT = "tokens/s"
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
-DRAFT_SOURCES = ["lossless_compressed_kv_vc_gb300/csrc/draft.cu", "lossless_compressed_kv_vc_gb300/csrc/vc_internal.cuh"]
+DRAFT_SOURCES = ["lossless_compressed_kv_vc_gb300/csrc/draft.cu", "lossless_compressed_kv_vc_gb300/csrc/draft_common.cuh",
+                 "lossless_compressed_kv_vc_gb300/csrc/vc_internal.cuh"]
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 300 for this implementation; 20 for --impl reference, whose "
+                         "steps are one request's whole round on the host cores each)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=None)
@@ -74,6 +77,8 @@ def parse():
                     help="offload and stagger workloads: drafts per round for every request (default: the "
                          "workload's L)")
     a = ap.parse_args()
+    if a.steps is None:
+        a.steps = 20 if a.impl == "reference" else 300
     global _BATCH, _WORKLOAD
     _BATCH = a.batch
     _WORKLOAD = a.workload
