@@ -103,7 +103,11 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 // One 16-token tile: scores, online softmax (per query head, exp2 domain) and P V accumulation.
 // qb: Q^T B fragments [head block][k-step][2]; o: O^T accumulators [head block][channel tile][4];
 // m, l: running max and (lane-partial) sum for this lane's two heads of each head block.
-template <int D, int NHB>
+// PLO: the weights enter P V as two bf16 parts (p = hi + lo, each MMA'd against V), which keeps
+// their 16 significant bits instead of 8. The quantised kernels take it for their window tiles:
+// a request with only a few hundred bf16 rows (a short context, all residual) and peaked weights
+// otherwise carries the weights' bf16 rounding almost undamped into its output.
+template <int D, int NHB, bool PLO = false>
 __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt, int cnt, float scale_log2,
                                             const uint32_t (&qb)[NHB][D / 16][2], float (&o)[NHB][D / 16][4],
                                             float (&m)[NHB][2], float (&l)[NHB][2], int lane) {
@@ -169,11 +173,19 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
       l[hb][e] += p[hb][e][0] + p[hb][e][1];
     }
   // P^T as the B operand (k = token, n = head): transpose the two 8x8 bf16 blocks of the accumulator
-  uint32_t pb[NHB][2];
+  uint32_t pb[NHB][2], pl[NHB][2];
 #pragma unroll
   for (int hb = 0; hb < NHB; ++hb) {
-    pb[hb][0] = movmatrix_t(pack_bf16x2(p[hb][0][0], p[hb][1][0]));  // tokens 0-7
-    pb[hb][1] = movmatrix_t(pack_bf16x2(p[hb][0][1], p[hb][1][1]));  // tokens 8-15
+    const uint32_t h0 = pack_bf16x2(p[hb][0][0], p[hb][1][0]), h1 = pack_bf16x2(p[hb][0][1], p[hb][1][1]);
+    pb[hb][0] = movmatrix_t(h0);  // tokens 0-7
+    pb[hb][1] = movmatrix_t(h1);  // tokens 8-15
+    if constexpr (PLO) {
+      // the remainders p - bf16(p) (exact in fp32), rounded to bf16 in turn
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h0));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h1));
+      pl[hb][0] = movmatrix_t(pack_bf16x2(p[hb][0][0] - f0.x, p[hb][1][0] - f0.y));
+      pl[hb][1] = movmatrix_t(pack_bf16x2(p[hb][0][1] - f1.x, p[hb][1][1] - f1.y));
+    }
   }
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
@@ -181,7 +193,10 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
     uint32_t a[4];
     ldsm_x4_t(a[0], a[1], a[2], a[3], a_ptr);
 #pragma unroll
-    for (int hb = 0; hb < NHB; ++hb) mma_bf16_16816(o[hb][mt], a, pb[hb][0], pb[hb][1]);
+    for (int hb = 0; hb < NHB; ++hb) {
+      mma_bf16_16816(o[hb][mt], a, pb[hb][0], pb[hb][1]);
+      if constexpr (PLO) mma_bf16_16816(o[hb][mt], a, pl[hb][0], pl[hb][1]);
+    }
   }
 }
 
@@ -806,7 +821,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
         q_f16 = false;
       }
       const int cnt = (lc < r.n_mc) ? min(16, r.n_main - lc * 16) : min(16, r.n_win + 1 - (lc - r.n_mc) * 16);
-      tile_attend<D, NHB>(sb, sb + C::TILE, cnt, p.scale_log2, qb, o, m, l, lane);
+      tile_attend<D, NHB, !BF16_ROWS>(sb, sb + C::TILE, cnt, p.scale_log2, qb, o, m, l, lane);
     }
     __syncwarp();
     // next issue: a KV_comp chunk into the stage just read (NST ahead), or -- spanning the ring --

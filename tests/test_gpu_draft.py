@@ -93,6 +93,20 @@ def test_draft_quant_d64_ragged(bits):
     _check_all_steps(w, [0, 1, 2])
 
 
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+@pytest.mark.parametrize("bits", [2, 4])
+def test_draft_quant_d128_ragged(kernel, bits, monkeypatch):
+    """d = 128, G = 5, contexts that leave 0, 1, 3, 5 and 61 quantised groups (a window-only
+    request; partial four-group blocks of the tcgen05 kernel; residuals of 128-150 rows, window
+    blocks of up to 156 rows): most CTAs of a KV head's grid row hold a little of a request, some
+    none, so the split partials and their merge are exercised with empty slots."""
+    monkeypatch.setenv("VC_DRAFT_TC", "1" if kernel == "tc" else "0")
+    w = configs.scaled(configs.qwen32b_quant2(), batch=5, L=6)
+    w.bits = bits
+    w.ctx = [150, 160, 224, 300, 2100]
+    _check_all_steps(w, [0, 1, 2, 3, 4])
+
+
 @pytest.mark.parametrize("keep,ctx,L", [(10, 64, 3), (17, 40, 17), (1, 8, 2)])
 def test_draft_fewer_chunks_than_warps(keep, ctx, L):
     """One request whose step has only 2-3 chunks per head (16-row kept chunks, then window
