@@ -33,6 +33,11 @@
  *     VC_SPIN_LIMIT (read by each vc_draft_attn call) sets how many tries a draft warp's wait for its
  *     next stage of data makes before it gives up (default 4194304; 0 gives up at once): a short
  *     limit makes that wait run out without any fault, which is how its error path is tested.
+ *   - Kernel choices read from the environment by each call, with the same results either way:
+ *     VC_DRAFT_TC=1 runs vc_draft_attn for quantised caches at d = 128 with at most 8 query heads
+ *     per KV head on the tcgen05 draft kernel (the mma.sync kernel is the default and faster);
+ *     VC_VERIFY_ROWS=1 verifies every 128-row tile of a (request, KV head) in one CTA, reading its
+ *     KV_full once (by default each row tile is a unit of its own and reads it again).
  */
 #ifndef VC_H_
 #define VC_H_
