@@ -56,7 +56,11 @@ struct VerifyReqDev {
 // unit is the KV head, each K/V tile is loaded once and serves all its row tiles (up to VROWS), one
 // O accumulator per row tile in TMEM. By default a KV head with more than 128 rows (L x G > 128) is
 // one unit per row tile and streams its K and V once per row tile.
-constexpr int VMODE_ATTN = 0, VMODE_STATS = 1, VMODE_VOTES = 2, VMODE_ROWS = 3;
+// VMODE_PAIR (the default for a KV head of exactly two row tiles): both row tiles of the head in one
+// CTA with a softmax warpgroup each (warps 0-3 and 6-9), each with its own Q and P tiles, S double
+// buffer and O accumulator; a K/V tile is loaded once and serves both, and the two warpgroups keep
+// the softmax throughput of two one-tile CTAs.
+constexpr int VMODE_ATTN = 0, VMODE_STATS = 1, VMODE_VOTES = 2, VMODE_ROWS = 3, VMODE_PAIR = 4;
 constexpr int VROWS = 3;  // row tiles a row-tile-mode CTA holds (3 x 128 O columns + S fill TMEM)
 
 struct VerifyParams {
@@ -72,14 +76,14 @@ struct VerifyParams {
   int32_t* dev_status;
 };
 
-template <int D, int NQ = 1>
+template <int D, int NQ = 1, bool PAIR = false>
 struct VCfg {
   static constexpr int KB = D / 64;                // 64-channel (128-byte) blocks
   static constexpr int Q_BYTES = KB * VM * 128;    // Q tile, K-major SW128 (NQ of them)
   static constexpr int P_BYTES = VM * 128;         // P tile (64 tokens), K-major SW128
   static constexpr int KV_BYTES = KB * VBN * 128;  // one K (or V) tile
-  static constexpr int OFF_P = NQ * Q_BYTES;
-  static constexpr int OFF_K = OFF_P + P_BYTES;    // K stages [2]
+  static constexpr int OFF_P = NQ * Q_BYTES;       // P tile (pair mode: one per warpgroup)
+  static constexpr int OFF_K = OFF_P + (PAIR ? 2 : 1) * P_BYTES;  // K stages [2]
   static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;  // V stages [2]
   static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr int SMEM = OFF_BAR + 256;
@@ -87,7 +91,11 @@ struct VCfg {
   static constexpr int OCOL = 128;                 // O: TMEM columns [128, 128 + D) (row tile m: + m D)
   static constexpr uint32_t TCOLS = NQ == 1 ? 256 : 512;
   static_assert(OCOL + NQ * D <= (int)TCOLS, "O accumulators fit the TMEM allocation");
-  static constexpr int THREADS = 192;              // warps 0-3 softmax, 4 MMA issue, 5 TMA loads
+  static constexpr int THREADS = PAIR ? 352 : 192;  // warps 0-3 softmax, 4 MMA issue, 5 TMA loads (pair: 6-9 softmax, 10 MMA issue)
+  // pair mode: warpgroup m's S double buffer at TMEM columns [m 128, m 128 + 128), its O at 256 + m D
+  static constexpr int PSCOL = 128;
+  static constexpr int POCOL = 256;
+  static_assert(!PAIR || (POCOL + 2 * D <= (int)TCOLS && NQ == 2), "pair mode fits TMEM");
   // votes mode: an fp16 all-ones [128][128] A operand over the (unused) V stages
   static constexpr int ONES_BYTES = VM * 128 * 2;
   static constexpr int OFF_BAR_VOTES = OFF_V + ONES_BYTES > OFF_BAR ? OFF_V + ONES_BYTES : OFF_BAR;
@@ -131,8 +139,9 @@ __device__ __forceinline__ VPiece verify_piece(const VerifyParams& p, int64_t po
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_kernel(const __grid_constant__ VerifyParams p) {
-  using C = VCfg<D, MODE == VMODE_ROWS ? VROWS : 1>;
+__global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE_ROWS || MODE == VMODE_PAIR) ? 1 : 2)
+    verify_attn_kernel(const __grid_constant__ VerifyParams p) {
+  using C = VCfg<D, MODE == VMODE_ROWS ? VROWS : (MODE == VMODE_PAIR ? 2 : 1), MODE == VMODE_PAIR>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte aligned tiles
@@ -155,6 +164,12 @@ __global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_k
   uint64_t* xbar = bars + 13;   // drain on the error path
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 15);
+  // pair mode, warpgroup 1: its S buffers' fills, P tile, P V done, Q tile (warpgroup 0 uses the above)
+  uint64_t* sfull1 = bars + 16;  // [2]
+  uint64_t* pfull1 = bars + 18;
+  uint64_t* ofull1 = bars + 19;
+  uint64_t* qfull1 = bars + 20;
+  uint64_t* xbar1 = bars + 21;  // warpgroup 1's MMA issuer's drain
 
   if (warp == 0) tc05::alloc(tslot, C::TCOLS);
   if (tid == 0) {
@@ -171,6 +186,19 @@ __global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_k
     mbar_init(ofull, 1);
     mbar_init(qfull, 4);
     mbar_init(xbar, 1);
+    if (MODE == VMODE_PAIR) {
+      // a K (V) stage is free once both warpgroups' issuers have committed their S (P V) of it
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&kempty[i], 2);
+        mbar_init(&vempty[i], 2);
+      }
+      mbar_init(xbar1, 1);
+      mbar_init(&sfull1[0], 1);
+      mbar_init(&sfull1[1], 1);
+      mbar_init(pfull1, 4);
+      mbar_init(ofull1, 1);
+      mbar_init(qfull1, 4);
+    }
     fence_mbar_init();
     *s_abort = 0;
   }
@@ -188,6 +216,75 @@ __global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_k
 
   const int64_t T = p.total_tiles, N = p.n_cta, c = blockIdx.x;
   const int64_t beg = c * T / N, end = (c + 1) * T / N;
+
+  // pair mode: the MMA chain of warpgroup m's row tile over the CTA's units, issued by one thread
+  // (warp 4 for warpgroup 0, warp 10 for warpgroup 1): S of tile g before P V of tile g - 1, as in
+  // the one-tile mode; both issuers commit every K and V stage's release (two arrivals each), the
+  // second also for tiles of a one-tile head, where it has no MMA of its own
+  auto pair_issue = [&](int m) -> bool {
+    constexpr uint32_t IDESC_S = tc05::idesc_bf16(VM, VBN, false);
+    constexpr uint32_t IDESC_O = tc05::idesc_bf16(VM, D, true);
+    const uint32_t aQ = smem_u32(sQ) + m * C::Q_BYTES, aP = smem_u32(sP) + m * C::P_BYTES,
+                   aK = smem_u32(smem + C::OFF_K), aV = smem_u32(smem + C::OFF_V);
+    uint64_t* sf = m ? sfull1 : sfull;
+    uint64_t* pf = m ? pfull1 : pfull;
+    uint64_t* of = m ? ofull1 : ofull;
+    uint64_t* qf = m ? qfull1 : qfull;
+    uint32_t g = 0, t = 0, pw = 0, uq = 0;
+    bool ok = true;
+    auto pv = [&](uint32_t gp, bool acc, bool mine) -> bool {
+      if (!vwait(&vfull[gp & 1], (gp >> 1) & 1, p.dev_status, s_abort)) return false;
+      if (mine) {
+        if (!vwait(pf, pw & 1, p.dev_status, s_abort)) return false;
+        tc05::fence_after();
+        const uint32_t vaddr = aV + (gp & 1) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < VBN / 16; ++kk) {
+          const uint64_t da = tc05::sdesc_sw128(aP + kk * 32, 16, 1024);
+          const uint64_t db = tc05::sdesc_sw128(vaddr + kk * 2048, VBN * 128, 1024);
+          tc05::mma_bf16(tmem + C::POCOL + m * D, da, db, IDESC_O, (acc || kk > 0) ? 1u : 0u);
+        }
+        tc05::commit(of);
+        ++pw;
+      }
+      tc05::commit(&vempty[gp & 1]);
+      return true;
+    };
+    for (int64_t pos = beg; pos < end && ok;) {
+      const VPiece q = verify_piece(p, pos, end);
+      const int nt = q.j1 - q.j0;
+      const bool mine = m < p.req[q.b].mtiles;
+      if (mine) {
+        ok = vwait(qf, uq & 1, p.dev_status, s_abort);
+        ++uq;
+      }
+      for (int jj = 0; jj < nt && ok; ++jj) {
+        const uint32_t gc = g + jj;
+        if (!vwait(&kfull[gc & 1], (gc >> 1) & 1, p.dev_status, s_abort)) {
+          ok = false;
+          break;
+        }
+        if (mine) {
+          tc05::fence_after();
+          const uint32_t kaddr = aK + (gc & 1) * C::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t da = tc05::sdesc_sw128(aQ + (kk >> 2) * (VM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = tc05::sdesc_sw128(kaddr + (kk >> 2) * (VBN * 128) + (kk & 3) * 32, 16, 1024);
+            tc05::mma_bf16(tmem + m * C::PSCOL + (t & 1) * C::SCOL, da, db, IDESC_S, kk > 0);
+          }
+          tc05::commit(&sf[t & 1]);
+          ++t;
+        }
+        tc05::commit(&kempty[gc & 1]);
+        if (jj > 0) ok = pv(gc - 1, jj > 1, mine);
+      }
+      if (ok) ok = pv(g + nt - 1, nt > 1, mine);
+      g += nt;
+      pos += nt;
+    }
+    return ok;
+  };
 
   if (warp == 5) {
     // ---- TMA producer: K of tile g, then V of tile g - 1 (K runs a tile ahead of V) ----------
@@ -212,11 +309,11 @@ __global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_k
       bool ok = true;
       for (int64_t pos = beg; pos < end && ok;) {
         const VPiece q = verify_piece(p, pos, end);
-        const int hk = p.h0 + (MODE == VMODE_ROWS ? q.ul : q.ul / p.req[q.b].mtiles);
+        const int hk = p.h0 + ((MODE == VMODE_ROWS || MODE == VMODE_PAIR) ? q.ul : q.ul / p.req[q.b].mtiles);
         for (int j = q.j0; j < q.j1 && ok; ++j, ++g) {
           ok = load(false, gk, q.b, hk, j);
           if (ok) ++gk;
-          if ((MODE == VMODE_ATTN || MODE == VMODE_ROWS) && ok && pv_pending) {
+          if ((MODE == VMODE_ATTN || MODE == VMODE_ROWS || MODE == VMODE_PAIR) && ok && pv_pending) {
             ok = load(true, gv, pv_b, pv_hk, pv_j);
             if (ok) ++gv;
           }
@@ -224,7 +321,9 @@ __global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_k
         }
         pos += q.j1 - q.j0;
       }
-      if ((MODE == VMODE_ATTN || MODE == VMODE_ROWS) && ok && pv_pending && load(true, gv, pv_b, pv_hk, pv_j)) ++gv;
+      if ((MODE == VMODE_ATTN || MODE == VMODE_ROWS || MODE == VMODE_PAIR) && ok && pv_pending &&
+          load(true, gv, pv_b, pv_hk, pv_j))
+        ++gv;
       if (*s_abort) {
         // drain (bounded): the loads of the last two tiles of each kind may still be landing
         for (uint32_t gi = (gk > 2 ? gk - 2 : 0); gi < gk; ++gi) mbar_wait_bounded(&kfull[gi & 1], (gi >> 1) & 1, p.dev_status);
@@ -327,7 +426,11 @@ __global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_k
         g += nt;
         pos += nt;
       }
-      for (int64_t pos = beg; pos < end && ok && MODE != VMODE_ROWS;) {
+      // pair mode: this thread issues the MMAs of warpgroup 0 (warp 4) -- warpgroup 1 has its own
+      // issuer (warp 10, below) -- so the two row tiles' chains run independently; each commits its
+      // S and P V to the shared K and V stage releases (two arrivals each)
+      if constexpr (MODE == VMODE_PAIR) ok = pair_issue(0);
+      for (int64_t pos = beg; pos < end && ok && MODE != VMODE_ROWS && MODE != VMODE_PAIR;) {
         const VPiece q = verify_piece(p, pos, end);
         const int nt = q.j1 - q.j0;
         ok = vwait(qfull, u & 1, p.dev_status, s_abort);
@@ -358,11 +461,189 @@ __global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_k
       tc05::commit(xbar);
       mbar_wait_bounded(xbar, 0, p.dev_status);
     }
+  } else if (MODE == VMODE_PAIR && warp == 10) {
+    // ---- pair mode: warpgroup 1's MMA issue; its MMAs complete before TMEM is released ----------
+    if (lane == 0) {
+      pair_issue(1);
+      tc05::commit(xbar1);
+      mbar_wait_bounded(xbar1, 0, p.dev_status);
+    }
   } else {
     // ---- softmax warps: thread tid owns TMEM lane tid = query row tid of the tile ---------------
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     uint32_t g = 0;
     bool ok = true;
+    if constexpr (MODE == VMODE_PAIR) {
+      // warpgroup wg (warps 0-3: 0, warps 6-9: 1) owns row tile wg of each unit; thread rt =
+      // (warp % 4) * 32 + lane owns row rt of that tile, which is its TMEM lane
+      const int wg = warp >= 6 ? 1 : 0;
+      const int rt = (warp & 3) * 32 + lane;
+      const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
+      uint64_t* sf = wg ? sfull1 : sfull;
+      uint64_t* pf = wg ? pfull1 : pfull;
+      uint64_t* of = wg ? ofull1 : ofull;
+      uint64_t* qf = wg ? qfull1 : qfull;
+      uint8_t* sQw = sQ + wg * C::Q_BYTES;
+      uint8_t* sPw = sP + wg * C::P_BYTES;
+      const uint32_t t_s0 = tmem + lo + wg * C::PSCOL, t_o0 = tmem + lo + C::POCOL + wg * D;
+      uint32_t t = 0, sp = 0;  // this warpgroup's S tiles read and P tiles written
+      for (int64_t pos = beg; pos < end && ok;) {
+        const VPiece q = verify_piece(p, pos, end);
+        const VerifyReqDev& R = p.req[q.b];
+        const int nt = q.j1 - q.j0;
+        pos += nt;
+        if (wg >= R.mtiles) continue;  // a head of one row tile: warpgroup 1 holds nothing of it
+        const int hk = p.h0 + q.ul;
+        const int ug_global = R.ug_begin + q.ul;
+        const int Rw = wg * VM + rt, qi = Rw / p.G, qg = Rw % p.G;
+        const bool row_ok = qi < R.n_rows;
+        // this thread's query row into the warpgroup's swizzled Q tile; its previous unit's MMAs are
+        // complete (that unit's epilogue waited for its last P V, which follows all its S)
+        {
+          const uint4* src = reinterpret_cast<const uint4*>(R.q + ((size_t)qi * p.Hq + hk * p.G + qg) * D);
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint4 v = row_ok ? __ldg(src + kb * 8 + ch) : make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(sQw + kb * (VM * 128) + rt * 128 + ((ch ^ (rt & 7)) << 4)) = v;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qf);
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int jj = 0; jj < nt; ++jj) {
+          const int j = q.j0 + jj;
+          if (!vwait(&sf[t & 1], (t >> 1) & 1, p.dev_status, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          float x[VBN];
+          {
+            uint32_t r0[32], r1[32];
+            const uint32_t t_s = t_s0 + (t & 1) * C::SCOL;
+            tc05::ld32(t_s, r0);
+            tc05::ld32(t_s + 32, r1);
+            tc05::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              x[e] = __uint_as_float(r0[e]);
+              x[32 + e] = __uint_as_float(r1[e]);
+            }
+          }
+          ++t;
+          {
+            const int last = j < R.n_full ? R.ctx - j * VBN - 1 : qi - (j - R.n_full) * VBN;  // last visible key
+            if (last < VBN - 1) {
+#pragma unroll
+              for (int e = 0; e < VBN; ++e)
+                if (e > last) x[e] = -INFINITY;
+            }
+          }
+          float mx;
+          {
+            float tt[VBN / 2];
+#pragma unroll
+            for (int e = 0; e < VBN / 2; ++e) tt[e] = fmaxf(x[2 * e], x[2 * e + 1]);
+#pragma unroll
+            for (int w = VBN / 4; w >= 1; w >>= 1)
+#pragma unroll
+              for (int e = 0; e < w; ++e) tt[e] = fmaxf(tt[e], tt[e + w]);
+            mx = tt[0] * p.scale_log2;
+          }
+          const float m_new = fmaxf(m_run, mx);
+          const bool need = jj > 0 && m_new > m_run + 8.f;
+          if (jj > 0) {
+            // this warpgroup's P V of the previous tile: O is stable and its P tile is free
+            if (!vwait(of, (sp - 1) & 1, p.dev_status, s_abort)) {
+              ok = false;
+              break;
+            }
+            tc05::fence_after();
+          }
+          if (jj == 0) {
+            m_run = m_new;
+          } else {
+            float f = 1.f;
+            if (need) {
+              f = ex2_approx(m_run - m_new);
+              l_run *= f;
+              m_run = m_new;
+            }
+            if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+              for (int cb = 0; cb < D / 32; ++cb) {
+                uint32_t r[32];
+                tc05::ld32(t_o0 + cb * 32, r);
+                tc05::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                tc05::st32(t_o0 + cb * 32, r);
+              }
+              tc05::wait_st();
+            }
+          }
+          const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p0 = ex2_approx(fmaf(x[ch * 8 + 2 * e], p.scale_log2, -mu));
+              const float p1 = ex2_approx(fmaf(x[ch * 8 + 2 * e + 1], p.scale_log2, -mu));
+              ls[e] += p0 + p1;
+              w[e] = pack_bf16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(sPw + rt * 128 + ((ch ^ (rt & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          fence_proxy_async_smem();
+          tc05::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pf);
+          ++sp;
+        }
+        if (!ok) break;
+        // output: wait for this warpgroup's last P V of the unit
+        if (!vwait(of, (sp - 1) & 1, p.dev_status, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc05::fence_after();
+        const bool whole = (q.j0 == 0 && q.j1 == R.tiles);
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const size_t slot = (size_t)(c + ug_global) * VROWS + wg;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t r[32];
+          tc05::ld32(t_o0 + cb * 32, r);  // warp-collective: every lane loads
+          tc05::wait_ld();
+          if (!row_ok) continue;
+          if (whole) {
+            uint4* dst = reinterpret_cast<uint4*>(R.o + ((size_t)qi * p.Hq + hk * p.G + qg) * D + cb * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * e]) * inv, __uint_as_float(r[8 * v + 2 * e + 1]) * inv);
+              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * VM + rt) * D + cb * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                   __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+          }
+        }
+        if (row_ok && !whole) p.ws_lse[slot * VM + rt] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+        tc05::fence_before();
+      }
+    }
     // row-tile mode: thread tid owns row tid of every row tile of the unit; steps (KV tile, row
     // tile) in the MMA warp's order, one running maximum and sum per row tile
     uint32_t vg = 0;  // steps consumed
@@ -545,7 +826,7 @@ __global__ void __launch_bounds__(192, MODE == VMODE_ROWS ? 1 : 2) verify_attn_k
       tc05::fence_before();
       pos += nt;
     }
-    for (int64_t pos = beg; pos < end && ok && MODE != VMODE_ROWS;) {
+    for (int64_t pos = beg; pos < end && ok && MODE != VMODE_ROWS && MODE != VMODE_PAIR;) {
       const VPiece q = verify_piece(p, pos, end);
       const VerifyReqDev& R = p.req[q.b];
       const int nt = q.j1 - q.j0;
@@ -984,7 +1265,7 @@ size_t verify_workspace_size(const vc_shape* s, int32_t max_rows) {
 
 template <int D, int MODE>
 static cudaError_t launch_modes_t(const VerifyParams& p, cudaStream_t s) {
-  using C = VCfg<D, MODE == VMODE_ROWS ? VROWS : 1>;
+  using C = VCfg<D, MODE == VMODE_ROWS ? VROWS : (MODE == VMODE_PAIR ? 2 : 1), MODE == VMODE_PAIR>;
   constexpr int SMEM = MODE == VMODE_VOTES ? C::SMEM_VOTES : C::SMEM;
   static std::atomic<uint64_t> attr{0};
   {
@@ -996,7 +1277,9 @@ static cudaError_t launch_modes_t(const VerifyParams& p, cudaStream_t s) {
 
 template <int D>
 static cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
-  cudaError_t e = p.rows ? launch_modes_t<D, VMODE_ROWS>(p, s) : launch_modes_t<D, VMODE_ATTN>(p, s);
+  cudaError_t e = p.rows == 2   ? launch_modes_t<D, VMODE_PAIR>(p, s)
+                  : p.rows == 1 ? launch_modes_t<D, VMODE_ROWS>(p, s)
+                                : launch_modes_t<D, VMODE_ATTN>(p, s);
   if (e != cudaSuccess) return e;
   return launch_pdl(verify_combine_kernel<D>, dim3(p.n_units, VM / 8), dim3(256), 0, s, p);
 }
@@ -1090,22 +1373,17 @@ cudaError_t launch_obs_passes(const ObsArgs& a, cudaStream_t s) {
   return d == 128 ? launch_modes_t<128, VMODE_VOTES>(p, s) : launch_modes_t<64, VMODE_VOTES>(p, s);
 }
 
-cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h0, int h1, void* ws,
-                          size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, vc_status* st) {
-  *st = VC_OK;
-  if (!shape || shape->B < 1 || shape->B > VC_MAX_BATCH || shape->Hkv < 1 || shape->Hq < shape->Hkv ||
-      shape->Hq % shape->Hkv != 0 || !req || h0 < 0 || h1 <= h0 || h1 > shape->Hkv) {
-    *st = VC_ERR_INVALID;
-    return cudaSuccess;
-  }
-  if (shape->d != 64 && shape->d != 128) {
-    *st = VC_ERR_UNSUPPORTED;
-    return cudaSuccess;
-  }
+// One launch (verification kernel, then the combine of split units) over the requests sel[0..n):
+// rows 0 = one unit per (request, KV head, row tile); 1 = row-tile mode (every row tile of a head in
+// one CTA, one softmax warpgroup); 2 = pair mode (both row tiles of a two-tile head in one CTA, a
+// softmax warpgroup each).
+static cudaError_t verify_launch(const vc_shape* shape, const vc_verify_req* req, const int* sel, int n, int rows,
+                                 int h0, int h1, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream,
+                                 vc_status* st) {
   const int d = shape->d, G = shape->Hq / shape->Hkv;
   VerifyParams p;  // about 18 KB: the tensor maps travel as kernel parameters
   memset(&p, 0, sizeof(p));
-  p.B = shape->B;
+  p.B = n;
   p.Hq = shape->Hq;
   p.Hkv = shape->Hkv;
   p.G = G;
@@ -1113,24 +1391,11 @@ cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h
   const int nh = h1 - h0;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
   p.dev_status = dev_status;
-  // row-tile mode, on request (VC_VERIFY_ROWS=1), when some KV head has more than one 128-row tile
-  // and none more than VROWS. It reads each K/V tile once (1.00x the algorithmic bytes at 320 rows
-  // per KV head against 3.00x), but holding three O accumulators takes all of TMEM, so it runs one
-  // CTA (four softmax warps) per SM and its softmax is latency-bound: measured 1.36x slower at 320
-  // rows and 2x slower on the mixed serving batch than one unit per row tile at two CTAs per SM.
-  int max_mt = 1;
-  for (int b = 0; b < shape->B; ++b) {
-    const int mtb = (req[b].n_rows * G + VM - 1) / VM;
-    if (mtb > max_mt) max_mt = mtb;
-  }
-  {
-    const char* ev = getenv("VC_VERIFY_ROWS");
-    p.rows = max_mt >= 2 && max_mt <= VROWS && ev && atoi(ev) == 1 ? 1 : 0;
-  }
+  p.rows = rows;
   int64_t tiles = 0;
   int32_t units = 0, ugs = 0, max_rows = 0;
-  for (int b = 0; b < shape->B; ++b) {
-    const vc_verify_req& r = req[b];
+  for (int b = 0; b < n; ++b) {
+    const vc_verify_req& r = req[sel[b]];
     const vc_kv_full& f = r.full;
     if (!a16(f.k) || !a16(f.v) || !a16(r.q) || !a16(r.o) || !a16(r.k_new) || !a16(r.v_new) || f.ctx < 1 ||
         f.cap < f.ctx || r.n_rows < 1 || r.new_cap < r.n_rows) {
@@ -1173,5 +1438,62 @@ cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h
   p.ws_lse = p.ws_o + slots * VM * d;
   return d == 128 ? launch_verify_t<128>(p, stream) : launch_verify_t<64>(p, stream);
 }
+
+cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h0, int h1, void* ws,
+                          size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, vc_status* st) {
+  *st = VC_OK;
+  if (!shape || shape->B < 1 || shape->B > VC_MAX_BATCH || shape->Hkv < 1 || shape->Hq < shape->Hkv ||
+      shape->Hq % shape->Hkv != 0 || !req || h0 < 0 || h1 <= h0 || h1 > shape->Hkv) {
+    *st = VC_ERR_INVALID;
+    return cudaSuccess;
+  }
+  if (shape->d != 64 && shape->d != 128) {
+    *st = VC_ERR_UNSUPPORTED;
+    return cudaSuccess;
+  }
+  const int G = shape->Hq / shape->Hkv;
+  // How each request's KV heads are verified, by their 128-row tiles (L x G rows):
+  //   one tile: one unit per (request, KV head) at two CTAs per SM;
+  //   exactly two: pair mode (VC_VERIFY_PAIR=0 turns it off): each K/V tile read once for both
+  //     tiles, with a softmax warpgroup per tile;
+  //   three or more: one unit per row tile (each reads KV_full again), or with VC_VERIFY_ROWS=1 the
+  //     row-tile mode for up to VROWS tiles (read once; one softmax warpgroup per CTA, so slower:
+  //     1.36x at 320 rows per KV head).
+  // Requests of different kinds go to separate launches, one after the other on the stream; every
+  // request is checked before either is launched.
+  int sel_a[VC_MAX_BATCH], sel_p[VC_MAX_BATCH], na = 0, np = 0, max_mt = 1;
+  for (int b = 0; b < shape->B; ++b) {
+    const vc_verify_req& r = req[b];
+    const vc_kv_full& f = r.full;
+    if (!a16(f.k) || !a16(f.v) || !a16(r.q) || !a16(r.o) || !a16(r.k_new) || !a16(r.v_new) || f.ctx < 1 ||
+        f.cap < f.ctx || r.n_rows < 1 || r.new_cap < r.n_rows) {
+      *st = VC_ERR_INVALID;
+      return cudaSuccess;
+    }
+    const int mtb = (r.n_rows * G + VM - 1) / VM;
+    if (mtb > max_mt) max_mt = mtb;
+  }
+  const char* er = getenv("VC_VERIFY_ROWS");
+  if (max_mt >= 2 && max_mt <= VROWS && er && atoi(er) == 1) {
+    for (int b = 0; b < shape->B; ++b) sel_a[na++] = b;
+    return verify_launch(shape, req, sel_a, na, 1, h0, h1, ws, ws_bytes, dev_status, stream, st);
+  }
+  const char* ep = getenv("VC_VERIFY_PAIR");
+  const bool pair = !(ep && atoi(ep) == 0);
+  for (int b = 0; b < shape->B; ++b) {
+    const int mtb = (req[b].n_rows * G + VM - 1) / VM;
+    if (pair && mtb == 2)
+      sel_p[np++] = b;
+    else
+      sel_a[na++] = b;
+  }
+  if (na > 0) {
+    const cudaError_t e = verify_launch(shape, req, sel_a, na, 0, h0, h1, ws, ws_bytes, dev_status, stream, st);
+    if (e != cudaSuccess || *st != VC_OK) return e;
+  }
+  if (np > 0) return verify_launch(shape, req, sel_p, np, 2, h0, h1, ws, ws_bytes, dev_status, stream, st);
+  return cudaSuccess;
+}
+
 
 }  // namespace vc

@@ -91,14 +91,35 @@ def test_verify_row_tiles_split_layouts(ctas, rows_mode, monkeypatch):
     _check(w, [0, 1], env_ctas=ctas, monkeypatch=monkeypatch)
 
 
-@pytest.mark.parametrize("rows_mode", ["1", "0"])
-def test_verify_row_tiles_mixed_one_and_two(rows_mode, monkeypatch):
-    """One call with KV heads of one row tile (L 25 x G 4 = 100 rows) and of two (L 40: 160 rows):
-    the row-tile mode holds both kinds of units."""
-    monkeypatch.setenv("VC_VERIFY_ROWS", rows_mode)
+def _mode_env(monkeypatch, mode):
+    """rows: every row tile of a head in one CTA (VC_VERIFY_ROWS=1); pair: the default, two-tile
+    heads in pair mode and the rest one unit per row tile (two launches); units: one unit per row
+    tile for every head (VC_VERIFY_PAIR=0)."""
+    monkeypatch.setenv("VC_VERIFY_ROWS", "1" if mode == "rows" else "0")
+    monkeypatch.setenv("VC_VERIFY_PAIR", "0" if mode == "units" else "1")
+
+
+@pytest.mark.parametrize("mode", ["rows", "pair", "units"])
+def test_verify_row_tiles_mixed_one_and_two(mode, monkeypatch):
+    """One call with KV heads of one row tile (L 25 x G 4 = 100 rows, L 32: 128) and of two (L 40:
+    160 rows, L 33: 132): the row-tile mode holds both kinds of units; by default the two-tile
+    requests go to a pair-mode launch and the others to the one-unit-per-tile launch."""
+    _mode_env(monkeypatch, mode)
     w = configs.scaled(configs.mixed_serving(), ctx_div=32, batch=4)
     w.L = [25, 40, 33, 32]
     _check(w, [0, 1, 2, 3])
+
+
+@pytest.mark.parametrize("ctas", [1, 5, 1000])
+@pytest.mark.parametrize("mode", ["pair", "units"])
+def test_verify_two_row_tiles_split_layouts(ctas, mode, monkeypatch):
+    """Two row tiles per KV head (L 20 x G 8 = 160 rows), ragged contexts, the pair mode's launch
+    cut into one CTA, a few and one CTA per KV tile: the two warpgroups' partials of split heads
+    merge through the combine kernel."""
+    _mode_env(monkeypatch, mode)
+    w = configs.scaled(configs.llama70b_offload4(), ctx_div=256, batch=3, L=20)
+    w.ctx = [517, 1000, 64]
+    _check(w, [0, 1, 2], env_ctas=ctas, monkeypatch=monkeypatch)
 
 
 @pytest.mark.parametrize("L,ctx", [(1, 1), (1, 64), (70, 65), (64, 200), (3, 5000)])
