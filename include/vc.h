@@ -36,8 +36,11 @@
  *   - Kernel choices read from the environment by each call, with the same results either way:
  *     VC_DRAFT_TC=1 runs vc_draft_attn for quantised caches at d = 128 with at most 8 query heads
  *     per KV head on the tcgen05 draft kernel (the mma.sync kernel is the default and faster);
- *     VC_VERIFY_ROWS=1 verifies every 128-row tile of a (request, KV head) in one CTA, reading its
- *     KV_full once (by default each row tile is a unit of its own and reads it again).
+ *     a (request, KV head) whose drafts fill two 128-row tiles (129 to 256 rows) is verified by one
+ *     CTA that reads its KV_full once for both tiles, and VC_VERIFY_PAIR=0 gives each of those
+ *     tiles a unit of its own instead; a head of one tile, or of three or more, has a unit per
+ *     tile, each of which reads KV_full; VC_VERIFY_ROWS=1 verifies every tile of every head in one
+ *     CTA per head, reading KV_full once (slower at present).
  */
 #ifndef VC_H_
 #define VC_H_
