@@ -4,14 +4,17 @@ Tolerance for attention outputs (bf16 I/O, fp32 accumulation), oracle in float64
   1. every element: |gpu - oracle| <= max(1e-2, 2e-2 * |oracle|) (max-abs 1e-2 or max-rel 2e-2);
   2. every head (the outputs of one query head, over all rows compared): relative L2 error
      ||gpu - oracle|| / ||oracle|| <= 5e-3;
-  3. every element: |gpu - oracle| <= 2^-7 |oracle| + 2^-7 rms(oracle's output vector holding it),
+  3. every element: |gpu - oracle| <= 2^-6 |oracle| + 2^-6 rms(oracle's output vector holding it),
      the vector being one query row's d outputs for one head (each has its own scale: a row that
      one key dominates is as large as that key's value row).
 Check 1 alone cannot see a kernel that loses a few chunks of a long keep-set: at 8192 kept rows the
 outputs have a standard deviation near 0.011, far below its 1e-2 floor, while dropping 64 of the
-rows or scaling the scores by 0.95 moves them by several percent. A correct kernel rounds once to
-bf16 (relative 2^-9) after fp32 accumulation, so checks 2 and 3 leave it a wide margin
-(tests/test_tolerance.py plants both mistakes and checks that they fail here).
+rows or scaling the scores by 0.95 moves them by several percent (tests/test_tolerance.py plants
+both mistakes and checks that they fail here). A correct kernel rounds twice: the attention weights
+P to bf16 (fp16 in the quantised draft) as the operand of the P V product, and the output to bf16,
+each after fp32 accumulation. Check 3 allows 2^-7 for each rounding: on the CPU, that arithmetic
+(bf16 P, fp32 sums, bf16 output) reaches 0.9 of a single 2^-7 over 790K elements of the four
+verify row tile case, and one GPU element of 1.6M reached 1.02 of it.
 Integer, index and byte outputs are compared bit for bit.
 """
 from __future__ import annotations
@@ -23,7 +26,7 @@ from workloads import gen, DROP, QUANT
 
 ATOL, RTOL = 1e-2, 2e-2
 REL_L2 = 5e-3
-TIGHT = 2.0 ** -7
+TIGHT = 2.0 ** -6
 
 
 def _by_head(a):
@@ -69,7 +72,7 @@ def assert_attn_close(gpu, ref, what=""):
     if rel > REL_L2:
         raise AssertionError(f"{what}: relative L2 error {rel:.3g} of a head exceeds {REL_L2}")
     if n3:
-        raise AssertionError(f"{what}: {n3} elements beyond 2^-7 |oracle| + 2^-7 rms(oracle's output vector); {worst}")
+        raise AssertionError(f"{what}: {n3} elements beyond 2^-6 |oracle| + 2^-6 rms(oracle's output vector); {worst}")
     return float(err.max())
 
 
