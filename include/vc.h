@@ -39,8 +39,10 @@
  *     a (request, KV head) whose drafts fill two 128-row tiles (129 to 256 rows) is verified by one
  *     CTA that reads its KV_full once for both tiles, and VC_VERIFY_PAIR=0 gives each of those
  *     tiles a unit of its own instead; a head of one tile, or of three or more, has a unit per
- *     tile, each of which reads KV_full; VC_VERIFY_ROWS=1 verifies every tile of every head in one
- *     CTA per head, reading KV_full once (slower at present).
+ *     tile, each of which reads KV_full; VC_VERIFY_TRIO=1 verifies a head of exactly three tiles
+ *     in one CTA with two softmax warpgroups, reading KV_full once (slower at present);
+ *     VC_VERIFY_ROWS=1 verifies every tile of every head in one CTA per head with one softmax
+ *     warpgroup, reading KV_full once (slower still).
  */
 #ifndef VC_H_
 #define VC_H_

@@ -124,7 +124,12 @@ struct VerifyReqDev {
 // CTA with a softmax warpgroup each (warps 0-3 and 6-9), each with its own Q and P tiles, S double
 // buffer and O accumulator; a K/V tile is loaded once and serves both, and the two warpgroups keep
 // the softmax throughput of two one-tile CTAs.
-constexpr int VMODE_ATTN = 0, VMODE_STATS = 1, VMODE_VOTES = 2, VMODE_ROWS = 3, VMODE_PAIR = 4;
+// VMODE_TRIO (opt-in, VC_VERIFY_TRIO=1, for a KV head of exactly three row tiles): all three in
+// one CTA, reading each K/V tile once. Three O accumulators take 384 TMEM columns, which leaves one 64-column S
+// buffer for each of two softmax warpgroups: warpgroup 0 holds row tiles 0 and 2, warpgroup 1 row
+// tile 1. A warpgroup's S buffer is freed as soon as its softmax has read it into registers, so the
+// next S is computed while that softmax works; P alternates between two shared-memory tiles.
+constexpr int VMODE_ATTN = 0, VMODE_STATS = 1, VMODE_VOTES = 2, VMODE_ROWS = 3, VMODE_PAIR = 4, VMODE_TRIO = 5;
 constexpr int VROWS = 3;  // row tiles a row-tile-mode CTA holds (3 x 128 O columns + S fill TMEM)
 
 struct VerifyParams {
@@ -132,7 +137,7 @@ struct VerifyParams {
   VerifyReqDev req[VC_MAX_BATCH];
   int32_t B, Hq, Hkv, G, n_cta, n_units;
   int32_t h0;  // first KV head of the call's head range (units cover heads h0 .. h0 + nh - 1)
-  int32_t rows;  // 1: row-tile mode (the tile sequence runs over (request, KV head), all row tiles per unit)
+  int32_t rows;  // 0: a unit per row tile; 1 row-tile, 2 pair, 3 trio mode: a unit per (request, KV head)
   int64_t total_tiles;
   float scale_log2;
   float* ws_o;    // [slots][128][d]
@@ -140,31 +145,40 @@ struct VerifyParams {
   int32_t* dev_status;
 };
 
-template <int D, int NQ = 1, bool PAIR = false>
+// NQ: Q tiles a CTA holds; MWG: 0 one softmax warpgroup, 1 pair mode, 2 trio mode.
+template <int D, int NQ = 1, int MWG = 0>
 struct VCfg {
+  static constexpr bool PAIR = MWG == 1, TRIO = MWG == 2;
   static constexpr int KB = D / 64;                // 64-channel (128-byte) blocks
   static constexpr int Q_BYTES = KB * VM * 128;    // Q tile, K-major SW128 (NQ of them)
   static constexpr int P_BYTES = VM * 128;         // P tile (64 tokens), K-major SW128
   static constexpr int KV_BYTES = KB * VBN * 128;  // one K (or V) tile
-  static constexpr int OFF_P = NQ * Q_BYTES;       // P tile (pair mode: one per warpgroup)
-  static constexpr int OFF_K = OFF_P + (PAIR ? 2 : 1) * P_BYTES;  // K stages [2]
+  static constexpr int OFF_P = NQ * Q_BYTES;       // P tile (pair mode: one per warpgroup; trio: two)
+  static constexpr int OFF_K = OFF_P + (TRIO ? 4 : PAIR ? 2 : 1) * P_BYTES;  // K stages [2]
   static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;  // V stages [2]
   static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr int SMEM = OFF_BAR + 256;
+  static_assert(SMEM <= 227 * 1024, "one CTA's shared memory");
   static constexpr int SCOL = 64;                  // S double buffer: TMEM columns [0,64) and [64,128)
   static constexpr int OCOL = 128;                 // O: TMEM columns [128, 128 + D) (row tile m: + m D)
   static constexpr uint32_t TCOLS = NQ == 1 ? 256 : 512;
   static_assert(OCOL + NQ * D <= (int)TCOLS, "O accumulators fit the TMEM allocation");
-  static constexpr int THREADS = PAIR ? 352 : 192;  // warps 0-3 softmax, 4 MMA issue, 5 TMA loads (pair: 6-9 softmax, 10 MMA issue)
+  static constexpr int THREADS = MWG ? 352 : 192;  // warps 0-3 softmax, 4 MMA issue, 5 TMA loads (pair, trio: 6-9 softmax, 10 MMA issue)
   // pair mode: warpgroup m's S double buffer at TMEM columns [m 128, m 128 + 128), its O at 256 + m D
   static constexpr int PSCOL = 128;
   static constexpr int POCOL = 256;
   static_assert(!PAIR || (POCOL + 2 * D <= (int)TCOLS && NQ == 2), "pair mode fits TMEM");
+  // trio mode: warpgroup w's S buffer at TMEM columns [64 w, 64 w + 64), row tile m's O at 128 + m D
+  static_assert(!TRIO || (OCOL + 3 * D <= (int)TCOLS && NQ == 3), "trio mode fits TMEM");
   // votes mode: an fp16 all-ones [128][128] A operand over the (unused) V stages
   static constexpr int ONES_BYTES = VM * 128 * 2;
   static constexpr int OFF_BAR_VOTES = OFF_V + ONES_BYTES > OFF_BAR ? OFF_V + ONES_BYTES : OFF_BAR;
   static constexpr int SMEM_VOTES = OFF_BAR_VOTES + 256;
 };
+
+template <int D, int MODE>
+using VCfgOf = VCfg<D, MODE == VMODE_ROWS ? VROWS : MODE == VMODE_TRIO ? 3 : MODE == VMODE_PAIR ? 2 : 1,
+                    MODE == VMODE_TRIO ? 2 : MODE == VMODE_PAIR ? 1 : 0>;
 
 __device__ __forceinline__ int find_req(const VerifyParams& p, int64_t tile) {
   int b = 0;
@@ -203,9 +217,11 @@ __device__ __forceinline__ VPiece verify_piece(const VerifyParams& p, int64_t po
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE_ROWS || MODE == VMODE_PAIR) ? 1 : 2)
+__global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 352 : 192,
+                                  (MODE == VMODE_ROWS || MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 1 : 2)
     verify_attn_kernel(const __grid_constant__ VerifyParams p) {
-  using C = VCfg<D, MODE == VMODE_ROWS ? VROWS : (MODE == VMODE_PAIR ? 2 : 1), MODE == VMODE_PAIR>;
+  using C = VCfgOf<D, MODE>;
+  constexpr bool KV_HEAD_UNITS = MODE == VMODE_ROWS || MODE == VMODE_PAIR || MODE == VMODE_TRIO;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte aligned tiles
@@ -234,6 +250,10 @@ __global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE
   uint64_t* ofull1 = bars + 19;
   uint64_t* qfull1 = bars + 20;
   uint64_t* xbar1 = bars + 21;  // warpgroup 1's MMA issuer's drain
+  // trio mode, warpgroup w's block at bars + 16 + 8 w (in place of the pair block): S filled, S read
+  // into registers (4 softmax warps), P tile b written [2] (4 warps), P V of P tile b done [2], the
+  // unit's Q tiles written (4 warps), its MMA issuer's drain
+  auto trio_bars = [&](int w) { return bars + 16 + 8 * w; };
 
   if (warp == 0) tc05::alloc(tslot, C::TCOLS);
   if (tid == 0) {
@@ -250,12 +270,21 @@ __global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE
     mbar_init(ofull, 1);
     mbar_init(qfull, 4);
     mbar_init(xbar, 1);
-    if (MODE == VMODE_PAIR) {
+    if (MODE == VMODE_PAIR || MODE == VMODE_TRIO) {
       // a K (V) stage is free once both warpgroups' issuers have committed their S (P V) of it
       for (int i = 0; i < 2; ++i) {
         mbar_init(&kempty[i], 2);
         mbar_init(&vempty[i], 2);
       }
+    }
+    if (MODE == VMODE_TRIO) {
+      for (int w = 0; w < 2; ++w) {
+        uint64_t* tb = trio_bars(w);
+        const uint32_t cnt[8] = {1, 4, 4, 4, 1, 1, 4, 1};
+        for (int i = 0; i < 8; ++i) mbar_init(&tb[i], cnt[i]);
+      }
+    }
+    if (MODE == VMODE_PAIR) {
       mbar_init(xbar1, 1);
       mbar_init(&sfull1[0], 1);
       mbar_init(&sfull1[1], 1);
@@ -350,6 +379,97 @@ __global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE
     return ok;
   };
 
+  // trio mode: the MMA chain of warpgroup w (warp 4 for w = 0, warp 10 for w = 1) over the CTA's
+  // units. Its steps are (KV tile, row tile) pairs in order, its row tiles being w and w + 2 of the
+  // three. Step k's S goes into the warpgroup's one S buffer once the softmax has read step
+  // k - 1's out of it (early in that step), and S runs one KV tile ahead of P V: the P V of a
+  // step follows the S of the same row tile on the next KV tile (for warpgroup 0, two steps
+  // later). So warpgroup 0's next S never queues behind a P V that waits for the P of the step
+  // just finished, and the softmax of step k, which rewrites the P tile of step k - 2, finds that
+  // P V issued; a lag of one KV tile, not more, keeps each V stage in use for about one KV tile.
+  // A unit's pending P V are issued before the next unit's Q is awaited. Both issuers commit each
+  // K stage's release after their last S on it and each V stage's after their last P V on it.
+  auto trio_issue = [&](int w) -> bool {
+    constexpr uint32_t IDESC_S = tc05::idesc_bf16(VM, VBN, false);
+    constexpr uint32_t IDESC_O = tc05::idesc_bf16(VM, D, true);
+    uint64_t* tb = trio_bars(w);
+    uint64_t *sf = tb, *sr = tb + 1, *pf = tb + 2, *of = tb + 4, *qf = tb + 6;
+    const int ntw = w == 0 ? 2 : 1;
+    const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP) + 2 * w * C::P_BYTES, aK = smem_u32(smem + C::OFF_K),
+                   aV = smem_u32(smem + C::OFF_V), tS = tmem + w * VBN;
+    uint32_t g = 0, k = 0, uq = 0;
+    bool ok = true;
+    // a step whose P V is still to be issued: row tile m, KV tile (V stage) gp; acc: not the unit's
+    // first KV tile; last: this warpgroup's last row tile on that V tile
+    struct Pend {
+      uint32_t s, gp;
+      int m;
+      bool acc, last;
+    };
+    auto pv = [&](const Pend& e) -> bool {
+      if (!vwait(&vfull[e.gp & 1], (e.gp >> 1) & 1, p.dev_status, s_abort)) return false;
+      if (!vwait(&pf[e.s & 1], (e.s >> 1) & 1, p.dev_status, s_abort)) return false;
+      tc05::fence_after();
+      const uint32_t pbuf = aP + (e.s & 1) * C::P_BYTES, vaddr = aV + (e.gp & 1) * C::KV_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < VBN / 16; ++kk) {
+        const uint64_t da = tc05::sdesc_sw128(pbuf + kk * 32, 16, 1024);
+        const uint64_t db = tc05::sdesc_sw128(vaddr + kk * 2048, VBN * 128, 1024);
+        tc05::mma_bf16(tmem + C::OCOL + e.m * D, da, db, IDESC_O, (e.acc || kk > 0) ? 1u : 0u);
+      }
+      tc05::commit(&of[e.s & 1]);
+      if (e.last) tc05::commit(&vempty[e.gp & 1]);
+      return true;
+    };
+    for (int64_t pos = beg; pos < end && ok;) {
+      const VPiece q = verify_piece(p, pos, end);
+      const int nt = q.j1 - q.j0;
+      ok = vwait(qf, uq & 1, p.dev_status, s_abort);
+      ++uq;
+      Pend pa{}, pb{};  // pending P V, oldest first
+      int np = 0;
+      for (int jj = 0; jj < nt && ok; ++jj) {
+        const uint32_t gc = g + jj;
+        if (!vwait(&kfull[gc & 1], (gc >> 1) & 1, p.dev_status, s_abort)) {
+          ok = false;
+          break;
+        }
+        for (int i = 0; i < ntw && ok; ++i) {
+          const int m = w + 2 * i;
+          // the softmax has read step k - 1's S out of the buffer
+          if (k >= 1 && !vwait(sr, (k - 1) & 1, p.dev_status, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          const uint32_t kaddr = aK + (gc & 1) * C::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t da =
+                tc05::sdesc_sw128(aQ + m * C::Q_BYTES + (kk >> 2) * (VM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = tc05::sdesc_sw128(kaddr + (kk >> 2) * (VBN * 128) + (kk & 3) * 32, 16, 1024);
+            tc05::mma_bf16(tS, da, db, IDESC_S, kk > 0);
+          }
+          tc05::commit(sf);
+          if (i == ntw - 1) tc05::commit(&kempty[gc & 1]);
+          if (np == ntw) {
+            ok = pv(pa);
+            pa = pb;
+            --np;
+          }
+          (np == 0 ? pa : pb) = Pend{k, gc, m, jj > 0, i == ntw - 1};
+          ++np;
+          ++k;
+        }
+      }
+      if (np >= 1 && ok) ok = pv(pa);
+      if (np == 2 && ok) ok = pv(pb);
+      g += nt;
+      pos += nt;
+    }
+    return ok;
+  };
+
   if (warp == 5) {
     // ---- TMA producer: K of tile g, then V of tile g - 1 (K runs a tile ahead of V) ----------
     if (lane == 0) {
@@ -373,11 +493,11 @@ __global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE
       bool ok = true;
       for (int64_t pos = beg; pos < end && ok;) {
         const VPiece q = verify_piece(p, pos, end);
-        const int hk = p.h0 + ((MODE == VMODE_ROWS || MODE == VMODE_PAIR) ? q.ul : q.ul / p.req[q.b].mtiles);
+        const int hk = p.h0 + (KV_HEAD_UNITS ? q.ul : q.ul / p.req[q.b].mtiles);
         for (int j = q.j0; j < q.j1 && ok; ++j, ++g) {
           ok = load(false, gk, q.b, hk, j);
           if (ok) ++gk;
-          if ((MODE == VMODE_ATTN || MODE == VMODE_ROWS || MODE == VMODE_PAIR) && ok && pv_pending) {
+          if ((MODE == VMODE_ATTN || KV_HEAD_UNITS) && ok && pv_pending) {
             ok = load(true, gv, pv_b, pv_hk, pv_j);
             if (ok) ++gv;
           }
@@ -385,7 +505,7 @@ __global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE
         }
         pos += q.j1 - q.j0;
       }
-      if ((MODE == VMODE_ATTN || MODE == VMODE_ROWS || MODE == VMODE_PAIR) && ok && pv_pending &&
+      if ((MODE == VMODE_ATTN || KV_HEAD_UNITS) && ok && pv_pending &&
           load(true, gv, pv_b, pv_hk, pv_j))
         ++gv;
       if (*s_abort) {
@@ -494,7 +614,8 @@ __global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE
       // issuer (warp 10, below) -- so the two row tiles' chains run independently; each commits its
       // S and P V to the shared K and V stage releases (two arrivals each)
       if constexpr (MODE == VMODE_PAIR) ok = pair_issue(0);
-      for (int64_t pos = beg; pos < end && ok && MODE != VMODE_ROWS && MODE != VMODE_PAIR;) {
+      if constexpr (MODE == VMODE_TRIO) ok = trio_issue(0);
+      for (int64_t pos = beg; pos < end && ok && !KV_HEAD_UNITS;) {
         const VPiece q = verify_piece(p, pos, end);
         const int nt = q.j1 - q.j0;
         ok = vwait(qfull, u & 1, p.dev_status, s_abort);
@@ -531,6 +652,13 @@ __global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE
       pair_issue(1);
       tc05::commit(xbar1);
       mbar_wait_bounded(xbar1, 0, p.dev_status);
+    }
+  } else if (MODE == VMODE_TRIO && warp == 10) {
+    // ---- trio mode: warpgroup 1's MMA issue -------------------------------------------------------
+    if (lane == 0) {
+      trio_issue(1);
+      tc05::commit(&trio_bars(1)[7]);
+      mbar_wait_bounded(&trio_bars(1)[7], 0, p.dev_status);
     }
   } else {
     // ---- softmax warps: thread tid owns TMEM lane tid = query row tid of the tile ---------------
@@ -682,6 +810,180 @@ __global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE
           }
         }
         if (row_ok && !whole) p.ws_lse[slot * VM + rt] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+        tc05::fence_before();
+      }
+    }
+    if constexpr (MODE == VMODE_TRIO) {
+      // warpgroup w (warps 0-3: 0, warps 6-9: 1) owns row tiles w and w + 2 of each unit (warpgroup
+      // 1: tile 1 only); thread rt = (warp % 4) * 32 + lane owns row rt of each, its TMEM lane
+      const int w = warp >= 6 ? 1 : 0, ntw = w == 0 ? 2 : 1;
+      const int rt = (warp & 3) * 32 + lane;
+      const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
+      uint64_t* tb = trio_bars(w);
+      uint64_t *sf = tb, *sr = tb + 1, *pf = tb + 2, *of = tb + 4, *qf = tb + 6;
+      uint8_t* sPw = sP + 2 * w * C::P_BYTES;
+      const uint32_t t_s = tmem + lo + w * VBN;
+      uint32_t t = 0;  // this warpgroup's steps over the CTA's units
+      // P V of step k done (P tile k & 1). Every step t >= 2 waits for k = t - 2 before it rewrites
+      // that tile, so a wait for k finds the P V of k - 2 observed, and the P V of k + 2 cannot
+      // have been issued (it needs this warpgroup's P of k + 2): the parity wait is exact
+      auto pv_done = [&](uint32_t k) { return vwait(&of[k & 1], (k >> 1) & 1, p.dev_status, s_abort); };
+      for (int64_t pos = beg; pos < end && ok;) {
+        const VPiece q = verify_piece(p, pos, end);
+        const VerifyReqDev& R = p.req[q.b];
+        const int nt = q.j1 - q.j0;
+        pos += nt;
+        const int hk = p.h0 + q.ul;
+        const int ug_global = R.ug_begin + q.ul;
+        // this thread's query rows into the warpgroup's Q tiles (the previous unit's MMAs are
+        // complete: its outputs waited for its last P V, which follow all its S)
+        for (int i = 0; i < ntw; ++i) {
+          const int m = w + 2 * i;
+          const int Rw = m * VM + rt, qi = Rw / p.G, qg = Rw % p.G;
+          const bool row_ok = qi < R.n_rows;
+          const uint4* src = reinterpret_cast<const uint4*>(R.q + ((size_t)qi * p.Hq + hk * p.G + qg) * D);
+          uint8_t* dQ = sQ + m * C::Q_BYTES;
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint4 v = row_ok ? __ldg(src + kb * 8 + ch) : make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(dQ + kb * (VM * 128) + rt * 128 + ((ch ^ (rt & 7)) << 4)) = v;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qf);
+        float m_run0 = -INFINITY, l_run0 = 0.f, m_run1 = -INFINITY, l_run1 = 0.f;
+        for (int jj = 0; jj < nt && ok; ++jj) {
+          const int j = q.j0 + jj;
+          for (int i = 0; i < ntw; ++i) {
+            const int m = w + 2 * i;
+            const int qi = (m * VM + rt) / p.G;
+            if (!vwait(sf, t & 1, p.dev_status, s_abort)) {
+              ok = false;
+              break;
+            }
+            tc05::fence_after();
+            float x[VBN];
+            {
+              uint32_t r0[32], r1[32];
+              tc05::ld32(t_s, r0);
+              tc05::ld32(t_s + 32, r1);
+              tc05::wait_ld();
+              tc05::fence_before();  // the buffer may take the next step's S
+              __syncwarp();
+              if (lane == 0) mbar_arrive(sr);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                x[e] = __uint_as_float(r0[e]);
+                x[32 + e] = __uint_as_float(r1[e]);
+              }
+            }
+            {
+              const int last = j < R.n_full ? R.ctx - j * VBN - 1 : qi - (j - R.n_full) * VBN;  // last visible key
+              if (last < VBN - 1) {
+#pragma unroll
+                for (int e = 0; e < VBN; ++e)
+                  if (e > last) x[e] = -INFINITY;
+              }
+            }
+            const float mx = row_max(x) * p.scale_log2;
+            // P tile t & 1 was read by the P V of step t - 2 (for warpgroup 0, also the last P V into
+            // this row tile's O)
+            if (t >= 2 && !pv_done(t - 2)) {
+              ok = false;
+              break;
+            }
+            float mr = i ? m_run1 : m_run0, lr = i ? l_run1 : l_run0;
+            const float m_new = fmaxf(mr, mx);
+            const bool need = jj > 0 && m_new > mr + 8.f;
+            if (jj == 0) {
+              mr = m_new;
+            } else if (__any_sync(0xffffffffu, need)) {
+              // O is rescaled once its last P V has completed: warpgroup 1's is the previous step's,
+              // warpgroup 0's was waited for above
+              if (ntw == 1 && !pv_done(t - 1)) {
+                ok = false;
+                break;
+              }
+              tc05::fence_after();
+              float f = 1.f;
+              if (need) {
+                f = ex2_approx(mr - m_new);
+                lr *= f;
+                mr = m_new;
+              }
+              const uint32_t t_o = tmem + lo + C::OCOL + m * D;
+#pragma unroll 1
+              for (int cb = 0; cb < D / 32; ++cb) {
+                uint32_t r[32];
+                tc05::ld32(t_o + cb * 32, r);
+                tc05::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                tc05::st32(t_o + cb * 32, r);
+              }
+              tc05::wait_st();
+            }
+            const float mu = (mr == -INFINITY) ? 0.f : mr;
+            lr += row_exp_to_p(x, p.scale_log2, mu, sPw + (t & 1) * C::P_BYTES + rt * 128, rt);
+            if (i) {
+              m_run1 = mr;
+              l_run1 = lr;
+            } else {
+              m_run0 = mr;
+              l_run0 = lr;
+            }
+            fence_proxy_async_smem();
+            tc05::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pf[t & 1]);
+            ++t;
+          }
+        }
+        if (!ok) break;
+        // outputs: each row tile's last P V of the unit (steps t - ntw .. t - 1)
+        const bool whole = (q.j0 == 0 && q.j1 == R.tiles);
+        for (int i = 0; i < ntw && ok; ++i) {
+          const int m = w + 2 * i;
+          if (!pv_done(t - ntw + i)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          const int Rw = m * VM + rt, qi = Rw / p.G, qg = Rw % p.G;
+          const bool row_ok = qi < R.n_rows;
+          const float lr = i ? l_run1 : l_run0, mr = i ? m_run1 : m_run0;
+          const float inv = lr > 0.f ? 1.f / lr : 0.f;
+          const size_t slot = (size_t)(c + ug_global) * VROWS + m;
+          const uint32_t t_o = tmem + lo + C::OCOL + m * D;
+#pragma unroll 1
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t r[32];
+            tc05::ld32(t_o + cb * 32, r);  // warp-collective: every lane loads
+            tc05::wait_ld();
+            if (!row_ok) continue;
+            if (whole) {
+              uint4* dst = reinterpret_cast<uint4*>(R.o + ((size_t)qi * p.Hq + hk * p.G + qg) * D + cb * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint32_t wv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  wv[e] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * e]) * inv, __uint_as_float(r[8 * v + 2 * e + 1]) * inv);
+                dst[v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * VM + rt) * D + cb * 32);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                     __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+            }
+          }
+          if (row_ok && !whole) p.ws_lse[slot * VM + rt] = lr > 0.f ? mr + log2f(lr) : -INFINITY;
+        }
         tc05::fence_before();
       }
     }
@@ -844,7 +1146,7 @@ __global__ void __launch_bounds__(MODE == VMODE_PAIR ? 352 : 192, (MODE == VMODE
       tc05::fence_before();
       pos += nt;
     }
-    for (int64_t pos = beg; pos < end && ok && MODE != VMODE_ROWS && MODE != VMODE_PAIR;) {
+    for (int64_t pos = beg; pos < end && ok && !KV_HEAD_UNITS;) {
       const VPiece q = verify_piece(p, pos, end);
       const VerifyReqDev& R = p.req[q.b];
       const int nt = q.j1 - q.j0;
@@ -1250,7 +1552,7 @@ size_t verify_workspace_size(const vc_shape* s, int32_t max_rows) {
 
 template <int D, int MODE>
 static cudaError_t launch_modes_t(const VerifyParams& p, cudaStream_t s) {
-  using C = VCfg<D, MODE == VMODE_ROWS ? VROWS : (MODE == VMODE_PAIR ? 2 : 1), MODE == VMODE_PAIR>;
+  using C = VCfgOf<D, MODE>;
   constexpr int SMEM = MODE == VMODE_VOTES ? C::SMEM_VOTES : C::SMEM;
   static std::atomic<uint64_t> attr{0};
   {
@@ -1262,7 +1564,8 @@ static cudaError_t launch_modes_t(const VerifyParams& p, cudaStream_t s) {
 
 template <int D>
 static cudaError_t launch_verify_t(const VerifyParams& p, cudaStream_t s) {
-  cudaError_t e = p.rows == 2   ? launch_modes_t<D, VMODE_PAIR>(p, s)
+  cudaError_t e = p.rows == 3   ? launch_modes_t<D, VMODE_TRIO>(p, s)
+                  : p.rows == 2 ? launch_modes_t<D, VMODE_PAIR>(p, s)
                   : p.rows == 1 ? launch_modes_t<D, VMODE_ROWS>(p, s)
                                 : launch_modes_t<D, VMODE_ATTN>(p, s);
   if (e != cudaSuccess) return e;
@@ -1361,7 +1664,8 @@ cudaError_t launch_obs_passes(const ObsArgs& a, cudaStream_t s) {
 // One launch (verification kernel, then the combine of split units) over the requests sel[0..n):
 // rows 0 = one unit per (request, KV head, row tile); 1 = row-tile mode (every row tile of a head in
 // one CTA, one softmax warpgroup); 2 = pair mode (both row tiles of a two-tile head in one CTA, a
-// softmax warpgroup each).
+// softmax warpgroup each); 3 = trio mode (the three row tiles of a three-tile head in one CTA, two
+// softmax warpgroups).
 static cudaError_t verify_launch(const vc_shape* shape, const vc_verify_req* req, const int* sel, int n, int rows,
                                  int h0, int h1, void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream,
                                  vc_status* st) {
@@ -1441,12 +1745,14 @@ cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h
   //   one tile: one unit per (request, KV head) at two CTAs per SM;
   //   exactly two: pair mode (VC_VERIFY_PAIR=0 turns it off): each K/V tile read once for both
   //     tiles, with a softmax warpgroup per tile;
-  //   three or more: one unit per row tile (each reads KV_full again), or with VC_VERIFY_ROWS=1 the
-  //     row-tile mode for up to VROWS tiles (read once; one softmax warpgroup per CTA, so slower:
-  //     1.36x at 320 rows per KV head).
+  //   three or more: one unit per row tile (each reads KV_full again); with VC_VERIFY_TRIO=1 a head
+  //     of exactly three goes to trio mode (read once, two softmax warpgroups; slower at present:
+  //     its first warpgroup holds two of the three tiles);
+  //   with VC_VERIFY_ROWS=1, every request of the call in row-tile mode when none has more than
+  //     VROWS tiles (read once; one softmax warpgroup per CTA, so slower).
   // Requests of different kinds go to separate launches, one after the other on the stream; every
   // request is checked before either is launched.
-  int sel_a[VC_MAX_BATCH], sel_p[VC_MAX_BATCH], na = 0, np = 0, max_mt = 1;
+  int sel_a[VC_MAX_BATCH], sel_p[VC_MAX_BATCH], sel_t[VC_MAX_BATCH], na = 0, np = 0, nt = 0, max_mt = 1;
   for (int b = 0; b < shape->B; ++b) {
     const vc_verify_req& r = req[b];
     const vc_kv_full& f = r.full;
@@ -1464,11 +1770,14 @@ cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h
     return verify_launch(shape, req, sel_a, na, 1, h0, h1, ws, ws_bytes, dev_status, stream, st);
   }
   const char* ep = getenv("VC_VERIFY_PAIR");
-  const bool pair = !(ep && atoi(ep) == 0);
+  const char* et = getenv("VC_VERIFY_TRIO");
+  const bool pair = !(ep && atoi(ep) == 0), trio = et && atoi(et) == 1;
   for (int b = 0; b < shape->B; ++b) {
     const int mtb = (req[b].n_rows * G + VM - 1) / VM;
     if (pair && mtb == 2)
       sel_p[np++] = b;
+    else if (trio && mtb == 3)
+      sel_t[nt++] = b;
     else
       sel_a[na++] = b;
   }
@@ -1476,7 +1785,11 @@ cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h
     const cudaError_t e = verify_launch(shape, req, sel_a, na, 0, h0, h1, ws, ws_bytes, dev_status, stream, st);
     if (e != cudaSuccess || *st != VC_OK) return e;
   }
-  if (np > 0) return verify_launch(shape, req, sel_p, np, 2, h0, h1, ws, ws_bytes, dev_status, stream, st);
+  if (np > 0) {
+    const cudaError_t e = verify_launch(shape, req, sel_p, np, 2, h0, h1, ws, ws_bytes, dev_status, stream, st);
+    if (e != cudaSuccess || *st != VC_OK) return e;
+  }
+  if (nt > 0) return verify_launch(shape, req, sel_t, nt, 3, h0, h1, ws, ws_bytes, dev_status, stream, st);
   return cudaSuccess;
 }
 

@@ -12,6 +12,8 @@ bit on every request of every round; draft and verify attention on rounds 0 and 
 requests and KV heads ("VeriCache: Turning Lossy KV Cache into Lossless LLM Inference", "Core
 algorithm", "Architecture support", "Cross-resource staggering (P1)").
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -71,7 +73,8 @@ def _check_verify(w, b, r, hk, what, q=None, kn=None, vn=None, heads=None):
 def test_llama70b_offload_full_size_sampled():
     """4 x 131,072 tokens, 4-bit (4,092 blocks per head): all 40 draft steps run, steps 0 and 39
     checked on two KV heads; then the verification (3 row tiles of 128 rows per KV head) checked
-    on one KV head of every request."""
+    on one KV head of every request, and again in trio mode (VC_VERIFY_TRIO=1: every K/V tile read
+    once for the three row tiles) on two requests."""
     w = configs.llama70b_offload4()
     bt = make_batch(w, list(range(w.B)))
     bt.compress()
@@ -86,6 +89,18 @@ def test_llama70b_offload_full_size_sampled():
             for hk in (0, 7) if b == 0 else (5,):
                 _check_draft(w, b, r, hk, [0, w.L[b] - 1], w.name)
         _check_verify(w, b, r, (2 * b + 1) % w.Hkv, w.name)
+    # the same verification with every K/V tile read once for the three row tiles (trio mode)
+    os.environ["VC_VERIFY_TRIO"] = "1"
+    try:
+        for r in bt.reqs:
+            r.o_verify.zero_()
+        bt.verify()
+        torch.cuda.synchronize()
+    finally:
+        del os.environ["VC_VERIFY_TRIO"]
+    assert int(bt.dev_status.item()) == 0
+    for b in (1, 2):
+        _check_verify(w, b, bt.reqs[b], (2 * b + 1) % w.Hkv, w.name + " trio")
 
 
 def test_mixed_serving_whole_twenty_rounds():

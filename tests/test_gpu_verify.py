@@ -78,28 +78,51 @@ def test_verify_split_layouts(ctas, monkeypatch):
     _check(w, [0, 1], env_ctas=ctas, monkeypatch=monkeypatch)
 
 
+def _mode_env(monkeypatch, mode):
+    """rows: every row tile of a head in one CTA (VC_VERIFY_ROWS=1); default: two-tile heads in pair
+    mode and the rest one unit per row tile (a launch per kind); trio: the default plus three-tile
+    heads in trio mode (VC_VERIFY_TRIO=1); units: one unit per row tile for every head
+    (VC_VERIFY_PAIR=0)."""
+    monkeypatch.setenv("VC_VERIFY_ROWS", "1" if mode == "rows" else "0")
+    monkeypatch.setenv("VC_VERIFY_PAIR", "0" if mode == "units" else "1")
+    if mode == "trio":
+        monkeypatch.setenv("VC_VERIFY_TRIO", "1")
+    else:
+        monkeypatch.delenv("VC_VERIFY_TRIO", raising=False)
+
+
 @pytest.mark.parametrize("ctas", [1, 5, 1000])
-@pytest.mark.parametrize("rows_mode", ["1", "0"])
-def test_verify_row_tiles_split_layouts(ctas, rows_mode, monkeypatch):
+@pytest.mark.parametrize("mode", ["rows", "trio", "default"])
+def test_verify_row_tiles_split_layouts(ctas, mode, monkeypatch):
     """More than 128 query rows per KV head (L 40 x G 8 = 320: three row tiles), ragged context:
-    every row tile of a KV head in one CTA, each K/V tile loaded once for all of them (row-tile
-    mode, VC_VERIFY_ROWS=1) and one unit per row tile (the default), cut into
-    one CTA, a few CTAs and one CTA per KV tile, so units split across CTAs merge their partials."""
-    monkeypatch.setenv("VC_VERIFY_ROWS", rows_mode)
+    every row tile of a KV head in one CTA with one softmax warpgroup (row-tile mode), in trio mode
+    (two softmax warpgroups, tiles 0 and 2 on the first) and one unit per row tile (the default),
+    each cut into one CTA, a few CTAs and one CTA per KV tile, so heads split across CTAs merge
+    their partials."""
+    _mode_env(monkeypatch, mode)
     w = configs.scaled(configs.llama70b_offload4(), ctx_div=256, batch=2)
     w.ctx = [517, 1000]
     _check(w, [0, 1], env_ctas=ctas, monkeypatch=monkeypatch)
 
 
-def _mode_env(monkeypatch, mode):
-    """rows: every row tile of a head in one CTA (VC_VERIFY_ROWS=1); pair: the default, two-tile
-    heads in pair mode and the rest one unit per row tile (two launches); units: one unit per row
-    tile for every head (VC_VERIFY_PAIR=0)."""
-    monkeypatch.setenv("VC_VERIFY_ROWS", "1" if mode == "rows" else "0")
-    monkeypatch.setenv("VC_VERIFY_PAIR", "0" if mode == "units" else "1")
+@pytest.mark.parametrize("mode", ["trio", "default", "units"])
+@pytest.mark.parametrize("d128", [True, False])
+def test_verify_one_to_four_row_tiles(mode, d128, monkeypatch):
+    """One call whose KV heads have one row tile (L 25 x G 4 = 100 rows), two (160), three (280 and
+    384, the most trio mode takes) and four (388): with trio mode on, a launch each for the heads
+    of one, three or four tiles (a unit per tile), the pair-mode heads and the trio-mode heads. d =
+    128 and d = 64 (the tiny shape), both with G 4."""
+    _mode_env(monkeypatch, mode)
+    if d128:
+        w = configs.scaled(configs.mixed_serving(), ctx_div=64, batch=5)
+    else:
+        w = configs.scaled(configs.tiny(), batch=5)
+        w.ctx = [300, 1000, 517, 260, 2000]
+    w.L = [25, 40, 70, 96, 97]
+    _check(w, list(range(5)))
 
 
-@pytest.mark.parametrize("mode", ["rows", "pair", "units"])
+@pytest.mark.parametrize("mode", ["rows", "default", "units"])
 def test_verify_row_tiles_mixed_one_and_two(mode, monkeypatch):
     """One call with KV heads of one row tile (L 25 x G 4 = 100 rows, L 32: 128) and of two (L 40:
     160 rows, L 33: 132): the row-tile mode holds both kinds of units; by default the two-tile
@@ -111,7 +134,7 @@ def test_verify_row_tiles_mixed_one_and_two(mode, monkeypatch):
 
 
 @pytest.mark.parametrize("ctas", [1, 5, 1000])
-@pytest.mark.parametrize("mode", ["pair", "units"])
+@pytest.mark.parametrize("mode", ["default", "units"])
 def test_verify_two_row_tiles_split_layouts(ctas, mode, monkeypatch):
     """Two row tiles per KV head (L 20 x G 8 = 160 rows), ragged contexts, the pair mode's launch
     cut into one CTA, a few and one CTA per KV tile: the two warpgroups' partials of split heads
