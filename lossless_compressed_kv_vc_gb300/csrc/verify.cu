@@ -222,6 +222,9 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
     verify_attn_kernel(const __grid_constant__ VerifyParams p) {
   using C = VCfgOf<D, MODE>;
   constexpr bool KV_HEAD_UNITS = MODE == VMODE_ROWS || MODE == VMODE_PAIR || MODE == VMODE_TRIO;
+  // K stages: the statistics mode loads no V, so its K ring also takes the V stages (four K tiles
+  // in flight per CTA instead of two)
+  constexpr int KST = MODE == VMODE_STATS ? 4 : 2;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte aligned tiles
@@ -254,6 +257,10 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
   // into registers (4 softmax warps), P tile b written [2] (4 warps), P V of P tile b done [2], the
   // unit's Q tiles written (4 warps), its MMA issuer's drain
   auto trio_bars = [&](int w) { return bars + 16 + 8 * w; };
+  // the K ring's barriers: kfull / kempty, or in the statistics mode four of each in the block the
+  // pair and trio modes use
+  uint64_t* kf = MODE == VMODE_STATS ? bars + 16 : kfull;
+  uint64_t* ke = MODE == VMODE_STATS ? bars + 20 : kempty;
 
   if (warp == 0) tc05::alloc(tslot, C::TCOLS);
   if (tid == 0) {
@@ -265,6 +272,10 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
     if (MODE == VMODE_STATS) {
       mbar_init(&vfull[0], 4);
       mbar_init(&vfull[1], 4);
+      for (int i = 0; i < KST; ++i) {
+        mbar_init(&kf[i], 1);
+        mbar_init(&ke[i], 1);
+      }
     }
     mbar_init(pfull, 4);
     mbar_init(ofull, 1);
@@ -477,10 +488,12 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
       int pv_b = 0, pv_hk = 0, pv_j = 0;
       bool pv_pending = false;
       auto load = [&](bool isv, uint32_t gi, int b, int hk, int j) -> bool {
-        const int st = gi & 1;
-        if (gi >= 2 && !vwait(isv ? &vempty[st] : &kempty[st], ((gi - 2) >> 1) & 1, p.dev_status, s_abort)) return false;
+        const uint32_t nst = isv ? 2 : KST;
+        const int st = gi % nst;
+        if (gi >= nst && !vwait(isv ? &vempty[st] : &ke[st], ((gi - nst) / nst) & 1, p.dev_status, s_abort))
+          return false;
         const VerifyReqDev& R = p.req[b];
-        uint64_t* bar = isv ? &vfull[st] : &kfull[st];
+        uint64_t* bar = isv ? &vfull[st] : &kf[st];
         uint8_t* dst = smem + (isv ? C::OFF_V : C::OFF_K) + st * C::KV_BYTES;
         const bool isnew = j >= R.n_full;
         const int tok = isnew ? (j - R.n_full) * VBN : j * VBN;
@@ -509,8 +522,9 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
           load(true, gv, pv_b, pv_hk, pv_j))
         ++gv;
       if (*s_abort) {
-        // drain (bounded): the loads of the last two tiles of each kind may still be landing
-        for (uint32_t gi = (gk > 2 ? gk - 2 : 0); gi < gk; ++gi) mbar_wait_bounded(&kfull[gi & 1], (gi >> 1) & 1, p.dev_status);
+        // drain (bounded): the loads of the last tiles of each kind (a ring's worth) may still be landing
+        for (uint32_t gi = (gk > (uint32_t)KST ? gk - KST : 0); gi < gk; ++gi)
+          mbar_wait_bounded(&kf[gi % KST], (gi / KST) & 1, p.dev_status);
         for (uint32_t gi = (gv > 2 ? gv - 2 : 0); gi < gv; ++gi) mbar_wait_bounded(&vfull[gi & 1], (gi >> 1) & 1, p.dev_status);
       }
     }
@@ -622,12 +636,12 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
         ++u;
         for (int jj = 0; jj < nt && ok; ++jj) {
           const uint32_t gc = g + jj;
-          if (!vwait(&kfull[gc & 1], (gc >> 1) & 1, p.dev_status, s_abort)) {
+          if (!vwait(&kf[gc % KST], (gc / KST) & 1, p.dev_status, s_abort)) {
             ok = false;
             break;
           }
           tc05::fence_after();
-          const uint32_t kaddr = aK + (gc & 1) * C::KV_BYTES;
+          const uint32_t kaddr = aK + (gc % KST) * C::KV_BYTES;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t da = tc05::sdesc_sw128(aQ + (kk >> 2) * (VM * 128) + (kk & 3) * 32, 16, 1024);
@@ -635,7 +649,7 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
             tc05::mma_bf16(tmem + (gc & 1) * C::SCOL, da, db, IDESC_S, kk > 0);
           }
           tc05::commit(&sfull[gc & 1]);
-          tc05::commit(&kempty[gc & 1]);
+          tc05::commit(&ke[gc % KST]);
           if (jj > 0) ok = issue_pv(gc - 1, jj > 1);
         }
         if (ok) ok = issue_pv(g + nt - 1, nt > 1);
@@ -1321,12 +1335,17 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
           const float mx = row_max(x);
           const float m_new = fmaxf(m_run, mx);
           if (m_new != -INFINITY) {
-            float acc[8];
+            const uint64_t nm = f2_pack(-m_new, -m_new);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-            for (int e = 0; e < VBN; ++e) acc[e & 7] += ex2_approx(x[e] - m_new);
-            const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            for (int e = 0; e < VBN / 2; ++e) {
+              float a0, a1;
+              f2_unpack(f2_add(f2_pack(x[2 * e], x[2 * e + 1]), nm), a0, a1);
+              acc[e & 3] = f2_add(acc[e & 3], f2_pack(ex2_approx(a0), ex2_approx(a1)));
+            }
+            float s0, s1;
+            f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+            const float sum = s0 + s1;
             l_run = l_run * ex2_approx(m_run - m_new) + sum;
             m_run = m_new;
           }
