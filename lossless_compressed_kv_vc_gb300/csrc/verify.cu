@@ -170,9 +170,14 @@ struct VCfg {
   static_assert(!PAIR || (POCOL + 2 * D <= (int)TCOLS && NQ == 2), "pair mode fits TMEM");
   // trio mode: warpgroup w's S buffer at TMEM columns [64 w, 64 w + 64), row tile m's O at 128 + m D
   static_assert(!TRIO || (OCOL + 3 * D <= (int)TCOLS && NQ == 3), "trio mode fits TMEM");
-  // votes mode: an fp16 all-ones [128][128] A operand over the (unused) V stages
-  static constexpr int ONES_BYTES = VM * 128 * 2;
-  static constexpr int OFF_BAR_VOTES = OFF_V + ONES_BYTES > OFF_BAR ? OFF_V + ONES_BYTES : OFF_BAR;
+  // votes mode, over the (unused) V stages: a second P tile, then the all-ones A operand of the
+  // column-sum MMA. Its 128 rows are alike, so the operand's descriptor steps 16 bytes from one
+  // 8-row group to the next and every row it reads lies in the first 1,264 bytes of the tile
+  static constexpr int OFF_P1_VOTES = OFF_V;
+  static constexpr int OFF_ONES_VOTES = OFF_V + P_BYTES;
+  static constexpr int ONES_BYTES = 2048;
+  static constexpr int OFF_BAR_VOTES =
+      OFF_ONES_VOTES + ONES_BYTES > OFF_BAR ? OFF_ONES_VOTES + ONES_BYTES : OFF_BAR;
   static constexpr int SMEM_VOTES = OFF_BAR_VOTES + 256;
 };
 
@@ -261,6 +266,9 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
   // pair and trio modes use
   uint64_t* kf = MODE == VMODE_STATS ? bars + 16 : kfull;
   uint64_t* ke = MODE == VMODE_STATS ? bars + 20 : kempty;
+  // votes mode: P tile b written (4 softmax warps) and its column sums done, b = tile & 1
+  uint64_t* pfv = bars + 16;  // [2]
+  uint64_t* ofv = bars + 18;  // [2]
 
   if (warp == 0) tc05::alloc(tslot, C::TCOLS);
   if (tid == 0) {
@@ -269,6 +277,12 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
     // A single release barrier could complete two phases (two tiles read) before the MMA warp
     // waits for the first, and the parity wait would then miss it; per buffer, a phase can only
     // complete after the MMA warp has waited for the previous one (it issues that buffer's next S).
+    if (MODE == VMODE_VOTES) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&pfv[i], 4);
+        mbar_init(&ofv[i], 1);
+      }
+    }
     if (MODE == VMODE_STATS) {
       mbar_init(&vfull[0], 4);
       mbar_init(&vfull[1], 4);
@@ -308,7 +322,8 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
   }
   if constexpr (MODE == VMODE_VOTES) {
     for (int e = tid; e < C::ONES_BYTES / 16; e += C::THREADS)
-      reinterpret_cast<uint4*>(smem + C::OFF_V)[e] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+      reinterpret_cast<uint4*>(smem + C::OFF_ONES_VOTES)[e] =
+          make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
     fence_proxy_async_smem();  // the tensor cores read it
   }
   tc05::fence_before();
@@ -542,21 +557,24 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
           // tile gp's S has been read: its TMEM buffer may take tile gp + 2
           return vwait(&vfull[gp & 1], (gp >> 1) & 1, p.dev_status, s_abort);
         }
-        if (!vwait(pfull, gp & 1, p.dev_status, s_abort)) return false;
         if constexpr (MODE == VMODE_VOTES) {
-          // column sums of P (fp16, [128 rows = K][64 keys = N], MN-major) by an all-ones A
+          // column sums of P tile gp & 1 (fp16, [128 rows = K][64 keys = N], MN-major) by an
+          // all-ones A, into TMEM buffer gp & 1
+          if (!vwait(&pfv[gp & 1], (gp >> 1) & 1, p.dev_status, s_abort)) return false;
           constexpr uint32_t IDESC_C = tc05::idesc_f16(VM, VBN, true);
-          const uint32_t aOnes = smem_u32(smem + C::OFF_V);
+          const uint32_t aOnes = smem_u32(smem + C::OFF_ONES_VOTES);
+          const uint32_t aPb = (gp & 1) ? smem_u32(smem + C::OFF_P1_VOTES) : aP;
           tc05::fence_after();
 #pragma unroll
           for (int kk = 0; kk < VM / 16; ++kk) {
-            const uint64_t da = tc05::sdesc_sw128(aOnes + (kk >> 2) * (VM * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t db = tc05::sdesc_sw128(aP + kk * 2048, VM * 128, 1024);
+            const uint64_t da = tc05::sdesc_sw128(aOnes + (kk & 3) * 32, 16, 16);
+            const uint64_t db = tc05::sdesc_sw128(aPb + kk * 2048, VM * 128, 1024);
             tc05::mma_bf16(tmem + C::OCOL + (gp & 1) * VBN, da, db, IDESC_C, kk > 0 ? 1u : 0u);
           }
-          tc05::commit(ofull);
+          tc05::commit(&ofv[gp & 1]);
           return true;
         }
+        if (!vwait(pfull, gp & 1, p.dev_status, s_abort)) return false;
         if (!vwait(&vfull[gp & 1], (gp >> 1) & 1, p.dev_status, s_abort)) return false;
         tc05::fence_after();
         const uint32_t vaddr = aV + (gp & 1) * C::KV_BYTES;
@@ -1362,28 +1380,29 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
         }
       } else if constexpr (MODE == VMODE_VOTES) {
         // votes: P = 2^(s scale - lse) (0 for padding rows and invisible keys) in fp16 for the
-        // column-sum MMA; warp 0 reads each tile's sums (every row of them is the same) and stores
-        // the keys' votes of this 128-row tile
+        // column-sum MMA, alternating between two P tiles. Every row of a tile's sums is the same;
+        // warp w stores keys 16 w .. 16 w + 15 of them, two tiles after the tile's P (when the
+        // next P into that buffer needs its sums done anyway), the unit's last two at its end
         const float lse = row_ok ? R.lse[((size_t)hk * R.mtiles + mt) * VM + tid] : 0.f;
         float* vdst = R.votes + ((size_t)hk * R.mtiles + mt) * (size_t)(R.ctx + R.n_rows);
+        auto sums_done = [&](uint32_t gp) { return vwait(&ofv[gp & 1], (gp >> 1) & 1, p.dev_status, s_abort); };
         auto store_votes = [&](uint32_t gp, int jp) {
-          uint32_t r0[32], r1[32];
-          const uint32_t t_c = tmem + C::OCOL + (gp & 1) * VBN;  // warp 0: lanes 0-31
-          tc05::ld32(t_c, r0);
-          tc05::ld32(t_c + 32, r1);
+          uint32_t r0[8], r1[8];
+          const uint32_t t_c = tmem + lane_off + C::OCOL + (gp & 1) * VBN + 16 * warp;
+          tc05::ld8(t_c, r0);
+          tc05::ld8(t_c + 8, r1);
           tc05::wait_ld();
-          float v0 = 0.f, v1 = 0.f;
+          float v = 0.f;
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (e == lane) {
-              v0 = __uint_as_float(r0[e]);
-              v1 = __uint_as_float(r1[e]);
-            }
+          for (int e = 0; e < 8; ++e) {
+            if (e == lane) v = __uint_as_float(r0[e]);
+            if (e + 8 == lane) v = __uint_as_float(r1[e]);
+          }
           const int j = q.j0 + jp;
           const int key0 = j < R.n_full ? j * VBN : R.ctx + (j - R.n_full) * VBN;
           const int nv = j < R.n_full ? min(VBN, R.ctx - j * VBN) : min(VBN, R.n_rows - (j - R.n_full) * VBN);
-          if (lane < nv) vdst[key0 + lane] = v0;
-          if (32 + lane < nv) vdst[key0 + 32 + lane] = v1;
+          const int k = 16 * warp + lane;
+          if (lane < 16 && k < nv) vdst[key0 + k] = v;
         };
         for (int jj = 0; jj < nt; ++jj) {
           const int j = q.j0 + jj;
@@ -1407,15 +1426,18 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
             }
           }
           const int last = !row_ok ? -1 : j < R.n_full ? R.ctx - j * VBN - 1 : qi - (j - R.n_full) * VBN;
-          if (jj > 0) {
-            // the previous tile's column sums are done, so the P buffer is free
-            if (!vwait(ofull, (gc - 1) & 1, p.dev_status, s_abort)) {
+          if (gc >= 2) {
+            // P tile gc & 1 and TMEM sums buffer gc & 1 were last used by tile gc - 2: its column
+            // sums are done (a wait that is exact: tile gc - 4's were observed two tiles ago, and
+            // tile gc's cannot start before this tile's P); a tile of this unit has its votes stored
+            if (!sums_done(gc - 2)) {
               ok = false;
               break;
             }
             tc05::fence_after();
-            if (warp == 0) store_votes(gc - 1, jj - 1);
+            if (jj >= 2) store_votes(gc - 2, jj - 2);
           }
+          uint8_t* pb = (gc & 1) ? smem + C::OFF_P1_VOTES : sP;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             uint32_t w[4];
@@ -1427,20 +1449,24 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
               const __half2 h = __floats2half2_rn(p0, p1);
               w[e] = *reinterpret_cast<const uint32_t*>(&h);
             }
-            *reinterpret_cast<uint4*>(sP + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(pb + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
           fence_proxy_async_smem();
           tc05::fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(pfull);
+          if (lane == 0) mbar_arrive(&pfv[gc & 1]);
         }
         if (!ok) break;
-        if (!vwait(ofull, (g + nt - 1) & 1, p.dev_status, s_abort)) {
-          ok = false;
-          break;
+        // the unit's last two tiles: their sums, then their votes
+        for (int jp = nt > 2 ? nt - 2 : 0; jp < nt && ok; ++jp) {
+          if (!sums_done(g + jp)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after();
+          store_votes(g + jp, jp);
         }
-        tc05::fence_after();
-        if (warp == 0) store_votes(g + nt - 1, nt - 1);
+        if (!ok) break;
         g += nt;
       }
       tc05::fence_before();
