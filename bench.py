@@ -501,10 +501,10 @@ def run_native(args):
                 "kernel": "draft_attn_kernel<128,%d,1> (one vc_draft_attn call, partial merge included; mean over "
                           "the draft phase of each timed round)" % (0 if quant == 0 else w.bits),
                 "algorithmic_bytes_per_launch": alg, "avg_launch_ms": d_ms, "peak_kind": peak_kind}
-    # keep-set (+ gather when compacting), one draft launch per step, verify + its merge, accept (2)
     # keep-set (+ gather when compacting; quantised caches are built once, outside the round), one
-    # draft launch per step, verify + its merge, accept (2)
-    launches_per_step = (0 if quant else 1) + (1 if args.compact else 0) + w.L_max + 2 + 2
+    # draft launch per step, the verification's kernels and merges (as the library splits the
+    # batch's KV heads), accept (2)
+    launches_per_step = (0 if quant else 1) + (1 if args.compact else 0) + w.L_max + bt.verify_launches() + 2
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -730,7 +730,7 @@ def run_mixed(args):
     achieved = dom_alg / (dom_ms / 1e3) / 1e9
     kname = "draft_attn_kernel<128,%s,1>" % ("0" if dom == DROP else str(w.bits))
     total_kernel_ms = sum(kind_ms.values()) + ver_ms
-    launches = sum(len(bt._steps) + 2 * args.head_chunks + 2 for bts in groups for bt in bts)
+    launches = sum(len(bt._steps) + bt.verify_launches() * args.head_chunks + 2 for bts in groups for bt in bts)
     overlap = statistics.mean(_covered(iv, comp_iv) for iv in copy_iv) if copy_iv else None
     if args.timeline:
         tl = [{"period": k, "host_issue_start_ms": host_t[k],

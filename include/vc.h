@@ -313,6 +313,14 @@ vc_status vc_verify_attn_heads(const vc_shape* shape, const vc_verify_req* req, 
                                int32_t kv_head_end, void* ws, size_t ws_bytes, int32_t* dev_status,
                                cudaStream_t stream);
 
+/* vc_verify_launches — how many kernels one vc_verify_attn call (and each vc_verify_attn_heads
+ * call) launches for these requests: two (the verification kernel and the merge of heads split
+ * across CTAs) per kind of launch the requests need, by their KV heads' 128-row tiles (one tile,
+ * two, three in trio mode) and the environment switches described at the top of this file, as
+ * they are set when this is called. Host only: reads shape and each request's n_rows, new_cap and
+ * pointers' alignment, no device memory. Returns -1 for arguments vc_verify_attn would refuse. */
+int32_t vc_verify_launches(const vc_shape* shape, const vc_verify_req* req);
+
 /* ------------------------------------------------------------------------------------------ */
 /* vc_accept — greedy acceptance ("Core algorithm", step 3).
  *

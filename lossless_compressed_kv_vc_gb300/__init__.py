@@ -87,6 +87,8 @@ _lib.vc_draft_attn_noalloc.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_draft_r
 _lib.vc_verify_attn.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_verify_req), _p, C.c_size_t, _p, _p]
 _lib.vc_verify_attn_heads.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_verify_req), _i32, _i32, _p, C.c_size_t,
                                       _p, _p]
+_lib.vc_verify_launches.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_verify_req)]
+_lib.vc_verify_launches.restype = _i32
 _lib.vc_accept.argtypes = [_i32, _i32, _i32, _p, _p, _p, _p, _p, _p]
 _lib.vc_append_kv.argtypes = [C.POINTER(vc_shape), C.POINTER(vc_kv_full), C.POINTER(vc_kv_comp),
                               C.POINTER(vc_append_req), _i32, _p, _p]
@@ -205,6 +207,11 @@ def vc_verify_attn_heads(shape: vc_shape, req, kv_head_begin: int, kv_head_end: 
     st = _lib.vc_verify_attn_heads(C.byref(shape), req, kv_head_begin, kv_head_end, _ptr(ws), wsb, _ptr(dev_status),
                                    _stream(stream))
     return _check(st, "vc_verify_attn_heads", raise_on_error)
+
+
+def vc_verify_launches(shape: vc_shape, req) -> int:
+    """Kernels one vc_verify_attn call launches for these requests (host only; -1: invalid)."""
+    return int(_lib.vc_verify_launches(C.byref(shape), req))
 
 
 def vc_accept(B: int, L_max: int, V: int, logits, draft, L, out_tokens, n_acc, stream=None,

@@ -13,6 +13,7 @@ namespace vc {
 cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h0, int h1, void* ws,
                           size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, vc_status* st);
 size_t verify_workspace_size(const vc_shape* shape, int32_t max_rows);
+int32_t verify_launch_count(const vc_shape* shape, const vc_verify_req* req);
 }  // namespace vc
 
 using namespace vc;
@@ -489,6 +490,10 @@ vc_status vc_verify_attn(const vc_shape* shape, const vc_verify_req* req, void* 
                          int32_t* dev_status, cudaStream_t stream) {
   if (!shape) return VC_ERR_INVALID;
   return vc_verify_attn_heads(shape, req, 0, shape->Hkv, ws, ws_bytes, dev_status, stream);
+}
+
+int32_t vc_verify_launches(const vc_shape* shape, const vc_verify_req* req) {
+  return verify_launch_count(shape, req);
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -1773,70 +1773,79 @@ static cudaError_t verify_launch(const vc_shape* shape, const vc_verify_req* req
   return d == 128 ? launch_verify_t<128>(p, stream) : launch_verify_t<64>(p, stream);
 }
 
-cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h0, int h1, void* ws,
-                          size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, vc_status* st) {
-  *st = VC_OK;
+// How the requests of a call are verified, by their KV heads' 128-row tiles (L x G rows):
+//   one tile: one unit per (request, KV head) at two CTAs per SM;
+//   exactly two: pair mode (VC_VERIFY_PAIR=0 turns it off): each K/V tile read once for both
+//     tiles, with a softmax warpgroup per tile;
+//   three or more: one unit per row tile (each reads KV_full again); with VC_VERIFY_TRIO=1 a head
+//     of exactly three goes to trio mode (read once, two softmax warpgroups; slower at present:
+//     its first warpgroup holds two of the three tiles);
+//   with VC_VERIFY_ROWS=1, every request of the call in row-tile mode when none has more than
+//     VROWS tiles (read once; one softmax warpgroup per CTA, so slower).
+// Requests of different kinds go to separate launches (each a kernel and its merge), one after the
+// other on the stream, in the order of sel[] below; every request is checked first.
+struct VerifyPlan {
+  int sel[3][VC_MAX_BATCH];  // requests of the one-unit-per-tile, pair-mode and trio-mode launches
+  int n[3];
+  bool rows_all;             // one row-tile-mode launch over every request (listed in sel[0])
+};
+
+static vc_status plan_verify(const vc_shape* shape, const vc_verify_req* req, VerifyPlan* pl) {
   if (!shape || shape->B < 1 || shape->B > VC_MAX_BATCH || shape->Hkv < 1 || shape->Hq < shape->Hkv ||
-      shape->Hq % shape->Hkv != 0 || !req || h0 < 0 || h1 <= h0 || h1 > shape->Hkv) {
-    *st = VC_ERR_INVALID;
-    return cudaSuccess;
-  }
-  if (shape->d != 64 && shape->d != 128) {
-    *st = VC_ERR_UNSUPPORTED;
-    return cudaSuccess;
-  }
+      shape->Hq % shape->Hkv != 0 || !req)
+    return VC_ERR_INVALID;
+  if (shape->d != 64 && shape->d != 128) return VC_ERR_UNSUPPORTED;
   const int G = shape->Hq / shape->Hkv;
-  // How each request's KV heads are verified, by their 128-row tiles (L x G rows):
-  //   one tile: one unit per (request, KV head) at two CTAs per SM;
-  //   exactly two: pair mode (VC_VERIFY_PAIR=0 turns it off): each K/V tile read once for both
-  //     tiles, with a softmax warpgroup per tile;
-  //   three or more: one unit per row tile (each reads KV_full again); with VC_VERIFY_TRIO=1 a head
-  //     of exactly three goes to trio mode (read once, two softmax warpgroups; slower at present:
-  //     its first warpgroup holds two of the three tiles);
-  //   with VC_VERIFY_ROWS=1, every request of the call in row-tile mode when none has more than
-  //     VROWS tiles (read once; one softmax warpgroup per CTA, so slower).
-  // Requests of different kinds go to separate launches, one after the other on the stream; every
-  // request is checked before either is launched.
-  int sel_a[VC_MAX_BATCH], sel_p[VC_MAX_BATCH], sel_t[VC_MAX_BATCH], na = 0, np = 0, nt = 0, max_mt = 1;
+  int max_mt = 1;
   for (int b = 0; b < shape->B; ++b) {
     const vc_verify_req& r = req[b];
     const vc_kv_full& f = r.full;
     if (!a16(f.k) || !a16(f.v) || !a16(r.q) || !a16(r.o) || !a16(r.k_new) || !a16(r.v_new) || f.ctx < 1 ||
-        f.cap < f.ctx || r.n_rows < 1 || r.new_cap < r.n_rows) {
-      *st = VC_ERR_INVALID;
-      return cudaSuccess;
-    }
+        f.cap < f.ctx || r.n_rows < 1 || r.new_cap < r.n_rows)
+      return VC_ERR_INVALID;
     const int mtb = (r.n_rows * G + VM - 1) / VM;
     if (mtb > max_mt) max_mt = mtb;
   }
+  pl->n[0] = pl->n[1] = pl->n[2] = 0;
   const char* er = getenv("VC_VERIFY_ROWS");
-  if (max_mt >= 2 && max_mt <= VROWS && er && atoi(er) == 1) {
-    for (int b = 0; b < shape->B; ++b) sel_a[na++] = b;
-    return verify_launch(shape, req, sel_a, na, 1, h0, h1, ws, ws_bytes, dev_status, stream, st);
-  }
+  pl->rows_all = max_mt >= 2 && max_mt <= VROWS && er && atoi(er) == 1;
   const char* ep = getenv("VC_VERIFY_PAIR");
   const char* et = getenv("VC_VERIFY_TRIO");
   const bool pair = !(ep && atoi(ep) == 0), trio = et && atoi(et) == 1;
   for (int b = 0; b < shape->B; ++b) {
     const int mtb = (req[b].n_rows * G + VM - 1) / VM;
-    if (pair && mtb == 2)
-      sel_p[np++] = b;
-    else if (trio && mtb == 3)
-      sel_t[nt++] = b;
-    else
-      sel_a[na++] = b;
+    const int k = pl->rows_all ? 0 : (pair && mtb == 2) ? 1 : (trio && mtb == 3) ? 2 : 0;
+    pl->sel[k][pl->n[k]++] = b;
   }
-  if (na > 0) {
-    const cudaError_t e = verify_launch(shape, req, sel_a, na, 0, h0, h1, ws, ws_bytes, dev_status, stream, st);
+  return VC_OK;
+}
+
+cudaError_t launch_verify(const vc_shape* shape, const vc_verify_req* req, int h0, int h1, void* ws,
+                          size_t ws_bytes, int32_t* dev_status, cudaStream_t stream, vc_status* st) {
+  *st = VC_OK;
+  if (!shape || h0 < 0 || h1 <= h0 || h1 > shape->Hkv) {
+    *st = VC_ERR_INVALID;
+    return cudaSuccess;
+  }
+  VerifyPlan pl;
+  *st = plan_verify(shape, req, &pl);
+  if (*st != VC_OK) return cudaSuccess;
+  if (pl.rows_all) return verify_launch(shape, req, pl.sel[0], pl.n[0], 1, h0, h1, ws, ws_bytes, dev_status, stream, st);
+  constexpr int kRows[3] = {0, 2, 3};  // verify_launch's layout of each list
+  for (int k = 0; k < 3; ++k) {
+    if (pl.n[k] == 0) continue;
+    const cudaError_t e = verify_launch(shape, req, pl.sel[k], pl.n[k], kRows[k], h0, h1, ws, ws_bytes, dev_status,
+                                        stream, st);
     if (e != cudaSuccess || *st != VC_OK) return e;
   }
-  if (np > 0) {
-    const cudaError_t e = verify_launch(shape, req, sel_p, np, 2, h0, h1, ws, ws_bytes, dev_status, stream, st);
-    if (e != cudaSuccess || *st != VC_OK) return e;
-  }
-  if (nt > 0) return verify_launch(shape, req, sel_t, nt, 3, h0, h1, ws, ws_bytes, dev_status, stream, st);
   return cudaSuccess;
 }
 
+int32_t verify_launch_count(const vc_shape* shape, const vc_verify_req* req) {
+  VerifyPlan pl;
+  if (plan_verify(shape, req, &pl) != VC_OK) return -1;
+  if (pl.rows_all) return 2;
+  return 2 * ((pl.n[0] > 0) + (pl.n[1] > 0) + (pl.n[2] > 0));
+}
 
 }  // namespace vc

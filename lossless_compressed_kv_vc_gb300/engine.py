@@ -15,7 +15,7 @@ import torch
 
 from . import (vc_shape, vc_kv_full, vc_kv_comp, vc_draft_req, vc_verify_req, vc_append_req, vc_importance_req,
                vc_snapkv_importance, vc_importance_workspace_size, VC_POOL_MAX, vc_compress_kv, vc_comp_bytes,
-               vc_draft_attn, vc_verify_attn, vc_verify_attn_heads, vc_accept, vc_append_kv, vc_workspace_size,
+               vc_draft_attn, vc_verify_attn, vc_verify_attn_heads, vc_verify_launches, vc_accept, vc_append_kv, vc_workspace_size,
                VC_TOKEN_DROP, VC_QUANT, VC_CALL_DRAFT, VC_CALL_VERIFY)
 
 
@@ -311,6 +311,11 @@ class Batch:
     def verify(self, stream=None):
         self._order(stream)
         vc_verify_attn(self.shape, self.verify_requests(), self.ws_verify, self.dev_status, stream)
+
+    def verify_launches(self) -> int:
+        """Kernels one verify() launches for this batch (the library's own split of its KV heads by
+        row tiles, under the current environment switches)."""
+        return vc_verify_launches(self.shape, self.verify_requests())
 
 
 class _Slot:

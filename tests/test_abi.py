@@ -147,6 +147,36 @@ def test_verify_head_range_rejected_before_launch(lib):
         assert vc.vc_verify_attn_heads(shp, arr, h0, h1, None, None, stream=0, raise_on_error=False) == vc.VC_ERR_INVALID
 
 
+@pytest.mark.parametrize("env,rows,expect", [
+    ({}, [32], 2),                               # one row tile (G 4: 128 rows): units
+    ({}, [25, 40], 4),                           # one and two tiles: units + pair mode
+    ({"VC_VERIFY_PAIR": "0"}, [25, 40], 2),      # pair mode off: units only
+    ({}, [25, 40, 70, 97], 4),                   # three and four tiles go to units by default
+    ({"VC_VERIFY_TRIO": "1"}, [25, 40, 70], 6),  # units + pair + trio
+    ({"VC_VERIFY_TRIO": "1"}, [70, 96], 2),      # trio only (280 and 384 rows)
+    ({"VC_VERIFY_ROWS": "1"}, [25, 40, 70], 2),  # row-tile mode over the whole call
+    ({"VC_VERIFY_ROWS": "1"}, [25, 97], 2),      # four tiles: no row-tile mode; one and four: units
+])
+def test_verify_launch_count(lib, monkeypatch, env, rows, expect):
+    """vc_verify_launches: two kernels (verification and merge) per kind of launch the requests
+    need, host only (the pointers are never dereferenced)."""
+    import lossless_compressed_kv_vc_gb300 as vc
+    for k in ("VC_VERIFY_PAIR", "VC_VERIFY_TRIO", "VC_VERIFY_ROWS"):
+        monkeypatch.delenv(k, raising=False)
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    shp = vc.vc_shape(len(rows), 32, 8, 128)                     # G 4
+    arr = (vc.vc_verify_req * len(rows))()
+    for b, n in enumerate(rows):
+        e = arr[b]
+        e.full.k, e.full.v, e.full.ctx, e.full.cap = 1 << 12, 1 << 13, 1000, 1000
+        e.q, e.k_new, e.v_new, e.o = 1 << 14, 1 << 15, 1 << 16, 1 << 17
+        e.new_cap, e.n_rows = n, n
+    assert vc.vc_verify_launches(shp, arr) == expect
+    arr[0].n_rows = 0                                             # refused by vc_verify_attn too
+    assert vc.vc_verify_launches(shp, arr) == -1
+
+
 def test_plan_stagger_equals_oracle_brute_force():
     """The library's Gray-code enumeration against the oracle's itertools brute force: the same
     split (with the same tie-break) and period on random integer costs, resident requests mixed in."""
