@@ -339,16 +339,19 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
     }
     const int t0 = 16 * half + a8, t1 = t0 + 8;
     // the scales and zeros of all D/32 channel groups of tokens t0 and t1 (adjacent in the block);
-    // the zeros take the centring: z + C0 s (fp16, one rounding of a value of the data's size)
-    constexpr uint32_t c0b = BITS == 2 ? 0x3E003E00u : 0x47804780u;  // fp16 1.5 / 7.5, both halves
-    const __half2 c0h = *reinterpret_cast<const __half2*>(&c0b);
+    // v = s code + z with the codes as subnormals (code_frag_sub): for 2 bits the scales of token
+    // t1 (a B row 8-15 of the k-step) carry the factor 1/16 (exact in fp16 down to its subnormals;
+    // a factor 16 on token t0 instead could overflow for large scales)
+    constexpr uint32_t k16b = 0x2C002C00u;  // fp16 1/16, both halves
+    const __half2 k16 = *reinterpret_cast<const __half2*>(&k16b);
     __half2 vs0[D / 64], vs1[D / 64], vz0[D / 64], vz1[D / 64];
 #pragma unroll
     for (int k = 0; k < D / 64; ++k) {
       vs0[k] = reinterpret_cast<const __half2*>(vsc + t0 * (D / 32))[k];
       vs1[k] = reinterpret_cast<const __half2*>(vsc + t1 * (D / 32))[k];
-      vz0[k] = __hfma2(c0h, vs0[k], reinterpret_cast<const __half2*>(vze + t0 * (D / 32))[k]);
-      vz1[k] = __hfma2(c0h, vs1[k], reinterpret_cast<const __half2*>(vze + t1 * (D / 32))[k]);
+      if constexpr (BITS == 2) vs1[k] = __hmul2(vs1[k], k16);
+      vz0[k] = reinterpret_cast<const __half2*>(vze + t0 * (D / 32))[k];
+      vz1[k] = reinterpret_cast<const __half2*>(vze + t1 * (D / 32))[k];
     }
 #pragma unroll
     for (int g = 0; g < D / 32; ++g) {
@@ -368,7 +371,7 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
       for (int mm = 0; mm < 2; ++mm) {
         const int mt = 2 * g + mm;
         uint32_t a[4];
-        code_frag_centred<BITS>(vw[(half * STEPS + (BITS == 4 ? mt : mt >> 1)) * 32 + lane], mt, a);
+        code_frag_sub<BITS>(vw[(half * STEPS + (BITS == 4 ? mt : mt >> 1)) * 32 + lane], mt, a);
 #pragma unroll
         for (int hb = 0; hb < NHB; ++hb) mma_f16_16816(o[hb][mt], a, pb[hb][0], pb[hb][1]);
       }
@@ -376,9 +379,23 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
   }
 }
 
-// Add the value zero/offset terms into O (sum over the lanes' tokens first) and clear them.
-template <int D, int NHB>
+// End of a run of quantised groups: take O out of the value codes' power-of-two domain (channel
+// row g of each 16-channel tile at 2^-24, row g + 8 at 2^-22 (2 bits) or 2^-20 (4 bits), see
+// code_frag_sub; exact), add the value zero terms (sum over the lanes' tokens first) and clear
+// them.
+template <int D, int BITS, int NHB>
 __device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zs)[NHB][D / 32][2]) {
+  constexpr float R0 = 16777216.f;                         // 2^24
+  constexpr float R1 = BITS == 2 ? 4194304.f : 1048576.f;  // 2^22 / 2^20
+#pragma unroll
+  for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      o[hb][mt][0] *= R0;
+      o[hb][mt][1] *= R0;
+      o[hb][mt][2] *= R1;
+      o[hb][mt][3] *= R1;
+    }
 #pragma unroll
   for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
@@ -769,7 +786,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     locate(i, b, lc, cur_proc);
     if (b != cur_b) {
       if (!BF16_ROWS && zs_live) {
-        fold_zs<D, NHB>(o, zs);
+        fold_zs<D, C::BITS, NHB>(o, zs);
         zs_live = false;
       }
       reset();
@@ -813,7 +830,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       zs_live = true;
     } else {
       if (!BF16_ROWS && zs_live) {
-        fold_zs<D, NHB>(o, zs);
+        fold_zs<D, C::BITS, NHB>(o, zs);
         zs_live = false;
       }
       if (!BF16_ROWS && q_f16) {
@@ -839,7 +856,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   cp_async_wait<0>();
   const bool has = !aborted && cur_b >= 0;
   if (has) {
-    if (!BF16_ROWS && zs_live) fold_zs<D, NHB>(o, zs);
+    if (!BF16_ROWS && zs_live) fold_zs<D, C::BITS, NHB>(o, zs);
     finish();  // the stage ring is drained: the partial stays in shared memory
   }
   if (lane == 0) s_has[warp] = has ? 1 : 0;

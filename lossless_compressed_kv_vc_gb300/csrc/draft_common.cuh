@@ -99,6 +99,33 @@ __device__ __forceinline__ void code_frag_centred(uint32_t w, int ks, uint32_t (
   }
 }
 
+// The value side's A fragment (channels x tokens) as exact fp16 subnormals: each code keeps its
+// bit position P inside its 16-bit half and the exponent field stays zero, so the register holds
+// code x 2^(P-24) exactly, with no offset to remove and no centring to apply (one AND per
+// register). The positions, as for code_frag: 2-bit registers 0-3 at P = 0, 2, 4, 6 (the odd
+// k-step from bits 8-15 of each half), 4-bit registers 0 and 2 at P = 0, 1 and 3 at P = 4.
+// Registers 0 and 1 hold token rows 0-7 of the k-step, 2 and 3 rows 8-15; registers 0 and 2
+// channel row g, 1 and 3 row g + 8. So for 2 bits the B register of token rows 8-15 takes its
+// weights times 1/16 (rows 8-15 then meet rows 0-7 at 2^-24 for channel row g and 2^-22 for row
+// g + 8), and for 4 bits channel row g accumulates at 2^-24, row g + 8 at 2^-20: fold_zs takes O
+// back.
+template <int BITS>
+__device__ __forceinline__ void code_frag_sub(uint32_t w, int ks, uint32_t (&a)[4]) {
+  if constexpr (BITS == 2) {
+    const uint32_t x = (ks & 1) ? (w >> 8) : w;
+    a[0] = x & 0x00030003u;
+    a[1] = x & 0x000C000Cu;
+    a[2] = x & 0x00300030u;
+    a[3] = x & 0x00C000C0u;
+  } else {
+    const uint32_t x = w >> 8;
+    a[0] = w & 0x000F000Fu;
+    a[1] = w & 0x00F000F0u;
+    a[2] = x & 0x000F000Fu;
+    a[3] = x & 0x00F000F0u;
+  }
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, __half2 y) {
   const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&x), y);
   return *reinterpret_cast<const uint32_t*>(&r);
