@@ -217,7 +217,7 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
 template <int D, int BITS, int NHB>
 __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
                                               const uint32_t (&qn)[NHB][D / 16][2], float (&o)[NHB][D / 16][4],
-                                              float (&m)[NHB][2], float (&l)[NHB][2], float (&zs)[NHB][D / 32][2],
+                                              float (&m)[NHB][2], float (&l)[NHB][2], uint64_t (&zs)[NHB][D / 32],
                                               int lane) {
   using C = DraftCfg<D, BITS>;
   constexpr int MT = D / 16;
@@ -316,22 +316,29 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
           o[hb][mt][2] *= corr[0];
           o[hb][mt][3] *= corr[1];
         }
+        const uint64_t c2 = f2_pack(corr[0], corr[1]);
 #pragma unroll
-        for (int g = 0; g < D / 32; ++g) {
-          zs[hb][g][0] *= corr[0];
-          zs[hb][g][1] *= corr[1];
-        }
+        for (int g = 0; g < D / 32; ++g) zs[hb][g] = f2_fma(zs[hb][g], c2, 0ull);
       }
     }
     uint32_t pt0[NHB], pt1[NHB];  // fp16 weights of tokens t0, t1 for this lane's two heads
+    // the same weights as packed pairs over the lane's two heads: pp0 token t0, pp1 token t1
+    uint64_t pp0[NHB], pp1[NHB];
+    const uint64_t sc2 = f2_pack(scale_q, scale_q);
 #pragma unroll
-    for (int hb = 0; hb < NHB; ++hb)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        p[hb][e][0] = ex2_approx(fmaf(s[hb][e], scale_q, -m[hb][e]));
-        p[hb][e][1] = ex2_approx(fmaf(s[hb][e + 2], scale_q, -m[hb][e]));
-        l[hb][e] += p[hb][e][0] + p[hb][e][1];
-      }
+    for (int hb = 0; hb < NHB; ++hb) {
+      const uint64_t nm = f2_pack(-m[hb][0], -m[hb][1]);
+      float a0, a1, b0, b1;
+      f2_unpack(f2_fma(f2_pack(s[hb][0], s[hb][1]), sc2, nm), a0, a1);
+      f2_unpack(f2_fma(f2_pack(s[hb][2], s[hb][3]), sc2, nm), b0, b1);
+      p[hb][0][0] = ex2_approx(a0);
+      p[hb][1][0] = ex2_approx(a1);
+      p[hb][0][1] = ex2_approx(b0);
+      p[hb][1][1] = ex2_approx(b1);
+      pp0[hb] = f2_pack(p[hb][0][0], p[hb][1][0]);
+      pp1[hb] = f2_pack(p[hb][0][1], p[hb][1][1]);
+      f2_unpack(f2_add(f2_pack(l[hb][0], l[hb][1]), f2_add(pp0[hb], pp1[hb])), l[hb][0], l[hb][1]);
+    }
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) {
       pt0[hb] = pack_half2(p[hb][0][0], p[hb][1][0]);
@@ -362,8 +369,7 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
       uint32_t pb[NHB][2];
 #pragma unroll
       for (int hb = 0; hb < NHB; ++hb) {
-        zs[hb][g][0] += z0 * p[hb][0][0] + z1 * p[hb][0][1];
-        zs[hb][g][1] += z0 * p[hb][1][0] + z1 * p[hb][1][1];
+        zs[hb][g] = f2_fma(f2_pack(z1, z1), pp1[hb], f2_fma(f2_pack(z0, z0), pp0[hb], zs[hb][g]));
         pb[hb][0] = movmatrix_t(hmul2_u32(pt0[hb], s0));
         pb[hb][1] = movmatrix_t(hmul2_u32(pt1[hb], s1));
       }
@@ -384,7 +390,7 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
 // code_frag_sub; exact), add the value zero terms (sum over the lanes' tokens first) and clear
 // them.
 template <int D, int BITS, int NHB>
-__device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zs)[NHB][D / 32][2]) {
+__device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], uint64_t (&zs)[NHB][D / 32]) {
   constexpr float R0 = 16777216.f;                         // 2^24
   constexpr float R1 = BITS == 2 ? 4194304.f : 1048576.f;  // 2^22 / 2^20
 #pragma unroll
@@ -399,10 +405,12 @@ __device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zs)[
 #pragma unroll
   for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
-    for (int g = 0; g < D / 32; ++g)
+    for (int g = 0; g < D / 32; ++g) {
+      float zp[2];
+      f2_unpack(zs[hb][g], zp[0], zp[1]);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float z = zs[hb][g][e];
+        float z = zp[e];
         z += __shfl_xor_sync(0xffffffffu, z, 4);
         z += __shfl_xor_sync(0xffffffffu, z, 8);
         z += __shfl_xor_sync(0xffffffffu, z, 16);
@@ -410,8 +418,9 @@ __device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zs)[
         o[hb][2 * g][e + 2] += z;
         o[hb][2 * g + 1][e] += z;
         o[hb][2 * g + 1][e + 2] += z;
-        zs[hb][g][e] = 0.f;
       }
+      zs[hb][g] = 0ull;
+    }
 }
 
 // Edge w of T chunks cut into W equal ranges: w * T / W. The host bounds T * (W + 1) below 2^32,
@@ -671,7 +680,8 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
 
   float o[NHB][C::MT][4];
   float m[NHB][2], l[NHB][2];
-  float zs[NHB][D / 32][2];  // value zero/offset terms of quantised blocks not yet folded into o
+  uint64_t zs[NHB][D / 32];  // value zero terms of quantised blocks not yet folded into o (packed
+                             // pairs over the lane's two heads)
   uint32_t qb[NHB][C::MT][2];
   int cur_b = -1;
   bool zs_live = false;
@@ -686,7 +696,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       m[hb][0] = m[hb][1] = -INFINITY;
       l[hb][0] = l[hb][1] = 0.f;
 #pragma unroll
-      for (int g = 0; g < D / 32; ++g) zs[hb][g][0] = zs[hb][g][1] = 0.f;
+      for (int g = 0; g < D / 32; ++g) zs[hb][g] = 0ull;
     }
   };
   // Q^T B fragments: k = channel 16ks + 2(lane%4) (+8), n = head 8hb + lane/4 (zero beyond G)

@@ -37,33 +37,6 @@ namespace vc {
 constexpr int VM = 128;  // query rows per tile
 constexpr int VBN = 64;  // KV tokens per tile
 
-// Packed f32x2 arithmetic (two independent fp32 lanes per instruction, each rounded as its scalar
-// form) and a three-input maximum: a softmax row of 64 scores costs about a third fewer
-// instructions than with scalar FMAs, adds and two-input maxima.
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
 // The largest of a row's VBN scores (three-input maxima: 64 -> 22 -> 8 -> 3 -> 1).
 __device__ __forceinline__ float row_max(const float (&x)[VBN]) {
   static_assert(VBN == 64, "the tree is laid out for 64 scores");
