@@ -1411,18 +1411,36 @@ __global__ void __launch_bounds__((MODE == VMODE_PAIR || MODE == VMODE_TRIO) ? 3
             if (jj >= 2) store_votes(gc - 2, jj - 2);
           }
           uint8_t* pb = (gc & 1) ? smem + C::OFF_P1_VOTES : sP;
+          if (last >= VBN - 1) {
+            // every key of the tile visible (all but a unit's last tiles): packed f32x2 FMAs, no masks
+            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nl2 = f2_pack(-lse, -lse);
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint32_t w[4];
+            for (int ch = 0; ch < 8; ++ch) {
+              uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int k0 = ch * 8 + 2 * e;
-              const float p0 = k0 <= last ? ex2_approx(fmaf(x[k0], p.scale_log2, -lse)) : 0.f;
-              const float p1 = k0 + 1 <= last ? ex2_approx(fmaf(x[k0 + 1], p.scale_log2, -lse)) : 0.f;
-              const __half2 h = __floats2half2_rn(p0, p1);
-              w[e] = *reinterpret_cast<const uint32_t*>(&h);
+              for (int e = 0; e < 4; ++e) {
+                const int k0 = ch * 8 + 2 * e;
+                float a0, a1;
+                f2_unpack(f2_fma(f2_pack(x[k0], x[k0 + 1]), sc2, nl2), a0, a1);
+                const __half2 h = __floats2half2_rn(ex2_approx(a0), ex2_approx(a1));
+                w[e] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+              *reinterpret_cast<uint4*>(pb + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            *reinterpret_cast<uint4*>(pb + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k0 = ch * 8 + 2 * e;
+                const float p0 = k0 <= last ? ex2_approx(fmaf(x[k0], p.scale_log2, -lse)) : 0.f;
+                const float p1 = k0 + 1 <= last ? ex2_approx(fmaf(x[k0 + 1], p.scale_log2, -lse)) : 0.f;
+                const __half2 h = __floats2half2_rn(p0, p1);
+                w[e] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+              *reinterpret_cast<uint4*>(pb + tid * 128 + ((ch ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
           }
           fence_proxy_async_smem();
           tc05::fence_before();
