@@ -107,6 +107,30 @@ def test_draft_quant_d128_ragged(kernel, bits, monkeypatch):
     _check_all_steps(w, [0, 1, 2, 3, 4])
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("vscale", [1e-3, 300.0])
+def test_draft_quant_value_scales(bits, vscale):
+    """Value caches far from unit size (every value times 1e-3 or 300, then bf16): the quantised
+    kernel's fp16 operands -- value scales and zeros, weights times scales (for 2 bits with a
+    factor 1/16 on half the tokens), codes as fp16 subnormals -- against the oracle on every step.
+    Both sides are divided by the factor before the comparison: the outputs scale with the values,
+    and so does every rounding error, while the tolerance's absolute floor (1e-2) is set for
+    outputs of unit size."""
+    w = configs.scaled(configs.qwen32b_quant2(), ctx_div=64, batch=2, L=4)
+    w.bits = bits
+    reqs = [0, 1]
+    bt = make_batch(w, reqs)
+    for r in bt.reqs:
+        r.v_full.copy_((r.v_full.float() * vscale).to(torch.bfloat16))
+        r.v_new.copy_((r.v_new.float() * vscale).to(torch.bfloat16))
+    _run_round(bt)
+    for i, b in enumerate(reqs):
+        r = bt.reqs[i]
+        km, vm, kw0, vw0 = _oracle_main(w, b, r, i, bt)
+        ref = O.draft_round(f32(r.q), km, vm, kw0, vw0, f32(r.k_new), f32(r.v_new))
+        assert_attn_close(r.o_draft.float() / vscale, ref / vscale, f"{w.name} request {b} values x {vscale}")
+
+
 @pytest.mark.parametrize("keep,ctx,L", [(10, 64, 3), (17, 40, 17), (1, 8, 2)])
 def test_draft_fewer_chunks_than_warps(keep, ctx, L):
     """One request whose step has only 2-3 chunks per head (16-row kept chunks, then window
