@@ -94,6 +94,15 @@ struct DraftMapsOf<0> {
 // a 1024-byte aligned block, and it keeps the eight rows an ldmatrix reads on distinct banks.
 __device__ __forceinline__ int sw_off(int r, int cc) { return (cc >> 3) * 2048 + r * 128 + (((cc & 7) ^ (r & 7)) << 4); }
 
+// d = A B with a zero accumulator (m16n8k16, fp16 operands, fp32 result).
+__device__ __forceinline__ void mma_f16_16816_c0(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -202,22 +211,25 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
 
 // One quantised 32-token block, read in its stored form (see the block layout in compress.cu): each
 // lane's 32-bit word is its A fragment for an m16n8k16 MMA, turned into exact fp16 operands by one
-// LOP3 per register (code_frag); the tensor cores take the codes with no dequantised tile between.
+// AND per register (code_frag_sub: the code keeps its bit position P, the exponent field stays zero,
+// so the register holds code x 2^(P-24)); the tensor cores take the codes with no dequantised tile
+// between, and the powers of two are folded into the other operand or the result.
 // qn holds the query as fp16 scaled by 2^-E (|qn| < 1, E per warp), scale_q = log2(e)/sqrt(d) * 2^E.
 //   keys (scale s_c, zero z_c per channel):
 //     S^T[t][h] = sum_c code (s_c qn_hc) + sum_c z_c qn_hc
-//     -> B operand fp16(s o qn) per block (B <= s: no overflow); the per-head term z . qn and the
-//        removal of the code offsets are MMAs (z broadcast over tokens, resp. the constant offsets,
-//        against qn, resp. the scaled query), once per block for both 16-token halves;
+//     -> B operand fp16(s o qn) per block (B <= s: no overflow), the accumulator read back times
+//        2^24 over the row's power of two; the per-head term z . qn is an MMA (z broadcast over
+//        tokens) against qn, once per block for both 16-token halves;
 //   values (scale s_t, zero z_t per token and 32-channel group g), P <= 1 (the running maximum moves
-//   at every new maximum inside quantised blocks), codes centred (code_frag_centred, C0 = mid code):
-//     O^T[c][h] += sum_t (code - C0) (s_t p_th) + sum_t (z_t + C0 s_t) p_th
-//     -> A = exact fp16 code - C0, B operand fp16(s o p) per channel group, plus a per-(group,
-//        head) zero term zs accumulated in the softmax frame of O and added before O is read.
+//   at every new maximum inside quantised blocks), codes as exact fp16 subnormals (code_frag_sub):
+//     O^T[c][h] += sum_t code (s_t p_th) + sum_t z_t p_th
+//     -> A = the code times a power of two per register, B operand fp16(s o p) per channel group;
+//        the zero terms are one MMA per 16 tokens into zacc (rows = channel groups, B = the raw
+//        weights), in the softmax frame of O, added when a run of quantised groups ends (fold_zs).
 template <int D, int BITS, int NHB>
 __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
                                               const uint32_t (&qn)[NHB][D / 16][2], float (&o)[NHB][D / 16][4],
-                                              float (&m)[NHB][2], float (&l)[NHB][2], uint64_t (&zs)[NHB][D / 32],
+                                              float (&m)[NHB][2], float (&l)[NHB][2], float (&zacc)[NHB][4],
                                               int lane) {
   using C = DraftCfg<D, BITS>;
   constexpr int MT = D / 16;
@@ -229,59 +241,70 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
   const __half* vsc = reinterpret_cast<const __half*>(raw + C::OFF_VS);
   const __half* vze = reinterpret_cast<const __half*>(raw + C::OFF_VZ);
   const int b4 = lane & 3, a8 = lane >> 2;
-  uint32_t acorr[4];
-  code_offsets<BITS>(acorr);
-  // block setup: scaled query fragments and the per-(row half, head) term of both halves
-  // (the zero term and the offset removal accumulate in separate registers: two independent MMA
-  // chains of MT instead of one of 2 MT)
+  // block setup: the scaled query fragments qs = s o qn and the zero term z . qn of each head. The
+  // key codes enter as exact fp16 subnormals (code_frag_sub): 2 bits put channels 8-15 of a k-step
+  // 16x higher, which the query absorbs (its channels 8-15 arrive divided by 16), and token rows
+  // 8-15 4x higher (2 bits) or 16x (4 bits), which the score scale of those rows absorbs. For 2
+  // bits the zero term's A fragment keeps channels 0-7 in rows 0-7 and channels 8-15 in rows 8-15,
+  // so the two sums come out separately and the second takes back its factor 16.
   uint32_t qs[NHB][MT][2];
-  float cb[NHB][4], co[NHB][4];
+  float cz[NHB][4];
 #pragma unroll
   for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) cb[hb][e] = co[hb][e] = 0.f;
+    for (int e = 0; e < 4; ++e) cz[hb][e] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < MT; ++ks) {
     const int c = 16 * ks + 2 * b4;
     const __half2 s0 = *reinterpret_cast<const __half2*>(ksc + c);
     const __half2 s1 = *reinterpret_cast<const __half2*>(ksc + c + 8);
+    const uint32_t z0 = *reinterpret_cast<const uint32_t*>(kze + c), z1 = *reinterpret_cast<const uint32_t*>(kze + c + 8);
     uint32_t az[4];
-    az[0] = az[1] = *reinterpret_cast<const uint32_t*>(kze + c);
-    az[2] = az[3] = *reinterpret_cast<const uint32_t*>(kze + c + 8);
+    az[0] = z0;
+    az[1] = BITS == 2 ? 0u : z0;
+    az[2] = BITS == 2 ? 0u : z1;
+    az[3] = z1;
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) {
       qs[hb][ks][0] = hmul2_u32(qn[hb][ks][0], s0);
       qs[hb][ks][1] = hmul2_u32(qn[hb][ks][1], s1);
-      mma_f16_16816(cb[hb], az, qn[hb][ks][0], qn[hb][ks][1]);
-      mma_f16_16816(co[hb], acorr, qs[hb][ks][0], qs[hb][ks][1]);
+      mma_f16_16816(cz[hb], az, qn[hb][ks][0], qn[hb][ks][1]);
     }
   }
+  // scaled scores T = S scale_q = acc (2^24 scale_q / R) + z . qn scale_q, R = 1 for token rows 0-7
+  // and 4 (2 bits) or 16 (4 bits) for rows 8-15; cbq: the last term for the lane's two heads
+  const float kl = scale_q * 16777216.f, kh = kl * (BITS == 2 ? 0.25f : 0.0625f);
+  const uint64_t kl2 = f2_pack(kl, kl), kh2 = f2_pack(kh, kh), sq2 = f2_pack(scale_q, scale_q);
+  uint64_t cbq[NHB];
 #pragma unroll
-  for (int hb = 0; hb < NHB; ++hb)
+  for (int hb = 0; hb < NHB; ++hb) {
+    uint64_t cb = f2_pack(cz[hb][0], cz[hb][1]);
+    if constexpr (BITS == 2) cb = f2_fma(f2_pack(cz[hb][2], cz[hb][3]), f2_pack(16.f, 16.f), cb);
+    cbq[hb] = f2_fma(cb, sq2, 0ull);
+  }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) cb[hb][e] += co[hb][e];
-#pragma unroll 1
   for (int half = 0; half < 2; ++half) {
     // even and odd k-steps in separate accumulators (two chains of MT / 2), added afterwards
     float s[NHB][4], s2[NHB][4];
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        s[hb][e] = cb[hb][e];
-        s2[hb][e] = 0.f;
-      }
+      for (int e = 0; e < 4; ++e) s[hb][e] = s2[hb][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < MT; ++ks) {
       uint32_t a[4];
-      code_frag<BITS>(kw[(half * STEPS + (BITS == 4 ? ks : ks >> 1)) * 32 + lane], ks, a);
+      code_frag_sub<BITS>(kw[(half * STEPS + (BITS == 4 ? ks : ks >> 1)) * 32 + lane], ks, a);
 #pragma unroll
       for (int hb = 0; hb < NHB; ++hb) mma_f16_16816((ks & 1) ? s2[hb] : s[hb], a, qs[hb][ks][0], qs[hb][ks][1]);
     }
+    // s becomes the scaled scores of token rows lane/4 (s[0], s[1]) and lane/4 + 8 (s[2], s[3])
 #pragma unroll
-    for (int hb = 0; hb < NHB; ++hb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[hb][e] += s2[hb][e];
+    for (int hb = 0; hb < NHB; ++hb) {
+      f2_unpack(f2_fma(f2_add(f2_pack(s[hb][0], s[hb][1]), f2_pack(s2[hb][0], s2[hb][1])), kl2, cbq[hb]), s[hb][0],
+                s[hb][1]);
+      f2_unpack(f2_fma(f2_add(f2_pack(s[hb][2], s[hb][3]), f2_pack(s2[hb][2], s2[hb][3])), kh2, cbq[hb]), s[hb][2],
+                s[hb][3]);
+    }
     // online softmax over the 16 tokens (rows lane/4 and lane/4 + 8; all valid); inside quantised
     // blocks the running maximum follows every new maximum, so the weights stay <= 1 (fp16 B)
     float p[NHB][2][2];
@@ -295,7 +318,7 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        tmax[hb][e] = mx * scale_q;
+        tmax[hb][e] = mx;
         need |= tmax[hb][e] > m[hb][e];
       }
     if (__any_sync(0xffffffffu, need)) {
@@ -316,21 +339,19 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
           o[hb][mt][2] *= corr[0];
           o[hb][mt][3] *= corr[1];
         }
-        const uint64_t c2 = f2_pack(corr[0], corr[1]);
-#pragma unroll
-        for (int g = 0; g < D / 32; ++g) zs[hb][g] = f2_fma(zs[hb][g], c2, 0ull);
+        zacc[hb][0] *= corr[0];
+        zacc[hb][1] *= corr[1];
       }
     }
     uint32_t pt0[NHB], pt1[NHB];  // fp16 weights of tokens t0, t1 for this lane's two heads
     // the same weights as packed pairs over the lane's two heads: pp0 token t0, pp1 token t1
     uint64_t pp0[NHB], pp1[NHB];
-    const uint64_t sc2 = f2_pack(scale_q, scale_q);
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) {
       const uint64_t nm = f2_pack(-m[hb][0], -m[hb][1]);
       float a0, a1, b0, b1;
-      f2_unpack(f2_fma(f2_pack(s[hb][0], s[hb][1]), sc2, nm), a0, a1);
-      f2_unpack(f2_fma(f2_pack(s[hb][2], s[hb][3]), sc2, nm), b0, b1);
+      f2_unpack(f2_add(f2_pack(s[hb][0], s[hb][1]), nm), a0, a1);
+      f2_unpack(f2_add(f2_pack(s[hb][2], s[hb][3]), nm), b0, b1);
       p[hb][0][0] = ex2_approx(a0);
       p[hb][1][0] = ex2_approx(a1);
       p[hb][0][1] = ex2_approx(b0);
@@ -344,34 +365,70 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
       pt0[hb] = pack_half2(p[hb][0][0], p[hb][1][0]);
       pt1[hb] = pack_half2(p[hb][0][1], p[hb][1][1]);
     }
-    const int t0 = 16 * half + a8, t1 = t0 + 8;
-    // the scales and zeros of all D/32 channel groups of tokens t0 and t1 (adjacent in the block);
-    // v = s code + z with the codes as subnormals (code_frag_sub): for 2 bits the scales of token
-    // t1 (a B row 8-15 of the k-step) carry the factor 1/16 (exact in fp16 down to its subnormals;
-    // a factor 16 on token t0 instead could overflow for large scales)
     constexpr uint32_t k16b = 0x2C002C00u;  // fp16 1/16, both halves
     const __half2 k16 = *reinterpret_cast<const __half2*>(&k16b);
-    __half2 vs0[D / 64], vs1[D / 64], vz0[D / 64], vz1[D / 64];
+    // The weights as B fragments of the value MMAs, transposed once: the lane holds tokens u0, u0 + 1
+    // (pr0) and u0 + 8, u0 + 9 (pr1) of the half for head a8. Each channel group g then scales them
+    // by its own per-token value scales, which pair up over the same tokens. For 2 bits the codes of
+    // token rows 8-15 sit 16x higher (code_frag_sub), so those weights enter times 1/16 (exact: a
+    // power of two on weights <= 1).
+    constexpr int NG = D / 32;           // channel groups, one value scale and zero per token each
+    const int u0 = 16 * half + 2 * b4;  // the lane's first token of this half in the B layout
+    uint32_t pr0[NHB], pr1[NHB], pq1[NHB];
 #pragma unroll
-    for (int k = 0; k < D / 64; ++k) {
-      vs0[k] = reinterpret_cast<const __half2*>(vsc + t0 * (D / 32))[k];
-      vs1[k] = reinterpret_cast<const __half2*>(vsc + t1 * (D / 32))[k];
-      if constexpr (BITS == 2) vs1[k] = __hmul2(vs1[k], k16);
-      vz0[k] = reinterpret_cast<const __half2*>(vze + t0 * (D / 32))[k];
-      vz1[k] = reinterpret_cast<const __half2*>(vze + t1 * (D / 32))[k];
+    for (int hb = 0; hb < NHB; ++hb) {
+      pr0[hb] = movmatrix_t(pt0[hb]);
+      pr1[hb] = movmatrix_t(pt1[hb]);
+      pq1[hb] = BITS == 2 ? hmul2_u32(pr1[hb], k16) : pr1[hb];
+    }
+    // the value scales of the lane's four tokens, all NG groups of each: token-major, NG / 2 fp16
+    // pairs per token
+    uint32_t sv[4][NG / 2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half* row = vsc + (u0 + (j & 1) + 8 * (j >> 1)) * NG;  // 2 NG bytes per token
+      if constexpr (NG == 4) {
+        const uint2 w2 = *reinterpret_cast<const uint2*>(row);
+        sv[j][0] = w2.x;
+        sv[j][NG / 2 - 1] = w2.y;
+      } else {
+#pragma unroll
+        for (int k = 0; k < NG / 2; ++k) sv[j][k] = reinterpret_cast<const uint32_t*>(row)[k];
+      }
+    }
+    // Value zero terms sum_t z_tg p_th as one more MMA per half: the A fragment's row g holds the
+    // zeros of group g over the half's tokens (rows of lanes with a8 >= NG repeat a valid group and
+    // are never read; rows 8-15 repeat rows 0-7), B the raw transposed weights. Row g of zacc, in
+    // the lanes with a8 = g, accumulates group g's term for the lane's two heads. Each half's MMA
+    // starts from zero and its sum is added to zacc in fp32: the zero terms of a long range are
+    // large against an output in which they cancel with the code terms (by about 400x for
+    // N(0,1) values at 64K tokens), and the tensor cores' accumulation, truncating, would carry
+    // a bias of that size into the output if zacc were the MMA's accumulator.
+    {
+      const uint16_t* z16 = reinterpret_cast<const uint16_t*>(vze);
+      const int gz = a8 & (NG - 1);
+      uint32_t az[4];
+      az[0] = az[1] = (uint32_t)z16[u0 * NG + gz] | ((uint32_t)z16[(u0 + 1) * NG + gz] << 16);
+      az[2] = az[3] = (uint32_t)z16[(u0 + 8) * NG + gz] | ((uint32_t)z16[(u0 + 9) * NG + gz] << 16);
+#pragma unroll
+      for (int hb = 0; hb < NHB; ++hb) {
+        float zd[4];
+        mma_f16_16816_c0(zd, az, pr0[hb], pr1[hb]);
+        zacc[hb][0] += zd[0];
+        zacc[hb][1] += zd[1];
+      }
     }
 #pragma unroll
-    for (int g = 0; g < D / 32; ++g) {
-      const __half2 s0 = (g & 1) ? __high2half2(vs0[g >> 1]) : __low2half2(vs0[g >> 1]);
-      const __half2 s1 = (g & 1) ? __high2half2(vs1[g >> 1]) : __low2half2(vs1[g >> 1]);
-      const float z0 = (g & 1) ? __high2float(vz0[g >> 1]) : __low2float(vz0[g >> 1]);
-      const float z1 = (g & 1) ? __high2float(vz1[g >> 1]) : __low2float(vz1[g >> 1]);
+    for (int g = 0; g < NG; ++g) {
+      // (scale of token u0, scale of token u0 + 1) of group g, and the same for u0 + 8, u0 + 9
+      const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+      const uint32_t s01 = __byte_perm(sv[0][g >> 1], sv[1][g >> 1], sel);
+      const uint32_t s89 = __byte_perm(sv[2][g >> 1], sv[3][g >> 1], sel);
       uint32_t pb[NHB][2];
 #pragma unroll
       for (int hb = 0; hb < NHB; ++hb) {
-        zs[hb][g] = f2_fma(f2_pack(z1, z1), pp1[hb], f2_fma(f2_pack(z0, z0), pp0[hb], zs[hb][g]));
-        pb[hb][0] = movmatrix_t(hmul2_u32(pt0[hb], s0));
-        pb[hb][1] = movmatrix_t(hmul2_u32(pt1[hb], s1));
+        pb[hb][0] = hmul2_u32(pr0[hb], *reinterpret_cast<const __half2*>(&s01));
+        pb[hb][1] = hmul2_u32(pq1[hb], *reinterpret_cast<const __half2*>(&s89));
       }
 #pragma unroll
       for (int mm = 0; mm < 2; ++mm) {
@@ -387,10 +444,10 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
 
 // End of a run of quantised groups: take O out of the value codes' power-of-two domain (channel
 // row g of each 16-channel tile at 2^-24, row g + 8 at 2^-22 (2 bits) or 2^-20 (4 bits), see
-// code_frag_sub; exact), add the value zero terms (sum over the lanes' tokens first) and clear
-// them.
+// code_frag_sub; exact), add the value zero terms (group g's, for the lane's two heads, from the
+// lane of row g in zacc) and clear them.
 template <int D, int BITS, int NHB>
-__device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], uint64_t (&zs)[NHB][D / 32]) {
+__device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zacc)[NHB][4], int lane) {
   constexpr float R0 = 16777216.f;                         // 2^24
   constexpr float R1 = BITS == 2 ? 4194304.f : 1048576.f;  // 2^22 / 2^20
 #pragma unroll
@@ -403,24 +460,20 @@ __device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], uint64_t (&z
       o[hb][mt][3] *= R1;
     }
 #pragma unroll
-  for (int hb = 0; hb < NHB; ++hb)
+  for (int hb = 0; hb < NHB; ++hb) {
 #pragma unroll
-    for (int g = 0; g < D / 32; ++g) {
-      float zp[2];
-      f2_unpack(zs[hb][g], zp[0], zp[1]);
+    for (int g = 0; g < D / 32; ++g)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float z = zp[e];
-        z += __shfl_xor_sync(0xffffffffu, z, 4);
-        z += __shfl_xor_sync(0xffffffffu, z, 8);
-        z += __shfl_xor_sync(0xffffffffu, z, 16);
+        const float z = __shfl_sync(0xffffffffu, zacc[hb][e], 4 * g + (lane & 3));
         o[hb][2 * g][e] += z;
         o[hb][2 * g][e + 2] += z;
         o[hb][2 * g + 1][e] += z;
         o[hb][2 * g + 1][e + 2] += z;
       }
-      zs[hb][g] = 0ull;
-    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) zacc[hb][e] = 0.f;
+  }
 }
 
 // Edge w of T chunks cut into W equal ranges: w * T / W. The host bounds T * (W + 1) below 2^32,
@@ -680,8 +733,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
 
   float o[NHB][C::MT][4];
   float m[NHB][2], l[NHB][2];
-  uint64_t zs[NHB][D / 32];  // value zero terms of quantised blocks not yet folded into o (packed
-                             // pairs over the lane's two heads)
+  float zacc[NHB][4];  // value zero terms of quantised blocks not yet folded into o (row g: group g)
   uint32_t qb[NHB][C::MT][2];
   int cur_b = -1;
   bool zs_live = false;
@@ -696,7 +748,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       m[hb][0] = m[hb][1] = -INFINITY;
       l[hb][0] = l[hb][1] = 0.f;
 #pragma unroll
-      for (int g = 0; g < D / 32; ++g) zs[hb][g] = 0ull;
+      for (int e = 0; e < 4; ++e) zacc[hb][e] = 0.f;
     }
   };
   // Q^T B fragments: k = channel 16ks + 2(lane%4) (+8), n = head 8hb + lane/4 (zero beyond G)
@@ -741,8 +793,11 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       for (int ks = 0; ks < C::MT; ++ks)
 #pragma unroll
         for (int r2 = 0; r2 < 2; ++r2) {
+          // 2 bits: channels 8-15 of each k-step divided by 16 as well (their key codes sit 16x
+          // higher in the subnormal operands, see qblock_attend)
+          const float sc = (C::BITS == 2 && r2 == 1) ? inv * 0.0625f : inv;
           const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qb[hb][ks][r2]));
-          qb[hb][ks][r2] = pack_half2(f.x * inv, f.y * inv);
+          qb[hb][ks][r2] = pack_half2(f.x * sc, f.y * sc);
         }
     scale_q = ldexpf(p.scale_log2, E);
     q_f16 = true;
@@ -796,7 +851,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     locate(i, b, lc, cur_proc);
     if (b != cur_b) {
       if (!BF16_ROWS && zs_live) {
-        fold_zs<D, C::BITS, NHB>(o, zs);
+        fold_zs<D, C::BITS, NHB>(o, zacc, lane);
         zs_live = false;
       }
       reset();
@@ -834,13 +889,13 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     const DraftReqDev& r = p.req[b];
     uint8_t* sb = win_span ? wb : wb + st * C::STAGE;
     if (!BF16_ROWS && lc < r.n_mc) {
-      qblock_attend<D, C::BITS, NHB>(sb, scale_q, qb, o, m, l, zs, lane);
+      qblock_attend<D, C::BITS, NHB>(sb, scale_q, qb, o, m, l, zacc, lane);
       if (C::GPC == 2 && C::GPC * lc + 1 < q_ng)
-        qblock_attend<D, C::BITS, NHB>(sb + C::QRAW, scale_q, qb, o, m, l, zs, lane);
+        qblock_attend<D, C::BITS, NHB>(sb + C::QRAW, scale_q, qb, o, m, l, zacc, lane);
       zs_live = true;
     } else {
       if (!BF16_ROWS && zs_live) {
-        fold_zs<D, C::BITS, NHB>(o, zs);
+        fold_zs<D, C::BITS, NHB>(o, zacc, lane);
         zs_live = false;
       }
       if (!BF16_ROWS && q_f16) {
@@ -866,7 +921,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   cp_async_wait<0>();
   const bool has = !aborted && cur_b >= 0;
   if (has) {
-    if (!BF16_ROWS && zs_live) fold_zs<D, C::BITS, NHB>(o, zs);
+    if (!BF16_ROWS && zs_live) fold_zs<D, C::BITS, NHB>(o, zacc, lane);
     finish();  // the stage ring is drained: the partial stays in shared memory
   }
   if (lane == 0) s_has[warp] = has ? 1 : 0;

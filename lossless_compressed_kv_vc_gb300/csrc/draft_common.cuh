@@ -9,49 +9,12 @@ namespace vc {
 
 // Two stored codes of a block word as one fp16x2 operand, by a single LOP3: the code at bit position
 // P of each 16-bit half (P + BITS <= 8) lands in the mantissa of 2^(10-P), giving the exact value
-// 2^(10-P) + code. The offset depends only on P, so it is taken out afterwards by a constant MMA.
+// 2^(10-P) + code (code_centred_f16x2 takes the offset and the centre off again).
 template <int BITS, int P>
 __device__ __forceinline__ uint32_t code_f16x2(uint32_t w) {
   constexpr uint32_t m = ((1u << BITS) - 1u) << P;
   constexpr uint32_t e = (25u - P) << 10;  // fp16 exponent field of 2^(10-P)
   return (w & (m | (m << 16))) | (e | (e << 16));
-}
-
-// The four A-fragment registers of k-step ks held by block word w (see the block layout in
-// compress.cu): 2-bit words carry two k-steps (the odd one in bits 8-15 of each half), 4-bit words
-// one (registers 2 and 3 in bits 8-15). One shift per word, one LOP3 per register.
-template <int BITS>
-__device__ __forceinline__ void code_frag(uint32_t w, int ks, uint32_t (&a)[4]) {
-  if constexpr (BITS == 2) {
-    const uint32_t x = (ks & 1) ? (w >> 8) : w;
-    a[0] = code_f16x2<2, 0>(x);
-    a[1] = code_f16x2<2, 2>(x);
-    a[2] = code_f16x2<2, 4>(x);
-    a[3] = code_f16x2<2, 6>(x);
-  } else {
-    const uint32_t x = w >> 8;
-    a[0] = code_f16x2<4, 0>(w);
-    a[1] = code_f16x2<4, 4>(w);
-    a[2] = code_f16x2<4, 0>(x);
-    a[3] = code_f16x2<4, 4>(x);
-  }
-}
-
-// minus the offsets of code_frag's registers, as a constant A fragment (fp16 pairs): an MMA of it
-// with the same B operand subtracts exactly what the offsets added.
-template <int BITS>
-__device__ __forceinline__ void code_offsets(uint32_t (&a)[4]) {
-  if constexpr (BITS == 2) {
-    a[0] = 0xE400E400u;  // -1024
-    a[1] = 0xDC00DC00u;  // -256
-    a[2] = 0xD400D400u;  // -64
-    a[3] = 0xCC00CC00u;  // -16
-  } else {
-    a[0] = 0xE400E400u;  // -1024
-    a[1] = 0xD400D400u;  // -64
-    a[2] = 0xE400E400u;
-    a[3] = 0xD400D400u;
-  }
 }
 
 // The value side's A fragment as exact, centred fp16 codes: code - C0 with C0 = (2^BITS - 1) / 2, so
@@ -99,16 +62,19 @@ __device__ __forceinline__ void code_frag_centred(uint32_t w, int ks, uint32_t (
   }
 }
 
-// The value side's A fragment (channels x tokens) as exact fp16 subnormals: each code keeps its
-// bit position P inside its 16-bit half and the exponent field stays zero, so the register holds
-// code x 2^(P-24) exactly, with no offset to remove and no centring to apply (one AND per
-// register). The positions, as for code_frag: 2-bit registers 0-3 at P = 0, 2, 4, 6 (the odd
-// k-step from bits 8-15 of each half), 4-bit registers 0 and 2 at P = 0, 1 and 3 at P = 4.
-// Registers 0 and 1 hold token rows 0-7 of the k-step, 2 and 3 rows 8-15; registers 0 and 2
-// channel row g, 1 and 3 row g + 8. So for 2 bits the B register of token rows 8-15 takes its
-// weights times 1/16 (rows 8-15 then meet rows 0-7 at 2^-24 for channel row g and 2^-22 for row
-// g + 8), and for 4 bits channel row g accumulates at 2^-24, row g + 8 at 2^-20: fold_zs takes O
-// back.
+// The four A-fragment registers of k-step ks held by block word w (see the block layout in
+// compress.cu: 2-bit words carry two k-steps, the odd one in bits 8-15 of each half; 4-bit words
+// one, registers 2 and 3 in bits 8-15) as exact fp16 subnormals: each code keeps its bit position P
+// inside its 16-bit half and the exponent field stays zero, so the register holds code x 2^(P-24)
+// exactly, with no offset to remove (one shift per word, one AND per register). The positions:
+// 2-bit registers 0-3 at P = 0, 2, 4, 6, 4-bit registers 0 and 2 at P = 0, 1 and 3 at P = 4.
+// Registers 0 and 1 hold MMA columns (k) 0-7 of the k-step, 2 and 3 columns 8-15; registers 0 and
+// 2 rows 0-7, 1 and 3 rows 8-15. Relative to register 0, rows 8-15 therefore sit 4x higher (2 bits)
+// or 16x (4 bits) and columns 8-15 16x higher (2 bits) or equal (4 bits). Keys (rows = tokens,
+// columns = channels) take the column factor into the query and the row factor into the score
+// scale; values (rows = channels, columns = tokens) take the column factor into the weights of
+// tokens 8-15 and leave channel row g at 2^-24 and row g + 8 at 2^-22 (2 bits) or 2^-20 (4 bits),
+// which fold_zs takes back.
 template <int BITS>
 __device__ __forceinline__ void code_frag_sub(uint32_t w, int ks, uint32_t (&a)[4]) {
   if constexpr (BITS == 2) {
