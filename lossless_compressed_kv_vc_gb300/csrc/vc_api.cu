@@ -44,11 +44,20 @@ namespace vc {
 int draft_ctas_per_sm(int G, int kind);
 }
 
-// CTAs per KV head of a draft launch: one wave of CTAs over all heads (the workspace bound takes
-// the largest wave of any kind, G <= 8 and quantised).
-static int draft_ctas_per_head_max(int Hkv, int G = 1, int kind = 2) {
+// CTAs per KV head of a draft launch: one wave of CTAs over all heads.
+static int draft_ctas_per_head_max(int Hkv, int G, int kind) {
   const int n = vc::draft_ctas_per_sm(G, kind) * sm_count() / Hkv;
   return n > 1 ? n : 1;
+}
+
+// The largest wave of any draft launch (G <= 8 gives the most CTAs per SM), for the workspace bound.
+static int draft_ctas_per_head_bound(int Hkv) {
+  int n = 1;
+  for (int kind : {0, 2, 4}) {
+    const int k = draft_ctas_per_head_max(Hkv, 1, kind);
+    n = k > n ? k : n;
+  }
+  return n;
 }
 
 // Arrival counters at the start of the draft workspace: one 32-bit word per (KV head, request slot),
@@ -99,7 +108,7 @@ size_t vc_workspace_size(int32_t call, const vc_shape* shape, int32_t max_rows) 
   if (call == VC_CALL_DRAFT) {
     // CTA partials: slots (CTA + request) per head, CTAs per head at most one wave plus B
     const size_t G = shape->Hq / shape->Hkv;
-    const size_t slots = (size_t)shape->Hkv * (draft_ctas_per_head_max(shape->Hkv) + 2 * shape->B);
+    const size_t slots = (size_t)shape->Hkv * (draft_ctas_per_head_bound(shape->Hkv) + 2 * shape->B);
     return draft_counter_bytes() + slots * G * (shape->d + 1) * sizeof(float) + 256;
   }
   if (call == VC_CALL_VERIFY) return verify_workspace_size(shape, max_rows);
