@@ -139,16 +139,15 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
   // precision: the final division by l uses the same m).
   const bool ok0 = (lane >> 2) < cnt, ok1 = (lane >> 2) + 8 < cnt;
   float p[NHB][2][2];  // [head block][head e][token row 0/1]
+  // each lane tests its own scores; the reduction over the tile's lanes runs only when the
+  // running maximum moves (the tile's maximum exceeds it by 2^8 exactly when some lane's does)
   float tmax[NHB][2];
   bool need = false;
 #pragma unroll
   for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      float mx = fmaxf(ok0 ? s[hb][e] : -INFINITY, ok1 ? s[hb][e + 2] : -INFINITY);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mx = fmaxf(ok0 ? s[hb][e] : -INFINITY, ok1 ? s[hb][e + 2] : -INFINITY);
       tmax[hb][e] = mx * scale_log2;  // the scale is positive: it keeps the order
       need |= tmax[hb][e] > m[hb][e] + 8.f;
     }
@@ -158,7 +157,11 @@ __device__ __forceinline__ void tile_attend(const uint8_t* kt, const uint8_t* vt
       float corr[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float mn = fmaxf(m[hb][e], tmax[hb][e]);
+        float mx = tmax[hb][e];
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(m[hb][e], mx);
         corr[e] = ex2_approx(m[hb][e] - mn);  // 0 when m was -inf (nothing accumulated yet)
         l[hb][e] *= corr[e];
         m[hb][e] = mn;
@@ -307,6 +310,9 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
     }
     // online softmax over the 16 tokens (rows lane/4 and lane/4 + 8; all valid); inside quantised
     // blocks the running maximum follows every new maximum, so the weights stay <= 1 (fp16 B)
+    // The tile maximum decides only whether the running maximum moves, and it moves exactly when
+    // some lane's own scores exceed it, so each lane tests its own and the reduction over the
+    // tile's lanes runs only then (rarely, once a range has seen its first few blocks).
     float p[NHB][2][2];
     float tmax[NHB][2];
     bool need = false;
@@ -314,11 +320,7 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
     for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float mx = fmaxf(s[hb][e], s[hb][e + 2]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        tmax[hb][e] = mx;
+        tmax[hb][e] = fmaxf(s[hb][e], s[hb][e + 2]);
         need |= tmax[hb][e] > m[hb][e];
       }
     if (__any_sync(0xffffffffu, need)) {
@@ -327,7 +329,11 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
         float corr[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float mn = fmaxf(m[hb][e], tmax[hb][e]);
+          float mx = tmax[hb][e];
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mn = fmaxf(m[hb][e], mx);
           corr[e] = ex2_approx(m[hb][e] - mn);
           l[hb][e] *= corr[e];
           m[hb][e] = mn;
