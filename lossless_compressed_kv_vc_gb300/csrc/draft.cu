@@ -256,22 +256,30 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
   for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
     for (int e = 0; e < 4; ++e) cz[hb][e] = 0.f;
+  // The lane's key scales and zeros, channels 16 ks + 2 (lane % 4) + {0, 1} and the same + 8, by
+  // ldmatrix: one x4 load covers two k-steps (its four matrices: k-step 2t channels 0-7, 8-15,
+  // k-step 2t + 1 channels 0-7, 8-15), every row address of a matrix naming the same 16 bytes, so
+  // that each lane receives the pair at 2 (lane % 4) of them.
+  const int kchunk = 32 * (lane >> 4) + 16 * ((lane >> 3) & 1);
 #pragma unroll
-  for (int ks = 0; ks < MT; ++ks) {
-    const int c = 16 * ks + 2 * b4;
-    const __half2 s0 = *reinterpret_cast<const __half2*>(ksc + c);
-    const __half2 s1 = *reinterpret_cast<const __half2*>(ksc + c + 8);
-    const uint32_t z0 = *reinterpret_cast<const uint32_t*>(kze + c), z1 = *reinterpret_cast<const uint32_t*>(kze + c + 8);
-    uint32_t az[4];
-    az[0] = z0;
-    az[1] = BITS == 2 ? 0u : z0;
-    az[2] = BITS == 2 ? 0u : z1;
-    az[3] = z1;
+  for (int t = 0; t < MT / 2; ++t) {
+    uint32_t sv[2][2], zv[2][2];
+    ldsm_x4(sv[0][0], sv[0][1], sv[1][0], sv[1][1], reinterpret_cast<const uint8_t*>(ksc) + 64 * t + kchunk);
+    ldsm_x4(zv[0][0], zv[0][1], zv[1][0], zv[1][1], reinterpret_cast<const uint8_t*>(kze) + 64 * t + kchunk);
 #pragma unroll
-    for (int hb = 0; hb < NHB; ++hb) {
-      qs[hb][ks][0] = hmul2_u32(qn[hb][ks][0], s0);
-      qs[hb][ks][1] = hmul2_u32(qn[hb][ks][1], s1);
-      mma_f16_16816(cz[hb], az, qn[hb][ks][0], qn[hb][ks][1]);
+    for (int j = 0; j < 2; ++j) {
+      const int ks = 2 * t + j;
+      uint32_t az[4];
+      az[0] = zv[j][0];
+      az[1] = BITS == 2 ? 0u : zv[j][0];
+      az[2] = BITS == 2 ? 0u : zv[j][1];
+      az[3] = zv[j][1];
+#pragma unroll
+      for (int hb = 0; hb < NHB; ++hb) {
+        qs[hb][ks][0] = hmul2_u32(qn[hb][ks][0], *reinterpret_cast<const __half2*>(&sv[j][0]));
+        qs[hb][ks][1] = hmul2_u32(qn[hb][ks][1], *reinterpret_cast<const __half2*>(&sv[j][1]));
+        mma_f16_16816(cz[hb], az, qn[hb][ks][0], qn[hb][ks][1]);
+      }
     }
   }
   // scaled scores T = S scale_q = acc (2^24 scale_q / R) + z . qn scale_q, R = 1 for token rows 0-7
