@@ -94,6 +94,13 @@ struct DraftMapsOf<0> {
 // a 1024-byte aligned block, and it keeps the eight rows an ldmatrix reads on distinct banks.
 __device__ __forceinline__ int sw_off(int r, int cc) { return (cc >> 3) * 2048 + r * 128 + (((cc & 7) ^ (r & 7)) << 4); }
 
+// 2^x for a pair of fp16 arguments, as an fp16 pair (one SFU instruction).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // d = A B with a zero accumulator (m16n8k16, fp16 operands, fp32 result).
 __device__ __forceinline__ void mma_f16_16816_c0(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -237,6 +244,7 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
   using C = DraftCfg<D, BITS>;
   constexpr int MT = D / 16;
   constexpr int STEPS = BITS == 4 ? D / 16 : D / 32;  // words per (half, lane)
+  constexpr bool RS_MMA = BITS == 2;                   // row sums from the zero-term MMA (see below)
   const uint32_t* kw = reinterpret_cast<const uint32_t*>(raw + C::OFF_KC);
   const uint32_t* vw = reinterpret_cast<const uint32_t*>(raw + C::OFF_VC);
   const __half* ksc = reinterpret_cast<const __half*>(raw + C::OFF_KS);
@@ -321,7 +329,6 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
     // The tile maximum decides only whether the running maximum moves, and it moves exactly when
     // some lane's own scores exceed it, so each lane tests its own and the reduction over the
     // tile's lanes runs only then (rarely, once a range has seen its first few blocks).
-    float p[NHB][2][2];
     float tmax[NHB][2];
     bool need = false;
 #pragma unroll
@@ -357,27 +364,31 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
         zacc[hb][1] *= corr[1];
       }
     }
-    uint32_t pt0[NHB], pt1[NHB];  // fp16 weights of tokens t0, t1 for this lane's two heads
-    // the same weights as packed pairs over the lane's two heads: pp0 token t0, pp1 token t1
-    uint64_t pp0[NHB], pp1[NHB];
+    // fp16 weights of tokens t0, t1 for this lane's two heads. RS_MMA (2 bits): one fp16-pair
+    // exponential each (arguments <= 0: the running maximum covers the block), their row sums out
+    // of the zero-term MMA below, from the same fp16 weights. Otherwise fp32 exponentials, the row
+    // sums in fp32, then rounded (4 bits: the kernel runs at its register limit, and the fp16 form
+    // spilled there and measured slower).
+    uint32_t pt0[NHB], pt1[NHB];
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) {
       const uint64_t nm = f2_pack(-m[hb][0], -m[hb][1]);
       float a0, a1, b0, b1;
       f2_unpack(f2_add(f2_pack(s[hb][0], s[hb][1]), nm), a0, a1);
       f2_unpack(f2_add(f2_pack(s[hb][2], s[hb][3]), nm), b0, b1);
-      p[hb][0][0] = ex2_approx(a0);
-      p[hb][1][0] = ex2_approx(a1);
-      p[hb][0][1] = ex2_approx(b0);
-      p[hb][1][1] = ex2_approx(b1);
-      pp0[hb] = f2_pack(p[hb][0][0], p[hb][1][0]);
-      pp1[hb] = f2_pack(p[hb][0][1], p[hb][1][1]);
-      f2_unpack(f2_add(f2_pack(l[hb][0], l[hb][1]), f2_add(pp0[hb], pp1[hb])), l[hb][0], l[hb][1]);
-    }
-#pragma unroll
-    for (int hb = 0; hb < NHB; ++hb) {
-      pt0[hb] = pack_half2(p[hb][0][0], p[hb][1][0]);
-      pt1[hb] = pack_half2(p[hb][0][1], p[hb][1][1]);
+      if constexpr (RS_MMA) {
+        pt0[hb] = ex2_f16x2(pack_half2(a0, a1));
+        pt1[hb] = ex2_f16x2(pack_half2(b0, b1));
+      } else {
+        const uint64_t pp0 = f2_pack(ex2_approx(a0), ex2_approx(a1));  // token t0, the lane's two heads
+        const uint64_t pp1 = f2_pack(ex2_approx(b0), ex2_approx(b1));  // token t1
+        f2_unpack(f2_add(f2_pack(l[hb][0], l[hb][1]), f2_add(pp0, pp1)), l[hb][0], l[hb][1]);
+        float x0, x1, y0, y1;
+        f2_unpack(pp0, x0, x1);
+        f2_unpack(pp1, y0, y1);
+        pt0[hb] = pack_half2(x0, x1);
+        pt1[hb] = pack_half2(y0, y1);
+      }
     }
     constexpr uint32_t k16b = 0x2C002C00u;  // fp16 1/16, both halves
     const __half2 k16 = *reinterpret_cast<const __half2*>(&k16b);
@@ -410,10 +421,11 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
         for (int k = 0; k < NG / 2; ++k) sv[j][k] = reinterpret_cast<const uint32_t*>(row)[k];
       }
     }
-    // Value zero terms sum_t z_tg p_th as one more MMA per half: the A fragment's row g holds the
-    // zeros of group g over the half's tokens (rows of lanes with a8 >= NG repeat a valid group and
-    // are never read; rows 8-15 repeat rows 0-7), B the raw transposed weights. Row g of zacc, in
-    // the lanes with a8 = g, accumulates group g's term for the lane's two heads. Each half's MMA
+    // Value zero terms sum_t z_tg p_th (and with RS_MMA the row sums sum_t p_th) as one more MMA
+    // per half: the A fragment's row g < NG holds the zeros of group g over the half's tokens, rows
+    // NG..7 hold ones with RS_MMA (without, they repeat a valid group and are never read; rows 8-15
+    // repeat rows 0-7), B the raw transposed weights. Row g of zacc, in the lanes with a8 = g,
+    // accumulates group g's term for the lane's two heads; with RS_MMA row NG the row sums. Each half's MMA
     // starts from zero and its sum is added to zacc in fp32: the zero terms of a long range are
     // large against an output in which they cancel with the code terms (by about 400x for
     // N(0,1) values at 64K tokens), and the tensor cores' accumulation, truncating, would carry
@@ -421,9 +433,16 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
     {
       const uint16_t* z16 = reinterpret_cast<const uint16_t*>(vze);
       const int gz = a8 & (NG - 1);
+      const bool zrow = a8 < NG;
       uint32_t az[4];
-      az[0] = az[1] = (uint32_t)z16[u0 * NG + gz] | ((uint32_t)z16[(u0 + 1) * NG + gz] << 16);
-      az[2] = az[3] = (uint32_t)z16[(u0 + 8) * NG + gz] | ((uint32_t)z16[(u0 + 9) * NG + gz] << 16);
+      constexpr uint32_t ones = 0x3C003C00u;  // fp16 1, both halves
+      if constexpr (RS_MMA) {
+        az[0] = az[1] = zrow ? (uint32_t)z16[u0 * NG + gz] | ((uint32_t)z16[(u0 + 1) * NG + gz] << 16) : ones;
+        az[2] = az[3] = zrow ? (uint32_t)z16[(u0 + 8) * NG + gz] | ((uint32_t)z16[(u0 + 9) * NG + gz] << 16) : ones;
+      } else {
+        az[0] = az[1] = (uint32_t)z16[u0 * NG + gz] | ((uint32_t)z16[(u0 + 1) * NG + gz] << 16);
+        az[2] = az[3] = (uint32_t)z16[(u0 + 8) * NG + gz] | ((uint32_t)z16[(u0 + 9) * NG + gz] << 16);
+      }
 #pragma unroll
       for (int hb = 0; hb < NHB; ++hb) {
         float zd[4];
@@ -461,7 +480,8 @@ __device__ __forceinline__ void qblock_attend(const uint8_t* raw, float scale_q,
 // code_frag_sub; exact), add the value zero terms (group g's, for the lane's two heads, from the
 // lane of row g in zacc) and clear them.
 template <int D, int BITS, int NHB>
-__device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zacc)[NHB][4], int lane) {
+__device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zacc)[NHB][4], float (&l)[NHB][2],
+                                        int lane) {
   constexpr float R0 = 16777216.f;                         // 2^24
   constexpr float R1 = BITS == 2 ? 4194304.f : 1048576.f;  // 2^22 / 2^20
 #pragma unroll
@@ -485,6 +505,15 @@ __device__ __forceinline__ void fold_zs(float (&o)[NHB][D / 16][4], float (&zacc
         o[hb][2 * g + 1][e] += z;
         o[hb][2 * g + 1][e + 2] += z;
       }
+    // 2 bits: the row sums (row D / 32 of zacc) into the lane-partial sums, once per head (lanes
+    // 0-3)
+    if constexpr (BITS == 2) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float ls = __shfl_sync(0xffffffffu, zacc[hb][e], 4 * (D / 32) + (lane & 3));
+        if (lane < 4) l[hb][e] += ls;
+      }
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) zacc[hb][e] = 0.f;
   }
@@ -865,7 +894,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     locate(i, b, lc, cur_proc);
     if (b != cur_b) {
       if (!BF16_ROWS && zs_live) {
-        fold_zs<D, C::BITS, NHB>(o, zacc, lane);
+        fold_zs<D, C::BITS, NHB>(o, zacc, l, lane);
         zs_live = false;
       }
       reset();
@@ -909,7 +938,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
       zs_live = true;
     } else {
       if (!BF16_ROWS && zs_live) {
-        fold_zs<D, C::BITS, NHB>(o, zacc, lane);
+        fold_zs<D, C::BITS, NHB>(o, zacc, l, lane);
         zs_live = false;
       }
       if (!BF16_ROWS && q_f16) {
@@ -935,7 +964,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
   cp_async_wait<0>();
   const bool has = !aborted && cur_b >= 0;
   if (has) {
-    if (!BF16_ROWS && zs_live) fold_zs<D, C::BITS, NHB>(o, zacc, lane);
+    if (!BF16_ROWS && zs_live) fold_zs<D, C::BITS, NHB>(o, zacc, l, lane);
     finish();  // the stage ring is drained: the partial stays in shared memory
   }
   if (lane == 0) s_has[warp] = has ? 1 : 0;
