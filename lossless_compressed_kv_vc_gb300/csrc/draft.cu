@@ -745,7 +745,9 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
                       &bars[st], stream_pol);
         }
       }
-      cp_async_commit();
+      // cp.async groups count stages only where window tiles fit a stage; with WIN_SPANS a window
+      // chunk is issued alone and waited for with everything (the quantised kernels)
+      if constexpr (!C::WIN_SPANS) cp_async_commit();
       return;
     }
     ensure_wait();  // window rows: the previous step appended one
@@ -918,7 +920,7 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
     }
     if (win_span)
       cp_async_wait<0>();            // nothing else is in flight: all this lane's copies
-    else
+    else if constexpr (!C::WIN_SPANS)
       cp_async_wait<C::NST - 1>();   // this lane's copies of chunk i have landed
     __syncwarp();                    // ... and every other lane's
     if (!mbar_wait_bounded(&bars[st], (i / C::NST) & 1, p.dev_status, p.spin_limit)) {
@@ -955,9 +957,10 @@ __global__ void __launch_bounds__(128, NHB == 1 ? DraftCfg<D, KIND>::CTAS_PER_SM
                                  : (i + C::NST < n);
     if (go) {
       fence_proxy_async_smem();  // this warp's reads of the stage come before the TMA overwrites it
-      issue(issued, issued % C::NST, C::WIN_SPANS ? row_of(issued) : t_next);
+      // (with WIN_SPANS the row is needed for window chunks only: a quantised chunk ignores it)
+      issue(issued, issued % C::NST, C::WIN_SPANS ? (issued >= iw ? row_of(issued) : 0) : t_next);
       ++issued;
-    } else {
+    } else if constexpr (!C::WIN_SPANS) {
       cp_async_commit();  // empty group: the wait above always leaves NST-1 groups pending
     }
   }
