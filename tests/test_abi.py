@@ -84,6 +84,21 @@ def test_draft_counter_block_does_not_depend_on_the_shape(lib):
     assert vc.vc_draft_attn(big, req, stream=0, raise_on_error=False) == vc.VC_ERR_UNSUPPORTED
 
 
+def test_draft_workspace_covers_the_widest_wave(lib):
+    """The draft workspace holds, per KV head, a partial slot for every CTA of the widest draft
+    launch of any cache kind (one wave: 4 CTAs per SM for quantised caches with G <= 8, 3 for
+    token drop; 152 SMs when no GPU answers) plus two per request, each G (d + 1) floats, after the
+    fixed counter block. Sizing by one kind alone undersizes it as soon as the kinds' waves
+    differ."""
+    import lossless_compressed_kv_vc_gb300 as vc
+    sms, widest = 152, 4
+    for B, Hq, Hkv, d in ((1, 8, 2, 64), (8, 32, 8, 128), (16, 40, 8, 128), (32, 32, 8, 128), (2, 64, 8, 128)):
+        G = Hq // Hkv
+        per_head = max(1, widest * sms // Hkv)
+        need = vc.VC_DRAFT_COUNTER_BYTES + Hkv * (per_head + 2 * B) * G * (d + 1) * 4
+        assert vc.vc_workspace_size(vc.VC_CALL_DRAFT, vc.vc_shape(B, Hq, Hkv, d)) >= need, (B, Hq, Hkv, d)
+
+
 def test_comp_bytes_follows_the_layout_rule():
     """vc_comp_bytes (host only) against the oracle's statement of the quantised layout: blocks and
     residual at ctx, block capacity for the grown context, window rows = the largest residual on the
