@@ -1,7 +1,6 @@
-// Shared by the two draft kernels: quantised KV_comp blocks in their stored form (stored codes
-// turned into exact fp16 MMA operands by one logic instruction per register: centred codes for the
-// tcgen05 kernel, subnormal codes for the mma.sync kernel; the layout is described in compress.cu)
-// and the merge of per-CTA (o, lse) partials.
+// Shared by the two draft kernels: quantised KV_comp blocks in their stored form (the LOP3 turn of
+// stored codes into exact fp16 MMA operands; the layout is described in compress.cu) and the merge
+// of per-CTA (o, lse) partials.
 #pragma once
 
 #include "vc_internal.cuh"
